@@ -1,0 +1,637 @@
+"""Plain, slow, float64 CPU oracle of the compression + decode path.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring): nothing on the product
+path imports this module, and it shares no code with the CUDA library.
+
+Sources (web pages, cited by title and section):
+
+* [GK]  "GraceKV - Every Cache Entry Earns Its Place: Global Allocation of
+        Resolution and Coverage for KV Cache Compression" (project page):
+        sections "01 Curvature-guided partition", "02 Progressively refinable
+        representation" / "Inside one cache entry", "03 Bottom-up value flow",
+        "Exact-information safeguard", "04 Top-down budget flow",
+        "05 Physical cache packing", "Technical details and default settings",
+        and the budget-region strip under "Core idea".
+* [DC]  "DistillCache: KL-Guided Adaptive KV-Cache Eviction for Memory-Efficient
+        LLM Inference": section 3.1.1 (state space: the five token features),
+        section 3.1.4 (the eviction error bound), Algorithm 1 (top-B pruning).
+
+Where the pages leave a step open the oracle takes one stated reading; the
+readings are numbered R1..R15 and listed in the repository's design notes.
+Each function names the readings it uses.
+
+Parity status: the scoring, hop, prototype, decode, pack and budget steps are
+pinned by invariants and brute-force tests in ``tests/test_oracle_*.py``.  The
+exact numeric values of the distortion/utility formula (R4) and of the hop
+propagation (R2) are pinned only through their stated readings plus the
+invariants listed there (no page prints a worked example of them).
+"""
+from __future__ import annotations
+
+import heapq
+import math
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+N_NODES = 15          # depth-3 binary midpoint tree: 1 + 2 + 4 + 8 prototype nodes (R3)
+N_OPS = 16            # op 0 = Add(slot); op 1 + j = Split(node j)
+FIRST_LEAF = 7        # nodes 7..14 are the leaf prototypes
+
+
+# =============================================================================== RoPE
+def rope_theta(d: int, base: float) -> np.ndarray:
+    """theta_j = base^(-2j/d), j < d/2 (reading R9: rotate-half pairing)."""
+    return base ** (-2.0 * np.arange(d // 2, dtype=np.float64) / d)
+
+
+def rope_rotate(x: np.ndarray, pos, base: float) -> np.ndarray:
+    """Rotate ``x[..., d]`` by RoPE at real-valued position(s) ``pos``.
+
+    Pairing (j, j + d/2): out_j = x_j cos - x_{j+d/2} sin,
+    out_{j+d/2} = x_{j+d/2} cos + x_j sin, angle = pos * theta_j.  A negative
+    position is the inverse rotation.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    half = d // 2
+    ang = np.asarray(pos, dtype=np.float64)[..., None] * rope_theta(d, base)
+    c, s = np.cos(ang), np.sin(ang)
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+# =============================================================================== a1: scoring
+@dataclass
+class HeadScores:
+    lse: np.ndarray        # [R] log-sum-exp of each probe row
+    H_rows: np.ndarray     # [R] entropy of each probe row's attention
+    a: np.ndarray          # [R, n] attention probabilities
+    feats: np.ndarray      # [n, 5] (alpha, |v|, sigma, H, pos)
+
+
+def probe_attention(Kh: np.ndarray, Qh: np.ndarray, n: int, P: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Softmax attention of the probe rows over the keys, with the causal mask.
+
+    [GK] "03 Bottom-up value flow": direct attention from the question /
+    sequence-tail probes.  [DC] 3.1.1: the recent queries t-w+1..t.
+    Rows are rho = g*P + p (query head g of this KV group, probe p).  Probe p
+    sits at position n - P + p and sees keys i <= n - P + p (reading R15).
+    Returns (scores s[R, n] with -inf where masked, lse[R]).
+    """
+    G = Qh.shape[0]
+    d = Kh.shape[1]
+    q = np.asarray(Qh, np.float64).reshape(G * P, d)
+    s = q @ np.asarray(Kh, np.float64).T / math.sqrt(d)
+    p_of_row = np.tile(np.arange(P), G)
+    visible = np.arange(n)[None, :] <= (n - P + p_of_row)[:, None]
+    s = np.where(visible, s, -np.inf)
+    m = s.max(axis=1)
+    lse = m + np.log(np.exp(s - m[:, None]).sum(axis=1))
+    return s, lse
+
+
+def score_head(Kh: np.ndarray, Vh: np.ndarray, Qh: np.ndarray, n: int, P: int) -> HeadScores:
+    """Row statistics and the five per-token features of [DC] 3.1.1.
+
+    alpha_i  = mean over probe rows of a_rho(i)
+    |v_i|    = L2 norm of the value
+    sigma_i  = population variance over the G query heads of mean_p a_{g,p}(i)
+               (reading R14: "variance across heads" within the KV group)
+    H_i      = sum_rho a_rho(i) H(a_rho) / sum_rho a_rho(i)
+    pos_i    = i / (n - 1)
+    """
+    G = Qh.shape[0]
+    s, lse = probe_attention(Kh, Qh, n, P)
+    a = np.exp(s - lse[:, None])                       # masked entries -> exp(-inf) = 0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        alog = np.where(a > 0, a * np.log(np.where(a > 0, a, 1.0)), 0.0)
+    H_rows = -alog.sum(axis=1)
+    alpha = a.mean(axis=0)
+    vnorm = np.linalg.norm(np.asarray(Vh, np.float64), axis=1)
+    mass = a.sum(axis=0)
+    Hi = np.where(mass > 0, (a * H_rows[:, None]).sum(axis=0) / np.where(mass > 0, mass, 1.0), 0.0)
+    mg = a.reshape(G, P, n).mean(axis=1)
+    sigma = ((mg - mg.mean(axis=0)) ** 2).mean(axis=0)
+    pos = np.arange(n, dtype=np.float64) / max(n - 1, 1)
+    feats = np.stack([alpha, vnorm, sigma, Hi, pos], axis=1)
+    return HeadScores(lse=lse, H_rows=H_rows, a=a, feats=feats)
+
+
+# =============================================================================== a2: hops
+def top_indices(x: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the k largest entries, ties broken toward the lower index (R13)."""
+    order = np.lexsort((np.arange(x.shape[0]), -x))
+    return order[:k]
+
+
+def hop_relevance(alpha: np.ndarray, Kh: np.ndarray, Vh: np.ndarray, S_h: int,
+                  hop_weight: float, n_hops: int):
+    """Two rounds of token-to-token relevance propagation ([GK] "03", defaults:
+    two graph hops with weight 0.3), reading R2:
+
+        r^0 = alpha
+        seeds_k = the S_h tokens with the largest r^(k-1)
+        Prop_j  = sum_{s in seeds_k} r^(k-1)_s * softmax_j(v_s . k_j / sqrt(d))   (all j < n)
+        r^k     = r^0 + hop_weight * Prop
+
+    Returns (r^(n_hops), list of seed index arrays).
+    """
+    K = np.asarray(Kh, np.float64)
+    V = np.asarray(Vh, np.float64)
+    d = K.shape[1]
+    r0 = np.asarray(alpha, np.float64)
+    r = r0.copy()
+    seeds_all = []
+    for _ in range(n_hops):
+        seeds = top_indices(r, min(S_h, r.shape[0]))
+        sc = V[seeds] @ K.T / math.sqrt(d)
+        sc -= sc.max(axis=1, keepdims=True)
+        A = np.exp(sc)
+        A /= A.sum(axis=1, keepdims=True)
+        prop = (r[seeds][:, None] * A).sum(axis=0)
+        r = r0 + hop_weight * prop
+        seeds_all.append(seeds)
+    return r, seeds_all
+
+
+# =============================================================================== a3: trees and prototypes
+def tree_nodes(x: int, y: int) -> List[Tuple[int, int]]:
+    """The 15 prototype nodes of a slot [x, y) in breadth-first order (reading R3).
+
+    Node j has children 2j+1 and 2j+2; a node [a, b) splits at floor((a+b)/2).
+    Nodes 7..14 are the leaf prototypes; splitting one yields its tokens.
+    """
+    nodes = [(x, y)]
+    for j in range(7):
+        a, b = nodes[j]
+        mid = (a + b) // 2
+        nodes.append((a, mid))
+        nodes.append((mid, b))
+    return nodes
+
+
+def node_parent(j: int) -> int:
+    return -1 if j == 0 else (j - 1) // 2
+
+
+@dataclass
+class Prototype:
+    k_hat: np.ndarray   # [d] post-RoPE key at the representative position
+    v_hat: np.ndarray   # [d]
+    log_m: float
+    p_bar: float
+    m: float
+    kappa: float
+
+
+def prototype(Kpost: np.ndarray, V: np.ndarray, r: np.ndarray, x: int, y: int,
+              base: float, value_floor: float) -> Prototype:
+    """One merged cache entry for tokens [x, y) ([GK] "Inside one cache entry").
+
+    Key: inverse-rotate the post-RoPE keys to a shared frame, average, rotate
+    again at the representative position p_bar = (x + y - 1) / 2 (R8).
+    Multiplicity: m = c * clamp(kappa, 1/c, 1) with kappa the mean cosine of
+    each unrotated key to the unrotated mean (R7).
+    Value: weights w_i = (1 - f) r_i / sum r + f / c with f = value_floor
+    (uniform weights when sum r = 0).
+    """
+    c = y - x
+    pos = np.arange(x, y, dtype=np.float64)
+    ktil = rope_rotate(Kpost, -pos, base)
+    kbar = ktil.mean(axis=0)
+    p_bar = (x + y - 1) / 2.0
+    k_hat = rope_rotate(kbar, p_bar, base)
+    nb = np.linalg.norm(kbar)
+    nk = np.linalg.norm(ktil, axis=1)
+    cos = np.where((nk > 0) & (nb > 0), (ktil @ kbar) / np.where(nk * nb > 0, nk * nb, 1.0), 0.0)
+    kappa = float(cos.mean())
+    m = c * min(max(kappa, 1.0 / c), 1.0)
+    r = np.asarray(r, np.float64)
+    rs = r.sum()
+    w = (1.0 - value_floor) * r / rs + value_floor / c if rs > 0 else np.full(c, 1.0 / c)
+    v_hat = w @ np.asarray(V, np.float64)
+    return Prototype(k_hat=k_hat, v_hat=v_hat, log_m=math.log(m), p_bar=p_bar, m=m, kappa=kappa)
+
+
+# =============================================================================== a4: distortion, value, utility
+def node_distortion(a_node: np.ndarray, Vn: np.ndarray, q: np.ndarray, lse: np.ndarray,
+                    proto: Prototype, nu_bar: float, w_part: float, w_value: float):
+    """Probe-based fidelity of one prototype ([GK] technical details: attention-
+    partition error and value-aggregate error weighed 0.25 : 0.75), reading R4.
+
+    For each probe row rho:  A = sum_{i in N} a(i),  U = sum_{i in N} a(i) v_i,
+    A_hat = exp(q . k_hat / sqrt(d) + log m - LSE),  U_hat = A_hat v_hat.
+        D      = w_part mean|A - A_hat| + w_value mean|U - U_hat|_2 / nu_bar
+        D_drop = w_part mean A          + w_value mean|U|_2 / nu_bar
+    Returns (D, D_drop).
+    """
+    d = q.shape[1]
+    A = a_node.sum(axis=1)
+    U = a_node @ np.asarray(Vn, np.float64)
+    A_hat = np.exp(q @ proto.k_hat / math.sqrt(d) + proto.log_m - lse)
+    U_hat = A_hat[:, None] * proto.v_hat[None, :]
+    part = np.abs(A - A_hat).mean()
+    part_drop = A.mean()
+    if nu_bar > 0:
+        val = np.linalg.norm(U - U_hat, axis=1).mean() / nu_bar
+        val_drop = np.linalg.norm(U, axis=1).mean() / nu_bar
+    else:
+        val = val_drop = 0.0
+    return w_part * part + w_value * val, w_part * part_drop + w_value * val_drop
+
+
+def gain_fraction(x: float, ddrop: float) -> float:
+    """Fidelity gain as a fraction of the drop distortion, clamped to [0, 1] (R4)."""
+    if not ddrop > 0:
+        return 0.0
+    return min(max(x / ddrop, 0.0), 1.0)
+
+
+def slot_ops(D: np.ndarray, Ddrop: np.ndarray, Rv: np.ndarray, sizes: np.ndarray, sens: float):
+    """Utilities and costs of the 16 ops of one slot tree ([GK] "04 Top-down
+    budget flow": utility per entry = relevance x fidelity gain x head
+    sensitivity / new physical entries).
+
+    Add: cost 1, gain = 1 - D(root)/D_drop(root).
+    Split(internal N): cost 1, gain = (D(N) - D(c1) - D(c2)) / D_drop(N).
+    Split(leaf N of c tokens): cost c - 1, gain = D(N) / D_drop(N) (tokens are exact).
+    Relevance of a node is the sum of its tokens' relevance ([GK] "03": parent
+    value = sum of child values).
+    """
+    util = np.zeros(N_OPS, dtype=np.float64)
+    cost = np.zeros(N_OPS, dtype=np.int64)
+    cost[0] = 1
+    util[0] = Rv[0] * gain_fraction(Ddrop[0] - D[0], Ddrop[0]) * sens
+    for j in range(N_NODES):
+        if j < FIRST_LEAF:
+            c = 1
+            g = gain_fraction(D[j] - D[2 * j + 1] - D[2 * j + 2], Ddrop[j])
+        else:
+            c = int(sizes[j]) - 1
+            g = gain_fraction(D[j], Ddrop[j])
+        cost[1 + j] = c
+        util[1 + j] = Rv[j] * g * sens / c
+    return util, cost
+
+
+@dataclass
+class HeadResult:
+    lse: np.ndarray
+    feats: np.ndarray
+    r: np.ndarray
+    seeds: List[np.ndarray]
+    util: np.ndarray     # [S, 16] float64
+    cost: np.ndarray     # [S, 16] int64
+    D: np.ndarray        # [S, 15]
+    Ddrop: np.ndarray    # [S, 15]
+    protos: Optional[List[List[Prototype]]] = None
+
+
+def score_and_value_head(Kh, Vh, Qh, n: int, P: int, bounds: np.ndarray, sens: float,
+                         base: float = 10000.0, hop_weight: float = 0.3, n_hops: int = 2,
+                         w_part: float = 0.25, w_value: float = 0.75, value_floor: float = 0.1,
+                         S_h: Optional[int] = None, keep_protos: bool = False) -> HeadResult:
+    """Everything the scoring call produces for one (layer, KV head): a1 -> a4."""
+    Kh = np.asarray(Kh, np.float64)
+    Vh = np.asarray(Vh, np.float64)
+    G = Qh.shape[0]
+    d = Kh.shape[1]
+    sc = score_head(Kh, Vh, Qh, n, P)
+    S_h = P if S_h is None else S_h
+    r, seeds = hop_relevance(sc.feats[:, 0], Kh, Vh, S_h, hop_weight, n_hops)
+    q = np.asarray(Qh, np.float64).reshape(G * P, d)
+    nu_bar = float(sc.feats[:, 1].mean())
+    S = len(bounds) - 1
+    util = np.zeros((S, N_OPS))
+    cost = np.zeros((S, N_OPS), dtype=np.int64)
+    Dall = np.zeros((S, N_NODES))
+    Ddall = np.zeros((S, N_NODES))
+    protos_all = []
+    for s in range(S):
+        x0, y0 = int(bounds[s]), int(bounds[s + 1])
+        nodes = tree_nodes(x0, y0)
+        D = np.zeros(N_NODES)
+        Dd = np.zeros(N_NODES)
+        Rv = np.zeros(N_NODES)
+        sizes = np.zeros(N_NODES, dtype=np.int64)
+        plist = []
+        for j, (x, y) in enumerate(nodes):
+            pr = prototype(Kh[x:y], Vh[x:y], r[x:y], x, y, base, value_floor)
+            D[j], Dd[j] = node_distortion(sc.a[:, x:y], Vh[x:y], q, sc.lse, pr, nu_bar,
+                                          w_part, w_value)
+            Rv[j] = r[x:y].sum()
+            sizes[j] = y - x
+            plist.append(pr)
+        util[s], cost[s] = slot_ops(D, Dd, Rv, sizes, sens)
+        Dall[s], Ddall[s] = D, Dd
+        if keep_protos:
+            protos_all.append(plist)
+    return HeadResult(lse=sc.lse, feats=sc.feats, r=r, seeds=seeds, util=util, cost=cost,
+                      D=Dall, Ddrop=Ddall, protos=protos_all if keep_protos else None)
+
+
+# =============================================================================== a5: budget, floor, auction
+def budget(n: int, L: int, H: int, W: int, budget_ratio: float, budget_entries_per_lh: int,
+           floor_cap_frac: float):
+    """Physical budget of one sequence ([GK] "Core idea": one stored K/V pair is
+    one budget unit; the recent window is exact and counts toward the budget).
+
+    B_tot = floor(beta * n) * L * H (or entries_per_lh * L * H), reading R11;
+    B_alloc = B_tot - W * L * H; floor cap = floor(frac * B_alloc) entries (R6).
+    """
+    per_lh = budget_entries_per_lh if budget_entries_per_lh > 0 else int(math.floor(budget_ratio * n))
+    B_tot = per_lh * L * H
+    B_alloc = B_tot - W * L * H
+    if B_alloc < 0:
+        raise ValueError("budget smaller than the recent window")
+    cap = int(math.floor(floor_cap_frac * B_alloc))
+    return B_tot, B_alloc, cap
+
+
+def _leaf_of(i: int, x0: int, y0: int) -> Tuple[int, List[int]]:
+    """Leaf node containing token i and the node path root..leaf."""
+    nodes = tree_nodes(x0, y0)
+    j = 0
+    path = [0]
+    while j < FIRST_LEAF:
+        c1 = 2 * j + 1
+        j = c1 if i < nodes[c1][1] else c1 + 1
+        path.append(j)
+    return j, path
+
+
+@dataclass
+class Selection:
+    taken: np.ndarray        # bool [L, H, S, 16]
+    floor_spent: int
+    floor_tokens: int
+    auction_spent: int
+    B_tot: int
+    B_alloc: int
+    lens: np.ndarray         # int [L, H] entries per (l, h) incl. window
+
+
+def singleton_floor(r: np.ndarray, sens: np.ndarray, bounds: np.ndarray, cost: np.ndarray,
+                    cap_entries: int, cap_tokens: int, taken: np.ndarray):
+    """Capped singleton floor before the auction ([GK] "Exact-information
+    safeguard" and technical details), reading R6.
+
+    Candidates: every compressible (l, h, i) with r_i > 0, in order of
+    (r_i * sens[l, h] descending, (l, h, i) ascending).  A candidate's path is
+    Add(slot), Split of each ancestor, Split of its leaf prototype; its cost is
+    the cost of the path ops not yet taken (shared ancestors paid once).  A
+    token already exact is skipped at no cost.  If the path fits in the cap it
+    is taken and the token counted, otherwise the floor stops; it also stops
+    once cap_tokens tokens are counted (cap_tokens < 0: no token cap).
+    The key r * sens is computed in the precision of ``r``.
+    Mutates ``taken`` and returns (spent, tokens).
+    """
+    L, H, n_ = r.shape
+    end = int(bounds[-1])
+    S = len(bounds) - 1
+    keys = r[:, :, :end] * sens.astype(r.dtype)[:, :, None]
+    keys = keys.astype(r.dtype)
+    flat = keys.reshape(-1)
+    lhs = np.repeat(np.arange(L * H), end)
+    ii = np.tile(np.arange(end), L * H)
+    cand = (r[:, :, :end].reshape(-1) > 0)
+    cidx = lhs.astype(np.int64) * n_ + ii
+    sel = np.nonzero(cand)[0]
+    order = sel[np.lexsort((cidx[sel], -flat[sel].astype(np.float64)))]
+    slot_of = np.searchsorted(bounds, np.arange(end), side="right") - 1
+    spent = 0
+    tokens = 0
+    for k in order:
+        if cap_tokens >= 0 and tokens >= cap_tokens:
+            break
+        lh = int(lhs[k]); i = int(ii[k])
+        l, h = divmod(lh, H)
+        s = int(slot_of[i])
+        x0, y0 = int(bounds[s]), int(bounds[s + 1])
+        leaf, path = _leaf_of(i, x0, y0)
+        t = taken[l, h, s]
+        if t[1 + leaf]:
+            continue                                   # already exact
+        ops = [0] + [1 + j for j in path]
+        c = sum(int(cost[l, h, s, o]) for o in ops if not t[o])
+        if spent + c <= cap_entries:
+            for o in ops:
+                t[o] = True
+            spent += c
+            tokens += 1
+        else:
+            break
+    return spent, tokens
+
+
+def op_parent(o: int) -> int:
+    """Op whose taking exposes op o (-1 for Add)."""
+    if o == 0:
+        return -1
+    j = o - 1
+    return 0 if j == 0 else 1 + node_parent(j)
+
+
+def greedy_auction(util: np.ndarray, cost: np.ndarray, taken: np.ndarray, remaining: int) -> int:
+    """Global greedy Add/Split auction ([GK] "04 Top-down budget flow").
+
+    One queue holds every exposed op of every (l, h, slot): Add for an absent
+    slot, Split for a present, unsplit prototype.  Repeatedly pop the highest
+    (utility desc, op id asc) op; if its cost fits in the remaining budget take
+    it and expose its children's Splits, otherwise discard it (its subtree is
+    never exposed).  Runs until the queue is empty; zero-utility ops are still
+    bought while budget lasts.  Op id = ((l*H + h)*S + slot)*16 + local.
+    Mutates ``taken``; returns the entries spent.
+    """
+    L, H, S, _ = util.shape
+    heap = []
+
+    def push(l, h, s, o):
+        gid = ((l * H + h) * S + s) * N_OPS + o
+        heapq.heappush(heap, (-float(util[l, h, s, o]), gid, l, h, s, o))
+
+    for l in range(L):
+        for h in range(H):
+            for s in range(S):
+                t = taken[l, h, s]
+                if not t[0]:
+                    push(l, h, s, 0)
+                    continue
+                for j in range(N_NODES):
+                    present = t[0] if j == 0 else t[1 + node_parent(j)]
+                    if present and not t[1 + j]:
+                        push(l, h, s, 1 + j)
+    spent = 0
+    while heap:
+        _, _, l, h, s, o = heapq.heappop(heap)
+        c = int(cost[l, h, s, o])
+        if c <= remaining:
+            taken[l, h, s, o] = True
+            remaining -= c
+            spent += c
+            if o == 0:
+                push(l, h, s, 1)
+            else:
+                j = o - 1
+                if j < FIRST_LEAF:
+                    push(l, h, s, 1 + 2 * j + 1)
+                    push(l, h, s, 1 + 2 * j + 2)
+    return spent
+
+
+def select_sequence(util: np.ndarray, cost: np.ndarray, r: np.ndarray, sens: np.ndarray,
+                    bounds: np.ndarray, n: int, W: int, budget_ratio: float,
+                    budget_entries_per_lh: int, floor_cap_frac: float, floor_cap_tokens: int) -> Selection:
+    """Budget -> singleton floor -> greedy auction for one sequence (a5)."""
+    L, H, S, _ = util.shape
+    B_tot, B_alloc, cap = budget(n, L, H, W, budget_ratio, budget_entries_per_lh, floor_cap_frac)
+    taken = np.zeros((L, H, S, N_OPS), dtype=bool)
+    fs, ft = singleton_floor(r, sens, bounds, cost, min(cap, B_alloc), floor_cap_tokens, taken)
+    asp = greedy_auction(util, cost, taken, B_alloc - fs)
+    lens = W + (taken * cost).sum(axis=(2, 3))
+    return Selection(taken=taken, floor_spent=fs, floor_tokens=ft, auction_spent=asp,
+                     B_tot=B_tot, B_alloc=B_alloc, lens=lens.astype(np.int64))
+
+
+# =============================================================================== a6: pack
+def frontier(t: np.ndarray, x0: int, y0: int) -> List[Tuple[str, int]]:
+    """Stored entries of one slot tree, left to right ([GK] "05 Physical cache
+    packing"): an absent root stores nothing, a present unsplit node stores its
+    prototype, a split leaf prototype stores its tokens exactly."""
+    nodes = tree_nodes(x0, y0)
+
+    def visit(j):
+        if not t[1 + j]:
+            return [("node", j)]
+        if j < FIRST_LEAF:
+            return visit(2 * j + 1) + visit(2 * j + 2)
+        a, b = nodes[j]
+        return [("tok", i) for i in range(a, b)]
+
+    return visit(0) if t[0] else []
+
+
+@dataclass
+class Packed:
+    K: List[np.ndarray]      # per (b, l, h) flattened index: [len, d]
+    V: List[np.ndarray]
+    logm: List[np.ndarray]
+    pos: List[np.ndarray]
+    lens: np.ndarray         # [B, L, H]
+    caps: np.ndarray         # [B, L, H]
+    offs: np.ndarray         # [B, L, H] exclusive prefix sum of caps in (b, l, h) order
+
+
+def pack_head(Kh, Vh, r, bounds, t_lh, n: int, W: int, base: float, value_floor: float):
+    """Entries of one (l, h): slots ascending, frontier left to right, then the
+    window tokens [n - W, n).  Exact tokens keep their K/V and get log m = 0."""
+    Kh = np.asarray(Kh, np.float64)
+    Vh = np.asarray(Vh, np.float64)
+    ks, vs, lm, ps = [], [], [], []
+    for s in range(len(bounds) - 1):
+        x0, y0 = int(bounds[s]), int(bounds[s + 1])
+        nodes = tree_nodes(x0, y0)
+        for kind, j in frontier(t_lh[s], x0, y0):
+            if kind == "tok":
+                ks.append(Kh[j]); vs.append(Vh[j]); lm.append(0.0); ps.append(float(j))
+            else:
+                x, y = nodes[j]
+                pr = prototype(Kh[x:y], Vh[x:y], r[x:y], x, y, base, value_floor)
+                ks.append(pr.k_hat); vs.append(pr.v_hat); lm.append(pr.log_m); ps.append(pr.p_bar)
+    for i in range(n - W, n):
+        ks.append(Kh[i]); vs.append(Vh[i]); lm.append(0.0); ps.append(float(i))
+    d = Kh.shape[1]
+    return (np.asarray(ks).reshape(-1, d), np.asarray(vs).reshape(-1, d),
+            np.asarray(lm, np.float64), np.asarray(ps, np.float64))
+
+
+def offsets(lens: np.ndarray, reserve: int):
+    caps = lens + reserve
+    flat = caps.reshape(-1)
+    offs = np.concatenate([[0], np.cumsum(flat)[:-1]]).reshape(caps.shape)
+    return caps, offs
+
+
+# =============================================================================== a7: decode
+def decode_head(q: np.ndarray, Kp: np.ndarray, Vp: np.ndarray, logm: np.ndarray) -> np.ndarray:
+    """GQA attention of the G query heads of one KV head over its ragged entries
+    with the +log m multiplicity bias ([GK] "Inside one cache entry", "05")."""
+    q = np.asarray(q, np.float64)
+    d = q.shape[-1]
+    s = q @ np.asarray(Kp, np.float64).T / math.sqrt(d) + np.asarray(logm, np.float64)[None, :]
+    s -= s.max(axis=1, keepdims=True)
+    p = np.exp(s)
+    p /= p.sum(axis=1, keepdims=True)
+    return p @ np.asarray(Vp, np.float64)
+
+
+def decode_step_head(q, k_new, v_new, Kp, Vp, logm):
+    """Append (k_new, v_new) with multiplicity 1, then attend over all entries
+    including it (reading R10).  Returns (out [G, d], Kp', Vp', logm')."""
+    Kp2 = np.concatenate([np.asarray(Kp, np.float64), np.asarray(k_new, np.float64)[None]], 0)
+    Vp2 = np.concatenate([np.asarray(Vp, np.float64), np.asarray(v_new, np.float64)[None]], 0)
+    lm2 = np.concatenate([np.asarray(logm, np.float64), [0.0]])
+    return decode_head(q, Kp2, Vp2, lm2), Kp2, Vp2, lm2
+
+
+# =============================================================================== a0: partition
+def curvature(hidden: np.ndarray, scales: Sequence[int] = (1, 2, 4, 8)) -> np.ndarray:
+    """Multi-scale curvature of the normalized hidden-state trajectory ([GK]
+    "01 Curvature-guided partition"), reading R1:
+    kappa_w(t) = 1 - cos(h_t - h_{t-w}, h_{t+w} - h_t), averaged over the
+    scales w that fit (0 where none fits)."""
+    h = np.asarray(hidden, np.float64)
+    h = h / np.linalg.norm(h, axis=1, keepdims=True)
+    n = h.shape[0]
+    tot = np.zeros(n)
+    cnt = np.zeros(n)
+    for w in scales:
+        if n <= 2 * w:
+            continue
+        a = h[w:n - w] - h[:n - 2 * w]
+        b = h[2 * w:] - h[w:n - w]
+        na = np.linalg.norm(a, axis=1)
+        nb = np.linalg.norm(b, axis=1)
+        cos = np.where(na * nb > 0, (a * b).sum(1) / np.where(na * nb > 0, na * nb, 1.0), 1.0)
+        tot[w:n - w] += 1.0 - cos
+        cnt[w:n - w] += 1
+    return np.where(cnt > 0, tot / np.maximum(cnt, 1), 0.0)
+
+
+def partition_dp(kappa: np.ndarray, end: int, lmin: int = 16, lmax: int = 128,
+                 target: int = 64, lam: Optional[float] = None) -> np.ndarray:
+    """Dynamic program over cut positions in [0, end) (reading R1).
+
+    Maximise sum over interior cuts c of kappa(c) - lam * sum over slots of
+    ((len - target) / target)^2, with lmin <= len <= lmax; lam defaults to the
+    mean of kappa over [0, end).  Ties go to the smaller previous cut.
+    """
+    k = np.asarray(kappa, np.float64)
+    if lam is None:
+        lam = float(k[:end].mean()) if end > 0 else 0.0
+    NEG = -np.inf
+    best = np.full(end + 1, NEG)
+    prev = np.full(end + 1, -1, dtype=np.int64)
+    best[0] = 0.0
+    for y in range(1, end + 1):
+        gain_cut = k[y] if y < end else 0.0
+        for ln in range(lmin, lmax + 1):
+            x = y - ln
+            if x < 0:
+                break
+            if best[x] == NEG:
+                continue
+            v = best[x] - lam * ((ln - target) / target) ** 2 + gain_cut
+            if v > best[y] or (v == best[y] and x < prev[y]):
+                best[y] = v
+                prev[y] = x
+    if best[end] == NEG:
+        raise ValueError("no feasible partition")
+    cuts = [end]
+    y = end
+    while y > 0:
+        y = int(prev[y])
+        cuts.append(y)
+    return np.asarray(cuts[::-1], dtype=np.int32)
