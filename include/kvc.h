@@ -1,0 +1,210 @@
+/*
+ * kvc.h - C ABI of libkvc: budgeted KV-cache compression after prefill and
+ * GQA decode attention over the compressed (ragged) cache, for one GB300
+ * (sm_103a).
+ *
+ * The method follows two public pages:
+ *   [GK] "GraceKV - Every Cache Entry Earns Its Place: Global Allocation of
+ *        Resolution and Coverage for KV Cache Compression" (project page),
+ *   [DC] "DistillCache: KL-Guided Adaptive KV-Cache Eviction for
+ *        Memory-Efficient LLM Inference", section 3.1.1 (token features).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every pointer argument is caller-owned DEVICE memory unless the comment
+ *    says "host".  The library allocates nothing: scratch comes from the
+ *    caller's workspace (size from kvc_workspace_bytes).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL = the legacy default stream).  Argument errors are detected on the
+ *    host before anything is launched and return a negative status.
+ *  - Values the host cannot see (per-sequence lengths, slot boundaries,
+ *    append capacity) are checked on the device; a violation records a code in
+ *    the library's device error word and the offending unit is skipped.  Read
+ *    and clear it with kvc_device_error().  No kernel traps or asserts.
+ *  - Layouts (all row-major, contiguous).  "(l,h)" = (layer, KV head).
+ *      token arrays   sequence b occupies a block starting at token
+ *                     T_b = sum_{b'<b} L*H*n_{b'}; token i of (l,h) is row
+ *                     T_b + (l*H + h)*n_b + i.  K, V: [rows, d] in `dtype`;
+ *                     feats: [rows, 5] f32; relevance: [rows] f32.
+ *      probes Qp      [B, L, H*G, P, d] in `dtype`; query head h*G + g serves
+ *                     KV head h; probe p sits at position n_b - P + p.
+ *      lse            [B, L, H, R] f32 with R = G*P, row rho = g*P + p.
+ *      slot_bounds    [B, S_max + 1] int32, slots of b cover [0, n_b - W).
+ *      ops            [B, L, H, S_max, 16]: op 0 = Add(slot), op 1 + j =
+ *                     Split(node j) of the slot's depth-3 midpoint tree
+ *                     (nodes in breadth-first order, 7..14 = leaf prototypes).
+ *      per-(l,h)      [B, L, H] arrays (len_lh, cap_lh, off_lh).
+ *      packed cache   Kp, Vp: [capacity, d] in `dtype`; logm, pos: [capacity]
+ *                     f32.  Entries of (b,l,h) start at row off_lh[b,l,h].
+ *      decode         q, out: [B, L, H*G, d]; k_new, v_new: [B, L, H, d].
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes --------------------------------------------------------- */
+#define KVC_OK          0
+#define KVC_EINVAL     -1   /* bad argument (null pointer, shape, unsupported size) */
+#define KVC_EBUDGET    -2   /* budget smaller than the exact recent window          */
+#define KVC_ECAPACITY  -3   /* append past an (l,h)'s reserved capacity             */
+#define KVC_ECUDA      -4   /* a CUDA runtime call failed                           */
+#define KVC_ETIMEOUT   -5   /* a bounded device wait gave up                        */
+#define KVC_EWORKSPACE -6   /* workspace missing or smaller than required           */
+#define KVC_EDEVICE    -7   /* device-side check failed (see kvc_device_error)      */
+
+/* ---- element types -------------------------------------------------------- */
+#define KVC_F32  0
+#define KVC_BF16 1
+
+/* ---- workspace selectors for kvc_workspace_bytes --------------------------- */
+#define KVC_WS_SCORE  0
+#define KVC_WS_SELECT 1
+#define KVC_WS_PACK   2
+#define KVC_WS_DECODE 3
+#define KVC_WS_PARTITION 4
+
+/* One parameter block, passed by const pointer, owned by the caller (host). */
+typedef struct kvc_params {
+  int32_t B;            /* sequences in the batch                                 */
+  int32_t L;            /* layers                                                 */
+  int32_t H;            /* KV heads                                               */
+  int32_t G;            /* query heads per KV head (GQA group), 1..8              */
+  int32_t d;            /* head dim: 64 or 128                                    */
+  int32_t P;            /* probe positions (last P queries), R = G*P <= 256       */
+  int32_t W;            /* exact recent window (tokens per (l,h)), W >= P         */
+  int32_t dtype;        /* KVC_F32 or KVC_BF16 for K, V, Qp, q, packed K/V, out   */
+  int32_t n_max;        /* largest context length in the batch                    */
+  int32_t S_max;        /* largest slot count in the batch (ops are padded to it) */
+  float   rope_base;    /* RoPE base (rotate-half pairing), 10000 by default      */
+  float   hop_weight;   /* [GK] value flow: weight of each relevance hop, 0.3     */
+  int32_t n_hops;       /* [GK] value flow: number of hops, 2                     */
+  float   w_part;       /* [GK] fidelity: attention-partition error weight, 0.25  */
+  float   w_value;      /* [GK] fidelity: value-aggregate error weight, 0.75      */
+  float   value_floor;  /* [GK] value merge: uniform share of the weights, 0.10   */
+  double  budget_ratio; /* beta: floor(beta*n) entries per (l,h), pooled          */
+  int64_t budget_entries_per_lh; /* > 0 overrides budget_ratio                    */
+  double  floor_cap_frac;  /* [GK] singleton floor cap, fraction of B_alloc (0.6)  */
+  int64_t floor_cap_tokens;/* token cap of the floor; < 0 = none                   */
+  int32_t decode_reserve;  /* rows reserved per (l,h) for decode-time appends      */
+} kvc_params;
+
+/* Human-readable name of a status code (static string). */
+const char* kvc_status_string(int status);
+
+/* Reads and clears the device error word (synchronises `stream`).  Returns
+ * KVC_OK and writes 0 to *code when nothing was recorded, otherwise writes the
+ * first recorded code (a negative KVC_* value) to *code. */
+int kvc_device_error(void* stream, int32_t* code /* host */);
+
+/* Number of kernels this library has launched since load (host counter). */
+int64_t kvc_launch_count(void);
+
+/* Bytes of workspace `which` (KVC_WS_*) needs for this parameter block.  The
+ * workspace must be 256-byte aligned device memory; its contents need not be
+ * initialised except for KVC_WS_DECODE, which must be zeroed once before its
+ * first use and is left zeroed by every call. */
+size_t kvc_workspace_bytes(int which, const kvc_params* p /* host */);
+
+/* RoPE tables used by kvc_score and kvc_merge_pack.
+ * cos_tab[e, j] = cos((e/2) * theta_j), sin_tab likewise, theta_j =
+ * base^(-2j/d), for e in [0, n_half) and j < d/2; layout [n_half, d/2] f32.
+ * Entry e is position e/2, so half-integer representative positions
+ * ([GK] "Inside one cache entry": rerotate at the span's mean position) index
+ * it exactly.  Angles are formed and evaluated in double precision on the
+ * device.  n_half must be >= 2*n_max. */
+int kvc_rope_table(int32_t d, float base, int64_t n_half, float* cos_tab, float* sin_tab,
+                   void* stream);
+
+/* a1-a4: probe scoring, token features, relevance hops, prototype trees,
+ * distortion and per-entry utilities of every Add/Split op.
+ *   [DC] 3.1.1 (features alpha, |v|, sigma, H, pos); [GK] "03 Bottom-up value
+ *   flow" (direct probes + two hops, parent value = sum of children),
+ *   "Inside one cache entry" (merge math), technical details (0.25 : 0.75
+ *   fidelity), "04 Top-down budget flow" (utility per entry).
+ * In:  ctx_len [B] int32; K, V token arrays; Qp probes; rope tables;
+ *      slot_bounds [B, S_max+1]; n_slots [B] int32; head_sens [L, H] f32 or
+ *      NULL (= 1).
+ * Out: lse [B,L,H,R]; feats [rows,5] (alpha, |v|, sigma, H, pos);
+ *      relevance [rows]; op_util [B,L,H,S_max,16] f32 (0 for padding);
+ *      op_cost [B,L,H,S_max,16] int32 (0 for padding).
+ * Slots must have 16..128 tokens.  Errors: KVC_EINVAL, KVC_EWORKSPACE,
+ * KVC_ECUDA; bad per-sequence values are reported via kvc_device_error. */
+int kvc_score(const kvc_params* p, const int32_t* ctx_len, const void* K, const void* V,
+              const void* Qp, const float* rope_cos, const float* rope_sin,
+              const int32_t* slot_bounds, const int32_t* n_slots, const float* head_sens,
+              float* lse, float* feats, float* relevance, float* op_util, int32_t* op_cost,
+              void* workspace, size_t ws_bytes, void* stream);
+
+/* a5: per-sequence budget, capped singleton floor, global greedy Add/Split
+ * auction ([GK] "Core idea" budget regions, "Exact-information safeguard",
+ * "04 Top-down budget flow").  The result is identical to processing one
+ * queue of exposed ops in (utility desc, op id asc) order, taking each op
+ * whose cost fits the remaining budget and discarding the rest.
+ * In:  relevance (floor keys r*sens), op_util, op_cost from kvc_score.
+ * Out: taken [B,L,H,S_max,16] uint8 (1 = op bought); len_lh [B,L,H] int32
+ *      (stored entries incl. the W window tokens); cap_lh = len_lh +
+ *      decode_reserve; off_lh [B,L,H] int64 exclusive prefix sum of cap_lh in
+ *      (b,l,h) order; total_entries [1] int64 = sum of cap_lh (rows the packed
+ *      cache needs).
+ * Errors: KVC_EINVAL, KVC_EBUDGET (some sequence's budget < its window),
+ * KVC_EWORKSPACE, KVC_ECUDA. */
+int kvc_select(const kvc_params* p, const int32_t* ctx_len, const int32_t* slot_bounds,
+               const int32_t* n_slots, const float* relevance, const float* head_sens,
+               const float* op_util, const int32_t* op_cost, uint8_t* taken, int32_t* len_lh,
+               int32_t* cap_lh, int64_t* off_lh, int64_t* total_entries, void* workspace,
+               size_t ws_bytes, void* stream);
+
+/* a3 + a6: merge each stored frontier node into one entry and pack the ragged
+ * cache ([GK] "05 Physical cache packing"): per (b,l,h), slots ascending, each
+ * slot's frontier left to right, then the window tokens.  A split leaf stores
+ * its tokens bit-exact (log m = 0, pos = i); an unsplit node stores its
+ * prototype (k_hat, v_hat, ln m, mean position).  Rows between len and cap
+ * are left untouched for appends.  capacity = rows of Kp/Vp/logm/pos; a
+ * sequence whose entries would overflow it is skipped and reported via
+ * kvc_device_error.  Errors: KVC_EINVAL, KVC_EWORKSPACE, KVC_ECUDA. */
+int kvc_merge_pack(const kvc_params* p, const int32_t* ctx_len, const void* K, const void* V,
+                   const float* relevance, const float* rope_cos, const float* rope_sin,
+                   const int32_t* slot_bounds, const int32_t* n_slots, const uint8_t* taken,
+                   const int32_t* len_lh, const int64_t* off_lh, void* Kp, void* Vp,
+                   float* logm, float* pos, int64_t capacity, void* workspace, size_t ws_bytes,
+                   void* stream);
+
+/* a7: one decode step over the ragged cache, all layers in one launch
+ * ([GK] "05": new tokens are appended with multiplicity one; decode attends
+ * with the +ln m bias).  For every (b,l,h) the new (k_new, v_new) is appended
+ * at row off_lh + len_lh (log m = 0, pos = pos_new[b]) and the G query heads
+ * attend over all len_lh + 1 entries:
+ *   out = sum_e softmax_e(q . k_e / sqrt(d) + logm_e) v_e   (fp32 softmax).
+ * len_lh is incremented on the device.  An (l,h) with len_lh + 1 > cap_lh
+ * still attends (including the new token) but is not appended and reports
+ * KVC_ECAPACITY via kvc_device_error.  pos_new may be NULL.
+ * Workspace KVC_WS_DECODE holds split-K partials and per-(b,l,h) arrival
+ * counters (zero before first use; every call leaves them zero).
+ * Errors: KVC_EINVAL, KVC_EWORKSPACE, KVC_ECUDA. */
+int kvc_decode_attn(const kvc_params* p, const void* q, const void* k_new, const void* v_new,
+                    const float* pos_new, void* Kp, void* Vp, float* logm, float* pos,
+                    int32_t* len_lh, const int32_t* cap_lh, const int64_t* off_lh, void* out,
+                    void* workspace, size_t ws_bytes, void* stream);
+
+/* a0: curvature-guided slot partition ([GK] "01 Curvature-guided
+ * partition"): kappa(t) = mean over w in {1,2,4,8} of
+ * 1 - cos(h_t - h_{t-w}, h_{t+w} - h_t) on L2-normalised hidden states, then a
+ * dynamic program over cuts in [0, n_b - W) maximising
+ * sum kappa(cuts) - lambda * sum ((len - 64)/64)^2 with 16 <= len <= 128 and
+ * lambda = mean kappa.  hidden: [B, n_max, dh] in `dtype` (rows beyond n_b
+ * unused).  Out: kappa [B, n_max] f32, slot_bounds [B, S_max+1], n_slots [B].
+ * A sequence needing more than S_max slots reports KVC_EDEVICE. */
+int kvc_partition(const kvc_params* p, const int32_t* ctx_len, const void* hidden, int32_t dh,
+                  float* kappa, int32_t* slot_bounds, int32_t* n_slots, void* workspace,
+                  size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVC_H */

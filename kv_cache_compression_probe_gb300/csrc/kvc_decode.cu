@@ -1,0 +1,317 @@
+// a7: ragged GQA decode attention with the +ln m multiplicity bias and the
+// multiplicity-one append of the new token (GraceKV "05 Physical cache
+// packing": new tokens are appended with multiplicity one; the decoder attends
+// over each (layer, head)'s independently sized cache).
+//
+// Design (HBM-bound): one launch covers every (sequence, layer, KV head).  The
+// entries of an (l,h) are split into chunks of kChunk rows; one 128-thread CTA
+// streams a chunk.  Inside a warp each lane owns d/32 consecutive features of
+// every K/V row (a row is one fully coalesced 256-byte read for bf16, d=128),
+// the G query heads' partial dot products of 32/G rows are reduced with one
+// 31-shuffle transpose, and the softmax runs online in base 2.  Chunk partials
+// (max, sum, unnormalised output) go to the workspace; the last CTA of an
+// (l,h) to arrive (atomic counter, no waiting) merges them in log-sum-exp form.
+// A second tiny kernel commits the append (len += 1) after every chunk has read
+// the old length.
+#include <math.h>
+
+#include "kvc_common.cuh"
+#include "kvc_internal.h"
+
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kWarps = kThreads / 32;
+constexpr int kChunk = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DecodeArgs {
+  const void* q;
+  const void* k_new;
+  const void* v_new;
+  const float* pos_new;
+  void* Kp;
+  void* Vp;
+  float* logm;
+  float* pos;
+  const int32_t* len_lh;
+  const int32_t* cap_lh;
+  const int64_t* off_lh;
+  void* out;
+  float* partials;     // [BLH, n_chunk_max, G, D + 2]
+  int32_t* counters;   // [BLH], zero between calls
+  int H, L, n_chunk_max;
+  float scale_log2;    // log2(e) / sqrt(d)
+  int32_t* err;
+};
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kThreads) decode_chunk_kernel(DecodeArgs a) {
+  constexpr int VPL = D / 32;   // features per lane
+  constexpr int EB = 32 / G;    // rows per warp batch (EB * G = 32 dot products)
+  const int blh = blockIdx.y;
+  const int c = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int len = a.len_lh[blh];
+  const int E = len + 1;                                 // stored rows + the new token
+  const int nchunks = (E + kChunk - 1) / kChunk;
+  if (len < 0 || nchunks > a.n_chunk_max) {              // corrupt length: skip this (l,h)
+    if (c == 0 && tid == 0) kvcd::record_error(a.err, KVC_EDEVICE);
+    return;
+  }
+  if (c >= nchunks) return;
+  const int e0 = c * kChunk, e1 = min(e0 + kChunk, E);
+  const int64_t off = a.off_lh[blh];
+  const bool append_ok = (len + 1 <= a.cap_lh[blh]);
+  const int h = blh % a.H;
+  const int64_t bl = blh / a.H;                          // b * L + l
+
+  const T* Kp = static_cast<const T*>(a.Kp) + off * D;
+  const T* Vp = static_cast<const T*>(a.Vp) + off * D;
+  const float* lm = a.logm + off;
+  const T* kn = static_cast<const T*>(a.k_new) + (int64_t)blh * D;
+  const T* vn = static_cast<const T*>(a.v_new) + (int64_t)blh * D;
+  const T* qp = static_cast<const T*>(a.q) + (bl * a.H * G + (int64_t)h * G) * D;
+
+  float qv[G][VPL];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    kvcd::VecLoad<T, VPL>::ld(qp + g * D + lane * VPL, qv[g]);
+#pragma unroll
+    for (int t = 0; t < VPL; ++t) qv[g][t] *= a.scale_log2;
+  }
+
+  __shared__ float s_p[kWarps][32];
+  __shared__ float s_m[kWarps][G], s_l[kWarps][G];
+  __shared__ float s_o[kWarps][G][D];
+
+  float m_run[G], o[G][VPL];
+  float lsum = 0.f;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    m_run[g] = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < VPL; ++t) o[g][t] = 0.f;
+  }
+  const int gj = lane % G, kj = lane / G;
+
+  for (int eb = e0 + warp * EB; eb < e1; eb += kWarps * EB) {
+    float kk[EB][VPL], vv[EB][VPL];
+#pragma unroll
+    for (int k = 0; k < EB; ++k) {
+      const int e = eb + k;
+      if (e < len && e < e1) {
+        kvcd::VecLoad<T, VPL>::ld(Kp + (int64_t)e * D + lane * VPL, kk[k]);
+        kvcd::VecLoad<T, VPL>::ld(Vp + (int64_t)e * D + lane * VPL, vv[k]);
+      } else if (e == len) {
+        kvcd::VecLoad<T, VPL>::ld(kn + lane * VPL, kk[k]);
+        kvcd::VecLoad<T, VPL>::ld(vn + lane * VPL, vv[k]);
+      } else {
+#pragma unroll
+        for (int t = 0; t < VPL; ++t) kk[k][t] = vv[k][t] = 0.f;
+      }
+    }
+    // 32 partial dot products (row k, head g) -> index k * G + g
+    float part[32];
+#pragma unroll
+    for (int k = 0; k < EB; ++k)
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float acc = 0.f;
+#pragma unroll
+        for (int t = 0; t < VPL; ++t) acc = fmaf(qv[g][t], kk[k][t], acc);
+        part[k * G + g] = acc;
+      }
+    // transpose-reduce: afterwards lane j holds the full sum of index j
+#pragma unroll
+    for (int o_ = 16, n = 32; o_ >= 1; o_ >>= 1, n >>= 1) {
+      const bool upper = (lane & o_) != 0;
+#pragma unroll
+      for (int i = 0; i < n / 2; ++i) {
+        const float send = upper ? part[i] : part[i + n / 2];
+        const float keep = upper ? part[i + n / 2] : part[i];
+        part[i] = keep + __shfl_xor_sync(KVC_FULL_MASK, send, o_);
+      }
+    }
+    const int ej = eb + kj;
+    float s = -INFINITY;
+    if (ej < e1) s = part[0] + (ej < len ? __ldg(lm + ej) * kLog2e : 0.f);
+    float gm = s;
+#pragma unroll
+    for (int o_ = G; o_ < 32; o_ <<= 1) gm = fmaxf(gm, __shfl_xor_sync(KVC_FULL_MASK, gm, o_));
+    float alpha[G];
+    float my_m = -INFINITY, my_alpha = 1.f;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float mb = __shfl_sync(KVC_FULL_MASK, gm, g);
+      const float mn = fmaxf(m_run[g], mb);
+      alpha[g] = (mn == -INFINITY) ? 1.f : exp2f(m_run[g] - mn);
+      m_run[g] = mn;
+      if (g == gj) { my_m = mn; my_alpha = alpha[g]; }
+    }
+    const float pr = (s == -INFINITY) ? 0.f : exp2f(s - my_m);
+    lsum = lsum * my_alpha + pr;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int t = 0; t < VPL; ++t) o[g][t] *= alpha[g];
+    s_p[warp][lane] = pr;
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < EB; ++k)
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float pk = s_p[warp][k * G + g];
+#pragma unroll
+        for (int t = 0; t < VPL; ++t) o[g][t] = fmaf(pk, vv[k][t], o[g][t]);
+      }
+    __syncwarp();
+  }
+  // per-head row sums of this warp
+#pragma unroll
+  for (int o_ = G; o_ < 32; o_ <<= 1) lsum += __shfl_xor_sync(KVC_FULL_MASK, lsum, o_);
+  if (lane < G) {
+    s_l[warp][lane] = lsum;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      if (g == lane) s_m[warp][lane] = m_run[g];
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int t = 0; t < VPL; ++t) s_o[warp][g][lane * VPL + t] = o[g][t];
+
+  // the chunk holding row `len` stores the appended token
+  if (append_ok && e0 <= len && len < e1) {
+    T* Kw = static_cast<T*>(a.Kp) + (off + len) * D;
+    T* Vw = static_cast<T*>(a.Vp) + (off + len) * D;
+    for (int i = tid; i < D; i += kThreads) { Kw[i] = kn[i]; Vw[i] = vn[i]; }
+    if (tid == 0) {
+      a.logm[off + len] = 0.f;
+      a.pos[off + len] = a.pos_new ? a.pos_new[bl / a.L] : -1.f;
+    }
+  }
+  __syncthreads();
+
+  // merge the warps into this chunk's partial
+  float* part_out = a.partials + ((int64_t)blh * a.n_chunk_max + c) * G * (D + 2);
+  for (int idx = tid; idx < G * D; idx += kThreads) {
+    const int g = idx / D, dd = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_m[w][g]);
+    float acc = 0.f, l = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = (s_m[w][g] == -INFINITY) ? 0.f : exp2f(s_m[w][g] - M);
+      acc = fmaf(f, s_o[w][g][dd], acc);
+      l = fmaf(f, s_l[w][g], l);
+    }
+    part_out[g * (D + 2) + 2 + dd] = acc;
+    if (dd == 0) { part_out[g * (D + 2)] = M; part_out[g * (D + 2) + 1] = l; }
+  }
+  __threadfence();
+  __syncthreads();
+  __shared__ int s_last;
+  if (tid == 0) s_last = (atomicAdd(a.counters + blh, 1) == nchunks - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // last chunk to arrive: log-sum-exp merge of all chunk partials
+  const float* pb = a.partials + (int64_t)blh * a.n_chunk_max * G * (D + 2);
+  T* outp = static_cast<T*>(a.out) + (bl * a.H * G + (int64_t)h * G) * D;
+  for (int idx = tid; idx < G * D; idx += kThreads) {
+    const int g = idx / D, dd = idx % D;
+    float M = -INFINITY;
+    for (int cc = 0; cc < nchunks; ++cc) M = fmaxf(M, __ldcg(pb + (cc * G + g) * (D + 2)));
+    float acc = 0.f, l = 0.f;
+    for (int cc = 0; cc < nchunks; ++cc) {
+      const float* pc = pb + (cc * G + g) * (D + 2);
+      const float mc = __ldcg(pc);
+      const float f = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
+      acc = fmaf(f, __ldcg(pc + 2 + dd), acc);
+      l = fmaf(f, __ldcg(pc + 1), l);
+    }
+    outp[g * D + dd] = kvcd::from_f<T>(acc / l);
+  }
+  if (tid == 0) a.counters[blh] = 0;
+}
+
+// Commits the append once every chunk has read the old length.
+__global__ void decode_commit_kernel(int32_t* len_lh, const int32_t* cap_lh, int64_t n,
+                                     int n_chunk_max, int32_t* err) {
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int len = len_lh[i];
+  if (len < 0 || (len + kChunk) / kChunk > n_chunk_max) return;   // skipped by the attention
+  if (len + 1 <= cap_lh[i]) len_lh[i] = len + 1;
+  else kvcd::record_error(err, KVC_ECAPACITY);
+}
+
+inline int n_chunk_max(const kvc_params* p) {
+  const int64_t rows = (int64_t)p->n_max + p->decode_reserve + 1;
+  return (int)((rows + kChunk - 1) / kChunk);
+}
+
+template <typename T, int D>
+void launch_dg(const kvc_params* p, const DecodeArgs& a, dim3 grid, cudaStream_t s) {
+  switch (p->G) {
+    case 1: decode_chunk_kernel<T, D, 1><<<grid, kThreads, 0, s>>>(a); break;
+    case 2: decode_chunk_kernel<T, D, 2><<<grid, kThreads, 0, s>>>(a); break;
+    case 4: decode_chunk_kernel<T, D, 4><<<grid, kThreads, 0, s>>>(a); break;
+    default: decode_chunk_kernel<T, D, 8><<<grid, kThreads, 0, s>>>(a); break;
+  }
+}
+
+}  // namespace
+
+namespace kvc {
+size_t decode_workspace_bytes(const kvc_params* p) {
+  const size_t part = (size_t)lh_count(p) * n_chunk_max(p) * p->G * (p->d + 2) * sizeof(float);
+  return align256(part) + align256((size_t)lh_count(p) * sizeof(int32_t));
+}
+}  // namespace kvc
+
+extern "C" int kvc_decode_attn(const kvc_params* p, const void* q, const void* k_new,
+                               const void* v_new, const float* pos_new, void* Kp, void* Vp,
+                               float* logm, float* pos, int32_t* len_lh, const int32_t* cap_lh,
+                               const int64_t* off_lh, void* out, void* workspace,
+                               size_t ws_bytes, void* stream) {
+  int st = kvc::check_params(p);
+  if (st != KVC_OK) return st;
+  if (!q || !k_new || !v_new || !Kp || !Vp || !logm || !pos || !len_lh || !cap_lh || !off_lh ||
+      !out)
+    return KVC_EINVAL;
+  const size_t need = kvc::decode_workspace_bytes(p);
+  if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return KVC_EWORKSPACE;
+  const int64_t blh = kvc::lh_count(p);
+  if (blh > 65535) return KVC_EINVAL;
+  int32_t* err = kvc::err_word();
+  if (!err) return KVC_ECUDA;
+  DecodeArgs a;
+  a.q = q; a.k_new = k_new; a.v_new = v_new; a.pos_new = pos_new;
+  a.Kp = Kp; a.Vp = Vp; a.logm = logm; a.pos = pos;
+  a.len_lh = len_lh; a.cap_lh = cap_lh; a.off_lh = off_lh; a.out = out;
+  char* ws = static_cast<char*>(workspace);
+  a.partials = reinterpret_cast<float*>(ws);
+  a.counters = reinterpret_cast<int32_t*>(
+      ws + kvc::align256((size_t)blh * n_chunk_max(p) * p->G * (p->d + 2) * sizeof(float)));
+  a.H = p->H; a.L = p->L; a.n_chunk_max = n_chunk_max(p);
+  a.scale_log2 = kLog2e / sqrtf((float)p->d);
+  a.err = err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  dim3 grid(a.n_chunk_max, (unsigned)blh);
+  if (p->dtype == KVC_BF16) {
+    if (p->d == 128) launch_dg<__nv_bfloat16, 128>(p, a, grid, s);
+    else launch_dg<__nv_bfloat16, 64>(p, a, grid, s);
+  } else {
+    if (p->d == 128) launch_dg<float, 128>(p, a, grid, s);
+    else launch_dg<float, 64>(p, a, grid, s);
+  }
+  decode_commit_kernel<<<(unsigned)((blh + 255) / 256), 256, 0, s>>>(len_lh, cap_lh, blh,
+                                                                       a.n_chunk_max, err);
+  kvc::count_launch(2);
+  return kvc::cuda_status(cudaGetLastError());
+}

@@ -1,0 +1,53 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every entry point
+that include/kvc.h declares (host-only calls; no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "kvc.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvc_[a-z_0-9]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from kv_cache_compression_probe_gb300 import build as B
+    B.build()
+    from kv_cache_compression_probe_gb300 import kvc
+    return kvc.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    from kv_cache_compression_probe_gb300 import kvc
+    assert set(names) == set(kvc.EXPORTED)
+
+
+def test_host_only_calls(lib):
+    from kv_cache_compression_probe_gb300 import kvc
+    assert kvc.kvc_status_string(0) == "ok"
+    assert "budget" in kvc.kvc_status_string(kvc.KVC_EBUDGET)
+    assert kvc.kvc_launch_count() >= 0
+    p = kvc.make_params(B=1, L=32, H=8, G=4, d=128, P=64, W=128, dtype=kvc.KVC_BF16, n_max=16384,
+                        S_max=300, decode_reserve=256)
+    for w in range(5):
+        assert kvc.kvc_workspace_bytes(w, p) > 0
+    bad = kvc.make_params(B=1, L=1, H=1, G=3, d=128, P=64, W=128, dtype=1, n_max=1000, S_max=4)
+    assert kvc.kvc_workspace_bytes(kvc.KVC_WS_DECODE, bad) == 0
+
+
+def test_params_struct_layout_matches_header():
+    from kv_cache_compression_probe_gb300 import kvc
+    assert ctypes.sizeof(kvc.kvc_params) == 104
+    assert kvc.kvc_params.budget_ratio.offset == 64
+    assert kvc.kvc_params.floor_cap_tokens.offset == 88
+    assert kvc.kvc_params.decode_reserve.offset == 96

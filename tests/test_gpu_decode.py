@@ -1,0 +1,126 @@
+"""GPU parity of kvc_decode_attn against the float64 oracle decode (reading R10:
+append with multiplicity one, then attend including the new token)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from synth import workloads as W
+from tests.gpu_helpers import DT, assert_bf16_close, assert_f32_close, dev, params_for
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kvc():
+    from kv_cache_compression_probe_gb300 import build, kvc as K
+    build.build()
+    return K
+
+
+def _rand_cache(rng, B, L, H, d, lens, reserve, dtype):
+    lens = np.asarray(lens, dtype=np.int64).reshape(B, L, H)
+    caps, offs = O.offsets(lens, reserve)
+    rows = int(caps.sum())
+    Kp = rng.standard_normal((rows, d)).astype(np.float32)
+    Vp = rng.standard_normal((rows, d)).astype(np.float32)
+    lm = np.where(rng.uniform(size=rows) < 0.7, 0.0, rng.uniform(0, 3, size=rows)).astype(np.float32)
+    if dtype == "bf16":
+        Kp, Vp = W.round_bf16(Kp), W.round_bf16(Vp)
+    return lens, caps, offs, Kp, Vp, lm
+
+
+def _run_decode(kvc, cfg, lens, caps, offs, Kp, Vp, lm, steps, seed):
+    B, L, H, G, d = cfg.B, cfg.L, cfg.H, cfg.G, cfg.d
+    p = params_for(cfg, n_max=max(int(lens.max()) + 64, cfg.W + 16), S_max=1)
+    dt = DT[cfg.dtype]
+    dKp, dVp = dev(Kp, dt), dev(Vp, dt)
+    dlm = dev(lm)
+    dpos = torch.zeros(Kp.shape[0], dtype=torch.float32, device="cuda")
+    dlen = dev(lens.astype(np.int32))
+    dcap = dev(caps.astype(np.int32))
+    doff = dev(offs.astype(np.int64))
+    ws = kvc.workspace(kvc.KVC_WS_DECODE, p, zero=True)
+    out = torch.empty((B, L, H * G, d), dtype=dt, device="cuda")
+    cur = {}
+    for b in range(B):
+        for l in range(L):
+            for h in range(H):
+                o, c = int(offs[b, l, h]), int(lens[b, l, h])
+                cur[(b, l, h)] = (Kp[o:o + c].astype(np.float64), Vp[o:o + c].astype(np.float64),
+                                  lm[o:o + c].astype(np.float64))
+    rng = np.random.default_rng(seed)
+    outs = []
+    for t in range(steps):
+        q = rng.standard_normal((B, L, H * G, d)).astype(np.float32)
+        kn = rng.standard_normal((B, L, H, d)).astype(np.float32)
+        vn = rng.standard_normal((B, L, H, d)).astype(np.float32)
+        if cfg.dtype == "bf16":
+            q, kn, vn = W.round_bf16(q), W.round_bf16(kn), W.round_bf16(vn)
+        posn = torch.full((B,), 1000.0 + t, device="cuda")
+        kvc.kvc_decode_attn(p, dev(q, dt), dev(kn, dt), dev(vn, dt), posn, dKp, dVp, dlm, dpos, dlen,
+                            dcap, doff, out, ws)
+        err = kvc.kvc_device_error()
+        got = out.float().cpu().numpy()
+        want = np.zeros_like(got, dtype=np.float64)
+        cap_hit = False
+        for (b, l, h), (Kc, Vc, lc) in list(cur.items()):
+            o4, K2, V2, l2 = O.decode_step_head(q[b, l, h * G:(h + 1) * G], kn[b, l, h], vn[b, l, h],
+                                                Kc, Vc, lc)
+            want[b, l, h * G:(h + 1) * G] = o4
+            if Kc.shape[0] + 1 <= caps[b, l, h]:
+                cur[(b, l, h)] = (K2, V2, l2)
+            else:
+                cap_hit = True
+        outs.append((got, want, err, cap_hit))
+    return outs, dlen, dKp, dlm, doff
+
+
+@pytest.mark.parametrize("dtype,d,G", [("bf16", 128, 4), ("f32", 64, 4), ("bf16", 128, 1),
+                                       ("bf16", 64, 8), ("f32", 128, 2)])
+def test_decode_matches_oracle_ragged(kvc, dtype, d, G):
+    cfg = W.small_config(B=2, L=2, H=3, G=G, d=d, dtype=dtype, P=16, W=16, n_decode=3)
+    rng = np.random.default_rng(7)
+    lens = [0, 1, 255, 256, 257, 600, 1023, 31, 512, 2, 800, 100]
+    lens, caps, offs, Kp, Vp, lm = _rand_cache(rng, 2, 2, 3, d, lens, 3, dtype)
+    outs, dlen, dKp, dlm, doff = _run_decode(kvc, cfg, lens, caps, offs, Kp, Vp, lm, 3, seed=1)
+    for got, want, err, cap_hit in outs:
+        assert err == 0 and not cap_hit
+        if dtype == "bf16":
+            assert_bf16_close(got, want, "decode out")
+        else:
+            assert_f32_close(got, want, "decode out", rel=1e-5)
+    np.testing.assert_array_equal(dlen.cpu().numpy(), (lens + 3).astype(np.int32))
+    lmv = dlm.cpu().numpy()
+    for i in range(3):
+        assert (lmv[offs.reshape(-1) + lens.reshape(-1) + i] == 0).all()
+
+
+def test_decode_capacity_overflow_reports_and_still_attends(kvc):
+    cfg = W.small_config(B=1, L=1, H=2, G=4, d=128, dtype="bf16", P=16, W=16, n_decode=0)
+    rng = np.random.default_rng(3)
+    lens, caps, offs, Kp, Vp, lm = _rand_cache(rng, 1, 1, 2, 128, [300, 40], 0, "bf16")
+    outs, dlen, *_ = _run_decode(kvc, cfg, lens, caps, offs, Kp, Vp, lm, 1, seed=2)
+    got, want, err, cap_hit = outs[0]
+    assert err == kvc.KVC_ECAPACITY and cap_hit
+    assert_bf16_close(got, want, "decode out at capacity")
+    np.testing.assert_array_equal(dlen.cpu().numpy().reshape(-1), [300, 40])
+
+
+def test_decode_over_oracle_packed_tiny_cache(kvc):
+    """Decode over the cache the oracle packs for the tiny config."""
+    from tests.oracle_pipeline import pack_all, score_all, select_all
+    cfg = W.get_config("tiny")
+    wl = W.make_workload(cfg)
+    run = score_all(wl)
+    sels = select_all(wl, run.util, run.cost, run.r)
+    ent, lens, caps, offs = pack_all(wl, [s.taken for s in sels], run.r)
+    rows = int(caps.sum())
+    Kp = np.zeros((rows, cfg.d), np.float32); Vp = np.zeros_like(Kp); lm = np.zeros(rows, np.float32)
+    for (b, l, h), (K, V, m, _) in ent.items():
+        o = int(offs[b, l, h])
+        Kp[o:o + len(K)] = K; Vp[o:o + len(K)] = V; lm[o:o + len(K)] = m
+    outs, *_ = _run_decode(kvc, cfg, lens, caps, offs, Kp, Vp, lm, 4, seed=5)
+    for got, want, err, _ in outs:
+        assert err == 0
+        assert_f32_close(got, want, "tiny decode", rel=1e-5)
