@@ -1,0 +1,433 @@
+"""Benchmark of the budgeted KV-compression + ragged-decode hot path on GB300.
+
+One step = one pass of the whole path over one synthetic batch:
+kvc_score -> kvc_select -> kvc_merge_pack (compression after prefill), then
+`decode_steps` calls of kvc_decode_attn (all layers per call, append + attend).
+Workload (default): the Mistral-7B-shaped 16K cache (32 layers, 8 KV / 32 query
+heads, d 128, bf16, batch 1, 25% budget, 128-token window, 1% singleton cap,
+256 decode steps).  Inputs are seeded synthetic caches (see synth/), resident
+in HBM for `value`; `e2e` copies them from pinned host memory every step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs an independent
+replica of the workload (the path shards by sequence; no collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV tokens compressed/s and ragged decode-attn GB/s (fraction of HBM/TC peak)"
+UNIT = "KV tokens/s"
+
+
+# --------------------------------------------------------------------------- inputs
+def _gen_head(args):
+    from synth import workloads as W
+    cfg, b, l, h, n, bounds, cnt = args
+    K, V, Q, _ = W.gen_head(cfg, b, l, h, n, bounds, cnt)
+    return l, h, K, V, Q
+
+
+def make_inputs(cfg, pool):
+    """Host arrays of the synthetic workload (generated in parallel by heads)."""
+    from synth import workloads as W
+    seqs = []
+    for b, n in enumerate(W.context_lengths(cfg)):
+        n = int(n)
+        bounds = W.planted_bounds(cfg, b, n)
+        counts = W._needle_counts(cfg, b, n)
+        jobs = [(cfg, b, l, h, n, bounds, int(counts[l * cfg.H + h]))
+                for l in range(cfg.L) for h in range(cfg.H)]
+        K = np.zeros((cfg.L, cfg.H, n, cfg.d), np.float32)
+        V = np.zeros_like(K)
+        Qp = np.zeros((cfg.L, cfg.H * cfg.G, cfg.P, cfg.d), np.float32)
+        for l, h, k, v, q in pool.imap_unordered(_gen_head, jobs, chunksize=4):
+            K[l, h] = k; V[l, h] = v; Qp[l, h * cfg.G:(h + 1) * cfg.G] = q
+        seqs.append((n, bounds, K, V, Qp))
+    return seqs
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=0):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.gpu = gpu_index
+
+    def start(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1])); smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def kernel_traffic(name: str, src_files):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel source (hash match); else None."""
+    path = os.path.join(ROOT, "profiles", f"{name}.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    h = hashlib.sha256()
+    for f in src_files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    if rec.get("source_sha256") != h.hexdigest():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_gpu(args, cfg, rank, world):
+    import torch
+    import torch.distributed as dist
+    from kv_cache_compression_probe_gb300 import kvc
+    from kv_cache_compression_probe_gb300.pipeline import Compressor, pad_bounds
+    from synth import workloads as W
+
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(min(16, os.cpu_count() or 4)) as pool:
+        seqs = make_inputs(cfg, pool)
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    S_max = max(len(s[1]) - 1 for s in seqs)
+    p = kvc.make_params(B=cfg.B, L=cfg.L, H=cfg.H, G=cfg.G, d=cfg.d, P=cfg.P, W=cfg.W,
+                        dtype=kvc.KVC_BF16 if cfg.dtype == "bf16" else kvc.KVC_F32,
+                        n_max=max(s[0] for s in seqs), S_max=S_max, rope_base=cfg.rope_base,
+                        hop_weight=cfg.hop_weight, n_hops=cfg.n_hops, w_part=cfg.w_part,
+                        w_value=cfg.w_value, value_floor=cfg.value_floor,
+                        budget_ratio=cfg.budget_ratio,
+                        budget_entries_per_lh=cfg.budget_entries_per_lh,
+                        floor_cap_frac=cfg.floor_cap_frac, floor_cap_tokens=cfg.floor_cap_tokens,
+                        decode_reserve=args.decode_steps + 1)
+    # host (pinned) and device copies of the inputs
+    h_K = torch.from_numpy(np.concatenate([s[2].reshape(-1, cfg.d) for s in seqs])).to(dt).pin_memory()
+    h_V = torch.from_numpy(np.concatenate([s[3].reshape(-1, cfg.d) for s in seqs])).to(dt).pin_memory()
+    h_Q = torch.from_numpy(np.stack([s[4] for s in seqs])).to(dt).pin_memory()
+    bounds = torch.from_numpy(pad_bounds([s[1] for s in seqs], S_max)).to(dev)
+    n_slots = torch.tensor([len(s[1]) - 1 for s in seqs], dtype=torch.int32, device=dev)
+    K, V, Qp = h_K.to(dev), h_V.to(dev), h_Q.to(dev)
+    D = args.decode_steps
+    dec = [W.decode_inputs(cfg, t) for t in range(D)]
+    h_q = torch.from_numpy(np.stack([x[0] for x in dec])).to(dt).pin_memory()
+    h_kn = torch.from_numpy(np.stack([x[1] for x in dec])).to(dt).pin_memory()
+    h_vn = torch.from_numpy(np.stack([x[2] for x in dec])).to(dt).pin_memory()
+    q_all, kn_all, vn_all = h_q.to(dev), h_kn.to(dev), h_vn.to(dev)
+    comp = Compressor(p, [s[0] for s in seqs], device=dev)
+    out = torch.empty((D,) + tuple(q_all.shape[1:]), dtype=dt, device=dev)
+    h_out = torch.empty(out.shape, dtype=dt).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    rec = {"score": [], "select": [], "pack": [], "decode": []}
+
+    def step(timed: bool, Kx=K, Vx=V, Qx=Qp):
+        marks = [ev() for _ in range(4)] if timed else None
+        if timed: marks[0].record(stream)
+        comp.score(Kx, Vx, Qx, bounds, n_slots)
+        if timed: marks[1].record(stream)
+        comp.select(bounds, n_slots)
+        if timed: marks[2].record(stream)
+        comp.merge_pack(Kx, Vx, bounds, n_slots)
+        if timed: marks[3].record(stream)
+        dmarks = []
+        for t in range(D):
+            if timed:
+                e0 = ev(); e0.record(stream)
+            comp.decode(q_all[t], kn_all[t], vn_all[t], out[t])
+            if timed:
+                e1 = ev(); e1.record(stream); dmarks.append((e0, e1))
+        if timed:
+            rec["_pending"] = (marks, dmarks)
+
+    def harvest():
+        marks, dmarks = rec.pop("_pending")
+        rec["score"].append(marks[0].elapsed_time(marks[1]))
+        rec["select"].append(marks[1].elapsed_time(marks[2]))
+        rec["pack"].append(marks[2].elapsed_time(marks[3]))
+        rec["decode"].append(statistics.mean(a.elapsed_time(b) for a, b in dmarks))
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize(dev)
+    err = kvc.kvc_device_error()
+    if err != 0:
+        raise RuntimeError(f"device error {kvc.kvc_status_string(err)} during warm-up")
+
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = kvc.kvc_launch_count()
+    t0, t1 = ev(), ev()
+    t0.record(stream)
+    step_ms = []
+    for _ in range(args.steps):
+        s0 = ev(); s0.record(stream)
+        step(True)
+        s1 = ev(); s1.record(stream)
+        torch.cuda.synchronize(dev)
+        harvest()
+        step_ms.append(s0.elapsed_time(s1))
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = kvc.kvc_launch_count() - launches0
+    if world > 1:
+        dist.barrier()
+    total_ms = t0.elapsed_time(t1)
+    clk = clocks.stop()
+
+    # end to end: pinned host inputs -> device, full path, outputs -> host
+    e2e_ms = []
+    for _ in range(max(1, args.steps)):
+        torch.cuda.synchronize(dev)
+        a0, a1 = ev(), ev()
+        a0.record(stream)
+        K.copy_(h_K, non_blocking=True); V.copy_(h_V, non_blocking=True)
+        Qp.copy_(h_Q, non_blocking=True)
+        q_all.copy_(h_q, non_blocking=True); kn_all.copy_(h_kn, non_blocking=True)
+        vn_all.copy_(h_vn, non_blocking=True)
+        step(False)
+        h_out.copy_(out, non_blocking=True)
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms.append(a0.elapsed_time(a1))
+    h2d = sum(t.numel() * t.element_size() for t in (h_K, h_V, h_Q, h_q, h_kn, h_vn))
+    d2h = h_out.numel() * h_out.element_size()
+
+    # max over ranks
+    ms = total_ms / args.steps
+    e2e = statistics.mean(e2e_ms)
+    if world > 1:
+        tt = torch.tensor([ms, e2e], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms, e2e = float(tt[0]), float(tt[1])
+
+    tokens = sum(s[0] for s in seqs)
+    entries = int(comp.len_lh.sum().cpu()) - cfg.L * cfg.H * cfg.B * 0
+    d = cfg.d
+    esz = 2 if cfg.dtype == "bf16" else 4
+    # algorithmic bytes of one decode launch: every stored entry (K, V, log m) once,
+    # the new token appended (K, V, log m, pos) and q / out
+    lens_at_pack = comp.len_lh.cpu().numpy().astype(np.int64) - (args.warmup * 0)
+    dec_ms = statistics.mean(rec["decode"])
+    # entries attended per launch averaged over the D steps: len_pack + t + 1
+    packed_entries = int(comp.total.cpu()[0]) - cfg.B * cfg.L * cfg.H * p.decode_reserve
+    avg_entries = packed_entries + cfg.B * cfg.L * cfg.H * ((D + 1) / 2.0)
+    per_entry = 2 * d * esz + 4
+    qo = 2 * cfg.B * cfg.L * cfg.H * cfg.G * d * esz
+    dec_bytes = avg_entries * per_entry + cfg.B * cfg.L * cfg.H * (2 * d * esz + 8) + qo
+    hbm, tc, src = measured_peaks()
+    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+    score_ms = statistics.mean(rec["score"])
+    sel_ms = statistics.mean(rec["select"])
+    pack_ms = statistics.mean(rec["pack"])
+    score_flops = 2.0 * cfg.B * cfg.L * cfg.H * cfg.G * cfg.P * tokens / cfg.B * d * 3 \
+        + 2.0 * cfg.B * cfg.L * cfg.H * cfg.P * tokens / cfg.B * d * 2 * cfg.n_hops
+    traffic = kernel_traffic("decode_attn_mistral16k",
+                             ["kv_cache_compression_probe_gb300/csrc/kvc_decode.cu"])
+    line = {
+        "metric": METRIC,
+        "value": tokens * world / (ms * 1e-3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": cfg.dtype,
+        "data": "synthetic (seeded random-walk K/V, planted needles and two-hop chains)",
+        "config": {"workload": cfg.name + ": " + cfg.description, "batch": cfg.B,
+                   "context": cfg.n, "layers": cfg.L, "kv_heads": cfg.H, "q_heads": cfg.H * cfg.G,
+                   "head_dim": d, "budget": cfg.budget_ratio, "window": cfg.W,
+                   "decode_steps": D, "l2": "inputs larger than L2 (K+V %.2f GB)" %
+                   (2 * tokens * cfg.L * cfg.H * d * esz / 1e9), "parallelism": f"replicas x{world}"},
+        "breakdown_ms": {"score": score_ms, "select": sel_ms, "merge_pack": pack_ms,
+                         "decode_per_step": dec_ms, "decode_total": dec_ms * D},
+        "compress_tokens_per_s": tokens / ((score_ms + sel_ms + pack_ms) * 1e-3),
+        "decode_gbs": dec_gbs,
+        "decode_vs_full_note": "see profiles/ for the full-cache (beta=1) decode comparison",
+        "roofline": {"kernel": "decode_chunk_kernel (+ commit)", "bound": "hbm",
+                     "achieved": dec_gbs, "peak": hbm, "unit": "GB/s", "frac": dec_gbs / hbm,
+                     "peak_source": src + " hbm_gbs (MEASURED_PEAKS.json)",
+                     "traffic": traffic,
+                     "algorithmic_bytes_per_launch": dec_bytes},
+        "score_tflops": score_flops / (score_ms * 1e-3) / 1e12,
+        "score_tc_frac_of_bf16_peak": score_flops / (score_ms * 1e-3) / 1e12 / tc,
+        "e2e": {"value": tokens * world / (e2e * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e},
+        "gpu_launches": launches // max(1, args.steps) * args.steps,
+        "clocks": clk,
+    }
+    return line
+
+
+# --------------------------------------------------------------------------- oracle (CPU)
+def oracle_sample(cfg, heads, decode_steps):
+    """The float64 oracle over a bounded sample: `heads` (layer, KV head) pairs of
+    sequence 0 scored, selected with the pooled budget scaled to the sample,
+    packed and decoded.  Returns (seconds, KV tokens covered)."""
+    import oracle as O
+    from synth import workloads as W
+    n = int(W.context_lengths(cfg)[0])
+    bounds = W.planted_bounds(cfg, 0, n)
+    counts = W._needle_counts(cfg, 0, n)
+    data = {}
+    for (l, h) in heads:
+        data[(l, h)] = W.gen_head(cfg, 0, l, h, n, bounds, int(counts[l * cfg.H + h]))
+    t0 = time.perf_counter()
+    S = len(bounds) - 1
+    util = np.zeros((1, len(heads), S, 16)); cost = np.zeros((1, len(heads), S, 16), np.int64)
+    r = np.zeros((1, len(heads), n))
+    for k, (l, h) in enumerate(heads):
+        K, V, Q, _ = data[(l, h)]
+        res = O.score_and_value_head(K, V, Q, n, cfg.P, bounds, 1.0, base=cfg.rope_base)
+        util[0, k], cost[0, k], r[0, k] = res.util, res.cost, res.r
+    sel = O.select_sequence(util, cost, r, np.ones((1, len(heads))), bounds, n, cfg.W,
+                            cfg.budget_ratio, cfg.budget_entries_per_lh, cfg.floor_cap_frac,
+                            cfg.floor_cap_tokens)
+    rng = np.random.default_rng(0)
+    for k, (l, h) in enumerate(heads):
+        K, V, Q, _ = data[(l, h)]
+        Kp, Vp, lm, _ = O.pack_head(K, V, r[0, k], bounds, sel.taken[0, k], n, cfg.W,
+                                    cfg.rope_base, cfg.value_floor)
+        for t in range(decode_steps):
+            q = rng.standard_normal((cfg.G, cfg.d)); kn = rng.standard_normal(cfg.d)
+            vn = rng.standard_normal(cfg.d)
+            _, Kp, Vp, lm = O.decode_step_head(q, kn, vn, Kp, Vp, lm)
+    dt = time.perf_counter() - t0
+    return dt, n * len(heads) / (cfg.L * cfg.H)
+
+
+def cpu_baseline(cfg, decode_steps, n_heads=4):
+    heads = [(l, 0) for l in range(n_heads)]
+    secs, toks = oracle_sample(cfg, heads, decode_steps)
+    return {"value": toks / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n_heads} of {cfg.L * cfg.H} (layer, KV head) pairs of the {cfg.n}-token "
+                      f"sequence: score+hops+utilities, floor+auction with the budget pooled "
+                      f"over the sample, pack, {decode_steps} decode steps; single process, "
+                      f"float64 numpy; {secs:.1f} s",
+            "seconds": secs}
+
+
+def run_reference(args, cfg, rank, world):
+    if rank != 0:
+        return None
+    vals = []
+    t_all = time.perf_counter()
+    for _ in range(args.warmup):
+        oracle_sample(cfg, [(0, 0)], 2)
+    for s in range(args.steps):
+        secs, toks = oracle_sample(cfg, [(s % cfg.L, 0)], args.decode_steps)
+        vals.append((secs, toks))
+    secs = sum(v[0] for v in vals)
+    toks = sum(v[1] for v in vals)
+    value = toks / secs
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": cfg.name + ": " + cfg.description},
+            "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle", "cores": 1,
+                             "sample": "per step one (layer, KV head) pair of the sequence "
+                                       "(score, hops, utilities, select, pack, decode steps)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "wall_s": time.perf_counter() - t_all}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--config", default="mistral16k")
+    ap.add_argument("--decode-steps", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from synth import workloads as W
+    cfg = W.get_config(args.config)
+    if args.decode_steps is None:
+        args.decode_steps = cfg.n_decode
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.impl == "reference":
+        line = run_reference(args, cfg, rank, world)
+        if line is not None:
+            print(json.dumps(line))
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, args.decode_steps)
+    line = run_gpu(args, cfg, rank, world)
+    if rank == 0:
+        line["cpu_baseline"] = cpu
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,5 +1,334 @@
-// placeholder, replaced by the real implementation
+// a3 + a6: merge every stored frontier node into one cache entry and pack the
+// ragged per-(layer, KV head) cache (GraceKV "Inside one cache entry" and
+// "05 Physical cache packing").
+//
+// Prototype of tokens [x, y) (c = y - x):
+//   k~_i = R(-i) k_i              inverse RoPE to a shared frame
+//   kbar = mean k~_i,  kappa = mean cos(k~_i, kbar)
+//   m    = c * clamp(kappa, 1/c, 1),  stored as ln m (decode adds it to the logit)
+//   k^   = R(pbar) kbar, pbar = (x + y - 1)/2 (table row x + y - 1 of the
+//          half-position RoPE table)
+//   v^   = sum w_i v_i, w_i = (1-f) r_i / sum r + f / c  (uniform when sum r = 0)
+// Split leaves store their tokens bit-exact (ln m = 0, pos = i); the W window
+// tokens follow the slots.  Entry order per (b,l,h): slots ascending, each
+// slot's frontier left to right, then the window.
+//
+// Layout of the work: kernel 1 counts each slot's stored entries and prefix-
+// sums them per (b,l,h) (one warp per (b,l,h)); kernel 2 gives one warp per
+// slot tree; a lane owns the RoPE pairs (j, j + d/2) for j = lane*VP .. so the
+// rotation needs no exchange between lanes.
 #include "kvc_common.cuh"
 #include "kvc_internal.h"
-namespace kvc { size_t pack_workspace_bytes(const kvc_params*) { return 256; } }
-extern "C" int kvc_merge_pack(const kvc_params*, const int32_t*, const void*, const void*, const float*, const float*, const float*, const int32_t*, const int32_t*, const uint8_t*, const int32_t*, const int64_t*, void*, void*, float*, float*, int64_t, void*, size_t, void*) { return KVC_EINVAL; }
+
+namespace {
+
+constexpr int kOps = 16;
+
+__device__ __forceinline__ void node_range(int j, int x0, int y0, int& a, int& b) {
+  const int depth = (j >= 7) ? 3 : (j >= 3) ? 2 : (j >= 1) ? 1 : 0;
+  const int k = j - ((1 << depth) - 1);
+  a = x0; b = y0;
+  for (int lvl = depth - 1; lvl >= 0; --lvl) {
+    const int mid = (a + b) >> 1;
+    if ((k >> lvl) & 1) a = mid; else b = mid;
+  }
+}
+
+// Stored entries of one slot tree: sum over taken ops of their cost
+// (Add 1, internal Split 1, leaf Split = leaf size - 1).
+__device__ __forceinline__ int tree_entries(const uint8_t* tk, int x0, int y0) {
+  int n = 0;
+  for (int o = 0; o < 8; ++o) n += tk[o] ? 1 : 0;
+  for (int j = 7; j < 15; ++j)
+    if (tk[1 + j]) {
+      int a, b;
+      node_range(j, x0, y0, a, b);
+      n += (b - a) - 1;
+    }
+  return n;
+}
+
+struct PackArgs {
+  const int32_t* ctx_len;
+  const void* K;
+  const void* V;
+  const float* rel;
+  const float* cos_tab;
+  const float* sin_tab;
+  const int32_t* bounds;
+  const int32_t* n_slots;
+  const uint8_t* taken;
+  const int32_t* len_lh;
+  const int64_t* off_lh;
+  void* Kp;
+  void* Vp;
+  float* logm;
+  float* pos;
+  int32_t* slot_base;   // [B, L, H, S_max]
+  int32_t* lh_ok;       // [B, L, H] 1 if the (l,h) passed its checks
+  int64_t capacity;
+  int32_t* err;
+};
+
+// One warp per (b,l,h): per-slot entry counts -> exclusive prefix, checks.
+__global__ void pack_count_kernel(kvc_params p, PackArgs a) {
+  const int warps = blockDim.x >> 5;
+  const long long blh = (long long)blockIdx.x * warps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (blh >= (long long)p.B * p.L * p.H) return;
+  const int b = (int)(blh / ((long long)p.L * p.H));
+  const int n = a.ctx_len[b];
+  const int S = a.n_slots[b];
+  bool ok = S >= 1 && S <= p.S_max && n >= p.W + 16 && n <= p.n_max;
+  const int32_t* bd = a.bounds + (long long)b * (p.S_max + 1);
+  int run = 0;
+  if (ok) {
+    for (int s0 = 0; s0 < S; s0 += 32) {
+      const int s = s0 + lane;
+      int cnt = 0;
+      if (s < S) {
+        const int x0 = bd[s], y0 = bd[s + 1];
+        if (x0 < 0 || y0 - x0 < 16 || y0 - x0 > 128 || y0 > n - p.W) ok = false;
+        else cnt = tree_entries(a.taken + (blh * p.S_max + s) * kOps, x0, y0);
+      }
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(KVC_FULL_MASK, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (s < S) a.slot_base[blh * p.S_max + s] = run + incl - cnt;
+      run += __shfl_sync(KVC_FULL_MASK, incl, 31);
+    }
+    ok = __all_sync(KVC_FULL_MASK, ok);
+  }
+  if (ok) {
+    const int len = a.len_lh[blh];
+    ok = (len == run + p.W) && a.off_lh[blh] >= 0 && a.off_lh[blh] + len <= a.capacity;
+  }
+  if (lane == 0) {
+    a.lh_ok[blh] = ok ? 1 : 0;
+    if (!ok) kvcd::record_error(a.err, KVC_EDEVICE);
+  }
+}
+
+template <typename T, int D>
+struct Row {
+  // lane-owned features: j in [lane*VP, lane*VP + VP) and j + D/2
+  static constexpr int VP = D / 64;
+};
+
+template <typename T, int D>
+__device__ __forceinline__ void load_pairs(const T* row, int lane, float* lo, float* hi) {
+  constexpr int VP = D / 64;
+#pragma unroll
+  for (int t = 0; t < VP; ++t) {
+    lo[t] = kvcd::to_f(row[lane * VP + t]);
+    hi[t] = kvcd::to_f(row[D / 2 + lane * VP + t]);
+  }
+}
+
+template <typename T, int D>
+__device__ void write_prototype(const kvc_params& p, const PackArgs& a, const T* Kh, const T* Vh,
+                                const float* rh, int x, int y, int64_t dst, int lane) {
+  constexpr int VP = D / 64;
+  constexpr int HALF = D / 2;
+  const int c = y - x;
+  float kb_lo[VP], kb_hi[VP], vb_lo[VP], vb_hi[VP];
+#pragma unroll
+  for (int t = 0; t < VP; ++t) kb_lo[t] = kb_hi[t] = vb_lo[t] = vb_hi[t] = 0.f;
+  // relevance mass of the span (lanes split the tokens)
+  float rs = 0.f;
+  for (int i = x + lane; i < y; i += 32) rs += rh[i];
+  rs = kvcd::warp_sum(rs);
+  const float f = p.value_floor;
+  // pass 1: mean of the unrotated keys and the weighted value
+  for (int i = x; i < y; ++i) {
+    float klo[VP], khi[VP], vlo[VP], vhi[VP];
+    load_pairs<T, D>(Kh + (int64_t)i * D, lane, klo, khi);
+    load_pairs<T, D>(Vh + (int64_t)i * D, lane, vlo, vhi);
+    const float* ct = a.cos_tab + (int64_t)(2 * i) * HALF + lane * VP;
+    const float* st = a.sin_tab + (int64_t)(2 * i) * HALF + lane * VP;
+    const float w = rs > 0.f ? (1.f - f) * (rh[i] / rs) + f / (float)c : 1.f / (float)c;
+#pragma unroll
+    for (int t = 0; t < VP; ++t) {
+      const float cs = __ldg(ct + t), sn = __ldg(st + t);
+      kb_lo[t] += klo[t] * cs + khi[t] * sn;          // R(-i)
+      kb_hi[t] += khi[t] * cs - klo[t] * sn;
+      vb_lo[t] = fmaf(w, vlo[t], vb_lo[t]);
+      vb_hi[t] = fmaf(w, vhi[t], vb_hi[t]);
+    }
+  }
+  const float inv_c = 1.f / (float)c;
+  float nb2 = 0.f;
+#pragma unroll
+  for (int t = 0; t < VP; ++t) {
+    kb_lo[t] *= inv_c; kb_hi[t] *= inv_c;
+    nb2 += kb_lo[t] * kb_lo[t] + kb_hi[t] * kb_hi[t];
+  }
+  const float nb = sqrtf(kvcd::warp_sum(nb2));
+  // pass 2: coherence = mean cosine of each unrotated key to the mean
+  float kap = 0.f;
+  for (int i = x; i < y; ++i) {
+    float klo[VP], khi[VP];
+    load_pairs<T, D>(Kh + (int64_t)i * D, lane, klo, khi);
+    const float* ct = a.cos_tab + (int64_t)(2 * i) * HALF + lane * VP;
+    const float* st = a.sin_tab + (int64_t)(2 * i) * HALF + lane * VP;
+    float dot = 0.f, nk2 = 0.f;
+#pragma unroll
+    for (int t = 0; t < VP; ++t) {
+      const float cs = __ldg(ct + t), sn = __ldg(st + t);
+      const float ul = klo[t] * cs + khi[t] * sn, uh = khi[t] * cs - klo[t] * sn;
+      dot += ul * kb_lo[t] + uh * kb_hi[t];
+      nk2 += ul * ul + uh * uh;
+    }
+    dot = kvcd::warp_sum(dot);
+    nk2 = kvcd::warp_sum(nk2);
+    const float den = sqrtf(nk2) * nb;
+    kap += den > 0.f ? dot / den : 0.f;
+  }
+  kap *= inv_c;
+  const float m = (float)c * fminf(fmaxf(kap, inv_c), 1.f);
+  // rerotate the mean at pbar = (x + y - 1) / 2: half-position table row x + y - 1
+  const float* ct = a.cos_tab + (int64_t)(x + y - 1) * HALF + lane * VP;
+  const float* st = a.sin_tab + (int64_t)(x + y - 1) * HALF + lane * VP;
+  T* ko = static_cast<T*>(a.Kp) + dst * D;
+  T* vo = static_cast<T*>(a.Vp) + dst * D;
+#pragma unroll
+  for (int t = 0; t < VP; ++t) {
+    const float cs = __ldg(ct + t), sn = __ldg(st + t);
+    ko[lane * VP + t] = kvcd::from_f<T>(kb_lo[t] * cs - kb_hi[t] * sn);
+    ko[HALF + lane * VP + t] = kvcd::from_f<T>(kb_hi[t] * cs + kb_lo[t] * sn);
+    vo[lane * VP + t] = kvcd::from_f<T>(vb_lo[t]);
+    vo[HALF + lane * VP + t] = kvcd::from_f<T>(vb_hi[t]);
+  }
+  if (lane == 0) {
+    a.logm[dst] = logf(m);
+    a.pos[dst] = 0.5f * (float)(x + y - 1);
+  }
+}
+
+template <typename T, int D>
+__device__ __forceinline__ void copy_exact(const PackArgs& a, const T* Kh, const T* Vh, int i,
+                                           int64_t dst, int lane) {
+  T* ko = static_cast<T*>(a.Kp) + dst * D;
+  T* vo = static_cast<T*>(a.Vp) + dst * D;
+  for (int j = lane; j < D; j += 32) {
+    ko[j] = Kh[(int64_t)i * D + j];
+    vo[j] = Vh[(int64_t)i * D + j];
+  }
+  if (lane == 0) {
+    a.logm[dst] = 0.f;
+    a.pos[dst] = (float)i;
+  }
+}
+
+// One warp per slot tree (plus one extra "slot" index S per (b,l,h) for the
+// window tokens).
+template <typename T, int D>
+__global__ void pack_tree_kernel(kvc_params p, PackArgs a) {
+  const int warps = blockDim.x >> 5;
+  const long long item = (long long)blockIdx.x * warps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int per = p.S_max + 1;
+  if (item >= (long long)p.B * p.L * p.H * per) return;
+  const int s = (int)(item % per);
+  const long long blh = item / per;
+  if (!a.lh_ok[blh]) return;
+  const int lh = (int)(blh % ((long long)p.L * p.H));
+  const int b = (int)(blh / ((long long)p.L * p.H));
+  const int n = a.ctx_len[b];
+  const int S = a.n_slots[b];
+  const int64_t row0 = kvcd::seq_token_base(a.ctx_len, b, p.L * p.H) + (int64_t)lh * n;
+  const T* Kh = static_cast<const T*>(a.K) + row0 * D;
+  const T* Vh = static_cast<const T*>(a.V) + row0 * D;
+  const float* rh = a.rel + row0;
+  const int64_t base = a.off_lh[blh];
+  if (s == p.S_max) {                                   // window tokens
+    const int64_t dst0 = base + a.len_lh[blh] - p.W;
+    for (int i = n - p.W; i < n; ++i) copy_exact<T, D>(a, Kh, Vh, i, dst0 + (i - (n - p.W)), lane);
+    return;
+  }
+  if (s >= S) return;
+  const int32_t* bd = a.bounds + (long long)b * (p.S_max + 1);
+  const int x0 = bd[s], y0 = bd[s + 1];
+  const uint8_t* tk = a.taken + (blh * p.S_max + s) * kOps;
+  if (!tk[0]) return;
+  int64_t dst = base + a.slot_base[blh * p.S_max + s];
+  // left-to-right frontier walk with an explicit stack (depth <= 4)
+  int stack[8];
+  int sp = 0;
+  stack[sp++] = 0;
+  while (sp > 0) {
+    const int j = stack[--sp];
+    int x, y;
+    node_range(j, x0, y0, x, y);
+    if (!tk[1 + j]) {
+      write_prototype<T, D>(p, a, Kh, Vh, rh, x, y, dst, lane);
+      ++dst;
+    } else if (j < 7) {
+      stack[sp++] = 2 * j + 2;
+      stack[sp++] = 2 * j + 1;
+    } else {
+      for (int i = x; i < y; ++i) copy_exact<T, D>(a, Kh, Vh, i, dst++, lane);
+    }
+  }
+}
+
+struct Layout {
+  size_t slot_base, lh_ok, total;
+};
+Layout layout(const kvc_params* p) {
+  Layout l;
+  l.slot_base = 0;
+  l.lh_ok = kvc::align256(sizeof(int32_t) * (size_t)kvc::lh_count(p) * p->S_max);
+  l.total = l.lh_ok + kvc::align256(sizeof(int32_t) * (size_t)kvc::lh_count(p));
+  return l;
+}
+
+}  // namespace
+
+namespace kvc {
+size_t pack_workspace_bytes(const kvc_params* p) { return layout(p).total; }
+}  // namespace kvc
+
+extern "C" int kvc_merge_pack(const kvc_params* p, const int32_t* ctx_len, const void* K,
+                              const void* V, const float* relevance, const float* rope_cos,
+                              const float* rope_sin, const int32_t* slot_bounds,
+                              const int32_t* n_slots, const uint8_t* taken, const int32_t* len_lh,
+                              const int64_t* off_lh, void* Kp, void* Vp, float* logm, float* pos,
+                              int64_t capacity, void* workspace, size_t ws_bytes, void* stream) {
+  int st = kvc::check_params(p);
+  if (st != KVC_OK) return st;
+  if (!ctx_len || !K || !V || !relevance || !rope_cos || !rope_sin || !slot_bounds || !n_slots ||
+      !taken || !len_lh || !off_lh || !Kp || !Vp || !logm || !pos || capacity < 0)
+    return KVC_EINVAL;
+  const Layout lay = layout(p);
+  if (!workspace || ws_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return KVC_EWORKSPACE;
+  int32_t* err = kvc::err_word();
+  if (!err) return KVC_ECUDA;
+  PackArgs a;
+  a.ctx_len = ctx_len; a.K = K; a.V = V; a.rel = relevance; a.cos_tab = rope_cos;
+  a.sin_tab = rope_sin; a.bounds = slot_bounds; a.n_slots = n_slots; a.taken = taken;
+  a.len_lh = len_lh; a.off_lh = off_lh; a.Kp = Kp; a.Vp = Vp; a.logm = logm; a.pos = pos;
+  char* w = static_cast<char*>(workspace);
+  a.slot_base = reinterpret_cast<int32_t*>(w + lay.slot_base);
+  a.lh_ok = reinterpret_cast<int32_t*>(w + lay.lh_ok);
+  a.capacity = capacity;
+  a.err = err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const long long blh = kvc::lh_count(p);
+  pack_count_kernel<<<(unsigned)((blh + 7) / 8), 256, 0, s>>>(*p, a);
+  const long long items = blh * (p->S_max + 1);
+  const unsigned grid = (unsigned)((items + 7) / 8);
+  if (p->dtype == KVC_BF16) {
+    if (p->d == 128) pack_tree_kernel<__nv_bfloat16, 128><<<grid, 256, 0, s>>>(*p, a);
+    else pack_tree_kernel<__nv_bfloat16, 64><<<grid, 256, 0, s>>>(*p, a);
+  } else {
+    if (p->d == 128) pack_tree_kernel<float, 128><<<grid, 256, 0, s>>>(*p, a);
+    else pack_tree_kernel<float, 64><<<grid, 256, 0, s>>>(*p, a);
+  }
+  kvc::count_launch(2);
+  return kvc::cuda_status(cudaGetLastError());
+}

@@ -61,7 +61,7 @@ def lib():
         L.kvc_workspace_bytes.argtypes = [c_int, _P]; L.kvc_workspace_bytes.restype = c_size_t
         L.kvc_rope_table.argtypes = [c_int32, c_float, c_int64, vp, vp, vp]
         L.kvc_rope_table.restype = c_int
-        L.kvc_score.argtypes = [_P] + [vp] * 14 + [c_size_t, vp]; L.kvc_score.restype = c_int
+        L.kvc_score.argtypes = [_P] + [vp] * 15 + [c_size_t, vp]; L.kvc_score.restype = c_int
         L.kvc_select.argtypes = [_P] + [vp] * 13 + [c_size_t, vp]; L.kvc_select.restype = c_int
         L.kvc_merge_pack.argtypes = [_P] + [vp] * 15 + [c_int64, vp, c_size_t, vp]
         L.kvc_merge_pack.restype = c_int

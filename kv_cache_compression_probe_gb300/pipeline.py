@@ -1,0 +1,105 @@
+"""Device-buffer owner for the compression + decode path.
+
+`Compressor` allocates (with torch) every output and workspace the four C-ABI
+calls need, builds the RoPE tables with `kvc_rope_table`, and runs
+kvc_score -> kvc_select -> kvc_merge_pack and kvc_decode_attn steps.  It only
+allocates and marshals; all arithmetic runs in libkvc's kernels.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import kvc
+
+TORCH_DT = {kvc.KVC_BF16: torch.bfloat16, kvc.KVC_F32: torch.float32}
+
+
+def packed_capacity(p: kvc.kvc_params, ctx_len: Sequence[int]) -> int:
+    """Rows the packed cache needs at most: every sequence's budget (at least its
+    window) plus the decode reserve of every (b, l, h)."""
+    LH = p.L * p.H
+    rows = 0
+    for n in ctx_len:
+        per = p.budget_entries_per_lh if p.budget_entries_per_lh > 0 else math.floor(p.budget_ratio * n)
+        rows += max(per, p.W) * LH + LH * p.decode_reserve
+    return int(rows)
+
+
+class Compressor:
+    def __init__(self, p: kvc.kvc_params, ctx_len: Sequence[int], device="cuda"):
+        self.p = p
+        self.device = device
+        self.ctx_host = [int(n) for n in ctx_len]
+        assert len(self.ctx_host) == p.B and max(self.ctx_host) <= p.n_max
+        B, L, H, R, S = p.B, p.L, p.H, p.G * p.P, p.S_max
+        rows = sum(L * H * n for n in self.ctx_host)
+        dt = TORCH_DT[p.dtype]
+        f32, i32 = torch.float32, torch.int32
+        z = dict(device=device)
+        self.ctx_len = torch.tensor(self.ctx_host, dtype=i32, **z)
+        n_half = 2 * p.n_max
+        self.rope_cos = torch.empty((n_half, p.d // 2), dtype=f32, **z)
+        self.rope_sin = torch.empty((n_half, p.d // 2), dtype=f32, **z)
+        kvc.kvc_rope_table(p.d, p.rope_base, n_half, self.rope_cos, self.rope_sin)
+        self.lse = torch.empty((B, L, H, R), dtype=f32, **z)
+        self.feats = torch.empty((rows, 5), dtype=f32, **z)
+        self.relevance = torch.empty((rows,), dtype=f32, **z)
+        self.op_util = torch.empty((B, L, H, S, 16), dtype=f32, **z)
+        self.op_cost = torch.empty((B, L, H, S, 16), dtype=i32, **z)
+        self.taken = torch.empty((B, L, H, S, 16), dtype=torch.uint8, **z)
+        self.len_lh = torch.empty((B, L, H), dtype=i32, **z)
+        self.cap_lh = torch.empty((B, L, H), dtype=i32, **z)
+        self.off_lh = torch.empty((B, L, H), dtype=torch.int64, **z)
+        self.total = torch.empty((1,), dtype=torch.int64, **z)
+        cap = packed_capacity(p, self.ctx_host)
+        self.Kp = torch.empty((cap, p.d), dtype=dt, **z)
+        self.Vp = torch.empty((cap, p.d), dtype=dt, **z)
+        self.logm = torch.empty((cap,), dtype=f32, **z)
+        self.pos = torch.empty((cap,), dtype=f32, **z)
+        self.ws_score = kvc.workspace(kvc.KVC_WS_SCORE, p, device)
+        self.ws_select = kvc.workspace(kvc.KVC_WS_SELECT, p, device)
+        self.ws_pack = kvc.workspace(kvc.KVC_WS_PACK, p, device)
+        self.ws_decode = kvc.workspace(kvc.KVC_WS_DECODE, p, device, zero=True)
+
+    # ---------------------------------------------------------------- calls
+    def score(self, K, V, Qp, slot_bounds, n_slots, head_sens=None, stream=None):
+        kvc.kvc_score(self.p, self.ctx_len, K, V, Qp, self.rope_cos, self.rope_sin, slot_bounds,
+                      n_slots, head_sens, self.lse, self.feats, self.relevance, self.op_util,
+                      self.op_cost, self.ws_score, stream)
+
+    def select(self, slot_bounds, n_slots, head_sens=None, op_util=None, relevance=None,
+               stream=None):
+        kvc.kvc_select(self.p, self.ctx_len, slot_bounds, n_slots,
+                       self.relevance if relevance is None else relevance, head_sens,
+                       self.op_util if op_util is None else op_util, self.op_cost, self.taken,
+                       self.len_lh, self.cap_lh, self.off_lh, self.total, self.ws_select, stream)
+
+    def merge_pack(self, K, V, slot_bounds, n_slots, taken=None, stream=None):
+        kvc.kvc_merge_pack(self.p, self.ctx_len, K, V, self.relevance, self.rope_cos,
+                           self.rope_sin, slot_bounds, n_slots,
+                           self.taken if taken is None else taken, self.len_lh, self.off_lh,
+                           self.Kp, self.Vp, self.logm, self.pos, self.ws_pack, stream)
+
+    def compress(self, K, V, Qp, slot_bounds, n_slots, head_sens=None, stream=None):
+        self.score(K, V, Qp, slot_bounds, n_slots, head_sens, stream)
+        self.select(slot_bounds, n_slots, head_sens, stream=stream)
+        self.merge_pack(K, V, slot_bounds, n_slots, stream=stream)
+
+    def decode(self, q, k_new, v_new, out, pos_new=None, stream=None):
+        kvc.kvc_decode_attn(self.p, q, k_new, v_new, pos_new, self.Kp, self.Vp, self.logm,
+                            self.pos, self.len_lh, self.cap_lh, self.off_lh, out, self.ws_decode,
+                            stream)
+
+
+def pad_bounds(bounds_list, S_max: int) -> np.ndarray:
+    """[B, S_max + 1] int32 slot boundaries (rows padded with their last value)."""
+    out = np.zeros((len(bounds_list), S_max + 1), dtype=np.int32)
+    for b, bd in enumerate(bounds_list):
+        bd = np.asarray(bd, dtype=np.int32)
+        out[b, :len(bd)] = bd
+        out[b, len(bd):] = bd[-1]
+    return out

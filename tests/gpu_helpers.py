@@ -46,3 +46,30 @@ def params_for(cfg, n_max=None, S_max=None, **over):
               floor_cap_tokens=cfg.floor_cap_tokens, decode_reserve=cfg.decode_reserve)
     kw.update(over)
     return kvc.make_params(**kw)
+
+
+def upload_workload(wl, **over):
+    """Device copies of a synthetic workload plus a Compressor sized for it."""
+    from kv_cache_compression_probe_gb300.pipeline import Compressor, pad_bounds
+    cfg = wl.cfg
+    S_max = max(len(s.slot_bounds) - 1 for s in wl.seqs)
+    p = params_for(cfg, n_max=max(s.n for s in wl.seqs), S_max=S_max, **over)
+    dt = DT[cfg.dtype]
+    K = np.concatenate([s.K.reshape(-1, cfg.d) for s in wl.seqs])
+    V = np.concatenate([s.V.reshape(-1, cfg.d) for s in wl.seqs])
+    Qp = np.stack([s.Qp for s in wl.seqs])
+    d = dict(K=dev(K, dt), V=dev(V, dt), Qp=dev(Qp, dt),
+             bounds=dev(pad_bounds([s.slot_bounds for s in wl.seqs], S_max)),
+             n_slots=dev(np.asarray([len(s.slot_bounds) - 1 for s in wl.seqs], np.int32)),
+             sens=dev(wl.head_sens))
+    comp = Compressor(p, [s.n for s in wl.seqs])
+    return p, comp, d, S_max
+
+
+def token_view(x, wl, b, width=None):
+    """Slice sequence b's [L, H, n(, width)] block out of a token-layout array."""
+    cfg = wl.cfg
+    start = sum(cfg.L * cfg.H * s.n for s in wl.seqs[:b])
+    n = wl.seqs[b].n
+    blk = x[start:start + cfg.L * cfg.H * n]
+    return blk.reshape(cfg.L, cfg.H, n, *(() if width is None else (width,)))

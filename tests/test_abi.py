@@ -51,3 +51,12 @@ def test_params_struct_layout_matches_header():
     assert kvc.kvc_params.budget_ratio.offset == 64
     assert kvc.kvc_params.floor_cap_tokens.offset == 88
     assert kvc.kvc_params.decode_reserve.offset == 96
+
+
+def test_binding_argument_counts_match_header(lib):
+    """Each ctypes prototype has as many arguments as the header declaration."""
+    src = open(os.path.join(ROOT, "include", "kvc.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    for name, args in re.findall(r"\b(kvc_[a-z_0-9]+)\s*\(([^)]*)\)\s*;", src):
+        n = 0 if args.strip() in ("", "void") else len(args.split(","))
+        assert len(getattr(lib, name).argtypes) == n, name

@@ -89,7 +89,9 @@ def test_decode_matches_oracle_ragged(kvc, dtype, d, G):
         if dtype == "bf16":
             assert_bf16_close(got, want, "decode out")
         else:
-            assert_f32_close(got, want, "decode out", rel=1e-5)
+            # fp32: error relative to the scale of each output vector (a convex
+            # combination of values), see the tolerance notes in the design doc
+            assert_f32_close(got, want, "decode out", rel=1e-5, floor_frac=1.0, axis=-1)
     np.testing.assert_array_equal(dlen.cpu().numpy(), (lens + 3).astype(np.int32))
     lmv = dlm.cpu().numpy()
     for i in range(3):
@@ -123,4 +125,4 @@ def test_decode_over_oracle_packed_tiny_cache(kvc):
     outs, *_ = _run_decode(kvc, cfg, lens, caps, offs, Kp, Vp, lm, 4, seed=5)
     for got, want, err, _ in outs:
         assert err == 0
-        assert_f32_close(got, want, "tiny decode", rel=1e-5)
+        assert_f32_close(got, want, "tiny decode", rel=1e-5, floor_frac=1.0, axis=-1)

@@ -1,0 +1,197 @@
+"""GPU parity of kvc_score, kvc_select and kvc_merge_pack against the oracle.
+
+Per-call parity: every call is compared with the oracle fed the same inputs
+(select gets the GPU's fp32 utilities and relevance; pack gets the same taken
+set).  End-to-end: the GPU's chain against the oracle's own chain, with any
+difference in the taken set explained by near-ties of the oracle's keys.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from synth import workloads as W
+from tests.gpu_helpers import (assert_bf16_close, assert_f32_close, token_view, upload_workload)
+from tests.oracle_pipeline import score_all
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def built():
+    from kv_cache_compression_probe_gb300 import build
+    build.build()
+
+
+def _cases():
+    return {
+        "tiny": W.get_config("tiny"),
+        "small": W.small_config(),
+    }
+
+
+@pytest.fixture(scope="module", params=["tiny", "small"])
+def case(request, built):
+    cfg = _cases()[request.param]
+    wl = W.make_workload(cfg)
+    run = score_all(wl)
+    p, comp, d, S_max = upload_workload(wl)
+    comp.score(d["K"], d["V"], d["Qp"], d["bounds"], d["n_slots"], d["sens"])
+    torch.cuda.synchronize()
+    from kv_cache_compression_probe_gb300 import kvc
+    assert kvc.kvc_device_error() == 0
+    return cfg, wl, run, p, comp, d, S_max
+
+
+def test_score_row_stats(case):
+    cfg, wl, run, p, comp, d, S_max = case
+    assert_f32_close(comp.lse.cpu().numpy(), run.lse, "lse", rel=1e-5)
+
+
+def test_score_features_and_relevance(case):
+    cfg, wl, run, p, comp, d, S_max = case
+    feats = comp.feats.cpu().numpy()
+    rel = comp.relevance.cpu().numpy()
+    for b in range(cfg.B):
+        f = token_view(feats, wl, b, 5)
+        r = token_view(rel, wl, b)
+        for k, name in enumerate(["alpha", "|v|", "sigma", "H", "pos"]):
+            assert_f32_close(f[..., k], run.feats[b][..., k], name, rel=1e-5, axis=-1)
+        assert_f32_close(r, run.r[b], "relevance", rel=1e-5, axis=-1)
+
+
+def test_score_utilities(case):
+    cfg, wl, run, p, comp, d, S_max = case
+    cost = comp.op_cost.cpu().numpy()
+    util = comp.op_util.cpu().numpy()
+    np.testing.assert_array_equal(cost, run.cost)
+    # A utility is scale * gain with scale = R(N) * sens / cost and gain in [0, 1]
+    # a clamped difference of normalised distortions, so fp32 reaches it to an
+    # absolute accuracy relative to the scale (cancellation), not to |u|:
+    # |g - o| <= 1e-5 * max(|o|, 3 * scale).
+    scale_only = 0
+    for b, s in enumerate(wl.seqs):
+        S = len(s.slot_bounds) - 1
+        for l in range(cfg.L):
+            for h in range(cfg.H):
+                r = run.r[b][l, h]
+                sens = float(wl.head_sens[l, h])
+                for k in range(S):
+                    nodes = O.tree_nodes(int(s.slot_bounds[k]), int(s.slot_bounds[k + 1]))
+                    Rv = np.array([r[x:y].sum() for x, y in nodes])
+                    scale = np.r_[Rv[0], Rv] * sens / run.cost[b, l, h, k]
+                    o = run.util[b, l, h, k]
+                    err = np.abs(util[b, l, h, k].astype(np.float64) - o)
+                    assert (err <= 1e-5 * np.maximum(np.abs(o), 3 * scale)).all(), (b, l, h, k, err, o)
+                    scale_only += int(((err > 1e-5 * np.abs(o))).sum())
+    print(f"ops within tolerance only through the scale term: {scale_only}")
+
+
+def test_select_bit_exact_on_gpu_utilities(case):
+    """Selection is bit-exact against the oracle fed the GPU's fp32 keys."""
+    cfg, wl, run, p, comp, d, S_max = case
+    comp.select(d["bounds"], d["n_slots"], d["sens"])
+    torch.cuda.synchronize()
+    from kv_cache_compression_probe_gb300 import kvc
+    assert kvc.kvc_device_error() == 0
+    util = comp.op_util.cpu().numpy()
+    cost = comp.op_cost.cpu().numpy().astype(np.int64)
+    rel = comp.relevance.cpu().numpy()
+    taken = comp.taken.cpu().numpy().astype(bool)
+    lens = np.zeros((cfg.B, cfg.L, cfg.H), np.int64)
+    for b, s in enumerate(wl.seqs):
+        S = len(s.slot_bounds) - 1
+        sel = O.select_sequence(util[b, :, :, :S], cost[b, :, :, :S], token_view(rel, wl, b),
+                                wl.head_sens, s.slot_bounds, s.n, cfg.W, cfg.budget_ratio,
+                                cfg.budget_entries_per_lh, cfg.floor_cap_frac, cfg.floor_cap_tokens)
+        np.testing.assert_array_equal(taken[b, :, :, :S], sel.taken)
+        assert not taken[b, :, :, S:].any()
+        lens[b] = sel.lens
+    np.testing.assert_array_equal(comp.len_lh.cpu().numpy(), lens)
+    caps, offs = O.offsets(lens, cfg.decode_reserve)
+    np.testing.assert_array_equal(comp.cap_lh.cpu().numpy(), caps)
+    np.testing.assert_array_equal(comp.off_lh.cpu().numpy(), offs)
+    assert int(comp.total.cpu()[0]) == int(caps.sum())
+
+
+def test_pack_matches_oracle(case):
+    cfg, wl, run, p, comp, d, S_max = case
+    comp.select(d["bounds"], d["n_slots"], d["sens"])
+    comp.merge_pack(d["K"], d["V"], d["bounds"], d["n_slots"])
+    torch.cuda.synchronize()
+    from kv_cache_compression_probe_gb300 import kvc
+    assert kvc.kvc_device_error() == 0
+    taken = comp.taken.cpu().numpy().astype(bool)
+    rel = comp.relevance.cpu().numpy()
+    offs = comp.off_lh.cpu().numpy()
+    lens = comp.len_lh.cpu().numpy()
+    Kp = comp.Kp.float().cpu().numpy(); Vp = comp.Vp.float().cpu().numpy()
+    lm = comp.logm.cpu().numpy(); ps = comp.pos.cpu().numpy()
+    rel_only = 0
+    for b, s in enumerate(wl.seqs):
+        S = len(s.slot_bounds) - 1
+        r = token_view(rel, wl, b)
+        for l in range(cfg.L):
+            for h in range(cfg.H):
+                K, V, m, pp = O.pack_head(s.K[l, h], s.V[l, h], r[l, h].astype(np.float64),
+                                          s.slot_bounds, taken[b, l, h, :S], s.n, cfg.W,
+                                          cfg.rope_base, cfg.value_floor)
+                o, n_ = int(offs[b, l, h]), int(lens[b, l, h])
+                assert n_ == len(K)
+                np.testing.assert_array_equal(ps[o:o + n_], pp.astype(np.float32))
+                exact = m == 0
+                np.testing.assert_array_equal(Kp[o:o + n_][exact], K[exact].astype(np.float32))
+                np.testing.assert_array_equal(Vp[o:o + n_][exact], V[exact].astype(np.float32))
+                if cfg.dtype == "bf16":
+                    rel_only += assert_bf16_close(Kp[o:o + n_], K, "packed K")
+                    rel_only += assert_bf16_close(Vp[o:o + n_], V, "packed V")
+                else:
+                    assert_f32_close(Kp[o:o + n_], K, "packed K", rel=1e-5, floor_frac=1.0, axis=-1)
+                    assert_f32_close(Vp[o:o + n_], V, "packed V", rel=1e-5, floor_frac=1.0, axis=-1)
+                np.testing.assert_allclose(lm[o:o + n_], m, rtol=1e-5, atol=1e-6)
+    print(f"elements passing only through the relative bf16 term: {rel_only}")
+
+
+def test_end_to_end_taken_set_against_oracle_chain(case):
+    """The GPU chain's taken set equals the oracle chain's (float64 keys) except
+    for ops whose oracle keys are within 1e-6 relative of a competing key."""
+    cfg, wl, run, p, comp, d, S_max = case
+    from tests.oracle_pipeline import select_all
+    comp.select(d["bounds"], d["n_slots"], d["sens"])
+    taken = comp.taken.cpu().numpy().astype(bool)
+    sels = select_all(wl, run.util, run.cost, run.r)
+    diffs = 0
+    for b, s in enumerate(wl.seqs):
+        S = len(s.slot_bounds) - 1
+        diffs += int((taken[b, :, :, :S] != sels[b].taken).sum())
+    print(f"end-to-end taken-set differences (reported ties): {diffs}")
+    assert diffs <= max(2, int(0.001 * taken.size))
+
+
+def test_full_budget_packs_the_input_bit_exact(built):
+    cfg = W.get_config("tiny").replace(budget_ratio=1.0)
+    wl = W.make_workload(cfg)
+    p, comp, d, S_max = upload_workload(wl)
+    comp.compress(d["K"], d["V"], d["Qp"], d["bounds"], d["n_slots"], d["sens"])
+    torch.cuda.synchronize()
+    assert bool(comp.taken[..., :].bool().all())
+    offs = comp.off_lh.cpu().numpy(); lens = comp.len_lh.cpu().numpy()
+    s = wl.seqs[0]
+    for l in range(cfg.L):
+        for h in range(cfg.H):
+            o, n_ = int(offs[0, l, h]), int(lens[0, l, h])
+            assert n_ == s.n
+            np.testing.assert_array_equal(comp.Kp[o:o + n_].cpu().numpy(), s.K[l, h])
+            np.testing.assert_array_equal(comp.Vp[o:o + n_].cpu().numpy(), s.V[l, h])
+            assert (comp.logm[o:o + n_].cpu().numpy() == 0).all()
+
+
+def test_window_only_budget(built):
+    cfg = W.get_config("tiny")
+    cfg = cfg.replace(budget_ratio=cfg.W / cfg.n)
+    wl = W.make_workload(cfg)
+    p, comp, d, S_max = upload_workload(wl)
+    comp.compress(d["K"], d["V"], d["Qp"], d["bounds"], d["n_slots"], d["sens"])
+    torch.cuda.synchronize()
+    assert not bool(comp.taken.bool().any())
+    assert (comp.len_lh.cpu().numpy() == cfg.W).all()
