@@ -57,6 +57,7 @@ extern "C" {
 #define KVC_ETIMEOUT   -5   /* a bounded device wait gave up                        */
 #define KVC_EWORKSPACE -6   /* workspace missing or smaller than required           */
 #define KVC_EDEVICE    -7   /* device-side check failed (see kvc_device_error)      */
+#define KVC_ESCRATCH   -8   /* problem too large for the built-in scratch array      */
 
 /* ---- element types -------------------------------------------------------- */
 #define KVC_F32  0
@@ -191,6 +192,31 @@ int kvc_decode_attn(const kvc_params* p, const void* q, const void* k_new, const
                     const float* pos_new, void* Kp, void* Vp, float* logm, float* pos,
                     int32_t* len_lh, const int32_t* cap_lh, const int64_t* off_lh, void* out,
                     void* workspace, size_t ws_bytes, void* stream);
+
+/* Allocation-free variant of kvc_decode_attn (no counterpart on the pages: it
+ * is an interface convenience, not part of the method).  For callers that
+ * cannot allocate device memory on the library's behalf: a serving engine whose
+ * pool already holds every free byte of HBM for KV blocks, or a host framework
+ * whose plugin interface cannot pass a workspace and forbids cudaMalloc /
+ * cudaFree inside extensions (cudaFree also synchronises the device).
+ * Same arguments, results and errors as kvc_decode_attn, minus the workspace:
+ * the split-K scratch lives in one file-scope device array of
+ * KVC_DECODE_STATIC_SCRATCH_BYTES that every GPU loading the library holds
+ * until the process exits.  The call allocates nothing (no cudaMalloc, no
+ * cudaFree, no allocating library routine).
+ *  - Problems whose scratch (kvc_workspace_bytes(KVC_WS_DECODE)) exceeds the
+ *    array return KVC_ESCRATCH before anything is launched.
+ *  - The first call on a device looks up the array's device address with that
+ *    device current (cudaGetSymbolAddress); make that first call before any
+ *    stream capture.
+ *  - Every call clears the arrival counters it needs (cudaMemsetAsync on the
+ *    stream) and reuses the same array: calls that overlap on the GPU, on any
+ *    streams, race on it and must be serialised by the caller. */
+#define KVC_DECODE_STATIC_SCRATCH_BYTES (48u << 20)
+int kvc_decode_attn_noalloc(const kvc_params* p, const void* q, const void* k_new,
+                            const void* v_new, const float* pos_new, void* Kp, void* Vp,
+                            float* logm, float* pos, int32_t* len_lh, const int32_t* cap_lh,
+                            const int64_t* off_lh, void* out, void* stream);
 
 /* a0: curvature-guided slot partition ([GK] "01 Curvature-guided
  * partition"): kappa(t) = mean over w in {1,2,4,8} of

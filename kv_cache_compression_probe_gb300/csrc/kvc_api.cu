@@ -64,6 +64,7 @@ const char* kvc_status_string(int s) {
     case KVC_ETIMEOUT: return "bounded device wait timed out";
     case KVC_EWORKSPACE: return "workspace missing or too small";
     case KVC_EDEVICE: return "device-side check failed";
+    case KVC_ESCRATCH: return "problem too large for the allocation-free entry point's scratch";
     default: return "unknown status";
   }
 }

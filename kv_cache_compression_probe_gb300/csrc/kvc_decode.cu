@@ -15,6 +15,8 @@
 // the old length.
 #include <math.h>
 
+#include <mutex>
+
 #include "kvc_common.cuh"
 #include "kvc_internal.h"
 
@@ -302,6 +304,87 @@ extern "C" int kvc_decode_attn(const kvc_params* p, const void* q, const void* k
   a.scale_log2 = kLog2e / sqrtf((float)p->d);
   a.err = err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  dim3 grid(a.n_chunk_max, (unsigned)blh);
+  if (p->dtype == KVC_BF16) {
+    if (p->d == 128) launch_dg<__nv_bfloat16, 128>(p, a, grid, s);
+    else launch_dg<__nv_bfloat16, 64>(p, a, grid, s);
+  } else {
+    if (p->d == 128) launch_dg<float, 128>(p, a, grid, s);
+    else launch_dg<float, 64>(p, a, grid, s);
+  }
+  decode_commit_kernel<<<(unsigned)((blh + 255) / 256), 256, 0, s>>>(len_lh, cap_lh, blh,
+                                                                       a.n_chunk_max, err);
+  kvc::count_launch(2);
+  return kvc::cuda_status(cudaGetLastError());
+}
+
+// ---------------------------------------------------------------- allocation-free variant
+// Some callers cannot hand the library a workspace: a serving engine whose
+// memory pool has already reserved every free byte of HBM for KV blocks, or a
+// host framework whose plugin interface has no way to pass scratch and which
+// forbids extensions from calling cudaMalloc / cudaFree themselves (cudaFree
+// also synchronises the whole device, stalling every other stream).  For them
+// kvc_decode_attn_noalloc keeps the split-K scratch in a fixed array that lives
+// in this library's device image.
+namespace {
+
+constexpr size_t kStaticScratchBytes = (size_t)KVC_DECODE_STATIC_SCRATCH_BYTES;
+
+// Split-K partials followed by the per-(b,l,h) arrival counters.  Every GPU that
+// loads this library holds the array until the process exits.
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[256];
+
+// Device address of g_decode_scratch on the current device (looked up once per
+// device; in host code the symbol itself is only a host-side stand-in).
+void* static_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return nullptr;
+  std::lock_guard<std::mutex> g(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess || !ptr) return nullptr;
+    g_scratch_ptr[dev] = ptr;
+  }
+  return g_scratch_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" int kvc_decode_attn_noalloc(const kvc_params* p, const void* q, const void* k_new,
+                                       const void* v_new, const float* pos_new, void* Kp,
+                                       void* Vp, float* logm, float* pos, int32_t* len_lh,
+                                       const int32_t* cap_lh, const int64_t* off_lh, void* out,
+                                       void* stream) {
+  int st = kvc::check_params(p);
+  if (st != KVC_OK) return st;
+  if (!q || !k_new || !v_new || !Kp || !Vp || !logm || !pos || !len_lh || !cap_lh || !off_lh ||
+      !out)
+    return KVC_EINVAL;
+  const int64_t blh = kvc::lh_count(p);
+  if (blh > 65535) return KVC_EINVAL;
+  const size_t part_bytes =
+      kvc::align256((size_t)blh * n_chunk_max(p) * p->G * (p->d + 2) * sizeof(float));
+  if (part_bytes + kvc::align256((size_t)blh * sizeof(int32_t)) > kStaticScratchBytes)
+    return KVC_ESCRATCH;
+  int32_t* err = kvc::err_word();
+  char* ws = static_cast<char*>(static_scratch());
+  if (!err || !ws) return KVC_ECUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DecodeArgs a;
+  a.q = q; a.k_new = k_new; a.v_new = v_new; a.pos_new = pos_new;
+  a.Kp = Kp; a.Vp = Vp; a.logm = logm; a.pos = pos;
+  a.len_lh = len_lh; a.cap_lh = cap_lh; a.off_lh = off_lh; a.out = out;
+  a.partials = reinterpret_cast<float*>(ws);
+  a.counters = reinterpret_cast<int32_t*>(ws + part_bytes);
+  a.H = p->H; a.L = p->L; a.n_chunk_max = n_chunk_max(p);
+  a.scale_log2 = kLog2e / sqrtf((float)p->d);
+  a.err = err;
+  // the arrival counters must start at zero (the array keeps the last call's contents)
+  cudaError_t e = cudaMemsetAsync(a.counters, 0, (size_t)blh * sizeof(int32_t), s);
+  if (e != cudaSuccess) return KVC_ECUDA;
   dim3 grid(a.n_chunk_max, (unsigned)blh);
   if (p->dtype == KVC_BF16) {
     if (p->d == 128) launch_dg<__nv_bfloat16, 128>(p, a, grid, s);

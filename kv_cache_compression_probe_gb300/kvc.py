@@ -17,13 +17,13 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvc.so")
 
 KVC_OK, KVC_EINVAL, KVC_EBUDGET, KVC_ECAPACITY = 0, -1, -2, -3
-KVC_ECUDA, KVC_ETIMEOUT, KVC_EWORKSPACE, KVC_EDEVICE = -4, -5, -6, -7
+KVC_ECUDA, KVC_ETIMEOUT, KVC_EWORKSPACE, KVC_EDEVICE, KVC_ESCRATCH = -4, -5, -6, -7, -8
 KVC_F32, KVC_BF16 = 0, 1
 KVC_WS_SCORE, KVC_WS_SELECT, KVC_WS_PACK, KVC_WS_DECODE, KVC_WS_PARTITION = range(5)
 
 EXPORTED = ("kvc_status_string", "kvc_device_error", "kvc_launch_count", "kvc_workspace_bytes",
             "kvc_rope_table", "kvc_score", "kvc_select", "kvc_merge_pack", "kvc_decode_attn",
-            "kvc_partition")
+            "kvc_partition", "kvc_decode_attn_noalloc")
 
 
 class kvc_params(ctypes.Structure):
@@ -67,6 +67,8 @@ def lib():
         L.kvc_merge_pack.restype = c_int
         L.kvc_decode_attn.argtypes = [_P] + [vp] * 13 + [c_size_t, vp]
         L.kvc_decode_attn.restype = c_int
+        L.kvc_decode_attn_noalloc.argtypes = [_P] + [vp] * 13
+        L.kvc_decode_attn_noalloc.restype = c_int
         L.kvc_partition.argtypes = [_P, vp, vp, c_int32, vp, vp, vp, vp, c_size_t, vp]
         L.kvc_partition.restype = c_int
         _lib = L
@@ -170,6 +172,16 @@ def kvc_decode_attn(p, q, k_new, v_new, pos_new, Kp, Vp, logm, pos, len_lh, cap_
                                  _ptr(pos_new), _ptr(Kp), _ptr(Vp), _ptr(logm), _ptr(pos),
                                  _ptr(len_lh), _ptr(cap_lh), _ptr(off_lh), _ptr(out), w, wb,
                                  _stream(stream)), "kvc_decode_attn")
+
+
+def kvc_decode_attn_noalloc(p, q, k_new, v_new, pos_new, Kp, Vp, logm, pos, len_lh, cap_lh,
+                            off_lh, out, stream=None):
+    """kvc_decode_attn without a workspace: the library's fixed device scratch array
+    is used instead (for callers that cannot allocate device memory)."""
+    _check(lib().kvc_decode_attn_noalloc(ctypes.byref(p), _ptr(q), _ptr(k_new), _ptr(v_new),
+                                         _ptr(pos_new), _ptr(Kp), _ptr(Vp), _ptr(logm),
+                                         _ptr(pos), _ptr(len_lh), _ptr(cap_lh), _ptr(off_lh),
+                                         _ptr(out), _stream(stream)), "kvc_decode_attn_noalloc")
 
 
 def kvc_partition(p, ctx_len, hidden, dh, kappa, slot_bounds, n_slots, workspace, stream=None):
