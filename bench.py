@@ -235,7 +235,7 @@ def run_gpu(args, cfg, rank, world):
 
     # end to end: pinned host inputs -> device, full path, outputs -> host
     e2e_ms = []
-    for _ in range(max(1, args.steps)):
+    for _ in range(0 if args.profile else max(1, args.steps)):
         torch.cuda.synchronize(dev)
         a0, a1 = ev(), ev()
         a0.record(stream)
@@ -253,7 +253,7 @@ def run_gpu(args, cfg, rank, world):
 
     # max over ranks
     ms = total_ms / args.steps
-    e2e = statistics.mean(e2e_ms)
+    e2e = statistics.mean(e2e_ms) if e2e_ms else float("nan")
     if world > 1:
         tt = torch.tensor([ms, e2e], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -402,9 +402,17 @@ def main():
     ap.add_argument("--config", default="mistral16k")
     ap.add_argument("--decode-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="override the layer count (small profiling cases)")
+    ap.add_argument("--profile", action="store_true",
+                    help="profiling run: no warm-up, one step, no CPU baseline, no e2e leg")
     args = ap.parse_args()
     from synth import workloads as W
     cfg = W.get_config(args.config)
+    if args.layers:
+        cfg = cfg.replace(L=args.layers)
+    if args.profile:
+        args.steps, args.warmup, args.no_cpu_baseline = 1, 0, True
     if args.decode_steps is None:
         args.decode_steps = cfg.n_decode
     rank = int(os.environ.get("RANK", 0))
