@@ -186,7 +186,8 @@ int kvc_merge_pack(const kvc_params* p, const int32_t* ctx_len, const void* K, c
  * still attends (including the new token) but is not appended and reports
  * KVC_ECAPACITY via kvc_device_error.  pos_new may be NULL.
  * Workspace KVC_WS_DECODE holds split-K partials and per-(b,l,h) arrival
- * counters (zero before first use; every call leaves them zero).
+ * counters (zero before first use; every call leaves them zero, except after a
+ * KVC_ETIMEOUT report, when the caller must zero the workspace again).
  * Errors: KVC_EINVAL, KVC_EWORKSPACE, KVC_ECUDA. */
 int kvc_decode_attn(const kvc_params* p, const void* q, const void* k_new, const void* v_new,
                     const float* pos_new, void* Kp, void* Vp, float* logm, float* pos,

@@ -5,8 +5,10 @@
 //
 // Design (HBM-bound): one launch covers every (sequence, layer, KV head).  The
 // entries of an (l,h) are split into chunks of kChunk rows; one 128-thread CTA
-// streams a chunk.  Inside a warp each lane owns d/32 consecutive features of
-// every K/V row (a row is one fully coalesced 256-byte read for bf16, d=128),
+// streams a chunk through a kStages-deep shared-memory ring filled by 1-D bulk
+// asynchronous copies (K and V rows of an (l,h) are contiguous, so a stage is
+// two copies completing on one mbarrier).  Each lane owns d/32 consecutive
+// features of every K/V row read from shared memory,
 // the G query heads' partial dot products of 32/G rows are reduced with one
 // 31-shuffle transpose, and the softmax runs online in base 2.  Chunk partials
 // (max, sum, unnormalised output) go to the workspace; the last CTA of an
@@ -24,7 +26,9 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = 256;
+constexpr int kChunk = 512;       // rows per CTA (split-K chunk)
+constexpr int kStage = 32;        // rows per bulk-copy stage
+constexpr int kStages = 3;        // stages in the shared-memory ring
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeArgs {
@@ -48,9 +52,98 @@ struct DecodeArgs {
 };
 
 template <typename T, int D, int G>
+struct DecodeSmem {
+  T ring[kStages][2][kStage][D];   // K rows, V rows of each stage
+  float p[kWarps][32];
+  float m[kWarps][G], l[kWarps][G];
+  float o[kWarps][G][D];
+  uint64_t full[kStages];
+  int last;
+  int abort;
+};
+
+// One warp batch: rows k < nvalid (of EB = 32/G) at kb + k*D / vb + k*D, the
+// rest masked; 32 dot products, one transpose reduction, online softmax
+// update.  my_lm = log2(e) * log m of row lane / G (0 when masked).
+template <typename T, int D, int G>
+__device__ __forceinline__ void decode_batch(const float (&qv)[G][D / 32], const T* kb,
+                                             const T* vb, int nvalid, float my_lm, int lane,
+                                             float* s_p, float (&m_run)[G], float& lsum,
+                                             float (&o)[G][D / 32]) {
+  constexpr int VPL = D / 32;
+  constexpr int EB = 32 / G;
+  float kk[EB][VPL], vv[EB][VPL];
+#pragma unroll
+  for (int k = 0; k < EB; ++k) {
+    if (k < nvalid) {                       // kb / vb: shared memory, or the new token in global
+      kvcd::VecLoadAny<T, VPL>::ld(kb + k * D + lane * VPL, kk[k]);
+      kvcd::VecLoadAny<T, VPL>::ld(vb + k * D + lane * VPL, vv[k]);
+    } else {
+#pragma unroll
+      for (int t = 0; t < VPL; ++t) kk[k][t] = vv[k][t] = 0.f;
+    }
+  }
+  float part[32];
+#pragma unroll
+  for (int k = 0; k < EB; ++k)
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float acc = 0.f;
+#pragma unroll
+      for (int t = 0; t < VPL; ++t) acc = fmaf(qv[g][t], kk[k][t], acc);
+      part[k * G + g] = acc;
+    }
+#pragma unroll
+  for (int o_ = 16, n = 32; o_ >= 1; o_ >>= 1, n >>= 1) {
+    const bool upper = (lane & o_) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? part[i] : part[i + n / 2];
+      const float keep = upper ? part[i + n / 2] : part[i];
+      part[i] = keep + __shfl_xor_sync(KVC_FULL_MASK, send, o_);
+    }
+  }
+  const int gj = lane % G, kj = lane / G;
+  const float s = kj < nvalid ? part[0] + my_lm : -INFINITY;
+  float gm = s;
+#pragma unroll
+  for (int o_ = G; o_ < 32; o_ <<= 1) gm = fmaxf(gm, __shfl_xor_sync(KVC_FULL_MASK, gm, o_));
+  float alpha[G];
+  float my_m = -INFINITY, my_alpha = 1.f;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float mb = __shfl_sync(KVC_FULL_MASK, gm, g);
+    const float mn = fmaxf(m_run[g], mb);
+    alpha[g] = (mn == -INFINITY) ? 1.f : exp2f(m_run[g] - mn);
+    m_run[g] = mn;
+    if (g == gj) { my_m = mn; my_alpha = alpha[g]; }
+  }
+  const float pr = (s == -INFINITY) ? 0.f : exp2f(s - my_m);
+  lsum = lsum * my_alpha + pr;
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int t = 0; t < VPL; ++t) o[g][t] *= alpha[g];
+  s_p[lane] = pr;
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < EB; ++k)
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float pk = s_p[k * G + g];
+#pragma unroll
+      for (int t = 0; t < VPL; ++t) o[g][t] = fmaf(pk, vv[k][t], o[g][t]);
+    }
+  __syncwarp();
+}
+
+template <typename T, int D, int G>
 __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(DecodeArgs a) {
-  constexpr int VPL = D / 32;   // features per lane
-  constexpr int EB = 32 / G;    // rows per warp batch (EB * G = 32 dot products)
+  constexpr int VPL = D / 32;
+  constexpr int EB = 32 / G;
+  constexpr int RPW = kStage / kWarps;                   // rows of a stage per warp
+  extern __shared__ __align__(128) unsigned char dsm_raw[];
+  DecodeSmem<T, D, G>& sm = *reinterpret_cast<DecodeSmem<T, D, G>*>(dsm_raw);
   const int blh = blockIdx.y;
   const int c = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -63,6 +156,8 @@ __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(DecodeArgs a) {
   }
   if (c >= nchunks) return;
   const int e0 = c * kChunk, e1 = min(e0 + kChunk, E);
+  const int stored_end = min(e1, len);                   // rows [e0, stored_end) come from the cache
+  const int nst = stored_end > e0 ? (stored_end - e0 + kStage - 1) / kStage : 0;
   const int64_t off = a.off_lh[blh];
   const bool append_ok = (len + 1 <= a.cap_lh[blh]);
   const int h = blh % a.H;
@@ -75,6 +170,22 @@ __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(DecodeArgs a) {
   const T* vn = static_cast<const T*>(a.v_new) + (int64_t)blh * D;
   const T* qp = static_cast<const T*>(a.q) + (bl * a.H * G + (int64_t)h * G) * D;
 
+  auto issue = [&](int st) {                             // one thread: stage st -> slot st % kStages
+    const int slot = st % kStages;
+    const int r0 = e0 + st * kStage;
+    const int rows = min(kStage, stored_end - r0);
+    const uint32_t bytes = (uint32_t)(rows * D * sizeof(T));
+    kvcd::mbar_arrive_expect_tx(&sm.full[slot], 2 * bytes);
+    kvcd::bulk_g2s(&sm.ring[slot][0][0][0], Kp + (int64_t)r0 * D, bytes, &sm.full[slot]);
+    kvcd::bulk_g2s(&sm.ring[slot][1][0][0], Vp + (int64_t)r0 * D, bytes, &sm.full[slot]);
+  };
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) kvcd::mbar_init(&sm.full[i], 1);
+    kvcd::fence_mbar_init();
+    sm.abort = 0;
+    for (int st = 0; st < min(kStages, nst); ++st) issue(st);
+  }
+
   float qv[G][VPL];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
@@ -82,11 +193,6 @@ __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(DecodeArgs a) {
 #pragma unroll
     for (int t = 0; t < VPL; ++t) qv[g][t] *= a.scale_log2;
   }
-
-  __shared__ float s_p[kWarps][32];
-  __shared__ float s_m[kWarps][G], s_l[kWarps][G];
-  __shared__ float s_o[kWarps][G][D];
-
   float m_run[G], o[G][VPL];
   float lsum = 0.f;
 #pragma unroll
@@ -95,93 +201,56 @@ __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(DecodeArgs a) {
 #pragma unroll
     for (int t = 0; t < VPL; ++t) o[g][t] = 0.f;
   }
-  const int gj = lane % G, kj = lane / G;
+  __syncthreads();
 
-  for (int eb = e0 + warp * EB; eb < e1; eb += kWarps * EB) {
-    float kk[EB][VPL], vv[EB][VPL];
-#pragma unroll
-    for (int k = 0; k < EB; ++k) {
-      const int e = eb + k;
-      if (e < len && e < e1) {
-        kvcd::VecLoad<T, VPL>::ld(Kp + (int64_t)e * D + lane * VPL, kk[k]);
-        kvcd::VecLoad<T, VPL>::ld(Vp + (int64_t)e * D + lane * VPL, vv[k]);
-      } else if (e == len) {
-        kvcd::VecLoad<T, VPL>::ld(kn + lane * VPL, kk[k]);
-        kvcd::VecLoad<T, VPL>::ld(vn + lane * VPL, vv[k]);
-      } else {
-#pragma unroll
-        for (int t = 0; t < VPL; ++t) kk[k][t] = vv[k][t] = 0.f;
-      }
+  int consumed = 0;
+  for (int st = 0; st < nst; ++st) {
+    const int slot = st % kStages;
+    if (!kvcd::mbar_wait(&sm.full[slot], (uint32_t)((st / kStages) & 1))) sm.abort = 1;
+    const int r0 = e0 + st * kStage;
+    const int rows = min(kStage, stored_end - r0);
+    for (int rb = warp * RPW; rb < warp * RPW + RPW; rb += EB) {
+      const int nvalid = min(min(EB, rows - rb), warp * RPW + RPW - rb);
+      const int my_row = rb + lane / G;
+      const float my_lm = (lane / G < nvalid) ? __ldg(lm + r0 + my_row) * kLog2e : 0.f;
+      decode_batch<T, D, G>(qv, &sm.ring[slot][0][rb][0], &sm.ring[slot][1][rb][0], nvalid, my_lm,
+                            lane, sm.p[warp], m_run, lsum, o);
     }
-    // 32 partial dot products (row k, head g) -> index k * G + g
-    float part[32];
-#pragma unroll
-    for (int k = 0; k < EB; ++k)
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float acc = 0.f;
-#pragma unroll
-        for (int t = 0; t < VPL; ++t) acc = fmaf(qv[g][t], kk[k][t], acc);
-        part[k * G + g] = acc;
-      }
-    // transpose-reduce: afterwards lane j holds the full sum of index j
-#pragma unroll
-    for (int o_ = 16, n = 32; o_ >= 1; o_ >>= 1, n >>= 1) {
-      const bool upper = (lane & o_) != 0;
-#pragma unroll
-      for (int i = 0; i < n / 2; ++i) {
-        const float send = upper ? part[i] : part[i + n / 2];
-        const float keep = upper ? part[i + n / 2] : part[i];
-        part[i] = keep + __shfl_xor_sync(KVC_FULL_MASK, send, o_);
-      }
+    consumed = st + 1;
+    __syncthreads();
+    if (sm.abort) break;
+    if (tid == 0 && st + kStages < nst) {
+      kvcd::fence_proxy_async_smem();
+      issue(st + kStages);
     }
-    const int ej = eb + kj;
-    float s = -INFINITY;
-    if (ej < e1) s = part[0] + (ej < len ? __ldg(lm + ej) * kLog2e : 0.f);
-    float gm = s;
-#pragma unroll
-    for (int o_ = G; o_ < 32; o_ <<= 1) gm = fmaxf(gm, __shfl_xor_sync(KVC_FULL_MASK, gm, o_));
-    float alpha[G];
-    float my_m = -INFINITY, my_alpha = 1.f;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float mb = __shfl_sync(KVC_FULL_MASK, gm, g);
-      const float mn = fmaxf(m_run[g], mb);
-      alpha[g] = (mn == -INFINITY) ? 1.f : exp2f(m_run[g] - mn);
-      m_run[g] = mn;
-      if (g == gj) { my_m = mn; my_alpha = alpha[g]; }
+  }
+  if (sm.abort) {                                        // a bounded wait gave up
+    if (tid == 0) {
+      kvcd::record_error(a.err, KVC_ETIMEOUT);
+      // copies still in flight: the stage whose wait failed and those issued after it
+      const int first = max(0, consumed - 1);
+      for (int st = first; st < min(nst, first + kStages); ++st)
+        kvcd::mbar_wait(&sm.full[st % kStages], (uint32_t)((st / kStages) & 1));
     }
-    const float pr = (s == -INFINITY) ? 0.f : exp2f(s - my_m);
-    lsum = lsum * my_alpha + pr;
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int t = 0; t < VPL; ++t) o[g][t] *= alpha[g];
-    s_p[warp][lane] = pr;
-    __syncwarp();
-#pragma unroll
-    for (int k = 0; k < EB; ++k)
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float pk = s_p[warp][k * G + g];
-#pragma unroll
-        for (int t = 0; t < VPL; ++t) o[g][t] = fmaf(pk, vv[k][t], o[g][t]);
-      }
-    __syncwarp();
+    return;
+  }
+  // the new token (row len) when this chunk holds it
+  if (warp == 0 && e0 <= len && len < e1) {
+    decode_batch<T, D, G>(qv, kn, vn, 1, 0.f, lane, sm.p[0], m_run, lsum, o);
   }
   // per-head row sums of this warp
 #pragma unroll
   for (int o_ = G; o_ < 32; o_ <<= 1) lsum += __shfl_xor_sync(KVC_FULL_MASK, lsum, o_);
   if (lane < G) {
-    s_l[warp][lane] = lsum;
+    sm.l[warp][lane] = lsum;
 #pragma unroll
     for (int g = 0; g < G; ++g)
-      if (g == lane) s_m[warp][lane] = m_run[g];
+      if (g == lane) sm.m[warp][lane] = m_run[g];
   }
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int t = 0; t < VPL; ++t) s_o[warp][g][lane * VPL + t] = o[g][t];
+    for (int t = 0; t < VPL; ++t) sm.o[warp][g][lane * VPL + t] = o[g][t];
 
   // the chunk holding row `len` stores the appended token
   if (append_ok && e0 <= len && len < e1) {
@@ -201,23 +270,22 @@ __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(DecodeArgs a) {
     const int g = idx / D, dd = idx % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_m[w][g]);
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.m[w][g]);
     float acc = 0.f, l = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      const float f = (s_m[w][g] == -INFINITY) ? 0.f : exp2f(s_m[w][g] - M);
-      acc = fmaf(f, s_o[w][g][dd], acc);
-      l = fmaf(f, s_l[w][g], l);
+      const float f = (sm.m[w][g] == -INFINITY) ? 0.f : exp2f(sm.m[w][g] - M);
+      acc = fmaf(f, sm.o[w][g][dd], acc);
+      l = fmaf(f, sm.l[w][g], l);
     }
     part_out[g * (D + 2) + 2 + dd] = acc;
     if (dd == 0) { part_out[g * (D + 2)] = M; part_out[g * (D + 2) + 1] = l; }
   }
   __threadfence();
   __syncthreads();
-  __shared__ int s_last;
-  if (tid == 0) s_last = (atomicAdd(a.counters + blh, 1) == nchunks - 1);
+  if (tid == 0) sm.last = (atomicAdd(a.counters + blh, 1) == nchunks - 1);
   __syncthreads();
-  if (!s_last) return;
+  if (!sm.last) return;
   __threadfence();
 
   // last chunk to arrive: log-sum-exp merge of all chunk partials
@@ -256,13 +324,21 @@ inline int n_chunk_max(const kvc_params* p) {
   return (int)((rows + kChunk - 1) / kChunk);
 }
 
+template <typename T, int D, int G>
+void launch_one(const DecodeArgs& a, dim3 grid, cudaStream_t s) {
+  const size_t smem = sizeof(DecodeSmem<T, D, G>);
+  cudaFuncSetAttribute(decode_chunk_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)smem);
+  decode_chunk_kernel<T, D, G><<<grid, kThreads, smem, s>>>(a);
+}
+
 template <typename T, int D>
 void launch_dg(const kvc_params* p, const DecodeArgs& a, dim3 grid, cudaStream_t s) {
   switch (p->G) {
-    case 1: decode_chunk_kernel<T, D, 1><<<grid, kThreads, 0, s>>>(a); break;
-    case 2: decode_chunk_kernel<T, D, 2><<<grid, kThreads, 0, s>>>(a); break;
-    case 4: decode_chunk_kernel<T, D, 4><<<grid, kThreads, 0, s>>>(a); break;
-    default: decode_chunk_kernel<T, D, 8><<<grid, kThreads, 0, s>>>(a); break;
+    case 1: launch_one<T, D, 1>(a, grid, s); break;
+    case 2: launch_one<T, D, 2>(a, grid, s); break;
+    case 4: launch_one<T, D, 4>(a, grid, s); break;
+    default: launch_one<T, D, 8>(a, grid, s); break;
   }
 }
 
