@@ -93,6 +93,10 @@ typedef struct kvc_params {
   double  floor_cap_frac;  /* [GK] singleton floor cap, fraction of B_alloc (0.6)  */
   int64_t floor_cap_tokens;/* token cap of the floor; < 0 = none                   */
   int32_t decode_reserve;  /* rows reserved per (l,h) for decode-time appends      */
+  int64_t total_ctx;       /* sum of ctx_len over the batch (rows of K are
+                              L*H*total_ctx); 0 = unknown, which disables the
+                              tensor-core scoring passes (they need the exact
+                              extent of K for their TMA descriptor)             */
 } kvc_params;
 
 /* Human-readable name of a status code (static string). */

@@ -24,8 +24,12 @@
 // registers and the key tile broadcast from shared memory.
 #include <math.h>
 
+#include <algorithm>
+#include <type_traits>
+
 #include "kvc_common.cuh"
 #include "kvc_internal.h"
+#include "kvc_score_tc.h"
 
 namespace {
 
@@ -319,6 +323,44 @@ __global__ void numean_kernel(kvc_params p, ScoreArgs a) {
     float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
     v = kvcd::warp_sum(v);
     if (threadIdx.x == 0) a.nu[blh] = v / (float)n;
+  }
+}
+
+// |v_i| and pos_i features plus the mean |v| of one (b,l,h) (tensor-core path,
+// where the feature epilogue does not touch the values).
+template <typename T, int D>
+__global__ void vnorm_kernel(kvc_params p, ScoreArgs a) {
+  const long long blh = blockIdx.x;
+  if (!a.ok[blh]) return;
+  const int b = seq_of(p, blh);
+  const int lh = (int)(blh % ((long long)p.L * p.H));
+  const int n = a.ctx_len[b];
+  const int64_t row0 = kvcd::seq_token_base(a.ctx_len, b, p.L * p.H) + (int64_t)lh * n;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  constexpr int VPL = D / 32;
+  float acc = 0.f;
+  for (int i = warp; i < n; i += nw) {
+    float v[VPL];
+    kvcd::VecLoad<T, VPL>::ld(static_cast<const T*>(a.V) + (row0 + i) * D + lane * VPL, v);
+    float s2 = 0.f;
+#pragma unroll
+    for (int t = 0; t < VPL; ++t) s2 = fmaf(v[t], v[t], s2);
+    s2 = kvcd::warp_sum(s2);
+    const float nv = sqrtf(s2);
+    if (lane == 0) {
+      float* f = a.feats + (row0 + i) * 5;
+      f[1] = nv;
+      f[4] = (float)i / (float)max(n - 1, 1);
+      acc += nv;
+    }
+  }
+  __shared__ float red[32];
+  if (lane == 0) red[warp] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < nw; ++w) t += red[w];
+    a.nu[blh] = t / (float)n;
   }
 }
 
@@ -756,12 +798,18 @@ int chunk_for(const kvc_params* p) {
   return c;
 }
 
+// tensor-core passes: 16 key tiles of 128 per CTA
+constexpr int kTcChunkTiles = 16;
+int tc_chunks(const kvc_params* p) { return (p->n_max + kTcChunkTiles * 128 - 1) / (kTcChunkTiles * 128); }
+
+bool use_tc(const kvc_params* p) { return p->total_ctx > 0 && kvc::probe_tc_supported(p); }
+
 struct Layout {
   size_t part, lse2, hrow, nu, seeds, seed_w, lse2_h, ok, total;
 };
 Layout layout(const kvc_params* p) {
   const size_t blh = (size_t)kvc::lh_count(p);
-  const int nch = (p->n_max + chunk_for(p) - 1) / chunk_for(p);
+  const int nch = std::max((p->n_max + chunk_for(p) - 1) / chunk_for(p), tc_chunks(p));
   const int R = p->G * p->P;
   Layout l;
   size_t o = 0;
@@ -794,6 +842,35 @@ int launch_all(const kvc_params* p, ScoreArgs& a, cudaStream_t s) {
   cudaFuncSetAttribute(nodes_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)sm_nodes);
   score_check_kernel<<<(unsigned)((blh + 255) / 256), 256, 0, s>>>(*p, a); ++launches;
+  if (std::is_same<T, __nv_bfloat16>::value && D == 128 && use_tc(p)) {
+    // tensor-core probe-times-key passes
+    kvc::ProbeTcArgs t;
+    t.ctx_len = a.ctx_len; t.K = a.K; t.V = a.V; t.Qp = a.Qp; t.seeds = a.seeds;
+    t.seed_w = a.seed_w; t.lse2 = a.lse2; t.hrow = a.hrow; t.lse2_h = a.lse2_h; t.ok = a.ok;
+    t.part = a.part; t.feats = a.feats; t.rel = a.rel; t.err = a.err;
+    t.B = p->B; t.L = p->L; t.H = p->H; t.G = p->G; t.P = p->P;
+    t.chunk_tiles = kTcChunkTiles; t.n_chunks = tc_chunks(p);
+    t.q_scale2 = a.q_scale2; t.hop_weight = p->hop_weight;
+    a.n_chunks = t.n_chunks;                        // rowcombine loops over these partials
+    const int64_t rows_total = p->total_ctx * p->L * p->H;
+    int st;
+    if ((st = kvc::probe_tc_pass(kvc::kTcRowstatsProbes, t, rows_total, s)) != KVC_OK) return st;
+    rowcombine_kernel<false><<<(unsigned)blh, 256, 0, s>>>(*p, a);
+    if ((st = kvc::probe_tc_pass(kvc::kTcFeats, t, rows_total, s)) != KVC_OK) return st;
+    vnorm_kernel<T, D><<<(unsigned)blh, 256, 0, s>>>(*p, a);
+    launches += 2;
+    for (int hop = 0; hop < p->n_hops; ++hop) {
+      seeds_kernel<<<(unsigned)blh, 1024, 0, s>>>(*p, a);
+      if ((st = kvc::probe_tc_pass(kvc::kTcRowstatsSeeds, t, rows_total, s)) != KVC_OK) return st;
+      rowcombine_kernel<true><<<(unsigned)blh, 256, 0, s>>>(*p, a);
+      if ((st = kvc::probe_tc_pass(kvc::kTcProp, t, rows_total, s)) != KVC_OK) return st;
+      launches += 2;
+    }
+    nodes_kernel<T, D><<<(unsigned)(blh * p->S_max), 256, sm_nodes, s>>>(*p, a);
+    ++launches;
+    kvc::count_launch(launches);
+    return kvc::cuda_status(cudaGetLastError());
+  }
   const dim3 g_rows(a.n_chunks, (unsigned)blh);
   rowstats_kernel<T, D, false><<<g_rows, 256, sm_rows, s>>>(*p, a);
   rowcombine_kernel<false><<<(unsigned)blh, 256, 0, s>>>(*p, a);

@@ -1,0 +1,416 @@
+// Tensor-core (tcgen05 / TMEM / TMA) probe-times-key passes of kvc_score for
+// bf16 caches with d = 128 (DistillCache 3.1.1 features; GraceKV "03 Bottom-up
+// value flow": direct probe attention and the two relevance hops).
+//
+// One CTA = one (b,l,h) and a chunk of 128-key tiles.
+//   * The query rows (probe rows, or the hop seeds' values) are written once
+//     into shared memory in the 128-byte-swizzled K-major layout: NT tiles of
+//     128 rows x 128 features (two 64-feature swizzle blocks each).
+//   * One producer thread streams key tiles (128 keys x 128 features) with 2-D
+//     TMA copies (128B swizzle) through a 3-stage ring.
+//   * One MMA thread issues tcgen05.mma (M = 128, N = 128, K = 16, bf16 in,
+//     fp32 out) into a double-buffered TMEM accumulator (2 x NT x 128 columns).
+//   * 4*NT epilogue warps read their rows' scores with tcgen05.ld (warp w owns
+//     TMEM lanes 32*(w%4)..+31 of tile w/4) and run one of three epilogues:
+//       ROWSTATS  online max / sum / sum p*(s - max) per row  -> chunk partials
+//       FEATS     a = 2^(s - LSE); per key: sum a, sum a*H_row, per-head sums
+//                 -> alpha, sigma, H features and r0 = alpha
+//       PROP      per key: sum over seeds of w_s 2^(s - LSE_s)
+//                 -> r = alpha + hop_weight * Prop
+// Every mbarrier wait is bounded (KVC_ETIMEOUT); TMEM is always freed.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "kvc_common.cuh"
+#include "kvc_internal.h"
+#include "kvc_score_tc.h"
+
+namespace {
+
+constexpr int kBM = 128;                 // rows per M tile (TMEM lanes)
+constexpr int kBN = 128;                 // keys per tile (TMEM columns per tile)
+constexpr int kD = 128;                  // head dim
+constexpr int kStages = 3;
+constexpr uint32_t kTileBytes = kBN * kD * 2;      // 32 KB per key tile (two swizzle blocks)
+constexpr uint32_t kBlockBytes = kBN * 64 * 2;     // 16 KB per 64-feature swizzle block
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4)      // start address (16-byte units)
+         | ((uint64_t)1 << 16)                    // leading byte offset (unused for SW128 K-major)
+         | ((uint64_t)(1024 >> 4) << 32)          // stride byte offset: 8 rows x 128 B
+         | ((uint64_t)1 << 46)                    // descriptor version (tcgen05)
+         | ((uint64_t)2 << 61);                   // 128-byte swizzle
+}
+
+// kind::f16 instruction descriptor: D f32, A/B bf16, both K-major, M = 128, N = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
+                            ((uint32_t)(kBM >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(kIdesc), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          kvcd::smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3}], [%4];" ::"r"(kvcd::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(kvcd::smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void named_bar(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// After the call lane j holds the warp-wide sum of v[j] (31 shuffles).
+__device__ __forceinline__ float transpose_reduce(float (&v)[32], int lane) {
+#pragma unroll
+  for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? v[i] : v[i + n / 2];
+      const float keep = upper ? v[i + n / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(KVC_FULL_MASK, send, o);
+    }
+  }
+  return v[0];
+}
+
+template <int NT>
+struct TcSmem {
+  alignas(1024) unsigned char A[NT][2][kBlockBytes];       // query rows, swizzled
+  alignas(1024) unsigned char Bt[kStages][2][kBlockBytes]; // key tiles, swizzled
+  float red[4 * NT][kBN][2];                                // epilogue per-warp key sums
+  uint64_t full[kStages], empty[kStages], tfull[2], tempty[2];
+  uint32_t tmem_base;
+  int abort;
+  int issued;
+};
+
+template <int NT, int MODE>
+__global__ void __launch_bounds__((4 * NT + 2) * 32, 1)
+    probe_tc_kernel(const __grid_constant__ CUtensorMap kmap, kvc::ProbeTcArgs a) {
+  extern __shared__ __align__(1024) unsigned char tc_raw[];
+  // the dynamic shared memory base is aligned up to 1024 bytes by hand
+  TcSmem<NT>& sm = *reinterpret_cast<TcSmem<NT>*>(
+      (reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int kEpiWarps = 4 * NT;
+  constexpr int kThreads = (kEpiWarps + 2) * 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long blh = blockIdx.y;
+  const int LH = a.L * a.H;
+  const int b = (int)(blh / LH);
+  const int lh = (int)(blh % LH);
+  const int n = a.ctx_len[b];
+  const int k0 = blockIdx.x * a.chunk_tiles * kBN;
+  const bool seeds = (MODE == kvc::kTcRowstatsSeeds || MODE == kvc::kTcProp);
+  const int rows = seeds ? a.P : a.G * a.P;
+  float* part_out = nullptr;
+  if (MODE == kvc::kTcRowstatsProbes || MODE == kvc::kTcRowstatsSeeds)
+    part_out = a.part + (blh * a.n_chunks + blockIdx.x) * 256 * 3;
+  if (!a.ok[blh] || k0 >= n) {
+    if (part_out && tid < rows) {
+      part_out[tid * 3] = -INFINITY; part_out[tid * 3 + 1] = 0.f; part_out[tid * 3 + 2] = 0.f;
+    }
+    return;
+  }
+  const int k1 = min(n, k0 + a.chunk_tiles * kBN);
+  const int ntiles = (k1 - k0 + kBN - 1) / kBN;
+  const int64_t row0 = kvcd::seq_token_base(a.ctx_len, b, LH) + (int64_t)lh * n;
+
+  // ---- query rows -> swizzled K-major smem (generic stores, then a proxy fence)
+  for (int idx = tid; idx < NT * kBM * 16; idx += kThreads) {
+    const int r = idx >> 4, c = idx & 15;      // row, 16-byte chunk (8 per swizzle block)
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (r < rows) {
+      const __nv_bfloat16* src;
+      if (seeds) src = static_cast<const __nv_bfloat16*>(a.V) + (row0 + a.seeds[blh * a.P + r]) * kD;
+      else src = static_cast<const __nv_bfloat16*>(a.Qp) + (blh * rows + r) * kD;
+      val = __ldg(reinterpret_cast<const uint4*>(src) + c);
+    }
+    const int mt = r >> 7, rr = r & 127, kb = c >> 3, cc = c & 7;
+    *reinterpret_cast<uint4*>(&sm.A[mt][kb][rr * 128 + ((cc ^ (rr & 7)) << 4)]) = val;
+  }
+  kvcd::fence_proxy_async_smem();
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) { kvcd::mbar_init(&sm.full[s], 1); kvcd::mbar_init(&sm.empty[s], 1); }
+    for (int s = 0; s < 2; ++s) { kvcd::mbar_init(&sm.tfull[s], 1); kvcd::mbar_init(&sm.tempty[s], kEpiWarps); }
+    sm.abort = 0;
+    sm.issued = 0;
+    kvcd::fence_mbar_init();
+  }
+  constexpr uint32_t kCols = NT == 2 ? 512u : 256u;
+  if (warp == kEpiWarps + 1) {                     // MMA warp allocates TMEM
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     kvcd::smem_u32(&sm.tmem_base)), "r"(kCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == kEpiWarps) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % kStages;
+        if (t >= kStages && !kvcd::mbar_wait(&sm.empty[s], (uint32_t)(((t / kStages) - 1) & 1))) {
+          sm.abort = 1;
+          break;
+        }
+        kvcd::mbar_arrive_expect_tx(&sm.full[s], kTileBytes);
+        const int y = (int)(row0 + k0 + t * kBN);
+        tma_load_2d(sm.Bt[s][0], &kmap, 0, y, &sm.full[s]);
+        tma_load_2d(sm.Bt[s][1], &kmap, 64, y, &sm.full[s]);
+        sm.issued = t + 1;
+      }
+    }
+  } else if (warp == kEpiWarps + 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % kStages, bf = t & 1;
+        if (!kvcd::mbar_wait(&sm.full[s], (uint32_t)((t / kStages) & 1))) { sm.abort = 1; break; }
+        if (t >= 2 && !kvcd::mbar_wait(&sm.tempty[bf], (uint32_t)(((t >> 1) - 1) & 1))) {
+          sm.abort = 1;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int mt = 0; mt < NT; ++mt) {
+          const uint32_t d = tmem + (uint32_t)((bf * NT + mt) * kBN);
+#pragma unroll
+          for (int k = 0; k < kD / 16; ++k) {
+            const uint32_t aoff = kvcd::smem_u32(sm.A[mt][k >> 2]) + (k & 3) * 32;
+            const uint32_t boff = kvcd::smem_u32(sm.Bt[s][k >> 2]) + (k & 3) * 32;
+            mma_bf16(d, sw128_desc(aoff), sw128_desc(boff), k > 0 ? 1u : 0u);
+          }
+        }
+        mma_commit(&sm.empty[s]);
+        mma_commit(&sm.tfull[bf]);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int mt = warp >> 2, q = warp & 3;
+    const int r = mt * kBM + q * 32 + lane;
+    const bool rv = r < rows;
+    const int limit = seeds ? n - 1 : n - a.P + (r % a.P);
+    float l2 = 0.f, hr = 0.f, wr = 0.f;
+    if (MODE == kvc::kTcFeats && rv) { l2 = a.lse2[blh * rows + r]; hr = a.hrow[blh * rows + r]; }
+    if (MODE == kvc::kTcProp && rv) { l2 = a.lse2_h[blh * a.P + r]; wr = a.seed_w[blh * a.P + r]; }
+    float m = -INFINITY, l = 0.f, u = 0.f, cl = 0.f, cu = 0.f;
+    volatile int* abort_flag = &sm.abort;
+    for (int t = 0; t < ntiles; ++t) {
+      // every epilogue warp runs all ntiles iterations (they share named
+      // barriers); after an abort the waits are skipped and the work is void
+      const int bf = t & 1;
+      if (!*abort_flag && !kvcd::mbar_wait(&sm.tfull[bf], (uint32_t)((t >> 1) & 1))) *abort_flag = 1;
+      tc_fence_after();
+      const int kt = k0 + t * kBN;
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)((bf * NT + mt) * kBN + c * 32), v);
+        const int i0 = kt + c * 32;
+        if (MODE == kvc::kTcRowstatsProbes || MODE == kvc::kTcRowstatsSeeds) {
+          float mx = m;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const bool ok = rv && (i0 + j) < k1 && (i0 + j) <= limit;
+            v[j] = ok ? v[j] * a.q_scale2 : -INFINITY;
+            mx = fmaxf(mx, v[j]);
+          }
+          if (mx != -INFINITY) {
+            if (mx > m && m != -INFINITY) {
+              const float sc = exp2f(m - mx);
+              u = sc * (u + (m - mx) * l);
+              cu *= sc; l *= sc; cl *= sc;
+            }
+            m = mx;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (v[j] == -INFINITY) continue;
+              const float e = exp2f(v[j] - mx);
+              const float yl = e - cl, tl = l + yl;
+              cl = (tl - l) - yl; l = tl;
+              const float yu = e * (v[j] - mx) - cu, tu = u + yu;
+              cu = (tu - u) - yu; u = tu;
+            }
+          }
+        } else {
+          float w[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const bool ok = rv && (i0 + j) < k1 && (i0 + j) <= limit;
+            const float e = ok ? exp2f(v[j] * a.q_scale2 - l2) : 0.f;
+            v[j] = MODE == kvc::kTcProp ? wr * e : e;
+            w[j] = e * hr;
+          }
+          const float sa = transpose_reduce(v, lane);
+          sm.red[warp][c * 32 + lane][0] = sa;
+          if (MODE == kvc::kTcFeats) {
+            const float sh = transpose_reduce(w, lane);
+            sm.red[warp][c * 32 + lane][1] = sh;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) kvcd::mbar_arrive(&sm.tempty[bf]);
+      if (MODE == kvc::kTcFeats || MODE == kvc::kTcProp) {
+        named_bar(1, kEpiWarps * 32);
+        const int et = tid;                             // epilogue thread index
+        if (et < kBN && kt + et < k1) {
+          const int i = kt + et;
+          float sa = 0.f, sh = 0.f;
+          for (int w2 = 0; w2 < kEpiWarps; ++w2) { sa += sm.red[w2][et][0]; sh += sm.red[w2][et][1]; }
+          if (MODE == kvc::kTcFeats) {
+            // per query head: the rows of head g are warps [g*P/32, (g+1)*P/32)
+            const int wpg = a.P / 32;
+            float mean = 0.f, gs[8];
+            for (int g = 0; g < a.G; ++g) {
+              float x = 0.f;
+              for (int w2 = g * wpg; w2 < (g + 1) * wpg; ++w2) x += sm.red[w2][et][0];
+              gs[g] = x / (float)a.P;
+              mean += gs[g];
+            }
+            mean /= (float)a.G;
+            float var = 0.f;
+            for (int g = 0; g < a.G; ++g) { const float dd = gs[g] - mean; var += dd * dd; }
+            var /= (float)a.G;
+            float* f = a.feats + (row0 + i) * 5;
+            const float alpha = sa / (float)rows;
+            f[0] = alpha;
+            f[2] = var;
+            f[3] = sa > 0.f ? sh / sa : 0.f;
+            a.rel[row0 + i] = alpha;
+          } else {
+            a.rel[row0 + i] = a.feats[(row0 + i) * 5] + a.hop_weight * sa;
+          }
+        }
+        named_bar(1, kEpiWarps * 32);
+      }
+    }
+    if (part_out && rv) { part_out[r * 3] = m; part_out[r * 3 + 1] = l; part_out[r * 3 + 2] = u; }
+  }
+
+  // ---- teardown: every role has finished; wait out copies of an aborted run
+  __syncthreads();
+  if (sm.abort && tid == 0) {
+    kvcd::record_error(a.err, KVC_ETIMEOUT);
+    // bounded wait for the key tiles still in flight (the last kStages issued)
+    for (int t = max(0, sm.issued - kStages); t < sm.issued; ++t)
+      kvcd::mbar_wait(&sm.full[t % kStages], (uint32_t)((t / kStages) & 1), 100000000ull);
+  }
+  tc_fence_after();
+  if (warp == kEpiWarps + 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+template <int NT, int MODE>
+int launch(const CUtensorMap& map, const kvc::ProbeTcArgs& a, cudaStream_t s) {
+  const size_t smem = sizeof(TcSmem<NT>) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(probe_tc_kernel<NT, MODE>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return KVC_ECUDA;
+  dim3 grid(a.n_chunks, (unsigned)((long long)a.B * a.L * a.H));
+  probe_tc_kernel<NT, MODE><<<grid, (4 * NT + 2) * 32, smem, s>>>(map, a);
+  kvc::count_launch();
+  return kvc::cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+namespace kvc {
+
+bool probe_tc_supported(const kvc_params* p) {
+  return p->dtype == KVC_BF16 && p->d == 128 && p->P % 32 == 0 && p->G * p->P <= 256 &&
+         p->P <= 128 && encode_fn() != nullptr;
+}
+
+int probe_tc_pass(int mode, const ProbeTcArgs& a, int64_t total_rows, cudaStream_t s) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return KVC_ECUDA;
+  CUtensorMap map;
+  cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)total_rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kBN};
+  cuuint32_t estr[2] = {1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.K), dims, strides, box,
+          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return KVC_ECUDA;
+  const bool two = a.G * a.P > 128;
+  switch (mode) {
+    case kTcRowstatsProbes:
+      return two ? launch<2, kTcRowstatsProbes>(map, a, s) : launch<1, kTcRowstatsProbes>(map, a, s);
+    case kTcFeats:
+      return two ? launch<2, kTcFeats>(map, a, s) : launch<1, kTcFeats>(map, a, s);
+    case kTcRowstatsSeeds:
+      return launch<1, kTcRowstatsSeeds>(map, a, s);
+    default:
+      return launch<1, kTcProp>(map, a, s);
+  }
+}
+
+}  // namespace kvc

@@ -30,10 +30,13 @@ def packed_capacity(p: kvc.kvc_params, ctx_len: Sequence[int]) -> int:
 
 
 class Compressor:
-    def __init__(self, p: kvc.kvc_params, ctx_len: Sequence[int], device="cuda"):
+    def __init__(self, p: kvc.kvc_params, ctx_len: Sequence[int], device="cuda",
+                 tensor_cores: bool = True):
         self.p = p
         self.device = device
         self.ctx_host = [int(n) for n in ctx_len]
+        # the tensor-core scoring passes need the exact extent of K
+        p.total_ctx = sum(self.ctx_host) if tensor_cores else 0
         assert len(self.ctx_host) == p.B and max(self.ctx_host) <= p.n_max
         B, L, H, R, S = p.B, p.L, p.H, p.G * p.P, p.S_max
         rows = sum(L * H * n for n in self.ctx_host)

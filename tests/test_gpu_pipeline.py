@@ -30,12 +30,20 @@ def _cases():
     }
 
 
-@pytest.fixture(scope="module", params=["tiny", "small"])
+_ORACLE = {}
+
+
+@pytest.fixture(scope="module", params=["tiny", "small-tc", "small-simt"])
 def case(request, built):
-    cfg = _cases()[request.param]
-    wl = W.make_workload(cfg)
-    run = score_all(wl)
-    p, comp, d, S_max = upload_workload(wl)
+    """tiny: fp32, d 64 (SIMT scoring); small: bf16, d 128, scored with the
+    tcgen05 passes (small-tc) and with the SIMT passes (small-simt)."""
+    name = request.param.split("-")[0]
+    cfg = _cases()[name]
+    if name not in _ORACLE:
+        wl = W.make_workload(cfg)
+        _ORACLE[name] = (wl, score_all(wl))
+    wl, run = _ORACLE[name]
+    p, comp, d, S_max = upload_workload(wl, tensor_cores=not request.param.endswith("simt"))
     comp.score(d["K"], d["V"], d["Qp"], d["bounds"], d["n_slots"], d["sens"])
     torch.cuda.synchronize()
     from kv_cache_compression_probe_gb300 import kvc
