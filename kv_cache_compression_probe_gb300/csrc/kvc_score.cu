@@ -62,6 +62,8 @@ struct ScoreArgs {
   float* seed_w;       // [BLH, P]
   float* lse2_h;       // [BLH, P] base-2 LSE of seed rows
   int32_t* ok;         // [BLH] 1 if the (l,h) passed its checks
+  unsigned char* proto;  // [BLH * S_max] prototype records (tensor-core path)
+  float* npart;        // [BLH * S_max, 2, 15, 4] node statistics (tensor-core path)
   int32_t* err;
   int chunk;           // keys per rowstats chunk
   int n_chunks;
@@ -772,6 +774,203 @@ __global__ void __launch_bounds__(256, 1) nodes_kernel(kvc_params p, ScoreArgs a
   }
 }
 
+// ---------------------------------------------------------------- tensor-core node path
+// Per slot tree: the 15 prototypes (fp32), their keys split into three bf16
+// parts (k^ = p0 + p1 + p2 to fp32 accuracy) laid out as the 128-byte-swizzled
+// K-major operand of the tensor-core node kernel, and each node's relevance.
+template <int D>
+struct ProtoSmem {
+  __nv_bfloat16 K[128][D];
+  __nv_bfloat16 V[128][D];
+  float R[128];
+  float Kh[16][D];
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) proto_kernel(kvc_params p, ScoreArgs a, unsigned char* proto) {
+  static_assert(D == 128, "tensor-core node path is d = 128");
+  constexpr int HALF = D / 2, VP = D / 64;
+  extern __shared__ float4 proto_smem4[];
+  ProtoSmem<D>& psm = *reinterpret_cast<ProtoSmem<D>*>(proto_smem4);
+  auto& sK = psm.K;
+  auto& sV = psm.V;
+  auto& sR = psm.R;
+  auto& sKh = psm.Kh;
+  const long long tree = blockIdx.x;
+  const int s = (int)(tree % p.S_max);
+  const long long blh = tree / p.S_max;
+  const int b = seq_of(p, blh);
+  const int lh = (int)(blh % ((long long)p.L * p.H));
+  if (!a.ok[blh] || s >= a.n_slots[b]) return;
+  const int n = a.ctx_len[b];
+  const int x0 = a.bounds[(long long)b * (p.S_max + 1) + s];
+  const int y0 = a.bounds[(long long)b * (p.S_max + 1) + s + 1];
+  const int len = y0 - x0;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t row0 = kvcd::seq_token_base(a.ctx_len, b, p.L * p.H) + (int64_t)lh * n;
+  const uint4* gk = reinterpret_cast<const uint4*>(static_cast<const T*>(a.K) + (row0 + x0) * D);
+  const uint4* gv = reinterpret_cast<const uint4*>(static_cast<const T*>(a.V) + (row0 + x0) * D);
+  for (int i = tid; i < len * (D / 8); i += blockDim.x) {
+    reinterpret_cast<uint4*>(&sK[0][0])[i] = __ldg(gk + i);
+    reinterpret_cast<uint4*>(&sV[0][0])[i] = __ldg(gv + i);
+  }
+  for (int i = tid; i < len; i += blockDim.x) sR[i] = a.rel[row0 + x0 + i];
+  if (tid < D) sKh[15][tid] = 0.f;
+  __syncthreads();
+  unsigned char* out = proto + tree * kvc::kProtoBytes;
+  float* vh_out = reinterpret_cast<float*>(out + kvc::kProtoVhOff);
+  float* lm_out = reinterpret_cast<float*>(out + kvc::kProtoLogmOff);
+  float* rv_out = reinterpret_cast<float*>(out + kvc::kProtoRvOff);
+  for (int j = warp; j < 15; j += 8) {
+    int x, y;
+    node_range(j, x0, y0, x, y);
+    const int c = y - x;
+    float rs = 0.f;
+    for (int i = x + lane; i < y; i += 32) rs += sR[i - x0];
+    rs = kvcd::warp_sum(rs);
+    float kb_lo[VP], kb_hi[VP], vb_lo[VP], vb_hi[VP];
+#pragma unroll
+    for (int t = 0; t < VP; ++t) kb_lo[t] = kb_hi[t] = vb_lo[t] = vb_hi[t] = 0.f;
+    const float f = p.value_floor;
+    for (int i = x; i < y; ++i) {
+      const __nv_bfloat16* kr = sK[i - x0];
+      const __nv_bfloat16* vr = sV[i - x0];
+      const float* ct = a.cos_tab + (int64_t)(2 * i) * HALF + lane * VP;
+      const float* st = a.sin_tab + (int64_t)(2 * i) * HALF + lane * VP;
+      const float w = rs > 0.f ? (1.f - f) * (sR[i - x0] / rs) + f / (float)c : 1.f / (float)c;
+#pragma unroll
+      for (int t = 0; t < VP; ++t) {
+        const float cs = __ldg(ct + t), sn = __ldg(st + t);
+        const float lo = __bfloat162float(kr[lane * VP + t]), hi = __bfloat162float(kr[HALF + lane * VP + t]);
+        kb_lo[t] += lo * cs + hi * sn;
+        kb_hi[t] += hi * cs - lo * sn;
+        vb_lo[t] = fmaf(w, __bfloat162float(vr[lane * VP + t]), vb_lo[t]);
+        vb_hi[t] = fmaf(w, __bfloat162float(vr[HALF + lane * VP + t]), vb_hi[t]);
+      }
+    }
+    const float inv_c = 1.f / (float)c;
+    float nb2 = 0.f;
+#pragma unroll
+    for (int t = 0; t < VP; ++t) {
+      kb_lo[t] *= inv_c; kb_hi[t] *= inv_c;
+      nb2 += kb_lo[t] * kb_lo[t] + kb_hi[t] * kb_hi[t];
+    }
+    const float nb = sqrtf(kvcd::warp_sum(nb2));
+    float kap = 0.f;
+    for (int i = x; i < y; ++i) {
+      const __nv_bfloat16* kr = sK[i - x0];
+      const float* ct = a.cos_tab + (int64_t)(2 * i) * HALF + lane * VP;
+      const float* st = a.sin_tab + (int64_t)(2 * i) * HALF + lane * VP;
+      float dot = 0.f, nk2 = 0.f;
+#pragma unroll
+      for (int t = 0; t < VP; ++t) {
+        const float cs = __ldg(ct + t), sn = __ldg(st + t);
+        const float lo = __bfloat162float(kr[lane * VP + t]), hi = __bfloat162float(kr[HALF + lane * VP + t]);
+        const float ul = lo * cs + hi * sn, uh = hi * cs - lo * sn;
+        dot += ul * kb_lo[t] + uh * kb_hi[t];
+        nk2 += ul * ul + uh * uh;
+      }
+      dot = kvcd::warp_sum(dot);
+      nk2 = kvcd::warp_sum(nk2);
+      const float den = sqrtf(nk2) * nb;
+      kap += den > 0.f ? dot / den : 0.f;
+    }
+    kap *= inv_c;
+    const float m = (float)c * fminf(fmaxf(kap, inv_c), 1.f);
+    const float* ct = a.cos_tab + (int64_t)(x + y - 1) * HALF + lane * VP;
+    const float* st = a.sin_tab + (int64_t)(x + y - 1) * HALF + lane * VP;
+#pragma unroll
+    for (int t = 0; t < VP; ++t) {
+      const float cs = __ldg(ct + t), sn = __ldg(st + t);
+      sKh[j][lane * VP + t] = kb_lo[t] * cs - kb_hi[t] * sn;
+      sKh[j][HALF + lane * VP + t] = kb_hi[t] * cs + kb_lo[t] * sn;
+      vh_out[j * D + lane * VP + t] = vb_lo[t];
+      vh_out[j * D + HALF + lane * VP + t] = vb_hi[t];
+    }
+    if (lane == 0) { lm_out[j] = logf(m); rv_out[j] = rs; }
+  }
+  __syncthreads();
+  // three-part bf16 split of k^, rows 16p + j, 128-byte swizzle (K-major)
+  for (int idx = tid; idx < 48 * (D / 8); idx += blockDim.x) {
+    const int row = idx / (D / 8), ch = idx % (D / 8);
+    const int part = row >> 4, j = row & 15;
+    uint32_t w4[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      uint32_t h2[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float x = sKh[j][ch * 8 + 2 * e + u];
+        const __nv_bfloat16 p0 = __float2bfloat16_rn(x);
+        const float r1 = x - __bfloat162float(p0);
+        const __nv_bfloat16 p1 = __float2bfloat16_rn(r1);
+        const __nv_bfloat16 p2 = __float2bfloat16_rn(r1 - __bfloat162float(p1));
+        const __nv_bfloat16 v = part == 0 ? p0 : (part == 1 ? p1 : p2);
+        h2[u] = (uint32_t)__bfloat16_as_ushort(v);
+      }
+      w4[e] = h2[0] | (h2[1] << 16);
+    }
+    const int kb = ch >> 3, cc = ch & 7;
+    *reinterpret_cast<uint4*>(out + kb * 6144 + row * 128 + ((cc ^ (row & 7)) << 4)) =
+        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  }
+}
+
+// Per slot: combine the row-tile partial statistics into D, D_drop and the 16
+// op utilities / costs (same formulas as the node kernel's tail).
+__global__ void ops_kernel(kvc_params p, ScoreArgs a, const unsigned char* proto,
+                           const float* npart, int n_mt) {
+  const long long tree = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (tree >= (long long)p.B * p.L * p.H * p.S_max) return;
+  const int s = (int)(tree % p.S_max);
+  const long long blh = tree / p.S_max;
+  const int b = seq_of(p, blh);
+  const int lh = (int)(blh % ((long long)p.L * p.H));
+  float* util_out = a.op_util + tree * kOps;
+  int32_t* cost_out = a.op_cost + tree * kOps;
+  if (!a.ok[blh] || s >= a.n_slots[b]) {
+    for (int o = 0; o < kOps; ++o) { util_out[o] = 0.f; cost_out[o] = 0; }
+    return;
+  }
+  const int x0 = a.bounds[(long long)b * (p.S_max + 1) + s];
+  const int y0 = a.bounds[(long long)b * (p.S_max + 1) + s + 1];
+  const float* rv = reinterpret_cast<const float*>(proto + tree * kvc::kProtoBytes + kvc::kProtoRvOff);
+  const float nu = a.nu[blh];
+  const float invR = 1.f / (float)(p.G * p.P);
+  float Dn[15], Dd[15];
+  for (int j = 0; j < 15; ++j) {
+    float st[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int mt = 0; mt < n_mt; ++mt)
+      for (int k = 0; k < 4; ++k) st[k] += npart[((tree * 2 + mt) * 15 + j) * 4 + k];
+    const float vt = nu > 0.f ? st[2] * invR / nu : 0.f;
+    const float vd = nu > 0.f ? st[3] * invR / nu : 0.f;
+    Dn[j] = p.w_part * (st[0] * invR) + p.w_value * vt;
+    Dd[j] = p.w_part * (st[1] * invR) + p.w_value * vd;
+  }
+  const float sens = a.head_sens ? a.head_sens[lh] : 1.f;
+  auto gainf = [](float num, float dd) {
+    if (!(dd > 0.f)) return 0.f;
+    return fminf(fmaxf(num / dd, 0.f), 1.f);
+  };
+  util_out[0] = rv[0] * gainf(Dd[0] - Dn[0], Dd[0]) * sens;
+  cost_out[0] = 1;
+  for (int j = 0; j < 15; ++j) {
+    float g;
+    int c;
+    if (j < 7) {
+      g = gainf(Dn[j] - Dn[2 * j + 1] - Dn[2 * j + 2], Dd[j]);
+      c = 1;
+    } else {
+      int x, y;
+      node_range(j, x0, y0, x, y);
+      c = y - x - 1;
+      g = gainf(Dn[j], Dd[j]);
+    }
+    util_out[1 + j] = rv[j] * g * sens / (float)c;
+    cost_out[1 + j] = c;
+  }
+}
+
 // Per-(b,l,h) checks of the device-side inputs.
 __global__ void score_check_kernel(kvc_params p, ScoreArgs a) {
   const long long blh = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -802,10 +1001,16 @@ int chunk_for(const kvc_params* p) {
 constexpr int kTcChunkTiles = 16;
 int tc_chunks(const kvc_params* p) { return (p->n_max + kTcChunkTiles * 128 - 1) / (kTcChunkTiles * 128); }
 
-bool use_tc(const kvc_params* p) { return p->total_ctx > 0 && kvc::probe_tc_supported(p); }
+// Shapes the tensor-core passes handle (workspace sizing); at run time the TMA
+// descriptor encoder must also be available.
+bool tc_shape(const kvc_params* p) {
+  return p->total_ctx > 0 && p->dtype == KVC_BF16 && p->d == 128 && p->P % 32 == 0 &&
+         p->G * p->P <= 256 && p->P <= 128;
+}
+bool use_tc(const kvc_params* p) { return tc_shape(p) && kvc::probe_tc_supported(p); }
 
 struct Layout {
-  size_t part, lse2, hrow, nu, seeds, seed_w, lse2_h, ok, total;
+  size_t part, lse2, hrow, nu, seeds, seed_w, lse2_h, ok, proto, npart, total;
 };
 Layout layout(const kvc_params* p) {
   const size_t blh = (size_t)kvc::lh_count(p);
@@ -821,6 +1026,9 @@ Layout layout(const kvc_params* p) {
   l.seed_w = o; o += kvc::align256(blh * p->P * sizeof(float));
   l.lse2_h = o; o += kvc::align256(blh * p->P * sizeof(float));
   l.ok = o; o += kvc::align256(blh * sizeof(int32_t));
+  const size_t trees = tc_shape(p) ? blh * (size_t)p->S_max : 0;
+  l.proto = o; o += kvc::align256(trees * kvc::kProtoBytes);
+  l.npart = o; o += kvc::align256(trees * 2 * 15 * 4 * sizeof(float));
   l.total = o;
   return l;
 }
@@ -842,7 +1050,8 @@ int launch_all(const kvc_params* p, ScoreArgs& a, cudaStream_t s) {
   cudaFuncSetAttribute(nodes_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)sm_nodes);
   score_check_kernel<<<(unsigned)((blh + 255) / 256), 256, 0, s>>>(*p, a); ++launches;
-  if (std::is_same<T, __nv_bfloat16>::value && D == 128 && use_tc(p)) {
+  if constexpr (std::is_same<T, __nv_bfloat16>::value && D == 128) {
+   if (use_tc(p)) {
     // tensor-core probe-times-key passes
     kvc::ProbeTcArgs t;
     t.ctx_len = a.ctx_len; t.K = a.K; t.V = a.V; t.Qp = a.Qp; t.seeds = a.seeds;
@@ -866,10 +1075,23 @@ int launch_all(const kvc_params* p, ScoreArgs& a, cudaStream_t s) {
       if ((st = kvc::probe_tc_pass(kvc::kTcProp, t, rows_total, s)) != KVC_OK) return st;
       launches += 2;
     }
-    nodes_kernel<T, D><<<(unsigned)(blh * p->S_max), 256, sm_nodes, s>>>(*p, a);
-    ++launches;
+    // prototypes, tensor-core node statistics, utilities
+    cudaFuncSetAttribute(proto_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)sizeof(ProtoSmem<D>));
+    proto_kernel<T, D><<<(unsigned)(blh * p->S_max), 256, sizeof(ProtoSmem<D>), s>>>(*p, a, a.proto);
+    kvc::NodeTcArgs nd;
+    nd.ctx_len = a.ctx_len; nd.K = a.K; nd.V = a.V; nd.Qp = a.Qp; nd.lse2 = a.lse2; nd.ok = a.ok;
+    nd.bounds = a.bounds; nd.n_slots = a.n_slots; nd.proto = a.proto; nd.npart = a.npart;
+    nd.err = a.err; nd.B = p->B; nd.L = p->L; nd.H = p->H; nd.G = p->G; nd.P = p->P;
+    nd.S_max = p->S_max; nd.q_scale2 = a.q_scale2;
+    if ((st = kvc::nodes_tc_pass(nd, rows_total, s)) != KVC_OK) return st;
+    const long long trees = blh * p->S_max;
+    ops_kernel<<<(unsigned)((trees + 127) / 128), 128, 0, s>>>(*p, a, a.proto, a.npart,
+                                                               (p->G * p->P + 127) / 128);
+    launches += 2;
     kvc::count_launch(launches);
     return kvc::cuda_status(cudaGetLastError());
+   }
   }
   const dim3 g_rows(a.n_chunks, (unsigned)blh);
   rowstats_kernel<T, D, false><<<g_rows, 256, sm_rows, s>>>(*p, a);
@@ -929,6 +1151,8 @@ extern "C" int kvc_score(const kvc_params* p, const int32_t* ctx_len, const void
   a.seed_w = reinterpret_cast<float*>(w + lay.seed_w);
   a.lse2_h = reinterpret_cast<float*>(w + lay.lse2_h);
   a.ok = reinterpret_cast<int32_t*>(w + lay.ok);
+  a.proto = reinterpret_cast<unsigned char*>(w + lay.proto);
+  a.npart = reinterpret_cast<float*>(w + lay.npart);
   a.err = err;
   a.chunk = chunk_for(p);
   a.n_chunks = (p->n_max + a.chunk - 1) / a.chunk;

@@ -351,6 +351,382 @@ __global__ void __launch_bounds__((4 * NT + 2) * 32, 1)
   }
 }
 
+// ---------------------------------------------------------------- node statistics (a3 + a4)
+// One CTA = one (b,l,h), one 128-row tile of the probe rows, and up to
+// kNodeSlots consecutive slots.  Per slot:
+//   phase A  S = Q K^T (keys placed leaf by leaf on 16-row boundaries) and
+//            A^ = Q [k^0; k^1; k^2]^T (k^ in three bf16 parts, summed in fp32);
+//   epi A    a = 2^(s - LSE) split into three bf16 parts written as the
+//            K-major operand over the 128 leaf-padded key slots; per-row node
+//            masses A_N and A_hat_N to shared memory;
+//   phase B  for each of the 15 nodes: U_N = sum over parts and over the node's
+//            key slots of a_part V (V read as an MN-major operand straight from
+//            TMA) into one of two TMEM buffers;
+//   epi B    two warp groups alternate over the node buffers: per row
+//            |U - A^ v^|, |U|, |A - A^|, A, summed over the group's rows.
+// Per-(slot, tile) sums go to `npart`; a small kernel forms D and utilities.
+constexpr int kNodeSlots = 8;
+
+struct NodeSmem {
+  alignas(1024) unsigned char Q[2][kBlockBytes];
+  alignas(1024) unsigned char Kt[2][kBlockBytes];
+  alignas(1024) unsigned char Vt[2][kBlockBytes];
+  alignas(1024) unsigned char Ap[3][2][kBlockBytes];
+  alignas(1024) unsigned char Kh[kvc::kProtoKhBytes];
+  float An[15][128];
+  float Ah[15][128];
+  float red[8][15][4];
+  uint64_t k_full, k_empty, v_full, v_empty, s_full, a_ready, b_done, g1_done;
+  uint64_t nfull[2], nempty[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+// N = 48 (three 16-row parts of the prototype keys), both operands K-major.
+constexpr uint32_t kIdescN48 = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(48 >> 3) << 17) |
+                               ((uint32_t)(kBM >> 4) << 24);
+// N = 128 with B MN-major (values: features contiguous, key slots strided).
+constexpr uint32_t kIdescVmn = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                               ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16_i(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+// MN-major 128-byte-swizzled operand: 64-feature blocks LBO apart, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr, uint32_t lbo_bytes) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Leaf l of the slot [x0, y0): first token and token count (midpoint rule).
+__device__ __forceinline__ void leaf_range(int l, int x0, int y0, int& start, int& cnt) {
+  int a = x0, b = y0;
+#pragma unroll
+  for (int lvl = 2; lvl >= 0; --lvl) {
+    const int mid = (a + b) >> 1;
+    if ((l >> lvl) & 1) a = mid; else b = mid;
+  }
+  start = a; cnt = b - a;
+}
+
+// Leaves [l0, l1) covered by node j of the depth-3 tree.
+__device__ __forceinline__ void node_leaves(int j, int& l0, int& l1) {
+  const int depth = (j >= 7) ? 3 : (j >= 3) ? 2 : (j >= 1) ? 1 : 0;
+  const int k = j - ((1 << depth) - 1);
+  const int w = 8 >> depth;
+  l0 = k * w; l1 = l0 + w;
+}
+
+__global__ void __launch_bounds__(320, 1)
+    nodes_tc_kernel(const __grid_constant__ CUtensorMap kmap16,
+                    const __grid_constant__ CUtensorMap vmap16, kvc::NodeTcArgs a) {
+  extern __shared__ __align__(1024) unsigned char nd_raw[];
+  NodeSmem& sm = *reinterpret_cast<NodeSmem*>(
+      (reinterpret_cast<uintptr_t>(nd_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long blh = blockIdx.z;
+  const int mt = blockIdx.y;
+  const int LH = a.L * a.H;
+  const int b = (int)(blh / LH);
+  const int lh = (int)(blh % LH);
+  if (!a.ok[blh]) return;
+  const int S = a.n_slots[b];
+  const int s_begin = blockIdx.x * kNodeSlots;
+  const int s_end = min(S, s_begin + kNodeSlots);
+  if (s_begin >= s_end) return;
+  const int nsl = s_end - s_begin;
+  const int n = a.ctx_len[b];
+  const int R = a.G * a.P;
+  const int64_t row0 = kvcd::seq_token_base(a.ctx_len, b, LH) + (int64_t)lh * n;
+  const int32_t* bd = a.bounds + (long long)b * (a.S_max + 1);
+
+  // ---- this tile's query rows -> swizzled K-major smem
+  for (int idx = tid; idx < kBM * 16; idx += 320) {
+    const int r = idx >> 4, c = idx & 15;
+    const int rho = mt * kBM + r;
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (rho < R)
+      val = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.Qp) +
+                                                 (blh * R + rho) * kD) + c);
+    const int kb = c >> 3, cc = c & 7;
+    *reinterpret_cast<uint4*>(&sm.Q[kb][r * 128 + ((cc ^ (r & 7)) << 4)]) = val;
+  }
+  kvcd::fence_proxy_async_smem();
+  if (tid == 0) {
+    kvcd::mbar_init(&sm.k_full, 1); kvcd::mbar_init(&sm.k_empty, 1);
+    kvcd::mbar_init(&sm.v_full, 1); kvcd::mbar_init(&sm.v_empty, 1);
+    kvcd::mbar_init(&sm.s_full, 1); kvcd::mbar_init(&sm.a_ready, 4);
+    kvcd::mbar_init(&sm.b_done, 1); kvcd::mbar_init(&sm.g1_done, 4);
+    for (int i = 0; i < 2; ++i) { kvcd::mbar_init(&sm.nfull[i], 1); kvcd::mbar_init(&sm.nempty[i], 4); }
+    sm.abort = 0;
+    kvcd::fence_mbar_init();
+  }
+  if (warp == 9) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     kvcd::smem_u32(&sm.tmem_base)), "r"(512u)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  volatile int* abort_flag = &sm.abort;
+
+  if (warp == 8) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      for (int k = 0; k < nsl; ++k) {
+        const int s = s_begin + k;
+        const long long tree = blh * a.S_max + s;
+        const int x0 = bd[s], y0 = bd[s + 1];
+        if (k >= 1 && !kvcd::mbar_wait(&sm.k_empty, (uint32_t)((k - 1) & 1))) { *abort_flag = 1; break; }
+        kvcd::mbar_arrive_expect_tx(&sm.k_full, kTileBytes + kvc::kProtoKhBytes);
+        for (int l = 0; l < 8; ++l) {
+          int st, cnt;
+          leaf_range(l, x0, y0, st, cnt);
+          for (int fb = 0; fb < 2; ++fb)
+            tma_load_2d(&sm.Kt[fb][l * 2048], &kmap16, fb * 64, (int)(row0 + st), &sm.k_full);
+        }
+        kvcd::bulk_g2s(sm.Kh, a.proto + tree * kvc::kProtoBytes, kvc::kProtoKhBytes, &sm.k_full);
+        if (k >= 1 && !kvcd::mbar_wait(&sm.v_empty, (uint32_t)((k - 1) & 1))) { *abort_flag = 1; break; }
+        kvcd::mbar_arrive_expect_tx(&sm.v_full, kTileBytes);
+        for (int l = 0; l < 8; ++l) {
+          int st, cnt;
+          leaf_range(l, x0, y0, st, cnt);
+          for (int fb = 0; fb < 2; ++fb)
+            tma_load_2d(&sm.Vt[fb][l * 2048], &vmap16, fb * 64, (int)(row0 + st), &sm.v_full);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      for (int k = 0; k < nsl; ++k) {
+        if (!kvcd::mbar_wait(&sm.k_full, (uint32_t)(k & 1))) { *abort_flag = 1; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint64_t aq = sw128_desc(kvcd::smem_u32(sm.Q[kk >> 2]) + (kk & 3) * 32);
+          mma_bf16_i(tmem, aq, sw128_desc(kvcd::smem_u32(sm.Kt[kk >> 2]) + (kk & 3) * 32), kIdesc,
+                     kk > 0 ? 1u : 0u);
+          mma_bf16_i(tmem + 128, aq,
+                     sw128_desc(kvcd::smem_u32(sm.Kh) + (kk >> 2) * 6144 + (kk & 3) * 32),
+                     kIdescN48, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&sm.s_full);
+        mma_commit(&sm.k_empty);
+        if (!kvcd::mbar_wait(&sm.a_ready, (uint32_t)(k & 1)) ||
+            !kvcd::mbar_wait(&sm.v_full, (uint32_t)(k & 1))) { *abort_flag = 1; break; }
+        tc_fence_after();
+        bool ok = true;
+        for (int j = 0; j < 15; ++j) {
+          const int nn = k * 15 + j, bf = nn & 1;
+          if (nn >= 2 && !kvcd::mbar_wait(&sm.nempty[bf], (uint32_t)(((nn >> 1) - 1) & 1))) { ok = false; break; }
+          tc_fence_after();
+          int l0, l1;
+          node_leaves(j, l0, l1);
+          const uint32_t d = tmem + 256 + bf * 128;
+          uint32_t acc = 0;
+          for (int part = 0; part < 3; ++part)
+            for (int ks = l0; ks < l1; ++ks) {
+              const uint64_t aa = sw128_desc(kvcd::smem_u32(sm.Ap[part][ks >> 2]) + (ks & 3) * 32);
+              const uint64_t bb = sw128_mn_desc(kvcd::smem_u32(sm.Vt[0]) + ks * 2048, kBlockBytes);
+              mma_bf16_i(d, aa, bb, kIdescVmn, acc);
+              acc = 1;
+            }
+          mma_commit(&sm.nfull[bf]);
+        }
+        if (!ok) { *abort_flag = 1; break; }
+        mma_commit(&sm.b_done);
+        mma_commit(&sm.v_empty);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue groups
+    const int g = warp >> 2, q = warp & 3;
+    const int rl = q * 32 + lane;                      // row within the tile (TMEM lane)
+    const int rho = mt * kBM + rl;
+    const bool rv = rho < R;
+    const float l2 = rv ? a.lse2[blh * R + rho] : 0.f;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const int bar_id = 1 + g;
+    for (int k = 0; k < nsl; ++k) {
+      const int s = s_begin + k;
+      const long long tree = blh * a.S_max + s;
+      const int x0 = bd[s], y0 = bd[s + 1];
+      const float* proto_f = reinterpret_cast<const float*>(a.proto + tree * kvc::kProtoBytes);
+      if (g == 0) {
+        // ---- epilogue A: attention of this row to the slot keys and nodes
+        if (!*abort_flag && !kvcd::mbar_wait(&sm.s_full, (uint32_t)(k & 1))) *abort_flag = 1;
+        tc_fence_after();
+        float ah[15];
+        {
+          float d0[16], d1[16], d2[16];
+          tmem_ld16(tmem + lane_off + 128, d0);
+          tmem_ld16(tmem + lane_off + 144, d1);
+          tmem_ld16(tmem + lane_off + 160, d2);
+          const float* lmv = proto_f + kvc::kProtoLogmOff / 4;
+#pragma unroll
+          for (int j = 0; j < 15; ++j) {
+            const float sc = (d0[j] + d1[j] + d2[j]) * a.q_scale2 +
+                             __ldg(lmv + j) * 1.4426950408889634f - l2;
+            ah[j] = rv ? exp2f(sc) : 0.f;
+          }
+        }
+        int cnt[8];
+#pragma unroll
+        for (int l = 0; l < 8; ++l) { int st; leaf_range(l, x0, y0, st, cnt[l]); }
+        if (k >= 1 && !*abort_flag && !kvcd::mbar_wait(&sm.b_done, (uint32_t)((k - 1) & 1)))
+          *abort_flag = 1;
+        float lsum[8];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tmem_ld32(tmem + lane_off + (uint32_t)(c * 32), v);
+          float s0 = 0.f, s1 = 0.f;
+          uint32_t pk[3][16];
+#pragma unroll
+          for (int t = 0; t < 32; t += 2) {
+            float av[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int kap = c * 32 + t + u;
+              const bool valid = rv && ((kap & 15) < cnt[kap >> 4]);
+              av[u] = valid ? exp2f(v[t + u] * a.q_scale2 - l2) : 0.f;
+            }
+            if (t < 16) s0 += av[0] + av[1]; else s1 += av[0] + av[1];
+            uint32_t h[3][2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const __nv_bfloat16 p0 = __float2bfloat16_rn(av[u]);
+              const float r1 = av[u] - __bfloat162float(p0);
+              const __nv_bfloat16 p1 = __float2bfloat16_rn(r1);
+              const __nv_bfloat16 p2 = __float2bfloat16_rn(r1 - __bfloat162float(p1));
+              h[0][u] = __bfloat16_as_ushort(p0);
+              h[1][u] = __bfloat16_as_ushort(p1);
+              h[2][u] = __bfloat16_as_ushort(p2);
+            }
+#pragma unroll
+            for (int pt = 0; pt < 3; ++pt) pk[pt][t >> 1] = h[pt][0] | (h[pt][1] << 16);
+          }
+          lsum[2 * c] = s0;
+          lsum[2 * c + 1] = s1;
+          // 32 key slots = four 16-byte chunks per part
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            const int kap = c * 32 + ch * 8;
+            const int kb = kap >> 6, cidx = (kap & 63) >> 3;
+            const int off = rl * 128 + ((cidx ^ (rl & 7)) << 4);
+#pragma unroll
+            for (int pt = 0; pt < 3; ++pt)
+              *reinterpret_cast<uint4*>(&sm.Ap[pt][kb][off]) =
+                  make_uint4(pk[pt][ch * 4], pk[pt][ch * 4 + 1], pk[pt][ch * 4 + 2], pk[pt][ch * 4 + 3]);
+          }
+        }
+        // node masses: leaves, then their parents
+        float An[15];
+#pragma unroll
+        for (int l = 0; l < 8; ++l) An[7 + l] = lsum[l];
+#pragma unroll
+        for (int j = 6; j >= 0; --j) An[j] = An[2 * j + 1] + An[2 * j + 2];
+        if (k >= 1 && !*abort_flag && !kvcd::mbar_wait(&sm.g1_done, (uint32_t)((k - 1) & 1)))
+          *abort_flag = 1;
+#pragma unroll
+        for (int j = 0; j < 15; ++j) { sm.An[j][rl] = An[j]; sm.Ah[j][rl] = ah[j]; }
+        kvcd::fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) kvcd::mbar_arrive(&sm.a_ready);
+      } else {
+        if (!*abort_flag && !kvcd::mbar_wait(&sm.a_ready, (uint32_t)(k & 1))) *abort_flag = 1;
+      }
+      // ---- epilogue B: this group's node tiles
+      for (int j = 0; j < 15; ++j) {
+        const int nn = k * 15 + j, bf = nn & 1;
+        if (bf != g) continue;
+        if (!*abort_flag && !kvcd::mbar_wait(&sm.nfull[bf], (uint32_t)((nn >> 1) & 1))) *abort_flag = 1;
+        tc_fence_after();
+        const float Ahj = sm.Ah[j][rl], Anj = sm.An[j][rl];
+        const float4* vh = reinterpret_cast<const float4*>(proto_f + kvc::kProtoVhOff / 4 + j * kD);
+        float dd = 0.f, uu = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tmem_ld32(tmem + lane_off + 256 + bf * 128 + (uint32_t)(c * 32), v);
+#pragma unroll
+          for (int t4 = 0; t4 < 8; ++t4) {
+            const float4 w = __ldg(vh + c * 8 + t4);
+            const float wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float u = v[t4 * 4 + e];
+              const float df = u - Ahj * wv[e];
+              dd = fmaf(df, df, dd);
+              uu = fmaf(u, u, uu);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) kvcd::mbar_arrive(&sm.nempty[bf]);
+        float st[4];
+        st[0] = rv ? fabsf(Anj - Ahj) : 0.f;
+        st[1] = rv ? Anj : 0.f;
+        st[2] = rv ? sqrtf(dd) : 0.f;
+        st[3] = rv ? sqrtf(uu) : 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float t = kvcd::warp_sum(st[e]);
+          if (lane == 0) sm.red[warp][j][e] = t;
+        }
+      }
+      named_bar(bar_id, 128);
+      // sums over the group's four warps for the nodes it handled
+      {
+        const int et = tid - g * 128;                  // 0..127 within the group
+        if (et < 60) {
+          const int j = et >> 2, e = et & 3;
+          if (((k * 15 + j) & 1) == g) {
+            float t = 0.f;
+            for (int w = 0; w < 4; ++w) t += sm.red[g * 4 + w][j][e];
+            a.npart[((tree * 2 + mt) * 15 + j) * 4 + e] = t;
+          }
+        }
+      }
+      named_bar(bar_id, 128);
+      if (g == 1 && lane == 0) kvcd::mbar_arrive(&sm.g1_done);
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag && tid == 0) kvcd::record_error(a.err, KVC_ETIMEOUT);
+  tc_fence_after();
+  if (warp == 9) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512u)
+                 : "memory");
+  }
+}
+
 // ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -412,5 +788,38 @@ int probe_tc_pass(int mode, const ProbeTcArgs& a, int64_t total_rows, cudaStream
       return launch<1, kTcProp>(map, a, s);
   }
 }
+
+}  // namespace kvc
+
+namespace kvc {
+
+int nodes_tc_pass(const NodeTcArgs& a, int64_t total_rows, cudaStream_t s) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return KVC_ECUDA;
+  CUtensorMap km, vm;
+  cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)total_rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  cuuint32_t box[2] = {64, 16};
+  cuuint32_t estr[2] = {1, 1};
+  if (enc(&km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.K), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return KVC_ECUDA;
+  if (enc(&vm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.V), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return KVC_ECUDA;
+  const size_t smem = sizeof(NodeSmem) + 1024;
+  if (cudaFuncSetAttribute(nodes_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return KVC_ECUDA;
+  const int n_mt = (a.G * a.P + kBM - 1) / kBM;
+  dim3 grid((a.S_max + kNodeSlots - 1) / kNodeSlots, n_mt, (unsigned)((long long)a.B * a.L * a.H));
+  nodes_tc_kernel<<<grid, 320, smem, s>>>(km, vm, a);
+  kvc::count_launch();
+  return kvc::cuda_status(cudaGetLastError());
+}
+
+size_t nodes_tc_smem_bytes() { return sizeof(NodeSmem) + 1024; }
 
 }  // namespace kvc

@@ -9,6 +9,16 @@ namespace kvc {
 
 enum { kTcRowstatsProbes = 0, kTcRowstatsSeeds = 1, kTcFeats = 2, kTcProp = 3 };
 
+// Per-slot prototype record written by the prototype kernel and read by the
+// tensor-core node kernel: k^ split into three bf16 parts (rows 16*part + node,
+// 128-byte-swizzled K-major, two 64-feature blocks of 48 rows), v^ (fp32),
+// ln m and the node relevance sums.
+constexpr int kProtoKhBytes = 2 * 48 * 128;        // 12288
+constexpr int kProtoVhOff = kProtoKhBytes;          // float[15][128]
+constexpr int kProtoLogmOff = kProtoVhOff + 15 * 128 * 4;
+constexpr int kProtoRvOff = kProtoLogmOff + 16 * 4;
+constexpr int kProtoBytes = 20480;
+
 struct ProbeTcArgs {
   const int32_t* ctx_len;
   const void* K;
@@ -31,7 +41,25 @@ struct ProbeTcArgs {
   float hop_weight;
 };
 
+struct NodeTcArgs {
+  const int32_t* ctx_len;
+  const void* K;
+  const void* V;
+  const void* Qp;
+  const float* lse2;      // [BLH, R]
+  const int32_t* ok;
+  const int32_t* bounds;  // [B, S_max + 1]
+  const int32_t* n_slots;
+  const unsigned char* proto;   // [BLH * S_max] records of kProtoBytes
+  float* npart;           // [BLH * S_max, 2 tiles, 15 nodes, 4 sums]
+  int32_t* err;
+  int B, L, H, G, P, S_max;
+  float q_scale2;
+};
+
 bool probe_tc_supported(const kvc_params* p);
+int nodes_tc_pass(const NodeTcArgs& a, int64_t total_rows, cudaStream_t s);
+size_t nodes_tc_smem_bytes();
 int probe_tc_pass(int mode, const ProbeTcArgs& a, int64_t total_rows, cudaStream_t s);
 
 }  // namespace kvc
