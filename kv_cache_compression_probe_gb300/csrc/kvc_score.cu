@@ -64,6 +64,7 @@ struct ScoreArgs {
   int32_t* ok;         // [BLH] 1 if the (l,h) passed its checks
   unsigned char* proto;  // [BLH * S_max] prototype records (tensor-core path)
   float* npart;        // [BLH * S_max, 2, 15, 4] node statistics (tensor-core path)
+  float* nu_part;      // [BLH, vnorm chunks] block sums of |v| (tensor-core path)
   int32_t* err;
   int chunk;           // keys per rowstats chunk
   int n_chunks;
@@ -328,42 +329,54 @@ __global__ void numean_kernel(kvc_params p, ScoreArgs a) {
   }
 }
 
-// |v_i| and pos_i features plus the mean |v| of one (b,l,h) (tensor-core path,
-// where the feature epilogue does not touch the values).
+// |v_i| and pos_i features (tensor-core path, where the feature epilogue does
+// not touch the values): one thread per token row; per-block sums of |v| go to
+// nu_part[blh][chunk] (summed in a fixed order by the utility kernel).
+constexpr int kVnormRows = 256;
 template <typename T, int D>
-__global__ void vnorm_kernel(kvc_params p, ScoreArgs a) {
-  const long long blh = blockIdx.x;
+__global__ void __launch_bounds__(kVnormRows) vnorm_kernel(kvc_params p, ScoreArgs a) {
+  const long long blh = blockIdx.y;
   if (!a.ok[blh]) return;
   const int b = seq_of(p, blh);
   const int lh = (int)(blh % ((long long)p.L * p.H));
   const int n = a.ctx_len[b];
+  const int i = blockIdx.x * kVnormRows + threadIdx.x;
   const int64_t row0 = kvcd::seq_token_base(a.ctx_len, b, p.L * p.H) + (int64_t)lh * n;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  constexpr int VPL = D / 32;
-  float acc = 0.f;
-  for (int i = warp; i < n; i += nw) {
-    float v[VPL];
-    kvcd::VecLoad<T, VPL>::ld(static_cast<const T*>(a.V) + (row0 + i) * D + lane * VPL, v);
+  float nv = 0.f;
+  if (i < n) {
+    const T* vr = static_cast<const T*>(a.V) + (row0 + i) * D;
     float s2 = 0.f;
+#pragma unroll 8
+    for (int c = 0; c < D; c += 4) {
+      float v[4];
+      kvcd::VecLoad<T, 4>::ld(vr + c, v);
 #pragma unroll
-    for (int t = 0; t < VPL; ++t) s2 = fmaf(v[t], v[t], s2);
-    s2 = kvcd::warp_sum(s2);
-    const float nv = sqrtf(s2);
-    if (lane == 0) {
-      float* f = a.feats + (row0 + i) * 5;
-      f[1] = nv;
-      f[4] = (float)i / (float)max(n - 1, 1);
-      acc += nv;
+      for (int t = 0; t < 4; ++t) s2 = fmaf(v[t], v[t], s2);
     }
+    nv = sqrtf(s2);
+    float* f = a.feats + (row0 + i) * 5;
+    f[1] = nv;
+    f[4] = (float)i / (float)max(n - 1, 1);
   }
-  __shared__ float red[32];
-  if (lane == 0) red[warp] = acc;
+  __shared__ float red[kVnormRows / 32];
+  const float ws = kvcd::warp_sum(nv);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ws;
   __syncthreads();
   if (threadIdx.x == 0) {
     float t = 0.f;
-    for (int w = 0; w < nw; ++w) t += red[w];
-    a.nu[blh] = t / (float)n;
+    for (int w = 0; w < kVnormRows / 32; ++w) t += red[w];
+    a.nu_part[blh * gridDim.x + blockIdx.x] = t;
   }
+}
+
+// mean |v| of each (b,l,h) from the vnorm block sums (fixed order)
+__global__ void nu_finish_kernel(kvc_params p, ScoreArgs a, int chunks) {
+  const long long blh = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (blh >= (long long)p.B * p.L * p.H || !a.ok[blh]) return;
+  const int n = a.ctx_len[seq_of(p, blh)];
+  float t = 0.f;
+  for (int c = 0; c < chunks; ++c) t += a.nu_part[blh * chunks + c];
+  a.nu[blh] = t / (float)n;
 }
 
 // ---------------------------------------------------------------- hops (a2)
@@ -780,22 +793,26 @@ __global__ void __launch_bounds__(256, 1) nodes_kernel(kvc_params p, ScoreArgs a
 // K-major operand of the tensor-core node kernel, and each node's relevance.
 template <int D>
 struct ProtoSmem {
-  __nv_bfloat16 K[128][D];
-  __nv_bfloat16 V[128][D];
-  float R[128];
-  float Kh[16][D];
+  float Kt[128][D + 1];     // unrotated keys (padded rows: conflict-free column reads)
+  float Sk[15][D];          // per node: sum of unrotated keys
+  float Sv[15][D];          // per node: sum of values
+  float Srv[15][D];         // per node: sum of relevance * value
+  float kn[128];            // |unrotated key| per token
+  float cosv[4][128];       // cos(unrotated key, its depth-d node mean)
+  float r[128];
+  float Rn[15], kbn[15];
+  int nx[15], ny[15];
 };
 
+// Per slot tree: the 15 prototypes.  Unrotated keys, values and relevance-
+// weighted values are summed per leaf and then up the tree (every node's mean
+// is a sum over its leaves), so each token is touched once per quantity.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) proto_kernel(kvc_params p, ScoreArgs a, unsigned char* proto) {
   static_assert(D == 128, "tensor-core node path is d = 128");
-  constexpr int HALF = D / 2, VP = D / 64;
+  constexpr int HALF = D / 2;
   extern __shared__ float4 proto_smem4[];
-  ProtoSmem<D>& psm = *reinterpret_cast<ProtoSmem<D>*>(proto_smem4);
-  auto& sK = psm.K;
-  auto& sV = psm.V;
-  auto& sR = psm.R;
-  auto& sKh = psm.Kh;
+  ProtoSmem<D>& ps = *reinterpret_cast<ProtoSmem<D>*>(proto_smem4);
   const long long tree = blockIdx.x;
   const int s = (int)(tree % p.S_max);
   const long long blh = tree / p.S_max;
@@ -808,87 +825,117 @@ __global__ void __launch_bounds__(256) proto_kernel(kvc_params p, ScoreArgs a, u
   const int len = y0 - x0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row0 = kvcd::seq_token_base(a.ctx_len, b, p.L * p.H) + (int64_t)lh * n;
-  const uint4* gk = reinterpret_cast<const uint4*>(static_cast<const T*>(a.K) + (row0 + x0) * D);
-  const uint4* gv = reinterpret_cast<const uint4*>(static_cast<const T*>(a.V) + (row0 + x0) * D);
-  for (int i = tid; i < len * (D / 8); i += blockDim.x) {
-    reinterpret_cast<uint4*>(&sK[0][0])[i] = __ldg(gk + i);
-    reinterpret_cast<uint4*>(&sV[0][0])[i] = __ldg(gv + i);
+  const T* Kg = static_cast<const T*>(a.K) + (row0 + x0) * D;
+  const T* Vg = static_cast<const T*>(a.V) + (row0 + x0) * D;
+  if (tid < 15) { int x, y; node_range(tid, x0, y0, x, y); ps.nx[tid] = x; ps.ny[tid] = y; }
+  for (int i = tid; i < len; i += 256) ps.r[i] = a.rel[row0 + x0 + i];
+  // unrotate every key once: pair (j, j + D/2) at position x0 + i
+  for (int idx = tid; idx < len * HALF; idx += 256) {
+    const int i = idx / HALF, j = idx % HALF;
+    const float lo = kvcd::to_f(Kg[(int64_t)i * D + j]), hi = kvcd::to_f(Kg[(int64_t)i * D + HALF + j]);
+    const float cs = __ldg(a.cos_tab + (int64_t)(2 * (x0 + i)) * HALF + j);
+    const float sn = __ldg(a.sin_tab + (int64_t)(2 * (x0 + i)) * HALF + j);
+    ps.Kt[i][j] = lo * cs + hi * sn;
+    ps.Kt[i][HALF + j] = hi * cs - lo * sn;
   }
-  for (int i = tid; i < len; i += blockDim.x) sR[i] = a.rel[row0 + x0 + i];
-  if (tid < D) sKh[15][tid] = 0.f;
+  __syncthreads();
+  // leaf sums (nodes 7..14), one thread per (leaf, feature) x 4
+  for (int idx = tid; idx < 8 * D; idx += 256) {
+    const int l = idx / D, f = idx % D, j = 7 + l;
+    float sk = 0.f, sv = 0.f, srv = 0.f;
+    for (int i = ps.nx[j] - x0; i < ps.ny[j] - x0; ++i) {
+      const float v = kvcd::to_f(Vg[(int64_t)i * D + f]);
+      sk += ps.Kt[i][f];
+      sv += v;
+      srv = fmaf(ps.r[i], v, srv);
+    }
+    ps.Sk[j][f] = sk; ps.Sv[j][f] = sv; ps.Srv[j][f] = srv;
+  }
+  // token key norms
+  for (int i = warp; i < len; i += 8) {
+    float q2 = 0.f;
+    for (int f = lane; f < D; f += 32) q2 = fmaf(ps.Kt[i][f], ps.Kt[i][f], q2);
+    q2 = kvcd::warp_sum(q2);
+    if (lane == 0) ps.kn[i] = sqrtf(q2);
+  }
+  __syncthreads();
+  for (int lvl = 2; lvl >= 0; --lvl) {                  // parents from children
+    const int first = (1 << lvl) - 1, cnt = 1 << lvl;
+    for (int idx = tid; idx < cnt * D; idx += 256) {
+      const int j = first + idx / D, f = idx % D;
+      ps.Sk[j][f] = ps.Sk[2 * j + 1][f] + ps.Sk[2 * j + 2][f];
+      ps.Sv[j][f] = ps.Sv[2 * j + 1][f] + ps.Sv[2 * j + 2][f];
+      ps.Srv[j][f] = ps.Srv[2 * j + 1][f] + ps.Srv[2 * j + 2][f];
+    }
+    __syncthreads();
+  }
+  // node relevance and |mean unrotated key|
+  for (int j = warp; j < 15; j += 8) {
+    float rs = 0.f;
+    for (int i = ps.nx[j] - x0 + lane; i < ps.ny[j] - x0; i += 32) rs += ps.r[i];
+    rs = kvcd::warp_sum(rs);
+    const float inv_c = 1.f / (float)(ps.ny[j] - ps.nx[j]);
+    float q2 = 0.f;
+    for (int f = lane; f < D; f += 32) { const float m = ps.Sk[j][f] * inv_c; q2 = fmaf(m, m, q2); }
+    q2 = kvcd::warp_sum(q2);
+    if (lane == 0) { ps.Rn[j] = rs; ps.kbn[j] = sqrtf(q2); }
+  }
+  __syncthreads();
+  // cos(unrotated key, mean of its node) for the node on each of the 4 levels
+  for (int t = warp; t < len * 4; t += 8) {
+    const int i = t >> 2, lvl = t & 3;
+    const int xi = x0 + i;
+    int j = 0;
+    for (int d = 0; d < lvl; ++d) { const int c1 = 2 * j + 1; j = xi < ps.ny[c1] ? c1 : c1 + 1; }
+    const float inv_c = 1.f / (float)(ps.ny[j] - ps.nx[j]);
+    float dot = 0.f;
+    for (int f = lane; f < D; f += 32) dot = fmaf(ps.Kt[i][f], ps.Sk[j][f] * inv_c, dot);
+    dot = kvcd::warp_sum(dot);
+    if (lane == 0) {
+      const float den = ps.kn[i] * ps.kbn[j];
+      ps.cosv[lvl][i] = den > 0.f ? dot / den : 0.f;
+    }
+  }
   __syncthreads();
   unsigned char* out = proto + tree * kvc::kProtoBytes;
   float* vh_out = reinterpret_cast<float*>(out + kvc::kProtoVhOff);
   float* lm_out = reinterpret_cast<float*>(out + kvc::kProtoLogmOff);
   float* rv_out = reinterpret_cast<float*>(out + kvc::kProtoRvOff);
-  for (int j = warp; j < 15; j += 8) {
-    int x, y;
-    node_range(j, x0, y0, x, y);
-    const int c = y - x;
-    float rs = 0.f;
-    for (int i = x + lane; i < y; i += 32) rs += sR[i - x0];
-    rs = kvcd::warp_sum(rs);
-    float kb_lo[VP], kb_hi[VP], vb_lo[VP], vb_hi[VP];
-#pragma unroll
-    for (int t = 0; t < VP; ++t) kb_lo[t] = kb_hi[t] = vb_lo[t] = vb_hi[t] = 0.f;
-    const float f = p.value_floor;
-    for (int i = x; i < y; ++i) {
-      const __nv_bfloat16* kr = sK[i - x0];
-      const __nv_bfloat16* vr = sV[i - x0];
-      const float* ct = a.cos_tab + (int64_t)(2 * i) * HALF + lane * VP;
-      const float* st = a.sin_tab + (int64_t)(2 * i) * HALF + lane * VP;
-      const float w = rs > 0.f ? (1.f - f) * (sR[i - x0] / rs) + f / (float)c : 1.f / (float)c;
-#pragma unroll
-      for (int t = 0; t < VP; ++t) {
-        const float cs = __ldg(ct + t), sn = __ldg(st + t);
-        const float lo = __bfloat162float(kr[lane * VP + t]), hi = __bfloat162float(kr[HALF + lane * VP + t]);
-        kb_lo[t] += lo * cs + hi * sn;
-        kb_hi[t] += hi * cs - lo * sn;
-        vb_lo[t] = fmaf(w, __bfloat162float(vr[lane * VP + t]), vb_lo[t]);
-        vb_hi[t] = fmaf(w, __bfloat162float(vr[HALF + lane * VP + t]), vb_hi[t]);
-      }
-    }
-    const float inv_c = 1.f / (float)c;
-    float nb2 = 0.f;
-#pragma unroll
-    for (int t = 0; t < VP; ++t) {
-      kb_lo[t] *= inv_c; kb_hi[t] *= inv_c;
-      nb2 += kb_lo[t] * kb_lo[t] + kb_hi[t] * kb_hi[t];
-    }
-    const float nb = sqrtf(kvcd::warp_sum(nb2));
+  __shared__ float s_logm[15];
+  if (tid < 15) {
+    const int j = tid;
+    const int lvl = (j >= 7) ? 3 : (j >= 3) ? 2 : (j >= 1) ? 1 : 0;
+    const int c = ps.ny[j] - ps.nx[j];
     float kap = 0.f;
-    for (int i = x; i < y; ++i) {
-      const __nv_bfloat16* kr = sK[i - x0];
-      const float* ct = a.cos_tab + (int64_t)(2 * i) * HALF + lane * VP;
-      const float* st = a.sin_tab + (int64_t)(2 * i) * HALF + lane * VP;
-      float dot = 0.f, nk2 = 0.f;
-#pragma unroll
-      for (int t = 0; t < VP; ++t) {
-        const float cs = __ldg(ct + t), sn = __ldg(st + t);
-        const float lo = __bfloat162float(kr[lane * VP + t]), hi = __bfloat162float(kr[HALF + lane * VP + t]);
-        const float ul = lo * cs + hi * sn, uh = hi * cs - lo * sn;
-        dot += ul * kb_lo[t] + uh * kb_hi[t];
-        nk2 += ul * ul + uh * uh;
-      }
-      dot = kvcd::warp_sum(dot);
-      nk2 = kvcd::warp_sum(nk2);
-      const float den = sqrtf(nk2) * nb;
-      kap += den > 0.f ? dot / den : 0.f;
-    }
-    kap *= inv_c;
-    const float m = (float)c * fminf(fmaxf(kap, inv_c), 1.f);
-    const float* ct = a.cos_tab + (int64_t)(x + y - 1) * HALF + lane * VP;
-    const float* st = a.sin_tab + (int64_t)(x + y - 1) * HALF + lane * VP;
-#pragma unroll
-    for (int t = 0; t < VP; ++t) {
-      const float cs = __ldg(ct + t), sn = __ldg(st + t);
-      sKh[j][lane * VP + t] = kb_lo[t] * cs - kb_hi[t] * sn;
-      sKh[j][HALF + lane * VP + t] = kb_hi[t] * cs + kb_lo[t] * sn;
-      vh_out[j * D + lane * VP + t] = vb_lo[t];
-      vh_out[j * D + HALF + lane * VP + t] = vb_hi[t];
-    }
-    if (lane == 0) { lm_out[j] = logf(m); rv_out[j] = rs; }
+    for (int i = ps.nx[j] - x0; i < ps.ny[j] - x0; ++i) kap += ps.cosv[lvl][i];
+    kap /= (float)c;
+    const float m = (float)c * fminf(fmaxf(kap, 1.f / (float)c), 1.f);
+    s_logm[j] = logf(m);
+    lm_out[j] = logf(m);
+    rv_out[j] = ps.Rn[j];
   }
+  // k^ = R(pbar) mean, v^ = (1-f) sum(r v)/sum r + f mean(v)
+  float (*Kh)[D] = reinterpret_cast<float (*)[D]>(&ps.Kt[0][0]);   // reuse: 16 rows
+  __syncthreads();
+  const float fl = p.value_floor;
+  for (int idx = tid; idx < 15 * HALF; idx += 256) {
+    const int j = idx / HALF, t = idx % HALF;
+    const float inv_c = 1.f / (float)(ps.ny[j] - ps.nx[j]);
+    const float lo = ps.Sk[j][t] * inv_c, hi = ps.Sk[j][HALF + t] * inv_c;
+    const int e = ps.nx[j] + ps.ny[j] - 1;                 // half-position row of pbar
+    const float cs = __ldg(a.cos_tab + (int64_t)e * HALF + t);
+    const float sn = __ldg(a.sin_tab + (int64_t)e * HALF + t);
+    Kh[j][t] = lo * cs - hi * sn;
+    Kh[j][HALF + t] = hi * cs + lo * sn;
+    const float rs = ps.Rn[j];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int f = t + u * HALF;
+      vh_out[j * D + f] = rs > 0.f ? (1.f - fl) * (ps.Srv[j][f] / rs) + fl * ps.Sv[j][f] * inv_c
+                                   : ps.Sv[j][f] * inv_c;
+    }
+  }
+  if (tid < D) Kh[15][tid] = 0.f;
   __syncthreads();
   // three-part bf16 split of k^, rows 16p + j, 128-byte swizzle (K-major)
   for (int idx = tid; idx < 48 * (D / 8); idx += blockDim.x) {
@@ -900,7 +947,7 @@ __global__ void __launch_bounds__(256) proto_kernel(kvc_params p, ScoreArgs a, u
       uint32_t h2[2];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const float x = sKh[j][ch * 8 + 2 * e + u];
+        const float x = Kh[j][ch * 8 + 2 * e + u];
         const __nv_bfloat16 p0 = __float2bfloat16_rn(x);
         const float r1 = x - __bfloat162float(p0);
         const __nv_bfloat16 p1 = __float2bfloat16_rn(r1);
@@ -914,6 +961,7 @@ __global__ void __launch_bounds__(256) proto_kernel(kvc_params p, ScoreArgs a, u
     *reinterpret_cast<uint4*>(out + kb * 6144 + row * 128 + ((cc ^ (row & 7)) << 4)) =
         make_uint4(w4[0], w4[1], w4[2], w4[3]);
   }
+  (void)s_logm;
 }
 
 // Per slot: combine the row-tile partial statistics into D, D_drop and the 16
@@ -1010,7 +1058,7 @@ bool tc_shape(const kvc_params* p) {
 bool use_tc(const kvc_params* p) { return tc_shape(p) && kvc::probe_tc_supported(p); }
 
 struct Layout {
-  size_t part, lse2, hrow, nu, seeds, seed_w, lse2_h, ok, proto, npart, total;
+  size_t part, lse2, hrow, nu, seeds, seed_w, lse2_h, ok, proto, npart, nu_part, total;
 };
 Layout layout(const kvc_params* p) {
   const size_t blh = (size_t)kvc::lh_count(p);
@@ -1029,6 +1077,7 @@ Layout layout(const kvc_params* p) {
   const size_t trees = tc_shape(p) ? blh * (size_t)p->S_max : 0;
   l.proto = o; o += kvc::align256(trees * kvc::kProtoBytes);
   l.npart = o; o += kvc::align256(trees * 2 * 15 * 4 * sizeof(float));
+  l.nu_part = o; o += kvc::align256(blh * (size_t)((p->n_max + 255) / 256) * sizeof(float));
   l.total = o;
   return l;
 }
@@ -1066,8 +1115,10 @@ int launch_all(const kvc_params* p, ScoreArgs& a, cudaStream_t s) {
     if ((st = kvc::probe_tc_pass(kvc::kTcRowstatsProbes, t, rows_total, s)) != KVC_OK) return st;
     rowcombine_kernel<false><<<(unsigned)blh, 256, 0, s>>>(*p, a);
     if ((st = kvc::probe_tc_pass(kvc::kTcFeats, t, rows_total, s)) != KVC_OK) return st;
-    vnorm_kernel<T, D><<<(unsigned)blh, 256, 0, s>>>(*p, a);
-    launches += 2;
+    const int vchunks = (p->n_max + kVnormRows - 1) / kVnormRows;
+    vnorm_kernel<T, D><<<dim3(vchunks, (unsigned)blh), kVnormRows, 0, s>>>(*p, a);
+    nu_finish_kernel<<<(unsigned)((blh + 127) / 128), 128, 0, s>>>(*p, a, vchunks);
+    launches += 3;
     for (int hop = 0; hop < p->n_hops; ++hop) {
       seeds_kernel<<<(unsigned)blh, 1024, 0, s>>>(*p, a);
       if ((st = kvc::probe_tc_pass(kvc::kTcRowstatsSeeds, t, rows_total, s)) != KVC_OK) return st;
@@ -1153,6 +1204,7 @@ extern "C" int kvc_score(const kvc_params* p, const int32_t* ctx_len, const void
   a.ok = reinterpret_cast<int32_t*>(w + lay.ok);
   a.proto = reinterpret_cast<unsigned char*>(w + lay.proto);
   a.npart = reinterpret_cast<float*>(w + lay.npart);
+  a.nu_part = reinterpret_cast<float*>(w + lay.nu_part);
   a.err = err;
   a.chunk = chunk_for(p);
   a.n_chunks = (p->n_max + a.chunk - 1) / a.chunk;

@@ -372,11 +372,13 @@ struct NodeSmem {
   alignas(1024) unsigned char Kt[2][kBlockBytes];
   alignas(1024) unsigned char Vt[2][kBlockBytes];
   alignas(1024) unsigned char Ap[3][2][kBlockBytes];
-  alignas(1024) unsigned char Kh[kvc::kProtoKhBytes];
-  float An[15][128];
-  float Ah[15][128];
+  alignas(1024) unsigned char Kh[kvc::kProtoKhBytes];   // k^ parts (phase A operand)
+  alignas(16) float vh[15][128];                          // v^ of the slot's nodes
+  float An[8][128];        // node masses of the nodes group 1 handles (index j / 2)
+  float Ah[8][128];
   float red[8][15][4];
   uint64_t k_full, k_empty, v_full, v_empty, s_full, a_ready, b_done, g1_done;
+  uint64_t vh_full, vh_free;
   uint64_t nfull[2], nempty[2];
   uint32_t tmem_base;
   int abort;
@@ -476,6 +478,7 @@ __global__ void __launch_bounds__(320, 1)
     kvcd::mbar_init(&sm.v_full, 1); kvcd::mbar_init(&sm.v_empty, 1);
     kvcd::mbar_init(&sm.s_full, 1); kvcd::mbar_init(&sm.a_ready, 4);
     kvcd::mbar_init(&sm.b_done, 1); kvcd::mbar_init(&sm.g1_done, 4);
+    kvcd::mbar_init(&sm.vh_full, 1); kvcd::mbar_init(&sm.vh_free, 8);
     for (int i = 0; i < 2; ++i) { kvcd::mbar_init(&sm.nfull[i], 1); kvcd::mbar_init(&sm.nempty[i], 4); }
     sm.abort = 0;
     kvcd::fence_mbar_init();
@@ -516,6 +519,10 @@ __global__ void __launch_bounds__(320, 1)
           for (int fb = 0; fb < 2; ++fb)
             tma_load_2d(&sm.Vt[fb][l * 2048], &vmap16, fb * 64, (int)(row0 + st), &sm.v_full);
         }
+        if (k >= 1 && !kvcd::mbar_wait(&sm.vh_free, (uint32_t)((k - 1) & 1))) { *abort_flag = 1; break; }
+        kvcd::mbar_arrive_expect_tx(&sm.vh_full, 15 * 128 * 4);
+        kvcd::bulk_g2s(&sm.vh[0][0], a.proto + tree * kvc::kProtoBytes + kvc::kProtoVhOff,
+                       15 * 128 * 4, &sm.vh_full);
       }
     }
   } else if (warp == 9) {
@@ -570,6 +577,7 @@ __global__ void __launch_bounds__(320, 1)
     const float l2 = rv ? a.lse2[blh * R + rho] : 0.f;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const int bar_id = 1 + g;
+    float g0_An[15], g0_Ah[15];                         // group 0: its rows' node masses
     for (int k = 0; k < nsl; ++k) {
       const int s = s_begin + k;
       const long long tree = blh * a.S_max + s;
@@ -652,22 +660,27 @@ __global__ void __launch_bounds__(320, 1)
         if (k >= 1 && !*abort_flag && !kvcd::mbar_wait(&sm.g1_done, (uint32_t)((k - 1) & 1)))
           *abort_flag = 1;
 #pragma unroll
-        for (int j = 0; j < 15; ++j) { sm.An[j][rl] = An[j]; sm.Ah[j][rl] = ah[j]; }
+        for (int j = 0; j < 15; ++j)
+          if (((k * 15 + j) & 1) == 1) { sm.An[j >> 1][rl] = An[j]; sm.Ah[j >> 1][rl] = ah[j]; }
         kvcd::fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) kvcd::mbar_arrive(&sm.a_ready);
+        for (int j = 0; j < 15; ++j) { g0_An[j] = An[j]; g0_Ah[j] = ah[j]; }
       } else {
         if (!*abort_flag && !kvcd::mbar_wait(&sm.a_ready, (uint32_t)(k & 1))) *abort_flag = 1;
       }
+      if (!*abort_flag && !kvcd::mbar_wait(&sm.vh_full, (uint32_t)(k & 1))) *abort_flag = 1;
       // ---- epilogue B: this group's node tiles
+#pragma unroll
       for (int j = 0; j < 15; ++j) {
         const int nn = k * 15 + j, bf = nn & 1;
         if (bf != g) continue;
         if (!*abort_flag && !kvcd::mbar_wait(&sm.nfull[bf], (uint32_t)((nn >> 1) & 1))) *abort_flag = 1;
         tc_fence_after();
-        const float Ahj = sm.Ah[j][rl], Anj = sm.An[j][rl];
-        const float4* vh = reinterpret_cast<const float4*>(proto_f + kvc::kProtoVhOff / 4 + j * kD);
+        const float Ahj = g == 0 ? g0_Ah[j] : sm.Ah[j >> 1][rl];
+        const float Anj = g == 0 ? g0_An[j] : sm.An[j >> 1][rl];
+        const float4* vh = reinterpret_cast<const float4*>(&sm.vh[j][0]);
         float dd = 0.f, uu = 0.f;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
@@ -675,7 +688,7 @@ __global__ void __launch_bounds__(320, 1)
           tmem_ld32(tmem + lane_off + 256 + bf * 128 + (uint32_t)(c * 32), v);
 #pragma unroll
           for (int t4 = 0; t4 < 8; ++t4) {
-            const float4 w = __ldg(vh + c * 8 + t4);
+            const float4 w = vh[c * 8 + t4];
             const float wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -714,6 +727,7 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       named_bar(bar_id, 128);
+      if (lane == 0) kvcd::mbar_arrive(&sm.vh_free);
       if (g == 1 && lane == 0) kvcd::mbar_arrive(&sm.g1_done);
     }
   }
