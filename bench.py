@@ -280,8 +280,10 @@ def run_gpu(args, cfg, rank, world):
     pack_ms = statistics.mean(rec["pack"])
     score_flops = 2.0 * cfg.B * cfg.L * cfg.H * cfg.G * cfg.P * tokens / cfg.B * d * 3 \
         + 2.0 * cfg.B * cfg.L * cfg.H * cfg.P * tokens / cfg.B * d * 2 * cfg.n_hops
+    dec_tc = p.packed_rows > 0 and cfg.dtype == "bf16" and d == 128   # tensor-core decode
     traffic = kernel_traffic("decode_attn_mistral16k",
-                             ["kv_cache_compression_probe_gb300/csrc/kvc_decode.cu"])
+                             ["kv_cache_compression_probe_gb300/csrc/kvc_decode.cu",
+                              "kv_cache_compression_probe_gb300/csrc/kvc_decode_tc.cu"])
     line = {
         "metric": METRIC,
         "value": tokens * world / (ms * 1e-3),
@@ -305,7 +307,8 @@ def run_gpu(args, cfg, rank, world):
         "compress_tokens_per_s": tokens / ((score_ms + sel_ms + pack_ms) * 1e-3),
         "decode_gbs": dec_gbs,
         "decode_vs_full_note": "see profiles/ for the full-cache (beta=1) decode comparison",
-        "roofline": {"kernel": "decode_chunk_kernel (+ commit)", "bound": "hbm",
+        "roofline": {"kernel": ("decode_tc_kernel (+ plan)" if dec_tc
+                                else "decode_chunk_kernel (+ commit)"), "bound": "hbm",
                      "achieved": dec_gbs, "peak": hbm, "unit": "GB/s", "frac": dec_gbs / hbm,
                      "peak_source": src + " hbm_gbs (MEASURED_PEAKS.json)",
                      "traffic": traffic,

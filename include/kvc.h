@@ -97,6 +97,10 @@ typedef struct kvc_params {
                               L*H*total_ctx); 0 = unknown, which disables the
                               tensor-core scoring passes (they need the exact
                               extent of K for their TMA descriptor)             */
+  int64_t packed_rows;     /* rows of the packed cache Kp/Vp/logm/pos (the
+                              capacity given to kvc_merge_pack); 0 = unknown,
+                              which disables the tensor-core decode (its TMA
+                              descriptor needs the extent)                      */
 } kvc_params;
 
 /* Human-readable name of a status code (static string). */
@@ -189,9 +193,15 @@ int kvc_merge_pack(const kvc_params* p, const int32_t* ctx_len, const void* K, c
  * len_lh is incremented on the device.  An (l,h) with len_lh + 1 > cap_lh
  * still attends (including the new token) but is not appended and reports
  * KVC_ECAPACITY via kvc_device_error.  pos_new may be NULL.
- * Workspace KVC_WS_DECODE holds split-K partials and per-(b,l,h) arrival
- * counters (zero before first use; every call leaves them zero, except after a
- * KVC_ETIMEOUT report, when the caller must zero the workspace again).
+ * Workspace KVC_WS_DECODE holds split-K partials, per-(b,l,h) arrival
+ * counters and a work list (zero before first use; every call leaves the
+ * counters zero, except after a KVC_ETIMEOUT report, when the caller must zero
+ * the workspace again).
+ * With dtype KVC_BF16, d = 128 and packed_rows > 0 the attention runs on the
+ * tensor cores (P = softmax numerators rounded to bf16 for the PV product; the
+ * row sums use the same rounded values); every row the call touches must then
+ * lie in [0, packed_rows), and an (l,h) whose off_lh + len_lh exceeds it is
+ * skipped and reported as KVC_EDEVICE.
  * Errors: KVC_EINVAL, KVC_EWORKSPACE, KVC_ECUDA. */
 int kvc_decode_attn(const kvc_params* p, const void* q, const void* k_new, const void* v_new,
                     const float* pos_new, void* Kp, void* Vp, float* logm, float* pos,

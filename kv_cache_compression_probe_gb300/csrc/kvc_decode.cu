@@ -20,6 +20,7 @@
 #include <mutex>
 
 #include "kvc_common.cuh"
+#include "kvc_decode_tc.h"
 #include "kvc_internal.h"
 
 namespace {
@@ -342,13 +343,73 @@ void launch_dg(const kvc_params* p, const DecodeArgs& a, dim3 grid, cudaStream_t
   }
 }
 
+// Workspace: split-K partials, per-(b,l,h) arrival counters, and the
+// tensor-core path's work list and its length.
+struct DecodeLayout {
+  size_t partials, counters, items, n_items, total;
+};
+DecodeLayout decode_layout(const kvc_params* p) {
+  const int64_t blh = kvc::lh_count(p);
+  DecodeLayout w;
+  w.partials = 0;
+  w.counters = kvc::align256((size_t)blh * n_chunk_max(p) * p->G * (p->d + 2) * sizeof(float));
+  w.items = w.counters + kvc::align256((size_t)blh * sizeof(int32_t));
+  w.n_items = w.items + kvc::align256((size_t)blh * n_chunk_max(p) * sizeof(uint32_t));
+  w.total = w.n_items + 256;
+  return w;
+}
+
+// Both entry points: validated arguments, workspace `ws` laid out as above.
+int run_decode(const kvc_params* p, const void* q, const void* k_new, const void* v_new,
+               const float* pos_new, void* Kp, void* Vp, float* logm, float* pos,
+               int32_t* len_lh, const int32_t* cap_lh, const int64_t* off_lh, void* out,
+               char* ws, int32_t* err, cudaStream_t s) {
+  const int64_t blh = kvc::lh_count(p);
+  const DecodeLayout w = decode_layout(p);
+  const int ncm = n_chunk_max(p);
+  if (kvc::decode_tc_supported(p, ncm)) {
+    kvc::DecodeTcArgs t;
+    t.q = q; t.k_new = k_new; t.v_new = v_new; t.pos_new = pos_new;
+    t.Kp = Kp; t.Vp = Vp; t.logm = logm; t.pos = pos;
+    t.len_lh = len_lh; t.cap_lh = cap_lh; t.off_lh = off_lh; t.out = out;
+    t.partials = reinterpret_cast<float*>(ws + w.partials);
+    t.counters = reinterpret_cast<int32_t*>(ws + w.counters);
+    t.items = reinterpret_cast<uint32_t*>(ws + w.items);
+    t.n_items = reinterpret_cast<int32_t*>(ws + w.n_items);
+    t.packed_rows = p->packed_rows;
+    t.blh = blh;
+    t.H = p->H; t.L = p->L; t.G = p->G; t.n_chunk_max = ncm;
+    t.scale_log2 = kLog2e / sqrtf((float)p->d);
+    t.err = err;
+    return kvc::decode_tc_launch(t, s);
+  }
+  DecodeArgs a;
+  a.q = q; a.k_new = k_new; a.v_new = v_new; a.pos_new = pos_new;
+  a.Kp = Kp; a.Vp = Vp; a.logm = logm; a.pos = pos;
+  a.len_lh = len_lh; a.cap_lh = cap_lh; a.off_lh = off_lh; a.out = out;
+  a.partials = reinterpret_cast<float*>(ws + w.partials);
+  a.counters = reinterpret_cast<int32_t*>(ws + w.counters);
+  a.H = p->H; a.L = p->L; a.n_chunk_max = ncm;
+  a.scale_log2 = kLog2e / sqrtf((float)p->d);
+  a.err = err;
+  dim3 grid(a.n_chunk_max, (unsigned)blh);
+  if (p->dtype == KVC_BF16) {
+    if (p->d == 128) launch_dg<__nv_bfloat16, 128>(p, a, grid, s);
+    else launch_dg<__nv_bfloat16, 64>(p, a, grid, s);
+  } else {
+    if (p->d == 128) launch_dg<float, 128>(p, a, grid, s);
+    else launch_dg<float, 64>(p, a, grid, s);
+  }
+  decode_commit_kernel<<<(unsigned)((blh + 255) / 256), 256, 0, s>>>(len_lh, cap_lh, blh,
+                                                                       a.n_chunk_max, err);
+  kvc::count_launch(2);
+  return kvc::cuda_status(cudaGetLastError());
+}
+
 }  // namespace
 
 namespace kvc {
-size_t decode_workspace_bytes(const kvc_params* p) {
-  const size_t part = (size_t)lh_count(p) * n_chunk_max(p) * p->G * (p->d + 2) * sizeof(float);
-  return align256(part) + align256((size_t)lh_count(p) * sizeof(int32_t));
-}
+size_t decode_workspace_bytes(const kvc_params* p) { return decode_layout(p).total; }
 }  // namespace kvc
 
 extern "C" int kvc_decode_attn(const kvc_params* p, const void* q, const void* k_new,
@@ -364,34 +425,11 @@ extern "C" int kvc_decode_attn(const kvc_params* p, const void* q, const void* k
   const size_t need = kvc::decode_workspace_bytes(p);
   if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return KVC_EWORKSPACE;
-  const int64_t blh = kvc::lh_count(p);
-  if (blh > 65535) return KVC_EINVAL;
+  if (kvc::lh_count(p) > 65535) return KVC_EINVAL;
   int32_t* err = kvc::err_word();
   if (!err) return KVC_ECUDA;
-  DecodeArgs a;
-  a.q = q; a.k_new = k_new; a.v_new = v_new; a.pos_new = pos_new;
-  a.Kp = Kp; a.Vp = Vp; a.logm = logm; a.pos = pos;
-  a.len_lh = len_lh; a.cap_lh = cap_lh; a.off_lh = off_lh; a.out = out;
-  char* ws = static_cast<char*>(workspace);
-  a.partials = reinterpret_cast<float*>(ws);
-  a.counters = reinterpret_cast<int32_t*>(
-      ws + kvc::align256((size_t)blh * n_chunk_max(p) * p->G * (p->d + 2) * sizeof(float)));
-  a.H = p->H; a.L = p->L; a.n_chunk_max = n_chunk_max(p);
-  a.scale_log2 = kLog2e / sqrtf((float)p->d);
-  a.err = err;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  dim3 grid(a.n_chunk_max, (unsigned)blh);
-  if (p->dtype == KVC_BF16) {
-    if (p->d == 128) launch_dg<__nv_bfloat16, 128>(p, a, grid, s);
-    else launch_dg<__nv_bfloat16, 64>(p, a, grid, s);
-  } else {
-    if (p->d == 128) launch_dg<float, 128>(p, a, grid, s);
-    else launch_dg<float, 64>(p, a, grid, s);
-  }
-  decode_commit_kernel<<<(unsigned)((blh + 255) / 256), 256, 0, s>>>(len_lh, cap_lh, blh,
-                                                                       a.n_chunk_max, err);
-  kvc::count_launch(2);
-  return kvc::cuda_status(cudaGetLastError());
+  return run_decode(p, q, k_new, v_new, pos_new, Kp, Vp, logm, pos, len_lh, cap_lh, off_lh, out,
+                    static_cast<char*>(workspace), err, static_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------- allocation-free variant
@@ -406,7 +444,7 @@ namespace {
 
 constexpr size_t kStaticScratchBytes = (size_t)KVC_DECODE_STATIC_SCRATCH_BYTES;
 
-// Split-K partials followed by the per-(b,l,h) arrival counters.  Every GPU that
+// Decode workspace (partials, arrival counters, work list).  Every GPU that
 // loads this library holds the array until the process exits.
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
@@ -441,36 +479,15 @@ extern "C" int kvc_decode_attn_noalloc(const kvc_params* p, const void* q, const
     return KVC_EINVAL;
   const int64_t blh = kvc::lh_count(p);
   if (blh > 65535) return KVC_EINVAL;
-  const size_t part_bytes =
-      kvc::align256((size_t)blh * n_chunk_max(p) * p->G * (p->d + 2) * sizeof(float));
-  if (part_bytes + kvc::align256((size_t)blh * sizeof(int32_t)) > kStaticScratchBytes)
-    return KVC_ESCRATCH;
+  const DecodeLayout w = decode_layout(p);
+  if (w.total > kStaticScratchBytes) return KVC_ESCRATCH;
   int32_t* err = kvc::err_word();
   char* ws = static_cast<char*>(static_scratch());
   if (!err || !ws) return KVC_ECUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  DecodeArgs a;
-  a.q = q; a.k_new = k_new; a.v_new = v_new; a.pos_new = pos_new;
-  a.Kp = Kp; a.Vp = Vp; a.logm = logm; a.pos = pos;
-  a.len_lh = len_lh; a.cap_lh = cap_lh; a.off_lh = off_lh; a.out = out;
-  a.partials = reinterpret_cast<float*>(ws);
-  a.counters = reinterpret_cast<int32_t*>(ws + part_bytes);
-  a.H = p->H; a.L = p->L; a.n_chunk_max = n_chunk_max(p);
-  a.scale_log2 = kLog2e / sqrtf((float)p->d);
-  a.err = err;
   // the arrival counters must start at zero (the array keeps the last call's contents)
-  cudaError_t e = cudaMemsetAsync(a.counters, 0, (size_t)blh * sizeof(int32_t), s);
+  cudaError_t e = cudaMemsetAsync(ws + w.counters, 0, (size_t)blh * sizeof(int32_t), s);
   if (e != cudaSuccess) return KVC_ECUDA;
-  dim3 grid(a.n_chunk_max, (unsigned)blh);
-  if (p->dtype == KVC_BF16) {
-    if (p->d == 128) launch_dg<__nv_bfloat16, 128>(p, a, grid, s);
-    else launch_dg<__nv_bfloat16, 64>(p, a, grid, s);
-  } else {
-    if (p->d == 128) launch_dg<float, 128>(p, a, grid, s);
-    else launch_dg<float, 64>(p, a, grid, s);
-  }
-  decode_commit_kernel<<<(unsigned)((blh + 255) / 256), 256, 0, s>>>(len_lh, cap_lh, blh,
-                                                                       a.n_chunk_max, err);
-  kvc::count_launch(2);
-  return kvc::cuda_status(cudaGetLastError());
+  return run_decode(p, q, k_new, v_new, pos_new, Kp, Vp, logm, pos, len_lh, cap_lh, off_lh, out,
+                    ws, err, s);
 }

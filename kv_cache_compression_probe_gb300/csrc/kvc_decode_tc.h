@@ -1,0 +1,44 @@
+// Tensor-core decode attention of kvc_decode_attn (internal).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvc.h"
+
+namespace kvc {
+
+struct DecodeTcArgs {
+  const void* q;
+  const void* k_new;
+  const void* v_new;
+  const float* pos_new;
+  void* Kp;
+  void* Vp;
+  float* logm;
+  float* pos;
+  int32_t* len_lh;
+  const int32_t* cap_lh;
+  const int64_t* off_lh;
+  void* out;
+  float* partials;      // [BLH, n_chunk_max, G, d + 2]
+  int32_t* counters;    // [BLH], zero between calls
+  uint32_t* items;      // [BLH * n_chunk_max] work list: chunk << 16 | (b,l,h)
+  int32_t* n_items;     // [1]
+  int64_t packed_rows;  // rows of Kp / Vp / logm / pos
+  int64_t blh;
+  int H, L, G, n_chunk_max;
+  float scale_log2;     // log2(e) / sqrt(d)
+  int32_t* err;
+};
+
+// bf16, d = 128, G <= 8, a known packed extent below 2^31 rows, at most 65535
+// (b,l,h) and chunks per (l,h), and a driver that can encode tensor maps.
+bool decode_tc_supported(const kvc_params* p, int n_chunk_max);
+// Rows of one split-K chunk (equal to the SIMT kernel's chunk, so both share
+// the workspace layout).
+constexpr int kDecodeTcChunk = 512;
+// Plans the work list and launches the attention kernel (2 launches); the
+// append and the length update happen inside the attention kernel.
+int decode_tc_launch(const DecodeTcArgs& a, cudaStream_t s);
+
+}  // namespace kvc

@@ -59,6 +59,8 @@ class Compressor:
         self.off_lh = torch.empty((B, L, H), dtype=torch.int64, **z)
         self.total = torch.empty((1,), dtype=torch.int64, **z)
         cap = packed_capacity(p, self.ctx_host)
+        # the tensor-core decode needs the extent of the packed cache
+        p.packed_rows = cap if tensor_cores else 0
         self.Kp = torch.empty((cap, p.d), dtype=dt, **z)
         self.Vp = torch.empty((cap, p.d), dtype=dt, **z)
         self.logm = torch.empty((cap,), dtype=f32, **z)

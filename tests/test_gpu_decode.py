@@ -18,7 +18,7 @@ def kvc():
     return K
 
 
-def _rand_cache(rng, B, L, H, d, lens, reserve, dtype):
+def _rand_cache(rng, B, L, H, d, lens, reserve, dtype, nan_reserve=False):
     lens = np.asarray(lens, dtype=np.int64).reshape(B, L, H)
     caps, offs = O.offsets(lens, reserve)
     rows = int(caps.sum())
@@ -27,12 +27,21 @@ def _rand_cache(rng, B, L, H, d, lens, reserve, dtype):
     lm = np.where(rng.uniform(size=rows) < 0.7, 0.0, rng.uniform(0, 3, size=rows)).astype(np.float32)
     if dtype == "bf16":
         Kp, Vp = W.round_bf16(Kp), W.round_bf16(Vp)
+    if nan_reserve:
+        # rows past each (l,h)'s entries hold NaN: no kernel may let them reach an output
+        for o, n, c in zip(offs.reshape(-1), lens.reshape(-1), caps.reshape(-1)):
+            Kp[o + n:o + c] = np.nan
+            Vp[o + n:o + c] = np.nan
+            lm[o + n:o + c] = np.nan
     return lens, caps, offs, Kp, Vp, lm
 
 
-def _run_decode(kvc, cfg, lens, caps, offs, Kp, Vp, lm, steps, seed):
+def _run_decode(kvc, cfg, lens, caps, offs, Kp, Vp, lm, steps, seed, tc=False):
+    """tc: give the call the packed extent, which selects the tensor-core
+    decode for bf16 / d = 128 (without it the SIMT kernel runs)."""
     B, L, H, G, d = cfg.B, cfg.L, cfg.H, cfg.G, cfg.d
-    p = params_for(cfg, n_max=max(int(lens.max()) + 64, cfg.W + 16), S_max=1)
+    p = params_for(cfg, n_max=max(int(lens.max()) + 64, cfg.W + 16), S_max=1,
+                   packed_rows=Kp.shape[0] if tc else 0)
     dt = DT[cfg.dtype]
     dKp, dVp = dev(Kp, dt), dev(Vp, dt)
     dlm = dev(lm)
@@ -76,14 +85,19 @@ def _run_decode(kvc, cfg, lens, caps, offs, Kp, Vp, lm, steps, seed):
     return outs, dlen, dKp, dlm, doff
 
 
-@pytest.mark.parametrize("dtype,d,G", [("bf16", 128, 4), ("f32", 64, 4), ("bf16", 128, 1),
-                                       ("bf16", 64, 8), ("f32", 128, 2)])
-def test_decode_matches_oracle_ragged(kvc, dtype, d, G):
+@pytest.mark.parametrize("dtype,d,G,tc", [("bf16", 128, 4, False), ("f32", 64, 4, False),
+                                          ("bf16", 128, 1, False), ("bf16", 64, 8, False),
+                                          ("f32", 128, 2, False), ("bf16", 128, 4, True),
+                                          ("bf16", 128, 1, True), ("bf16", 128, 2, True),
+                                          ("bf16", 128, 8, True)])
+def test_decode_matches_oracle_ragged(kvc, dtype, d, G, tc):
     cfg = W.small_config(B=2, L=2, H=3, G=G, d=d, dtype=dtype, P=16, W=16, n_decode=3)
     rng = np.random.default_rng(7)
     lens = [0, 1, 255, 256, 257, 600, 1023, 31, 512, 2, 800, 100]
-    lens, caps, offs, Kp, Vp, lm = _rand_cache(rng, 2, 2, 3, d, lens, 3, dtype)
-    outs, dlen, dKp, dlm, doff = _run_decode(kvc, cfg, lens, caps, offs, Kp, Vp, lm, 3, seed=1)
+    lens, caps, offs, Kp, Vp, lm = _rand_cache(rng, 2, 2, 3, d, lens, 3, dtype,
+                                               nan_reserve=(dtype == "bf16"))
+    outs, dlen, dKp, dlm, doff = _run_decode(kvc, cfg, lens, caps, offs, Kp, Vp, lm, 3, seed=1,
+                                             tc=tc)
     for got, want, err, cap_hit in outs:
         assert err == 0 and not cap_hit
         if dtype == "bf16":
@@ -98,11 +112,12 @@ def test_decode_matches_oracle_ragged(kvc, dtype, d, G):
         assert (lmv[offs.reshape(-1) + lens.reshape(-1) + i] == 0).all()
 
 
-def test_decode_capacity_overflow_reports_and_still_attends(kvc):
+@pytest.mark.parametrize("tc", [False, True])
+def test_decode_capacity_overflow_reports_and_still_attends(kvc, tc):
     cfg = W.small_config(B=1, L=1, H=2, G=4, d=128, dtype="bf16", P=16, W=16, n_decode=0)
     rng = np.random.default_rng(3)
     lens, caps, offs, Kp, Vp, lm = _rand_cache(rng, 1, 1, 2, 128, [300, 40], 0, "bf16")
-    outs, dlen, *_ = _run_decode(kvc, cfg, lens, caps, offs, Kp, Vp, lm, 1, seed=2)
+    outs, dlen, *_ = _run_decode(kvc, cfg, lens, caps, offs, Kp, Vp, lm, 1, seed=2, tc=tc)
     got, want, err, cap_hit = outs[0]
     assert err == kvc.KVC_ECAPACITY and cap_hit
     assert_bf16_close(got, want, "decode out at capacity")
@@ -126,3 +141,32 @@ def test_decode_over_oracle_packed_tiny_cache(kvc):
     for got, want, err, _ in outs:
         assert err == 0
         assert_f32_close(got, want, "tiny decode", rel=1e-5, floor_frac=1.0, axis=-1)
+
+
+def test_tc_decode_skips_and_reports_entries_past_the_packed_extent(kvc):
+    """An (l,h) whose entries would run past packed_rows is skipped (length and
+    output untouched) and reported; the other (l,h) still decode."""
+    cfg = W.small_config(B=1, L=1, H=2, G=4, d=128, dtype="bf16", P=16, W=16, n_decode=2)
+    rng = np.random.default_rng(9)
+    lens, caps, offs, Kp, Vp, lm = _rand_cache(rng, 1, 1, 2, 128, [200, 300], 2, "bf16")
+    p = params_for(cfg, n_max=400, S_max=1, packed_rows=int(offs[0, 0, 1]) + 100)
+    bf = torch.bfloat16
+    dKp, dVp, dlm = dev(Kp, bf), dev(Vp, bf), dev(lm)
+    dpos = torch.zeros(Kp.shape[0], device="cuda")
+    dlen = dev(lens.astype(np.int32))
+    ws = kvc.workspace(kvc.KVC_WS_DECODE, p, zero=True)
+    out = torch.full((1, 1, 8, 128), 7.0, dtype=bf, device="cuda")
+    q = W.round_bf16(rng.standard_normal((1, 1, 8, 128)).astype(np.float32))
+    kn = W.round_bf16(rng.standard_normal((1, 1, 2, 128)).astype(np.float32))
+    vn = W.round_bf16(rng.standard_normal((1, 1, 2, 128)).astype(np.float32))
+    kvc.kvc_decode_attn(p, dev(q, bf), dev(kn, bf), dev(vn, bf), None, dKp, dVp, dlm, dpos, dlen,
+                        dev(caps.astype(np.int32)), dev(offs.astype(np.int64)), out, ws)
+    assert kvc.kvc_device_error() == kvc.KVC_EDEVICE
+    np.testing.assert_array_equal(dlen.cpu().numpy().reshape(-1), [201, 300])
+    got = out.float().cpu().numpy()
+    assert (got[0, 0, 4:] == 7.0).all()
+    o = int(offs[0, 0, 0])
+    want, *_ = O.decode_step_head(q[0, 0, :4], kn[0, 0, 0], vn[0, 0, 0],
+                                  Kp[o:o + 200].astype(np.float64), Vp[o:o + 200].astype(np.float64),
+                                  lm[o:o + 200].astype(np.float64))
+    assert_bf16_close(got[0, 0, :4], want, "decode of the in-extent head")
