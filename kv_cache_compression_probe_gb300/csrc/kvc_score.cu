@@ -791,29 +791,94 @@ __global__ void __launch_bounds__(256, 1) nodes_kernel(kvc_params p, ScoreArgs a
 // Per slot tree: the 15 prototypes (fp32), their keys split into three bf16
 // parts (k^ = p0 + p1 + p2 to fp32 accuracy) laid out as the 128-byte-swizzled
 // K-major operand of the tensor-core node kernel, and each node's relevance.
-template <int D>
-struct ProtoSmem {
-  float Kt[128][D + 1];     // unrotated keys (padded rows: conflict-free column reads)
-  float Sk[15][D];          // per node: sum of unrotated keys
-  float Sv[15][D];          // per node: sum of values
-  float Srv[15][D];         // per node: sum of relevance * value
-  float kn[128];            // |unrotated key| per token
-  float cosv[4][128];       // cos(unrotated key, its depth-d node mean)
-  float r[128];
-  float Rn[15], kbn[15];
-  int nx[15], ny[15];
+//
+// One warp per slot tree, one pass over its tokens in order.  Lane l owns the
+// RoPE pairs (2l, 2l + 64) and (2l + 1, 2l + 65).  Per token: unrotate the
+// key (u = R(-pos) k), its norm (one warp reduction), and accumulate, per
+// node, sum u, sum u/|u|, sum v, sum r v and sum r.  Every node's sums are
+// sums over its leaves, so the accumulators run depth-first (leaf, depth 2,
+// depth 1, root) and each node is finished the moment its last leaf ends:
+//   mu = sum u / c,   kappa = mean_i cos(u_i, mu) = (sum u/|u|) . mu / (c |mu|),
+//   m = c clamp(kappa, 1/c, 1),   k^ = R(pbar) mu,   pbar = (x + y - 1) / 2,
+//   v^ = (1 - f) sum(r v) / sum r + f sum v / c   (sum v / c when sum r = 0).
+struct ProtoAcc {
+  float k[4], u[4], v[4], rv[4], r;
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int t = 0; t < 4; ++t) k[t] = u[t] = v[t] = rv[t] = 0.f;
+    r = 0.f;
+  }
+  __device__ __forceinline__ void add(const ProtoAcc& o) {
+#pragma unroll
+    for (int t = 0; t < 4; ++t) { k[t] += o.k[t]; u[t] += o.u[t]; v[t] += o.v[t]; rv[t] += o.rv[t]; }
+    r += o.r;
+  }
 };
 
-// Per slot tree: the 15 prototypes.  Unrotated keys, values and relevance-
-// weighted values are summed per leaf and then up the tree (every node's mean
-// is a sum over its leaves), so each token is touched once per quantity.
+__device__ __forceinline__ uint32_t bf16_pair(float a, float b) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
+         ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
+}
+
+// Writes node j's record entries from its sums (lane l: features 2l, 2l+1,
+// 2l+64, 2l+65; t = 0..3 in that order).
+__device__ __forceinline__ void proto_finish(const ScoreArgs& a, float value_floor, int j, int x,
+                                             int y, const ProtoAcc& s, unsigned char* out,
+                                             int lane) {
+  const float inv_c = 1.f / (float)(y - x);
+  float mu[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) mu[t] = s.k[t] * inv_c;
+  const float mu2 = kvcd::warp_sum(mu[0] * mu[0] + mu[1] * mu[1] + mu[2] * mu[2] + mu[3] * mu[3]);
+  const float um = kvcd::warp_sum(s.u[0] * mu[0] + s.u[1] * mu[1] + s.u[2] * mu[2] + s.u[3] * mu[3]);
+  const float kbn = sqrtf(mu2);
+  const float kap = kbn > 0.f ? um / kbn * inv_c : 0.f;
+  const float m = (float)(y - x) * fminf(fmaxf(kap, inv_c), 1.f);
+  // rerotate the mean at the half-integer position pbar (table row x + y - 1)
+  const int e = x + y - 1;
+  const float2 cs = __ldg(reinterpret_cast<const float2*>(a.cos_tab + (int64_t)e * 64) + lane);
+  const float2 sn = __ldg(reinterpret_cast<const float2*>(a.sin_tab + (int64_t)e * 64) + lane);
+  float kh[4];
+  kh[0] = mu[0] * cs.x - mu[2] * sn.x;
+  kh[2] = mu[2] * cs.x + mu[0] * sn.x;
+  kh[1] = mu[1] * cs.y - mu[3] * sn.y;
+  kh[3] = mu[3] * cs.y + mu[1] * sn.y;
+  // three bf16 parts, rows 16 part + j of the two 64-feature blocks
+  float r1[4], r2[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    r1[t] = kh[t] - __bfloat162float(__float2bfloat16_rn(kh[t]));
+    r2[t] = r1[t] - __bfloat162float(__float2bfloat16_rn(r1[t]));
+  }
+  const int cc = lane >> 2, wo = (lane & 3) * 4;   // 16-byte chunk, byte within it
+#pragma unroll
+  for (int part = 0; part < 3; ++part) {
+    const float* src = part == 0 ? kh : (part == 1 ? r1 : r2);
+    const int row = 16 * part + j;
+    const int off = row * 128 + ((cc ^ (row & 7)) << 4) + wo;
+    *reinterpret_cast<uint32_t*>(out + off) = bf16_pair(src[0], src[1]);
+    *reinterpret_cast<uint32_t*>(out + 6144 + off) = bf16_pair(src[2], src[3]);
+  }
+  float* vh = reinterpret_cast<float*>(out + kvc::kProtoVhOff) + j * 128;
+  float vv[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t)
+    vv[t] = s.r > 0.f ? (1.f - value_floor) * (s.rv[t] / s.r) + value_floor * s.v[t] * inv_c
+                      : s.v[t] * inv_c;
+  *reinterpret_cast<float2*>(vh + 2 * lane) = make_float2(vv[0], vv[1]);
+  *reinterpret_cast<float2*>(vh + 64 + 2 * lane) = make_float2(vv[2], vv[3]);
+  if (lane == 0) {
+    reinterpret_cast<float*>(out + kvc::kProtoLogmOff)[j] = logf(m);
+    reinterpret_cast<float*>(out + kvc::kProtoRvOff)[j] = s.r;
+  }
+}
+
 template <typename T, int D>
-__global__ void __launch_bounds__(256) proto_kernel(kvc_params p, ScoreArgs a, unsigned char* proto) {
-  static_assert(D == 128, "tensor-core node path is d = 128");
-  constexpr int HALF = D / 2;
-  extern __shared__ float4 proto_smem4[];
-  ProtoSmem<D>& ps = *reinterpret_cast<ProtoSmem<D>*>(proto_smem4);
-  const long long tree = blockIdx.x;
+__global__ void __launch_bounds__(128) proto_kernel(kvc_params p, ScoreArgs a, unsigned char* proto) {
+  static_assert(D == 128 && sizeof(T) == 2, "tensor-core node path is bf16, d = 128");
+  const int lane = threadIdx.x & 31;
+  const long long tree = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (tree >= (long long)p.B * p.L * p.H * p.S_max) return;
   const int s = (int)(tree % p.S_max);
   const long long blh = tree / p.S_max;
   const int b = seq_of(p, blh);
@@ -822,146 +887,76 @@ __global__ void __launch_bounds__(256) proto_kernel(kvc_params p, ScoreArgs a, u
   const int n = a.ctx_len[b];
   const int x0 = a.bounds[(long long)b * (p.S_max + 1) + s];
   const int y0 = a.bounds[(long long)b * (p.S_max + 1) + s + 1];
-  const int len = y0 - x0;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row0 = kvcd::seq_token_base(a.ctx_len, b, p.L * p.H) + (int64_t)lh * n;
-  const T* Kg = static_cast<const T*>(a.K) + (row0 + x0) * D;
-  const T* Vg = static_cast<const T*>(a.V) + (row0 + x0) * D;
-  if (tid < 15) { int x, y; node_range(tid, x0, y0, x, y); ps.nx[tid] = x; ps.ny[tid] = y; }
-  for (int i = tid; i < len; i += 256) ps.r[i] = a.rel[row0 + x0 + i];
-  // unrotate every key once: pair (j, j + D/2) at position x0 + i
-  for (int idx = tid; idx < len * HALF; idx += 256) {
-    const int i = idx / HALF, j = idx % HALF;
-    const float lo = kvcd::to_f(Kg[(int64_t)i * D + j]), hi = kvcd::to_f(Kg[(int64_t)i * D + HALF + j]);
-    const float cs = __ldg(a.cos_tab + (int64_t)(2 * (x0 + i)) * HALF + j);
-    const float sn = __ldg(a.sin_tab + (int64_t)(2 * (x0 + i)) * HALF + j);
-    ps.Kt[i][j] = lo * cs + hi * sn;
-    ps.Kt[i][HALF + j] = hi * cs - lo * sn;
-  }
-  __syncthreads();
-  // leaf sums (nodes 7..14), one thread per (leaf, feature) x 4
-  for (int idx = tid; idx < 8 * D; idx += 256) {
-    const int l = idx / D, f = idx % D, j = 7 + l;
-    float sk = 0.f, sv = 0.f, srv = 0.f;
-    for (int i = ps.nx[j] - x0; i < ps.ny[j] - x0; ++i) {
-      const float v = kvcd::to_f(Vg[(int64_t)i * D + f]);
-      sk += ps.Kt[i][f];
-      sv += v;
-      srv = fmaf(ps.r[i], v, srv);
-    }
-    ps.Sk[j][f] = sk; ps.Sv[j][f] = sv; ps.Srv[j][f] = srv;
-  }
-  // token key norms
-  for (int i = warp; i < len; i += 8) {
-    float q2 = 0.f;
-    for (int f = lane; f < D; f += 32) q2 = fmaf(ps.Kt[i][f], ps.Kt[i][f], q2);
-    q2 = kvcd::warp_sum(q2);
-    if (lane == 0) ps.kn[i] = sqrtf(q2);
-  }
-  __syncthreads();
-  for (int lvl = 2; lvl >= 0; --lvl) {                  // parents from children
-    const int first = (1 << lvl) - 1, cnt = 1 << lvl;
-    for (int idx = tid; idx < cnt * D; idx += 256) {
-      const int j = first + idx / D, f = idx % D;
-      ps.Sk[j][f] = ps.Sk[2 * j + 1][f] + ps.Sk[2 * j + 2][f];
-      ps.Sv[j][f] = ps.Sv[2 * j + 1][f] + ps.Sv[2 * j + 2][f];
-      ps.Srv[j][f] = ps.Srv[2 * j + 1][f] + ps.Srv[2 * j + 2][f];
-    }
-    __syncthreads();
-  }
-  // node relevance and |mean unrotated key|
-  for (int j = warp; j < 15; j += 8) {
-    float rs = 0.f;
-    for (int i = ps.nx[j] - x0 + lane; i < ps.ny[j] - x0; i += 32) rs += ps.r[i];
-    rs = kvcd::warp_sum(rs);
-    const float inv_c = 1.f / (float)(ps.ny[j] - ps.nx[j]);
-    float q2 = 0.f;
-    for (int f = lane; f < D; f += 32) { const float m = ps.Sk[j][f] * inv_c; q2 = fmaf(m, m, q2); }
-    q2 = kvcd::warp_sum(q2);
-    if (lane == 0) { ps.Rn[j] = rs; ps.kbn[j] = sqrtf(q2); }
-  }
-  __syncthreads();
-  // cos(unrotated key, mean of its node) for the node on each of the 4 levels
-  for (int t = warp; t < len * 4; t += 8) {
-    const int i = t >> 2, lvl = t & 3;
-    const int xi = x0 + i;
-    int j = 0;
-    for (int d = 0; d < lvl; ++d) { const int c1 = 2 * j + 1; j = xi < ps.ny[c1] ? c1 : c1 + 1; }
-    const float inv_c = 1.f / (float)(ps.ny[j] - ps.nx[j]);
-    float dot = 0.f;
-    for (int f = lane; f < D; f += 32) dot = fmaf(ps.Kt[i][f], ps.Sk[j][f] * inv_c, dot);
-    dot = kvcd::warp_sum(dot);
-    if (lane == 0) {
-      const float den = ps.kn[i] * ps.kbn[j];
-      ps.cosv[lvl][i] = den > 0.f ? dot / den : 0.f;
-    }
-  }
-  __syncthreads();
+  const uint32_t* Kw = reinterpret_cast<const uint32_t*>(static_cast<const T*>(a.K) + row0 * D);
+  const uint32_t* Vw = reinterpret_cast<const uint32_t*>(static_cast<const T*>(a.V) + row0 * D);
+  const float* rel = a.rel + row0;
   unsigned char* out = proto + tree * kvc::kProtoBytes;
-  float* vh_out = reinterpret_cast<float*>(out + kvc::kProtoVhOff);
-  float* lm_out = reinterpret_cast<float*>(out + kvc::kProtoLogmOff);
-  float* rv_out = reinterpret_cast<float*>(out + kvc::kProtoRvOff);
-  __shared__ float s_logm[15];
-  if (tid < 15) {
-    const int j = tid;
-    const int lvl = (j >= 7) ? 3 : (j >= 3) ? 2 : (j >= 1) ? 1 : 0;
-    const int c = ps.ny[j] - ps.nx[j];
-    float kap = 0.f;
-    for (int i = ps.nx[j] - x0; i < ps.ny[j] - x0; ++i) kap += ps.cosv[lvl][i];
-    kap /= (float)c;
-    const float m = (float)c * fminf(fmaxf(kap, 1.f / (float)c), 1.f);
-    s_logm[j] = logf(m);
-    lm_out[j] = logf(m);
-    rv_out[j] = ps.Rn[j];
-  }
-  // k^ = R(pbar) mean, v^ = (1-f) sum(r v)/sum r + f mean(v)
-  float (*Kh)[D] = reinterpret_cast<float (*)[D]>(&ps.Kt[0][0]);   // reuse: 16 rows
-  __syncthreads();
-  const float fl = p.value_floor;
-  for (int idx = tid; idx < 15 * HALF; idx += 256) {
-    const int j = idx / HALF, t = idx % HALF;
-    const float inv_c = 1.f / (float)(ps.ny[j] - ps.nx[j]);
-    const float lo = ps.Sk[j][t] * inv_c, hi = ps.Sk[j][HALF + t] * inv_c;
-    const int e = ps.nx[j] + ps.ny[j] - 1;                 // half-position row of pbar
-    const float cs = __ldg(a.cos_tab + (int64_t)e * HALF + t);
-    const float sn = __ldg(a.sin_tab + (int64_t)e * HALF + t);
-    Kh[j][t] = lo * cs - hi * sn;
-    Kh[j][HALF + t] = hi * cs + lo * sn;
-    const float rs = ps.Rn[j];
+  ProtoAcc leaf, d2, d1, root;
+  d2.zero(); d1.zero(); root.zero();
+  for (int L = 0; L < 8; ++L) {
+    int x, y;
+    node_range(7 + L, x0, y0, x, y);
+    leaf.zero();
+#pragma unroll 4
+    for (int i = x; i < y; ++i) {
+      const uint32_t klo = __ldg(Kw + (int64_t)i * (D / 2) + lane);
+      const uint32_t khi = __ldg(Kw + (int64_t)i * (D / 2) + 32 + lane);
+      const uint32_t vlo = __ldg(Vw + (int64_t)i * (D / 2) + lane);
+      const uint32_t vhi = __ldg(Vw + (int64_t)i * (D / 2) + 32 + lane);
+      const float2 cs = __ldg(reinterpret_cast<const float2*>(a.cos_tab + (int64_t)(2 * i) * 64) + lane);
+      const float2 sn = __ldg(reinterpret_cast<const float2*>(a.sin_tab + (int64_t)(2 * i) * 64) + lane);
+      const float ri = __ldg(rel + i);
+      const float k0 = __uint_as_float(klo << 16), k1 = __uint_as_float(klo & 0xFFFF0000u);
+      const float k2 = __uint_as_float(khi << 16), k3 = __uint_as_float(khi & 0xFFFF0000u);
+      float u[4];
+      u[0] = k0 * cs.x + k2 * sn.x;
+      u[2] = k2 * cs.x - k0 * sn.x;
+      u[1] = k1 * cs.y + k3 * sn.y;
+      u[3] = k3 * cs.y - k1 * sn.y;
+      const float nk = sqrtf(kvcd::warp_sum(u[0] * u[0] + u[1] * u[1] + u[2] * u[2] + u[3] * u[3]));
+      const float inv = nk > 0.f ? 1.f / nk : 0.f;
+      const float v[4] = {__uint_as_float(vlo << 16), __uint_as_float(vlo & 0xFFFF0000u),
+                          __uint_as_float(vhi << 16), __uint_as_float(vhi & 0xFFFF0000u)};
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int f = t + u * HALF;
-      vh_out[j * D + f] = rs > 0.f ? (1.f - fl) * (ps.Srv[j][f] / rs) + fl * ps.Sv[j][f] * inv_c
-                                   : ps.Sv[j][f] * inv_c;
-    }
-  }
-  if (tid < D) Kh[15][tid] = 0.f;
-  __syncthreads();
-  // three-part bf16 split of k^, rows 16p + j, 128-byte swizzle (K-major)
-  for (int idx = tid; idx < 48 * (D / 8); idx += blockDim.x) {
-    const int row = idx / (D / 8), ch = idx % (D / 8);
-    const int part = row >> 4, j = row & 15;
-    uint32_t w4[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      uint32_t h2[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const float x = Kh[j][ch * 8 + 2 * e + u];
-        const __nv_bfloat16 p0 = __float2bfloat16_rn(x);
-        const float r1 = x - __bfloat162float(p0);
-        const __nv_bfloat16 p1 = __float2bfloat16_rn(r1);
-        const __nv_bfloat16 p2 = __float2bfloat16_rn(r1 - __bfloat162float(p1));
-        const __nv_bfloat16 v = part == 0 ? p0 : (part == 1 ? p1 : p2);
-        h2[u] = (uint32_t)__bfloat16_as_ushort(v);
+      for (int t = 0; t < 4; ++t) {
+        leaf.k[t] += u[t];
+        leaf.u[t] = fmaf(u[t], inv, leaf.u[t]);
+        leaf.v[t] += v[t];
+        leaf.rv[t] = fmaf(ri, v[t], leaf.rv[t]);
       }
-      w4[e] = h2[0] | (h2[1] << 16);
+      leaf.r += ri;
     }
-    const int kb = ch >> 3, cc = ch & 7;
-    *reinterpret_cast<uint4*>(out + kb * 6144 + row * 128 + ((cc ^ (row & 7)) << 4)) =
-        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    proto_finish(a, p.value_floor, 7 + L, x, y, leaf, out, lane);
+    d2.add(leaf);
+    if (L & 1) {
+      const int j2 = 3 + (L >> 1);
+      node_range(j2, x0, y0, x, y);
+      proto_finish(a, p.value_floor, j2, x, y, d2, out, lane);
+      d1.add(d2);
+      d2.zero();
+      if ((L & 3) == 3) {
+        const int j1 = 1 + (L >> 2);
+        node_range(j1, x0, y0, x, y);
+        proto_finish(a, p.value_floor, j1, x, y, d1, out, lane);
+        root.add(d1);
+        d1.zero();
+      }
+    }
   }
-  (void)s_logm;
+  proto_finish(a, p.value_floor, 0, x0, y0, root, out, lane);
+  // row 15 of every part is padding: zero key, ln m = 0, no relevance
+#pragma unroll
+  for (int part = 0; part < 3; ++part) {
+    const int row = 16 * part + 15;
+    const int off = row * 128 + lane * 4;
+    *reinterpret_cast<uint32_t*>(out + off) = 0u;
+    *reinterpret_cast<uint32_t*>(out + 6144 + off) = 0u;
+  }
+  if (lane == 0) {
+    reinterpret_cast<float*>(out + kvc::kProtoLogmOff)[15] = 0.f;
+    reinterpret_cast<float*>(out + kvc::kProtoRvOff)[15] = 0.f;
+  }
 }
 
 // Per slot: combine the row-tile partial statistics into D, D_drop and the 16
@@ -1127,9 +1122,7 @@ int launch_all(const kvc_params* p, ScoreArgs& a, cudaStream_t s) {
       launches += 2;
     }
     // prototypes, tensor-core node statistics, utilities
-    cudaFuncSetAttribute(proto_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)sizeof(ProtoSmem<D>));
-    proto_kernel<T, D><<<(unsigned)(blh * p->S_max), 256, sizeof(ProtoSmem<D>), s>>>(*p, a, a.proto);
+    proto_kernel<T, D><<<(unsigned)((blh * p->S_max + 3) / 4), 128, 0, s>>>(*p, a, a.proto);
     kvc::NodeTcArgs nd;
     nd.ctx_len = a.ctx_len; nd.K = a.K; nd.V = a.V; nd.Qp = a.Qp; nd.lse2 = a.lse2; nd.ok = a.ok;
     nd.bounds = a.bounds; nd.n_slots = a.n_slots; nd.proto = a.proto; nd.npart = a.npart;
