@@ -106,6 +106,10 @@ typedef struct kvc_params {
 /* Human-readable name of a status code (static string). */
 const char* kvc_status_string(int status);
 
+/* Text of the last CUDA runtime error behind a KVC_ECUDA status from any call
+ * in this process ("none" if there was none); a static string. */
+const char* kvc_last_cuda_error(void);
+
 /* Reads and clears the device error word (synchronises `stream`).  Returns
  * KVC_OK and writes 0 to *code when nothing was recorded, otherwise writes the
  * first recorded code (a negative KVC_* value) to *code. */

@@ -25,7 +25,13 @@ static int32_t* g_err_ptr[256];
 
 void count_launch(int64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? KVC_OK : KVC_ECUDA; }
+// Last CUDA runtime error seen by any call (diagnostics for KVC_ECUDA).
+std::atomic<int> g_last_cuda_error{0};
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return KVC_OK;
+  g_last_cuda_error.store((int)e, std::memory_order_relaxed);
+  return KVC_ECUDA;
+}
 
 int32_t* err_word() {
   int dev = 0;
@@ -55,6 +61,11 @@ int check_params(const kvc_params* p) {
 }  // namespace kvc
 
 extern "C" {
+
+const char* kvc_last_cuda_error(void) {
+  const int e = kvc::g_last_cuda_error.load(std::memory_order_relaxed);
+  return e == 0 ? "none" : cudaGetErrorString((cudaError_t)e);
+}
 
 const char* kvc_status_string(int s) {
   switch (s) {

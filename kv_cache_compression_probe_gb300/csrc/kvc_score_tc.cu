@@ -357,15 +357,25 @@ __global__ void __launch_bounds__((4 * NT + 2) * 32, 1)
 //   phase A  S = Q K^T (keys placed leaf by leaf on 16-row boundaries) and
 //            A^ = Q [k^0; k^1; k^2]^T (k^ in three bf16 parts, summed in fp32);
 //   epi A    a = 2^(s - LSE) split into three bf16 parts written as the
-//            K-major operand over the 128 leaf-padded key slots; per-row node
-//            masses A_N and A_hat_N to shared memory;
+//            K-major operand over the 128 leaf-padded key slots (each of the
+//            four epilogue groups takes 32 key slots = two leaves); per-row
+//            leaf masses to shared memory;
 //   phase B  for each of the 15 nodes: U_N = sum over parts and over the node's
 //            key slots of a_part V (V read as an MN-major operand straight from
 //            TMA) into one of two TMEM buffers;
-//   epi B    two warp groups alternate over the node buffers: per row
-//            |U - A^ v^|, |U|, |A - A^|, A, summed over the group's rows.
+//   epi B    every group reads 32 of the 128 features of each node buffer and
+//            forms per-row partial sums of |U - A^ v^|^2 and |U|^2 (packed
+//            f32x2 FMAs); the four warps sharing a row quarter add the partials
+//            and one of them (rotating with the node) finishes the row's
+//            |U - A^ v^|, |U|, |A - A^| and A and sums them over its 32 rows.
 // Per-(slot, tile) sums go to `npart`; a small kernel forms D and utilities.
 constexpr int kNodeSlots = 8;
+constexpr int kEpiWarps = 16;                      // 4 groups x 4 row quarters
+constexpr int kNodeThreads = (kEpiWarps + 2) * 32; // + producer + MMA issuer
+constexpr int kProdWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1;
+// Registers are reserved for whole groups of 4 warps: 18 warps count as 20, so
+// a thread may use at most 65536 / (20 * 32) = 102, i.e. 96 registers.
+constexpr int kNodeMaxRegs = 96;
 
 struct NodeSmem {
   alignas(1024) unsigned char Q[2][kBlockBytes];
@@ -374,15 +384,19 @@ struct NodeSmem {
   alignas(1024) unsigned char Ap[3][2][kBlockBytes];
   alignas(1024) unsigned char Kh[kvc::kProtoKhBytes];   // k^ parts (phase A operand)
   alignas(16) float vh[15][128];                          // v^ of the slot's nodes
-  float An[8][128];        // node masses of the nodes group 1 handles (index j / 2)
-  float Ah[8][128];
-  float red[8][15][4];
-  uint64_t k_full, k_empty, v_full, v_empty, s_full, a_ready, b_done, g1_done;
+  union {                                                 // live in turn within a slot:
+    float Al[8][128];                                     //   per-row leaf masses (epi A)
+    float2 part[2][4][128];                               //   per-row |U-A^v^|^2, |U|^2 (epi B)
+  };
+  float red[2][4][15][4];                                 // per-quarter node sums
+  uint64_t k_full, k_empty, v_full, v_empty, s_full, a_ready, b_done;
   uint64_t vh_full, vh_free;
   uint64_t nfull[2], nempty[2];
+  uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(NodeSmem) + 1024 <= 232448, "node kernel shared memory");
 
 // N = 48 (three 16-row parts of the prototype keys), both operands K-major.
 constexpr uint32_t kIdescN48 = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(48 >> 3) << 17) |
@@ -405,7 +419,8 @@ __device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr, uint32_t lbo_b
          ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+// 16 consecutive TMEM columns of this thread's lane (issue only; see tmem_wait).
+__device__ __forceinline__ void tmem_ld16_nw(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -414,9 +429,26 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
         "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Packed pair of fp32 (a in the low half) and d = a * b + d on both halves.
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ float hsum2(uint64_t x) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+  return lo + hi;
 }
 
 // Leaf l of the slot [x0, y0): first token and token count (midpoint rule).
@@ -438,7 +470,7 @@ __device__ __forceinline__ void node_leaves(int j, int& l0, int& l1) {
   l0 = k * w; l1 = l0 + w;
 }
 
-__global__ void __launch_bounds__(320, 1)
+__global__ void __maxnreg__(kNodeMaxRegs)
     nodes_tc_kernel(const __grid_constant__ CUtensorMap kmap16,
                     const __grid_constant__ CUtensorMap vmap16, kvc::NodeTcArgs a) {
   extern __shared__ __align__(1024) unsigned char nd_raw[];
@@ -462,7 +494,7 @@ __global__ void __launch_bounds__(320, 1)
   const int32_t* bd = a.bounds + (long long)b * (a.S_max + 1);
 
   // ---- this tile's query rows -> swizzled K-major smem
-  for (int idx = tid; idx < kBM * 16; idx += 320) {
+  for (int idx = tid; idx < kBM * 16; idx += kNodeThreads) {
     const int r = idx >> 4, c = idx & 15;
     const int rho = mt * kBM + r;
     uint4 val = make_uint4(0, 0, 0, 0);
@@ -476,14 +508,18 @@ __global__ void __launch_bounds__(320, 1)
   if (tid == 0) {
     kvcd::mbar_init(&sm.k_full, 1); kvcd::mbar_init(&sm.k_empty, 1);
     kvcd::mbar_init(&sm.v_full, 1); kvcd::mbar_init(&sm.v_empty, 1);
-    kvcd::mbar_init(&sm.s_full, 1); kvcd::mbar_init(&sm.a_ready, 4);
-    kvcd::mbar_init(&sm.b_done, 1); kvcd::mbar_init(&sm.g1_done, 4);
-    kvcd::mbar_init(&sm.vh_full, 1); kvcd::mbar_init(&sm.vh_free, 8);
-    for (int i = 0; i < 2; ++i) { kvcd::mbar_init(&sm.nfull[i], 1); kvcd::mbar_init(&sm.nempty[i], 4); }
+    kvcd::mbar_init(&sm.s_full, 1); kvcd::mbar_init(&sm.a_ready, kEpiWarps);
+    kvcd::mbar_init(&sm.b_done, 1);
+    kvcd::mbar_init(&sm.mma_done, 1);
+    kvcd::mbar_init(&sm.vh_full, 1); kvcd::mbar_init(&sm.vh_free, kEpiWarps);
+    for (int i = 0; i < 2; ++i) {
+      kvcd::mbar_init(&sm.nfull[i], 1);
+      kvcd::mbar_init(&sm.nempty[i], kEpiWarps);
+    }
     sm.abort = 0;
     kvcd::fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      kvcd::smem_u32(&sm.tmem_base)), "r"(512u)
                  : "memory");
@@ -495,14 +531,16 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort_flag = &sm.abort;
 
-  if (warp == 8) {
+  if (warp == kProdWarp) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
+      int nk = 0, nv = 0, nh = 0;                    // loads issued per barrier
       for (int k = 0; k < nsl; ++k) {
         const int s = s_begin + k;
         const long long tree = blh * a.S_max + s;
         const int x0 = bd[s], y0 = bd[s + 1];
         if (k >= 1 && !kvcd::mbar_wait(&sm.k_empty, (uint32_t)((k - 1) & 1))) { *abort_flag = 1; break; }
+        ++nk;
         kvcd::mbar_arrive_expect_tx(&sm.k_full, kTileBytes + kvc::kProtoKhBytes);
         for (int l = 0; l < 8; ++l) {
           int st, cnt;
@@ -512,6 +550,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         kvcd::bulk_g2s(sm.Kh, a.proto + tree * kvc::kProtoBytes, kvc::kProtoKhBytes, &sm.k_full);
         if (k >= 1 && !kvcd::mbar_wait(&sm.v_empty, (uint32_t)((k - 1) & 1))) { *abort_flag = 1; break; }
+        ++nv;
         kvcd::mbar_arrive_expect_tx(&sm.v_full, kTileBytes);
         for (int l = 0; l < 8; ++l) {
           int st, cnt;
@@ -520,12 +559,18 @@ __global__ void __launch_bounds__(320, 1)
             tma_load_2d(&sm.Vt[fb][l * 2048], &vmap16, fb * 64, (int)(row0 + st), &sm.v_full);
         }
         if (k >= 1 && !kvcd::mbar_wait(&sm.vh_free, (uint32_t)((k - 1) & 1))) { *abort_flag = 1; break; }
+        ++nh;
         kvcd::mbar_arrive_expect_tx(&sm.vh_full, 15 * 128 * 4);
         kvcd::bulk_g2s(&sm.vh[0][0], a.proto + tree * kvc::kProtoBytes + kvc::kProtoVhOff,
                        15 * 128 * 4, &sm.vh_full);
       }
+      if (*abort_flag) {                               // let copies in flight land
+        if (nk) kvcd::mbar_wait(&sm.k_full, (uint32_t)((nk - 1) & 1));
+        if (nv) kvcd::mbar_wait(&sm.v_full, (uint32_t)((nv - 1) & 1));
+        if (nh) kvcd::mbar_wait(&sm.vh_full, (uint32_t)((nh - 1) & 1));
+      }
     }
-  } else if (warp == 9) {
+  } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       for (int k = 0; k < nsl; ++k) {
@@ -567,175 +612,187 @@ __global__ void __launch_bounds__(320, 1)
         mma_commit(&sm.b_done);
         mma_commit(&sm.v_empty);
       }
+      if (*abort_flag) {                               // issued MMAs finish before TMEM is freed
+        mma_commit(&sm.mma_done);
+        kvcd::mbar_wait(&sm.mma_done, 0);
+      }
     }
   } else {
     // ---------------------------------------------------------------- epilogue groups
-    const int g = warp >> 2, q = warp & 3;
-    const int rl = q * 32 + lane;                      // row within the tile (TMEM lane)
+    const int g = warp >> 2, q = warp & 3;          // group (feature / key quarter), row quarter
+    const int rl = q * 32 + lane;                   // row within the tile (TMEM lane)
     const int rho = mt * kBM + rl;
     const bool rv = rho < R;
     const float l2 = rv ? a.lse2[blh * R + rho] : 0.f;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    const int bar_id = 1 + g;
-    float g0_An[15], g0_Ah[15];                         // group 0: its rows' node masses
+    const int qbar = 1 + q;                          // the 4 warps sharing these rows
     for (int k = 0; k < nsl; ++k) {
       const int s = s_begin + k;
       const long long tree = blh * a.S_max + s;
       const int x0 = bd[s], y0 = bd[s + 1];
       const float* proto_f = reinterpret_cast<const float*>(a.proto + tree * kvc::kProtoBytes);
-      if (g == 0) {
-        // ---- epilogue A: attention of this row to the slot keys and nodes
-        if (!*abort_flag && !kvcd::mbar_wait(&sm.s_full, (uint32_t)(k & 1))) *abort_flag = 1;
-        tc_fence_after();
-        float ah[15];
-        {
-          float d0[16], d1[16], d2[16];
-          tmem_ld16(tmem + lane_off + 128, d0);
-          tmem_ld16(tmem + lane_off + 144, d1);
-          tmem_ld16(tmem + lane_off + 160, d2);
-          const float* lmv = proto_f + kvc::kProtoLogmOff / 4;
+      // ---- epilogue A: attention of this row to the slot's nodes and its key quarter
+      if (!*abort_flag && !kvcd::mbar_wait(&sm.s_full, (uint32_t)(k & 1))) *abort_flag = 1;
+      tc_fence_after();
+      float ah[15];
+      {
+        float d0[16], d1[16], d2[16];
+        tmem_ld16_nw(tmem + lane_off + 128, d0);
+        tmem_ld16_nw(tmem + lane_off + 144, d1);
+        tmem_ld16_nw(tmem + lane_off + 160, d2);
+        tmem_wait();
+        const float* lmv = proto_f + kvc::kProtoLogmOff / 4;
 #pragma unroll
-          for (int j = 0; j < 15; ++j) {
-            const float sc = (d0[j] + d1[j] + d2[j]) * a.q_scale2 +
-                             __ldg(lmv + j) * 1.4426950408889634f - l2;
-            ah[j] = rv ? exp2f(sc) : 0.f;
-          }
+        for (int j = 0; j < 15; ++j) {
+          const float sc = (d0[j] + d1[j] + d2[j]) * a.q_scale2 +
+                           __ldg(lmv + j) * 1.4426950408889634f - l2;
+          ah[j] = rv ? exp2f(sc) : 0.f;
         }
-        int cnt[8];
-#pragma unroll
-        for (int l = 0; l < 8; ++l) { int st; leaf_range(l, x0, y0, st, cnt[l]); }
-        if (k >= 1 && !*abort_flag && !kvcd::mbar_wait(&sm.b_done, (uint32_t)((k - 1) & 1)))
-          *abort_flag = 1;
-        float lsum[8];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tmem_ld32(tmem + lane_off + (uint32_t)(c * 32), v);
-          float s0 = 0.f, s1 = 0.f;
-          uint32_t pk[3][16];
-#pragma unroll
-          for (int t = 0; t < 32; t += 2) {
-            float av[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int kap = c * 32 + t + u;
-              const bool valid = rv && ((kap & 15) < cnt[kap >> 4]);
-              av[u] = valid ? exp2f(v[t + u] * a.q_scale2 - l2) : 0.f;
-            }
-            if (t < 16) s0 += av[0] + av[1]; else s1 += av[0] + av[1];
-            uint32_t h[3][2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const __nv_bfloat16 p0 = __float2bfloat16_rn(av[u]);
-              const float r1 = av[u] - __bfloat162float(p0);
-              const __nv_bfloat16 p1 = __float2bfloat16_rn(r1);
-              const __nv_bfloat16 p2 = __float2bfloat16_rn(r1 - __bfloat162float(p1));
-              h[0][u] = __bfloat16_as_ushort(p0);
-              h[1][u] = __bfloat16_as_ushort(p1);
-              h[2][u] = __bfloat16_as_ushort(p2);
-            }
-#pragma unroll
-            for (int pt = 0; pt < 3; ++pt) pk[pt][t >> 1] = h[pt][0] | (h[pt][1] << 16);
-          }
-          lsum[2 * c] = s0;
-          lsum[2 * c + 1] = s1;
-          // 32 key slots = four 16-byte chunks per part
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            const int kap = c * 32 + ch * 8;
-            const int kb = kap >> 6, cidx = (kap & 63) >> 3;
-            const int off = rl * 128 + ((cidx ^ (rl & 7)) << 4);
-#pragma unroll
-            for (int pt = 0; pt < 3; ++pt)
-              *reinterpret_cast<uint4*>(&sm.Ap[pt][kb][off]) =
-                  make_uint4(pk[pt][ch * 4], pk[pt][ch * 4 + 1], pk[pt][ch * 4 + 2], pk[pt][ch * 4 + 3]);
-          }
-        }
-        // node masses: leaves, then their parents
-        float An[15];
-#pragma unroll
-        for (int l = 0; l < 8; ++l) An[7 + l] = lsum[l];
-#pragma unroll
-        for (int j = 6; j >= 0; --j) An[j] = An[2 * j + 1] + An[2 * j + 2];
-        if (k >= 1 && !*abort_flag && !kvcd::mbar_wait(&sm.g1_done, (uint32_t)((k - 1) & 1)))
-          *abort_flag = 1;
-#pragma unroll
-        for (int j = 0; j < 15; ++j)
-          if (((k * 15 + j) & 1) == 1) { sm.An[j >> 1][rl] = An[j]; sm.Ah[j >> 1][rl] = ah[j]; }
-        kvcd::fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) kvcd::mbar_arrive(&sm.a_ready);
-        for (int j = 0; j < 15; ++j) { g0_An[j] = An[j]; g0_Ah[j] = ah[j]; }
-      } else {
-        if (!*abort_flag && !kvcd::mbar_wait(&sm.a_ready, (uint32_t)(k & 1))) *abort_flag = 1;
       }
+      int cnt0, cnt1;
+      {
+        int st;
+        leaf_range(2 * g, x0, y0, st, cnt0);
+        leaf_range(2 * g + 1, x0, y0, st, cnt1);
+      }
+      if (k >= 1 && !*abort_flag && !kvcd::mbar_wait(&sm.b_done, (uint32_t)((k - 1) & 1)))
+        *abort_flag = 1;
+      float lsum[2];
+#pragma unroll
+      for (int hq = 0; hq < 2; ++hq) {                 // leaf 2g + hq: key slots 32g + 16hq ..
+        float v[16];
+        tmem_ld16_nw(tmem + lane_off + (uint32_t)(32 * g + 16 * hq), v);
+        tmem_wait();
+        const int cntl = hq ? cnt1 : cnt0;
+        float sacc = 0.f;
+        uint32_t pk[3][8];
+#pragma unroll
+        for (int t = 0; t < 16; t += 2) {
+          float av[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            av[u] = (rv && t + u < cntl) ? exp2f(v[t + u] * a.q_scale2 - l2) : 0.f;
+          sacc += av[0] + av[1];
+          uint32_t h[3][2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const __nv_bfloat16 p0 = __float2bfloat16_rn(av[u]);
+            const float r1 = av[u] - __bfloat162float(p0);
+            const __nv_bfloat16 p1 = __float2bfloat16_rn(r1);
+            const __nv_bfloat16 p2 = __float2bfloat16_rn(r1 - __bfloat162float(p1));
+            h[0][u] = __bfloat16_as_ushort(p0);
+            h[1][u] = __bfloat16_as_ushort(p1);
+            h[2][u] = __bfloat16_as_ushort(p2);
+          }
+#pragma unroll
+          for (int pt = 0; pt < 3; ++pt) pk[pt][t >> 1] = h[pt][0] | (h[pt][1] << 16);
+        }
+        lsum[hq] = sacc;
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          const int kap = 32 * g + 16 * hq + ch * 8;
+          const int kb = kap >> 6, cidx = (kap & 63) >> 3;
+          const int off = rl * 128 + ((cidx ^ (rl & 7)) << 4);
+#pragma unroll
+          for (int pt = 0; pt < 3; ++pt)
+            *reinterpret_cast<uint4*>(&sm.Ap[pt][kb][off]) =
+                make_uint4(pk[pt][ch * 4], pk[pt][ch * 4 + 1], pk[pt][ch * 4 + 2], pk[pt][ch * 4 + 3]);
+        }
+      }
+      sm.Al[2 * g][rl] = lsum[0];
+      sm.Al[2 * g + 1][rl] = lsum[1];
+      kvcd::fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) kvcd::mbar_arrive(&sm.a_ready);
+      named_bar(qbar, 128);                          // leaf masses of these rows complete
+      float an_fin[4];                               // masses of the nodes g, g+4, g+8, g+12
+      {
+        float an[15];
+#pragma unroll
+        for (int l = 0; l < 8; ++l) an[7 + l] = sm.Al[l][rl];
+#pragma unroll
+        for (int j = 6; j >= 0; --j) an[j] = an[2 * j + 1] + an[2 * j + 2];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float v = 0.f;
+#pragma unroll
+          for (int j = i * 4; j < i * 4 + 4 && j < 15; ++j)
+            if ((j & 3) == g) v = an[j];
+          an_fin[i] = v;
+        }
+      }
+      named_bar(5, kEpiWarps * 32);                  // every row read its leaf masses
       if (!*abort_flag && !kvcd::mbar_wait(&sm.vh_full, (uint32_t)(k & 1))) *abort_flag = 1;
-      // ---- epilogue B: this group's node tiles
+      // ---- epilogue B: 32 features of every node
 #pragma unroll
       for (int j = 0; j < 15; ++j) {
         const int nn = k * 15 + j, bf = nn & 1;
-        if (bf != g) continue;
         if (!*abort_flag && !kvcd::mbar_wait(&sm.nfull[bf], (uint32_t)((nn >> 1) & 1))) *abort_flag = 1;
         tc_fence_after();
-        const float Ahj = g == 0 ? g0_Ah[j] : sm.Ah[j >> 1][rl];
-        const float Anj = g == 0 ? g0_An[j] : sm.An[j >> 1][rl];
-        const float4* vh = reinterpret_cast<const float4*>(&sm.vh[j][0]);
-        float dd = 0.f, uu = 0.f;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float v[32];
-          tmem_ld32(tmem + lane_off + 256 + bf * 128 + (uint32_t)(c * 32), v);
+        float v[32];
+        {
+          float v0[16], v1[16];
+          const uint32_t col = tmem + lane_off + 256 + bf * 128 + 32 * g;
+          tmem_ld16_nw(col, v0);
+          tmem_ld16_nw(col + 16, v1);
+          tmem_wait();
 #pragma unroll
-          for (int t4 = 0; t4 < 8; ++t4) {
-            const float4 w = vh[c * 8 + t4];
-            const float wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float u = v[t4 * 4 + e];
-              const float df = u - Ahj * wv[e];
-              dd = fmaf(df, df, dd);
-              uu = fmaf(u, u, uu);
-            }
-          }
+          for (int i = 0; i < 16; ++i) { v[i] = v0[i]; v[16 + i] = v1[i]; }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) kvcd::mbar_arrive(&sm.nempty[bf]);
-        float st[4];
-        st[0] = rv ? fabsf(Anj - Ahj) : 0.f;
-        st[1] = rv ? Anj : 0.f;
-        st[2] = rv ? sqrtf(dd) : 0.f;
-        st[3] = rv ? sqrtf(uu) : 0.f;
+        const uint64_t nah = f2(-ah[j], -ah[j]);
+        const ulonglong2* w2 = reinterpret_cast<const ulonglong2*>(&sm.vh[j][32 * g]);
+        uint64_t dd0 = 0, dd1 = 0, uu0 = 0, uu1 = 0;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float t = kvcd::warp_sum(st[e]);
-          if (lane == 0) sm.red[warp][j][e] = t;
+        for (int t = 0; t < 8; ++t) {
+          const ulonglong2 w = w2[t];
+          const uint64_t ua = f2(v[4 * t], v[4 * t + 1]), ub = f2(v[4 * t + 2], v[4 * t + 3]);
+          const uint64_t da = fma2(nah, w.x, ua), db = fma2(nah, w.y, ub);
+          dd0 = fma2(da, da, dd0);
+          dd1 = fma2(db, db, dd1);
+          uu0 = fma2(ua, ua, uu0);
+          uu1 = fma2(ub, ub, uu1);
         }
-      }
-      named_bar(bar_id, 128);
-      // sums over the group's four warps for the nodes it handled
-      {
-        const int et = tid - g * 128;                  // 0..127 within the group
-        if (et < 60) {
-          const int j = et >> 2, e = et & 3;
-          if (((k * 15 + j) & 1) == g) {
-            float t = 0.f;
-            for (int w = 0; w < 4; ++w) t += sm.red[g * 4 + w][j][e];
-            a.npart[((tree * 2 + mt) * 15 + j) * 4 + e] = t;
+        sm.part[j & 1][g][rl] = make_float2(hsum2(dd0) + hsum2(dd1), hsum2(uu0) + hsum2(uu1));
+        named_bar(qbar, 128);
+        if (g == (j & 3)) {                            // finisher of node j for these rows
+          float dd = 0.f, uu = 0.f;
+#pragma unroll
+          for (int gg = 0; gg < 4; ++gg) {
+            const float2 pp = sm.part[j & 1][gg][rl];
+            dd += pp.x;
+            uu += pp.y;
+          }
+          float st[4];
+          st[0] = rv ? fabsf(an_fin[j >> 2] - ah[j]) : 0.f;
+          st[1] = rv ? an_fin[j >> 2] : 0.f;
+          st[2] = rv ? sqrtf(dd) : 0.f;
+          st[3] = rv ? sqrtf(uu) : 0.f;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float t = kvcd::warp_sum(st[e]);
+            if (lane == 0) sm.red[k & 1][q][j][e] = t;
           }
         }
       }
-      named_bar(bar_id, 128);
+      named_bar(5, kEpiWarps * 32);                  // every node of this slot finished
+      if (tid < 60) {
+        const int j = tid >> 2, e = tid & 3;
+        const float t = (sm.red[k & 1][0][j][e] + sm.red[k & 1][1][j][e]) +
+                        (sm.red[k & 1][2][j][e] + sm.red[k & 1][3][j][e]);
+        a.npart[((tree * 2 + mt) * 15 + j) * 4 + e] = t;
+      }
       if (lane == 0) kvcd::mbar_arrive(&sm.vh_free);
-      if (g == 1 && lane == 0) kvcd::mbar_arrive(&sm.g1_done);
     }
   }
 
   __syncthreads();
   if (*abort_flag && tid == 0) kvcd::record_error(a.err, KVC_ETIMEOUT);
   tc_fence_after();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512u)
                  : "memory");
   }
@@ -829,7 +886,7 @@ int nodes_tc_pass(const NodeTcArgs& a, int64_t total_rows, cudaStream_t s) {
     return KVC_ECUDA;
   const int n_mt = (a.G * a.P + kBM - 1) / kBM;
   dim3 grid((a.S_max + kNodeSlots - 1) / kNodeSlots, n_mt, (unsigned)((long long)a.B * a.L * a.H));
-  nodes_tc_kernel<<<grid, 320, smem, s>>>(km, vm, a);
+  nodes_tc_kernel<<<grid, kNodeThreads, smem, s>>>(km, vm, a);
   kvc::count_launch();
   return kvc::cuda_status(cudaGetLastError());
 }

@@ -21,7 +21,7 @@ KVC_ECUDA, KVC_ETIMEOUT, KVC_EWORKSPACE, KVC_EDEVICE, KVC_ESCRATCH = -4, -5, -6,
 KVC_F32, KVC_BF16 = 0, 1
 KVC_WS_SCORE, KVC_WS_SELECT, KVC_WS_PACK, KVC_WS_DECODE, KVC_WS_PARTITION = range(5)
 
-EXPORTED = ("kvc_status_string", "kvc_device_error", "kvc_launch_count", "kvc_workspace_bytes",
+EXPORTED = ("kvc_status_string", "kvc_last_cuda_error", "kvc_device_error", "kvc_launch_count", "kvc_workspace_bytes",
             "kvc_rope_table", "kvc_score", "kvc_select", "kvc_merge_pack", "kvc_decode_attn",
             "kvc_partition", "kvc_decode_attn_noalloc")
 
@@ -41,7 +41,10 @@ class kvc_params(ctypes.Structure):
 
 class KvcError(RuntimeError):
     def __init__(self, status: int, what: str):
-        super().__init__(f"{what}: {kvc_status_string(status)} ({status})")
+        msg = f"{what}: {kvc_status_string(status)} ({status})"
+        if status == KVC_ECUDA:
+            msg += f": {lib().kvc_last_cuda_error().decode()}"
+        super().__init__(msg)
         self.status = status
 
 
@@ -58,6 +61,7 @@ def lib():
         L = ctypes.CDLL(LIB_PATH)
         vp = c_void_p
         L.kvc_status_string.argtypes = [c_int]; L.kvc_status_string.restype = ctypes.c_char_p
+        L.kvc_last_cuda_error.argtypes = []; L.kvc_last_cuda_error.restype = ctypes.c_char_p
         L.kvc_device_error.argtypes = [vp, ctypes.POINTER(c_int32)]; L.kvc_device_error.restype = c_int
         L.kvc_launch_count.argtypes = []; L.kvc_launch_count.restype = c_int64
         L.kvc_workspace_bytes.argtypes = [c_int, _P]; L.kvc_workspace_bytes.restype = c_size_t
