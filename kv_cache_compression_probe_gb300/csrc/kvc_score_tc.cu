@@ -365,9 +365,10 @@ __global__ void __launch_bounds__((4 * NT + 2) * 32, 1)
 //            TMA) into one of two TMEM buffers;
 //   epi B    every group reads 32 of the 128 features of each node buffer and
 //            forms per-row partial sums of |U - A^ v^|^2 and |U|^2 (packed
-//            f32x2 FMAs); the four warps sharing a row quarter add the partials
-//            and one of them (rotating with the node) finishes the row's
-//            |U - A^ v^|, |U|, |A - A^| and A and sums them over its 32 rows.
+//            f32x2 FMAs) into spare TMEM columns; after each pair of nodes the
+//            four warps sharing a row quarter meet, and one of them (rotating
+//            with the node) adds the partials in a fixed order and finishes the
+//            row's |U - A^ v^|, |U|, |A - A^| and A, summed over its 32 rows.
 // Per-(slot, tile) sums go to `npart`; a small kernel forms D and utilities.
 constexpr int kNodeSlots = 8;
 constexpr int kEpiWarps = 16;                      // 4 groups x 4 row quarters
@@ -382,12 +383,9 @@ struct NodeSmem {
   alignas(1024) unsigned char Kt[2][kBlockBytes];
   alignas(1024) unsigned char Vt[2][kBlockBytes];
   alignas(1024) unsigned char Ap[3][2][kBlockBytes];
-  alignas(1024) unsigned char Kh[kvc::kProtoKhBytes];   // k^ parts (phase A operand)
+  alignas(1024) unsigned char Kh[kvc::kProtoHeadBytes]; // k^ parts (phase A operand), ln m, Rv
   alignas(16) float vh[15][128];                          // v^ of the slot's nodes
-  union {                                                 // live in turn within a slot:
-    float Al[8][128];                                     //   per-row leaf masses (epi A)
-    float2 part[2][4][128];                               //   per-row |U-A^v^|^2, |U|^2 (epi B)
-  };
+  float Al[8][128];                                       // per-row leaf masses
   float red[2][4][15][4];                                 // per-quarter node sums
   uint64_t k_full, k_empty, v_full, v_empty, s_full, a_ready, b_done;
   uint64_t vh_full, vh_free;
@@ -449,6 +447,27 @@ __device__ __forceinline__ float hsum2(uint64_t x) {
   float lo, hi;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
   return lo + hi;
+}
+
+// Spare TMEM columns 176..207 (no MMA writes there) hold the per-row partial
+// sums of node j from group g: pair parity, node parity, group, (dd, uu).
+__device__ __forceinline__ uint32_t part_col(int j, int g) {
+  return 176u + (uint32_t)(((j >> 1) & 1) * 16 + (j & 1) * 8 + 2 * g);
+}
+__device__ __forceinline__ void tmem_st2(uint32_t taddr, float a, float b) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr),
+               "r"(__float_as_uint(a)), "r"(__float_as_uint(b))
+               : "memory");
+}
+__device__ __forceinline__ void tld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Leaf l of the slot [x0, y0): first token and token count (midpoint rule).
@@ -539,16 +558,22 @@ __global__ void __maxnreg__(kNodeMaxRegs)
         const int s = s_begin + k;
         const long long tree = blh * a.S_max + s;
         const int x0 = bd[s], y0 = bd[s + 1];
-        if (k >= 1 && !kvcd::mbar_wait(&sm.k_empty, (uint32_t)((k - 1) & 1))) { *abort_flag = 1; break; }
+        // Kt / Kh are free once phase A of the previous slot completed and its
+        // epilogue read ln m from Kh (a_ready)
+        if (k >= 1 && (!kvcd::mbar_wait(&sm.k_empty, (uint32_t)((k - 1) & 1)) ||
+                       !kvcd::mbar_wait(&sm.a_ready, (uint32_t)((k - 1) & 1)))) {
+          *abort_flag = 1;
+          break;
+        }
         ++nk;
-        kvcd::mbar_arrive_expect_tx(&sm.k_full, kTileBytes + kvc::kProtoKhBytes);
+        kvcd::mbar_arrive_expect_tx(&sm.k_full, kTileBytes + kvc::kProtoHeadBytes);
         for (int l = 0; l < 8; ++l) {
           int st, cnt;
           leaf_range(l, x0, y0, st, cnt);
           for (int fb = 0; fb < 2; ++fb)
             tma_load_2d(&sm.Kt[fb][l * 2048], &kmap16, fb * 64, (int)(row0 + st), &sm.k_full);
         }
-        kvcd::bulk_g2s(sm.Kh, a.proto + tree * kvc::kProtoBytes, kvc::kProtoKhBytes, &sm.k_full);
+        kvcd::bulk_g2s(sm.Kh, a.proto + tree * kvc::kProtoBytes, kvc::kProtoHeadBytes, &sm.k_full);
         if (k >= 1 && !kvcd::mbar_wait(&sm.v_empty, (uint32_t)((k - 1) & 1))) { *abort_flag = 1; break; }
         ++nv;
         kvcd::mbar_arrive_expect_tx(&sm.v_full, kTileBytes);
@@ -630,7 +655,6 @@ __global__ void __maxnreg__(kNodeMaxRegs)
       const int s = s_begin + k;
       const long long tree = blh * a.S_max + s;
       const int x0 = bd[s], y0 = bd[s + 1];
-      const float* proto_f = reinterpret_cast<const float*>(a.proto + tree * kvc::kProtoBytes);
       // ---- epilogue A: attention of this row to the slot's nodes and its key quarter
       if (!*abort_flag && !kvcd::mbar_wait(&sm.s_full, (uint32_t)(k & 1))) *abort_flag = 1;
       tc_fence_after();
@@ -641,11 +665,10 @@ __global__ void __maxnreg__(kNodeMaxRegs)
         tmem_ld16_nw(tmem + lane_off + 144, d1);
         tmem_ld16_nw(tmem + lane_off + 160, d2);
         tmem_wait();
-        const float* lmv = proto_f + kvc::kProtoLogmOff / 4;
+        const float* lmv = reinterpret_cast<const float*>(sm.Kh + kvc::kProtoLogmOff);
 #pragma unroll
         for (int j = 0; j < 15; ++j) {
-          const float sc = (d0[j] + d1[j] + d2[j]) * a.q_scale2 +
-                           __ldg(lmv + j) * 1.4426950408889634f - l2;
+          const float sc = (d0[j] + d1[j] + d2[j]) * a.q_scale2 + lmv[j] * 1.4426950408889634f - l2;
           ah[j] = rv ? exp2f(sc) : 0.f;
         }
       }
@@ -673,19 +696,16 @@ __global__ void __maxnreg__(kNodeMaxRegs)
           for (int u = 0; u < 2; ++u)
             av[u] = (rv && t + u < cntl) ? exp2f(v[t + u] * a.q_scale2 - l2) : 0.f;
           sacc += av[0] + av[1];
-          uint32_t h[3][2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const __nv_bfloat16 p0 = __float2bfloat16_rn(av[u]);
-            const float r1 = av[u] - __bfloat162float(p0);
-            const __nv_bfloat16 p1 = __float2bfloat16_rn(r1);
-            const __nv_bfloat16 p2 = __float2bfloat16_rn(r1 - __bfloat162float(p1));
-            h[0][u] = __bfloat16_as_ushort(p0);
-            h[1][u] = __bfloat16_as_ushort(p1);
-            h[2][u] = __bfloat16_as_ushort(p2);
-          }
-#pragma unroll
-          for (int pt = 0; pt < 3; ++pt) pk[pt][t >> 1] = h[pt][0] | (h[pt][1] << 16);
+          // a = p0 + p1 + p2 in bf16 pairs (element t in the low half)
+          const __nv_bfloat162 p0 = __floats2bfloat162_rn(av[0], av[1]);
+          const float2 f0 = __bfloat1622float2(p0);
+          const float r0 = av[0] - f0.x, r1 = av[1] - f0.y;
+          const __nv_bfloat162 p1 = __floats2bfloat162_rn(r0, r1);
+          const float2 f1 = __bfloat1622float2(p1);
+          const __nv_bfloat162 p2 = __floats2bfloat162_rn(r0 - f1.x, r1 - f1.y);
+          pk[0][t >> 1] = *reinterpret_cast<const uint32_t*>(&p0);
+          pk[1][t >> 1] = *reinterpret_cast<const uint32_t*>(&p1);
+          pk[2][t >> 1] = *reinterpret_cast<const uint32_t*>(&p2);
         }
         lsum[hq] = sacc;
 #pragma unroll
@@ -722,7 +742,6 @@ __global__ void __maxnreg__(kNodeMaxRegs)
           an_fin[i] = v;
         }
       }
-      named_bar(5, kEpiWarps * 32);                  // every row read its leaf masses
       if (!*abort_flag && !kvcd::mbar_wait(&sm.vh_full, (uint32_t)(k & 1))) *abort_flag = 1;
       // ---- epilogue B: 32 features of every node
 #pragma unroll
@@ -756,25 +775,32 @@ __global__ void __maxnreg__(kNodeMaxRegs)
           uu0 = fma2(ua, ua, uu0);
           uu1 = fma2(ub, ub, uu1);
         }
-        sm.part[j & 1][g][rl] = make_float2(hsum2(dd0) + hsum2(dd1), hsum2(uu0) + hsum2(uu1));
-        named_bar(qbar, 128);
-        if (g == (j & 3)) {                            // finisher of node j for these rows
-          float dd = 0.f, uu = 0.f;
+        // partials of nodes 2t, 2t+1 go to the spare TMEM columns of pair parity
+        // t & 1 (one barrier per pair; the finisher adds them in group order)
+        tmem_st2(tmem + lane_off + part_col(j, g), hsum2(dd0) + hsum2(dd1), hsum2(uu0) + hsum2(uu1));
+        if ((j & 1) == 1 || j == 14) {
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          tc_fence_before();
+          named_bar(qbar, 128);
+          tc_fence_after();
 #pragma unroll
-          for (int gg = 0; gg < 4; ++gg) {
-            const float2 pp = sm.part[j & 1][gg][rl];
-            dd += pp.x;
-            uu += pp.y;
-          }
-          float st[4];
-          st[0] = rv ? fabsf(an_fin[j >> 2] - ah[j]) : 0.f;
-          st[1] = rv ? an_fin[j >> 2] : 0.f;
-          st[2] = rv ? sqrtf(dd) : 0.f;
-          st[3] = rv ? sqrtf(uu) : 0.f;
+          for (int jj = (j == 14 ? 14 : j - 1); jj <= j; ++jj) {
+            if (g == (jj & 3)) {                         // finisher of node jj for these rows
+              float pp[8];
+              tld8(tmem + lane_off + part_col(jj, 0), pp);
+              const float ddt = (pp[0] + pp[2]) + (pp[4] + pp[6]);
+              const float uut = (pp[1] + pp[3]) + (pp[5] + pp[7]);
+              float st[4];
+              st[0] = rv ? fabsf(an_fin[jj >> 2] - ah[jj]) : 0.f;
+              st[1] = rv ? an_fin[jj >> 2] : 0.f;
+              st[2] = rv ? sqrtf(ddt) : 0.f;
+              st[3] = rv ? sqrtf(uut) : 0.f;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float t = kvcd::warp_sum(st[e]);
-            if (lane == 0) sm.red[k & 1][q][j][e] = t;
+              for (int e = 0; e < 4; ++e) {
+                const float t = kvcd::warp_sum(st[e]);
+                if (lane == 0) sm.red[k & 1][q][jj][e] = t;
+              }
+            }
           }
         }
       }

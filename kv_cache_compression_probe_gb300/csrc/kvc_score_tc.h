@@ -11,13 +11,16 @@ enum { kTcRowstatsProbes = 0, kTcRowstatsSeeds = 1, kTcFeats = 2, kTcProp = 3 };
 
 // Per-slot prototype record written by the prototype kernel and read by the
 // tensor-core node kernel: k^ split into three bf16 parts (rows 16*part + node,
-// 128-byte-swizzled K-major, two 64-feature blocks of 48 rows), v^ (fp32),
-// ln m and the node relevance sums.
+// 128-byte-swizzled K-major, two 64-feature blocks of 48 rows), ln m and the
+// node relevance sums (16 floats each; these three travel in one copy), then
+// v^ (fp32).
 constexpr int kProtoKhBytes = 2 * 48 * 128;        // 12288
-constexpr int kProtoVhOff = kProtoKhBytes;          // float[15][128]
-constexpr int kProtoLogmOff = kProtoVhOff + 15 * 128 * 4;
-constexpr int kProtoRvOff = kProtoLogmOff + 16 * 4;
+constexpr int kProtoLogmOff = kProtoKhBytes;        // float[16]
+constexpr int kProtoRvOff = kProtoLogmOff + 16 * 4; // float[16]
+constexpr int kProtoHeadBytes = kProtoRvOff + 16 * 4;   // 12416: k^ parts, ln m, Rv
+constexpr int kProtoVhOff = kProtoHeadBytes;        // float[15][128]
 constexpr int kProtoBytes = 20480;
+static_assert(kProtoVhOff % 16 == 0 && kProtoVhOff + 15 * 128 * 4 <= kProtoBytes, "proto record");
 
 struct ProbeTcArgs {
   const int32_t* ctx_len;
