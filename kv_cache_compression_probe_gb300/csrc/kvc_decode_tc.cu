@@ -4,8 +4,9 @@
 // bias; new tokens are appended with multiplicity one).
 //
 // A plan kernel lists the work: every (b,l,h) with len entries contributes
-// max(1, ceil(len / 512)) chunks.  One CTA of the attention kernel takes one
-// chunk of up to 4 tiles of 128 cached entries:
+// max(1, ceil(len / 512)) chunks.  The attention kernel is persistent (two
+// CTAs per SM loop over the list); one work item is one chunk of up to 4
+// tiles of 128 cached entries:
 //   QK   S^T[128 keys x 16] = K_tile x Q^T: the K tile arrives by TMA in
 //        128-byte-swizzled K-major form (A operand), the G query heads are the
 //        K-major B operand padded to 16 rows; fp32 accumulators in TMEM, one
@@ -16,11 +17,12 @@
 //        row sums add the rounded values, so the normalisation matches P.
 //   PV   O^T[128 features x 16] += V_tile^T x P: the V tile is read as an
 //        MN-major A operand straight from the TMA buffer.
-// K and V tiles share one 2-slot ring (load order K0..Kn-1, V0..Vn-1), so a
-// CTA needs 86 KB of shared memory and two CTAs fit on an SM.  The chunk
-// partial (max, sum, O) goes to the workspace; the last CTA of an (l,h) to
-// arrive merges the partials with the new token, appends it and increments
-// len (every CTA of that (l,h) has read len by then).
+// K and V tiles share one 2-slot ring (load order K0..Kn-1, V0..Vn-1 per item,
+// items back to back; an item's 16 query rows arrive by TMA with its first
+// tile), so a CTA needs 90 KB of shared memory and two CTAs fit on an SM.  The
+// chunk partial (max, sum, O) goes to the workspace.  A merge kernel (one CTA
+// per (b,l,h)) then combines the partials with the new token in log-sum-exp
+// form, appends the token and increments len.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -172,46 +174,51 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(kvc::DecodeTcArgs a, 
 struct DecSmem {
   alignas(1024) unsigned char ring[kSlots][2][kBlock];      // K or V tile per slot
   alignas(1024) unsigned char Pt[kChunkTc / 64][16 * 128];  // P: 16 head rows x 512 keys, K-major
-  alignas(1024) unsigned char Qt[2][16 * 128];              // Q: 16 head rows x 128 features
+  alignas(1024) unsigned char Qt[2][2][16 * 128];           // Q of alternate items, per 64-feature block
   float red_m[4][8], red_l[4][8];
-  float m[8], l[8], s_new[8];
+  float m[8], l[8];
   uint64_t full[kSlots], empty[kSlots], s_ready, p_ready, o_ready, mma_done;
   uint32_t tmem;
   int abort;
-  int last;
 };
 
+// One work-list entry: chunk c of (b,l,h) blh.
+struct Item {
+  int blh, c, len, nchunks, nvalid, ntiles;
+  int64_t off;
+};
+__device__ __forceinline__ Item item_at(const kvc::DecodeTcArgs& a, int idx) {
+  Item it;
+  const uint32_t w = a.items[idx];
+  it.blh = (int)(w & 0xFFFFu);
+  it.c = (int)(w >> 16);
+  it.len = __ldcg(a.len_lh + it.blh);      // read before this (l,h)'s last chunk arrives
+  it.off = a.off_lh[it.blh];
+  it.nchunks = it.len > 0 ? (it.len + kChunkTc - 1) / kChunkTc : 1;
+  it.nvalid = max(0, min(kChunkTc, it.len - it.c * kChunkTc));
+  it.ntiles = (it.nvalid + kTileRows - 1) / kTileRows;
+  return it;
+}
+
+// Persistent: CTA x takes work items x, x + gridDim.x, ...  The producer streams
+// K then V tiles of consecutive items through the 2-slot ring (the item's Q
+// rides on its first tile's barrier), the MMA warp runs QK(i), waits for P(i),
+// runs PV(i), and the epilogue warps do softmax(i), then the chunk partial and,
+// for the last chunk of an (l,h), the merge while the next item streams in.
+// Registers are reserved per group of 4 warps, so the 6-warp CTA counts as 8:
+// two CTAs per SM need <= 65536 / (2 * 256) = 128 registers a thread.
 template <int G>
-__global__ void __launch_bounds__(kThreadsTc, 2)
+__global__ void __launch_bounds__(256, 2)
     decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                     kvc::DecodeTcArgs a) {
+                     const __grid_constant__ CUtensorMap qmap, kvc::DecodeTcArgs a) {
   extern __shared__ __align__(1024) unsigned char dec_raw[];
-  if ((int)blockIdx.x >= *a.n_items) return;
+  const int n_items = *a.n_items;
+  if ((int)blockIdx.x >= n_items) return;
   DecSmem& sm = *reinterpret_cast<DecSmem*>((reinterpret_cast<uintptr_t>(dec_raw) + 1023) &
                                             ~uintptr_t(1023));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t item = a.items[blockIdx.x];
-  const int blh = (int)(item & 0xFFFFu), c = (int)(item >> 16);
-  const int len = a.len_lh[blh];                     // checked by the plan
-  const int nchunks = len > 0 ? (len + kChunkTc - 1) / kChunkTc : 1;
-  const int e0 = c * kChunkTc;
-  const int nvalid = max(0, min(kChunkTc, len - e0));
-  const int ntiles = (nvalid + kTileRows - 1) / kTileRows;
-  const int64_t off = a.off_lh[blh];
-  const int h = blh % a.H;
-  const int64_t bl = blh / a.H;                      // b * L + l
-  const __nv_bfloat16* qp = static_cast<const __nv_bfloat16*>(a.q) + (bl * a.H * G + (int64_t)h * G) * kD;
-  const float* lm = a.logm + off + e0;
 
-  // Q rows into the swizzled B operand (rows >= G zero); P rows >= G zero
-  for (int idx = tid; idx < 16 * 16; idx += kThreadsTc) {
-    const int r = idx >> 4, ch = idx & 15;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < G) v = __ldg(reinterpret_cast<const uint4*>(qp + r * kD) + ch);
-    const int kb = ch >> 3, cc = ch & 7;
-    *reinterpret_cast<uint4*>(&sm.Qt[kb][r * 128 + ((cc ^ (r & 7)) << 4)]) = v;
-  }
-  for (int idx = tid; idx < (16 - G) * 64; idx += kThreadsTc) {
+  for (int idx = tid; idx < (16 - G) * 64; idx += kThreadsTc) {   // P rows >= G stay zero
     const int r = G + (idx >> 6), kb = (idx >> 3) & 7, ch = idx & 7;
     *reinterpret_cast<uint4*>(&sm.Pt[kb][r * 128 + ch * 16]) = make_uint4(0, 0, 0, 0);
   }
@@ -239,171 +246,194 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
   fence_after();
   const uint32_t tmem = sm.tmem;
   volatile int* abort_flag = &sm.abort;
-  const int y_base = (int)(off + e0);
   int last_issue[kSlots] = {-1, -1};                 // producer: last load per slot
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      int t = 0;                                     // tile loads issued so far
       bool ok = true;
-      for (int i = 0; i < 2 * ntiles; ++i) {
-        const int s = i & 1;
-        if (i >= kSlots && !kvcd::mbar_wait(&sm.empty[s], (uint32_t)(((i >> 1) - 1) & 1))) {
-          ok = false;
-          break;
+      int li = 0;
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++li) {
+        const Item it = item_at(a, idx);
+        const int y_base = (int)(it.off + it.c * kChunkTc);
+        for (int i = 0; i < 2 * it.ntiles; ++i, ++t) {
+          const int s = t & 1;
+          if (t >= kSlots && !kvcd::mbar_wait(&sm.empty[s], (uint32_t)(((t >> 1) - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          if (*abort_flag) { ok = false; break; }
+          const bool is_k = i < it.ntiles;
+          const int tt = is_k ? i : i - it.ntiles;
+          kvcd::mbar_arrive_expect_tx(&sm.full[s], kTileBytes + (i == 0 ? 2u * 16 * 128 : 0u));
+          tma2d(sm.ring[s][0], is_k ? &kmap : &vmap, 0, y_base + tt * kTileRows, &sm.full[s]);
+          tma2d(sm.ring[s][1], is_k ? &kmap : &vmap, 64, y_base + tt * kTileRows, &sm.full[s]);
+          if (i == 0) {                              // this item's query heads (16 rows)
+            tma2d(sm.Qt[li & 1][0], &qmap, 0, it.blh * G, &sm.full[s]);
+            tma2d(sm.Qt[li & 1][1], &qmap, 64, it.blh * G, &sm.full[s]);
+          }
+          last_issue[s] = t;
         }
-        if (*abort_flag) break;
-        const bool is_k = i < ntiles;
-        const int t = is_k ? i : i - ntiles;
-        kvcd::mbar_arrive_expect_tx(&sm.full[s], kTileBytes);
-        tma2d(sm.ring[s][0], is_k ? &kmap : &vmap, 0, y_base + t * kTileRows, &sm.full[s]);
-        tma2d(sm.ring[s][1], is_k ? &kmap : &vmap, 64, y_base + t * kTileRows, &sm.full[s]);
-        last_issue[s] = i;
       }
       if (!ok) *abort_flag = 1;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (lane 0 issues)
-    if (ntiles > 0) {
-      bool ok = true;
-      for (int i = 0; i < 2 * ntiles && ok; ++i) {
-        const int s = i & 1;
-        if (i == ntiles) {                           // every S block issued: hand over, wait for P
-          if (lane == 0) commit(&sm.s_ready);
-          ok = __all_sync(KVC_FULL_MASK, kvcd::mbar_wait(&sm.p_ready, 0));
-          if (!ok) break;
-        }
-        ok = __all_sync(KVC_FULL_MASK, kvcd::mbar_wait(&sm.full[s], (uint32_t)((i >> 1) & 1)));
+    // s_ready, p_ready and o_ready complete once per item with tiles (ne counts
+    // them on both sides), so neither side can get two phases ahead
+    int t = 0, li = 0, ne = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++li) {
+      const Item it = item_at(a, idx);
+      if (it.ntiles == 0) continue;
+      for (int i = 0; i < it.ntiles; ++i, ++t) {     // S^T blocks
+        const int s = t & 1;
+        ok = __all_sync(KVC_FULL_MASK, kvcd::mbar_wait(&sm.full[s], (uint32_t)((t >> 1) & 1)));
         if (!ok) break;
-        if (i < ntiles) {
-          fence_after();
-          if (lane == 0) {
+        fence_after();
+        if (lane == 0) {
 #pragma unroll
-            for (int k = 0; k < kD / 16; ++k)
-              mma(tmem + i * 16, desc_k(kvcd::smem_u32(sm.ring[s][k >> 2]) + (k & 3) * 32),
-                  desc_k(kvcd::smem_u32(sm.Qt[k >> 2]) + (k & 3) * 32), kIdQK, k > 0 ? 1u : 0u);
-            commit(&sm.empty[s]);
-          }
-        } else {
-          const int t = i - ntiles;
-          const int nrem = nvalid - t * kTileRows;   // valid rows of this V tile
-          if (nrem < kTileRows) {                    // rows past the chunk: zero (P is 0 there)
-            for (int z = lane; z < (kTileRows - nrem) * 16; z += 32) {
-              const int r = nrem + (z >> 4), kb = (z >> 3) & 1, ch = z & 7;
-              *reinterpret_cast<uint4*>(&sm.ring[s][kb][r * 128 + ch * 16]) = make_uint4(0, 0, 0, 0);
-            }
-            kvcd::fence_proxy_async_smem();
-            __syncwarp();
-          }
-          fence_after();
-          if (lane == 0) {
-#pragma unroll
-            for (int k = 0; k < kTileRows / 16; ++k) {
-              const int kk = t * (kTileRows / 16) + k;           // 16-key step within the chunk
-              mma(tmem + 64, desc_mn(kvcd::smem_u32(sm.ring[s][0]) + k * 2048, kBlock),
-                  desc_k(kvcd::smem_u32(sm.Pt[kk >> 2]) + (kk & 3) * 32), kIdPV,
-                  (t > 0 || k > 0) ? 1u : 0u);
-            }
-            commit(&sm.empty[s]);
-          }
+          for (int k = 0; k < kD / 16; ++k)
+            mma(tmem + i * 16, desc_k(kvcd::smem_u32(sm.ring[s][k >> 2]) + (k & 3) * 32),
+                desc_k(kvcd::smem_u32(sm.Qt[li & 1][k >> 2]) + (k & 3) * 32), kIdQK, k > 0 ? 1u : 0u);
+          commit(&sm.empty[s]);
         }
         __syncwarp();
       }
-      if (ok) {
-        if (lane == 0) commit(&sm.o_ready);
-      } else if (lane == 0) {
-        *abort_flag = 1;
+      if (!ok) break;
+      if (lane == 0) commit(&sm.s_ready);
+      ok = __all_sync(KVC_FULL_MASK, kvcd::mbar_wait(&sm.p_ready, (uint32_t)(ne & 1)));
+      if (!ok) break;
+      fence_after();
+      for (int i = 0; i < it.ntiles; ++i, ++t) {     // O^T += V^T P
+        const int s = t & 1;
+        ok = __all_sync(KVC_FULL_MASK, kvcd::mbar_wait(&sm.full[s], (uint32_t)((t >> 1) & 1)));
+        if (!ok) break;
+        const int nrem = it.nvalid - i * kTileRows;  // valid rows of this V tile
+        if (nrem < kTileRows) {                      // rows past the chunk: zero (P is 0 there)
+          for (int z = lane; z < (kTileRows - nrem) * 16; z += 32) {
+            const int r = nrem + (z >> 4), kb = (z >> 3) & 1, ch = z & 7;
+            *reinterpret_cast<uint4*>(&sm.ring[s][kb][r * 128 + ch * 16]) = make_uint4(0, 0, 0, 0);
+          }
+          kvcd::fence_proxy_async_smem();
+          __syncwarp();
+        }
+        fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int k = 0; k < kTileRows / 16; ++k) {
+            const int kk = i * (kTileRows / 16) + k;           // 16-key step within the chunk
+            mma(tmem + 64, desc_mn(kvcd::smem_u32(sm.ring[s][0]) + k * 2048, kBlock),
+                desc_k(kvcd::smem_u32(sm.Pt[kk >> 2]) + (kk & 3) * 32), kIdPV,
+                (i > 0 || k > 0) ? 1u : 0u);
+          }
+          commit(&sm.empty[s]);
+        }
+        __syncwarp();
       }
+      if (!ok) break;
+      if (lane == 0) commit(&sm.o_ready);
+      ++ne;
     }
+    if (!ok && lane == 0) *abort_flag = 1;
   } else {
     // ------------------------------------------------------------ softmax / output warps
     const int ew = warp - 2;
     const int q = warp & 3;                          // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;                   // key row within a tile / feature of O
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
-    float bias[kTiles];
+    int li = 0, ne = 0;                              // items, items with tiles
+    for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++li) {
+      const Item it = item_at(a, idx);
+      const int e0 = it.c * kChunkTc;
+      const float* lm = a.logm + it.off + e0;
+      float bias[kTiles];
 #pragma unroll
-    for (int t = 0; t < kTiles; ++t) {
-      const int e = t * kTileRows + row;
-      bias[t] = e < nvalid ? __ldg(lm + e) * kLog2e : -INFINITY;
-    }
-    float sv[kTiles][G], mh[G], lh[G];
+      for (int t = 0; t < kTiles; ++t) {
+        const int e = t * kTileRows + row;
+        bias[t] = e < it.nvalid ? __ldg(lm + e) * kLog2e : -INFINITY;
+      }
+      float sv[kTiles][G], mh[G], lh[G];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      mh[g] = -INFINITY;
-      lh[g] = 0.f;
-    }
-    if (ntiles > 0) {
-      if (!*abort_flag && !kvcd::mbar_wait(&sm.s_ready, 0)) *abort_flag = 1;
-      fence_after();
+      for (int g = 0; g < G; ++g) {
+        mh[g] = -INFINITY;
+        lh[g] = 0.f;
+      }
+      if (it.ntiles > 0) {
+        if (!*abort_flag && !kvcd::mbar_wait(&sm.s_ready, (uint32_t)(ne & 1))) *abort_flag = 1;
+        fence_after();
 #pragma unroll
-      for (int t = 0; t < kTiles; ++t)
-        if (t < ntiles) tld<G>(tl + t * 16, sv[t]);
-      wait_ld();
+        for (int t = 0; t < kTiles; ++t)
+          if (t < it.ntiles) tld<G>(tl + t * 16, sv[t]);
+        wait_ld();
 #pragma unroll
-      for (int t = 0; t < kTiles; ++t)
+        for (int t = 0; t < kTiles; ++t)
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float s = (t < ntiles && bias[t] != -INFINITY) ? fmaf(sv[t][g], a.scale_log2, bias[t])
-                                                               : -INFINITY;
-          sv[t][g] = s;
-          mh[g] = fmaxf(mh[g], s);
-        }
-    }
+          for (int g = 0; g < G; ++g) {
+            const float sc = (t < it.ntiles && bias[t] != -INFINITY)
+                                 ? fmaf(sv[t][g], a.scale_log2, bias[t]) : -INFINITY;
+            sv[t][g] = sc;
+            mh[g] = fmaxf(mh[g], sc);
+          }
+      }
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      mh[g] = kvcd::warp_max(mh[g]);
-      if (lane == 0) sm.red_m[ew][g] = mh[g];
-    }
-    named_sync(1, 128);
+      for (int g = 0; g < G; ++g) {
+        mh[g] = kvcd::warp_max(mh[g]);
+        if (lane == 0) sm.red_m[ew][g] = mh[g];
+      }
+      named_sync(1, 128);
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-      mh[g] = fmaxf(fmaxf(sm.red_m[0][g], sm.red_m[1][g]), fmaxf(sm.red_m[2][g], sm.red_m[3][g]));
+      for (int g = 0; g < G; ++g)
+        mh[g] = fmaxf(fmaxf(sm.red_m[0][g], sm.red_m[1][g]), fmaxf(sm.red_m[2][g], sm.red_m[3][g]));
 #pragma unroll
-    for (int t = 0; t < kTiles; ++t) {
-      if (t < ntiles) {
-        const int key = t * kTileRows + row;         // within the chunk
-        unsigned char* pb = &sm.Pt[key >> 6][(key & 7) * 2];
-        const int cidx = (key & 63) >> 3;
+      for (int t = 0; t < kTiles; ++t) {
+        if (t < it.ntiles) {
+          const int key = t * kTileRows + row;       // within the chunk
+          unsigned char* pb = &sm.Pt[key >> 6][(key & 7) * 2];
+          const int cidx = (key & 63) >> 3;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float pv = sv[t][g] == -INFINITY ? 0.f : exp2f(sv[t][g] - mh[g]);
-          const __nv_bfloat16 p16 = __float2bfloat16_rn(pv);
-          lh[g] += __bfloat162float(p16);
-          *reinterpret_cast<__nv_bfloat16*>(pb + g * 128 + ((cidx ^ (g & 7)) << 4)) = p16;
+          for (int g = 0; g < G; ++g) {
+            const float pv = sv[t][g] == -INFINITY ? 0.f : exp2f(sv[t][g] - mh[g]);
+            const __nv_bfloat16 p16 = __float2bfloat16_rn(pv);
+            lh[g] += __bfloat162float(p16);
+            *reinterpret_cast<__nv_bfloat16*>(pb + g * 128 + ((cidx ^ (g & 7)) << 4)) = p16;
+          }
         }
       }
-    }
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      lh[g] = kvcd::warp_sum(lh[g]);
-      if (lane == 0) sm.red_l[ew][g] = lh[g];
-    }
-    kvcd::fence_proxy_async_smem();
-    fence_before();
-    named_sync(1, 128);
-    if (ew == 0 && lane < G) {
-      sm.m[lane] = fmaxf(fmaxf(sm.red_m[0][lane], sm.red_m[1][lane]),
-                         fmaxf(sm.red_m[2][lane], sm.red_m[3][lane]));
-      sm.l[lane] = (sm.red_l[0][lane] + sm.red_l[1][lane]) + (sm.red_l[2][lane] + sm.red_l[3][lane]);
-    }
-    __syncwarp();
-    if (lane == 0) kvcd::mbar_arrive(&sm.p_ready);
-    float* part_out = a.partials + ((int64_t)blh * a.n_chunk_max + c) * G * (kD + 2);
-    float ov[G];
+      for (int g = 0; g < G; ++g) {
+        lh[g] = kvcd::warp_sum(lh[g]);
+        if (lane == 0) sm.red_l[ew][g] = lh[g];
+      }
+      kvcd::fence_proxy_async_smem();
+      fence_before();
+      named_sync(1, 128);
+      if (ew == 0 && lane < G) {
+        sm.m[lane] = fmaxf(fmaxf(sm.red_m[0][lane], sm.red_m[1][lane]),
+                           fmaxf(sm.red_m[2][lane], sm.red_m[3][lane]));
+        sm.l[lane] = (sm.red_l[0][lane] + sm.red_l[1][lane]) + (sm.red_l[2][lane] + sm.red_l[3][lane]);
+      }
+      __syncwarp();
+      if (lane == 0 && it.ntiles > 0) kvcd::mbar_arrive(&sm.p_ready);
+      float* part_out = a.partials + ((int64_t)it.blh * a.n_chunk_max + it.c) * G * (kD + 2);
+      float ov[G];
 #pragma unroll
-    for (int g = 0; g < G; ++g) ov[g] = 0.f;
-    if (ntiles > 0) {
-      if (!*abort_flag && !kvcd::mbar_wait(&sm.o_ready, 0)) *abort_flag = 1;
-      fence_after();
-      tld<G>(tl + 64, ov);
-      wait_ld();
-    }
+      for (int g = 0; g < G; ++g) ov[g] = 0.f;
+      if (it.ntiles > 0) {
+        if (!*abort_flag && !kvcd::mbar_wait(&sm.o_ready, (uint32_t)(ne & 1))) *abort_flag = 1;
+        fence_after();
+        tld<G>(tl + 64, ov);
+        wait_ld();
+        fence_before();
+        ++ne;
+      }
 #pragma unroll
-    for (int g = 0; g < G; ++g) part_out[g * (kD + 2) + 2 + row] = ov[g];
-    if (ew == 0 && lane < G) {
-      part_out[lane * (kD + 2)] = sm.m[lane];
-      part_out[lane * (kD + 2) + 1] = sm.l[lane];
+      for (int g = 0; g < G; ++g) part_out[g * (kD + 2) + 2 + row] = ov[g];
+      if (ew == 0 && lane < G) {
+        part_out[lane * (kD + 2)] = sm.m[lane];
+        part_out[lane * (kD + 2) + 1] = sm.l[lane];
+      }
     }
   }
 
@@ -423,52 +453,71 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
   if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(128u)
                  : "memory");
-  if (*abort_flag) {
-    if (tid == 0) kvcd::record_error(a.err, KVC_ETIMEOUT);
-    return;
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) sm.last = (atomicAdd(a.counters + blh, 1) == nchunks - 1);
-  __syncthreads();
-  if (!sm.last) return;
-  __threadfence();
+  if (*abort_flag && tid == 0) kvcd::record_error(a.err, KVC_ETIMEOUT);
+}
 
-  // ---- last chunk of this (l,h): merge with the new token, append, len += 1
+// One CTA (128 G threads, one per output) per (b,l,h): log-sum-exp merge of the
+// chunk partials with the new token (appended with multiplicity one), then the
+// append itself and len += 1 (the attention kernel has read len by now).
+template <int G>
+__global__ void __launch_bounds__(128 * G) decode_merge_kernel(kvc::DecodeTcArgs a) {
+  __shared__ float s_new[G], mM[G], lL[G];
+  const int blh = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int len = a.len_lh[blh];
+  const int64_t off = a.off_lh[blh];
+  if (len < 0 || off < 0 || off + len > a.packed_rows || (len + kChunkTc) / kChunkTc > a.n_chunk_max)
+    return;                                          // reported by the plan
+  const int nch = len > 0 ? (len + kChunkTc - 1) / kChunkTc : 1;
+  const int h = blh % a.H;
+  const int64_t bl = blh / a.H;
+  const __nv_bfloat16* qp = static_cast<const __nv_bfloat16*>(a.q) + (int64_t)blh * G * kD;
   const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(a.k_new) + (int64_t)blh * kD;
   const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(a.v_new) + (int64_t)blh * kD;
-  for (int g = warp; g < G; g += kThreadsTc / 32) {
+  const float* pbase = a.partials + (int64_t)blh * a.n_chunk_max * G * (kD + 2);
+  if (warp < G) {                                    // the new token's score, then max and sum
+    const int g = warp;
     float acc = 0.f;
 #pragma unroll
     for (int f = lane; f < kD; f += 32)
       acc = fmaf(__bfloat162float(qp[g * kD + f]), __bfloat162float(kn[f]), acc);
-    acc = kvcd::warp_sum(acc);
-    if (lane == 0) sm.s_new[g] = acc * a.scale_log2;
+    const float sn = kvcd::warp_sum(acc) * a.scale_log2;
+    float mx = sn;
+    for (int cc = lane; cc < nch; cc += 32) mx = fmaxf(mx, pbase[(cc * G + g) * (kD + 2)]);
+    mx = kvcd::warp_max(mx);
+    float ls = 0.f;
+    for (int cc = lane; cc < nch; cc += 32) {
+      const float mc = pbase[(cc * G + g) * (kD + 2)];
+      if (mc != -INFINITY) ls = fmaf(exp2f(mc - mx), pbase[(cc * G + g) * (kD + 2) + 1], ls);
+    }
+    ls = kvcd::warp_sum(ls);
+    if (lane == 0) {
+      s_new[g] = sn;
+      mM[g] = mx;
+      lL[g] = ls + exp2f(sn - mx);
+    }
   }
   __syncthreads();
-  const float* pbase = a.partials + (int64_t)blh * a.n_chunk_max * G * (kD + 2);
-  __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out) + (bl * a.H * G + (int64_t)h * G) * kD;
-  for (int idx = tid; idx < G * kD; idx += kThreadsTc) {
-    const int g = idx / kD, dd = idx % kD;
-    float M = sm.s_new[g];
-    for (int cc = 0; cc < nchunks; ++cc) M = fmaxf(M, __ldcg(pbase + (cc * G + g) * (kD + 2)));
-    const float fn = exp2f(sm.s_new[g] - M);
-    float acc = fn * __bfloat162float(vn[dd]), l = fn;
-    for (int cc = 0; cc < nchunks; ++cc) {
+  {
+    const int g = tid / kD, dd = tid % kD;
+    const float M = mM[g];
+    float acc = exp2f(s_new[g] - M) * __bfloat162float(vn[dd]);
+#pragma unroll 4
+    for (int cc = 0; cc < nch; ++cc) {
       const float* pc = pbase + (cc * G + g) * (kD + 2);
-      const float mc = __ldcg(pc);
-      const float f = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
-      acc = fmaf(f, __ldcg(pc + 2 + dd), acc);
-      l = fmaf(f, __ldcg(pc + 1), l);
+      const float mc = pc[0];
+      const float o = pc[2 + dd];
+      acc = fmaf(mc == -INFINITY ? 0.f : exp2f(mc - M), o, acc);
     }
-    outp[g * kD + dd] = __float2bfloat16_rn(acc / l);
+    __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out) + (bl * a.H * G + (int64_t)h * G) * kD;
+    outp[g * kD + dd] = __float2bfloat16_rn(acc / lL[g]);
   }
   if (len + 1 <= a.cap_lh[blh] && off + len + 1 <= a.packed_rows) {
     __nv_bfloat16* Kw = static_cast<__nv_bfloat16*>(a.Kp) + (off + len) * kD;
     __nv_bfloat16* Vw = static_cast<__nv_bfloat16*>(a.Vp) + (off + len) * kD;
-    for (int i = tid; i < kD; i += kThreadsTc) {
-      Kw[i] = kn[i];
-      Vw[i] = vn[i];
+    if (tid < kD) {
+      Kw[tid] = kn[tid];
+      Vw[tid] = vn[tid];
     }
     if (tid == 0) {
       a.logm[off + len] = 0.f;
@@ -478,7 +527,6 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
   } else if (tid == 0) {
     kvcd::record_error(a.err, KVC_ECAPACITY);
   }
-  if (tid == 0) a.counters[blh] = 0;
 }
 
 // ---------------------------------------------------------------- host side
@@ -496,35 +544,52 @@ PFN_cuTensorMapEncodeTiled_v12000 enc_fn() {
   return g_enc;
 }
 
-// Tensor maps of the last (K, V, rows) seen, re-encoded only when they change.
+// Tensor maps of the last (K, V, rows) and (q, rows) seen, re-encoded only when
+// they change.
 struct MapCache {
   std::mutex mu;
   const void* K = nullptr;
   const void* V = nullptr;
   int64_t rows = 0;
-  CUtensorMap km, vm;
+  const void* Q = nullptr;
+  int64_t qrows = 0;
+  CUtensorMap km, vm, qm;
 };
 MapCache g_maps;
 
-bool encode(CUtensorMap* m, void* base, int64_t rows) {
+// bf16 [rows, 128] in 128-byte-swizzled boxes of 64 features x box_rows rows.
+bool encode(CUtensorMap* m, const void* base, int64_t rows, int box_rows) {
   cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kTileRows};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return enc_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return enc_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int G>
-cudaError_t launch_attn(const CUtensorMap& km, const CUtensorMap& vm, const kvc::DecodeTcArgs& a,
-                        unsigned grid, cudaStream_t s) {
+cudaError_t launch_attn(const CUtensorMap& km, const CUtensorMap& vm, const CUtensorMap& qm,
+                        const kvc::DecodeTcArgs& a, unsigned grid, cudaStream_t s) {
   const size_t smem = sizeof(DecSmem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<G><<<grid, kThreadsTc, smem, s>>>(km, vm, a);
+  decode_tc_kernel<G><<<grid, kThreadsTc, smem, s>>>(km, vm, qm, a);
+  decode_merge_kernel<G><<<(unsigned)a.blh, 128 * G, 0, s>>>(a);
   return cudaGetLastError();
+}
+
+int sm_count() {
+  static std::once_flag once;
+  static int n = 0;
+  std::call_once(once, [] {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      n = 0;
+  });
+  return n;
 }
 
 }  // namespace
@@ -538,34 +603,45 @@ bool decode_tc_supported(const kvc_params* p, int n_chunk_max) {
 }
 
 int decode_tc_launch(const DecodeTcArgs& a, cudaStream_t s) {
-  CUtensorMap km, vm;
+  CUtensorMap km, vm, qm;
+  const int64_t qrows = a.blh * a.G;
   {
     std::lock_guard<std::mutex> g(g_maps.mu);
     if (g_maps.K != a.Kp || g_maps.V != a.Vp || g_maps.rows != a.packed_rows) {
-      if (!encode(&g_maps.km, a.Kp, a.packed_rows) || !encode(&g_maps.vm, a.Vp, a.packed_rows)) {
-        g_maps.K = g_maps.V = nullptr;
+      g_maps.K = g_maps.V = nullptr;
+      if (!encode(&g_maps.km, a.Kp, a.packed_rows, kTileRows) ||
+          !encode(&g_maps.vm, a.Vp, a.packed_rows, kTileRows))
         return KVC_ECUDA;
-      }
       g_maps.K = a.Kp;
       g_maps.V = a.Vp;
       g_maps.rows = a.packed_rows;
     }
+    if (g_maps.Q != a.q || g_maps.qrows != qrows) {
+      g_maps.Q = nullptr;
+      if (!encode(&g_maps.qm, a.q, qrows, 16)) return KVC_ECUDA;
+      g_maps.Q = a.q;
+      g_maps.qrows = qrows;
+    }
     km = g_maps.km;
     vm = g_maps.vm;
+    qm = g_maps.qm;
   }
   // every (l,h) has max(1, ceil(len / chunk)) <= len / chunk + 1 chunks and the
   // lengths sum to at most the packed extent
   const int64_t bound = std::min<int64_t>(a.blh * a.n_chunk_max, a.packed_rows / kChunkTc + a.blh);
+  const int sms = sm_count();
+  if (sms <= 0) return KVC_ECUDA;
+  const unsigned grid = (unsigned)std::min<int64_t>(bound, 2LL * sms);   // persistent, 2 per SM
   decode_plan_kernel<<<1, 1024, 0, s>>>(a, bound);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_status(e);
   switch (a.G) {
-    case 1: e = launch_attn<1>(km, vm, a, (unsigned)bound, s); break;
-    case 2: e = launch_attn<2>(km, vm, a, (unsigned)bound, s); break;
-    case 4: e = launch_attn<4>(km, vm, a, (unsigned)bound, s); break;
-    default: e = launch_attn<8>(km, vm, a, (unsigned)bound, s); break;
+    case 1: e = launch_attn<1>(km, vm, qm, a, grid, s); break;
+    case 2: e = launch_attn<2>(km, vm, qm, a, grid, s); break;
+    case 4: e = launch_attn<4>(km, vm, qm, a, grid, s); break;
+    default: e = launch_attn<8>(km, vm, qm, a, grid, s); break;
   }
-  count_launch(2);
+  count_launch(3);
   return cuda_status(e);
 }
 

@@ -21,7 +21,7 @@ struct DecodeTcArgs {
   const int64_t* off_lh;
   void* out;
   float* partials;      // [BLH, n_chunk_max, G, d + 2]
-  int32_t* counters;    // [BLH], zero between calls
+  int32_t* counters;    // [BLH], zero between calls (unused by this path)
   uint32_t* items;      // [BLH * n_chunk_max] work list: chunk << 16 | (b,l,h)
   int32_t* n_items;     // [1]
   int64_t packed_rows;  // rows of Kp / Vp / logm / pos
@@ -37,8 +37,8 @@ bool decode_tc_supported(const kvc_params* p, int n_chunk_max);
 // Rows of one split-K chunk (equal to the SIMT kernel's chunk, so both share
 // the workspace layout).
 constexpr int kDecodeTcChunk = 512;
-// Plans the work list and launches the attention kernel (2 launches); the
-// append and the length update happen inside the attention kernel.
+// Plans the work list, runs the attention kernel and the merge kernel (3
+// launches); the merge kernel appends the new token and updates len.
 int decode_tc_launch(const DecodeTcArgs& a, cudaStream_t s);
 
 }  // namespace kvc
