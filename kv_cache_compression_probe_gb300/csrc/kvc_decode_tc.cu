@@ -129,15 +129,18 @@ __device__ __forceinline__ int chunks_of(const kvc::DecodeTcArgs& a, int64_t i) 
 // One CTA: the work list in (b,l,h) order.  A corrupt (b,l,h) gets no chunk
 // (its output and length stay untouched) and is reported.
 __global__ void __launch_bounds__(1024) decode_plan_kernel(kvc::DecodeTcArgs a, int64_t grid_items) {
+  constexpr int kPer = 4;                             // entries kept in registers
   __shared__ long long wsum[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t per = (a.blh + 1023) / 1024;
   const int64_t b0 = min(a.blh, (int64_t)tid * per), b1 = min(a.blh, b0 + per);
+  int nk[kPer];
   long long cnt = 0;
   for (int64_t i = b0; i < b1; ++i) {
     const int n = chunks_of(a, i);
     if (n < 0) kvcd::record_error(a.err, KVC_EDEVICE);
-    else cnt += n;
+    if (i - b0 < kPer) nk[i - b0] = n;
+    cnt += max(n, 0);
   }
   long long incl = cnt;                             // inclusive scan over the block
 #pragma unroll
@@ -164,7 +167,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(kvc::DecodeTcArgs a, 
   }
   long long start = incl - cnt + (warp > 0 ? wsum[warp - 1] : 0);
   for (int64_t i = b0; i < b1; ++i) {
-    const int n = chunks_of(a, i);
+    const int n = i - b0 < kPer ? nk[i - b0] : chunks_of(a, i);
     for (int c = 0; c < n; ++c) a.items[start + c] = ((uint32_t)c << 16) | (uint32_t)i;
     start += max(n, 0);
   }
@@ -461,7 +464,7 @@ __global__ void __launch_bounds__(256, 2)
 // append itself and len += 1 (the attention kernel has read len by now).
 template <int G>
 __global__ void __launch_bounds__(128 * G) decode_merge_kernel(kvc::DecodeTcArgs a) {
-  __shared__ float s_new[G], mM[G], lL[G];
+  __shared__ float s_new[G];
   const int blh = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int len = a.len_lh[blh];
@@ -475,42 +478,55 @@ __global__ void __launch_bounds__(128 * G) decode_merge_kernel(kvc::DecodeTcArgs
   const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(a.k_new) + (int64_t)blh * kD;
   const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(a.v_new) + (int64_t)blh * kD;
   const float* pbase = a.partials + (int64_t)blh * a.n_chunk_max * G * (kD + 2);
-  if (warp < G) {                                    // the new token's score, then max and sum
-    const int g = warp;
+  if (warp < G) {                                    // warp g: the new token's score for head g
     float acc = 0.f;
 #pragma unroll
     for (int f = lane; f < kD; f += 32)
-      acc = fmaf(__bfloat162float(qp[g * kD + f]), __bfloat162float(kn[f]), acc);
+      acc = fmaf(__bfloat162float(qp[warp * kD + f]), __bfloat162float(kn[f]), acc);
     const float sn = kvcd::warp_sum(acc) * a.scale_log2;
-    float mx = sn;
-    for (int cc = lane; cc < nch; cc += 32) mx = fmaxf(mx, pbase[(cc * G + g) * (kD + 2)]);
-    mx = kvcd::warp_max(mx);
-    float ls = 0.f;
-    for (int cc = lane; cc < nch; cc += 32) {
-      const float mc = pbase[(cc * G + g) * (kD + 2)];
-      if (mc != -INFINITY) ls = fmaf(exp2f(mc - mx), pbase[(cc * G + g) * (kD + 2) + 1], ls);
+    if (lane == 0) s_new[warp] = sn;
+  }
+  // thread (g, dd): partials of every chunk, 8 chunks of loads in flight at a
+  // time, rescaled online to the running max (every thread of head g sees the
+  // same maxima, so the sums agree across the head's threads)
+  const int g = tid / kD, dd = tid % kD;
+  float M = -INFINITY, acc = 0.f, l = 0.f;
+  for (int c0 = 0; c0 < nch; c0 += 8) {
+    float mc[8], lc[8], oc[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float* pc = pbase + ((c0 + u) * G + g) * (kD + 2);
+      const bool in = c0 + u < nch;
+      mc[u] = in ? pc[0] : -INFINITY;
+      lc[u] = in ? pc[1] : 0.f;
+      oc[u] = in ? pc[2 + dd] : 0.f;
     }
-    ls = kvcd::warp_sum(ls);
-    if (lane == 0) {
-      s_new[g] = sn;
-      mM[g] = mx;
-      lL[g] = ls + exp2f(sn - mx);
+    float Mb = M;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) Mb = fmaxf(Mb, mc[u]);
+    if (Mb != -INFINITY) {
+      const float sc = M == -INFINITY ? 0.f : exp2f(M - Mb);
+      acc *= sc;
+      l *= sc;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float f = mc[u] == -INFINITY ? 0.f : exp2f(mc[u] - Mb);
+        acc = fmaf(f, oc[u], acc);
+        l = fmaf(f, lc[u], l);
+      }
+      M = Mb;
     }
   }
   __syncthreads();
   {
-    const int g = tid / kD, dd = tid % kD;
-    const float M = mM[g];
-    float acc = exp2f(s_new[g] - M) * __bfloat162float(vn[dd]);
-#pragma unroll 4
-    for (int cc = 0; cc < nch; ++cc) {
-      const float* pc = pbase + (cc * G + g) * (kD + 2);
-      const float mc = pc[0];
-      const float o = pc[2 + dd];
-      acc = fmaf(mc == -INFINITY ? 0.f : exp2f(mc - M), o, acc);
-    }
+    const float sn = s_new[g];
+    const float Mf = fmaxf(M, sn);
+    const float sc = M == -INFINITY ? 0.f : exp2f(M - Mf);
+    const float fn = exp2f(sn - Mf);
+    const float o = fmaf(fn, __bfloat162float(vn[dd]), acc * sc);
+    const float lt = fmaf(l, sc, fn);
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out) + (bl * a.H * G + (int64_t)h * G) * kD;
-    outp[g * kD + dd] = __float2bfloat16_rn(acc / lL[g]);
+    outp[g * kD + dd] = __float2bfloat16_rn(o / lt);
   }
   if (len + 1 <= a.cap_lh[blh] && off + len + 1 <= a.packed_rows) {
     __nv_bfloat16* Kw = static_cast<__nv_bfloat16*>(a.Kp) + (off + len) * kD;
