@@ -132,6 +132,31 @@ def kernel_traffic(name: str, src_files):
 
 
 # --------------------------------------------------------------------------- GPU arm
+def replica_config(cfg, rank: int):
+    """The workload replica `rank` runs: sequences are independent auctions, so
+    every rank compresses and decodes its own seeded batch (no collective on the
+    data path); rank 0 keeps the base seed."""
+    return cfg.replace(seed=cfg.seed + rank) if rank else cfg
+
+
+def max_over_ranks(vals, world: int, device=None):
+    """Element-wise max of `vals` over the ranks of the default process group
+    (the job's time is its slowest rank's); identity for one rank."""
+    if world <= 1:
+        return [float(v) for v in vals]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_throughput(units_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job units per second: every rank processes `units_per_rank` per
+    step and the step takes the slowest rank's time."""
+    return units_per_rank * world / (ms_per_step * 1e-3)
+
+
 def run_gpu(args, cfg, rank, world):
     import torch
     import torch.distributed as dist
@@ -139,6 +164,7 @@ def run_gpu(args, cfg, rank, world):
     from kv_cache_compression_probe_gb300.pipeline import Compressor, pad_bounds
     from synth import workloads as W
 
+    cfg = replica_config(cfg, rank)
     ctx = mp.get_context("spawn")
     with ctx.Pool(min(16, os.cpu_count() or 4)) as pool:
         seqs = make_inputs(cfg, pool)
@@ -254,10 +280,7 @@ def run_gpu(args, cfg, rank, world):
     # max over ranks
     ms = total_ms / args.steps
     e2e = statistics.mean(e2e_ms) if e2e_ms else float("nan")
-    if world > 1:
-        tt = torch.tensor([ms, e2e], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms, e2e = float(tt[0]), float(tt[1])
+    ms, e2e = max_over_ranks([ms, e2e], world, dev)
 
     tokens = sum(s[0] for s in seqs)
     entries = int(comp.len_lh.sum().cpu()) - cfg.L * cfg.H * cfg.B * 0
@@ -286,7 +309,7 @@ def run_gpu(args, cfg, rank, world):
                               "kv_cache_compression_probe_gb300/csrc/kvc_decode_tc.cu"])
     line = {
         "metric": METRIC,
-        "value": tokens * world / (ms * 1e-3),
+        "value": job_throughput(tokens, world, ms),
         "unit": UNIT,
         "n_gpus": world,
         "steps": args.steps,
@@ -315,7 +338,7 @@ def run_gpu(args, cfg, rank, world):
                      "algorithmic_bytes_per_launch": dec_bytes},
         "score_tflops": score_flops / (score_ms * 1e-3) / 1e12,
         "score_tc_frac_of_bf16_peak": score_flops / (score_ms * 1e-3) / 1e12 / tc,
-        "e2e": {"value": tokens * world / (e2e * 1e-3), "unit": UNIT,
+        "e2e": {"value": job_throughput(tokens, world, e2e), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e},
         "gpu_launches": launches // max(1, args.steps) * args.steps,
         "clocks": clk,
