@@ -2,21 +2,19 @@
 // bf16 caches with d = 128 (DistillCache 3.1.1 features; GraceKV "03 Bottom-up
 // value flow": direct probe attention and the two relevance hops).
 //
-// One CTA = one (b,l,h) and a chunk of 128-key tiles.
-//   * The query rows (probe rows, or the hop seeds' values) are written once
-//     into shared memory in the 128-byte-swizzled K-major layout: NT tiles of
-//     128 rows x 128 features (two 64-feature swizzle blocks each).
-//   * One producer thread streams key tiles (128 keys x 128 features) with 2-D
-//     TMA copies (128B swizzle) through a 3-stage ring.
-//   * One MMA thread issues tcgen05.mma (M = 128, N = 128, K = 16, bf16 in,
-//     fp32 out) into a double-buffered TMEM accumulator (2 x NT x 128 columns).
-//   * 4*NT epilogue warps read their rows' scores with tcgen05.ld (warp w owns
-//     TMEM lanes 32*(w%4)..+31 of tile w/4) and run one of three epilogues:
-//       ROWSTATS  online max / sum / sum p*(s - max) per row  -> chunk partials
-//       FEATS     a = 2^(s - LSE); per key: sum a, sum a*H_row, per-head sums
-//                 -> alpha, sigma, H features and r0 = alpha
-//       PROP      per key: sum over seeds of w_s 2^(s - LSE_s)
-//                 -> r = alpha + hop_weight * Prop
+// One CTA = one (b,l,h) and a chunk of 128-key tiles.  The query rows (probe
+// rows, or the hop seeds' values) are written once into shared memory in the
+// 128-byte-swizzled K-major layout; one producer thread streams key tiles (128
+// keys x 128 features) with 2-D TMA copies (128B swizzle) through a 3-stage
+// ring; one MMA thread issues tcgen05.mma (bf16 in, fp32 out) into a
+// double-buffered TMEM accumulator; epilogue warps read it with tcgen05.ld.
+//   ROWSTATS (probe_tc_kernel: rows on the TMEM lanes, S[rows x 128 keys])
+//            max / sum / sum p*(s - max) per row -> chunk partials
+//   FEATS    (probe_tcT_kernel: keys on the lanes, S^T[128 keys x rows])
+//            a = 2^(s - LSE); per key: sum a, sum a*H_row, per-head sums
+//            -> alpha, sigma, H features and r0 = alpha
+//   PROP     (probe_tcT_kernel) per key: sum over seeds of w_s 2^(s - LSE_s)
+//            -> r = alpha + hop_weight * Prop
 // Every mbarrier wait is bounded (KVC_ETIMEOUT); TMEM is always freed.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -70,22 +68,6 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-        "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
                                             uint64_t* bar) {
@@ -100,26 +82,34 @@ __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// After the call lane j holds the warp-wide sum of v[j] (31 shuffles).
-__device__ __forceinline__ float transpose_reduce(float (&v)[32], int lane) {
-#pragma unroll
-  for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
-    const bool upper = (lane & o) != 0;
-#pragma unroll
-    for (int i = 0; i < n / 2; ++i) {
-      const float send = upper ? v[i] : v[i + n / 2];
-      const float keep = upper ? v[i + n / 2] : v[i];
-      v[i] = keep + __shfl_xor_sync(KVC_FULL_MASK, send, o);
-    }
-  }
-  return v[0];
+__device__ __forceinline__ void mma_bf16_i(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
+
+// 16 consecutive TMEM columns of this thread's lane (issue only; see tmem_wait).
+__device__ __forceinline__ void tmem_ld16_nw(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 
 template <int NT>
 struct TcSmem {
   alignas(1024) unsigned char A[NT][2][kBlockBytes];       // query rows, swizzled
   alignas(1024) unsigned char Bt[kStages][2][kBlockBytes]; // key tiles, swizzled
-  float red[4 * NT][kBN][2];                                // epilogue per-warp key sums
   uint64_t full[kStages], empty[kStages], tfull[2], tempty[2];
   uint32_t tmem_base;
   int abort;
@@ -129,6 +119,8 @@ struct TcSmem {
 template <int NT, int MODE>
 __global__ void __launch_bounds__((4 * NT + 2) * 32, 1)
     probe_tc_kernel(const __grid_constant__ CUtensorMap kmap, kvc::ProbeTcArgs a) {
+  static_assert(MODE == kvc::kTcRowstatsProbes || MODE == kvc::kTcRowstatsSeeds,
+                "row-statistics passes only (the per-key passes use probe_tcT_kernel)");
   extern __shared__ __align__(1024) unsigned char tc_raw[];
   // the dynamic shared memory base is aligned up to 1024 bytes by hand
   TcSmem<NT>& sm = *reinterpret_cast<TcSmem<NT>*>(
@@ -142,11 +134,9 @@ __global__ void __launch_bounds__((4 * NT + 2) * 32, 1)
   const int lh = (int)(blh % LH);
   const int n = a.ctx_len[b];
   const int k0 = blockIdx.x * a.chunk_tiles * kBN;
-  const bool seeds = (MODE == kvc::kTcRowstatsSeeds || MODE == kvc::kTcProp);
+  const bool seeds = MODE == kvc::kTcRowstatsSeeds;
   const int rows = seeds ? a.P : a.G * a.P;
-  float* part_out = nullptr;
-  if (MODE == kvc::kTcRowstatsProbes || MODE == kvc::kTcRowstatsSeeds)
-    part_out = a.part + (blh * a.n_chunks + blockIdx.x) * 256 * 3;
+  float* part_out = a.part + (blh * a.n_chunks + blockIdx.x) * 256 * 3;
   if (!a.ok[blh] || k0 >= n) {
     if (part_out && tid < rows) {
       part_out[tid * 3] = -INFINITY; part_out[tid * 3 + 1] = 0.f; part_out[tid * 3 + 2] = 0.f;
@@ -233,105 +223,86 @@ __global__ void __launch_bounds__((4 * NT + 2) * 32, 1)
     }
   } else {
     // ---------------------------------------------------------------- epilogue
+    // Row statistics over the keys: m (running max of s = S log2e / sqrt(d)),
+    // l = sum 2^(s - m) and, for probe rows, u = sum 2^(s - m) (s - m) <= 0.
+    // Per 32-key chunk the terms are summed as a tree and added to l and u with
+    // one compensated (Kahan) step; masks are applied only on boundary chunks.
+    constexpr bool kU = MODE == kvc::kTcRowstatsProbes;
     const int mt = warp >> 2, q = warp & 3;
     const int r = mt * kBM + q * 32 + lane;
     const bool rv = r < rows;
     const int limit = seeds ? n - 1 : n - a.P + (r % a.P);
-    float l2 = 0.f, hr = 0.f, wr = 0.f;
-    if (MODE == kvc::kTcFeats && rv) { l2 = a.lse2[blh * rows + r]; hr = a.hrow[blh * rows + r]; }
-    if (MODE == kvc::kTcProp && rv) { l2 = a.lse2_h[blh * a.P + r]; wr = a.seed_w[blh * a.P + r]; }
     float m = -INFINITY, l = 0.f, u = 0.f, cl = 0.f, cu = 0.f;
     volatile int* abort_flag = &sm.abort;
+    const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
     for (int t = 0; t < ntiles; ++t) {
-      // every epilogue warp runs all ntiles iterations (they share named
-      // barriers); after an abort the waits are skipped and the work is void
+      // every epilogue warp runs all ntiles iterations; after an abort the
+      // waits are skipped and the work is void
       const int bf = t & 1;
       if (!*abort_flag && !kvcd::mbar_wait(&sm.tfull[bf], (uint32_t)((t >> 1) & 1))) *abort_flag = 1;
       tc_fence_after();
       const int kt = k0 + t * kBN;
-#pragma unroll 1
+      const uint32_t col0 = tbase + (uint32_t)((bf * NT + mt) * kBN);
+      float v[32];
+      tmem_ld16_nw(col0, *reinterpret_cast<float(*)[16]>(v));
+      tmem_ld16_nw(col0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      tmem_wait();
+#pragma unroll
       for (int c = 0; c < kBN / 32; ++c) {
-        float v[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)((bf * NT + mt) * kBN + c * 32), v);
+        float vn[32];
+        if (c + 1 < kBN / 32) {                        // next chunk in flight
+          tmem_ld16_nw(col0 + (c + 1) * 32, *reinterpret_cast<float(*)[16]>(vn));
+          tmem_ld16_nw(col0 + (c + 1) * 32 + 16, *reinterpret_cast<float(*)[16]>(vn + 16));
+        }
         const int i0 = kt + c * 32;
-        if (MODE == kvc::kTcRowstatsProbes || MODE == kvc::kTcRowstatsSeeds) {
-          float mx = m;
+        const bool fullc = rv && i0 + 31 < k1 && i0 + 31 <= limit;
+        float mx = m;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          float sv = v[j] * a.q_scale2;
+          if (!fullc) sv = (rv && i0 + j < k1 && i0 + j <= limit) ? sv : -INFINITY;
+          v[j] = sv;
+          mx = fmaxf(mx, sv);
+        }
+        if (mx != -INFINITY) {
+          if (mx > m && m != -INFINITY) {
+            const float sc = exp2f(m - mx);
+            if (kU) { u = sc * (u + (m - mx) * l); cu *= sc; }
+            l *= sc;
+            cl *= sc;
+          }
+          m = mx;
+          float e[32], d[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const bool ok = rv && (i0 + j) < k1 && (i0 + j) <= limit;
-            v[j] = ok ? v[j] * a.q_scale2 : -INFINITY;
-            mx = fmaxf(mx, v[j]);
+            e[j] = exp2f(v[j] - mx);                   // -inf -> 0
+            if (kU) d[j] = (fullc || v[j] != -INFINITY) ? e[j] * (v[j] - mx) : 0.f;
           }
-          if (mx != -INFINITY) {
-            if (mx > m && m != -INFINITY) {
-              const float sc = exp2f(m - mx);
-              u = sc * (u + (m - mx) * l);
-              cu *= sc; l *= sc; cl *= sc;
-            }
-            m = mx;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (v[j] == -INFINITY) continue;
-              const float e = exp2f(v[j] - mx);
-              const float yl = e - cl, tl = l + yl;
-              cl = (tl - l) - yl; l = tl;
-              const float yu = e * (v[j] - mx) - cu, tu = u + yu;
-              cu = (tu - u) - yu; u = tu;
-            }
-          }
-        } else {
-          float w[32];
+          for (int w = 16; w >= 1; w >>= 1)
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const bool ok = rv && (i0 + j) < k1 && (i0 + j) <= limit;
-            const float e = ok ? exp2f(v[j] * a.q_scale2 - l2) : 0.f;
-            v[j] = MODE == kvc::kTcProp ? wr * e : e;
-            w[j] = e * hr;
+            for (int j = 0; j < w; ++j) {
+              e[j] += e[j + w];
+              if (kU) d[j] += d[j + w];
+            }
+          const float yl = e[0] - cl, tl = l + yl;
+          cl = (tl - l) - yl;
+          l = tl;
+          if (kU) {
+            const float yu = d[0] - cu, tu = u + yu;
+            cu = (tu - u) - yu;
+            u = tu;
           }
-          const float sa = transpose_reduce(v, lane);
-          sm.red[warp][c * 32 + lane][0] = sa;
-          if (MODE == kvc::kTcFeats) {
-            const float sh = transpose_reduce(w, lane);
-            sm.red[warp][c * 32 + lane][1] = sh;
-          }
+        }
+        if (c + 1 < kBN / 32) {
+          tmem_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = vn[j];
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) kvcd::mbar_arrive(&sm.tempty[bf]);
-      if (MODE == kvc::kTcFeats || MODE == kvc::kTcProp) {
-        named_bar(1, kEpiWarps * 32);
-        const int et = tid;                             // epilogue thread index
-        if (et < kBN && kt + et < k1) {
-          const int i = kt + et;
-          float sa = 0.f, sh = 0.f;
-          for (int w2 = 0; w2 < kEpiWarps; ++w2) { sa += sm.red[w2][et][0]; sh += sm.red[w2][et][1]; }
-          if (MODE == kvc::kTcFeats) {
-            // per query head: the rows of head g are warps [g*P/32, (g+1)*P/32)
-            const int wpg = a.P / 32;
-            float mean = 0.f, gs[8];
-            for (int g = 0; g < a.G; ++g) {
-              float x = 0.f;
-              for (int w2 = g * wpg; w2 < (g + 1) * wpg; ++w2) x += sm.red[w2][et][0];
-              gs[g] = x / (float)a.P;
-              mean += gs[g];
-            }
-            mean /= (float)a.G;
-            float var = 0.f;
-            for (int g = 0; g < a.G; ++g) { const float dd = gs[g] - mean; var += dd * dd; }
-            var /= (float)a.G;
-            float* f = a.feats + (row0 + i) * 5;
-            const float alpha = sa / (float)rows;
-            f[0] = alpha;
-            f[2] = var;
-            f[3] = sa > 0.f ? sh / sa : 0.f;
-            a.rel[row0 + i] = alpha;
-          } else {
-            a.rel[row0 + i] = a.feats[(row0 + i) * 5] + a.hop_weight * sa;
-          }
-        }
-        named_bar(1, kEpiWarps * 32);
-      }
     }
     if (part_out && rv) { part_out[r * 3] = m; part_out[r * 3 + 1] = l; part_out[r * 3 + 2] = u; }
   }
@@ -341,6 +312,260 @@ __global__ void __launch_bounds__((4 * NT + 2) * 32, 1)
   if (sm.abort && tid == 0) {
     kvcd::record_error(a.err, KVC_ETIMEOUT);
     // bounded wait for the key tiles still in flight (the last kStages issued)
+    for (int t = max(0, sm.issued - kStages); t < sm.issued; ++t)
+      kvcd::mbar_wait(&sm.full[t % kStages], (uint32_t)((t / kStages) & 1), 100000000ull);
+  }
+  tc_fence_after();
+  if (warp == kEpiWarps + 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------- transposed per-key passes
+// FEATS and PROP reduce over the query rows for every key, so here the keys
+// sit on the TMEM lanes: S^T[128 keys x N rows] = K_tile Q^T (K tile = A
+// operand straight from the TMA ring, the query rows = K-major B operand; FEATS
+// N = 256 probe rows as two N = 128 products, PROP N = P <= 128 seed rows).
+// One epilogue thread owns one key and sums over its columns without any
+// cross-thread reduction; FEATS splits the 256 columns between two warp halves
+// that meet once per tile.
+template <int NT>
+struct TcTSmem {
+  alignas(1024) unsigned char A[NT][2][kBlockBytes];       // query rows (B operand), swizzled
+  alignas(1024) unsigned char Bt[kStages][2][kBlockBytes]; // key tiles (A operand), swizzled
+  alignas(16) float col_a[NT * kBM];                        // per row: base-2 LSE (+inf: no row)
+  alignas(16) float col_b[NT * kBM];                        // per row: H (FEATS) or seed weight (PROP)
+  float xch[kBN][9];                                        // FEATS: second half's per-key sums
+  uint64_t full[kStages], empty[kStages], tfull[2], tempty[2];
+  uint32_t tmem_base;
+  int abort;
+  int issued;
+};
+
+template <int MODE, int PN>
+__global__ void __launch_bounds__((MODE == kvc::kTcFeats ? 8 : 4) * 32 + 64, 1)
+    probe_tcT_kernel(const __grid_constant__ CUtensorMap kmap, kvc::ProbeTcArgs a) {
+  constexpr int NT = MODE == kvc::kTcFeats ? 2 : 1;          // 128-row blocks of B
+  constexpr int kEpiWarps = MODE == kvc::kTcFeats ? 8 : 4;
+  constexpr int kThreads = kEpiWarps * 32 + 64;
+  constexpr int kN = MODE == kvc::kTcFeats ? 256 : PN;       // columns per TMEM buffer (PROP: PN >= P)
+  extern __shared__ __align__(1024) unsigned char tt_raw[];
+  TcTSmem<NT>& sm = *reinterpret_cast<TcTSmem<NT>*>(
+      (reinterpret_cast<uintptr_t>(tt_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long blh = blockIdx.y;
+  const int LH = a.L * a.H;
+  const int b = (int)(blh / LH);
+  const int lh = (int)(blh % LH);
+  const int n = a.ctx_len[b];
+  const int k0 = blockIdx.x * a.chunk_tiles * kBN;
+  const int rows = MODE == kvc::kTcProp ? a.P : a.G * a.P;
+  if (!a.ok[blh] || k0 >= n) return;
+  const int k1 = min(n, k0 + a.chunk_tiles * kBN);
+  const int ntiles = (k1 - k0 + kBN - 1) / kBN;
+  const int64_t row0 = kvcd::seq_token_base(a.ctx_len, b, LH) + (int64_t)lh * n;
+
+  for (int idx = tid; idx < NT * kBM * 16; idx += kThreads) {
+    const int r = idx >> 4, c = idx & 15;
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (r < rows) {
+      const __nv_bfloat16* src;
+      if (MODE == kvc::kTcProp) src = static_cast<const __nv_bfloat16*>(a.V) + (row0 + a.seeds[blh * a.P + r]) * kD;
+      else src = static_cast<const __nv_bfloat16*>(a.Qp) + (blh * rows + r) * kD;
+      val = __ldg(reinterpret_cast<const uint4*>(src) + c);
+    }
+    const int mt = r >> 7, rr = r & 127, kb = c >> 3, cc = c & 7;
+    *reinterpret_cast<uint4*>(&sm.A[mt][kb][rr * 128 + ((cc ^ (rr & 7)) << 4)]) = val;
+  }
+  for (int c = tid; c < NT * kBM; c += kThreads) {
+    const bool in = c < rows;
+    if (MODE == kvc::kTcProp) {
+      sm.col_a[c] = in ? a.lse2_h[blh * a.P + c] : INFINITY;
+      sm.col_b[c] = in ? a.seed_w[blh * a.P + c] : 0.f;
+    } else {
+      sm.col_a[c] = in ? a.lse2[blh * rows + c] : INFINITY;
+      sm.col_b[c] = in ? a.hrow[blh * rows + c] : 0.f;
+    }
+  }
+  kvcd::fence_proxy_async_smem();
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) { kvcd::mbar_init(&sm.full[s], 1); kvcd::mbar_init(&sm.empty[s], 1); }
+    for (int s = 0; s < 2; ++s) { kvcd::mbar_init(&sm.tfull[s], 1); kvcd::mbar_init(&sm.tempty[s], kEpiWarps); }
+    sm.abort = 0;
+    sm.issued = 0;
+    kvcd::fence_mbar_init();
+  }
+  constexpr uint32_t kCols = 2 * kN <= 128 ? 128u : (2 * kN <= 256 ? 256u : 512u);   // power of 2
+  if (warp == kEpiWarps + 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     kvcd::smem_u32(&sm.tmem_base)), "r"(kCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == kEpiWarps) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % kStages;
+        if (t >= kStages && !kvcd::mbar_wait(&sm.empty[s], (uint32_t)(((t / kStages) - 1) & 1))) {
+          sm.abort = 1;
+          break;
+        }
+        kvcd::mbar_arrive_expect_tx(&sm.full[s], kTileBytes);
+        const int y = (int)(row0 + k0 + t * kBN);
+        tma_load_2d(sm.Bt[s][0], &kmap, 0, y, &sm.full[s]);
+        tma_load_2d(sm.Bt[s][1], &kmap, 64, y, &sm.full[s]);
+        sm.issued = t + 1;
+      }
+    }
+  } else if (warp == kEpiWarps + 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      // M = 128 keys, N = 128 (FEATS, twice) or N = 64 (PROP), both operands K-major
+      constexpr uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                 ((uint32_t)((MODE == kvc::kTcFeats ? 128 : PN) >> 3) << 17) |
+                                 ((uint32_t)(kBM >> 4) << 24);
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % kStages, bf = t & 1;
+        if (!kvcd::mbar_wait(&sm.full[s], (uint32_t)((t / kStages) & 1))) { sm.abort = 1; break; }
+        if (t >= 2 && !kvcd::mbar_wait(&sm.tempty[bf], (uint32_t)(((t >> 1) - 1) & 1))) {
+          sm.abort = 1;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int nb = 0; nb < NT; ++nb) {
+          const uint32_t d = tmem + (uint32_t)(bf * kN + nb * 128);
+#pragma unroll
+          for (int k = 0; k < kD / 16; ++k) {
+            const uint32_t aoff = kvcd::smem_u32(sm.Bt[s][k >> 2]) + (k & 3) * 32;
+            const uint32_t boff = kvcd::smem_u32(sm.A[nb][k >> 2]) + (k & 3) * 32;
+            mma_bf16_i(d, sw128_desc(aoff), sw128_desc(boff), idesc, k > 0 ? 1u : 0u);
+          }
+        }
+        mma_commit(&sm.empty[s]);
+        mma_commit(&sm.tfull[bf]);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue: thread = key
+    const int half = MODE == kvc::kTcFeats ? (warp >> 2) : 0;
+    const int q = warp & 3;
+    const int kl = q * 32 + lane;                    // key within the tile (TMEM lane)
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    volatile int* abort_flag = &sm.abort;
+    constexpr int kChunks = MODE == kvc::kTcFeats ? 4 : PN / 32;   // 32-column chunks per thread
+    for (int t = 0; t < ntiles; ++t) {
+      const int bf = t & 1;
+      if (!*abort_flag && !kvcd::mbar_wait(&sm.tfull[bf], (uint32_t)((t >> 1) & 1))) *abort_flag = 1;
+      tc_fence_after();
+      const int key = k0 + t * kBN + kl;
+      const bool kvalid = key < k1;
+      // FEATS: probe row c sees keys <= n - P + (c % P), i.e. c % P >= thr
+      const int thr = MODE == kvc::kTcFeats ? key - (n - a.P) : 0;
+      const bool full_cols = kvalid && thr <= 0;
+      float gs[8], sh = 0.f, acc = 0.f;
+#pragma unroll
+      for (int g = 0; g < 8; ++g) gs[g] = 0.f;
+      float v[32];
+      tmem_ld16_nw(tmem + lane_off + (uint32_t)(bf * kN + half * 128), *reinterpret_cast<float(*)[16]>(v));
+      tmem_ld16_nw(tmem + lane_off + (uint32_t)(bf * kN + half * 128 + 16), *reinterpret_cast<float(*)[16]>(v + 16));
+      tmem_wait();
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        float vn[32];
+        if (c + 1 < kChunks) {                       // next chunk in flight while this one computes
+          const uint32_t col = tmem + lane_off + (uint32_t)(bf * kN + half * 128 + (c + 1) * 32);
+          tmem_ld16_nw(col, *reinterpret_cast<float(*)[16]>(vn));
+          tmem_ld16_nw(col + 16, *reinterpret_cast<float(*)[16]>(vn + 16));
+        }
+        const int cb = half * 128 + c * 32;          // first column of the chunk
+        const float4* ca = reinterpret_cast<const float4*>(&sm.col_a[cb]);
+        const float4* cbv = reinterpret_cast<const float4*>(&sm.col_b[cb]);
+        float cs = 0.f, chs = 0.f;
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 la = ca[j4], lb = cbv[j4];
+          const float las[4] = {la.x, la.y, la.z, la.w}, lbs[4] = {lb.x, lb.y, lb.z, lb.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = j4 * 4 + u;
+            float e = exp2f(fmaf(v[j], a.q_scale2, -las[u]));
+            if (!full_cols) {
+              const bool ok = kvalid && (MODE == kvc::kTcProp || ((cb + j) % a.P) >= thr);
+              e = ok ? e : 0.f;
+            }
+            if (MODE == kvc::kTcFeats) {
+              cs += e;
+              chs = fmaf(e, lbs[u], chs);
+            } else {
+              acc = fmaf(lbs[u], e, acc);
+            }
+          }
+        }
+        if (MODE == kvc::kTcFeats) {
+          const int head = cb / a.P;                 // P % 32 == 0: one head per chunk
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            if (g == head) gs[g] += cs;
+          sh += chs;
+        }
+        if (c + 1 < kChunks) {
+          tmem_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = vn[j];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) kvcd::mbar_arrive(&sm.tempty[bf]);
+      if (MODE == kvc::kTcProp) {
+        if (kvalid) a.rel[row0 + key] = a.feats[(row0 + key) * 5] + a.hop_weight * acc;
+      } else {
+        if (half == 1) {
+#pragma unroll
+          for (int g = 0; g < 8; ++g) sm.xch[kl][g] = gs[g];
+          sm.xch[kl][8] = sh;
+        }
+        named_bar(1 + q, 64);                        // warps q and q + 4 hold the same keys
+        if (half == 0 && kvalid) {
+          float sa = 0.f, mean = 0.f;
+#pragma unroll
+          for (int g = 0; g < 8; ++g) gs[g] += sm.xch[kl][g];
+          sh += sm.xch[kl][8];
+#pragma unroll
+          for (int g = 0; g < 8; ++g) sa += gs[g];
+          const float invP = 1.f / (float)a.P;
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            if (g < a.G) mean += gs[g] * invP;
+          mean /= (float)a.G;
+          float var = 0.f;
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            if (g < a.G) { const float dd = gs[g] * invP - mean; var += dd * dd; }
+          var /= (float)a.G;
+          float* f = a.feats + (row0 + key) * 5;
+          const float alpha = sa / (float)rows;
+          f[0] = alpha;
+          f[2] = var;
+          f[3] = sa > 0.f ? sh / sa : 0.f;
+          a.rel[row0 + key] = alpha;
+        }
+        named_bar(1 + q, 64);                        // xch is free for the next tile
+      }
+    }
+  }
+
+  __syncthreads();
+  if (sm.abort && tid == 0) {
+    kvcd::record_error(a.err, KVC_ETIMEOUT);
     for (int t = max(0, sm.issued - kStages); t < sm.issued; ++t)
       kvcd::mbar_wait(&sm.full[t % kStages], (uint32_t)((t / kStages) & 1), 100000000ull);
   }
@@ -403,13 +628,6 @@ constexpr uint32_t kIdescN48 = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(
 constexpr uint32_t kIdescVmn = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
                                ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
 
-__device__ __forceinline__ void mma_bf16_i(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                           uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
 
 // MN-major 128-byte-swizzled operand: 64-feature blocks LBO apart, 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr, uint32_t lbo_bytes) {
@@ -417,20 +635,6 @@ __device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr, uint32_t lbo_b
          ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// 16 consecutive TMEM columns of this thread's lane (issue only; see tmem_wait).
-__device__ __forceinline__ void tmem_ld16_nw(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tmem_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Packed pair of fp32 (a in the low half) and d = a * b + d on both halves.
 __device__ __forceinline__ uint64_t f2(float a, float b) {
@@ -840,6 +1044,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return g_encode;
 }
 
+template <int MODE, int PN>
+int launch_t(const CUtensorMap& map, const kvc::ProbeTcArgs& a, cudaStream_t s) {
+  constexpr int NT = MODE == kvc::kTcFeats ? 2 : 1;
+  constexpr int kThreads = (MODE == kvc::kTcFeats ? 8 : 4) * 32 + 64;
+  const size_t smem = sizeof(TcTSmem<NT>) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(probe_tcT_kernel<MODE, PN>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return kvc::cuda_status(e);
+  dim3 grid(a.n_chunks, (unsigned)((long long)a.B * a.L * a.H));
+  probe_tcT_kernel<MODE, PN><<<grid, kThreads, smem, s>>>(map, a);
+  kvc::count_launch();
+  return kvc::cuda_status(cudaGetLastError());
+}
+
 template <int NT, int MODE>
 int launch(const CUtensorMap& map, const kvc::ProbeTcArgs& a, cudaStream_t s) {
   const size_t smem = sizeof(TcSmem<NT>) + 1024;
@@ -878,11 +1096,11 @@ int probe_tc_pass(int mode, const ProbeTcArgs& a, int64_t total_rows, cudaStream
     case kTcRowstatsProbes:
       return two ? launch<2, kTcRowstatsProbes>(map, a, s) : launch<1, kTcRowstatsProbes>(map, a, s);
     case kTcFeats:
-      return two ? launch<2, kTcFeats>(map, a, s) : launch<1, kTcFeats>(map, a, s);
+      return launch_t<kTcFeats, 0>(map, a, s);
     case kTcRowstatsSeeds:
       return launch<1, kTcRowstatsSeeds>(map, a, s);
     default:
-      return launch<1, kTcProp>(map, a, s);
+      return a.P <= 64 ? launch_t<kTcProp, 64>(map, a, s) : launch_t<kTcProp, 128>(map, a, s);
   }
 }
 
