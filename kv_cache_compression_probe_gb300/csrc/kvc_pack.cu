@@ -5,6 +5,7 @@
 // Prototype of tokens [x, y) (c = y - x):
 //   k~_i = R(-i) k_i              inverse RoPE to a shared frame
 //   kbar = mean k~_i,  kappa = mean cos(k~_i, kbar)
+//          (= (sum k~_i/|k~_i|) . kbar / (c |kbar|), accumulated in one pass)
 //   m    = c * clamp(kappa, 1/c, 1),  stored as ln m (decode adds it to the logit)
 //   k^   = R(pbar) kbar, pbar = (x + y - 1)/2 (table row x + y - 1 of the
 //          half-position RoPE table)
@@ -118,77 +119,91 @@ struct Row {
   static constexpr int VP = D / 64;
 };
 
+// Lane l owns the RoPE pairs (l*VP + t, D/2 + l*VP + t), t < VP = D/64.
 template <typename T, int D>
 __device__ __forceinline__ void load_pairs(const T* row, int lane, float* lo, float* hi) {
   constexpr int VP = D / 64;
+  if constexpr (sizeof(T) == 2 && VP == 2) {            // bf16 x 2 per half: one 4-byte load each
+    const uint32_t a = __ldg(reinterpret_cast<const unsigned int*>(row) + lane);
+    const uint32_t b = __ldg(reinterpret_cast<const unsigned int*>(row + D / 2) + lane);
+    lo[0] = __uint_as_float(a << 16); lo[1] = __uint_as_float(a & 0xFFFF0000u);
+    hi[0] = __uint_as_float(b << 16); hi[1] = __uint_as_float(b & 0xFFFF0000u);
+  } else {
 #pragma unroll
-  for (int t = 0; t < VP; ++t) {
-    lo[t] = kvcd::to_f(row[lane * VP + t]);
-    hi[t] = kvcd::to_f(row[D / 2 + lane * VP + t]);
+    for (int t = 0; t < VP; ++t) {
+      lo[t] = kvcd::to_f(row[lane * VP + t]);
+      hi[t] = kvcd::to_f(row[D / 2 + lane * VP + t]);
+    }
   }
 }
 
+// Prototype of tokens [x, y) in one pass: per token the unrotated key u (one
+// warp reduction for |u|) feeds sum u and sum u/|u|; then
+//   kappa = mean cos(u_i, mean u) = (sum u/|u|) . mean u / (c |mean u|),
+//   v^    = (1 - f) sum(r v) / sum r + f sum v / c   (sum v / c when sum r = 0).
 template <typename T, int D>
 __device__ void write_prototype(const kvc_params& p, const PackArgs& a, const T* Kh, const T* Vh,
                                 const float* rh, int x, int y, int64_t dst, int lane) {
   constexpr int VP = D / 64;
   constexpr int HALF = D / 2;
   const int c = y - x;
-  float kb_lo[VP], kb_hi[VP], vb_lo[VP], vb_hi[VP];
+  float ku_lo[VP], ku_hi[VP], kn_lo[VP], kn_hi[VP], v_lo[VP], v_hi[VP], rv_lo[VP], rv_hi[VP];
 #pragma unroll
-  for (int t = 0; t < VP; ++t) kb_lo[t] = kb_hi[t] = vb_lo[t] = vb_hi[t] = 0.f;
-  // relevance mass of the span (lanes split the tokens)
+  for (int t = 0; t < VP; ++t)
+    ku_lo[t] = ku_hi[t] = kn_lo[t] = kn_hi[t] = v_lo[t] = v_hi[t] = rv_lo[t] = rv_hi[t] = 0.f;
   float rs = 0.f;
-  for (int i = x + lane; i < y; i += 32) rs += rh[i];
-  rs = kvcd::warp_sum(rs);
-  const float f = p.value_floor;
-  // pass 1: mean of the unrotated keys and the weighted value
+#pragma unroll 2
   for (int i = x; i < y; ++i) {
-    float klo[VP], khi[VP], vlo[VP], vhi[VP];
+    float klo[VP], khi[VP], vlo[VP], vhi[VP], cs[VP], sn[VP];
     load_pairs<T, D>(Kh + (int64_t)i * D, lane, klo, khi);
     load_pairs<T, D>(Vh + (int64_t)i * D, lane, vlo, vhi);
     const float* ct = a.cos_tab + (int64_t)(2 * i) * HALF + lane * VP;
     const float* st = a.sin_tab + (int64_t)(2 * i) * HALF + lane * VP;
-    const float w = rs > 0.f ? (1.f - f) * (rh[i] / rs) + f / (float)c : 1.f / (float)c;
+    if constexpr (VP == 2) {
+      const float2 c2 = __ldg(reinterpret_cast<const float2*>(ct));
+      const float2 s2 = __ldg(reinterpret_cast<const float2*>(st));
+      cs[0] = c2.x; cs[1] = c2.y; sn[0] = s2.x; sn[1] = s2.y;
+    } else {
+#pragma unroll
+      for (int t = 0; t < VP; ++t) { cs[t] = __ldg(ct + t); sn[t] = __ldg(st + t); }
+    }
+    const float ri = __ldg(rh + i);
+    float ul[VP], uh[VP], nk2 = 0.f;
 #pragma unroll
     for (int t = 0; t < VP; ++t) {
-      const float cs = __ldg(ct + t), sn = __ldg(st + t);
-      kb_lo[t] += klo[t] * cs + khi[t] * sn;          // R(-i)
-      kb_hi[t] += khi[t] * cs - klo[t] * sn;
-      vb_lo[t] = fmaf(w, vlo[t], vb_lo[t]);
-      vb_hi[t] = fmaf(w, vhi[t], vb_hi[t]);
+      ul[t] = klo[t] * cs[t] + khi[t] * sn[t];           // R(-i)
+      uh[t] = khi[t] * cs[t] - klo[t] * sn[t];
+      nk2 += ul[t] * ul[t] + uh[t] * uh[t];
     }
+    const float nk = sqrtf(kvcd::warp_sum(nk2));
+    const float inv = nk > 0.f ? 1.f / nk : 0.f;
+#pragma unroll
+    for (int t = 0; t < VP; ++t) {
+      ku_lo[t] += ul[t];
+      ku_hi[t] += uh[t];
+      kn_lo[t] = fmaf(ul[t], inv, kn_lo[t]);
+      kn_hi[t] = fmaf(uh[t], inv, kn_hi[t]);
+      v_lo[t] += vlo[t];
+      v_hi[t] += vhi[t];
+      rv_lo[t] = fmaf(ri, vlo[t], rv_lo[t]);
+      rv_hi[t] = fmaf(ri, vhi[t], rv_hi[t]);
+    }
+    rs += ri;
   }
   const float inv_c = 1.f / (float)c;
-  float nb2 = 0.f;
+  float mu2 = 0.f, um = 0.f;
 #pragma unroll
   for (int t = 0; t < VP; ++t) {
-    kb_lo[t] *= inv_c; kb_hi[t] *= inv_c;
-    nb2 += kb_lo[t] * kb_lo[t] + kb_hi[t] * kb_hi[t];
+    ku_lo[t] *= inv_c;
+    ku_hi[t] *= inv_c;
+    mu2 += ku_lo[t] * ku_lo[t] + ku_hi[t] * ku_hi[t];
+    um += kn_lo[t] * ku_lo[t] + kn_hi[t] * ku_hi[t];
   }
-  const float nb = sqrtf(kvcd::warp_sum(nb2));
-  // pass 2: coherence = mean cosine of each unrotated key to the mean
-  float kap = 0.f;
-  for (int i = x; i < y; ++i) {
-    float klo[VP], khi[VP];
-    load_pairs<T, D>(Kh + (int64_t)i * D, lane, klo, khi);
-    const float* ct = a.cos_tab + (int64_t)(2 * i) * HALF + lane * VP;
-    const float* st = a.sin_tab + (int64_t)(2 * i) * HALF + lane * VP;
-    float dot = 0.f, nk2 = 0.f;
-#pragma unroll
-    for (int t = 0; t < VP; ++t) {
-      const float cs = __ldg(ct + t), sn = __ldg(st + t);
-      const float ul = klo[t] * cs + khi[t] * sn, uh = khi[t] * cs - klo[t] * sn;
-      dot += ul * kb_lo[t] + uh * kb_hi[t];
-      nk2 += ul * ul + uh * uh;
-    }
-    dot = kvcd::warp_sum(dot);
-    nk2 = kvcd::warp_sum(nk2);
-    const float den = sqrtf(nk2) * nb;
-    kap += den > 0.f ? dot / den : 0.f;
-  }
-  kap *= inv_c;
+  const float nb = sqrtf(kvcd::warp_sum(mu2));
+  um = kvcd::warp_sum(um);
+  const float kap = nb > 0.f ? um / nb * inv_c : 0.f;
   const float m = (float)c * fminf(fmaxf(kap, inv_c), 1.f);
+  const float f = p.value_floor;
   // rerotate the mean at pbar = (x + y - 1) / 2: half-position table row x + y - 1
   const float* ct = a.cos_tab + (int64_t)(x + y - 1) * HALF + lane * VP;
   const float* st = a.sin_tab + (int64_t)(x + y - 1) * HALF + lane * VP;
@@ -197,10 +212,12 @@ __device__ void write_prototype(const kvc_params& p, const PackArgs& a, const T*
 #pragma unroll
   for (int t = 0; t < VP; ++t) {
     const float cs = __ldg(ct + t), sn = __ldg(st + t);
-    ko[lane * VP + t] = kvcd::from_f<T>(kb_lo[t] * cs - kb_hi[t] * sn);
-    ko[HALF + lane * VP + t] = kvcd::from_f<T>(kb_hi[t] * cs + kb_lo[t] * sn);
-    vo[lane * VP + t] = kvcd::from_f<T>(vb_lo[t]);
-    vo[HALF + lane * VP + t] = kvcd::from_f<T>(vb_hi[t]);
+    ko[lane * VP + t] = kvcd::from_f<T>(ku_lo[t] * cs - ku_hi[t] * sn);
+    ko[HALF + lane * VP + t] = kvcd::from_f<T>(ku_hi[t] * cs + ku_lo[t] * sn);
+    vo[lane * VP + t] = kvcd::from_f<T>(rs > 0.f ? (1.f - f) * (rv_lo[t] / rs) + f * v_lo[t] * inv_c
+                                                 : v_lo[t] * inv_c);
+    vo[HALF + lane * VP + t] = kvcd::from_f<T>(rs > 0.f ? (1.f - f) * (rv_hi[t] / rs) + f * v_hi[t] * inv_c
+                                                        : v_hi[t] * inv_c);
   }
   if (lane == 0) {
     a.logm[dst] = logf(m);
@@ -208,18 +225,26 @@ __device__ void write_prototype(const kvc_params& p, const PackArgs& a, const T*
   }
 }
 
+// Tokens [i0, i0 + cnt) stored bit-exact at rows dst.. (16-byte vector copies:
+// a row is D * sizeof(T) bytes, a multiple of 16).
 template <typename T, int D>
-__device__ __forceinline__ void copy_exact(const PackArgs& a, const T* Kh, const T* Vh, int i,
-                                           int64_t dst, int lane) {
-  T* ko = static_cast<T*>(a.Kp) + dst * D;
-  T* vo = static_cast<T*>(a.Vp) + dst * D;
-  for (int j = lane; j < D; j += 32) {
-    ko[j] = Kh[(int64_t)i * D + j];
-    vo[j] = Vh[(int64_t)i * D + j];
+__device__ __forceinline__ void copy_exact(const PackArgs& a, const T* Kh, const T* Vh, int i0,
+                                           int cnt, int64_t dst, int lane) {
+  constexpr int kRowVec = D * (int)sizeof(T) / 16;
+  const uint4* ks = reinterpret_cast<const uint4*>(Kh + (int64_t)i0 * D);
+  const uint4* vs = reinterpret_cast<const uint4*>(Vh + (int64_t)i0 * D);
+  uint4* kd = reinterpret_cast<uint4*>(static_cast<T*>(a.Kp) + dst * D);
+  uint4* vd = reinterpret_cast<uint4*>(static_cast<T*>(a.Vp) + dst * D);
+  const int nvec = cnt * kRowVec;
+#pragma unroll 4
+  for (int e = lane; e < nvec; e += 32) {
+    const uint4 kv = __ldg(ks + e), vv = __ldg(vs + e);
+    kd[e] = kv;
+    vd[e] = vv;
   }
-  if (lane == 0) {
-    a.logm[dst] = 0.f;
-    a.pos[dst] = (float)i;
+  for (int r = lane; r < cnt; r += 32) {
+    a.logm[dst + r] = 0.f;
+    a.pos[dst + r] = (float)(i0 + r);
   }
 }
 
@@ -245,8 +270,7 @@ __global__ void pack_tree_kernel(kvc_params p, PackArgs a) {
   const float* rh = a.rel + row0;
   const int64_t base = a.off_lh[blh];
   if (s == p.S_max) {                                   // window tokens
-    const int64_t dst0 = base + a.len_lh[blh] - p.W;
-    for (int i = n - p.W; i < n; ++i) copy_exact<T, D>(a, Kh, Vh, i, dst0 + (i - (n - p.W)), lane);
+    copy_exact<T, D>(a, Kh, Vh, n - p.W, p.W, base + a.len_lh[blh] - p.W, lane);
     return;
   }
   if (s >= S) return;
@@ -270,7 +294,8 @@ __global__ void pack_tree_kernel(kvc_params p, PackArgs a) {
       stack[sp++] = 2 * j + 2;
       stack[sp++] = 2 * j + 1;
     } else {
-      for (int i = x; i < y; ++i) copy_exact<T, D>(a, Kh, Vh, i, dst++, lane);
+      copy_exact<T, D>(a, Kh, Vh, x, y - x, dst, lane);
+      dst += y - x;
     }
   }
 }
