@@ -64,7 +64,9 @@ def make_inputs(cfg, pool):
 
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi every 20 ms during the timed region: median SM clock, max clock and
+    any throttle reason seen; only samples stamped inside [begin, end] count."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -72,6 +74,7 @@ class ClockSampler:
         self.proc = None
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
         self.gpu = gpu_index
+        self.t_begin = self.t_end = None
 
     def start(self):
         os.makedirs(os.path.dirname(self.path), exist_ok=True)
@@ -79,14 +82,28 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                 "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+            return
+        t0 = time.time()                              # sampling is live once a line lands
+        while time.time() - t0 < 10.0 and self.proc.poll() is None:
+            self.f.flush()
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.01)
+
+    def begin(self):
+        self.t_begin = time.time()
+
+    def end(self):
+        self.t_end = time.time()
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.05)
         self.proc.terminate()
         self.proc.wait()
         self.f.close()
@@ -94,13 +111,21 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1])); smax.append(float(parts[2]))
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+            except (ValueError, IndexError):
+                ts = None
+            if ts is not None and self.t_begin is not None and self.t_end is not None:
+                if ts < self.t_begin - 0.02 or ts > self.t_end + 0.02:
+                    continue
+            try:
+                sm.append(float(parts[2])); smax.append(float(parts[3]))
             except ValueError:
                 continue
-            for nm, v in zip(names, parts[5:9]):
+            for nm, v in zip(names, parts[6:10]):
                 if v.lower().startswith("active"):
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None,
@@ -132,6 +157,71 @@ def kernel_traffic(name: str, src_files):
 
 
 # --------------------------------------------------------------------------- GPU arm
+def full_cache_decode_ms(p, cfg, seqs, K, V, q_all, kn_all, vn_all, D, dev, stream):
+    """Mean ms per decode step of the same decode call over the uncompressed cache.
+    At budget 1 every token is stored exact with ln m = 0 (the full-budget pack
+    is the input, bit for bit), so the beta = 1 pack is the token layout with
+    the decode reserve after each (b, l, h) range."""
+    import torch
+    from kv_cache_compression_probe_gb300 import kvc
+    LH = cfg.L * cfg.H
+    res = p.decode_reserve
+    lens, tok0 = [], 0
+    for s in seqs:
+        lens += [s[0]] * LH
+    caps = np.asarray(lens, np.int64) + res
+    offs = np.concatenate([[0], np.cumsum(caps)[:-1]])
+    rows = int(caps.sum())
+    Kf = torch.empty((rows, cfg.d), dtype=K.dtype, device=dev)
+    Vf = torch.empty_like(Kf)
+    k = 0
+    for s in seqs:
+        n = s[0]
+        dst = Kf[int(offs[k]):int(offs[k]) + LH * (n + res)].view(LH, n + res, cfg.d)
+        dst[:, :n] = K[tok0:tok0 + LH * n].view(LH, n, cfg.d)
+        dst = Vf[int(offs[k]):int(offs[k]) + LH * (n + res)].view(LH, n + res, cfg.d)
+        dst[:, :n] = V[tok0:tok0 + LH * n].view(LH, n, cfg.d)
+        tok0 += LH * n
+        k += LH
+    pf = type(p).from_buffer_copy(p)
+    pf.packed_rows = rows
+    logm = torch.zeros(rows, dtype=torch.float32, device=dev)
+    pos = torch.zeros(rows, dtype=torch.float32, device=dev)
+    len0 = torch.tensor(lens, dtype=torch.int32, device=dev)
+    cap = torch.tensor(caps.astype(np.int32), device=dev)
+    off = torch.tensor(offs.astype(np.int64), device=dev)
+    ws = kvc.workspace(kvc.KVC_WS_DECODE, pf, dev, zero=True)
+    out = torch.empty(q_all.shape[1:], dtype=q_all.dtype, device=dev)
+    ln = len0.clone()
+
+    def run(steps):
+        for t in range(steps):
+            kvc.kvc_decode_attn(pf, q_all[t], kn_all[t], vn_all[t], None, Kf, Vf, logm, pos, ln,
+                                cap, off, out, ws, stream)
+
+    run(min(3, D))                                       # warm-up
+    ln.copy_(len0)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run(D)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if kvc.kvc_device_error() != 0:
+        raise RuntimeError("device error in the full-cache decode")
+    ms = e0.elapsed_time(e1) / D
+    del Kf, Vf
+    torch.cuda.empty_cache()
+    return ms
+
+
+def full_bytes_ratio(cfg, seqs, avg_entries, D):
+    """Entries the full cache streams per decode step over the compressed one."""
+    full = sum(s[0] for s in seqs) * cfg.L * cfg.H
+    LHB = cfg.L * cfg.H * len(seqs)
+    return (full + LHB * (D + 1) / 2.0) / avg_entries
+
+
 def replica_config(cfg, rank: int):
     """The workload replica `rank` runs: sequences are independent auctions, so
     every rank compresses and decodes its own seeded batch (no collective on the
@@ -242,6 +332,7 @@ def run_gpu(args, cfg, rank, world):
     torch.cuda.synchronize(dev)
     launches0 = kvc.kvc_launch_count()
     t0, t1 = ev(), ev()
+    clocks.begin()
     t0.record(stream)
     step_ms = []
     for _ in range(args.steps):
@@ -253,6 +344,7 @@ def run_gpu(args, cfg, rank, world):
         step_ms.append(s0.elapsed_time(s1))
     t1.record(stream)
     torch.cuda.synchronize(dev)
+    clocks.end()
     launches = kvc.kvc_launch_count() - launches0
     if world > 1:
         dist.barrier()
@@ -276,6 +368,10 @@ def run_gpu(args, cfg, rank, world):
         e2e_ms.append(a0.elapsed_time(a1))
     h2d = sum(t.numel() * t.element_size() for t in (h_K, h_V, h_Q, h_q, h_kn, h_vn))
     d2h = h_out.numel() * h_out.element_size()
+
+    # compressed vs full: the same decode kernel on the beta = 1 pack
+    full_ms = None if args.profile else full_cache_decode_ms(p, cfg, seqs, K, V, q_all, kn_all,
+                                                            vn_all, D, dev, stream)
 
     # max over ranks
     ms = total_ms / args.steps
@@ -329,7 +425,11 @@ def run_gpu(args, cfg, rank, world):
                          "decode_per_step": dec_ms, "decode_total": dec_ms * D},
         "compress_tokens_per_s": tokens / ((score_ms + sel_ms + pack_ms) * 1e-3),
         "decode_gbs": dec_gbs,
-        "decode_vs_full_note": "see profiles/ for the full-cache (beta=1) decode comparison",
+        "decode_full_ms_per_step": full_ms,
+        "decode_speedup_vs_full": (full_ms / dec_ms) if full_ms else None,
+        "decode_full_note": "full = the same decode call on the beta = 1 pack (every token "
+                            "stored exact, ln m = 0); ideal speedup = bytes ratio",
+        "decode_bytes_ratio_full": full_bytes_ratio(cfg, seqs, avg_entries, D),
         "roofline": {"kernel": ("decode_tc_kernel (+ plan)" if dec_tc
                                 else "decode_chunk_kernel (+ commit)"), "bound": "hbm",
                      "achieved": dec_gbs, "peak": hbm, "unit": "GB/s", "frac": dec_gbs / hbm,
@@ -383,37 +483,119 @@ def oracle_sample(cfg, heads, decode_steps):
     return dt, n * len(heads) / (cfg.L * cfg.H)
 
 
+_BLAS_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+
+
+def _oracle_head_job(job):
+    """One (layer, KV head) of the oracle sample, in a worker process: the head is
+    generated untimed, then phase 0 (score, hops, utilities) or phase 1 (pack
+    and decode steps) is timed."""
+    cfg, l, h, phase, payload = job
+    import oracle as O
+    from synth import workloads as W
+    n = int(W.context_lengths(cfg)[0])
+    bounds = W.planted_bounds(cfg, 0, n)
+    counts = W._needle_counts(cfg, 0, n)
+    K, V, Q, _ = W.gen_head(cfg, 0, l, h, n, bounds, int(counts[l * cfg.H + h]))
+    t0 = time.perf_counter()
+    if phase == 0:
+        res = O.score_and_value_head(K, V, Q, n, cfg.P, bounds, 1.0, base=cfg.rope_base)
+        out = (res.util, res.cost, res.r)
+    else:
+        r, taken, steps, seed = payload
+        Kp, Vp, lm, _ = O.pack_head(K, V, r, bounds, taken, n, cfg.W, cfg.rope_base,
+                                    cfg.value_floor)
+        rng = np.random.default_rng(seed)
+        for _ in range(steps):
+            q = rng.standard_normal((cfg.G, cfg.d)); kn = rng.standard_normal(cfg.d)
+            vn = rng.standard_normal(cfg.d)
+            _, Kp, Vp, lm = O.decode_step_head(q, kn, vn, Kp, Vp, lm)
+        out = None
+    return time.perf_counter() - t0, out
+
+
+def oracle_sample_parallel(cfg, heads, decode_steps, workers):
+    """The oracle sample of `oracle_sample` with its per-head phases spread over a
+    spawn process pool (one head per worker); wall = slowest scoring worker +
+    the pooled selection + slowest pack/decode worker."""
+    import oracle as O
+    from synth import workloads as W
+    n = int(W.context_lengths(cfg)[0])
+    bounds = W.planted_bounds(cfg, 0, n)
+    ctx = mp.get_context("spawn")
+    # one BLAS thread per worker (spawned children read these at start)
+    saved = {k: os.environ.get(k) for k in _BLAS_VARS}
+    os.environ.update({k: "1" for k in _BLAS_VARS})
+    try:
+        pool = ctx.Pool(workers)
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    with pool:
+        ph0 = pool.map(_oracle_head_job, [(cfg, l, h, 0, None) for (l, h) in heads])
+        t0 = time.perf_counter()
+        util = np.stack([o[1][0] for o in ph0])[None]
+        cost = np.stack([o[1][1] for o in ph0])[None]
+        r = np.stack([o[1][2] for o in ph0])[None]
+        sel = O.select_sequence(util, cost, r, np.ones((1, len(heads))), bounds, n, cfg.W,
+                                cfg.budget_ratio, cfg.budget_entries_per_lh, cfg.floor_cap_frac,
+                                cfg.floor_cap_tokens)
+        t_sel = time.perf_counter() - t0
+        ph1 = pool.map(_oracle_head_job, [(cfg, l, h, 1, (r[0, k], sel.taken[0, k], decode_steps, k))
+                                          for k, (l, h) in enumerate(heads)])
+    wall = max(o[0] for o in ph0) + t_sel + max(o[0] for o in ph1)
+    return wall, n * len(heads) / (cfg.L * cfg.H)
+
+
 def cpu_baseline(cfg, decode_steps, n_heads=4):
-    heads = [(l, 0) for l in range(n_heads)]
-    secs, toks = oracle_sample(cfg, heads, decode_steps)
-    return {"value": toks / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n_heads} of {cfg.L * cfg.H} (layer, KV head) pairs of the {cfg.n}-token "
-                      f"sequence: score+hops+utilities, floor+auction with the budget pooled "
-                      f"over the sample, pack, {decode_steps} decode steps; single process, "
-                      f"float64 numpy; {secs:.1f} s",
-            "seconds": secs}
+    """The oracle on the host cores: all cores (one (layer, KV head) per worker)
+    as the reported baseline, and one process on `n_heads` heads beside it."""
+    workers = max(1, min(os.cpu_count() or 1, 16, cfg.L * cfg.H))
+    heads = [(k % cfg.L, k // cfg.L) for k in range(workers)]
+    pwall, ptoks = oracle_sample_parallel(cfg, heads, decode_steps, workers)
+    n_heads = min(n_heads, cfg.L * cfg.H)
+    secs, toks = oracle_sample(cfg, [(k % cfg.L, k // cfg.L) for k in range(n_heads)], decode_steps)
+    return {"value": ptoks / pwall, "unit": UNIT, "cores": workers, "kind": "oracle",
+            "sample": f"{workers} of {cfg.L * cfg.H} (layer, KV head) pairs of the {cfg.n}-token "
+                      f"sequence, one per worker process: score+hops+utilities, floor+auction "
+                      f"with the budget pooled over the sample, pack, {decode_steps} decode "
+                      f"steps; float64 numpy; wall {pwall:.1f} s (host reports "
+                      f"{os.cpu_count()} cores)",
+            "seconds": pwall,
+            "single_process": {"value": toks / secs, "cores": os.cpu_count(), "heads": n_heads,
+                               "seconds": secs,
+                               "note": "one process; numpy's BLAS threads use every core"}}
 
 
 def run_reference(args, cfg, rank, world):
+    """The oracle as the reference arm: each step is the all-cores oracle sample
+    (one (layer, KV head) per worker process) on a fresh set of heads."""
     if rank != 0:
         return None
-    vals = []
+    workers = max(1, min(os.cpu_count() or 1, 16, cfg.L * cfg.H))
     t_all = time.perf_counter()
-    for _ in range(args.warmup):
-        oracle_sample(cfg, [(0, 0)], 2)
+    pairs = [(k % cfg.L, (k // cfg.L) % cfg.H) for k in range(cfg.L * cfg.H)]
+    for w in range(args.warmup):
+        oracle_sample_parallel(cfg, pairs[:1], 2, 1)
+    vals = []
     for s in range(args.steps):
-        secs, toks = oracle_sample(cfg, [(s % cfg.L, 0)], args.decode_steps)
-        vals.append((secs, toks))
+        heads = [pairs[(s * workers + k) % len(pairs)] for k in range(workers)]
+        vals.append(oracle_sample_parallel(cfg, heads, args.decode_steps, workers))
     secs = sum(v[0] for v in vals)
     toks = sum(v[1] for v in vals)
     value = toks / secs
+    sample = (f"per step {workers} (layer, KV head) pairs of the {cfg.n}-token sequence, one per "
+              f"worker process (score, hops, utilities, pooled select, pack, "
+              f"{args.decode_steps} decode steps); float64 numpy")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": cfg.name + ": " + cfg.description},
-            "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle", "cores": 1,
-                             "sample": "per step one (layer, KV head) pair of the sequence "
-                                       "(score, hops, utilities, select, pack, decode steps)"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle", "cores": workers,
+                             "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "wall_s": time.perf_counter() - t_all}
