@@ -301,22 +301,21 @@ def run_gpu(args, cfg, rank, world):
         if timed: marks[2].record(stream)
         comp.merge_pack(Kx, Vx, bounds, n_slots)
         if timed: marks[3].record(stream)
-        dmarks = []
-        for t in range(D):
-            if timed:
-                e0 = ev(); e0.record(stream)
-            comp.decode(q_all[t], kn_all[t], vn_all[t], out[t])
-            if timed:
-                e1 = ev(); e1.record(stream); dmarks.append((e0, e1))
+        # D decode steps: one CUDA graph replay (captured on first use) or D calls
+        d0, d1 = ev(), ev()
+        d0.record(stream)
+        nl = comp.decode_many(q_all, kn_all, vn_all, out, graph=not args.eager_decode)
+        d1.record(stream)
+        rec["graph_launches"] = rec.get("graph_launches", 0) + (0 if args.eager_decode else nl)
         if timed:
-            rec["_pending"] = (marks, dmarks)
+            rec["_pending"] = (marks, [(d0, d1)])
 
     def harvest():
         marks, dmarks = rec.pop("_pending")
         rec["score"].append(marks[0].elapsed_time(marks[1]))
         rec["select"].append(marks[1].elapsed_time(marks[2]))
         rec["pack"].append(marks[2].elapsed_time(marks[3]))
-        rec["decode"].append(statistics.mean(a.elapsed_time(b) for a, b in dmarks))
+        rec["decode"].append(sum(a.elapsed_time(b) for a, b in dmarks) / D)
 
     for _ in range(args.warmup):
         step(False)
@@ -331,6 +330,7 @@ def run_gpu(args, cfg, rank, world):
         dist.barrier()
     torch.cuda.synchronize(dev)
     launches0 = kvc.kvc_launch_count()
+    rec["graph_launches"] = 0
     t0, t1 = ev(), ev()
     clocks.begin()
     t0.record(stream)
@@ -345,7 +345,20 @@ def run_gpu(args, cfg, rank, world):
     t1.record(stream)
     torch.cuda.synchronize(dev)
     clocks.end()
-    launches = kvc.kvc_launch_count() - launches0
+    host_launches = kvc.kvc_launch_count() - launches0
+    launches = host_launches + rec["graph_launches"]
+    # the same D decode steps issued one call at a time, for comparison
+    eager_ms = None
+    if not args.eager_decode and not args.profile:
+        comp.select(bounds, n_slots)                      # fresh lengths
+        comp.merge_pack(K, V, bounds, n_slots)
+        torch.cuda.synchronize(dev)
+        x0, x1 = ev(), ev()
+        x0.record(stream)
+        comp.decode_many(q_all, kn_all, vn_all, out, graph=False)
+        x1.record(stream)
+        torch.cuda.synchronize(dev)
+        eager_ms = x0.elapsed_time(x1) / D
     if world > 1:
         dist.barrier()
     total_ms = t0.elapsed_time(t1)
@@ -425,6 +438,7 @@ def run_gpu(args, cfg, rank, world):
                          "decode_per_step": dec_ms, "decode_total": dec_ms * D},
         "compress_tokens_per_s": tokens / ((score_ms + sel_ms + pack_ms) * 1e-3),
         "decode_gbs": dec_gbs,
+        "decode_eager_ms_per_step": eager_ms,
         "decode_full_ms_per_step": full_ms,
         "decode_speedup_vs_full": (full_ms / dec_ms) if full_ms else None,
         "decode_full_note": "full = the same decode call on the beta = 1 pack (every token "
@@ -440,7 +454,9 @@ def run_gpu(args, cfg, rank, world):
         "score_tc_frac_of_bf16_peak": score_flops / (score_ms * 1e-3) / 1e12 / tc,
         "e2e": {"value": job_throughput(tokens, world, e2e), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e},
-        "gpu_launches": launches // max(1, args.steps) * args.steps,
+        "gpu_launches": launches,
+        "gpu_launches_detail": {"issued_by_host": host_launches,
+                                "in_decode_graph_replays": rec["graph_launches"]},
         "clocks": clk,
     }
     return line
@@ -612,6 +628,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the layer count (small profiling cases)")
+    ap.add_argument("--eager-decode", action="store_true",
+                    help="issue the decode steps one call at a time instead of one CUDA graph")
     ap.add_argument("--profile", action="store_true",
                     help="profiling run: no warm-up, one step, no CPU baseline, no e2e leg")
     args = ap.parse_args()

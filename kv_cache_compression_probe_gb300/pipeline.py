@@ -69,6 +69,7 @@ class Compressor:
         self.ws_select = kvc.workspace(kvc.KVC_WS_SELECT, p, device)
         self.ws_pack = kvc.workspace(kvc.KVC_WS_PACK, p, device)
         self.ws_decode = kvc.workspace(kvc.KVC_WS_DECODE, p, device, zero=True)
+        self._graphs = {}
 
     # ---------------------------------------------------------------- calls
     def score(self, K, V, Qp, slot_bounds, n_slots, head_sens=None, stream=None):
@@ -98,6 +99,59 @@ class Compressor:
         kvc.kvc_decode_attn(self.p, q, k_new, v_new, pos_new, self.Kp, self.Vp, self.logm,
                             self.pos, self.len_lh, self.cap_lh, self.off_lh, out, self.ws_decode,
                             stream)
+
+    def decode_many(self, q_all, kn_all, vn_all, out_all, pos_all=None, graph=True):
+        """T = q_all.shape[0] decode steps back to back (step t reads q_all[t],
+        kn_all[t], vn_all[t] and writes out_all[t]).  With graph=True the T calls
+        are captured once per set of buffers into a CUDA graph and replayed, so
+        the steps pay no per-launch host cost; the cache lengths advance on the
+        device either way.  Returns the number of library kernels launched."""
+        if not graph:
+            n0 = kvc.kvc_launch_count()
+            for t in range(q_all.shape[0]):
+                self.decode(q_all[t], kn_all[t], vn_all[t], out_all[t],
+                            None if pos_all is None else pos_all[t])
+            return kvc.kvc_launch_count() - n0
+        key = tuple(x.data_ptr() if x is not None else 0
+                    for x in (q_all, kn_all, vn_all, out_all, pos_all)) + (q_all.shape[0],)
+        g = self._graphs.get(key)
+        if g is None:
+            g = DecodeGraph(self.p, q_all, kn_all, vn_all, pos_all, self.Kp, self.Vp, self.logm,
+                            self.pos, self.len_lh, self.cap_lh, self.off_lh, out_all,
+                            self.ws_decode)
+            self._graphs[key] = g
+        g.replay()
+        return g.launches
+
+
+class DecodeGraph:
+    """T kvc_decode_attn calls captured into one CUDA graph.
+
+    The buffers are baked into the graph: replay() runs the T steps on the
+    current stream over whatever the buffers then hold.  The library's one-time
+    device lookups run before capture (a kvc_device_error call)."""
+
+    def __init__(self, p, q_all, kn_all, vn_all, pos_all, Kp, Vp, logm, pos, len_lh, cap_lh,
+                 off_lh, out_all, ws):
+        dev = q_all.device
+        kvc.kvc_device_error()                       # error-word lookup outside capture
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        self.graph = torch.cuda.CUDAGraph()
+        n0 = kvc.kvc_launch_count()
+        with torch.cuda.graph(self.graph, stream=side):
+            for t in range(q_all.shape[0]):
+                kvc.kvc_decode_attn(p, q_all[t], kn_all[t], vn_all[t],
+                                    None if pos_all is None else pos_all[t], Kp, Vp, logm, pos,
+                                    len_lh, cap_lh, off_lh, out_all[t], ws, side)
+        self.launches = kvc.kvc_launch_count() - n0
+        torch.cuda.current_stream(dev).wait_stream(side)
+        # keep the baked buffers alive as long as the graph
+        self._keep = (q_all, kn_all, vn_all, pos_all, Kp, Vp, logm, pos, len_lh, cap_lh, off_lh,
+                      out_all, ws)
+
+    def replay(self):
+        self.graph.replay()
 
 
 def pad_bounds(bounds_list, S_max: int) -> np.ndarray:
