@@ -346,7 +346,8 @@ def run_gpu(args, cfg, rank, world):
     torch.cuda.synchronize(dev)
     clocks.end()
     host_launches = kvc.kvc_launch_count() - launches0
-    launches = host_launches + rec["graph_launches"]
+    graph_launches = rec["graph_launches"]
+    launches = host_launches + graph_launches
     # the same D decode steps issued one call at a time, for comparison
     eager_ms = None
     if not args.eager_decode and not args.profile:
@@ -456,7 +457,7 @@ def run_gpu(args, cfg, rank, world):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e},
         "gpu_launches": launches,
         "gpu_launches_detail": {"issued_by_host": host_launches,
-                                "in_decode_graph_replays": rec["graph_launches"]},
+                                "in_decode_graph_replays": graph_launches},
         "clocks": clk,
     }
     return line

@@ -325,6 +325,41 @@ def make_workload(cfg: Config, heads: Optional[Sequence[Tuple[int, int]]] = None
     return Workload(cfg=cfg, seqs=seqs, head_sens=np.ones((cfg.L, cfg.H), dtype=np.float32))
 
 
+def _gen_job(job):
+    cfg, b, l, h, n, planted, count = job
+    return b, l, h, gen_head(cfg, b, l, h, n, planted, count)
+
+
+def make_workload_parallel(cfg: Config, processes: int) -> Workload:
+    """``make_workload(cfg)`` with the (b, l, h) heads generated by a spawn
+    process pool (each head has its own seeded stream, so the result is the
+    same array for array)."""
+    import multiprocessing as mp
+    ns = context_lengths(cfg)
+    planted = [planted_bounds(cfg, b, int(ns[b])) for b in range(cfg.B)]
+    counts = [_needle_counts(cfg, b, int(ns[b])) for b in range(cfg.B)]
+    seqs = []
+    for b in range(cfg.B):
+        n = int(ns[b])
+        seqs.append(SeqInputs(n=n, K=np.zeros((cfg.L, cfg.H, n, cfg.d), dtype=np.float32),
+                              V=np.zeros((cfg.L, cfg.H, n, cfg.d), dtype=np.float32),
+                              Qp=np.zeros((cfg.L, cfg.H * cfg.G, cfg.P, cfg.d), dtype=np.float32),
+                              slot_bounds=planted[b].copy(), planted=planted[b], needles=[]))
+    jobs = [(cfg, b, l, h, int(ns[b]), planted[b], int(counts[b][l * cfg.H + h]))
+            for b in range(cfg.B) for l in range(cfg.L) for h in range(cfg.H)]
+    nd_all = {}
+    with mp.get_context("spawn").Pool(max(1, processes)) as pool:
+        for b, l, h, (k, v, q, nd) in pool.imap_unordered(_gen_job, jobs, chunksize=2):
+            s = seqs[b]
+            s.K[l, h] = k
+            s.V[l, h] = v
+            s.Qp[l, h * cfg.G:(h + 1) * cfg.G] = q
+            nd_all[(b, l, h)] = nd
+    for (b, l, h) in sorted(nd_all):                      # the serial order of make_workload
+        seqs[b].needles += nd_all[(b, l, h)]
+    return Workload(cfg=cfg, seqs=seqs, head_sens=np.ones((cfg.L, cfg.H), dtype=np.float32))
+
+
 def decode_inputs(cfg: Config, step: int, B: Optional[int] = None):
     """Decode-step inputs: q [B, L, H*G, d], k_new / v_new [B, L, H, d], N(0, 1)."""
     B = cfg.B if B is None else B

@@ -9,5 +9,6 @@ if ROOT not in sys.path:
 
 
 def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu_full: full-size parity cases (also marked gpu; minutes each)")
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built libkvc.so")
     config.addinivalue_line("markers", "slow: full-size CPU work")

@@ -68,3 +68,11 @@ def test_replicas_draw_distinct_workloads():
     b = W.make_workload(bench.replica_config(cfg, 1))
     assert bench.replica_config(cfg, 0).seed == cfg.seed
     assert not np.array_equal(a.seqs[0].K, b.seqs[0].K)
+
+
+def test_parallel_workload_builder_is_the_serial_one():
+    cfg = W.small_config(B=2, L=2, H=2, n=700, n_min=500)
+    a, b = W.make_workload(cfg), W.make_workload_parallel(cfg, 2)
+    for x, y in zip(a.seqs, b.seqs):
+        assert np.array_equal(x.K, y.K) and np.array_equal(x.V, y.V) and np.array_equal(x.Qp, y.Qp)
+        assert x.needles == y.needles and np.array_equal(x.slot_bounds, y.slot_bounds)
