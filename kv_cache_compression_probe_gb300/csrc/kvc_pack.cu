@@ -152,43 +152,65 @@ __device__ void write_prototype(const kvc_params& p, const PackArgs& a, const T*
   for (int t = 0; t < VP; ++t)
     ku_lo[t] = ku_hi[t] = kn_lo[t] = kn_hi[t] = v_lo[t] = v_hi[t] = rv_lo[t] = rv_hi[t] = 0.f;
   float rs = 0.f;
-#pragma unroll 2
-  for (int i = x; i < y; ++i) {
-    float klo[VP], khi[VP], vlo[VP], vhi[VP], cs[VP], sn[VP];
-    load_pairs<T, D>(Kh + (int64_t)i * D, lane, klo, khi);
-    load_pairs<T, D>(Vh + (int64_t)i * D, lane, vlo, vhi);
-    const float* ct = a.cos_tab + (int64_t)(2 * i) * HALF + lane * VP;
-    const float* st = a.sin_tab + (int64_t)(2 * i) * HALF + lane * VP;
-    if constexpr (VP == 2) {
-      const float2 c2 = __ldg(reinterpret_cast<const float2*>(ct));
-      const float2 s2 = __ldg(reinterpret_cast<const float2*>(st));
-      cs[0] = c2.x; cs[1] = c2.y; sn[0] = s2.x; sn[1] = s2.y;
-    } else {
+  // tokens in groups of kG: every load of a group is issued before any use and
+  // the groups' |u| reductions run interleaved
+  constexpr int kG = 4;
+  for (int i0 = x; i0 < y; i0 += kG) {
+    const int ng = min(kG, y - i0);
+    float klo[kG][VP], khi[kG][VP], vlo[kG][VP], vhi[kG][VP], cs[kG][VP], sn[kG][VP], ri[kG];
 #pragma unroll
-      for (int t = 0; t < VP; ++t) { cs[t] = __ldg(ct + t); sn[t] = __ldg(st + t); }
-    }
-    const float ri = __ldg(rh + i);
-    float ul[VP], uh[VP], nk2 = 0.f;
+    for (int g = 0; g < kG; ++g) {
+      const int i = i0 + (g < ng ? g : 0);              // a repeated row is loaded, not used
+      load_pairs<T, D>(Kh + (int64_t)i * D, lane, klo[g], khi[g]);
+      load_pairs<T, D>(Vh + (int64_t)i * D, lane, vlo[g], vhi[g]);
+      const float* ct = a.cos_tab + (int64_t)(2 * i) * HALF + lane * VP;
+      const float* st = a.sin_tab + (int64_t)(2 * i) * HALF + lane * VP;
+      if constexpr (VP == 2) {
+        const float2 c2 = __ldg(reinterpret_cast<const float2*>(ct));
+        const float2 s2 = __ldg(reinterpret_cast<const float2*>(st));
+        cs[g][0] = c2.x; cs[g][1] = c2.y; sn[g][0] = s2.x; sn[g][1] = s2.y;
+      } else {
 #pragma unroll
-    for (int t = 0; t < VP; ++t) {
-      ul[t] = klo[t] * cs[t] + khi[t] * sn[t];           // R(-i)
-      uh[t] = khi[t] * cs[t] - klo[t] * sn[t];
-      nk2 += ul[t] * ul[t] + uh[t] * uh[t];
+        for (int t = 0; t < VP; ++t) { cs[g][t] = __ldg(ct + t); sn[g][t] = __ldg(st + t); }
+      }
+      ri[g] = __ldg(rh + i);
     }
-    const float nk = sqrtf(kvcd::warp_sum(nk2));
-    const float inv = nk > 0.f ? 1.f / nk : 0.f;
+    float nk2[kG];
 #pragma unroll
-    for (int t = 0; t < VP; ++t) {
-      ku_lo[t] += ul[t];
-      ku_hi[t] += uh[t];
-      kn_lo[t] = fmaf(ul[t], inv, kn_lo[t]);
-      kn_hi[t] = fmaf(uh[t], inv, kn_hi[t]);
-      v_lo[t] += vlo[t];
-      v_hi[t] += vhi[t];
-      rv_lo[t] = fmaf(ri, vlo[t], rv_lo[t]);
-      rv_hi[t] = fmaf(ri, vhi[t], rv_hi[t]);
+    for (int g = 0; g < kG; ++g) {
+      nk2[g] = 0.f;
+#pragma unroll
+      for (int t = 0; t < VP; ++t) {
+        const float ul = klo[g][t] * cs[g][t] + khi[g][t] * sn[g][t];   // R(-i)
+        const float uh = khi[g][t] * cs[g][t] - klo[g][t] * sn[g][t];
+        klo[g][t] = ul;
+        khi[g][t] = uh;
+        nk2[g] += ul * ul + uh * uh;
+      }
     }
-    rs += ri;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int g = 0; g < kG; ++g) nk2[g] += __shfl_xor_sync(KVC_FULL_MASK, nk2[g], o);
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+      if (g < ng) {
+        const float nk = sqrtf(nk2[g]);
+        const float inv = nk > 0.f ? 1.f / nk : 0.f;
+#pragma unroll
+        for (int t = 0; t < VP; ++t) {
+          ku_lo[t] += klo[g][t];
+          ku_hi[t] += khi[g][t];
+          kn_lo[t] = fmaf(klo[g][t], inv, kn_lo[t]);
+          kn_hi[t] = fmaf(khi[g][t], inv, kn_hi[t]);
+          v_lo[t] += vlo[g][t];
+          v_hi[t] += vhi[g][t];
+          rv_lo[t] = fmaf(ri[g], vlo[g][t], rv_lo[t]);
+          rv_hi[t] = fmaf(ri[g], vhi[g][t], rv_hi[t]);
+        }
+        rs += ri[g];
+      }
+    }
   }
   const float inv_c = 1.f / (float)c;
   float mu2 = 0.f, um = 0.f;

@@ -873,10 +873,44 @@ __device__ __forceinline__ void proto_finish(const ScoreArgs& a, float value_flo
   }
 }
 
+// Accumulators of the depth-2, depth-1 and root nodes live in shared memory
+// (lane-indexed, conflict-free); only the current leaf's sums are registers.
+struct ProtoLevels {
+  float v[3][17][32];
+};
+
+__device__ __forceinline__ void acc_to_smem(ProtoLevels& sm, int lvl, const ProtoAcc& s, int lane,
+                                            bool add) {
+  float* f = &sm.v[lvl][0][lane];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    f[(0 + t) * 32] = (add ? f[(0 + t) * 32] : 0.f) + s.k[t];
+    f[(4 + t) * 32] = (add ? f[(4 + t) * 32] : 0.f) + s.u[t];
+    f[(8 + t) * 32] = (add ? f[(8 + t) * 32] : 0.f) + s.v[t];
+    f[(12 + t) * 32] = (add ? f[(12 + t) * 32] : 0.f) + s.rv[t];
+  }
+  f[16 * 32] = (add ? f[16 * 32] : 0.f) + s.r;
+}
+__device__ __forceinline__ ProtoAcc acc_from_smem(const ProtoLevels& sm, int lvl, int lane) {
+  ProtoAcc s;
+  const float* f = &sm.v[lvl][0][lane];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    s.k[t] = f[(0 + t) * 32];
+    s.u[t] = f[(4 + t) * 32];
+    s.v[t] = f[(8 + t) * 32];
+    s.rv[t] = f[(12 + t) * 32];
+  }
+  s.r = f[16 * 32];
+  return s;
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(128) proto_kernel(kvc_params p, ScoreArgs a, unsigned char* proto) {
   static_assert(D == 128 && sizeof(T) == 2, "tensor-core node path is bf16, d = 128");
+  __shared__ ProtoLevels levels[4];
   const int lane = threadIdx.x & 31;
+  ProtoLevels& lv = levels[threadIdx.x >> 5];
   const long long tree = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
   if (tree >= (long long)p.B * p.L * p.H * p.S_max) return;
   const int s = (int)(tree % p.S_max);
@@ -892,58 +926,80 @@ __global__ void __launch_bounds__(128) proto_kernel(kvc_params p, ScoreArgs a, u
   const uint32_t* Vw = reinterpret_cast<const uint32_t*>(static_cast<const T*>(a.V) + row0 * D);
   const float* rel = a.rel + row0;
   unsigned char* out = proto + tree * kvc::kProtoBytes;
-  ProtoAcc leaf, d2, d1, root;
-  d2.zero(); d1.zero(); root.zero();
   for (int L = 0; L < 8; ++L) {
     int x, y;
     node_range(7 + L, x0, y0, x, y);
+    ProtoAcc leaf;
     leaf.zero();
-#pragma unroll 4
-    for (int i = x; i < y; ++i) {
-      const uint32_t klo = __ldg(Kw + (int64_t)i * (D / 2) + lane);
-      const uint32_t khi = __ldg(Kw + (int64_t)i * (D / 2) + 32 + lane);
-      const uint32_t vlo = __ldg(Vw + (int64_t)i * (D / 2) + lane);
-      const uint32_t vhi = __ldg(Vw + (int64_t)i * (D / 2) + 32 + lane);
-      const float2 cs = __ldg(reinterpret_cast<const float2*>(a.cos_tab + (int64_t)(2 * i) * 64) + lane);
-      const float2 sn = __ldg(reinterpret_cast<const float2*>(a.sin_tab + (int64_t)(2 * i) * 64) + lane);
-      const float ri = __ldg(rel + i);
-      const float k0 = __uint_as_float(klo << 16), k1 = __uint_as_float(klo & 0xFFFF0000u);
-      const float k2 = __uint_as_float(khi << 16), k3 = __uint_as_float(khi & 0xFFFF0000u);
-      float u[4];
-      u[0] = k0 * cs.x + k2 * sn.x;
-      u[2] = k2 * cs.x - k0 * sn.x;
-      u[1] = k1 * cs.y + k3 * sn.y;
-      u[3] = k3 * cs.y - k1 * sn.y;
-      const float nk = sqrtf(kvcd::warp_sum(u[0] * u[0] + u[1] * u[1] + u[2] * u[2] + u[3] * u[3]));
-      const float inv = nk > 0.f ? 1.f / nk : 0.f;
-      const float v[4] = {__uint_as_float(vlo << 16), __uint_as_float(vlo & 0xFFFF0000u),
-                          __uint_as_float(vhi << 16), __uint_as_float(vhi & 0xFFFF0000u)};
+    // tokens in groups of 4: all loads of a group first, then four interleaved
+    // |u| reductions
+    for (int i0 = x; i0 < y; i0 += 4) {
+      const int ng = min(4, y - i0);
+      uint32_t kl[4], kh[4], vl[4], vh[4];
+      float2 cs[4], sn[4];
+      float ri[4];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        leaf.k[t] += u[t];
-        leaf.u[t] = fmaf(u[t], inv, leaf.u[t]);
-        leaf.v[t] += v[t];
-        leaf.rv[t] = fmaf(ri, v[t], leaf.rv[t]);
+      for (int g = 0; g < 4; ++g) {
+        const int i = i0 + (g < ng ? g : 0);            // a repeated row is loaded, not used
+        kl[g] = __ldg(Kw + (int64_t)i * (D / 2) + lane);
+        kh[g] = __ldg(Kw + (int64_t)i * (D / 2) + 32 + lane);
+        vl[g] = __ldg(Vw + (int64_t)i * (D / 2) + lane);
+        vh[g] = __ldg(Vw + (int64_t)i * (D / 2) + 32 + lane);
+        cs[g] = __ldg(reinterpret_cast<const float2*>(a.cos_tab + (int64_t)(2 * i) * 64) + lane);
+        sn[g] = __ldg(reinterpret_cast<const float2*>(a.sin_tab + (int64_t)(2 * i) * 64) + lane);
+        ri[g] = __ldg(rel + i);
       }
-      leaf.r += ri;
+      float u[4][4], nk2[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const float k0 = __uint_as_float(kl[g] << 16), k1 = __uint_as_float(kl[g] & 0xFFFF0000u);
+        const float k2 = __uint_as_float(kh[g] << 16), k3 = __uint_as_float(kh[g] & 0xFFFF0000u);
+        u[g][0] = k0 * cs[g].x + k2 * sn[g].x;
+        u[g][2] = k2 * cs[g].x - k0 * sn[g].x;
+        u[g][1] = k1 * cs[g].y + k3 * sn[g].y;
+        u[g][3] = k3 * cs[g].y - k1 * sn[g].y;
+        nk2[g] = u[g][0] * u[g][0] + u[g][1] * u[g][1] + u[g][2] * u[g][2] + u[g][3] * u[g][3];
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int g = 0; g < 4; ++g) nk2[g] += __shfl_xor_sync(KVC_FULL_MASK, nk2[g], o);
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        if (g < ng) {
+          const float nk = sqrtf(nk2[g]);
+          const float inv = nk > 0.f ? 1.f / nk : 0.f;
+          const float v[4] = {__uint_as_float(vl[g] << 16), __uint_as_float(vl[g] & 0xFFFF0000u),
+                              __uint_as_float(vh[g] << 16), __uint_as_float(vh[g] & 0xFFFF0000u)};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            leaf.k[t] += u[g][t];
+            leaf.u[t] = fmaf(u[g][t], inv, leaf.u[t]);
+            leaf.v[t] += v[t];
+            leaf.rv[t] = fmaf(ri[g], v[t], leaf.rv[t]);
+          }
+          leaf.r += ri[g];
+        }
+      }
     }
     proto_finish(a, p.value_floor, 7 + L, x, y, leaf, out, lane);
-    d2.add(leaf);
+    acc_to_smem(lv, 0, leaf, lane, (L & 1) != 0);           // depth 2 = leaf pair
     if (L & 1) {
       const int j2 = 3 + (L >> 1);
       node_range(j2, x0, y0, x, y);
+      const ProtoAcc d2 = acc_from_smem(lv, 0, lane);
       proto_finish(a, p.value_floor, j2, x, y, d2, out, lane);
-      d1.add(d2);
-      d2.zero();
+      acc_to_smem(lv, 1, d2, lane, (L & 3) == 3);            // depth 1 = depth-2 pair
       if ((L & 3) == 3) {
         const int j1 = 1 + (L >> 2);
         node_range(j1, x0, y0, x, y);
+        const ProtoAcc d1 = acc_from_smem(lv, 1, lane);
         proto_finish(a, p.value_floor, j1, x, y, d1, out, lane);
-        root.add(d1);
-        d1.zero();
+        acc_to_smem(lv, 2, d1, lane, L == 7);                // root = depth-1 pair
       }
     }
   }
+  const ProtoAcc root = acc_from_smem(lv, 2, lane);
   proto_finish(a, p.value_floor, 0, x0, y0, root, out, lane);
   // row 15 of every part is padding: zero key, ln m = 0, no relevance
 #pragma unroll
