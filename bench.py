@@ -413,6 +413,18 @@ def run_gpu(args, cfg, rank, world):
     pack_ms = statistics.mean(rec["pack"])
     score_flops = 2.0 * cfg.B * cfg.L * cfg.H * cfg.G * cfg.P * tokens / cfg.B * d * 3 \
         + 2.0 * cfg.B * cfg.L * cfg.H * cfg.P * tokens / cfg.B * d * 2 * cfg.n_hops
+    # merge_pack: every token of a covered slot read once (prototype span or exact
+    # copy) with its relevance, the window rows, and every stored entry written
+    taken_add = comp.taken[..., 0].bool().cpu().numpy()
+    covered = 0
+    for b, sq in enumerate(seqs):
+        slot_len = np.diff(np.asarray(sq[1], np.int64))
+        covered += int((taken_add[b, :, :, :len(slot_len)] * slot_len[None, None, :]).sum())
+    stored = packed_entries
+    pack_bytes = (covered * (2 * d * esz + 4) + cfg.B * cfg.L * cfg.H * cfg.W * 2 * d * esz
+                  + stored * (2 * d * esz + 8))
+    # score: K and V read once, features written (the spec accounting)
+    score_bytes = tokens * cfg.L * cfg.H * (2 * d * esz + 5 * 4)
     dec_tc = p.packed_rows > 0 and cfg.dtype == "bf16" and d == 128   # tensor-core decode
     traffic = kernel_traffic("decode_attn_mistral16k",
                              ["kv_cache_compression_probe_gb300/csrc/kvc_decode.cu",
@@ -451,6 +463,11 @@ def run_gpu(args, cfg, rank, world):
                      "peak_source": src + " hbm_gbs (MEASURED_PEAKS.json)",
                      "traffic": traffic,
                      "algorithmic_bytes_per_launch": dec_bytes},
+        "merge_pack_roofline": {"bound": "hbm", "achieved": pack_bytes / (pack_ms * 1e-3) / 1e9,
+                                "peak": hbm, "unit": "GB/s",
+                                "frac": pack_bytes / (pack_ms * 1e-3) / 1e9 / hbm,
+                                "algorithmic_bytes": pack_bytes},
+        "score_hbm_frac": score_bytes / (score_ms * 1e-3) / 1e9 / hbm,
         "score_tflops": score_flops / (score_ms * 1e-3) / 1e12,
         "score_tc_frac_of_bf16_peak": score_flops / (score_ms * 1e-3) / 1e12 / tc,
         "e2e": {"value": job_throughput(tokens, world, e2e), "unit": UNIT,

@@ -188,15 +188,12 @@ __device__ void write_prototype(const kvc_params& p, const PackArgs& a, const T*
         nk2[g] += ul * ul + uh * uh;
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-      for (int g = 0; g < kG; ++g) nk2[g] += __shfl_xor_sync(KVC_FULL_MASK, nk2[g], o);
+    static_assert(kG == 4, "warp_sum4");
+    kvcd::warp_sum4(nk2, lane);
 #pragma unroll
     for (int g = 0; g < kG; ++g) {
       if (g < ng) {
-        const float nk = sqrtf(nk2[g]);
-        const float inv = nk > 0.f ? 1.f / nk : 0.f;
+        const float inv = nk2[g] > 0.f ? rsqrtf(nk2[g]) : 0.f;
 #pragma unroll
         for (int t = 0; t < VP; ++t) {
           ku_lo[t] += klo[g][t];
@@ -367,14 +364,16 @@ extern "C" int kvc_merge_pack(const kvc_params* p, const int32_t* ctx_len, const
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const long long blh = kvc::lh_count(p);
   pack_count_kernel<<<(unsigned)((blh + 7) / 8), 256, 0, s>>>(*p, a);
+  // one warp per slot tree (+ one per window); 4-warp blocks so a long slot
+  // holds few idle neighbours
   const long long items = blh * (p->S_max + 1);
-  const unsigned grid = (unsigned)((items + 7) / 8);
+  const unsigned grid = (unsigned)((items + 3) / 4);
   if (p->dtype == KVC_BF16) {
-    if (p->d == 128) pack_tree_kernel<__nv_bfloat16, 128><<<grid, 256, 0, s>>>(*p, a);
-    else pack_tree_kernel<__nv_bfloat16, 64><<<grid, 256, 0, s>>>(*p, a);
+    if (p->d == 128) pack_tree_kernel<__nv_bfloat16, 128><<<grid, 128, 0, s>>>(*p, a);
+    else pack_tree_kernel<__nv_bfloat16, 64><<<grid, 128, 0, s>>>(*p, a);
   } else {
-    if (p->d == 128) pack_tree_kernel<float, 128><<<grid, 256, 0, s>>>(*p, a);
-    else pack_tree_kernel<float, 64><<<grid, 256, 0, s>>>(*p, a);
+    if (p->d == 128) pack_tree_kernel<float, 128><<<grid, 128, 0, s>>>(*p, a);
+    else pack_tree_kernel<float, 64><<<grid, 128, 0, s>>>(*p, a);
   }
   kvc::count_launch(2);
   return kvc::cuda_status(cudaGetLastError());

@@ -960,15 +960,11 @@ __global__ void __launch_bounds__(128) proto_kernel(kvc_params p, ScoreArgs a, u
         u[g][3] = k3 * cs[g].y - k1 * sn[g].y;
         nk2[g] = u[g][0] * u[g][0] + u[g][1] * u[g][1] + u[g][2] * u[g][2] + u[g][3] * u[g][3];
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-        for (int g = 0; g < 4; ++g) nk2[g] += __shfl_xor_sync(KVC_FULL_MASK, nk2[g], o);
+      kvcd::warp_sum4(nk2, lane);
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         if (g < ng) {
-          const float nk = sqrtf(nk2[g]);
-          const float inv = nk > 0.f ? 1.f / nk : 0.f;
+          const float inv = nk2[g] > 0.f ? rsqrtf(nk2[g]) : 0.f;
           const float v[4] = {__uint_as_float(vl[g] << 16), __uint_as_float(vl[g] & 0xFFFF0000u),
                               __uint_as_float(vh[g] << 16), __uint_as_float(vh[g] & 0xFFFF0000u)};
 #pragma unroll
