@@ -481,13 +481,42 @@ def greedy_auction(util: np.ndarray, cost: np.ndarray, taken: np.ndarray, remain
     return spent
 
 
+def full_heads(r: np.ndarray, end: int, frac: float) -> np.ndarray:
+    """Head-level hybrid ([DC] App. E.3: the top 20% of heads by an attention
+    statistic keep the full cache), reading R16: the statistic of (l, h) is its
+    relevance mass outside the recent window, sum of r_i over i < end, summed in
+    float64 over the float32 relevances; the floor(frac * L * H) heads with the
+    largest statistic (ties: lower l*H + h first) are full.  Returns bool [L, H]."""
+    L, H, _ = r.shape
+    F = int(math.floor(frac * L * H))
+    imp = np.asarray(r[:, :, :end], dtype=np.float64).sum(axis=-1).reshape(-1)
+    order = np.lexsort((np.arange(L * H), -imp))
+    full = np.zeros(L * H, dtype=bool)
+    full[order[:F]] = True
+    return full.reshape(L, H)
+
+
 def select_sequence(util: np.ndarray, cost: np.ndarray, r: np.ndarray, sens: np.ndarray,
                     bounds: np.ndarray, n: int, W: int, budget_ratio: float,
-                    budget_entries_per_lh: int, floor_cap_frac: float, floor_cap_tokens: int) -> Selection:
-    """Budget -> singleton floor -> greedy auction for one sequence (a5)."""
+                    budget_entries_per_lh: int, floor_cap_frac: float, floor_cap_tokens: int,
+                    head_full_frac: float = 0.0) -> Selection:
+    """Budget -> singleton floor -> greedy auction for one sequence (a5).
+
+    With head_full_frac > 0 (the head-level hybrid, R16) the full heads store
+    every token exact (all ops taken, len = n) and pay n - W beyond their
+    window from the same budget; the floor and the auction run on the other
+    heads with B_alloc = B_tot - W*L*H - F*(n - W) and the floor cap taken of
+    that reduced pool."""
     L, H, S, _ = util.shape
     B_tot, B_alloc, cap = budget(n, L, H, W, budget_ratio, budget_entries_per_lh, floor_cap_frac)
     taken = np.zeros((L, H, S, N_OPS), dtype=bool)
+    if head_full_frac > 0:
+        full = full_heads(r, int(bounds[-1]), head_full_frac)
+        taken[full] = True
+        B_alloc -= int(full.sum()) * (n - W)
+        if B_alloc < 0:
+            raise ValueError("budget smaller than the full heads and the windows")
+        cap = int(math.floor(floor_cap_frac * B_alloc))
     fs, ft = singleton_floor(r, sens, bounds, cost, min(cap, B_alloc), floor_cap_tokens, taken)
     asp = greedy_auction(util, cost, taken, B_alloc - fs)
     lens = W + (taken * cost).sum(axis=(2, 3))

@@ -317,3 +317,77 @@ def test_pack_order_lengths_and_offsets(tiny_scored):
     # cache bytes: entries x (2 d esize + 8) (K, V, log m, position)
     assert sel.lens.sum() * (2 * cfg.d * 4 + 8) == sel.B_tot * (2 * cfg.d * 4 + 8) or \
         sel.lens.sum() <= sel.B_tot
+
+
+# ------------------------------------------------------------------ head-level hybrid (R16)
+def _hybrid_instance(seed, L=3, H=2):
+    util, cost, _, bounds, n = _instance(seed, L=L, H=H)
+    rng = np.random.default_rng(1000 + seed)
+    # multiples of 1/64: every float64 sum of them is exact, so the ranking is fixed
+    r = rng.choice(np.asarray([0.0, 1 / 64, 1 / 32, 5 / 64], np.float32), size=(L, H, n))
+    return util, cost, r, bounds, n
+
+
+def _brute_full(r, end, F):
+    L, H, _ = r.shape
+    imp = [(sum(float(x) for x in r[l, h, :end]), l * H + h) for l in range(L) for h in range(H)]
+    ranked = sorted(imp, key=lambda t: (-t[0], t[1]))
+    full = np.zeros(L * H, dtype=bool)
+    for _, k in ranked[:F]:
+        full[k] = True
+    return full.reshape(L, H)
+
+
+@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("frac", [0.2, 0.4, 0.5])
+def test_hybrid_full_heads_budget_and_lengths(seed, frac):
+    util, cost, r, bounds, n = _hybrid_instance(seed)
+    L, H = 3, 2
+    W, end = n - int(bounds[-1]), int(bounds[-1])
+    F = int(math.floor(frac * L * H))
+    sens = np.ones((L, H), np.float32)
+    sel = O.select_sequence(util, cost, r, sens, bounds, n, W, 0.7, 0, 0.3, -1,
+                            head_full_frac=frac)
+    full = _brute_full(r, end, F)
+    assert full.sum() == F
+    np.testing.assert_array_equal(full, O.full_heads(r, end, frac))
+    assert sel.taken[full].all()                               # every token exact
+    np.testing.assert_array_equal(sel.lens[full], n)
+    B_tot, B_alloc, _ = O.budget(n, L, H, W, 0.7, 0, 0.3)
+    assert sel.B_alloc == B_alloc - F * (n - W)
+    assert int(sel.lens.sum()) <= B_tot                        # the budget holds overall
+    assert int(sel.lens[~full].sum()) - W * (L * H - F) == sel.floor_spent + sel.auction_spent
+    _tree_closed(sel.taken)
+
+
+def test_hybrid_off_is_the_plain_selection():
+    util, cost, r, bounds, n = _hybrid_instance(3)
+    sens = np.ones((3, 2), np.float32)
+    W = n - int(bounds[-1])
+    a = O.select_sequence(util, cost, r, sens, bounds, n, W, 0.5, 0, 0.3, -1)
+    b = O.select_sequence(util, cost, r, sens, bounds, n, W, 0.5, 0, 0.3, -1, head_full_frac=0.0)
+    np.testing.assert_array_equal(a.taken, b.taken)
+
+
+def test_hybrid_with_every_head_full_is_the_full_cache():
+    util, cost, r, bounds, n = _hybrid_instance(5)
+    sens = np.ones((3, 2), np.float32)
+    W = n - int(bounds[-1])
+    sel = O.select_sequence(util, cost, r, sens, bounds, n, W, 1.0, 0, 0.3, -1, head_full_frac=1.0)
+    assert sel.taken.all() and (sel.lens == n).all() and sel.B_alloc == 0
+
+
+def test_hybrid_leaving_no_budget_keeps_only_the_other_windows():
+    # L*H = 4, F = 2: per-(l,h) budget W + (n - W) / 2 leaves B_alloc = 0
+    util, cost, r, bounds, n = _hybrid_instance(6, L=2, H=2)
+    W = n - int(bounds[-1])
+    per_lh = W + (n - W) // 2
+    assert (n - W) % 2 == 0
+    sens = np.ones((2, 2), np.float32)
+    sel = O.select_sequence(util, cost, r, sens, bounds, n, W, 0.0, per_lh, 0.3, -1,
+                            head_full_frac=0.5)
+    full = O.full_heads(r, int(bounds[-1]), 0.5)
+    assert sel.B_alloc == 0
+    np.testing.assert_array_equal(sel.lens[full], n)
+    np.testing.assert_array_equal(sel.lens[~full], W)
+    assert not sel.taken[~full].any()
