@@ -101,6 +101,9 @@ typedef struct kvc_params {
                               capacity given to kvc_merge_pack); 0 = unknown,
                               which disables the tensor-core decode (its TMA
                               descriptor needs the extent)                      */
+  double  head_full_frac;  /* [DC] App. E.3 head-level hybrid: the
+                              floor(frac*L*H) heads with the largest relevance
+                              mass outside the window keep every token; 0 = off */
 } kvc_params;
 
 /* Human-readable name of a status code (static string). */
@@ -160,6 +163,10 @@ int kvc_score(const kvc_params* p, const int32_t* ctx_len, const void* K, const 
  * queue of exposed ops in (utility desc, op id asc) order, taking each op
  * whose cost fits the remaining budget and discarding the rest.
  * In:  relevance (floor keys r*sens), op_util, op_cost from kvc_score.
+ * With head_full_frac > 0 the floor(frac*L*H) heads of each sequence with the
+ * largest relevance mass outside the window (float64 sums; ties to the lower
+ * l*H+h) take every op (every token exact, len = n) and pay n - W beyond their
+ * window from the same budget; the floor and auction run on the other heads.
  * Out: taken [B,L,H,S_max,16] uint8 (1 = op bought); len_lh [B,L,H] int32
  *      (stored entries incl. the W window tokens); cap_lh = len_lh +
  *      decode_reserve; off_lh [B,L,H] int64 exclusive prefix sum of cap_lh in

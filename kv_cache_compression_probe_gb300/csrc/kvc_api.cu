@@ -8,7 +8,8 @@
 #include "kvc_internal.h"
 
 #include <cstddef>
-static_assert(sizeof(kvc_params) == 120, "kvc_params layout");
+static_assert(sizeof(kvc_params) == 128, "kvc_params layout");
+static_assert(offsetof(kvc_params, head_full_frac) == 120, "kvc_params layout");
 static_assert(offsetof(kvc_params, packed_rows) == 112, "kvc_params layout");
 static_assert(offsetof(kvc_params, total_ctx) == 104, "kvc_params layout");
 static_assert(offsetof(kvc_params, budget_ratio) == 64, "kvc_params layout");
@@ -55,6 +56,7 @@ int check_params(const kvc_params* p) {
   if (!(p->dtype == KVC_F32 || p->dtype == KVC_BF16)) return KVC_EINVAL;
   if (p->n_max < p->W + 16 || p->S_max < 1) return KVC_EINVAL;
   if (p->decode_reserve < 0 || p->total_ctx < 0 || p->packed_rows < 0) return KVC_EINVAL;
+  if (!(p->head_full_frac >= 0.0 && p->head_full_frac <= 1.0)) return KVC_EINVAL;
   return KVC_OK;
 }
 

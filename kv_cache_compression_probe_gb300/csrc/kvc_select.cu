@@ -60,6 +60,8 @@ struct SelWs {
   unsigned long long* hist;  // [kSelects][kPasses][B][256]
   uint8_t* tok_w;            // floor weight per token row (0 = not a floor item)
   unsigned long long* keys;  // auction sort key per op (0 = not in the auction)
+  double* imp;               // head-level hybrid: relevance mass per (b,l,h) outside the window
+  uint8_t* full;             // head-level hybrid: 1 = the (b,l,h) keeps every token
 };
 
 __device__ __forceinline__ int op_parent(int o) {
@@ -108,6 +110,8 @@ __global__ void sel_init_kernel(kvc_params p, const int32_t* ctx_len, const int3
   const long long per_lh = p.budget_entries_per_lh > 0 ? p.budget_entries_per_lh
                                                        : (long long)floor(p.budget_ratio * (double)n);
   long long B_alloc = per_lh * LH - (long long)p.W * LH;
+  if (p.head_full_frac > 0.0)                          // full heads pay n - W beyond their window
+    B_alloc -= (long long)floor(p.head_full_frac * (double)LH) * (n - p.W);
   bool bad = false;
   if (B_alloc < 0) { kvcd::record_error(err, KVC_EBUDGET); bad = true; }
   if (n < p.W + 16 || n > p.n_max || n_slots[b] < 1 || n_slots[b] > p.S_max) {
@@ -164,6 +168,7 @@ __global__ void floor_weights_kernel(kvc_params p, const int32_t* ctx_len,
   const int b = (int)(blh / ((long long)p.L * p.H));
   if (ws.seq[b].pad) return;
   if (s >= n_slots[b]) return;
+  if (p.head_full_frac > 0.0 && ws.full[blh]) return;   // already exact: not a floor item
   const int n = ctx_len[b];
   const int x0 = slot_bounds[(long long)b * (p.S_max + 1) + s];
   const int y0 = slot_bounds[(long long)b * (p.S_max + 1) + s + 1];
@@ -206,6 +211,57 @@ __global__ void floor_weights_kernel(kvc_params p, const int32_t* ctx_len,
       }
     }
     ws.tok_w[row0 + i] = (uint8_t)min(c, 255);
+  }
+}
+
+// ---------------------------------------------------------------- head-level hybrid
+// DistillCache App. E.3: the top fraction of heads by an attention statistic
+// keep the full cache.  Statistic: relevance mass outside the recent window,
+// summed in float64 (one warp per (b,l,h)).
+__global__ void hybrid_importance_kernel(kvc_params p, const int32_t* ctx_len,
+                                         const int32_t* slot_bounds, const int32_t* n_slots,
+                                         const float* relevance, SelWs ws) {
+  const long long LH = (long long)p.L * p.H;
+  const long long blh = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (blh >= (long long)p.B * LH) return;
+  const int b = (int)(blh / LH);
+  const long long lh = blh % LH;
+  const int n = ctx_len[b];
+  const int ns = min(max(n_slots[b], 0), p.S_max);
+  const int end = min(max(slot_bounds[(long long)b * (p.S_max + 1) + ns], 0), n);
+  const long long row0 = kvcd::seq_token_base(ctx_len, b, (int)LH) + lh * n;
+  double acc = 0.0;
+  for (int i = lane; i < end; i += 32) acc += (double)relevance[row0 + i];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(KVC_FULL_MASK, acc, o);
+  if (lane == 0) ws.imp[blh] = acc;
+}
+
+// One CTA per sequence: the floor(frac * L * H) heads with the largest statistic
+// (ties: lower l*H + h) are full, and every op of their trees is taken.
+__global__ void hybrid_mark_kernel(kvc_params p, const int32_t* n_slots, SelWs ws,
+                                   uint8_t* taken) {
+  const int b = blockIdx.x;
+  const long long LH = (long long)p.L * p.H;
+  const long long F = (long long)floor(p.head_full_frac * (double)LH);
+  const double* imp = ws.imp + (long long)b * LH;
+  for (long long k = threadIdx.x; k < LH; k += blockDim.x) {
+    const double v = imp[k];
+    long long rank = 0;
+    for (long long j = 0; j < LH; ++j) {
+      const double u = imp[j];
+      rank += (u > v || (u == v && j < k)) ? 1 : 0;
+    }
+    ws.full[(long long)b * LH + k] = rank < F ? 1 : 0;
+  }
+  __syncthreads();
+  const int S = min(max(n_slots[b], 0), p.S_max);
+  const long long per = (long long)S * kOps;
+  for (long long idx = threadIdx.x; idx < LH * per; idx += blockDim.x) {
+    const long long lh = idx / per, rem = idx % per;
+    if (ws.full[(long long)b * LH + lh])
+      taken[(((long long)b * LH + lh) * p.S_max + rem / kOps) * kOps + rem % kOps] = 1;
   }
 }
 
@@ -543,7 +599,7 @@ __global__ void offsets_kernel(long long n, const int32_t* cap_lh, int64_t* off_
 }
 
 struct Layout {
-  size_t seq, rs, hist, tok_w, keys, total;
+  size_t seq, rs, hist, tok_w, keys, imp, full, total;
 };
 
 Layout layout(const kvc_params* p) {
@@ -555,6 +611,8 @@ Layout layout(const kvc_params* p) {
   l.tok_w = off; off += kvc::align256((size_t)p->B * p->L * p->H * p->n_max);
   l.keys = off; off += kvc::align256(sizeof(unsigned long long) * (size_t)p->B * p->L * p->H *
                                      p->S_max * kOps);
+  l.imp = off; off += kvc::align256(sizeof(double) * (size_t)p->B * p->L * p->H);
+  l.full = off; off += kvc::align256((size_t)p->B * p->L * p->H);
   l.total = off;
   return l;
 }
@@ -591,6 +649,8 @@ extern "C" int kvc_select(const kvc_params* p, const int32_t* ctx_len, const int
   ws.hist = reinterpret_cast<unsigned long long*>(w + lay.hist);
   ws.tok_w = reinterpret_cast<uint8_t*>(w + lay.tok_w);
   ws.keys = reinterpret_cast<unsigned long long*>(w + lay.keys);
+  ws.imp = reinterpret_cast<double*>(w + lay.imp);
+  ws.full = reinterpret_cast<uint8_t*>(w + lay.full);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const kvc_params P = *p;
   const long long trees = (long long)p->B * p->L * p->H * p->S_max;
@@ -604,6 +664,12 @@ extern "C" int kvc_select(const kvc_params* p, const int32_t* ctx_len, const int
   zero_u8_kernel<<<sms * 4, 256, 0, s>>>(taken, ops); ++launches;
   zero_u8_kernel<<<sms * 4, 256, 0, s>>>(ws.tok_w, (long long)p->B * p->L * p->H * p->n_max);
   ++launches;
+  if (p->head_full_frac > 0.0) {                       // head-level hybrid: full heads first
+    hybrid_importance_kernel<<<(unsigned)((kvc::lh_count(p) + 7) / 8), 256, 0, s>>>(
+        P, ctx_len, slot_bounds, n_slots, relevance, ws);
+    hybrid_mark_kernel<<<p->B, 256, 0, s>>>(P, n_slots, ws, taken);
+    launches += 2;
+  }
   floor_weights_kernel<<<(unsigned)((trees + 7) / 8), 256, 0, s>>>(
       P, ctx_len, slot_bounds, n_slots, relevance, head_sens, op_cost, ws, err);
   ++launches;

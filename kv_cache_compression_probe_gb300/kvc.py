@@ -36,6 +36,7 @@ class kvc_params(ctypes.Structure):
         ("floor_cap_frac", c_double), ("floor_cap_tokens", c_int64), ("decode_reserve", c_int32),
         ("total_ctx", c_int64),
         ("packed_rows", c_int64),
+        ("head_full_frac", c_double),
     ]
 
 
@@ -113,7 +114,7 @@ def make_params(**kw) -> kvc_params:
     defaults = dict(rope_base=10000.0, hop_weight=0.3, n_hops=2, w_part=0.25, w_value=0.75,
                     value_floor=0.1, budget_ratio=0.25, budget_entries_per_lh=0,
                     floor_cap_frac=0.6, floor_cap_tokens=-1, decode_reserve=0, total_ctx=0,
-                    packed_rows=0)
+                    packed_rows=0, head_full_frac=0.0)
     defaults.update(kw)
     for k, v in defaults.items():
         setattr(p, k, v)
