@@ -270,7 +270,7 @@ def run_gpu(args, cfg, rank, world):
                         budget_ratio=cfg.budget_ratio,
                         budget_entries_per_lh=cfg.budget_entries_per_lh,
                         floor_cap_frac=cfg.floor_cap_frac, floor_cap_tokens=cfg.floor_cap_tokens,
-                        decode_reserve=args.decode_steps + 1)
+                        decode_reserve=args.decode_steps + 1, head_full_frac=args.head_full_frac)
     # host (pinned) and device copies of the inputs
     h_K = torch.from_numpy(np.concatenate([s[2].reshape(-1, cfg.d) for s in seqs])).to(dt).pin_memory()
     h_V = torch.from_numpy(np.concatenate([s[3].reshape(-1, cfg.d) for s in seqs])).to(dt).pin_memory()
@@ -446,7 +446,8 @@ def run_gpu(args, cfg, rank, world):
                    "context": cfg.n, "layers": cfg.L, "kv_heads": cfg.H, "q_heads": cfg.H * cfg.G,
                    "head_dim": d, "budget": cfg.budget_ratio, "window": cfg.W,
                    "decode_steps": D, "l2": "inputs larger than L2 (K+V %.2f GB)" %
-                   (2 * tokens * cfg.L * cfg.H * d * esz / 1e9), "parallelism": f"replicas x{world}"},
+                   (2 * tokens * cfg.L * cfg.H * d * esz / 1e9), "parallelism": f"replicas x{world}",
+                   "head_full_frac": args.head_full_frac},
         "breakdown_ms": {"score": score_ms, "select": sel_ms, "merge_pack": pack_ms,
                          "decode_per_step": dec_ms, "decode_total": dec_ms * D},
         "compress_tokens_per_s": tokens / ((score_ms + sel_ms + pack_ms) * 1e-3),
@@ -646,6 +647,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the layer count (small profiling cases)")
+    ap.add_argument("--head-full-frac", type=float, default=0.0,
+                    help="head-level hybrid: fraction of heads that keep the full cache")
     ap.add_argument("--eager-decode", action="store_true",
                     help="issue the decode steps one call at a time instead of one CUDA graph")
     ap.add_argument("--profile", action="store_true",

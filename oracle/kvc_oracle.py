@@ -605,6 +605,54 @@ def decode_step_head(q, k_new, v_new, Kp, Vp, logm):
     return decode_head(q, Kp2, Vp2, lm2), Kp2, Vp2, lm2
 
 
+# =============================================================================== f2: per-step top-B eviction
+def evict_budget(n_seen: int, ratio: float, b_min: int) -> int:
+    """[DC] Algorithm 1: B = max(floor(r * |C_t|), B_min); reading R17: |C_t| is the
+    unpruned cache size, i.e. the tokens seen so far (prompt and generated,
+    including this step's)."""
+    return max(int(math.floor(ratio * n_seen)), b_min)
+
+
+def evict_step(q: np.ndarray, k_new: np.ndarray, v_new: np.ndarray, K: np.ndarray, V: np.ndarray,
+               n_seen: int, ratio: float, b_min: int):
+    """One DistillCache inference step with the heuristic score s_i = alpha_i ([DC]
+    Algorithm 1 and 3.1.1; the learned policy is replaced by its first feature,
+    reading R17).  One sequence: K, V [L, H, c, d] hold the same c tokens in every
+    (layer, KV head); q [L, H*G, d]; k_new, v_new [L, H, d].
+
+    The new token is appended to every (l, h); every query head attends over
+    the c + 1 entries (fp64 softmax); alpha_i = mean over (l, h, g) of the
+    attention probability of entry i; B = evict_budget(n_seen, ...); the kept
+    entries are the top-B by alpha (ties: lower cache index), in cache order.
+    Returns (out [L, H*G, d], alpha [c + 1], keep [min(B, c + 1)] cache indices).
+    """
+    L, H, c, d = K.shape
+    G = q.shape[1] // H
+    q = np.asarray(q, np.float64)
+    out = np.zeros((L, H * G, d))
+    alpha = np.zeros(c + 1)
+    for l in range(L):
+        for h in range(H):
+            Kc = np.concatenate([np.asarray(K[l, h], np.float64), np.asarray(k_new[l, h], np.float64)[None]])
+            Vc = np.concatenate([np.asarray(V[l, h], np.float64), np.asarray(v_new[l, h], np.float64)[None]])
+            sc = q[l, h * G:(h + 1) * G] @ Kc.T / math.sqrt(d)
+            sc -= sc.max(axis=1, keepdims=True)
+            pr = np.exp(sc)
+            pr /= pr.sum(axis=1, keepdims=True)
+            out[l, h * G:(h + 1) * G] = pr @ Vc
+            alpha += pr.sum(axis=0)
+    alpha /= L * H * G
+    B = evict_budget(n_seen, ratio, b_min)
+    keep = top_b(alpha, B)
+    return out, alpha, keep
+
+
+def top_b(score: np.ndarray, B: int) -> np.ndarray:
+    """Indices of the B largest scores (ties: lower index first), ascending."""
+    order = np.lexsort((np.arange(len(score)), -np.asarray(score, np.float64)))
+    return np.sort(order[:min(B, len(score))])
+
+
 # =============================================================================== a0: partition
 def curvature(hidden: np.ndarray, scales: Sequence[int] = (1, 2, 4, 8)) -> np.ndarray:
     """Multi-scale curvature of the normalized hidden-state trajectory ([GK]
