@@ -215,6 +215,91 @@ def full_cache_decode_ms(p, cfg, seqs, K, V, q_all, kn_all, vn_all, D, dev, stre
     return ms
 
 
+def evict_leg(p, cfg, seqs, K, V, q_all, kn_all, vn_all, D, dev, stream):
+    """NEXT f2 on the same workload: DistillCache per-step top-B eviction with the
+    attention score (budget ratio = the workload's, minimum budget = its window),
+    starting from the full prompt cache.  Times the D steps (decode with LSE,
+    alpha, top-B + compaction) as one CUDA graph replay and, eagerly, each call
+    kind; returns a dict for the JSON line."""
+    import torch
+    from kv_cache_compression_probe_gb300 import kvc
+    from kv_cache_compression_probe_gb300.pipeline import EvictingCache
+    LH = cfg.L * cfg.H
+    ns = [s[0] for s in seqs]
+    B, n_max = len(ns), max(ns)
+    if B == 1:
+        Kb = K[:LH * ns[0]].view(1, cfg.L, cfg.H, ns[0], cfg.d)
+        Vb = V[:LH * ns[0]].view(1, cfg.L, cfg.H, ns[0], cfg.d)
+    else:
+        Kb = torch.zeros((B, cfg.L, cfg.H, n_max, cfg.d), dtype=K.dtype, device=dev)
+        Vb = torch.zeros_like(Kb)
+        tok0 = 0
+        for b, n in enumerate(ns):
+            Kb[b, :, :, :n] = K[tok0:tok0 + LH * n].view(cfg.L, cfg.H, n, cfg.d)
+            Vb[b, :, :, :n] = V[tok0:tok0 + LH * n].view(cfg.L, cfg.H, n, cfg.d)
+            tok0 += LH * n
+    pe = type(p).from_buffer_copy(p)
+    pe.decode_reserve = 0
+    cache = EvictingCache(pe, Kb, Vb, ns, D + 1, cfg.budget_ratio, cfg.W)
+    nseen = torch.tensor([[n + t + 1 for n in ns] for t in range(D)], dtype=torch.int64, device=dev)
+    posn = torch.tensor([[n + t for n in ns] for t in range(D)], dtype=torch.float32, device=dev)
+    out = torch.empty(tuple(q_all.shape), dtype=q_all.dtype, device=dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    cache.run_many(q_all, kn_all, vn_all, out, nseen, posn, graph=True)     # capture + warm-up
+    lens_end = cache.len_lh.cpu().numpy().astype(np.int64)
+    reps = []
+    for _ in range(3):
+        cache.reset()
+        torch.cuda.synchronize(dev)
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        launches = cache.run_many(q_all, kn_all, vn_all, out, nseen, posn, graph=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        reps.append(e0.elapsed_time(e1) / D)
+    # eager, per call kind (events between calls)
+    cache.reset()
+    torch.cuda.synchronize(dev)
+    part = {"decode_lse": 0.0, "alpha": 0.0, "topb_evict": 0.0}
+    for t in range(D):
+        m = [ev() for _ in range(4)]
+        m[0].record(stream)
+        kvc.kvc_decode_attn_lse(pe, q_all[t], kn_all[t], vn_all[t], posn[t], cache.K, cache.V,
+                                cache.logm, cache.pos, cache.len_lh, cache.cap_lh, cache.off_lh,
+                                out[t], cache.lse, cache.scores, cache.ws_decode, stream)
+        m[1].record(stream)
+        kvc.kvc_token_alpha(pe, q_all[t], cache.K, cache.scores, cache.len_lh, cache.off_lh,
+                            cache.lse, cache.alpha, cache.ws_evict, stream)
+        m[2].record(stream)
+        kvc.kvc_evict_topb(pe, cache.alpha, nseen[t], cache.ratio, cache.b_min, cache.K, cache.V,
+                           cache.pos, cache.logm, cache.off_lh, cache.len_lh, cache.ws_evict,
+                           stream)
+        m[3].record(stream)
+        torch.cuda.synchronize(dev)
+        part["decode_lse"] += m[0].elapsed_time(m[1]) / D
+        part["alpha"] += m[1].elapsed_time(m[2]) / D
+        part["topb_evict"] += m[2].elapsed_time(m[3]) / D
+    if kvc.kvc_device_error() != 0:
+        raise RuntimeError("device error in the eviction leg")
+    esz = 2 if cfg.dtype == "bf16" else 4
+    kept = int(lens_end.sum())                       # entries after the last eviction
+    # algorithmic bytes of a steady-state step: decode streams the kept entries
+    # (K, V, log m) plus the new token and writes each entry's G scores; alpha
+    # reads the scores; the eviction moves one row per (l,h) (read + write K,
+    # V, pos, log m)
+    LHB = LH * B
+    per_step = (kept * (2 * cfg.d * esz + 4) + LHB * (2 * cfg.d * esz + 8) + 2 * kept * cfg.G * 4
+                + LHB * 2 * (2 * cfg.d * esz + 8))
+    ms = min(reps)
+    return {"ms_per_step": ms, "launches_per_step": launches / D,
+            "breakdown_ms_per_step_eager": part,
+            "entries_after_eviction": kept, "ratio": cfg.budget_ratio, "b_min": cfg.W,
+            "algorithmic_bytes_per_step": per_step,
+            "hbm_gbs": per_step / (ms * 1e-3) / 1e9,
+            "note": "DistillCache Algorithm 1 with the attention score alpha; prompt cache "
+                    "evicted to the budget at the first step, then one entry per step"}
+
+
 def full_bytes_ratio(cfg, seqs, avg_entries, D):
     """Entries the full cache streams per decode step over the compressed one."""
     full = sum(s[0] for s in seqs) * cfg.L * cfg.H
@@ -387,6 +472,12 @@ def run_gpu(args, cfg, rank, world):
     full_ms = None if args.profile else full_cache_decode_ms(p, cfg, seqs, K, V, q_all, kn_all,
                                                             vn_all, D, dev, stream)
 
+    evict = None
+    if args.evict and not args.profile:
+        evict = evict_leg(p, cfg, seqs, K, V, q_all, kn_all, vn_all, D, dev, stream)
+        evict["hbm_frac"] = evict["hbm_gbs"] / measured_peaks()[0]
+        evict["step_over_compressed_decode"] = evict["ms_per_step"] / statistics.mean(rec["decode"])
+
     # max over ranks
     ms = total_ms / args.steps
     e2e = statistics.mean(e2e_ms) if e2e_ms else float("nan")
@@ -473,6 +564,7 @@ def run_gpu(args, cfg, rank, world):
         "score_tc_frac_of_bf16_peak": score_flops / (score_ms * 1e-3) / 1e12 / tc,
         "e2e": {"value": job_throughput(tokens, world, e2e), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e},
+        "evict_per_step_next_f2": evict,
         "gpu_launches": launches,
         "gpu_launches_detail": {"issued_by_host": host_launches,
                                 "in_decode_graph_replays": graph_launches},
@@ -649,6 +741,8 @@ def main():
                     help="override the layer count (small profiling cases)")
     ap.add_argument("--head-full-frac", type=float, default=0.0,
                     help="head-level hybrid: fraction of heads that keep the full cache")
+    ap.add_argument("--evict", action="store_true",
+                    help="also time per-step top-B eviction (DistillCache) on the workload")
     ap.add_argument("--eager-decode", action="store_true",
                     help="issue the decode steps one call at a time instead of one CUDA graph")
     ap.add_argument("--profile", action="store_true",

@@ -219,6 +219,64 @@ int kvc_decode_attn(const kvc_params* p, const void* q, const void* k_new, const
                     int32_t* len_lh, const int32_t* cap_lh, const int64_t* off_lh, void* out,
                     void* workspace, size_t ws_bytes, void* stream);
 
+/* kvc_decode_attn that also returns the base-2 log-sum-exp of each query
+ * head's scores over the len_lh + 1 entries it attended:
+ *   lse_out[(b,l,h), g] = log2 sum_e 2^(s_e),  s_e = (q_g . k_e / sqrt(d) + logm_e) log2 e.
+ * (kvc_token_alpha needs it to form the DistillCache attention feature.)
+ * On the tensor-core path the sum runs over the bf16-rounded numerators that
+ * also normalise `out` (relative error of each term at most 2^-9).
+ * lse_out: [B*L*H, G] f32 device, required.
+ * scores_out: NULL, or f32 device rows laid out like Kp ([rows, G]): row
+ * off_lh + e receives, per query head g, the base-2 score s_e of that
+ * attended entry (e < len_lh + 1; the appended token's row only when it was
+ * appended).  Everything else, results and errors as kvc_decode_attn. */
+int kvc_decode_attn_lse(const kvc_params* p, const void* q, const void* k_new, const void* v_new,
+                        const float* pos_new, void* Kp, void* Vp, float* logm, float* pos,
+                        int32_t* len_lh, const int32_t* cap_lh, const int64_t* off_lh, void* out,
+                        float* lse_out, float* scores_out, void* workspace, size_t ws_bytes,
+                        void* stream);
+
+/* NEXT f2, DistillCache inference with the heuristic score (DistillCache
+ * Algorithm 1; the learned policy is replaced by its first feature, the
+ * attention received, 3.1.1).  An evicting cache holds the same tokens in the
+ * same rows of every (layer, KV head) of a sequence (row i is one token
+ * everywhere; len_lh equal across the sequence's (l,h)), every entry with
+ * log m = 0 and an integer position pos in [0, 2^24).
+ *
+ * kvc_token_alpha: per cache row i of sequence b
+ *   alpha[b, i] = 1/(L H G) sum_{l,h,g} 2^(s_i - lse_out[(b,l,h), g])
+ * with q the step's queries [B, L, H*G, d] and lse_out from
+ * kvc_decode_attn_lse of the same step (so the rows include its appended
+ * token).  With `scores` (that call's scores_out) s_i is read from it and q,
+ * Kp may be NULL; with scores == NULL s_i is recomputed in fp32 from q and K
+ * (every log m taken as 0).  The (l,h) are summed in fixed groups, so the
+ * result is deterministic.  alpha: [B, alpha_cols] f32;
+ * rows i >= len are not written.  A sequence whose len_lh differ across (l,h),
+ * or exceed alpha_cols, reports KVC_EDEVICE.  Workspace: kvc_evict_workspace_bytes.
+ * Errors: KVC_EINVAL, KVC_EWORKSPACE, KVC_ECUDA. */
+int kvc_token_alpha(const kvc_params* p, const void* q, const void* Kp, const float* scores,
+                    const int32_t* len_lh, const int64_t* off_lh, const float* lse_out,
+                    float* alpha, int32_t alpha_cols, void* workspace, size_t ws_bytes,
+                    void* stream);
+
+/* Workspace bytes of kvc_token_alpha and kvc_evict_topb (one buffer may serve
+ * both; 256-byte aligned device memory, no initialisation needed); 0 for
+ * invalid arguments. */
+size_t kvc_evict_workspace_bytes(const kvc_params* p /* host */, int32_t alpha_cols);
+
+/* kvc_evict_topb: per sequence B_b = min(len, max(floor(ratio * n_seen[b]),
+ * b_min)); keeps the B_b rows with the largest alpha, ties to the earlier
+ * token (smaller pos of the sequence's first (l,h)), and sets len_lh = B_b.
+ * In place: the kept rows at index >= B_b move into the evicted rows below
+ * B_b (K, V, pos and logm rows of every (l,h) alike), so after the call the
+ * rows are in no particular position order.  n_seen [B] int64 device: tokens
+ * seen so far, this step's included.  Errors: KVC_EINVAL, KVC_EWORKSPACE,
+ * KVC_ECUDA; inconsistent lengths report KVC_EDEVICE. */
+int kvc_evict_topb(const kvc_params* p, const float* alpha, int32_t alpha_cols,
+                   const int64_t* n_seen, double ratio, int32_t b_min, void* K, void* V,
+                   float* pos, float* logm, const int64_t* off_lh, int32_t* len_lh,
+                   void* workspace, size_t ws_bytes, void* stream);
+
 /* Allocation-free variant of kvc_decode_attn (no counterpart on the pages: it
  * is an interface convenience, not part of the method).  For callers that
  * cannot allocate device memory on the library's behalf: a serving engine whose

@@ -47,6 +47,8 @@ struct DecodeArgs {
   void* out;
   float* partials;     // [BLH, n_chunk_max, G, D + 2]
   int32_t* counters;   // [BLH], zero between calls
+  float* lse_out;      // [BLH, G] base-2 LSE of the step's scores, or null
+  float* scores_out;   // [rows, G] base-2 score of cache row off + i per query head, or null
   int H, L, n_chunk_max;
   float scale_log2;    // log2(e) / sqrt(d)
   int32_t* err;
@@ -65,12 +67,13 @@ struct DecodeSmem {
 
 // One warp batch: rows k < nvalid (of EB = 32/G) at kb + k*D / vb + k*D, the
 // rest masked; 32 dot products, one transpose reduction, online softmax
-// update.  my_lm = log2(e) * log m of row lane / G (0 when masked).
+// update.  my_lm = log2(e) * log m of row lane / G (0 when masked).  With
+// s_out the batch's scores are stored there ([row][G], lane = row * G + g).
 template <typename T, int D, int G>
 __device__ __forceinline__ void decode_batch(const float (&qv)[G][D / 32], const T* kb,
                                              const T* vb, int nvalid, float my_lm, int lane,
                                              float* s_p, float (&m_run)[G], float& lsum,
-                                             float (&o)[G][D / 32]) {
+                                             float (&o)[G][D / 32], float* s_out) {
   constexpr int VPL = D / 32;
   constexpr int EB = 32 / G;
   float kk[EB][VPL], vv[EB][VPL];
@@ -106,6 +109,7 @@ __device__ __forceinline__ void decode_batch(const float (&qv)[G][D / 32], const
   }
   const int gj = lane % G, kj = lane / G;
   const float s = kj < nvalid ? part[0] + my_lm : -INFINITY;
+  if (s_out && kj < nvalid) s_out[lane] = s;
   float gm = s;
 #pragma unroll
   for (int o_ = G; o_ < 32; o_ <<= 1) gm = fmaxf(gm, __shfl_xor_sync(KVC_FULL_MASK, gm, o_));
@@ -215,7 +219,8 @@ __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(DecodeArgs a) {
       const int my_row = rb + lane / G;
       const float my_lm = (lane / G < nvalid) ? __ldg(lm + r0 + my_row) * kLog2e : 0.f;
       decode_batch<T, D, G>(qv, &sm.ring[slot][0][rb][0], &sm.ring[slot][1][rb][0], nvalid, my_lm,
-                            lane, sm.p[warp], m_run, lsum, o);
+                            lane, sm.p[warp], m_run, lsum, o,
+                            a.scores_out ? a.scores_out + (off + r0 + rb) * G : nullptr);
     }
     consumed = st + 1;
     __syncthreads();
@@ -237,7 +242,8 @@ __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(DecodeArgs a) {
   }
   // the new token (row len) when this chunk holds it
   if (warp == 0 && e0 <= len && len < e1) {
-    decode_batch<T, D, G>(qv, kn, vn, 1, 0.f, lane, sm.p[0], m_run, lsum, o);
+    decode_batch<T, D, G>(qv, kn, vn, 1, 0.f, lane, sm.p[0], m_run, lsum, o,
+                          a.scores_out && append_ok ? a.scores_out + (off + len) * G : nullptr);
   }
   // per-head row sums of this warp
 #pragma unroll
@@ -305,6 +311,7 @@ __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(DecodeArgs a) {
       l = fmaf(f, __ldcg(pc + 1), l);
     }
     outp[g * D + dd] = kvcd::from_f<T>(acc / l);
+    if (a.lse_out && dd == 0) a.lse_out[(int64_t)blh * G + g] = M + log2f(l);
   }
   if (tid == 0) a.counters[blh] = 0;
 }
@@ -363,7 +370,7 @@ DecodeLayout decode_layout(const kvc_params* p) {
 int run_decode(const kvc_params* p, const void* q, const void* k_new, const void* v_new,
                const float* pos_new, void* Kp, void* Vp, float* logm, float* pos,
                int32_t* len_lh, const int32_t* cap_lh, const int64_t* off_lh, void* out,
-               char* ws, int32_t* err, cudaStream_t s) {
+               float* lse_out, float* scores_out, char* ws, int32_t* err, cudaStream_t s) {
   const int64_t blh = kvc::lh_count(p);
   const DecodeLayout w = decode_layout(p);
   const int ncm = n_chunk_max(p);
@@ -381,6 +388,8 @@ int run_decode(const kvc_params* p, const void* q, const void* k_new, const void
     t.H = p->H; t.L = p->L; t.G = p->G; t.n_chunk_max = ncm;
     t.scale_log2 = kLog2e / sqrtf((float)p->d);
     t.err = err;
+    t.lse_out = lse_out;
+    t.scores_out = scores_out;
     return kvc::decode_tc_launch(t, s);
   }
   DecodeArgs a;
@@ -392,6 +401,8 @@ int run_decode(const kvc_params* p, const void* q, const void* k_new, const void
   a.H = p->H; a.L = p->L; a.n_chunk_max = ncm;
   a.scale_log2 = kLog2e / sqrtf((float)p->d);
   a.err = err;
+  a.lse_out = lse_out;
+  a.scores_out = scores_out;
   dim3 grid(a.n_chunk_max, (unsigned)blh);
   if (p->dtype == KVC_BF16) {
     if (p->d == 128) launch_dg<__nv_bfloat16, 128>(p, a, grid, s);
@@ -429,7 +440,30 @@ extern "C" int kvc_decode_attn(const kvc_params* p, const void* q, const void* k
   int32_t* err = kvc::err_word();
   if (!err) return KVC_ECUDA;
   return run_decode(p, q, k_new, v_new, pos_new, Kp, Vp, logm, pos, len_lh, cap_lh, off_lh, out,
-                    static_cast<char*>(workspace), err, static_cast<cudaStream_t>(stream));
+                    nullptr, nullptr, static_cast<char*>(workspace), err,
+                    static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int kvc_decode_attn_lse(const kvc_params* p, const void* q, const void* k_new,
+                                   const void* v_new, const float* pos_new, void* Kp, void* Vp,
+                                   float* logm, float* pos, int32_t* len_lh, const int32_t* cap_lh,
+                                   const int64_t* off_lh, void* out, float* lse_out,
+                                   float* scores_out, void* workspace, size_t ws_bytes,
+                                   void* stream) {
+  int st = kvc::check_params(p);
+  if (st != KVC_OK) return st;
+  if (!q || !k_new || !v_new || !Kp || !Vp || !logm || !pos || !len_lh || !cap_lh || !off_lh ||
+      !out || !lse_out)
+    return KVC_EINVAL;
+  const size_t need = kvc::decode_workspace_bytes(p);
+  if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return KVC_EWORKSPACE;
+  if (kvc::lh_count(p) > 65535) return KVC_EINVAL;
+  int32_t* err = kvc::err_word();
+  if (!err) return KVC_ECUDA;
+  return run_decode(p, q, k_new, v_new, pos_new, Kp, Vp, logm, pos, len_lh, cap_lh, off_lh, out,
+                    lse_out, scores_out, static_cast<char*>(workspace), err,
+                    static_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------- allocation-free variant
@@ -489,5 +523,5 @@ extern "C" int kvc_decode_attn_noalloc(const kvc_params* p, const void* q, const
   cudaError_t e = cudaMemsetAsync(ws + w.counters, 0, (size_t)blh * sizeof(int32_t), s);
   if (e != cudaSuccess) return KVC_ECUDA;
   return run_decode(p, q, k_new, v_new, pos_new, Kp, Vp, logm, pos, len_lh, cap_lh, off_lh, out,
-                    ws, err, s);
+                    nullptr, nullptr, ws, err, s);
 }

@@ -379,6 +379,17 @@ __global__ void __launch_bounds__(256, 2)
             sv[t][g] = sc;
             mh[g] = fmaxf(mh[g], sc);
           }
+        if (a.scores_out) {                         // the step's scores, one row per thread
+#pragma unroll
+          for (int t = 0; t < kTiles; ++t) {
+            const int e = t * kTileRows + row;
+            if (t < it.ntiles && e < it.nvalid) {
+              float* so = a.scores_out + (it.off + e0 + e) * G;
+#pragma unroll
+              for (int g = 0; g < G; ++g) so[g] = sv[t][g];
+            }
+          }
+        }
       }
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -485,6 +496,8 @@ __global__ void __launch_bounds__(128 * G) decode_merge_kernel(kvc::DecodeTcArgs
       acc = fmaf(__bfloat162float(qp[warp * kD + f]), __bfloat162float(kn[f]), acc);
     const float sn = kvcd::warp_sum(acc) * a.scale_log2;
     if (lane == 0) s_new[warp] = sn;
+    if (a.scores_out && lane == 0 && len + 1 <= a.cap_lh[blh] && off + len + 1 <= a.packed_rows)
+      a.scores_out[(off + len) * G + warp] = sn;
   }
   // thread (g, dd): partials of every chunk, 8 chunks of loads in flight at a
   // time, rescaled online to the running max (every thread of head g sees the
@@ -527,6 +540,7 @@ __global__ void __launch_bounds__(128 * G) decode_merge_kernel(kvc::DecodeTcArgs
     const float lt = fmaf(l, sc, fn);
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out) + (bl * a.H * G + (int64_t)h * G) * kD;
     outp[g * kD + dd] = __float2bfloat16_rn(o / lt);
+    if (a.lse_out && dd == 0) a.lse_out[(int64_t)blh * G + g] = Mf + log2f(lt);
   }
   if (len + 1 <= a.cap_lh[blh] && off + len + 1 <= a.packed_rows) {
     __nv_bfloat16* Kw = static_cast<__nv_bfloat16*>(a.Kp) + (off + len) * kD;

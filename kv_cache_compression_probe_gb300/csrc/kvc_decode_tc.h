@@ -29,6 +29,8 @@ struct DecodeTcArgs {
   int H, L, G, n_chunk_max;
   float scale_log2;     // log2(e) / sqrt(d)
   int32_t* err;
+  float* lse_out;       // [BLH, G] base-2 LSE of the step's scores, or null
+  float* scores_out;    // [rows, G] base-2 score of cache row off + i per query head, or null
 };
 
 // bf16, d = 128, G <= 8, a known packed extent below 2^31 rows, at most 65535

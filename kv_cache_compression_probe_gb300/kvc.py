@@ -23,7 +23,8 @@ KVC_WS_SCORE, KVC_WS_SELECT, KVC_WS_PACK, KVC_WS_DECODE, KVC_WS_PARTITION = rang
 
 EXPORTED = ("kvc_status_string", "kvc_last_cuda_error", "kvc_device_error", "kvc_launch_count", "kvc_workspace_bytes",
             "kvc_rope_table", "kvc_score", "kvc_select", "kvc_merge_pack", "kvc_decode_attn",
-            "kvc_partition", "kvc_decode_attn_noalloc")
+            "kvc_partition", "kvc_decode_attn_noalloc", "kvc_decode_attn_lse", "kvc_token_alpha",
+            "kvc_evict_workspace_bytes", "kvc_evict_topb")
 
 
 class kvc_params(ctypes.Structure):
@@ -76,6 +77,14 @@ def lib():
         L.kvc_decode_attn.restype = c_int
         L.kvc_decode_attn_noalloc.argtypes = [_P] + [vp] * 13
         L.kvc_decode_attn_noalloc.restype = c_int
+        L.kvc_decode_attn_lse.argtypes = [_P] + [vp] * 15 + [c_size_t, vp]
+        L.kvc_decode_attn_lse.restype = c_int
+        L.kvc_token_alpha.argtypes = [_P] + [vp] * 7 + [c_int32, vp, c_size_t, vp]
+        L.kvc_token_alpha.restype = c_int
+        L.kvc_evict_workspace_bytes.argtypes = [_P, c_int32]
+        L.kvc_evict_workspace_bytes.restype = c_size_t
+        L.kvc_evict_topb.argtypes = [_P, vp, c_int32, vp, c_double, c_int32] + [vp] * 7 + [c_size_t, vp]
+        L.kvc_evict_topb.restype = c_int
         L.kvc_partition.argtypes = [_P, vp, vp, c_int32, vp, vp, vp, vp, c_size_t, vp]
         L.kvc_partition.restype = c_int
         _lib = L
@@ -190,6 +199,36 @@ def kvc_decode_attn_noalloc(p, q, k_new, v_new, pos_new, Kp, Vp, logm, pos, len_
                                          _ptr(pos_new), _ptr(Kp), _ptr(Vp), _ptr(logm),
                                          _ptr(pos), _ptr(len_lh), _ptr(cap_lh), _ptr(off_lh),
                                          _ptr(out), _stream(stream)), "kvc_decode_attn_noalloc")
+
+
+def kvc_decode_attn_lse(p, q, k_new, v_new, pos_new, Kp, Vp, logm, pos, len_lh, cap_lh, off_lh,
+                        out, lse_out, scores_out, workspace, stream=None):
+    w, wb = _ws(workspace)
+    _check(lib().kvc_decode_attn_lse(ctypes.byref(p), _ptr(q), _ptr(k_new), _ptr(v_new),
+                                     _ptr(pos_new), _ptr(Kp), _ptr(Vp), _ptr(logm), _ptr(pos),
+                                     _ptr(len_lh), _ptr(cap_lh), _ptr(off_lh), _ptr(out),
+                                     _ptr(lse_out), _ptr(scores_out), w, wb, _stream(stream)),
+           "kvc_decode_attn_lse")
+
+
+def kvc_token_alpha(p, q, Kp, scores, len_lh, off_lh, lse_out, alpha, workspace, stream=None):
+    w, wb = _ws(workspace)
+    _check(lib().kvc_token_alpha(ctypes.byref(p), _ptr(q), _ptr(Kp), _ptr(scores), _ptr(len_lh),
+                                 _ptr(off_lh), _ptr(lse_out), _ptr(alpha), alpha.shape[1], w, wb,
+                                 _stream(stream)), "kvc_token_alpha")
+
+
+def kvc_evict_workspace_bytes(p, alpha_cols: int) -> int:
+    return int(lib().kvc_evict_workspace_bytes(ctypes.byref(p), alpha_cols))
+
+
+def kvc_evict_topb(p, alpha, n_seen, ratio, b_min, K, V, pos, logm, off_lh, len_lh, workspace,
+                   stream=None):
+    w, wb = _ws(workspace)
+    _check(lib().kvc_evict_topb(ctypes.byref(p), _ptr(alpha), alpha.shape[1], _ptr(n_seen),
+                                float(ratio), int(b_min), _ptr(K), _ptr(V), _ptr(pos),
+                                _ptr(logm), _ptr(off_lh), _ptr(len_lh), w, wb, _stream(stream)),
+           "kvc_evict_topb")
 
 
 def kvc_partition(p, ctx_len, hidden, dh, kappa, slot_bounds, n_slots, workspace, stream=None):

@@ -154,6 +154,117 @@ class DecodeGraph:
         self.graph.replay()
 
 
+class EvictingCache:
+    """NEXT f2: DistillCache per-step top-B eviction with the heuristic score
+    (DistillCache Algorithm 1; the score is the attention feature alpha of 3.1.1).
+
+    Every (b, l, h) holds the same tokens of sequence b (its prompt to start
+    with) in the same rows of its `cap`-row range at off_lh = (b*L*H + l*H + h)
+    * cap.  One step is kvc_decode_attn_lse (append + attend, base-2 LSE per
+    query head and, with scores=True, every entry's score) -> kvc_token_alpha
+    (from those scores, else recomputed from K) -> kvc_evict_topb (in place);
+    every entry keeps log m = 0.  The class only allocates and marshals.
+    """
+
+    def __init__(self, p: kvc.kvc_params, K, V, ctx_len: Sequence[int], reserve: int,
+                 ratio: float, b_min: int, tensor_cores: bool = True, scores: bool = True):
+        B, L, H = p.B, p.L, p.H
+        assert K.shape[:3] == (B, L, H) and K.shape == V.shape
+        dev = K.device
+        self.p, self.ratio, self.b_min = p, float(ratio), int(b_min)
+        self.ctx = [int(n) for n in ctx_len]
+        self.cap = max(self.ctx) + int(reserve)
+        rows = B * L * H * self.cap
+        p.packed_rows = rows if tensor_cores else 0
+        dt = TORCH_DT[p.dtype]
+        self.K = torch.zeros((rows, p.d), dtype=dt, device=dev)
+        self.V = torch.zeros((rows, p.d), dtype=dt, device=dev)
+        self.pos = torch.zeros((rows,), dtype=torch.float32, device=dev)
+        self.logm = torch.zeros((rows,), dtype=torch.float32, device=dev)
+        self._prompt = (K, V)
+        self.len_lh = torch.zeros((B * L * H,), dtype=torch.int32, device=dev)
+        self.cap_lh = torch.full((B * L * H,), self.cap, dtype=torch.int32, device=dev)
+        self.off_lh = torch.arange(B * L * H, dtype=torch.int64, device=dev) * self.cap
+        self.lse = torch.zeros((B * L * H, p.G), dtype=torch.float32, device=dev)
+        # the decode's per-entry scores feed alpha (else alpha recomputes them from K)
+        self.scores = (torch.zeros((rows, p.G), dtype=torch.float32, device=dev)
+                       if scores else None)
+        self.alpha = torch.zeros((B, self.cap), dtype=torch.float32, device=dev)
+        self.ws_decode = torch.zeros(kvc.kvc_workspace_bytes(kvc.KVC_WS_DECODE, p),
+                                     dtype=torch.uint8, device=dev)
+        self.ws_evict = torch.empty(kvc.kvc_evict_workspace_bytes(p, self.cap),
+                                    dtype=torch.uint8, device=dev)
+        self._graphs = {}
+        self.reset()
+
+    def reset(self):
+        """Back to the prompt: every (b, l, h) holds the prompt tokens in order."""
+        p, (K, V) = self.p, self._prompt
+        B, L, H = p.B, p.L, p.H
+        Kc = self.K.view(B, L, H, self.cap, p.d)
+        Vc = self.V.view(B, L, H, self.cap, p.d)
+        Pc = self.pos.view(B, L, H, self.cap)
+        for b, n in enumerate(self.ctx):
+            assert n <= K.shape[3]
+            Kc[b, :, :, :n] = K[b, :, :, :n]
+            Vc[b, :, :, :n] = V[b, :, :, :n]
+            Pc[b, :, :, :n] = torch.arange(n, dtype=torch.float32, device=K.device)
+        lens = np.repeat(np.asarray(self.ctx, np.int32), L * H)
+        self.len_lh.copy_(torch.from_numpy(lens))
+        self.logm.zero_()
+
+    def step(self, q, k_new, v_new, out, n_seen, pos_new=None, stream=None):
+        """One decode step then one eviction; n_seen [B] int64 = tokens seen so far,
+        this step's included."""
+        kvc.kvc_decode_attn_lse(self.p, q, k_new, v_new, pos_new, self.K, self.V, self.logm,
+                                self.pos, self.len_lh, self.cap_lh, self.off_lh, out, self.lse,
+                                self.scores, self.ws_decode, stream)
+        kvc.kvc_token_alpha(self.p, q, self.K, self.scores, self.len_lh, self.off_lh, self.lse,
+                            self.alpha, self.ws_evict, stream)
+        kvc.kvc_evict_topb(self.p, self.alpha, n_seen, self.ratio, self.b_min, self.K, self.V,
+                           self.pos, self.logm, self.off_lh, self.len_lh, self.ws_evict, stream)
+
+    def run_many(self, q_all, kn_all, vn_all, out_all, nseen_all, pos_all=None, graph=True):
+        """T steps back to back (step t reads row t of every *_all tensor); with
+        graph=True they are captured once per set of buffers into a CUDA graph
+        and replayed.  Returns the library kernels launched."""
+        T = q_all.shape[0]
+        if not graph:
+            n0 = kvc.kvc_launch_count()
+            for t in range(T):
+                self.step(q_all[t], kn_all[t], vn_all[t], out_all[t], nseen_all[t],
+                          None if pos_all is None else pos_all[t])
+            return kvc.kvc_launch_count() - n0
+        key = tuple(x.data_ptr() if x is not None else 0
+                    for x in (q_all, kn_all, vn_all, out_all, nseen_all, pos_all)) + (T,)
+        g = self._graphs.get(key)
+        if g is None:
+            dev = q_all.device
+            kvc.kvc_device_error()                   # error-word lookup outside capture
+            side = torch.cuda.Stream(device=dev)
+            side.wait_stream(torch.cuda.current_stream(dev))
+            graph_ = torch.cuda.CUDAGraph()
+            n0 = kvc.kvc_launch_count()
+            with torch.cuda.graph(graph_, stream=side):
+                for t in range(T):
+                    self.step(q_all[t], kn_all[t], vn_all[t], out_all[t], nseen_all[t],
+                              None if pos_all is None else pos_all[t], side)
+            torch.cuda.current_stream(dev).wait_stream(side)
+            g = (graph_, kvc.kvc_launch_count() - n0,
+                 (q_all, kn_all, vn_all, out_all, nseen_all, pos_all))
+            self._graphs[key] = g
+        g[0].replay()
+        return g[1]
+
+    def entries(self, b: int, l: int, h: int):
+        """(K, V, pos) rows the (b, l, h) currently holds, in row order (host copies)."""
+        blh = (b * self.p.L + l) * self.p.H + h
+        n = int(self.len_lh[blh])
+        o = blh * self.cap
+        return (self.K[o:o + n].float().cpu().numpy(), self.V[o:o + n].float().cpu().numpy(),
+                self.pos[o:o + n].cpu().numpy())
+
+
 def pad_bounds(bounds_list, S_max: int) -> np.ndarray:
     """[B, S_max + 1] int32 slot boundaries (rows padded with their last value)."""
     out = np.zeros((len(bounds_list), S_max + 1), dtype=np.int32)
