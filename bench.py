@@ -473,7 +473,7 @@ def run_gpu(args, cfg, rank, world):
                                                             vn_all, D, dev, stream)
 
     evict = None
-    if args.evict and not args.profile:
+    if args.evict:
         evict = evict_leg(p, cfg, seqs, K, V, q_all, kn_all, vn_all, D, dev, stream)
         evict["hbm_frac"] = evict["hbm_gbs"] / measured_peaks()[0]
         evict["step_over_compressed_decode"] = evict["ms_per_step"] / statistics.mean(rec["decode"])
