@@ -106,10 +106,19 @@ __device__ __forceinline__ void tmem_ld16_nw(uint32_t taddr, float (&v)[16]) {
 __device__ __forceinline__ void tmem_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 
+// Row-statistics passes: 16 epilogue warps; the NT row blocks' lane quarters
+// are covered 4 / NT times, each copy taking its share of a tile's columns.
+constexpr int kRsEpiWarps = 16;
+constexpr int kRsThreads = (kRsEpiWarps + 2) * 32;
+// Registers are reserved for whole groups of 4 warps: 18 warps count as 20, so
+// a thread may use at most 65536 / (20 * 32) = 102, i.e. 96 registers.
+constexpr int kRsMaxRegs = 96;
+
 template <int NT>
 struct TcSmem {
   alignas(1024) unsigned char A[NT][2][kBlockBytes];       // query rows, swizzled
   alignas(1024) unsigned char Bt[kStages][2][kBlockBytes]; // key tiles, swizzled
+  float xch[4 / NT - 1][NT * kBM][3];                       // other column shares' (m, l, u)
   uint64_t full[kStages], empty[kStages], tfull[2], tempty[2];
   uint32_t tmem_base;
   int abort;
@@ -117,7 +126,7 @@ struct TcSmem {
 };
 
 template <int NT, int MODE>
-__global__ void __launch_bounds__((4 * NT + 2) * 32, 1)
+__global__ void __maxnreg__(kRsMaxRegs)
     probe_tc_kernel(const __grid_constant__ CUtensorMap kmap, kvc::ProbeTcArgs a) {
   static_assert(MODE == kvc::kTcRowstatsProbes || MODE == kvc::kTcRowstatsSeeds,
                 "row-statistics passes only (the per-key passes use probe_tcT_kernel)");
@@ -125,8 +134,8 @@ __global__ void __launch_bounds__((4 * NT + 2) * 32, 1)
   // the dynamic shared memory base is aligned up to 1024 bytes by hand
   TcSmem<NT>& sm = *reinterpret_cast<TcSmem<NT>*>(
       (reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
-  constexpr int kEpiWarps = 4 * NT;
-  constexpr int kThreads = (kEpiWarps + 2) * 32;
+  constexpr int kEpiWarps = kRsEpiWarps;
+  constexpr int kThreads = kRsThreads;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long blh = blockIdx.y;
   const int LH = a.L * a.H;
@@ -225,10 +234,16 @@ __global__ void __launch_bounds__((4 * NT + 2) * 32, 1)
     // ---------------------------------------------------------------- epilogue
     // Row statistics over the keys: m (running max of s = S log2e / sqrt(d)),
     // l = sum 2^(s - m) and, for probe rows, u = sum 2^(s - m) (s - m) <= 0.
-    // Per 32-key chunk the terms are summed as a tree and added to l and u with
-    // one compensated (Kahan) step; masks are applied only on boundary chunks.
+    // Warp w reads lane quarter w % 4 of row block (w / 4) % NT and column
+    // share w / (4 NT) (kCW columns of every tile, in 16-column batches).  Per
+    // batch the terms are summed as a tree and added to l and u with one
+    // compensated (Kahan) step; masks are applied only on boundary batches.
+    // The shares of a row meet once at the end (rescaled to a common max).
     constexpr bool kU = MODE == kvc::kTcRowstatsProbes;
-    const int mt = warp >> 2, q = warp & 3;
+    constexpr int kSplit = 4 / NT;
+    constexpr int kCW = kBN / kSplit;
+    constexpr int kCh = 16;
+    const int q = warp & 3, mt = (warp >> 2) % NT, sp = warp / (4 * NT);
     const int r = mt * kBM + q * 32 + lane;
     const bool rv = r < rows;
     const int limit = seeds ? n - 1 : n - a.P + (r % a.P);
@@ -241,24 +256,20 @@ __global__ void __launch_bounds__((4 * NT + 2) * 32, 1)
       const int bf = t & 1;
       if (!*abort_flag && !kvcd::mbar_wait(&sm.tfull[bf], (uint32_t)((t >> 1) & 1))) *abort_flag = 1;
       tc_fence_after();
-      const int kt = k0 + t * kBN;
-      const uint32_t col0 = tbase + (uint32_t)((bf * NT + mt) * kBN);
-      float v[32];
-      tmem_ld16_nw(col0, *reinterpret_cast<float(*)[16]>(v));
-      tmem_ld16_nw(col0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+      const int kt = k0 + t * kBN + sp * kCW;
+      const uint32_t col0 = tbase + (uint32_t)((bf * NT + mt) * kBN + sp * kCW);
+      float v[kCh];
+      tmem_ld16_nw(col0, v);
       tmem_wait();
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        float vn[32];
-        if (c + 1 < kBN / 32) {                        // next chunk in flight
-          tmem_ld16_nw(col0 + (c + 1) * 32, *reinterpret_cast<float(*)[16]>(vn));
-          tmem_ld16_nw(col0 + (c + 1) * 32 + 16, *reinterpret_cast<float(*)[16]>(vn + 16));
-        }
-        const int i0 = kt + c * 32;
-        const bool fullc = rv && i0 + 31 < k1 && i0 + 31 <= limit;
+      for (int c = 0; c < kCW / kCh; ++c) {
+        float vn[kCh];
+        if (c + 1 < kCW / kCh) tmem_ld16_nw(col0 + (c + 1) * kCh, vn);   // next batch in flight
+        const int i0 = kt + c * kCh;
+        const bool fullc = rv && i0 + kCh - 1 < k1 && i0 + kCh - 1 <= limit;
         float mx = m;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < kCh; ++j) {
           float sv = v[j] * a.q_scale2;
           if (!fullc) sv = (rv && i0 + j < k1 && i0 + j <= limit) ? sv : -INFINITY;
           v[j] = sv;
@@ -272,14 +283,14 @@ __global__ void __launch_bounds__((4 * NT + 2) * 32, 1)
             cl *= sc;
           }
           m = mx;
-          float e[32], d[32];
+          float e[kCh], d[kCh];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
+          for (int j = 0; j < kCh; ++j) {
             e[j] = exp2f(v[j] - mx);                   // -inf -> 0
             if (kU) d[j] = (fullc || v[j] != -INFINITY) ? e[j] * (v[j] - mx) : 0.f;
           }
 #pragma unroll
-          for (int w = 16; w >= 1; w >>= 1)
+          for (int w = kCh / 2; w >= 1; w >>= 1)
 #pragma unroll
             for (int j = 0; j < w; ++j) {
               e[j] += e[j + w];
@@ -294,17 +305,40 @@ __global__ void __launch_bounds__((4 * NT + 2) * 32, 1)
             u = tu;
           }
         }
-        if (c + 1 < kBN / 32) {
+        if (c + 1 < kCW / kCh) {
           tmem_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = vn[j];
+          for (int j = 0; j < kCh; ++j) v[j] = vn[j];
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) kvcd::mbar_arrive(&sm.tempty[bf]);
     }
-    if (part_out && rv) { part_out[r * 3] = m; part_out[r * 3 + 1] = l; part_out[r * 3 + 2] = u; }
+    // the column shares of each row: share 0 adds the others in share order
+    if (sp > 0) {
+      sm.xch[sp - 1][r][0] = m;
+      sm.xch[sp - 1][r][1] = l;
+      sm.xch[sp - 1][r][2] = u;
+    }
+    named_bar(1, kEpiWarps * 32);
+    if (sp == 0) {
+#pragma unroll
+      for (int o = 0; o < kSplit - 1; ++o) {
+        const float mo = sm.xch[o][r][0], lo = sm.xch[o][r][1], uo = sm.xch[o][r][2];
+        const float M = fmaxf(m, mo);
+        if (M != -INFINITY) {
+          const float f0 = m == -INFINITY ? 0.f : exp2f(m - M);
+          const float f1 = mo == -INFINITY ? 0.f : exp2f(mo - M);
+          if (kU)
+            u = (m == -INFINITY ? 0.f : f0 * (u + (m - M) * l)) +
+                (mo == -INFINITY ? 0.f : f1 * (uo + (mo - M) * lo));
+          l = f0 * l + f1 * lo;
+          m = M;
+        }
+      }
+      if (part_out && rv) { part_out[r * 3] = m; part_out[r * 3 + 1] = l; part_out[r * 3 + 2] = u; }
+    }
   }
 
   // ---- teardown: every role has finished; wait out copies of an aborted run
@@ -1065,7 +1099,7 @@ int launch(const CUtensorMap& map, const kvc::ProbeTcArgs& a, cudaStream_t s) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return KVC_ECUDA;
   dim3 grid(a.n_chunks, (unsigned)((long long)a.B * a.L * a.H));
-  probe_tc_kernel<NT, MODE><<<grid, (4 * NT + 2) * 32, smem, s>>>(map, a);
+  probe_tc_kernel<NT, MODE><<<grid, kRsThreads, smem, s>>>(map, a);
   kvc::count_launch();
   return kvc::cuda_status(cudaGetLastError());
 }
