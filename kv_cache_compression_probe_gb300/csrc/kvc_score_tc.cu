@@ -361,16 +361,17 @@ __global__ void __maxnreg__(kRsMaxRegs)
 // sit on the TMEM lanes: S^T[128 keys x N rows] = K_tile Q^T (K tile = A
 // operand straight from the TMA ring, the query rows = K-major B operand; FEATS
 // N = 256 probe rows as two N = 128 products, PROP N = P <= 128 seed rows).
-// One epilogue thread owns one key and sums over its columns without any
-// cross-thread reduction; FEATS splits the 256 columns between two warp halves
-// that meet once per tile.
+// Sixteen epilogue warps: warp w reads lane quarter w % 4 (32 keys) and
+// column share w / 4 (a quarter of the buffer's columns, in 16-column
+// batches); the four shares of a key meet once per tile in shared memory and
+// share 0 adds them in share order.
 template <int NT>
 struct TcTSmem {
   alignas(1024) unsigned char A[NT][2][kBlockBytes];       // query rows (B operand), swizzled
   alignas(1024) unsigned char Bt[kStages][2][kBlockBytes]; // key tiles (A operand), swizzled
   alignas(16) float col_a[NT * kBM];                        // per row: base-2 LSE (+inf: no row)
   alignas(16) float col_b[NT * kBM];                        // per row: H (FEATS) or seed weight (PROP)
-  float xch[kBN][9];                                        // FEATS: second half's per-key sums
+  float xch[3][kBN][9];                                     // shares 1..3: per-key sums
   uint64_t full[kStages], empty[kStages], tfull[2], tempty[2];
   uint32_t tmem_base;
   int abort;
@@ -378,11 +379,11 @@ struct TcTSmem {
 };
 
 template <int MODE, int PN>
-__global__ void __launch_bounds__((MODE == kvc::kTcFeats ? 8 : 4) * 32 + 64, 1)
+__global__ void __maxnreg__(kRsMaxRegs)
     probe_tcT_kernel(const __grid_constant__ CUtensorMap kmap, kvc::ProbeTcArgs a) {
   constexpr int NT = MODE == kvc::kTcFeats ? 2 : 1;          // 128-row blocks of B
-  constexpr int kEpiWarps = MODE == kvc::kTcFeats ? 8 : 4;
-  constexpr int kThreads = kEpiWarps * 32 + 64;
+  constexpr int kEpiWarps = kRsEpiWarps;
+  constexpr int kThreads = kRsThreads;
   constexpr int kN = MODE == kvc::kTcFeats ? 256 : PN;       // columns per TMEM buffer (PROP: PN >= P)
   extern __shared__ __align__(1024) unsigned char tt_raw[];
   TcTSmem<NT>& sm = *reinterpret_cast<TcTSmem<NT>*>(
@@ -489,12 +490,13 @@ __global__ void __launch_bounds__((MODE == kvc::kTcFeats ? 8 : 4) * 32 + 64, 1)
     }
   } else {
     // ---------------------------------------------------------------- epilogue: thread = key
-    const int half = MODE == kvc::kTcFeats ? (warp >> 2) : 0;
-    const int q = warp & 3;
+    constexpr int kCW = kN / 4;                      // columns of one share
+    constexpr int kCh = 16;                          // columns per batch
+    static_assert(kCW % kCh == 0, "share width");
+    const int sp = warp >> 2, q = warp & 3;
     const int kl = q * 32 + lane;                    // key within the tile (TMEM lane)
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     volatile int* abort_flag = &sm.abort;
-    constexpr int kChunks = MODE == kvc::kTcFeats ? 4 : PN / 32;   // 32-column chunks per thread
     for (int t = 0; t < ntiles; ++t) {
       const int bf = t & 1;
       if (!*abort_flag && !kvcd::mbar_wait(&sm.tfull[bf], (uint32_t)((t >> 1) & 1))) *abort_flag = 1;
@@ -507,24 +509,20 @@ __global__ void __launch_bounds__((MODE == kvc::kTcFeats ? 8 : 4) * 32 + 64, 1)
       float gs[8], sh = 0.f, acc = 0.f;
 #pragma unroll
       for (int g = 0; g < 8; ++g) gs[g] = 0.f;
-      float v[32];
-      tmem_ld16_nw(tmem + lane_off + (uint32_t)(bf * kN + half * 128), *reinterpret_cast<float(*)[16]>(v));
-      tmem_ld16_nw(tmem + lane_off + (uint32_t)(bf * kN + half * 128 + 16), *reinterpret_cast<float(*)[16]>(v + 16));
+      const uint32_t col0 = tmem + lane_off + (uint32_t)(bf * kN + sp * kCW);
+      float v[kCh];
+      tmem_ld16_nw(col0, v);
       tmem_wait();
 #pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        float vn[32];
-        if (c + 1 < kChunks) {                       // next chunk in flight while this one computes
-          const uint32_t col = tmem + lane_off + (uint32_t)(bf * kN + half * 128 + (c + 1) * 32);
-          tmem_ld16_nw(col, *reinterpret_cast<float(*)[16]>(vn));
-          tmem_ld16_nw(col + 16, *reinterpret_cast<float(*)[16]>(vn + 16));
-        }
-        const int cb = half * 128 + c * 32;          // first column of the chunk
+      for (int c = 0; c < kCW / kCh; ++c) {
+        float vn[kCh];
+        if (c + 1 < kCW / kCh) tmem_ld16_nw(col0 + (c + 1) * kCh, vn);   // next batch in flight
+        const int cb = sp * kCW + c * kCh;           // first column of the batch
         const float4* ca = reinterpret_cast<const float4*>(&sm.col_a[cb]);
         const float4* cbv = reinterpret_cast<const float4*>(&sm.col_b[cb]);
         float cs = 0.f, chs = 0.f;
 #pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
+        for (int j4 = 0; j4 < kCh / 4; ++j4) {
           const float4 la = ca[j4], lb = cbv[j4];
           const float las[4] = {la.x, la.y, la.z, la.w}, lbs[4] = {lb.x, lb.y, lb.z, lb.w};
 #pragma unroll
@@ -544,35 +542,45 @@ __global__ void __launch_bounds__((MODE == kvc::kTcFeats ? 8 : 4) * 32 + 64, 1)
           }
         }
         if (MODE == kvc::kTcFeats) {
-          const int head = cb / a.P;                 // P % 32 == 0: one head per chunk
+          const int head = cb / a.P;                 // P % 32 == 0: one head per batch
 #pragma unroll
           for (int g = 0; g < 8; ++g)
             if (g == head) gs[g] += cs;
           sh += chs;
         }
-        if (c + 1 < kChunks) {
+        if (c + 1 < kCW / kCh) {
           tmem_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = vn[j];
+          for (int j = 0; j < kCh; ++j) v[j] = vn[j];
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) kvcd::mbar_arrive(&sm.tempty[bf]);
-      if (MODE == kvc::kTcProp) {
-        if (kvalid) a.rel[row0 + key] = a.feats[(row0 + key) * 5] + a.hop_weight * acc;
-      } else {
-        if (half == 1) {
+      // the four shares of these keys: share 0 adds the others in share order
+      if (sp > 0) {
+        if (MODE == kvc::kTcFeats) {
 #pragma unroll
-          for (int g = 0; g < 8; ++g) sm.xch[kl][g] = gs[g];
-          sm.xch[kl][8] = sh;
+          for (int g = 0; g < 8; ++g) sm.xch[sp - 1][kl][g] = gs[g];
+          sm.xch[sp - 1][kl][8] = sh;
+        } else {
+          sm.xch[sp - 1][kl][0] = acc;
         }
-        named_bar(1 + q, 64);                        // warps q and q + 4 hold the same keys
-        if (half == 0 && kvalid) {
-          float sa = 0.f, mean = 0.f;
+      }
+      named_bar(1 + q, 128);                         // warps q, q + 4, q + 8, q + 12
+      if (sp == 0 && kvalid) {
+        if (MODE == kvc::kTcProp) {
 #pragma unroll
-          for (int g = 0; g < 8; ++g) gs[g] += sm.xch[kl][g];
-          sh += sm.xch[kl][8];
+          for (int o = 0; o < 3; ++o) acc += sm.xch[o][kl][0];
+          a.rel[row0 + key] = a.feats[(row0 + key) * 5] + a.hop_weight * acc;
+        } else {
+#pragma unroll
+          for (int o = 0; o < 3; ++o) {
+#pragma unroll
+            for (int g = 0; g < 8; ++g) gs[g] += sm.xch[o][kl][g];
+            sh += sm.xch[o][kl][8];
+          }
+          float sa = 0.f, mean = 0.f;
 #pragma unroll
           for (int g = 0; g < 8; ++g) sa += gs[g];
           const float invP = 1.f / (float)a.P;
@@ -592,8 +600,8 @@ __global__ void __launch_bounds__((MODE == kvc::kTcFeats ? 8 : 4) * 32 + 64, 1)
           f[3] = sa > 0.f ? sh / sa : 0.f;
           a.rel[row0 + key] = alpha;
         }
-        named_bar(1 + q, 64);                        // xch is free for the next tile
       }
+      named_bar(1 + q, 128);                         // xch is free for the next tile
     }
   }
 
@@ -1081,7 +1089,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 template <int MODE, int PN>
 int launch_t(const CUtensorMap& map, const kvc::ProbeTcArgs& a, cudaStream_t s) {
   constexpr int NT = MODE == kvc::kTcFeats ? 2 : 1;
-  constexpr int kThreads = (MODE == kvc::kTcFeats ? 8 : 4) * 32 + 64;
+  constexpr int kThreads = kRsThreads;
   const size_t smem = sizeof(TcTSmem<NT>) + 1024;
   cudaError_t e = cudaFuncSetAttribute(probe_tcT_kernel<MODE, PN>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
