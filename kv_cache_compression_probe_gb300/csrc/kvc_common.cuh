@@ -143,6 +143,14 @@ __device__ __forceinline__ void warp_sum4(float (&v)[4], int lane) {
   for (int g = 0; g < 4; ++g) v[g] = __shfl_sync(KVC_FULL_MASK, t, 8 * g);
 }
 
+// 2^x with the PTX approximate base-2 exponential instruction; results below
+// 2^-126 flush to zero (the callers sum probabilities relative to a maximum).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(KVC_FULL_MASK, v, o));

@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(256, 2)
           const int cidx = (key & 63) >> 3;
 #pragma unroll
           for (int g = 0; g < G; ++g) {
-            const float pv = sv[t][g] == -INFINITY ? 0.f : exp2f(sv[t][g] - mh[g]);
+            const float pv = sv[t][g] == -INFINITY ? 0.f : kvcd::ex2(sv[t][g] - mh[g]);
             const __nv_bfloat16 p16 = __float2bfloat16_rn(pv);
             lh[g] += __bfloat162float(p16);
             *reinterpret_cast<__nv_bfloat16*>(pb + g * 128 + ((cidx ^ (g & 7)) << 4)) = p16;

@@ -267,14 +267,20 @@ __global__ void __maxnreg__(kRsMaxRegs)
         if (c + 1 < kCW / kCh) tmem_ld16_nw(col0 + (c + 1) * kCh, vn);   // next batch in flight
         const int i0 = kt + c * kCh;
         const bool fullc = rv && i0 + kCh - 1 < k1 && i0 + kCh - 1 <= limit;
-        float mx = m;
+        float mt4[kCh / 2];
 #pragma unroll
         for (int j = 0; j < kCh; ++j) {
           float sv = v[j] * a.q_scale2;
           if (!fullc) sv = (rv && i0 + j < k1 && i0 + j <= limit) ? sv : -INFINITY;
           v[j] = sv;
-          mx = fmaxf(mx, sv);
         }
+#pragma unroll
+        for (int j = 0; j < kCh / 2; ++j) mt4[j] = fmaxf(v[j], v[j + kCh / 2]);   // max as a tree
+#pragma unroll
+        for (int w = kCh / 4; w >= 1; w >>= 1)
+#pragma unroll
+          for (int j = 0; j < w; ++j) mt4[j] = fmaxf(mt4[j], mt4[j + w]);
+        const float mx = fmaxf(m, mt4[0]);
         if (mx != -INFINITY) {
           if (mx > m && m != -INFINITY) {
             const float sc = exp2f(m - mx);
@@ -286,7 +292,7 @@ __global__ void __maxnreg__(kRsMaxRegs)
           float e[kCh], d[kCh];
 #pragma unroll
           for (int j = 0; j < kCh; ++j) {
-            e[j] = exp2f(v[j] - mx);                   // -inf -> 0
+            e[j] = kvcd::ex2(v[j] - mx);               // -inf -> 0
             if (kU) d[j] = (fullc || v[j] != -INFINITY) ? e[j] * (v[j] - mx) : 0.f;
           }
 #pragma unroll
@@ -528,7 +534,7 @@ __global__ void __maxnreg__(kRsMaxRegs)
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int j = j4 * 4 + u;
-            float e = exp2f(fmaf(v[j], a.q_scale2, -las[u]));
+            float e = kvcd::ex2(fmaf(v[j], a.q_scale2, -las[u]));
             if (!full_cols) {
               const bool ok = kvalid && (MODE == kvc::kTcProp || ((cb + j) % a.P) >= thr);
               e = ok ? e : 0.f;
@@ -915,7 +921,7 @@ __global__ void __maxnreg__(kNodeMaxRegs)
 #pragma unroll
         for (int j = 0; j < 15; ++j) {
           const float sc = (d0[j] + d1[j] + d2[j]) * a.q_scale2 + lmv[j] * 1.4426950408889634f - l2;
-          ah[j] = rv ? exp2f(sc) : 0.f;
+          ah[j] = rv ? kvcd::ex2(sc) : 0.f;
         }
       }
       int cnt0, cnt1;
@@ -940,7 +946,7 @@ __global__ void __maxnreg__(kNodeMaxRegs)
           float av[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u)
-            av[u] = (rv && t + u < cntl) ? exp2f(v[t + u] * a.q_scale2 - l2) : 0.f;
+            av[u] = (rv && t + u < cntl) ? kvcd::ex2(v[t + u] * a.q_scale2 - l2) : 0.f;
           sacc += av[0] + av[1];
           // a = p0 + p1 + p2 in bf16 pairs (element t in the low half)
           const __nv_bfloat162 p0 = __floats2bfloat162_rn(av[0], av[1]);
