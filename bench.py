@@ -302,6 +302,33 @@ def evict_leg(p, cfg, seqs, K, V, q_all, kn_all, vn_all, D, dev, stream):
                     "evicted to the budget at the first step, then one entry per step"}
 
 
+def scoring_gemm(comp, K, V, Qp, bounds, n_slots, cfg, tokens, tc_peak, dev):
+    """Device time of the probe-times-key contraction passes of one kvc_score
+    call (CUDA events the library records between its phases when phase
+    timing is on; one untimed call outside the timed region).  The
+    row-statistics pass and the per-key feature pass each contract every key
+    with every probe row: 2 * (G*P) * n * d flops per (b, l, h)."""
+    import torch
+    from kv_cache_compression_probe_gb300 import kvc
+    torch.cuda.synchronize(dev)
+    kvc.kvc_set_phase_timing(True)
+    try:
+        comp.score(K, V, Qp, bounds, n_slots)
+        ms = kvc.kvc_score_phase_ms(5)
+    finally:
+        kvc.kvc_set_phase_timing(False)
+    flops = 2.0 * cfg.G * cfg.P * tokens * cfg.L * cfg.H * cfg.d   # one contraction pass
+    out = {}
+    for name, t in (("probe_rowstats", ms[0]), ("probe_feats", ms[1])):
+        tf = flops / (t * 1e-3) / 1e12
+        out[name] = {"ms": t, "tflops": tf, "frac_of_bf16_peak": tf / tc_peak}
+    out["other_phases_ms"] = {"norms_and_hops": ms[2], "prototypes": ms[3],
+                              "node_statistics": ms[4]}
+    out["note"] = ("CUDA events between kvc_score's phases (one untimed call); flops = "
+                   "2 * G*P * n * d per (b, l, h); peak = measured bf16 burst")
+    return out
+
+
 def full_bytes_ratio(cfg, seqs, avg_entries, D):
     """Entries the full cache streams per decode step over the compressed one."""
     full = sum(s[0] for s in seqs) * cfg.L * cfg.H
@@ -474,6 +501,9 @@ def run_gpu(args, cfg, rank, world):
     full_ms = None if args.profile else full_cache_decode_ms(p, cfg, seqs, K, V, q_all, kn_all,
                                                             vn_all, D, dev, stream)
 
+    gemm = None if args.profile else scoring_gemm(comp, K, V, Qp, bounds, n_slots, cfg,
+                                                  sum(s[0] for s in seqs), measured_peaks()[1],
+                                                  dev)
     evict = None
     if args.evict:
         evict = evict_leg(p, cfg, seqs, K, V, q_all, kn_all, vn_all, D, dev, stream)
@@ -568,6 +598,7 @@ def run_gpu(args, cfg, rank, world):
         "score_hbm_frac": score_bytes / (score_ms * 1e-3) / 1e9 / hbm,
         "score_tflops": score_flops / (score_ms * 1e-3) / 1e12,
         "score_tc_frac_of_bf16_peak": score_flops / (score_ms * 1e-3) / 1e12 / tc,
+        "scoring_gemm": gemm,
         "e2e": {"value": job_throughput(tokens, world, e2e), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e},
         "evict_per_step_next_f2": evict,

@@ -157,6 +157,18 @@ int kvc_score(const kvc_params* p, const int32_t* ctx_len, const void* K, const 
               float* lse, float* feats, float* relevance, float* op_util, int32_t* op_cost,
               void* workspace, size_t ws_bytes, void* stream);
 
+/* Phase timing of kvc_score's tensor-core path (a measurement aid; no
+ * counterpart on the pages).  With timing on, each kvc_score call on that
+ * path records CUDA events on its stream between its phases (not for use
+ * during stream capture); the events are created on the device current at
+ * the first timed call, and calls on other devices are not timed.
+ * kvc_score_phase_ms waits for the last timed call and writes up to n
+ * durations in ms: [0] probe row statistics, [1] per-key features, [2] value
+ * norms and relevance hops, [3] prototypes, [4] node statistics.  Returns the
+ * number written, or KVC_EINVAL when no timed call completed its phases. */
+void kvc_set_phase_timing(int on);
+int kvc_score_phase_ms(float* ms_out /* host */, int32_t n);
+
 /* a5: per-sequence budget, capped singleton floor, global greedy Add/Split
  * auction ([GK] "Core idea" budget regions, "Exact-information safeguard",
  * "04 Top-down budget flow").  The result is identical to processing one

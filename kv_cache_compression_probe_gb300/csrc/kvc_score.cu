@@ -24,6 +24,9 @@
 // registers and the key tile broadcast from shared memory.
 #include <math.h>
 
+#include <atomic>
+#include <mutex>
+
 #include <algorithm>
 #include <type_traits>
 
@@ -1129,6 +1132,36 @@ Layout layout(const kvc_params* p) {
   return l;
 }
 
+// Optional phase timing of the tensor-core path (kvc_set_phase_timing): CUDA
+// events recorded on the call's stream between its phases.
+constexpr int kPhaseMarks = 7;
+std::atomic<int> g_phase_on{0};
+std::mutex g_phase_mu;
+cudaEvent_t g_phase_ev[kPhaseMarks];
+bool g_phase_made = false, g_phase_valid = false;
+int g_phase_dev = -1;
+
+void phase_mark(int i, cudaStream_t s) {
+  if (g_phase_on.load(std::memory_order_relaxed)) cudaEventRecord(g_phase_ev[i], s);
+}
+// Called once per kvc_score: creates the events on first use (on the current
+// device) and reports whether this call is timed.
+bool phase_begin() {
+  if (!g_phase_on.load(std::memory_order_relaxed)) return false;
+  std::lock_guard<std::mutex> g(g_phase_mu);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (g_phase_made && dev != g_phase_dev) return false;
+  if (!g_phase_made) {
+    for (int i = 0; i < kPhaseMarks; ++i)
+      if (cudaEventCreate(&g_phase_ev[i]) != cudaSuccess) return false;
+    g_phase_made = true;
+    g_phase_dev = dev;
+  }
+  g_phase_valid = false;
+  return true;
+}
+
 template <typename T, int D>
 int launch_all(const kvc_params* p, ScoreArgs& a, cudaStream_t s) {
   const long long blh = kvc::lh_count(p);
@@ -1158,10 +1191,15 @@ int launch_all(const kvc_params* p, ScoreArgs& a, cudaStream_t s) {
     t.q_scale2 = a.q_scale2; t.hop_weight = p->hop_weight;
     a.n_chunks = t.n_chunks;                        // rowcombine loops over these partials
     const int64_t rows_total = p->total_ctx * p->L * p->H;
+    const bool timed = phase_begin();
     int st;
+    if (timed) phase_mark(0, s);
     if ((st = kvc::probe_tc_pass(kvc::kTcRowstatsProbes, t, rows_total, s)) != KVC_OK) return st;
+    if (timed) phase_mark(1, s);
     rowcombine_kernel<false><<<(unsigned)blh, 256, 0, s>>>(*p, a);
+    if (timed) phase_mark(2, s);
     if ((st = kvc::probe_tc_pass(kvc::kTcFeats, t, rows_total, s)) != KVC_OK) return st;
+    if (timed) phase_mark(3, s);
     const int vchunks = (p->n_max + kVnormRows - 1) / kVnormRows;
     vnorm_kernel<T, D><<<dim3(vchunks, (unsigned)blh), kVnormRows, 0, s>>>(*p, a);
     nu_finish_kernel<<<(unsigned)((blh + 127) / 128), 128, 0, s>>>(*p, a, vchunks);
@@ -1174,13 +1212,20 @@ int launch_all(const kvc_params* p, ScoreArgs& a, cudaStream_t s) {
       launches += 2;
     }
     // prototypes, tensor-core node statistics, utilities
+    if (timed) phase_mark(4, s);
     proto_kernel<T, D><<<(unsigned)((blh * p->S_max + 3) / 4), 128, 0, s>>>(*p, a, a.proto);
+    if (timed) phase_mark(5, s);
     kvc::NodeTcArgs nd;
     nd.ctx_len = a.ctx_len; nd.K = a.K; nd.V = a.V; nd.Qp = a.Qp; nd.lse2 = a.lse2; nd.ok = a.ok;
     nd.bounds = a.bounds; nd.n_slots = a.n_slots; nd.proto = a.proto; nd.npart = a.npart;
     nd.err = a.err; nd.B = p->B; nd.L = p->L; nd.H = p->H; nd.G = p->G; nd.P = p->P;
     nd.S_max = p->S_max; nd.q_scale2 = a.q_scale2;
     if ((st = kvc::nodes_tc_pass(nd, rows_total, s)) != KVC_OK) return st;
+    if (timed) {
+      phase_mark(6, s);
+      std::lock_guard<std::mutex> g(g_phase_mu);
+      g_phase_valid = true;
+    }
     const long long trees = blh * p->S_max;
     ops_kernel<<<(unsigned)((trees + 127) / 128), 128, 0, s>>>(*p, a, a.proto, a.npart,
                                                                (p->G * p->P + 127) / 128);
@@ -1215,6 +1260,23 @@ int launch_all(const kvc_params* p, ScoreArgs& a, cudaStream_t s) {
 namespace kvc {
 size_t score_workspace_bytes(const kvc_params* p) { return layout(p).total; }
 }  // namespace kvc
+
+extern "C" void kvc_set_phase_timing(int on) { g_phase_on.store(on ? 1 : 0); }
+
+extern "C" int kvc_score_phase_ms(float* ms_out, int32_t n) {
+  if (!ms_out || n < 1) return KVC_EINVAL;
+  std::lock_guard<std::mutex> g(g_phase_mu);
+  if (!g_phase_made || !g_phase_valid) return KVC_EINVAL;
+  // phases: row statistics, per-key features, norms and hops, prototypes, node statistics
+  const int pairs[5][2] = {{0, 1}, {2, 3}, {3, 4}, {4, 5}, {5, 6}};
+  if (cudaEventSynchronize(g_phase_ev[kPhaseMarks - 1]) != cudaSuccess) return KVC_ECUDA;
+  const int m = n < 5 ? n : 5;
+  for (int i = 0; i < m; ++i)
+    if (cudaEventElapsedTime(&ms_out[i], g_phase_ev[pairs[i][0]], g_phase_ev[pairs[i][1]]) !=
+        cudaSuccess)
+      return KVC_ECUDA;
+  return m;
+}
 
 extern "C" int kvc_score(const kvc_params* p, const int32_t* ctx_len, const void* K, const void* V,
                          const void* Qp, const float* rope_cos, const float* rope_sin,

@@ -24,7 +24,8 @@ KVC_WS_SCORE, KVC_WS_SELECT, KVC_WS_PACK, KVC_WS_DECODE, KVC_WS_PARTITION = rang
 EXPORTED = ("kvc_status_string", "kvc_last_cuda_error", "kvc_device_error", "kvc_launch_count", "kvc_workspace_bytes",
             "kvc_rope_table", "kvc_score", "kvc_select", "kvc_merge_pack", "kvc_decode_attn",
             "kvc_partition", "kvc_decode_attn_noalloc", "kvc_decode_attn_lse", "kvc_token_alpha",
-            "kvc_evict_workspace_bytes", "kvc_evict_topb")
+            "kvc_evict_workspace_bytes", "kvc_evict_topb", "kvc_set_phase_timing",
+            "kvc_score_phase_ms")
 
 
 class kvc_params(ctypes.Structure):
@@ -85,6 +86,9 @@ def lib():
         L.kvc_evict_workspace_bytes.restype = c_size_t
         L.kvc_evict_topb.argtypes = [_P, vp, c_int32, vp, c_double, c_int32] + [vp] * 7 + [c_size_t, vp]
         L.kvc_evict_topb.restype = c_int
+        L.kvc_set_phase_timing.argtypes = [c_int]; L.kvc_set_phase_timing.restype = None
+        L.kvc_score_phase_ms.argtypes = [ctypes.POINTER(c_float), c_int32]
+        L.kvc_score_phase_ms.restype = c_int
         L.kvc_partition.argtypes = [_P, vp, vp, c_int32, vp, vp, vp, vp, c_size_t, vp]
         L.kvc_partition.restype = c_int
         _lib = L
@@ -229,6 +233,19 @@ def kvc_evict_topb(p, alpha, n_seen, ratio, b_min, K, V, pos, logm, off_lh, len_
                                 float(ratio), int(b_min), _ptr(K), _ptr(V), _ptr(pos),
                                 _ptr(logm), _ptr(off_lh), _ptr(len_lh), w, wb, _stream(stream)),
            "kvc_evict_topb")
+
+
+def kvc_set_phase_timing(on: bool):
+    lib().kvc_set_phase_timing(1 if on else 0)
+
+
+def kvc_score_phase_ms(n: int = 5):
+    """Durations (ms) of the phases of the last timed kvc_score call."""
+    buf = (c_float * n)()
+    st = lib().kvc_score_phase_ms(buf, n)
+    if st < 0:
+        raise KvcError(st, "kvc_score_phase_ms")
+    return [float(buf[i]) for i in range(st)]
 
 
 def kvc_partition(p, ctx_len, hidden, dh, kappa, slot_bounds, n_slots, workspace, stream=None):
