@@ -20,6 +20,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "kvc_common.cuh"
 #include "kvc_internal.h"
@@ -267,23 +268,26 @@ __global__ void __maxnreg__(kRsMaxRegs)
         if (c + 1 < kCW / kCh) tmem_ld16_nw(col0 + (c + 1) * kCh, vn);   // next batch in flight
         const int i0 = kt + c * kCh;
         const bool fullc = rv && i0 + kCh - 1 < k1 && i0 + kCh - 1 <= limit;
-        float mt4[kCh / 2];
+        // One batch: the max is taken on the raw products (the scale is
+        // positive), each exponent argument t = S c - m is one FMA, and the
+        // masked form is separate code that only boundary batches run.
+        auto batch = [&](auto masked_tag) {
+          constexpr bool kMasked = decltype(masked_tag)::value;
+          float raw[kCh];
 #pragma unroll
-        for (int j = 0; j < kCh; ++j) {
-          float sv = v[j] * a.q_scale2;
-          if (!fullc) sv = (rv && i0 + j < k1 && i0 + j <= limit) ? sv : -INFINITY;
-          v[j] = sv;
-        }
+          for (int j = 0; j < kCh; ++j)
+            raw[j] = (!kMasked || (rv && i0 + j < k1 && i0 + j <= limit)) ? v[j] : -INFINITY;
+          float mt4[kCh / 2];
 #pragma unroll
-        for (int j = 0; j < kCh / 2; ++j) mt4[j] = fmaxf(v[j], v[j + kCh / 2]);   // max as a tree
+          for (int j = 0; j < kCh / 2; ++j) mt4[j] = fmaxf(raw[j], raw[j + kCh / 2]);
 #pragma unroll
-        for (int w = kCh / 4; w >= 1; w >>= 1)
+          for (int w = kCh / 4; w >= 1; w >>= 1)
 #pragma unroll
-          for (int j = 0; j < w; ++j) mt4[j] = fmaxf(mt4[j], mt4[j + w]);
-        const float mx = fmaxf(m, mt4[0]);
-        if (mx != -INFINITY) {
+            for (int j = 0; j < w; ++j) mt4[j] = fmaxf(mt4[j], mt4[j + w]);
+          if (kMasked && mt4[0] == -INFINITY) return;        // nothing valid in the batch
+          const float mx = fmaxf(m, mt4[0] * a.q_scale2);
           if (mx > m && m != -INFINITY) {
-            const float sc = exp2f(m - mx);
+            const float sc = kvcd::ex2(m - mx);
             if (kU) { u = sc * (u + (m - mx) * l); cu *= sc; }
             l *= sc;
             cl *= sc;
@@ -292,8 +296,9 @@ __global__ void __maxnreg__(kRsMaxRegs)
           float e[kCh], d[kCh];
 #pragma unroll
           for (int j = 0; j < kCh; ++j) {
-            e[j] = kvcd::ex2(v[j] - mx);               // -inf -> 0
-            if (kU) d[j] = (fullc || v[j] != -INFINITY) ? e[j] * (v[j] - mx) : 0.f;
+            const float tj = fmaf(raw[j], a.q_scale2, -mx);
+            e[j] = kvcd::ex2(tj);                            // -inf -> 0
+            if (kU) d[j] = (!kMasked || raw[j] != -INFINITY) ? e[j] * tj : 0.f;
           }
 #pragma unroll
           for (int w = kCh / 2; w >= 1; w >>= 1)
@@ -310,7 +315,9 @@ __global__ void __maxnreg__(kRsMaxRegs)
             cu = (tu - u) - yu;
             u = tu;
           }
-        }
+        };
+        if (fullc) batch(std::false_type{});
+        else batch(std::true_type{});
         if (c + 1 < kCW / kCh) {
           tmem_wait();
 #pragma unroll
@@ -527,26 +534,33 @@ __global__ void __maxnreg__(kRsMaxRegs)
         const float4* ca = reinterpret_cast<const float4*>(&sm.col_a[cb]);
         const float4* cbv = reinterpret_cast<const float4*>(&sm.col_b[cb]);
         float cs = 0.f, chs = 0.f;
+        // the masked form (keys past the chunk, causal probe limits) is
+        // separate code that only boundary keys run
+        auto batch = [&](auto masked_tag) {
+          constexpr bool kMasked = decltype(masked_tag)::value;
 #pragma unroll
-        for (int j4 = 0; j4 < kCh / 4; ++j4) {
-          const float4 la = ca[j4], lb = cbv[j4];
-          const float las[4] = {la.x, la.y, la.z, la.w}, lbs[4] = {lb.x, lb.y, lb.z, lb.w};
+          for (int j4 = 0; j4 < kCh / 4; ++j4) {
+            const float4 la = ca[j4], lb = cbv[j4];
+            const float las[4] = {la.x, la.y, la.z, la.w}, lbs[4] = {lb.x, lb.y, lb.z, lb.w};
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int j = j4 * 4 + u;
-            float e = kvcd::ex2(fmaf(v[j], a.q_scale2, -las[u]));
-            if (!full_cols) {
-              const bool ok = kvalid && (MODE == kvc::kTcProp || ((cb + j) % a.P) >= thr);
-              e = ok ? e : 0.f;
-            }
-            if (MODE == kvc::kTcFeats) {
-              cs += e;
-              chs = fmaf(e, lbs[u], chs);
-            } else {
-              acc = fmaf(lbs[u], e, acc);
+            for (int u = 0; u < 4; ++u) {
+              const int j = j4 * 4 + u;
+              float e = kvcd::ex2(fmaf(v[j], a.q_scale2, -las[u]));
+              if (kMasked) {
+                const bool ok = kvalid && (MODE == kvc::kTcProp || ((cb + j) % a.P) >= thr);
+                e = ok ? e : 0.f;
+              }
+              if (MODE == kvc::kTcFeats) {
+                cs += e;
+                chs = fmaf(e, lbs[u], chs);
+              } else {
+                acc = fmaf(lbs[u], e, acc);
+              }
             }
           }
-        }
+        };
+        if (full_cols) batch(std::false_type{});
+        else batch(std::true_type{});
         if (MODE == kvc::kTcFeats) {
           const int head = cb / a.P;                 // P % 32 == 0: one head per batch
 #pragma unroll
