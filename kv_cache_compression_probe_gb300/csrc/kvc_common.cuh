@@ -143,6 +143,16 @@ __device__ __forceinline__ void warp_sum4(float (&v)[4], int lane) {
   for (int g = 0; g < 4; ++g) v[g] = __shfl_sync(KVC_FULL_MASK, t, 8 * g);
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while its predecessor in the stream finishes;
+// pdl_wait() blocks until the predecessor grids have completed and their
+// memory is visible (immediately when there is no such predecessor), and
+// pdl_trigger() lets this grid's own dependents be scheduled early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 2^x with the PTX approximate base-2 exponential instruction; results below
 // 2^-126 flush to zero (the callers sum probabilities relative to a maximum).
 __device__ __forceinline__ float ex2(float x) {

@@ -28,6 +28,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <utility>
 
 #include "kvc_common.cuh"
 #include "kvc_decode_tc.h"
@@ -131,6 +132,8 @@ __device__ __forceinline__ int chunks_of(const kvc::DecodeTcArgs& a, int64_t i) 
 __global__ void __launch_bounds__(1024) decode_plan_kernel(kvc::DecodeTcArgs a, int64_t grid_items) {
   constexpr int kPer = 4;                             // entries kept in registers
   __shared__ long long wsum[32];
+  kvcd::pdl_trigger();
+  kvcd::pdl_wait();                                   // lengths from the previous step
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t per = (a.blh + 1023) / 1024;
   const int64_t b0 = min(a.blh, (int64_t)tid * per), b1 = min(a.blh, b0 + per);
@@ -215,8 +218,7 @@ __global__ void __launch_bounds__(256, 2)
     decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                      const __grid_constant__ CUtensorMap qmap, kvc::DecodeTcArgs a) {
   extern __shared__ __align__(1024) unsigned char dec_raw[];
-  const int n_items = *a.n_items;
-  if ((int)blockIdx.x >= n_items) return;
+  kvcd::pdl_trigger();
   DecSmem& sm = *reinterpret_cast<DecSmem*>((reinterpret_cast<uintptr_t>(dec_raw) + 1023) &
                                             ~uintptr_t(1023));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -247,6 +249,9 @@ __global__ void __launch_bounds__(256, 2)
   fence_before();
   __syncthreads();
   fence_after();
+  // the set-up above overlaps the plan kernel; the work list is read after it
+  kvcd::pdl_wait();
+  const int n_items = *a.n_items;
   const uint32_t tmem = sm.tmem;
   volatile int* abort_flag = &sm.abort;
   int last_issue[kSlots] = {-1, -1};                 // producer: last load per slot
@@ -476,6 +481,8 @@ __global__ void __launch_bounds__(256, 2)
 template <int G>
 __global__ void __launch_bounds__(128 * G) decode_merge_kernel(kvc::DecodeTcArgs a) {
   __shared__ float s_new[G];
+  kvcd::pdl_trigger();
+  kvcd::pdl_wait();                                   // the attention kernel's partials
   const int blh = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int len = a.len_lh[blh];
@@ -598,6 +605,24 @@ bool encode(CUtensorMap* m, const void* base, int64_t rows, int box_rows) {
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Launch with programmatic stream serialization (the kernel waits for its
+// predecessor with pdl_wait before reading what that predecessor writes).
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <int G>
 cudaError_t launch_attn(const CUtensorMap& km, const CUtensorMap& vm, const CUtensorMap& qm,
                         const kvc::DecodeTcArgs& a, unsigned grid, cudaStream_t s) {
@@ -605,9 +630,9 @@ cudaError_t launch_attn(const CUtensorMap& km, const CUtensorMap& vm, const CUte
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<G><<<grid, kThreadsTc, smem, s>>>(km, vm, qm, a);
-  decode_merge_kernel<G><<<(unsigned)a.blh, 128 * G, 0, s>>>(a);
-  return cudaGetLastError();
+  e = launch_pdl(decode_tc_kernel<G>, dim3(grid), dim3(kThreadsTc), smem, s, km, vm, qm, a);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(decode_merge_kernel<G>, dim3((unsigned)a.blh), dim3(128 * G), 0, s, a);
 }
 
 int sm_count() {
@@ -662,8 +687,7 @@ int decode_tc_launch(const DecodeTcArgs& a, cudaStream_t s) {
   const int sms = sm_count();
   if (sms <= 0) return KVC_ECUDA;
   const unsigned grid = (unsigned)std::min<int64_t>(bound, 2LL * sms);   // persistent, 2 per SM
-  decode_plan_kernel<<<1, 1024, 0, s>>>(a, bound);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(decode_plan_kernel, dim3(1), dim3(1024), 0, s, a, bound);
   if (e != cudaSuccess) return cuda_status(e);
   switch (a.G) {
     case 1: e = launch_attn<1>(km, vm, qm, a, grid, s); break;
