@@ -107,6 +107,38 @@ __device__ __forceinline__ void tmem_ld16_nw(uint32_t taddr, float (&v)[16]) {
 __device__ __forceinline__ void tmem_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 
+// Packed pairs of fp32 (a in the low half): element-wise a * b + c, a * b,
+// a + b on both halves with one instruction each.
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 uf2(uint64_t x) {
+  float2 f;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(x));
+  return f;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float hsum2(uint64_t x) {
+  const float2 f = uf2(x);
+  return f.x + f.y;
+}
+
 // Row-statistics passes: 16 epilogue warps; the NT row blocks' lane quarters
 // are covered 4 / NT times, each copy taking its share of a tile's columns.
 constexpr int kRsEpiWarps = 16;
@@ -293,25 +325,50 @@ __global__ void __maxnreg__(kRsMaxRegs)
             cl *= sc;
           }
           m = mx;
-          float e[kCh], d[kCh];
+          float esum, dsum = 0.f;
+          if constexpr (!kMasked) {
+            // arguments, products and the two tree sums on packed pairs
+            const uint64_t c2 = f2(a.q_scale2, a.q_scale2), nm2 = f2(-mx, -mx);
+            uint64_t e2[kCh / 2], d2[kCh / 2];
 #pragma unroll
-          for (int j = 0; j < kCh; ++j) {
-            const float tj = fmaf(raw[j], a.q_scale2, -mx);
-            e[j] = kvcd::ex2(tj);                            // -inf -> 0
-            if (kU) d[j] = (!kMasked || raw[j] != -INFINITY) ? e[j] * tj : 0.f;
-          }
-#pragma unroll
-          for (int w = kCh / 2; w >= 1; w >>= 1)
-#pragma unroll
-            for (int j = 0; j < w; ++j) {
-              e[j] += e[j + w];
-              if (kU) d[j] += d[j + w];
+            for (int j = 0; j < kCh / 2; ++j) {
+              const uint64_t t2 = fma2(f2(raw[2 * j], raw[2 * j + 1]), c2, nm2);
+              const float2 tt = uf2(t2);
+              e2[j] = f2(kvcd::ex2(tt.x), kvcd::ex2(tt.y));
+              if (kU) d2[j] = mul2(e2[j], t2);
             }
-          const float yl = e[0] - cl, tl = l + yl;
+#pragma unroll
+            for (int w = kCh / 4; w >= 1; w >>= 1)
+#pragma unroll
+              for (int j = 0; j < w; ++j) {
+                e2[j] = add2(e2[j], e2[j + w]);
+                if (kU) d2[j] = add2(d2[j], d2[j + w]);
+              }
+            esum = hsum2(e2[0]);
+            if (kU) dsum = hsum2(d2[0]);
+          } else {
+            float e[kCh], d[kCh];
+#pragma unroll
+            for (int j = 0; j < kCh; ++j) {
+              const float tj = fmaf(raw[j], a.q_scale2, -mx);
+              e[j] = kvcd::ex2(tj);                          // -inf -> 0
+              if (kU) d[j] = raw[j] != -INFINITY ? e[j] * tj : 0.f;
+            }
+#pragma unroll
+            for (int w = kCh / 2; w >= 1; w >>= 1)
+#pragma unroll
+              for (int j = 0; j < w; ++j) {
+                e[j] += e[j + w];
+                if (kU) d[j] += d[j + w];
+              }
+            esum = e[0];
+            if (kU) dsum = d[0];
+          }
+          const float yl = esum - cl, tl = l + yl;
           cl = (tl - l) - yl;
           l = tl;
           if (kU) {
-            const float yu = d[0] - cu, tu = u + yu;
+            const float yu = dsum - cu, tu = u + yu;
             cu = (tu - u) - yu;
             u = tu;
           }
@@ -384,7 +441,7 @@ struct TcTSmem {
   alignas(1024) unsigned char Bt[kStages][2][kBlockBytes]; // key tiles (A operand), swizzled
   alignas(16) float col_a[NT * kBM];                        // per row: base-2 LSE (+inf: no row)
   alignas(16) float col_b[NT * kBM];                        // per row: H (FEATS) or seed weight (PROP)
-  float xch[3][kBN][9];                                     // shares 1..3: per-key sums
+  float xch[2][3][kBN][9];                                  // shares 1..3: per-key sums, by tile parity
   uint64_t full[kStages], empty[kStages], tfull[2], tempty[2];
   uint32_t tmem_base;
   int abort;
@@ -577,28 +634,32 @@ __global__ void __maxnreg__(kRsMaxRegs)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) kvcd::mbar_arrive(&sm.tempty[bf]);
-      // the four shares of these keys: share 0 adds the others in share order
+      // the four shares of these keys: share 0 adds the others in share order.
+      // The exchange buffer alternates with the tile, so one barrier per tile
+      // suffices: a share writes buffer t & 1 again only after the barrier of
+      // tile t + 1, which share 0 reaches after reading it.
+      float (*xc)[kBN][9] = sm.xch[t & 1];
       if (sp > 0) {
         if (MODE == kvc::kTcFeats) {
 #pragma unroll
-          for (int g = 0; g < 8; ++g) sm.xch[sp - 1][kl][g] = gs[g];
-          sm.xch[sp - 1][kl][8] = sh;
+          for (int g = 0; g < 8; ++g) xc[sp - 1][kl][g] = gs[g];
+          xc[sp - 1][kl][8] = sh;
         } else {
-          sm.xch[sp - 1][kl][0] = acc;
+          xc[sp - 1][kl][0] = acc;
         }
       }
       named_bar(1 + q, 128);                         // warps q, q + 4, q + 8, q + 12
       if (sp == 0 && kvalid) {
         if (MODE == kvc::kTcProp) {
 #pragma unroll
-          for (int o = 0; o < 3; ++o) acc += sm.xch[o][kl][0];
+          for (int o = 0; o < 3; ++o) acc += xc[o][kl][0];
           a.rel[row0 + key] = a.feats[(row0 + key) * 5] + a.hop_weight * acc;
         } else {
 #pragma unroll
           for (int o = 0; o < 3; ++o) {
 #pragma unroll
-            for (int g = 0; g < 8; ++g) gs[g] += sm.xch[o][kl][g];
-            sh += sm.xch[o][kl][8];
+            for (int g = 0; g < 8; ++g) gs[g] += xc[o][kl][g];
+            sh += xc[o][kl][8];
           }
           float sa = 0.f, mean = 0.f;
 #pragma unroll
@@ -621,7 +682,6 @@ __global__ void __maxnreg__(kRsMaxRegs)
           a.rel[row0 + key] = alpha;
         }
       }
-      named_bar(1 + q, 128);                         // xch is free for the next tile
     }
   }
 
@@ -698,22 +758,6 @@ __device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr, uint32_t lbo_b
 }
 
 
-// Packed pair of fp32 (a in the low half) and d = a * b + d on both halves.
-__device__ __forceinline__ uint64_t f2(float a, float b) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ float hsum2(uint64_t x) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
-  return lo + hi;
-}
 
 // Spare TMEM columns 176..207 (no MMA writes there) hold the per-row partial
 // sums of node j from group g: pair parity, node parity, group, (dd, uu).
