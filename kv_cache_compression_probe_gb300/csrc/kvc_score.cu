@@ -1095,8 +1095,9 @@ int chunk_for(const kvc_params* p) {
   return c;
 }
 
-// tensor-core passes: 16 key tiles of 128 per CTA
-constexpr int kTcChunkTiles = 16;
+// tensor-core passes: 32 key tiles of 128 per CTA (measured at 16K: 16 tiles
+// repeat the query-row set-up too often, 64 leave a long last wave)
+constexpr int kTcChunkTiles = 32;
 int tc_chunks(const kvc_params* p) { return (p->n_max + kTcChunkTiles * 128 - 1) / (kTcChunkTiles * 128); }
 
 // Shapes the tensor-core passes handle (workspace sizing); at run time the TMA
