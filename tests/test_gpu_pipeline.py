@@ -203,3 +203,31 @@ def test_window_only_budget(built):
     torch.cuda.synchronize()
     assert not bool(comp.taken.bool().any())
     assert (comp.len_lh.cpu().numpy() == cfg.W).all()
+
+
+def test_phase_timing_reports_the_tensor_core_phases(built):
+    """kvc_set_phase_timing / kvc_score_phase_ms: a timed tensor-core kvc_score
+    call reports five positive phase durations whose sum stays within the
+    call's own event-timed duration; results are the same as untimed."""
+    from kv_cache_compression_probe_gb300 import kvc
+    cfg = W.small_config()
+    wl = W.make_workload(cfg)
+    p, comp, d, S_max = upload_workload(wl, tensor_cores=True)
+    comp.score(d["K"], d["V"], d["Qp"], d["bounds"], d["n_slots"], d["sens"])
+    torch.cuda.synchronize()
+    ref = comp.op_util.clone()
+    kvc.kvc_set_phase_timing(True)
+    try:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        comp.score(d["K"], d["V"], d["Qp"], d["bounds"], d["n_slots"], d["sens"])
+        e1.record()
+        ms = kvc.kvc_score_phase_ms(5)
+    finally:
+        kvc.kvc_set_phase_timing(False)
+    torch.cuda.synchronize()
+    assert kvc.kvc_device_error() == 0
+    assert len(ms) == 5 and all(x > 0.0 for x in ms)
+    assert sum(ms) <= e0.elapsed_time(e1) * 1.01 + 1e-3
+    assert torch.equal(comp.op_util, ref)
+    assert kvc.kvc_score_phase_ms(2) == ms[:2]     # the last timed call, re-read
