@@ -67,7 +67,7 @@ struct ScoreArgs {
   int32_t* ok;         // [BLH] 1 if the (l,h) passed its checks
   unsigned char* proto;  // [BLH * S_max] prototype records (tensor-core path)
   float* npart;        // [BLH * S_max, 2, 15, 4] node statistics (tensor-core path)
-  float* nu_part;      // [BLH, vnorm chunks] block sums of |v| (tensor-core path)
+  float* nu_part;      // [BLH, S_max + 1] sums of |v| per slot, then the window (tensor-core path)
   int32_t* err;
   int chunk;           // keys per rowstats chunk
   int n_chunks;
@@ -332,21 +332,21 @@ __global__ void numean_kernel(kvc_params p, ScoreArgs a) {
   }
 }
 
-// |v_i| and pos_i features (tensor-core path, where the feature epilogue does
-// not touch the values): one thread per token row; per-block sums of |v| go to
-// nu_part[blh][chunk] (summed in a fixed order by the utility kernel).
-constexpr int kVnormRows = 256;
+// Tensor-core path: the slots' |v| and position features come from the
+// prototype kernel (one sum of |v| per slot); this kernel covers the W window
+// tokens (one thread per token) and nu_finish_slots forms the mean |v| of each
+// (b,l,h) from the slot sums and the window sum in a fixed order.
 template <typename T, int D>
-__global__ void __launch_bounds__(kVnormRows) vnorm_kernel(kvc_params p, ScoreArgs a) {
-  const long long blh = blockIdx.y;
+__global__ void __launch_bounds__(128) vnorm_window_kernel(kvc_params p, ScoreArgs a) {
+  const long long blh = blockIdx.x;
   if (!a.ok[blh]) return;
   const int b = seq_of(p, blh);
   const int lh = (int)(blh % ((long long)p.L * p.H));
   const int n = a.ctx_len[b];
-  const int i = blockIdx.x * kVnormRows + threadIdx.x;
   const int64_t row0 = kvcd::seq_token_base(a.ctx_len, b, p.L * p.H) + (int64_t)lh * n;
-  float nv = 0.f;
-  if (i < n) {
+  __shared__ float red[4];
+  float acc = 0.f;
+  for (int i = n - p.W + (int)threadIdx.x; i < n; i += 128) {
     const T* vr = static_cast<const T*>(a.V) + (row0 + i) * D;
     float s2 = 0.f;
 #pragma unroll 8
@@ -356,30 +356,29 @@ __global__ void __launch_bounds__(kVnormRows) vnorm_kernel(kvc_params p, ScoreAr
 #pragma unroll
       for (int t = 0; t < 4; ++t) s2 = fmaf(v[t], v[t], s2);
     }
-    nv = sqrtf(s2);
+    const float nv = sqrtf(s2);
     float* f = a.feats + (row0 + i) * 5;
     f[1] = nv;
     f[4] = (float)i / (float)max(n - 1, 1);
+    acc += nv;
   }
-  __shared__ float red[kVnormRows / 32];
-  const float ws = kvcd::warp_sum(nv);
+  const float ws = kvcd::warp_sum(acc);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ws;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float t = 0.f;
-    for (int w = 0; w < kVnormRows / 32; ++w) t += red[w];
-    a.nu_part[blh * gridDim.x + blockIdx.x] = t;
-  }
+  if (threadIdx.x == 0)
+    a.nu_part[blh * (p.S_max + 1) + p.S_max] = (red[0] + red[1]) + (red[2] + red[3]);
 }
 
-// mean |v| of each (b,l,h) from the vnorm block sums (fixed order)
-__global__ void nu_finish_kernel(kvc_params p, ScoreArgs a, int chunks) {
+__global__ void nu_finish_slots_kernel(kvc_params p, ScoreArgs a) {
   const long long blh = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (blh >= (long long)p.B * p.L * p.H || !a.ok[blh]) return;
-  const int n = a.ctx_len[seq_of(p, blh)];
+  const int b = seq_of(p, blh);
+  const int S = a.n_slots[b];
+  const float* ps = a.nu_part + blh * (p.S_max + 1);
   float t = 0.f;
-  for (int c = 0; c < chunks; ++c) t += a.nu_part[blh * chunks + c];
-  a.nu[blh] = t / (float)n;
+  for (int s = 0; s < S; ++s) t += ps[s];
+  t += ps[p.S_max];
+  a.nu[blh] = t / (float)a.ctx_len[b];
 }
 
 // ---------------------------------------------------------------- hops (a2)
@@ -929,6 +928,8 @@ __global__ void __launch_bounds__(128) proto_kernel(kvc_params p, ScoreArgs a, u
   const uint32_t* Vw = reinterpret_cast<const uint32_t*>(static_cast<const T*>(a.V) + row0 * D);
   const float* rel = a.rel + row0;
   unsigned char* out = proto + tree * kvc::kProtoBytes;
+  const float inv_pos = 1.f / (float)max(n - 1, 1);
+  float nv_sum = 0.f;                                    // sum of |v| over the slot's tokens
   for (int L = 0; L < 8; ++L) {
     int x, y;
     node_range(7 + L, x0, y0, x, y);
@@ -952,7 +953,7 @@ __global__ void __launch_bounds__(128) proto_kernel(kvc_params p, ScoreArgs a, u
         sn[g] = __ldg(reinterpret_cast<const float2*>(a.sin_tab + (int64_t)(2 * i) * 64) + lane);
         ri[g] = __ldg(rel + i);
       }
-      float u[4][4], nk2[4];
+      float u[4][4], nk2[4], nv2[4];
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         const float k0 = __uint_as_float(kl[g] << 16), k1 = __uint_as_float(kl[g] & 0xFFFF0000u);
@@ -962,8 +963,25 @@ __global__ void __launch_bounds__(128) proto_kernel(kvc_params p, ScoreArgs a, u
         u[g][1] = k1 * cs[g].y + k3 * sn[g].y;
         u[g][3] = k3 * cs[g].y - k1 * sn[g].y;
         nk2[g] = u[g][0] * u[g][0] + u[g][1] * u[g][1] + u[g][2] * u[g][2] + u[g][3] * u[g][3];
+        const float v0 = __uint_as_float(vl[g] << 16), v1 = __uint_as_float(vl[g] & 0xFFFF0000u);
+        const float v2 = __uint_as_float(vh[g] << 16), v3 = __uint_as_float(vh[g] & 0xFFFF0000u);
+        nv2[g] = v0 * v0 + v1 * v1 + v2 * v2 + v3 * v3;
       }
       kvcd::warp_sum4(nk2, lane);
+      kvcd::warp_sum4(nv2, lane);
+      // the value-norm and position features of these tokens (lane g writes token g)
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        if (g < ng) {
+          const float nv = sqrtf(nv2[g]);
+          nv_sum += nv;
+          if (lane == g) {
+            float* f = a.feats + (row0 + i0 + g) * 5;
+            f[1] = nv;
+            f[4] = (float)(i0 + g) * inv_pos;
+          }
+        }
+      }
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         if (g < ng) {
@@ -1000,6 +1018,7 @@ __global__ void __launch_bounds__(128) proto_kernel(kvc_params p, ScoreArgs a, u
   }
   const ProtoAcc root = acc_from_smem(lv, 2, lane);
   proto_finish(a, p.value_floor, 0, x0, y0, root, out, lane);
+  if (lane == 0) a.nu_part[blh * (p.S_max + 1) + s] = nv_sum;
   // row 15 of every part is padding: zero key, ln m = 0, no relevance
 #pragma unroll
   for (int part = 0; part < 3; ++part) {
@@ -1128,7 +1147,8 @@ Layout layout(const kvc_params* p) {
   const size_t trees = tc_shape(p) ? blh * (size_t)p->S_max : 0;
   l.proto = o; o += kvc::align256(trees * kvc::kProtoBytes);
   l.npart = o; o += kvc::align256(trees * 2 * 15 * 4 * sizeof(float));
-  l.nu_part = o; o += kvc::align256(blh * (size_t)((p->n_max + 255) / 256) * sizeof(float));
+  l.nu_part = o;
+  o += kvc::align256(blh * (size_t)std::max((p->n_max + 255) / 256, p->S_max + 1) * sizeof(float));
   l.total = o;
   return l;
 }
@@ -1201,10 +1221,8 @@ int launch_all(const kvc_params* p, ScoreArgs& a, cudaStream_t s) {
     if (timed) phase_mark(2, s);
     if ((st = kvc::probe_tc_pass(kvc::kTcFeats, t, rows_total, s)) != KVC_OK) return st;
     if (timed) phase_mark(3, s);
-    const int vchunks = (p->n_max + kVnormRows - 1) / kVnormRows;
-    vnorm_kernel<T, D><<<dim3(vchunks, (unsigned)blh), kVnormRows, 0, s>>>(*p, a);
-    nu_finish_kernel<<<(unsigned)((blh + 127) / 128), 128, 0, s>>>(*p, a, vchunks);
-    launches += 3;
+    vnorm_window_kernel<T, D><<<(unsigned)blh, 128, 0, s>>>(*p, a);
+    launches += 2;
     for (int hop = 0; hop < p->n_hops; ++hop) {
       seeds_kernel<<<(unsigned)blh, 1024, 0, s>>>(*p, a);
       if ((st = kvc::probe_tc_pass(kvc::kTcRowstatsSeeds, t, rows_total, s)) != KVC_OK) return st;
@@ -1215,6 +1233,8 @@ int launch_all(const kvc_params* p, ScoreArgs& a, cudaStream_t s) {
     // prototypes, tensor-core node statistics, utilities
     if (timed) phase_mark(4, s);
     proto_kernel<T, D><<<(unsigned)((blh * p->S_max + 3) / 4), 128, 0, s>>>(*p, a, a.proto);
+    nu_finish_slots_kernel<<<(unsigned)((blh + 127) / 128), 128, 0, s>>>(*p, a);
+    ++launches;
     if (timed) phase_mark(5, s);
     kvc::NodeTcArgs nd;
     nd.ctx_len = a.ctx_len; nd.K = a.K; nd.V = a.V; nd.Qp = a.Qp; nd.lse2 = a.lse2; nd.ok = a.ok;
