@@ -314,13 +314,22 @@ __global__ void radix_hist_kernel(kvc_params p, Items it, SelWs ws, int sel, int
     count = (long long)p.L * p.H * n;
     row0 = kvcd::seq_token_base(it.ctx_len, b, p.L * p.H);
   }
-  for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < count;
-       k += (long long)gridDim.x * blockDim.x) {
-    unsigned long long key;
-    long long w;
-    if (!item_at(p, it, ws, b, k, row0, n, key, w)) continue;
-    if ((key & hi_mask) != (st.prefix & hi_mask) || w <= 0) continue;
-    atomicAdd(&sh[(key >> shift) & 255u], (unsigned long long)w);
+  // warp-uniform trip count; the lanes of a warp that fall in the same bin add
+  // their weights first (keys of one sequence share long prefixes, so most
+  // items of a pass land in a few bins)
+  const int lane = threadIdx.x & 31;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long base = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < count;
+       base += stride) {
+    const long long k = base + lane;
+    unsigned long long key = 0ull;
+    long long w = 0;
+    bool ok = k < count && item_at(p, it, ws, b, k, row0, n, key, w);
+    ok = ok && (key & hi_mask) == (st.prefix & hi_mask) && w > 0;
+    const unsigned dig = ok ? (unsigned)((key >> shift) & 255u) : 256u;
+    const unsigned peers = __match_any_sync(KVC_FULL_MASK, dig);
+    const unsigned sum = __reduce_add_sync(peers, ok ? (unsigned)w : 0u);   // <= 32 x a cost
+    if (ok && lane == __ffs(peers) - 1) atomicAdd(&sh[dig], (unsigned long long)sum);
   }
   __syncthreads();
   unsigned long long* gh = ws.hist + (((long long)sel * kPasses + pass) * p.B + b) * 256;
@@ -523,17 +532,37 @@ __global__ void tail_find_kernel(kvc_params p, SelWs ws, const int32_t* op_cost,
                                  const uint8_t* taken) {
   const long long total = (long long)p.B * p.L * p.H * p.S_max * kOps;
   const long long per_seq = (long long)p.L * p.H * p.S_max * kOps;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const unsigned long long k = ws.keys[i];
-    const int b = (int)(i / per_seq);
-    if (k == 0ull || taken[i]) continue;
-    const SeqBudget& sb = ws.seq[b];
-    if (sb.tail_done || k > sb.tail_last || op_cost[i] > sb.tail_rem) continue;
-    const int o = (int)(i & (kOps - 1));
-    const int par = op_parent(o);
-    if (par >= 0 && !taken[i - o + par]) continue;
-    atomicMax(&ws.seq[b].tail_best, k);
+  // warp-uniform trip count; a warp's candidates of one sequence are reduced
+  // to their maximum with shuffles before the one atomic.  A sequence owns a
+  // multiple of 16 ops and warps start at multiples of 32, so a warp holds at
+  // most two sequences split at lane 16: the xor-16 step is the only one that
+  // crosses them (skipped then) and lanes 0 and 16 end with their half's max.
+  const int lane = threadIdx.x & 31;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long base = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < total;
+       base += stride) {
+    const long long i = base + lane;
+    unsigned long long cand = 0ull;
+    int b = -1;
+    if (i < total) {
+      const unsigned long long k = ws.keys[i];
+      b = (int)(i / per_seq);
+      const SeqBudget& sb = ws.seq[b];
+      bool ok = k != 0ull && !taken[i] && !sb.tail_done && k <= sb.tail_last &&
+                op_cost[i] <= sb.tail_rem;
+      const int o = (int)(i & (kOps - 1));
+      const int par = op_parent(o);
+      if (ok && par >= 0 && !taken[i - o + par]) ok = false;
+      cand = ok ? k : 0ull;
+    }
+    const unsigned same = __match_any_sync(KVC_FULL_MASK, b);   // lanes of one sequence
+    unsigned long long m = cand;
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long v = __shfl_xor_sync(KVC_FULL_MASK, m, o);
+      const int bv = __shfl_xor_sync(KVC_FULL_MASK, b, o);
+      if (bv == b && v > m) m = v;
+    }
+    if (b >= 0 && m != 0ull && lane == __ffs(same) - 1) atomicMax(&ws.seq[b].tail_best, m);
   }
 }
 
