@@ -406,14 +406,20 @@ def run_gpu(args, cfg, rank, world):
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     rec = {"score": [], "select": [], "pack": [], "decode": []}
 
+    cg = not args.eager_compress                     # compression calls as graph replays
+
     def step(timed: bool, Kx=K, Vx=V, Qx=Qp):
         marks = [ev() for _ in range(4)] if timed else None
         if timed: marks[0].record(stream)
-        comp.score(Kx, Vx, Qx, bounds, n_slots)
+        comp.score(Kx, Vx, Qx, bounds, n_slots, graph=cg)
+        nl = comp.graph_launches if cg else 0
         if timed: marks[1].record(stream)
-        comp.select(bounds, n_slots)
+        comp.select(bounds, n_slots, graph=cg)
+        nl += comp.graph_launches if cg else 0
         if timed: marks[2].record(stream)
-        comp.merge_pack(Kx, Vx, bounds, n_slots)
+        comp.merge_pack(Kx, Vx, bounds, n_slots, graph=cg)
+        nl += comp.graph_launches if cg else 0
+        rec["graph_launches"] = rec.get("graph_launches", 0) + nl
         if timed: marks[3].record(stream)
         # D decode steps: one CUDA graph replay (captured on first use) or D calls
         d0, d1 = ev(), ev()
@@ -606,7 +612,9 @@ def run_gpu(args, cfg, rank, world):
         "evict_per_step_next_f2": evict,
         "gpu_launches": launches,
         "gpu_launches_detail": {"issued_by_host": host_launches,
-                                "in_decode_graph_replays": graph_launches},
+                                "in_graph_replays": graph_launches,
+                                "compression_as_graphs": cg,
+                                "decode_as_graph": not args.eager_decode},
         "clocks": clk,
     }
     return line
@@ -782,6 +790,8 @@ def main():
                     help="head-level hybrid: fraction of heads that keep the full cache")
     ap.add_argument("--evict", action="store_true",
                     help="also time per-step top-B eviction (DistillCache) on the workload")
+    ap.add_argument("--eager-compress", action="store_true",
+                    help="issue the compression calls directly instead of as CUDA graph replays")
     ap.add_argument("--eager-decode", action="store_true",
                     help="issue the decode steps one call at a time instead of one CUDA graph")
     ap.add_argument("--profile", action="store_true",

@@ -72,28 +72,71 @@ class Compressor:
         self._graphs = {}
 
     # ---------------------------------------------------------------- calls
-    def score(self, K, V, Qp, slot_bounds, n_slots, head_sens=None, stream=None):
-        kvc.kvc_score(self.p, self.ctx_len, K, V, Qp, self.rope_cos, self.rope_sin, slot_bounds,
-                      n_slots, head_sens, self.lse, self.feats, self.relevance, self.op_util,
-                      self.op_cost, self.ws_score, stream)
+    # With graph=True a call is captured into a CUDA graph once per set of
+    # buffers and replayed on the current stream (the library launches many
+    # small kernels per call); the last replay's kernel count is kept in
+    # `graph_launches`.
+    def _graphed(self, key, fn):
+        g = self._graphs.get(key)
+        if g is None:
+            dev = self.Kp.device
+            kvc.kvc_device_error()                   # error-word lookup outside capture
+            side = torch.cuda.Stream(device=dev)
+            side.wait_stream(torch.cuda.current_stream(dev))
+            graph = torch.cuda.CUDAGraph()
+            n0 = kvc.kvc_launch_count()
+            with torch.cuda.graph(graph, stream=side):
+                fn(side)
+            torch.cuda.current_stream(dev).wait_stream(side)
+            g = (graph, kvc.kvc_launch_count() - n0)
+            self._graphs[key] = g
+        g[0].replay()
+        self.graph_launches = g[1]
+
+    @staticmethod
+    def _key(name, *tensors):
+        return (name,) + tuple(t.data_ptr() if t is not None else 0 for t in tensors)
+
+    def score(self, K, V, Qp, slot_bounds, n_slots, head_sens=None, stream=None, graph=False):
+        def run(st):
+            kvc.kvc_score(self.p, self.ctx_len, K, V, Qp, self.rope_cos, self.rope_sin,
+                          slot_bounds, n_slots, head_sens, self.lse, self.feats, self.relevance,
+                          self.op_util, self.op_cost, self.ws_score, st)
+        if graph:
+            self._graphed(self._key("score", K, V, Qp, slot_bounds, n_slots, head_sens), run)
+        else:
+            run(stream)
 
     def select(self, slot_bounds, n_slots, head_sens=None, op_util=None, relevance=None,
-               stream=None):
-        kvc.kvc_select(self.p, self.ctx_len, slot_bounds, n_slots,
-                       self.relevance if relevance is None else relevance, head_sens,
-                       self.op_util if op_util is None else op_util, self.op_cost, self.taken,
-                       self.len_lh, self.cap_lh, self.off_lh, self.total, self.ws_select, stream)
+               stream=None, graph=False):
+        rel = self.relevance if relevance is None else relevance
+        util = self.op_util if op_util is None else op_util
 
-    def merge_pack(self, K, V, slot_bounds, n_slots, taken=None, stream=None):
-        kvc.kvc_merge_pack(self.p, self.ctx_len, K, V, self.relevance, self.rope_cos,
-                           self.rope_sin, slot_bounds, n_slots,
-                           self.taken if taken is None else taken, self.len_lh, self.off_lh,
-                           self.Kp, self.Vp, self.logm, self.pos, self.ws_pack, stream)
+        def run(st):
+            kvc.kvc_select(self.p, self.ctx_len, slot_bounds, n_slots, rel, head_sens, util,
+                           self.op_cost, self.taken, self.len_lh, self.cap_lh, self.off_lh,
+                           self.total, self.ws_select, st)
+        if graph:
+            self._graphed(self._key("select", slot_bounds, n_slots, head_sens, rel, util), run)
+        else:
+            run(stream)
 
-    def compress(self, K, V, Qp, slot_bounds, n_slots, head_sens=None, stream=None):
-        self.score(K, V, Qp, slot_bounds, n_slots, head_sens, stream)
-        self.select(slot_bounds, n_slots, head_sens, stream=stream)
-        self.merge_pack(K, V, slot_bounds, n_slots, stream=stream)
+    def merge_pack(self, K, V, slot_bounds, n_slots, taken=None, stream=None, graph=False):
+        tk = self.taken if taken is None else taken
+
+        def run(st):
+            kvc.kvc_merge_pack(self.p, self.ctx_len, K, V, self.relevance, self.rope_cos,
+                               self.rope_sin, slot_bounds, n_slots, tk, self.len_lh, self.off_lh,
+                               self.Kp, self.Vp, self.logm, self.pos, self.ws_pack, st)
+        if graph:
+            self._graphed(self._key("pack", K, V, slot_bounds, n_slots, tk), run)
+        else:
+            run(stream)
+
+    def compress(self, K, V, Qp, slot_bounds, n_slots, head_sens=None, stream=None, graph=False):
+        self.score(K, V, Qp, slot_bounds, n_slots, head_sens, stream, graph)
+        self.select(slot_bounds, n_slots, head_sens, stream=stream, graph=graph)
+        self.merge_pack(K, V, slot_bounds, n_slots, stream=stream, graph=graph)
 
     def decode(self, q, k_new, v_new, out, pos_new=None, stream=None):
         kvc.kvc_decode_attn(self.p, q, k_new, v_new, pos_new, self.Kp, self.Vp, self.logm,
