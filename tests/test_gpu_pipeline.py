@@ -231,3 +231,24 @@ def test_phase_timing_reports_the_tensor_core_phases(built):
     assert sum(ms) <= e0.elapsed_time(e1) * 1.01 + 1e-3
     assert torch.equal(comp.op_util, ref)
     assert kvc.kvc_score_phase_ms(2) == ms[:2]     # the last timed call, re-read
+
+
+def test_compression_graph_replay_equals_eager(built):
+    """Compressor.compress(graph=True): the captured score, select and pack
+    calls replayed (twice) give the eager calls' results bit for bit."""
+    from kv_cache_compression_probe_gb300 import kvc
+    cfg = W.small_config()
+    wl = W.make_workload(cfg)
+    p, comp, d, S_max = upload_workload(wl, tensor_cores=True)
+    args = (d["K"], d["V"], d["Qp"], d["bounds"], d["n_slots"], d["sens"])
+    comp.compress(*args)
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in (comp.op_util, comp.taken, comp.len_lh, comp.Kp, comp.Vp, comp.logm)]
+    for _ in range(2):
+        comp.compress(*args, graph=True)
+        torch.cuda.synchronize()
+        assert kvc.kvc_device_error() == 0
+        got = (comp.op_util, comp.taken, comp.len_lh, comp.Kp, comp.Vp, comp.logm)
+        for a, b in zip(ref, got):
+            assert torch.equal(a, b)
+    assert comp.graph_launches > 0
