@@ -1105,10 +1105,10 @@ __global__ void __maxnreg__(kNodeMaxRegs)
               st[1] = rv ? an_fin[jj >> 2] : 0.f;
               st[2] = rv ? sqrtf(ddt) : 0.f;
               st[3] = rv ? sqrtf(uut) : 0.f;
+              kvcd::warp_sum4(st, lane);               // totals on every lane
+              if (lane == 0) {
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float t = kvcd::warp_sum(st[e]);
-                if (lane == 0) sm.red[k & 1][q][jj][e] = t;
+                for (int e = 0; e < 4; ++e) sm.red[k & 1][q][jj][e] = st[e];
               }
             }
           }
