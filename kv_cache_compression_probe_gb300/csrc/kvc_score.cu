@@ -908,7 +908,7 @@ __device__ __forceinline__ ProtoAcc acc_from_smem(const ProtoLevels& sm, int lvl
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(128) proto_kernel(kvc_params p, ScoreArgs a, unsigned char* proto) {
+__global__ void __launch_bounds__(128, 5) proto_kernel(kvc_params p, ScoreArgs a, unsigned char* proto) {
   static_assert(D == 128 && sizeof(T) == 2, "tensor-core node path is bf16, d = 128");
   __shared__ ProtoLevels levels[4];
   const int lane = threadIdx.x & 31;
