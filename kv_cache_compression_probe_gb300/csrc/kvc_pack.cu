@@ -270,7 +270,7 @@ __device__ __forceinline__ void copy_exact(const PackArgs& a, const T* Kh, const
 // One warp per slot tree (plus one extra "slot" index S per (b,l,h) for the
 // window tokens).
 template <typename T, int D>
-__global__ void pack_tree_kernel(kvc_params p, PackArgs a) {
+__global__ void __launch_bounds__(128, 8) pack_tree_kernel(kvc_params p, PackArgs a) {
   const int warps = blockDim.x >> 5;
   const long long item = (long long)blockIdx.x * warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
