@@ -712,10 +712,10 @@ __global__ void __maxnreg__(kRsMaxRegs)
 //            TMA) into one of two TMEM buffers;
 //   epi B    every group reads 32 of the 128 features of each node buffer and
 //            forms per-row partial sums of |U - A^ v^|^2 and |U|^2 (packed
-//            f32x2 FMAs) into spare TMEM columns; after each pair of nodes the
-//            four warps sharing a row quarter meet, and one of them (rotating
-//            with the node) adds the partials in a fixed order and finishes the
-//            row's |U - A^ v^|, |U|, |A - A^| and A, summed over its 32 rows.
+//            f32x2 FMAs) into spare TMEM columns; after every four nodes the
+//            four warps sharing a row quarter meet, and warp g finishes node
+//            4t + g: it adds the partials in a fixed order and forms the row's
+//            |U - A^ v^|, |U|, |A - A^| and A, summed over its 32 rows.
 // Per-(slot, tile) sums go to `npart`; a small kernel forms D and utilities.
 constexpr int kNodeSlots = 8;
 constexpr int kEpiWarps = 16;                      // 4 groups x 4 row quarters
@@ -759,10 +759,11 @@ __device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr, uint32_t lbo_b
 
 
 
-// Spare TMEM columns 176..207 (no MMA writes there) hold the per-row partial
-// sums of node j from group g: pair parity, node parity, group, (dd, uu).
+// Spare TMEM columns 176..239 (no MMA writes there) hold the per-row partial
+// sums of node j from group g: parity of j's group of four nodes, j mod 4,
+// group, (dd, uu).
 __device__ __forceinline__ uint32_t part_col(int j, int g) {
-  return 176u + (uint32_t)(((j >> 1) & 1) * 16 + (j & 1) * 8 + 2 * g);
+  return 176u + (uint32_t)(((j >> 2) & 1) * 32 + (j & 3) * 8 + 2 * g);
 }
 __device__ __forceinline__ void tmem_st2(uint32_t taddr, float a, float b) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr),
@@ -1085,16 +1086,17 @@ __global__ void __maxnreg__(kNodeMaxRegs)
           uu0 = fma2(ua, ua, uu0);
           uu1 = fma2(ub, ub, uu1);
         }
-        // partials of nodes 2t, 2t+1 go to the spare TMEM columns of pair parity
-        // t & 1 (one barrier per pair; the finisher adds them in group order)
+        // partials of nodes 4t .. 4t+3 go to the spare TMEM columns of parity
+        // t & 1 (one barrier per four nodes; group jj & 3 finishes node jj,
+        // adding the groups' partials in group order)
         tmem_st2(tmem + lane_off + part_col(j, g), hsum2(dd0) + hsum2(dd1), hsum2(uu0) + hsum2(uu1));
-        if ((j & 1) == 1 || j == 14) {
+        if ((j & 3) == 3 || j == 14) {
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
           tc_fence_before();
           named_bar(qbar, 128);
           tc_fence_after();
 #pragma unroll
-          for (int jj = (j == 14 ? 14 : j - 1); jj <= j; ++jj) {
+          for (int jj = j & ~3; jj <= j; ++jj) {
             if (g == (jj & 3)) {                         // finisher of node jj for these rows
               float pp[8];
               tld8(tmem + lane_off + part_col(jj, 0), pp);
