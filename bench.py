@@ -788,8 +788,8 @@ def main():
                     help="override the layer count (small profiling cases)")
     ap.add_argument("--head-full-frac", type=float, default=0.0,
                     help="head-level hybrid: fraction of heads that keep the full cache")
-    ap.add_argument("--evict", action="store_true",
-                    help="also time per-step top-B eviction (DistillCache) on the workload")
+    ap.add_argument("--no-evict", dest="evict", action="store_false",
+                    help="skip the per-step top-B eviction (DistillCache) leg")
     ap.add_argument("--eager-compress", action="store_true",
                     help="issue the compression calls directly instead of as CUDA graph replays")
     ap.add_argument("--eager-decode", action="store_true",
