@@ -513,7 +513,7 @@ def run_gpu(args, cfg, rank, world):
                                                   sum(s[0] for s in seqs), measured_peaks()[1],
                                                   dev)
     evict = None
-    if args.evict:
+    if (args.evict or not args.profile) and not args.no_evict:
         evict = evict_leg(p, cfg, seqs, K, V, q_all, kn_all, vn_all, D, dev, stream)
         evict["hbm_frac"] = evict["hbm_gbs"] / measured_peaks()[0]
         evict["step_over_compressed_decode"] = evict["ms_per_step"] / statistics.mean(rec["decode"])
@@ -788,8 +788,10 @@ def main():
                     help="override the layer count (small profiling cases)")
     ap.add_argument("--head-full-frac", type=float, default=0.0,
                     help="head-level hybrid: fraction of heads that keep the full cache")
-    ap.add_argument("--no-evict", dest="evict", action="store_false",
-                    help="skip the per-step top-B eviction (DistillCache) leg")
+    ap.add_argument("--evict", action="store_true",
+                    help="time the per-step top-B eviction (DistillCache) leg also under --profile")
+    ap.add_argument("--no-evict", action="store_true",
+                    help="skip the per-step top-B eviction leg (on by default)")
     ap.add_argument("--eager-compress", action="store_true",
                     help="issue the compression calls directly instead of as CUDA graph replays")
     ap.add_argument("--eager-decode", action="store_true",
