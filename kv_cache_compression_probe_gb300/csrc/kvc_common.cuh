@@ -153,6 +153,13 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// max of three floats in one instruction (PTX three-input max).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // 2^x with the PTX approximate base-2 exponential instruction; results below
 // 2^-126 flush to zero (the callers sum probabilities relative to a maximum).
 __device__ __forceinline__ float ex2(float x) {

@@ -309,15 +309,15 @@ __global__ void __maxnreg__(kRsMaxRegs)
 #pragma unroll
           for (int j = 0; j < kCh; ++j)
             raw[j] = (!kMasked || (rv && i0 + j < k1 && i0 + j <= limit)) ? v[j] : -INFINITY;
-          float mt4[kCh / 2];
-#pragma unroll
-          for (int j = 0; j < kCh / 2; ++j) mt4[j] = fmaxf(raw[j], raw[j + kCh / 2]);
-#pragma unroll
-          for (int w = kCh / 4; w >= 1; w >>= 1)
-#pragma unroll
-            for (int j = 0; j < w; ++j) mt4[j] = fmaxf(mt4[j], mt4[j + w]);
-          if (kMasked && mt4[0] == -INFINITY) return;        // nothing valid in the batch
-          const float mx = fmaxf(m, mt4[0] * a.q_scale2);
+          static_assert(kCh == 16, "three-input max tree over 16 values");
+          const float r0 = kvcd::fmax3(raw[0], raw[1], raw[2]);
+          const float r1 = kvcd::fmax3(raw[3], raw[4], raw[5]);
+          const float r2 = kvcd::fmax3(raw[6], raw[7], raw[8]);
+          const float r3 = kvcd::fmax3(raw[9], raw[10], raw[11]);
+          const float r4 = kvcd::fmax3(raw[12], raw[13], raw[14]);
+          const float rmax = kvcd::fmax3(kvcd::fmax3(r0, r1, r2), fmaxf(r3, r4), raw[15]);
+          if (kMasked && rmax == -INFINITY) return;          // nothing valid in the batch
+          const float mx = fmaxf(m, rmax * a.q_scale2);
           if (mx > m && m != -INFINITY) {
             const float sc = kvcd::ex2(m - mx);
             if (kU) { u = sc * (u + (m - mx) * l); cu *= sc; }
