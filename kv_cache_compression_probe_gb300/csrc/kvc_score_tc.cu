@@ -439,7 +439,7 @@ template <int NT>
 struct TcTSmem {
   alignas(1024) unsigned char A[NT][2][kBlockBytes];       // query rows (B operand), swizzled
   alignas(1024) unsigned char Bt[kStages][2][kBlockBytes]; // key tiles (A operand), swizzled
-  alignas(16) float col_a[NT * kBM];                        // per row: base-2 LSE (+inf: no row)
+  alignas(16) float col_a[NT * kBM];                        // per row: minus its base-2 LSE (-inf: no row)
   alignas(16) float col_b[NT * kBM];                        // per row: H (FEATS) or seed weight (PROP)
   float xch[2][3][kBN][9];                                  // shares 1..3: per-key sums, by tile parity
   uint64_t full[kStages], empty[kStages], tfull[2], tempty[2];
@@ -486,10 +486,10 @@ __global__ void __maxnreg__(kRsMaxRegs)
   for (int c = tid; c < NT * kBM; c += kThreads) {
     const bool in = c < rows;
     if (MODE == kvc::kTcProp) {
-      sm.col_a[c] = in ? a.lse2_h[blh * a.P + c] : INFINITY;
+      sm.col_a[c] = in ? -a.lse2_h[blh * a.P + c] : -INFINITY;
       sm.col_b[c] = in ? a.seed_w[blh * a.P + c] : 0.f;
     } else {
-      sm.col_a[c] = in ? a.lse2[blh * rows + c] : INFINITY;
+      sm.col_a[c] = in ? -a.lse2[blh * rows + c] : -INFINITY;
       sm.col_b[c] = in ? a.hrow[blh * rows + c] : 0.f;
     }
   }
@@ -591,10 +591,34 @@ __global__ void __maxnreg__(kRsMaxRegs)
         const float4* ca = reinterpret_cast<const float4*>(&sm.col_a[cb]);
         const float4* cbv = reinterpret_cast<const float4*>(&sm.col_b[cb]);
         float cs = 0.f, chs = 0.f;
-        // the masked form (keys past the chunk, causal probe limits) is
-        // separate code that only boundary keys run
-        auto batch = [&](auto masked_tag) {
-          constexpr bool kMasked = decltype(masked_tag)::value;
+        if (full_cols) {
+          // unmasked batch on packed pairs: t = S c - LSE, e = 2^t,
+          // FEATS: sum e and sum e H; PROP: sum w e
+          const uint64_t c2 = f2(a.q_scale2, a.q_scale2);
+          uint64_t s1 = f2(0.f, 0.f), s2 = f2(0.f, 0.f);
+#pragma unroll
+          for (int j4 = 0; j4 < kCh / 4; ++j4) {
+            const float4 la = ca[j4], lb = cbv[j4];
+            const uint64_t t0 = fma2(f2(v[4 * j4], v[4 * j4 + 1]), c2, f2(la.x, la.y));
+            const uint64_t t1 = fma2(f2(v[4 * j4 + 2], v[4 * j4 + 3]), c2, f2(la.z, la.w));
+            const float2 u0 = uf2(t0), u1 = uf2(t1);
+            const uint64_t e0 = f2(kvcd::ex2(u0.x), kvcd::ex2(u0.y));
+            const uint64_t e1 = f2(kvcd::ex2(u1.x), kvcd::ex2(u1.y));
+            if (MODE == kvc::kTcFeats) {
+              s1 = add2(s1, add2(e0, e1));
+              s2 = fma2(e0, f2(lb.x, lb.y), fma2(e1, f2(lb.z, lb.w), s2));
+            } else {
+              s1 = fma2(e0, f2(lb.x, lb.y), fma2(e1, f2(lb.z, lb.w), s1));
+            }
+          }
+          if (MODE == kvc::kTcFeats) {
+            cs = hsum2(s1);
+            chs = hsum2(s2);
+          } else {
+            acc += hsum2(s1);
+          }
+        } else {
+          // masked form (keys past the chunk, causal probe limits): boundary keys only
 #pragma unroll
           for (int j4 = 0; j4 < kCh / 4; ++j4) {
             const float4 la = ca[j4], lb = cbv[j4];
@@ -602,11 +626,9 @@ __global__ void __maxnreg__(kRsMaxRegs)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const int j = j4 * 4 + u;
-              float e = kvcd::ex2(fmaf(v[j], a.q_scale2, -las[u]));
-              if (kMasked) {
-                const bool ok = kvalid && (MODE == kvc::kTcProp || ((cb + j) % a.P) >= thr);
-                e = ok ? e : 0.f;
-              }
+              float e = kvcd::ex2(fmaf(v[j], a.q_scale2, las[u]));
+              const bool ok = kvalid && (MODE == kvc::kTcProp || ((cb + j) % a.P) >= thr);
+              e = ok ? e : 0.f;
               if (MODE == kvc::kTcFeats) {
                 cs += e;
                 chs = fmaf(e, lbs[u], chs);
@@ -615,9 +637,7 @@ __global__ void __maxnreg__(kRsMaxRegs)
               }
             }
           }
-        };
-        if (full_cols) batch(std::false_type{});
-        else batch(std::true_type{});
+        }
         if (MODE == kvc::kTcFeats) {
           const int head = cb / a.P;                 // P % 32 == 0: one head per batch
 #pragma unroll
