@@ -177,6 +177,11 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(kvc::DecodeTcArgs a, 
   if (tid == 0) *a.n_items = (int32_t)total;
 }
 
+// Up to this many (b,l,h) the attention kernel builds the work list itself
+// (each CTA scans the chunk counts into shared memory); beyond, a plan kernel
+// writes it to the workspace.
+constexpr int kInPlanMax = 1024;
+
 struct DecSmem {
   alignas(1024) unsigned char ring[kSlots][2][kBlock];      // K or V tile per slot
   alignas(1024) unsigned char Pt[kChunkTc / 64][16 * 128];  // P: 16 head rows x 512 keys, K-major
@@ -186,6 +191,8 @@ struct DecSmem {
   uint64_t full[kSlots], empty[kSlots], s_ready, p_ready, o_ready, mma_done;
   uint32_t tmem;
   int abort;
+  int wsum[8];                                             // block scan of the chunk counts
+  int pref[kInPlanMax + 1];                                // work items before (b,l,h) i
 };
 
 // One work-list entry: chunk c of (b,l,h) blh.
@@ -193,11 +200,23 @@ struct Item {
   int blh, c, len, nchunks, nvalid, ntiles;
   int64_t off;
 };
-__device__ __forceinline__ Item item_at(const kvc::DecodeTcArgs& a, int idx) {
+// pref: the in-kernel work list (items before each (b,l,h)), or null to read
+// the plan kernel's list.
+__device__ __forceinline__ Item item_at(const kvc::DecodeTcArgs& a, int idx, const int* pref) {
   Item it;
-  const uint32_t w = a.items[idx];
-  it.blh = (int)(w & 0xFFFFu);
-  it.c = (int)(w >> 16);
+  if (pref) {                                    // pref[lo] <= idx < pref[lo + 1]
+    int lo = 0, hi = (int)a.blh;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (pref[mid] <= idx) lo = mid; else hi = mid;
+    }
+    it.blh = lo;
+    it.c = idx - pref[lo];
+  } else {
+    const uint32_t w = a.items[idx];
+    it.blh = (int)(w & 0xFFFFu);
+    it.c = (int)(w >> 16);
+  }
   it.len = __ldcg(a.len_lh + it.blh);      // read before this (l,h)'s last chunk arrives
   it.off = a.off_lh[it.blh];
   it.nchunks = it.len > 0 ? (it.len + kChunkTc - 1) / kChunkTc : 1;
@@ -249,9 +268,50 @@ __global__ void __launch_bounds__(256, 2)
   fence_before();
   __syncthreads();
   fence_after();
-  // the set-up above overlaps the plan kernel; the work list is read after it
+  // the set-up above overlaps the predecessor (plan kernel or previous step)
   kvcd::pdl_wait();
-  const int n_items = *a.n_items;
+  const int* pref = nullptr;
+  int n_items;
+  if (a.inplan) {
+    // work list in shared memory: chunk counts of every (b,l,h), block scan
+    const int nb = (int)a.blh;
+    const int per = (nb + kThreadsTc - 1) / kThreadsTc;
+    const int b0 = min(nb, tid * per), b1 = min(nb, b0 + per);
+    int cnt = 0;
+    for (int i = b0; i < b1; ++i) {
+      int n = chunks_of(a, i);
+      if (n < 0) {                                   // corrupt (b,l,h): no chunk
+        if (blockIdx.x == 0) kvcd::record_error(a.err, KVC_EDEVICE);
+        n = 0;
+      }
+      sm.pref[i + 1] = n;
+      cnt += n;
+    }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(KVC_FULL_MASK, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) sm.wsum[warp] = incl;
+    __syncthreads();
+    int run = incl - cnt;
+    for (int w = 0; w < warp; ++w) run += sm.wsum[w];
+    for (int i = b0; i < b1; ++i) {
+      run += sm.pref[i + 1];
+      sm.pref[i + 1] = run;
+    }
+    if (tid == 0) sm.pref[0] = 0;
+    __syncthreads();
+    n_items = sm.pref[nb];
+    if (n_items > a.grid_items) {                    // lengths exceed the packed extent
+      if (blockIdx.x == 0 && tid == 0) kvcd::record_error(a.err, KVC_EDEVICE);
+      n_items = 0;
+    }
+    pref = sm.pref;
+  } else {
+    n_items = *a.n_items;
+  }
   const uint32_t tmem = sm.tmem;
   volatile int* abort_flag = &sm.abort;
   int last_issue[kSlots] = {-1, -1};                 // producer: last load per slot
@@ -263,7 +323,7 @@ __global__ void __launch_bounds__(256, 2)
       bool ok = true;
       int li = 0;
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++li) {
-        const Item it = item_at(a, idx);
+        const Item it = item_at(a, idx, pref);
         const int y_base = (int)(it.off + it.c * kChunkTc);
         for (int i = 0; i < 2 * it.ntiles; ++i, ++t) {
           const int s = t & 1;
@@ -293,7 +353,7 @@ __global__ void __launch_bounds__(256, 2)
     int t = 0, li = 0, ne = 0;
     bool ok = true;
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++li) {
-      const Item it = item_at(a, idx);
+      const Item it = item_at(a, idx, pref);
       if (it.ntiles == 0) continue;
       for (int i = 0; i < it.ntiles; ++i, ++t) {     // S^T blocks
         const int s = t & 1;
@@ -353,7 +413,7 @@ __global__ void __launch_bounds__(256, 2)
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
     int li = 0, ne = 0;                              // items, items with tiles
     for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x, ++li) {
-      const Item it = item_at(a, idx);
+      const Item it = item_at(a, idx, pref);
       const int e0 = it.c * kChunkTc;
       const float* lm = a.logm + it.off + e0;
       float bias[kTiles];
@@ -687,15 +747,21 @@ int decode_tc_launch(const DecodeTcArgs& a, cudaStream_t s) {
   const int sms = sm_count();
   if (sms <= 0) return KVC_ECUDA;
   const unsigned grid = (unsigned)std::min<int64_t>(bound, 2LL * sms);   // persistent, 2 per SM
-  cudaError_t e = launch_pdl(decode_plan_kernel, dim3(1), dim3(1024), 0, s, a, bound);
-  if (e != cudaSuccess) return cuda_status(e);
-  switch (a.G) {
-    case 1: e = launch_attn<1>(km, vm, qm, a, grid, s); break;
-    case 2: e = launch_attn<2>(km, vm, qm, a, grid, s); break;
-    case 4: e = launch_attn<4>(km, vm, qm, a, grid, s); break;
-    default: e = launch_attn<8>(km, vm, qm, a, grid, s); break;
+  DecodeTcArgs t = a;
+  t.inplan = a.blh <= kInPlanMax ? 1 : 0;
+  t.grid_items = bound;
+  cudaError_t e = cudaSuccess;
+  if (!t.inplan) {
+    e = launch_pdl(decode_plan_kernel, dim3(1), dim3(1024), 0, s, t, bound);
+    if (e != cudaSuccess) return cuda_status(e);
   }
-  count_launch(3);
+  switch (t.G) {
+    case 1: e = launch_attn<1>(km, vm, qm, t, grid, s); break;
+    case 2: e = launch_attn<2>(km, vm, qm, t, grid, s); break;
+    case 4: e = launch_attn<4>(km, vm, qm, t, grid, s); break;
+    default: e = launch_attn<8>(km, vm, qm, t, grid, s); break;
+  }
+  count_launch(t.inplan ? 2 : 3);
   return cuda_status(e);
 }
 

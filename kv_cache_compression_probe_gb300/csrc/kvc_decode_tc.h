@@ -31,6 +31,10 @@ struct DecodeTcArgs {
   int32_t* err;
   float* lse_out;       // [BLH, G] base-2 LSE of the step's scores, or null
   float* scores_out;    // [rows, G] base-2 score of cache row off + i per query head, or null
+  // set by decode_tc_launch: with inplan the attention kernel builds the work
+  // list itself (no plan kernel); grid_items bounds the work-list length
+  int inplan;
+  int64_t grid_items;
 };
 
 // bf16, d = 128, G <= 8, a known packed extent below 2^31 rows, at most 65535

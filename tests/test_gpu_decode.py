@@ -112,6 +112,21 @@ def test_decode_matches_oracle_ragged(kvc, dtype, d, G, tc):
         assert (lmv[offs.reshape(-1) + lens.reshape(-1) + i] == 0).all()
 
 
+def test_tensor_core_decode_with_more_than_1024_heads(kvc):
+    """Above 1024 (b,l,h) the work list comes from the plan kernel instead of
+    each attention CTA's own scan: the same parity over 1056 ragged caches."""
+    cfg = W.small_config(B=1, L=33, H=32, G=1, d=128, dtype="bf16", P=16, W=16, n_decode=2)
+    rng = np.random.default_rng(11)
+    lens = rng.integers(0, 700, size=33 * 32)
+    lens, caps, offs, Kp, Vp, lm = _rand_cache(rng, 1, 33, 32, 128, lens, 2, "bf16")
+    outs, dlen, dKp, dlm, doff = _run_decode(kvc, cfg, lens, caps, offs, Kp, Vp, lm, 2, seed=5,
+                                             tc=True)
+    for got, want, err, cap_hit in outs:
+        assert err == 0 and not cap_hit
+        assert_bf16_close(got, want, "decode out")
+    np.testing.assert_array_equal(dlen.cpu().numpy(), (lens + 2).astype(np.int32))
+
+
 @pytest.mark.parametrize("tc", [False, True])
 def test_decode_capacity_overflow_reports_and_still_attends(kvc, tc):
     cfg = W.small_config(B=1, L=1, H=2, G=4, d=128, dtype="bf16", P=16, W=16, n_decode=0)

@@ -152,8 +152,9 @@ def test_graph_replay_equals_eager(kvc):
         launches = cache.run_many(q, kn, vn, out, nseen, posn, graph=graph)
         torch.cuda.synchronize()
         assert kvc.kvc_device_error() == 0
-        # decode (plan, attention, merge), alpha (groups, sum), eviction (plan, moves)
-        assert launches == T * 7
+        # decode (attention with its own work list, merge), alpha (groups, sum),
+        # eviction (plan, moves)
+        assert launches == T * 6
         rows = [int(x) for x in cache.len_lh.cpu()]
         res.append((out.float().cpu(), cache.K.float().cpu(), cache.pos.cpu(), rows))
     (o1, k1, p1, r1), (o2, k2, p2, r2) = res
