@@ -3,10 +3,12 @@
 // attends over each (layer, head)'s independently sized cache with the +ln m
 // bias; new tokens are appended with multiplicity one).
 //
-// A plan kernel lists the work: every (b,l,h) with len entries contributes
-// max(1, ceil(len / 512)) chunks.  The attention kernel is persistent (two
-// CTAs per SM loop over the list); one work item is one chunk of up to 4
-// tiles of 128 cached entries:
+// The work list: every (b,l,h) with len entries contributes
+// max(1, ceil(len / 512)) chunks, in (b,l,h) order.  Up to 1024 (b,l,h) each
+// attention CTA builds it in shared memory; beyond, a plan kernel writes it to
+// the workspace.  The attention kernel is persistent (two CTAs per SM loop
+// over the list); one work item is one chunk of up to 4 tiles of 128 cached
+// entries:
 //   QK   S^T[128 keys x 16] = K_tile x Q^T: the K tile arrives by TMA in
 //        128-byte-swizzled K-major form (A operand), the G query heads are the
 //        K-major B operand padded to 16 rows; fp32 accumulators in TMEM, one
@@ -19,10 +21,12 @@
 //        MN-major A operand straight from the TMA buffer.
 // K and V tiles share one 2-slot ring (load order K0..Kn-1, V0..Vn-1 per item,
 // items back to back; an item's 16 query rows arrive by TMA with its first
-// tile), so a CTA needs 90 KB of shared memory and two CTAs fit on an SM.  The
+// tile), so a CTA needs 94 KB of shared memory and two CTAs fit on an SM.  The
 // chunk partial (max, sum, O) goes to the workspace.  A merge kernel (one CTA
 // per (b,l,h)) then combines the partials with the new token in log-sum-exp
-// form, appends the token and increments len.
+// form, appends the token and increments len.  Plan, attention and merge are
+// launched with programmatic dependent launch (each waits for its predecessor
+// before reading its results).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
