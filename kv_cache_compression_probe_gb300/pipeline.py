@@ -138,6 +138,50 @@ class Compressor:
         self.select(slot_bounds, n_slots, head_sens, stream=stream, graph=graph)
         self.merge_pack(K, V, slot_bounds, n_slots, stream=stream, graph=graph)
 
+    def compress_from_host(self, h_K, h_V, h_Qp, K, V, Qp, slot_bounds, n_slots,
+                           head_sens=None, chunks: int = 4, copy_stream=None, graph=False):
+        """Batch 1, inputs in pinned host memory: copies K, V and the probes into the
+        device buffers K, V, Qp one layer chunk at a time on `copy_stream` while the
+        chunks already on the device are scored on the current stream (scoring has
+        no coupling across layers; the budget couples them only in select), then
+        selects and packs (as graph replays with graph=True).  Same results as
+        copying everything, then compress()."""
+        p = self.p
+        if p.B != 1:
+            raise ValueError("compress_from_host copies layer chunks of one sequence")
+        L, H, n = p.L, p.H, self.ctx_host[0]
+        dev = K.device
+        cur = torch.cuda.current_stream(dev)
+        cs = copy_stream if copy_stream is not None else torch.cuda.Stream(device=dev)
+        cs.wait_stream(cur)                          # the buffers are free to overwrite
+        cuts = [round(c * L / chunks) for c in range(chunks + 1)]
+        events = []
+        for c in range(chunks):
+            l0, l1 = cuts[c], cuts[c + 1]
+            r0, r1 = l0 * H * n, l1 * H * n
+            with torch.cuda.stream(cs):
+                K[r0:r1].copy_(h_K[r0:r1], non_blocking=True)
+                V[r0:r1].copy_(h_V[r0:r1], non_blocking=True)
+                Qp[:, l0:l1].copy_(h_Qp[:, l0:l1], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(cs)
+            events.append(ev)
+        for c in range(chunks):
+            l0, l1 = cuts[c], cuts[c + 1]
+            if l1 == l0:
+                continue
+            r0, r1 = l0 * H * n, l1 * H * n
+            cur.wait_event(events[c])
+            pc = kvc.kvc_params.from_buffer_copy(p)
+            pc.L = l1 - l0
+            kvc.kvc_score(pc, self.ctx_len, K[r0:r1], V[r0:r1], Qp[:, l0:l1], self.rope_cos,
+                          self.rope_sin, slot_bounds, n_slots,
+                          None if head_sens is None else head_sens[l0:l1], self.lse[:, l0:l1],
+                          self.feats[r0:r1], self.relevance[r0:r1], self.op_util[:, l0:l1],
+                          self.op_cost[:, l0:l1], self.ws_score, cur)
+        self.select(slot_bounds, n_slots, head_sens, graph=graph)
+        self.merge_pack(K, V, slot_bounds, n_slots, graph=graph)
+
     def decode(self, q, k_new, v_new, out, pos_new=None, stream=None):
         kvc.kvc_decode_attn(self.p, q, k_new, v_new, pos_new, self.Kp, self.Vp, self.logm,
                             self.pos, self.len_lh, self.cap_lh, self.off_lh, out, self.ws_decode,
