@@ -34,6 +34,19 @@ int cuda_status(cudaError_t e) {
   return KVC_ECUDA;
 }
 
+static int g_sms[256];
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return 0;
+  std::lock_guard<std::mutex> g(g_err_mu);
+  if (g_sms[dev] <= 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sms[dev] = n;
+  }
+  return g_sms[dev];
+}
+
 int32_t* err_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return nullptr;

@@ -21,6 +21,9 @@ void count_launch(int64_t n = 1);
 int cuda_status(cudaError_t e);
 // Common validation of a parameter block.
 int check_params(const kvc_params* p);
+// Streaming multiprocessors of the current device (queried once per device; 0
+// when the query fails).
+int sm_count();
 
 inline int64_t lh_count(const kvc_params* p) { return (int64_t)p->B * p->L * p->H; }
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }

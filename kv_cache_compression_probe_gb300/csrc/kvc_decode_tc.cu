@@ -699,18 +699,6 @@ cudaError_t launch_attn(const CUtensorMap& km, const CUtensorMap& vm, const CUte
   return launch_pdl(decode_merge_kernel<G>, dim3((unsigned)a.blh), dim3(128 * G), 0, s, a);
 }
 
-int sm_count() {
-  static std::once_flag once;
-  static int n = 0;
-  std::call_once(once, [] {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      n = 0;
-  });
-  return n;
-}
-
 }  // namespace
 
 namespace kvc {
@@ -748,7 +736,7 @@ int decode_tc_launch(const DecodeTcArgs& a, cudaStream_t s) {
   // every (l,h) has max(1, ceil(len / chunk)) <= len / chunk + 1 chunks and the
   // lengths sum to at most the packed extent
   const int64_t bound = std::min<int64_t>(a.blh * a.n_chunk_max, a.packed_rows / kChunkTc + a.blh);
-  const int sms = sm_count();
+  const int sms = kvc::sm_count();
   if (sms <= 0) return KVC_ECUDA;
   const unsigned grid = (unsigned)std::min<int64_t>(bound, 2LL * sms);   // persistent, 2 per SM
   DecodeTcArgs t = a;

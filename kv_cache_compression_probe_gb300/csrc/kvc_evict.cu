@@ -412,7 +412,8 @@ void launch_move(const kvc_params* p, void* K, void* V, float* pos, float* logm,
   // grid of about 4 CTAs per SM strides over them
   const int64_t blh = kvc::lh_count(p);
   const int need = (cols / 2 + kMoveRows) / kMoveRows;
-  const int x = (int)std::max<int64_t>(1, std::min<int64_t>(need, (4 * 152 + blh - 1) / blh));
+  const int64_t sms = std::max(1, kvc::sm_count());
+  const int x = (int)std::max<int64_t>(1, std::min<int64_t>(need, (4 * sms + blh - 1) / blh));
   dim3 grid(x, (unsigned)blh);
   evict_move_kernel<T, D><<<grid, 128, 0, s>>>(*p, static_cast<T*>(K), static_cast<T*>(V), pos,
                                                logm, off_lh, len_lh, dst, src, meta, cols);

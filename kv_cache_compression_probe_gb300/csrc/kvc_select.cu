@@ -684,7 +684,7 @@ extern "C" int kvc_select(const kvc_params* p, const int32_t* ctx_len, const int
   const kvc_params P = *p;
   const long long trees = (long long)p->B * p->L * p->H * p->S_max;
   const long long ops = trees * kOps;
-  const int sms = 152;
+  const int sms = std::max(1, kvc::sm_count());
   int launches = 0;
 
   sel_init_kernel<<<(p->B + 63) / 64, 64, 0, s>>>(P, ctx_len, n_slots, ws, err); ++launches;
