@@ -231,6 +231,21 @@ int kvc_decode_attn(const kvc_params* p, const void* q, const void* k_new, const
                     int32_t* len_lh, const int32_t* cap_lh, const int64_t* off_lh, void* out,
                     void* workspace, size_t ws_bytes, void* stream);
 
+/* kvc_decode_attn over the layers [layer_begin, layer_end) only, for callers
+ * that run the model layer by layer (each layer's queries exist only after the
+ * previous layer).  q, k_new, v_new and out cover the range:
+ * [B, layer_end - layer_begin, H*G (or H), d]; len_lh, cap_lh and off_lh are
+ * the whole [B, L, H] arrays (only the range's entries are read or advanced);
+ * p describes all L layers and the workspace is the one for p (shared with
+ * kvc_decode_attn; the same zeroing rule).  Results equal the range's part of
+ * a kvc_decode_attn call.  Errors: as kvc_decode_attn, and KVC_EINVAL unless
+ * 0 <= layer_begin < layer_end <= L. */
+int kvc_decode_attn_layers(const kvc_params* p, int32_t layer_begin, int32_t layer_end,
+                           const void* q, const void* k_new, const void* v_new,
+                           const float* pos_new, void* Kp, void* Vp, float* logm, float* pos,
+                           int32_t* len_lh, const int32_t* cap_lh, const int64_t* off_lh,
+                           void* out, void* workspace, size_t ws_bytes, void* stream);
+
 /* kvc_decode_attn that also returns the base-2 log-sum-exp of each query
  * head's scores over the len_lh + 1 entries it attended:
  *   lse_out[(b,l,h), g] = log2 sum_e 2^(s_e),  s_e = (q_g . k_e / sqrt(d) + logm_e) log2 e.

@@ -49,6 +49,7 @@ struct DecodeArgs {
   int32_t* counters;   // [BLH], zero between calls
   float* lse_out;      // [BLH, G] base-2 LSE of the step's scores, or null
   float* scores_out;   // [rows, G] base-2 score of cache row off + i per query head, or null
+  int64_t lh_span, lh_gap, lh_base;   // layer range (see kvc::lh_global)
   int H, L, n_chunk_max;
   float scale_log2;    // log2(e) / sqrt(d)
   int32_t* err;
@@ -152,7 +153,8 @@ __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(DecodeArgs a) {
   const int blh = blockIdx.y;
   const int c = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int len = a.len_lh[blh];
+  const int64_t gblh = kvc::lh_global(blh, a.lh_span, a.lh_gap, a.lh_base);
+  const int len = a.len_lh[gblh];
   const int E = len + 1;                                 // stored rows + the new token
   const int nchunks = (E + kChunk - 1) / kChunk;
   if (len < 0 || nchunks > a.n_chunk_max) {              // corrupt length: skip this (l,h)
@@ -163,8 +165,8 @@ __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(DecodeArgs a) {
   const int e0 = c * kChunk, e1 = min(e0 + kChunk, E);
   const int stored_end = min(e1, len);                   // rows [e0, stored_end) come from the cache
   const int nst = stored_end > e0 ? (stored_end - e0 + kStage - 1) / kStage : 0;
-  const int64_t off = a.off_lh[blh];
-  const bool append_ok = (len + 1 <= a.cap_lh[blh]);
+  const int64_t off = a.off_lh[gblh];
+  const bool append_ok = (len + 1 <= a.cap_lh[gblh]);
   const int h = blh % a.H;
   const int64_t bl = blh / a.H;                          // b * L + l
 
@@ -318,9 +320,11 @@ __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(DecodeArgs a) {
 
 // Commits the append once every chunk has read the old length.
 __global__ void decode_commit_kernel(int32_t* len_lh, const int32_t* cap_lh, int64_t n,
-                                     int n_chunk_max, int32_t* err) {
-  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
+                                     int n_chunk_max, int64_t span, int64_t gap, int64_t base,
+                                     int32_t* err) {
+  const int64_t li = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (li >= n) return;
+  const int64_t i = kvc::lh_global(li, span, gap, base);
   const int len = len_lh[i];
   if (len < 0 || (len + kChunk) / kChunk > n_chunk_max) return;   // skipped by the attention
   if (len + 1 <= cap_lh[i]) len_lh[i] = len + 1;
@@ -370,9 +374,14 @@ DecodeLayout decode_layout(const kvc_params* p) {
 int run_decode(const kvc_params* p, const void* q, const void* k_new, const void* v_new,
                const float* pos_new, void* Kp, void* Vp, float* logm, float* pos,
                int32_t* len_lh, const int32_t* cap_lh, const int64_t* off_lh, void* out,
-               float* lse_out, float* scores_out, char* ws, int32_t* err, cudaStream_t s) {
+               float* lse_out, float* scores_out, char* ws, int32_t* err, cudaStream_t s,
+               int64_t lh_span = 0, int64_t lh_gap = 0, int64_t lh_base = 0,
+               const kvc_params* layout_p = nullptr) {
+  if (lh_span <= 0) lh_span = (int64_t)p->L * p->H;         // all layers: identity map
   const int64_t blh = kvc::lh_count(p);
-  const DecodeLayout w = decode_layout(p);
+  // the workspace layout always follows the full parameter block, so calls on
+  // layer ranges and on all layers share the same arrival-counter words
+  const DecodeLayout w = decode_layout(layout_p ? layout_p : p);
   const int ncm = n_chunk_max(p);
   if (kvc::decode_tc_supported(p, ncm)) {
     kvc::DecodeTcArgs t;
@@ -390,6 +399,7 @@ int run_decode(const kvc_params* p, const void* q, const void* k_new, const void
     t.err = err;
     t.lse_out = lse_out;
     t.scores_out = scores_out;
+    t.lh_span = lh_span; t.lh_gap = lh_gap; t.lh_base = lh_base;
     return kvc::decode_tc_launch(t, s);
   }
   DecodeArgs a;
@@ -403,6 +413,7 @@ int run_decode(const kvc_params* p, const void* q, const void* k_new, const void
   a.err = err;
   a.lse_out = lse_out;
   a.scores_out = scores_out;
+  a.lh_span = lh_span; a.lh_gap = lh_gap; a.lh_base = lh_base;
   dim3 grid(a.n_chunk_max, (unsigned)blh);
   if (p->dtype == KVC_BF16) {
     if (p->d == 128) launch_dg<__nv_bfloat16, 128>(p, a, grid, s);
@@ -411,8 +422,8 @@ int run_decode(const kvc_params* p, const void* q, const void* k_new, const void
     if (p->d == 128) launch_dg<float, 128>(p, a, grid, s);
     else launch_dg<float, 64>(p, a, grid, s);
   }
-  decode_commit_kernel<<<(unsigned)((blh + 255) / 256), 256, 0, s>>>(len_lh, cap_lh, blh,
-                                                                       a.n_chunk_max, err);
+  decode_commit_kernel<<<(unsigned)((blh + 255) / 256), 256, 0, s>>>(
+      len_lh, cap_lh, blh, a.n_chunk_max, lh_span, lh_gap, lh_base, err);
   kvc::count_launch(2);
   return kvc::cuda_status(cudaGetLastError());
 }
@@ -442,6 +453,34 @@ extern "C" int kvc_decode_attn(const kvc_params* p, const void* q, const void* k
   return run_decode(p, q, k_new, v_new, pos_new, Kp, Vp, logm, pos, len_lh, cap_lh, off_lh, out,
                     nullptr, nullptr, static_cast<char*>(workspace), err,
                     static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int kvc_decode_attn_layers(const kvc_params* p, int32_t layer_begin,
+                                      int32_t layer_end, const void* q, const void* k_new,
+                                      const void* v_new, const float* pos_new, void* Kp, void* Vp,
+                                      float* logm, float* pos, int32_t* len_lh,
+                                      const int32_t* cap_lh, const int64_t* off_lh, void* out,
+                                      void* workspace, size_t ws_bytes, void* stream) {
+  int st = kvc::check_params(p);
+  if (st != KVC_OK) return st;
+  if (!q || !k_new || !v_new || !Kp || !Vp || !logm || !pos || !len_lh || !cap_lh || !off_lh ||
+      !out || layer_begin < 0 || layer_end > p->L || layer_begin >= layer_end)
+    return KVC_EINVAL;
+  const size_t need = kvc::decode_workspace_bytes(p);
+  if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return KVC_EWORKSPACE;
+  if (kvc::lh_count(p) > 65535) return KVC_EINVAL;
+  int32_t* err = kvc::err_word();
+  if (!err) return KVC_ECUDA;
+  // the range's (b,l,h) are local to the call; the per-(b,l,h) arrays stay whole
+  kvc_params pr = *p;
+  pr.L = layer_end - layer_begin;
+  const int64_t span = (int64_t)pr.L * p->H;
+  const int64_t gap = (int64_t)(p->L - pr.L) * p->H;
+  const int64_t base = (int64_t)layer_begin * p->H;
+  return run_decode(&pr, q, k_new, v_new, pos_new, Kp, Vp, logm, pos, len_lh, cap_lh, off_lh, out,
+                    nullptr, nullptr, static_cast<char*>(workspace), err,
+                    static_cast<cudaStream_t>(stream), span, gap, base, p);
 }
 
 extern "C" int kvc_decode_attn_lse(const kvc_params* p, const void* q, const void* k_new,

@@ -123,8 +123,9 @@ __device__ __forceinline__ void named_sync(int id, int n) {
 
 // Chunks of (b,l,h) i; -1 for a corrupt entry.
 __device__ __forceinline__ int chunks_of(const kvc::DecodeTcArgs& a, int64_t i) {
-  const int len = a.len_lh[i];
-  const int64_t off = a.off_lh[i];
+  const int64_t gi = kvc::lh_global(i, a.lh_span, a.lh_gap, a.lh_base);
+  const int len = a.len_lh[gi];
+  const int64_t off = a.off_lh[gi];
   if (len < 0 || off < 0 || off + len > a.packed_rows ||
       (len + kChunkTc) / kChunkTc > a.n_chunk_max)
     return -1;
@@ -221,8 +222,9 @@ __device__ __forceinline__ Item item_at(const kvc::DecodeTcArgs& a, int idx, con
     it.blh = (int)(w & 0xFFFFu);
     it.c = (int)(w >> 16);
   }
-  it.len = __ldcg(a.len_lh + it.blh);      // read before this (l,h)'s last chunk arrives
-  it.off = a.off_lh[it.blh];
+  const int64_t gi = kvc::lh_global(it.blh, a.lh_span, a.lh_gap, a.lh_base);
+  it.len = __ldcg(a.len_lh + gi);          // read before this (l,h)'s last chunk arrives
+  it.off = a.off_lh[gi];
   it.nchunks = it.len > 0 ? (it.len + kChunkTc - 1) / kChunkTc : 1;
   it.nvalid = max(0, min(kChunkTc, it.len - it.c * kChunkTc));
   it.ntiles = (it.nvalid + kTileRows - 1) / kTileRows;
@@ -549,8 +551,9 @@ __global__ void __launch_bounds__(128 * G) decode_merge_kernel(kvc::DecodeTcArgs
   kvcd::pdl_wait();                                   // the attention kernel's partials
   const int blh = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int len = a.len_lh[blh];
-  const int64_t off = a.off_lh[blh];
+  const int64_t gblh = kvc::lh_global(blh, a.lh_span, a.lh_gap, a.lh_base);
+  const int len = a.len_lh[gblh];
+  const int64_t off = a.off_lh[gblh];
   if (len < 0 || off < 0 || off + len > a.packed_rows || (len + kChunkTc) / kChunkTc > a.n_chunk_max)
     return;                                          // reported by the plan
   const int nch = len > 0 ? (len + kChunkTc - 1) / kChunkTc : 1;
@@ -567,7 +570,7 @@ __global__ void __launch_bounds__(128 * G) decode_merge_kernel(kvc::DecodeTcArgs
       acc = fmaf(__bfloat162float(qp[warp * kD + f]), __bfloat162float(kn[f]), acc);
     const float sn = kvcd::warp_sum(acc) * a.scale_log2;
     if (lane == 0) s_new[warp] = sn;
-    if (a.scores_out && lane == 0 && len + 1 <= a.cap_lh[blh] && off + len + 1 <= a.packed_rows)
+    if (a.scores_out && lane == 0 && len + 1 <= a.cap_lh[gblh] && off + len + 1 <= a.packed_rows)
       a.scores_out[(off + len) * G + warp] = sn;
   }
   // thread (g, dd): partials of every chunk, 8 chunks of loads in flight at a
@@ -613,7 +616,7 @@ __global__ void __launch_bounds__(128 * G) decode_merge_kernel(kvc::DecodeTcArgs
     outp[g * kD + dd] = __float2bfloat16_rn(o / lt);
     if (a.lse_out && dd == 0) a.lse_out[(int64_t)blh * G + g] = Mf + log2f(lt);
   }
-  if (len + 1 <= a.cap_lh[blh] && off + len + 1 <= a.packed_rows) {
+  if (len + 1 <= a.cap_lh[gblh] && off + len + 1 <= a.packed_rows) {
     __nv_bfloat16* Kw = static_cast<__nv_bfloat16*>(a.Kp) + (off + len) * kD;
     __nv_bfloat16* Vw = static_cast<__nv_bfloat16*>(a.Vp) + (off + len) * kD;
     if (tid < kD) {
@@ -623,7 +626,7 @@ __global__ void __launch_bounds__(128 * G) decode_merge_kernel(kvc::DecodeTcArgs
     if (tid == 0) {
       a.logm[off + len] = 0.f;
       a.pos[off + len] = a.pos_new ? a.pos_new[bl / a.L] : -1.f;
-      a.len_lh[blh] = len + 1;
+      a.len_lh[gblh] = len + 1;
     }
   } else if (tid == 0) {
     kvcd::record_error(a.err, KVC_ECAPACITY);

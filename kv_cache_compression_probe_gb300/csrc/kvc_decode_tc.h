@@ -35,7 +35,15 @@ struct DecodeTcArgs {
   // list itself (no plan kernel); grid_items bounds the work-list length
   int inplan;
   int64_t grid_items;
+  // layer range: local (b,l,h) i indexes the per-(b,l,h) arrays (len_lh,
+  // cap_lh, off_lh) at i + (i / lh_span) * lh_gap + lh_base (identity for all
+  // layers: span = L*H, gap = 0, base = 0); everything else is local
+  int64_t lh_span, lh_gap, lh_base;
 };
+
+__host__ __device__ inline int64_t lh_global(int64_t i, int64_t span, int64_t gap, int64_t base) {
+  return i + (i / span) * gap + base;
+}
 
 // bf16, d = 128, G <= 8, a known packed extent below 2^31 rows, at most 65535
 // (b,l,h) and chunks per (l,h), and a driver that can encode tensor maps.

@@ -25,7 +25,7 @@ EXPORTED = ("kvc_status_string", "kvc_last_cuda_error", "kvc_device_error", "kvc
             "kvc_rope_table", "kvc_score", "kvc_select", "kvc_merge_pack", "kvc_decode_attn",
             "kvc_partition", "kvc_decode_attn_noalloc", "kvc_decode_attn_lse", "kvc_token_alpha",
             "kvc_evict_workspace_bytes", "kvc_evict_topb", "kvc_set_phase_timing",
-            "kvc_score_phase_ms")
+            "kvc_score_phase_ms", "kvc_decode_attn_layers")
 
 
 class kvc_params(ctypes.Structure):
@@ -78,6 +78,8 @@ def lib():
         L.kvc_decode_attn.restype = c_int
         L.kvc_decode_attn_noalloc.argtypes = [_P] + [vp] * 13
         L.kvc_decode_attn_noalloc.restype = c_int
+        L.kvc_decode_attn_layers.argtypes = [_P, c_int32, c_int32] + [vp] * 13 + [c_size_t, vp]
+        L.kvc_decode_attn_layers.restype = c_int
         L.kvc_decode_attn_lse.argtypes = [_P] + [vp] * 15 + [c_size_t, vp]
         L.kvc_decode_attn_lse.restype = c_int
         L.kvc_token_alpha.argtypes = [_P] + [vp] * 7 + [c_int32, vp, c_size_t, vp]
@@ -193,6 +195,18 @@ def kvc_decode_attn(p, q, k_new, v_new, pos_new, Kp, Vp, logm, pos, len_lh, cap_
                                  _ptr(pos_new), _ptr(Kp), _ptr(Vp), _ptr(logm), _ptr(pos),
                                  _ptr(len_lh), _ptr(cap_lh), _ptr(off_lh), _ptr(out), w, wb,
                                  _stream(stream)), "kvc_decode_attn")
+
+
+def kvc_decode_attn_layers(p, layer_begin, layer_end, q, k_new, v_new, pos_new, Kp, Vp, logm,
+                           pos, len_lh, cap_lh, off_lh, out, workspace, stream=None):
+    """kvc_decode_attn over layers [layer_begin, layer_end) (q, k_new, v_new, out
+    cover the range; the per-(b,l,h) arrays are whole)."""
+    w, wb = _ws(workspace)
+    _check(lib().kvc_decode_attn_layers(ctypes.byref(p), int(layer_begin), int(layer_end), _ptr(q),
+                                        _ptr(k_new), _ptr(v_new), _ptr(pos_new), _ptr(Kp),
+                                        _ptr(Vp), _ptr(logm), _ptr(pos), _ptr(len_lh),
+                                        _ptr(cap_lh), _ptr(off_lh), _ptr(out), w, wb,
+                                        _stream(stream)), "kvc_decode_attn_layers")
 
 
 def kvc_decode_attn_noalloc(p, q, k_new, v_new, pos_new, Kp, Vp, logm, pos, len_lh, cap_lh,

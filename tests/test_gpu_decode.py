@@ -185,3 +185,51 @@ def test_tc_decode_skips_and_reports_entries_past_the_packed_extent(kvc):
                                   Kp[o:o + 200].astype(np.float64), Vp[o:o + 200].astype(np.float64),
                                   lm[o:o + 200].astype(np.float64))
     assert_bf16_close(got[0, 0, :4], want, "decode of the in-extent head")
+
+
+@pytest.mark.parametrize("tc", [False, True])
+def test_layer_range_decode_equals_all_layers(kvc, tc):
+    """kvc_decode_attn_layers called layer by layer (batch 2, so a layer's
+    (b,l,h) are strided in the per-(b,l,h) arrays) gives, bit for bit, the
+    outputs, lengths and appended rows of kvc_decode_attn over all layers."""
+    B, L, H, G, d = 2, 3, 2, 4, 128
+    cfg = W.small_config(B=B, L=L, H=H, G=G, d=d, dtype="bf16", P=16, W=16, n_decode=2)
+    rng = np.random.default_rng(21)
+    lens = rng.integers(0, 900, size=B * L * H)
+    lens, caps, offs, Kp, Vp, lm = _rand_cache(rng, B, L, H, d, lens, 3, "bf16")
+    p = params_for(cfg, n_max=max(int(lens.max()) + 64, cfg.W + 16), S_max=1,
+                   packed_rows=Kp.shape[0] if tc else 0)
+    bf = torch.bfloat16
+    caches = []
+    for _ in range(2):
+        caches.append(dict(K=dev(Kp, bf), V=dev(Vp, bf), lm=dev(lm),
+                           pos=torch.zeros(Kp.shape[0], device="cuda"),
+                           len=dev(lens.astype(np.int32)),
+                           ws=kvc.workspace(kvc.KVC_WS_DECODE, p, zero=True)))
+    cap, off = dev(caps.astype(np.int32)), dev(offs.astype(np.int64))
+    for t in range(2):
+        q = dev(W.round_bf16(rng.standard_normal((B, L, H * G, d)).astype(np.float32)), bf)
+        kn = dev(W.round_bf16(rng.standard_normal((B, L, H, d)).astype(np.float32)), bf)
+        vn = dev(W.round_bf16(rng.standard_normal((B, L, H, d)).astype(np.float32)), bf)
+        posn = torch.full((B,), 500.0 + t, device="cuda")
+        a, c = caches
+        out_a = torch.empty((B, L, H * G, d), dtype=bf, device="cuda")
+        kvc.kvc_decode_attn(p, q, kn, vn, posn, a["K"], a["V"], a["lm"], a["pos"], a["len"], cap,
+                            off, out_a, a["ws"])
+        out_c = torch.empty_like(out_a)
+        for l in range(L):
+            o = torch.empty((B, 1, H * G, d), dtype=bf, device="cuda")
+            kvc.kvc_decode_attn_layers(p, l, l + 1, q[:, l:l + 1].contiguous(),
+                                       kn[:, l:l + 1].contiguous(), vn[:, l:l + 1].contiguous(),
+                                       posn, c["K"], c["V"], c["lm"], c["pos"], c["len"], cap, off,
+                                       o, c["ws"])
+            out_c[:, l:l + 1] = o
+        torch.cuda.synchronize()
+        assert kvc.kvc_device_error() == 0
+        assert torch.equal(out_a, out_c)
+        for k in ("len", "K", "V", "lm", "pos"):
+            assert torch.equal(a[k], c[k]), k
+    with pytest.raises(kvc.KvcError):
+        kvc.kvc_decode_attn_layers(p, 2, 2, q[:, :1].contiguous(), kn[:, :1].contiguous(),
+                                   vn[:, :1].contiguous(), posn, c["K"], c["V"], c["lm"], c["pos"],
+                                   c["len"], cap, off, out_c[:, :1].contiguous(), c["ws"])
