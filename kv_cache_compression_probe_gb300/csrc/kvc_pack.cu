@@ -7,8 +7,9 @@
 //   kbar = mean k~_i,  kappa = mean cos(k~_i, kbar)
 //          (= (sum k~_i/|k~_i|) . kbar / (c |kbar|), accumulated in one pass)
 //   m    = c * clamp(kappa, 1/c, 1),  stored as ln m (decode adds it to the logit)
-//   k^   = R(pbar) kbar, pbar = (x + y - 1)/2 (table row x + y - 1 of the
-//          half-position RoPE table)
+//   k^   = R(pbar) kbar, pbar = (x + y - 1)/2; computed in the frame of the
+//          node start x (rotations add up: k^ = R(pbar - x) mean R(-(i - x)) k_i),
+//          so every angle is a half-position table row below 256
 //   v^   = sum w_i v_i, w_i = (1-f) r_i / sum r + f / c  (uniform when sum r = 0)
 // Split leaves store their tokens bit-exact (ln m = 0, pos = i); the W window
 // tokens follow the slots.  Entry order per (b,l,h): slots ascending, each
@@ -163,8 +164,11 @@ __device__ void write_prototype(const kvc_params& p, const PackArgs& a, const T*
       const int i = i0 + (g < ng ? g : 0);              // a repeated row is loaded, not used
       load_pairs<T, D>(Kh + (int64_t)i * D, lane, klo[g], khi[g]);
       load_pairs<T, D>(Vh + (int64_t)i * D, lane, vlo[g], vhi[g]);
-      const float* ct = a.cos_tab + (int64_t)(2 * i) * HALF + lane * VP;
-      const float* st = a.sin_tab + (int64_t)(2 * i) * HALF + lane * VP;
+      // angles relative to the node start x (rows 0..254 of the half-position
+      // table, hot in L1 for every node): the mean of R(-i) k_i is R(-x) times
+      // the mean of R(-(i - x)) k_i, and R(-x) cancels in the rerotation below
+      const float* ct = a.cos_tab + (int64_t)(2 * (i - x)) * HALF + lane * VP;
+      const float* st = a.sin_tab + (int64_t)(2 * (i - x)) * HALF + lane * VP;
       if constexpr (VP == 2) {
         const float2 c2 = __ldg(reinterpret_cast<const float2*>(ct));
         const float2 s2 = __ldg(reinterpret_cast<const float2*>(st));
@@ -224,8 +228,8 @@ __device__ void write_prototype(const kvc_params& p, const PackArgs& a, const T*
   const float m = (float)c * fminf(fmaxf(kap, inv_c), 1.f);
   const float f = p.value_floor;
   // rerotate the mean at pbar = (x + y - 1) / 2: half-position table row x + y - 1
-  const float* ct = a.cos_tab + (int64_t)(x + y - 1) * HALF + lane * VP;
-  const float* st = a.sin_tab + (int64_t)(x + y - 1) * HALF + lane * VP;
+  const float* ct = a.cos_tab + (int64_t)(y - x - 1) * HALF + lane * VP;   // pbar - x
+  const float* st = a.sin_tab + (int64_t)(y - x - 1) * HALF + lane * VP;
   T* ko = static_cast<T*>(a.Kp) + dst * D;
   T* vo = static_cast<T*>(a.Vp) + dst * D;
 #pragma unroll
