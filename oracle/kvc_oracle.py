@@ -17,7 +17,7 @@ Sources (web pages, cited by title and section):
         section 3.1.4 (the eviction error bound), Algorithm 1 (top-B pruning).
 
 Where the pages leave a step open the oracle takes one stated reading; the
-readings are numbered R1..R15 and listed in the repository's design notes.
+readings are numbered R1..R18 and listed in the repository's design notes.
 Each function names the readings it uses.
 
 Parity status: the scoring, hop, prototype, decode, pack and budget steps are
@@ -157,16 +157,20 @@ def hop_relevance(alpha: np.ndarray, Kh: np.ndarray, Vh: np.ndarray, S_h: int,
 
 
 # =============================================================================== a3: trees and prototypes
-def tree_nodes(x: int, y: int) -> List[Tuple[int, int]]:
+def tree_nodes(x: int, y: int, cuts: Optional[Sequence[int]] = None) -> List[Tuple[int, int]]:
     """The 15 prototype nodes of a slot [x, y) in breadth-first order (reading R3).
 
-    Node j has children 2j+1 and 2j+2; a node [a, b) splits at floor((a+b)/2).
-    Nodes 7..14 are the leaf prototypes; splitting one yields its tokens.
+    Node j has children 2j+1 and 2j+2; a node [a, b) splits at floor((a+b)/2),
+    or, when ``cuts`` is given, at the absolute position cuts[j] (j < 7; the
+    curvature-chosen trees of reading R18).  Nodes 7..14 are the leaf
+    prototypes; splitting one yields its tokens.
     """
     nodes = [(x, y)]
     for j in range(7):
         a, b = nodes[j]
-        mid = (a + b) // 2
+        mid = (a + b) // 2 if cuts is None else int(cuts[j])
+        if not a < mid < b:
+            raise ValueError(f"cut {mid} of node {j} outside ({a}, {b})")
         nodes.append((a, mid))
         nodes.append((mid, b))
     return nodes
@@ -292,8 +296,10 @@ class HeadResult:
 def score_and_value_head(Kh, Vh, Qh, n: int, P: int, bounds: np.ndarray, sens: float,
                          base: float = 10000.0, hop_weight: float = 0.3, n_hops: int = 2,
                          w_part: float = 0.25, w_value: float = 0.75, value_floor: float = 0.1,
-                         S_h: Optional[int] = None, keep_protos: bool = False) -> HeadResult:
-    """Everything the scoring call produces for one (layer, KV head): a1 -> a4."""
+                         S_h: Optional[int] = None, keep_protos: bool = False,
+                         cuts: Optional[np.ndarray] = None) -> HeadResult:
+    """Everything the scoring call produces for one (layer, KV head): a1 -> a4.
+    ``cuts`` [S, 7] gives the trees' cut positions (R18); None = midpoint trees."""
     Kh = np.asarray(Kh, np.float64)
     Vh = np.asarray(Vh, np.float64)
     G = Qh.shape[0]
@@ -311,7 +317,7 @@ def score_and_value_head(Kh, Vh, Qh, n: int, P: int, bounds: np.ndarray, sens: f
     protos_all = []
     for s in range(S):
         x0, y0 = int(bounds[s]), int(bounds[s + 1])
-        nodes = tree_nodes(x0, y0)
+        nodes = tree_nodes(x0, y0, None if cuts is None else cuts[s])
         D = np.zeros(N_NODES)
         Dd = np.zeros(N_NODES)
         Rv = np.zeros(N_NODES)
@@ -332,6 +338,81 @@ def score_and_value_head(Kh, Vh, Qh, n: int, P: int, bounds: np.ndarray, sens: f
                       D=Dall, Ddrop=Ddall, protos=protos_all if keep_protos else None)
 
 
+# =============================================================================== f3: curvature-chosen trees
+LEAF_MAX = 16         # R18: a cut may not leave a leaf prototype of more than 16 tokens
+
+
+def key_curvature(Kh: np.ndarray, base: float, scales: Sequence[int] = (1, 2, 4, 8)) -> np.ndarray:
+    """Curvature of one (layer, KV head)'s key trajectory (reading R18).
+
+    [GK] "01 Curvature-guided partition" measures where a normalized trajectory
+    turns; the tree of a (layer, KV head, slot) is cut with the same measure
+    taken on that head's own keys with RoPE removed (k~_i = R(-i) k_i, so the
+    position rotation itself is no turn): the multi-scale curvature of
+    ``curvature`` on the rows k~_i."""
+    Kh = np.asarray(Kh, np.float64)
+    u = rope_rotate(Kh, -np.arange(Kh.shape[0], dtype=np.float64), base)
+    return curvature(u, scales)
+
+
+def tree_cuts(kappa: np.ndarray, x0: int, y0: int, dtype=np.float64) -> List[int]:
+    """Cut positions of the 7 internal nodes (breadth-first) of slot [x0, y0)
+    ([GK] "Technical details": tree construction considers high-curvature split
+    candidates plus the midpoint), reading R18.
+
+    Top-down, node [a, b) of depth k (c = b - a tokens, midpoint m =
+    floor((a+b)/2)) is cut at the valid t maximising
+        score(t) = kappa[t] - lam * ((t - m) / (c / 2))^2,   lam = mean kappa[a:b)
+    (the partition's curvature gain with its length-balance penalty, so the
+    midpoint, penalty 0, wins unless a turn outweighs its imbalance).  A cut at
+    t makes children [a, t) and [t, b); it is valid when each child keeps one
+    token per leaf below it (2^(2-k)) and at most LEAF_MAX per leaf
+    (LEAF_MAX * 2^(2-k)); the midpoint of every slot of 16..128 tokens always
+    is.  Ties go to the midpoint, then to the smaller t.  Every operation is
+    rounded to ``dtype`` in the order written (lam summed in index order), so
+    ``dtype=np.float32`` reproduces a single-precision evaluation exactly.
+    """
+    f = np.dtype(dtype).type
+    k = np.asarray(kappa).astype(dtype)
+    nodes = [(x0, y0)]
+    cuts = []
+    for j in range(7):
+        a, b = nodes[j]
+        depth = 0 if j == 0 else (1 if j < 3 else 2)
+        lo = 2 ** (2 - depth)
+        hi = LEAF_MAX * lo
+        c = b - a
+        m = (a + b) // 2
+        acc = f(0)
+        for i in range(a, b):
+            acc = f(acc + k[i])
+        lam = f(acc / f(c))
+        half = f(f(c) * f(0.5))
+
+        def score(t):
+            r = f(f(t - m) / half)
+            return f(k[t] - f(lam * f(r * r)))
+
+        best_t, best = m, score(m)
+        for t in range(a + lo, b - lo + 1):
+            if not (lo <= t - a <= hi and lo <= b - t <= hi):
+                continue
+            sc = score(t)
+            if sc > best:
+                best_t, best = t, sc
+        cuts.append(best_t)
+        nodes.append((a, best_t))
+        nodes.append((best_t, b))
+    return cuts
+
+
+def slot_cuts(kappa: np.ndarray, bounds: np.ndarray, dtype=np.float64) -> np.ndarray:
+    """``tree_cuts`` of every slot of one (layer, KV head): [S, 7] absolute positions."""
+    S = len(bounds) - 1
+    return np.asarray([tree_cuts(kappa, int(bounds[s]), int(bounds[s + 1]), dtype)
+                       for s in range(S)], dtype=np.int64).reshape(S, 7)
+
+
 # =============================================================================== a5: budget, floor, auction
 def budget(n: int, L: int, H: int, W: int, budget_ratio: float, budget_entries_per_lh: int,
            floor_cap_frac: float):
@@ -350,9 +431,9 @@ def budget(n: int, L: int, H: int, W: int, budget_ratio: float, budget_entries_p
     return B_tot, B_alloc, cap
 
 
-def _leaf_of(i: int, x0: int, y0: int) -> Tuple[int, List[int]]:
+def _leaf_of(i: int, x0: int, y0: int, cuts=None) -> Tuple[int, List[int]]:
     """Leaf node containing token i and the node path root..leaf."""
-    nodes = tree_nodes(x0, y0)
+    nodes = tree_nodes(x0, y0, cuts)
     j = 0
     path = [0]
     while j < FIRST_LEAF:
@@ -374,7 +455,8 @@ class Selection:
 
 
 def singleton_floor(r: np.ndarray, sens: np.ndarray, bounds: np.ndarray, cost: np.ndarray,
-                    cap_entries: int, cap_tokens: int, taken: np.ndarray):
+                    cap_entries: int, cap_tokens: int, taken: np.ndarray,
+                    cuts: Optional[np.ndarray] = None):
     """Capped singleton floor before the auction ([GK] "Exact-information
     safeguard" and technical details), reading R6.
 
@@ -385,7 +467,8 @@ def singleton_floor(r: np.ndarray, sens: np.ndarray, bounds: np.ndarray, cost: n
     token already exact is skipped at no cost.  If the path fits in the cap it
     is taken and the token counted, otherwise the floor stops; it also stops
     once cap_tokens tokens are counted (cap_tokens < 0: no token cap).
-    The key r * sens is computed in the precision of ``r``.
+    The key r * sens is computed in the precision of ``r``.  ``cuts`` [L, H,
+    S, 7] gives the trees' cut positions (R18); None = midpoint trees.
     Mutates ``taken`` and returns (spent, tokens).
     """
     L, H, n_ = r.shape
@@ -410,7 +493,7 @@ def singleton_floor(r: np.ndarray, sens: np.ndarray, bounds: np.ndarray, cost: n
         l, h = divmod(lh, H)
         s = int(slot_of[i])
         x0, y0 = int(bounds[s]), int(bounds[s + 1])
-        leaf, path = _leaf_of(i, x0, y0)
+        leaf, path = _leaf_of(i, x0, y0, None if cuts is None else cuts[l, h, s])
         t = taken[l, h, s]
         if t[1 + leaf]:
             continue                                   # already exact
@@ -499,14 +582,14 @@ def full_heads(r: np.ndarray, end: int, frac: float) -> np.ndarray:
 def select_sequence(util: np.ndarray, cost: np.ndarray, r: np.ndarray, sens: np.ndarray,
                     bounds: np.ndarray, n: int, W: int, budget_ratio: float,
                     budget_entries_per_lh: int, floor_cap_frac: float, floor_cap_tokens: int,
-                    head_full_frac: float = 0.0) -> Selection:
+                    head_full_frac: float = 0.0, cuts: Optional[np.ndarray] = None) -> Selection:
     """Budget -> singleton floor -> greedy auction for one sequence (a5).
 
     With head_full_frac > 0 (the head-level hybrid, R16) the full heads store
     every token exact (all ops taken, len = n) and pay n - W beyond their
     window from the same budget; the floor and the auction run on the other
     heads with B_alloc = B_tot - W*L*H - F*(n - W) and the floor cap taken of
-    that reduced pool."""
+    that reduced pool.  ``cuts`` [L, H, S, 7]: the trees' cut positions (R18)."""
     L, H, S, _ = util.shape
     B_tot, B_alloc, cap = budget(n, L, H, W, budget_ratio, budget_entries_per_lh, floor_cap_frac)
     taken = np.zeros((L, H, S, N_OPS), dtype=bool)
@@ -517,7 +600,8 @@ def select_sequence(util: np.ndarray, cost: np.ndarray, r: np.ndarray, sens: np.
         if B_alloc < 0:
             raise ValueError("budget smaller than the full heads and the windows")
         cap = int(math.floor(floor_cap_frac * B_alloc))
-    fs, ft = singleton_floor(r, sens, bounds, cost, min(cap, B_alloc), floor_cap_tokens, taken)
+    fs, ft = singleton_floor(r, sens, bounds, cost, min(cap, B_alloc), floor_cap_tokens, taken,
+                             cuts)
     asp = greedy_auction(util, cost, taken, B_alloc - fs)
     lens = W + (taken * cost).sum(axis=(2, 3))
     return Selection(taken=taken, floor_spent=fs, floor_tokens=ft, auction_spent=asp,
@@ -525,11 +609,11 @@ def select_sequence(util: np.ndarray, cost: np.ndarray, r: np.ndarray, sens: np.
 
 
 # =============================================================================== a6: pack
-def frontier(t: np.ndarray, x0: int, y0: int) -> List[Tuple[str, int]]:
+def frontier(t: np.ndarray, x0: int, y0: int, cuts=None) -> List[Tuple[str, int]]:
     """Stored entries of one slot tree, left to right ([GK] "05 Physical cache
     packing"): an absent root stores nothing, a present unsplit node stores its
     prototype, a split leaf prototype stores its tokens exactly."""
-    nodes = tree_nodes(x0, y0)
+    nodes = tree_nodes(x0, y0, cuts)
 
     def visit(j):
         if not t[1 + j]:
@@ -553,7 +637,8 @@ class Packed:
     offs: np.ndarray         # [B, L, H] exclusive prefix sum of caps in (b, l, h) order
 
 
-def pack_head(Kh, Vh, r, bounds, t_lh, n: int, W: int, base: float, value_floor: float):
+def pack_head(Kh, Vh, r, bounds, t_lh, n: int, W: int, base: float, value_floor: float,
+              cuts: Optional[np.ndarray] = None):
     """Entries of one (l, h): slots ascending, frontier left to right, then the
     window tokens [n - W, n).  Exact tokens keep their K/V and get log m = 0."""
     Kh = np.asarray(Kh, np.float64)
@@ -561,8 +646,9 @@ def pack_head(Kh, Vh, r, bounds, t_lh, n: int, W: int, base: float, value_floor:
     ks, vs, lm, ps = [], [], [], []
     for s in range(len(bounds) - 1):
         x0, y0 = int(bounds[s]), int(bounds[s + 1])
-        nodes = tree_nodes(x0, y0)
-        for kind, j in frontier(t_lh[s], x0, y0):
+        cs = None if cuts is None else cuts[s]
+        nodes = tree_nodes(x0, y0, cs)
+        for kind, j in frontier(t_lh[s], x0, y0, cs):
             if kind == "tok":
                 ks.append(Kh[j]); vs.append(Vh[j]); lm.append(0.0); ps.append(float(j))
             else:
