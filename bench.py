@@ -302,6 +302,44 @@ def evict_leg(p, cfg, seqs, K, V, q_all, kn_all, vn_all, D, dev, stream):
                     "evicted to the budget at the first step, then one entry per step"}
 
 
+def tree_cuts_leg(comp, K, bounds, n_slots, cfg, tokens, hbm, dev, reps=5):
+    """f3: device time of kvc_tree_cuts alone (curvature of every key, then the
+    cut of every internal tree node), CUDA events around `reps` calls after one
+    untimed call.  Algorithmic bytes: K read once, the curvature written and
+    read back, 8 bytes of cut table per slot tree."""
+    import torch
+    from kv_cache_compression_probe_gb300 import kvc
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        kvc.kvc_tree_cuts(comp.p, comp.ctx_len, K, comp.rope_cos, comp.rope_sin, bounds,
+                          n_slots, comp.tree_kappa, comp.cuts, stream)
+    call()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / reps
+    esz = 2 if cfg.dtype == "bf16" else 4
+    rows = tokens * cfg.L * cfg.H
+    trees = cfg.B * cfg.L * cfg.H * comp.p.S_max
+    nbytes = rows * (cfg.d * esz + 8) + trees * 8
+    cuts = comp.cuts[..., :7].to(torch.int64)
+    bd = bounds.to(torch.int64)
+    x0 = bd[:, None, None, :-1].expand(-1, cfg.L, cfg.H, -1)
+    y0 = bd[:, None, None, 1:].expand(-1, cfg.L, cfg.H, -1)
+    valid = (torch.arange(comp.p.S_max, device=bd.device)[None, :] < n_slots[:, None].to(torch.int64))
+    root_off = (cuts[..., 0] != (y0 - x0) // 2)[valid[:, None, None, :].expand_as(x0)]
+    return {"ms": ms, "hbm_gbs": nbytes / (ms * 1e-3) / 1e9, "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm,
+            "algorithmic_bytes": nbytes,
+            "root_cut_off_midpoint_frac": float(root_off.float().mean().cpu()),
+            "note": "kvc_tree_cuts (key_curv_kernel + tree_cut_kernel), timed alone; it also "
+                    "runs inside every timed step's scoring call"}
+
+
 def scoring_gemm(comp, K, V, Qp, bounds, n_slots, cfg, tokens, tc_peak, dev):
     """Device time of the probe-times-key contraction passes of one kvc_score
     call (CUDA events the library records between its phases when phase
@@ -398,7 +436,7 @@ def run_gpu(args, cfg, rank, world):
     h_kn = torch.from_numpy(np.stack([x[1] for x in dec])).to(dt).pin_memory()
     h_vn = torch.from_numpy(np.stack([x[2] for x in dec])).to(dt).pin_memory()
     q_all, kn_all, vn_all = h_q.to(dev), h_kn.to(dev), h_vn.to(dev)
-    comp = Compressor(p, [s[0] for s in seqs], device=dev)
+    comp = Compressor(p, [s[0] for s in seqs], device=dev, tree_cuts=args.tree_cuts)
     out = torch.empty((D,) + tuple(q_all.shape[1:]), dtype=dt, device=dev)
     h_out = torch.empty(out.shape, dtype=dt).pin_memory()
     stream = torch.cuda.current_stream(dev)
@@ -521,6 +559,10 @@ def run_gpu(args, cfg, rank, world):
     gemm = None if args.profile else scoring_gemm(comp, K, V, Qp, bounds, n_slots, cfg,
                                                   sum(s[0] for s in seqs), measured_peaks()[1],
                                                   dev)
+    tree = None
+    if args.tree_cuts and not args.profile:
+        tree = tree_cuts_leg(comp, K, bounds, n_slots, cfg, sum(s[0] for s in seqs),
+                             measured_peaks()[0], dev)
     evict = None
     if (args.evict or not args.profile) and not args.no_evict:
         evict = evict_leg(p, cfg, seqs, K, V, q_all, kn_all, vn_all, D, dev, stream)
@@ -568,7 +610,7 @@ def run_gpu(args, cfg, rank, world):
     dec_tc = p.packed_rows > 0 and cfg.dtype == "bf16" and d == 128   # tensor-core decode
     # the committed DRAM capture covers the full 16K workload's launch (256 steps)
     full_16k = (cfg.name == "mistral16k" and not args.layers and D == 256
-                and args.head_full_frac == 0.0)
+                and args.head_full_frac == 0.0 and not args.tree_cuts)
     traffic = kernel_traffic("decode_attn_mistral16k",
                              ["kv_cache_compression_probe_gb300/csrc/kvc_decode.cu",
                               "kv_cache_compression_probe_gb300/csrc/kvc_decode_tc.cu"]) \
@@ -591,7 +633,8 @@ def run_gpu(args, cfg, rank, world):
                    "head_dim": d, "budget": cfg.budget_ratio, "window": cfg.W,
                    "decode_steps": D, "l2": "inputs larger than L2 (K+V %.2f GB)" %
                    (2 * tokens * cfg.L * cfg.H * d * esz / 1e9), "parallelism": f"replicas x{world}",
-                   "head_full_frac": args.head_full_frac},
+                   "head_full_frac": args.head_full_frac,
+                   "trees": "curvature-chosen (kvc_tree_cuts)" if args.tree_cuts else "midpoint"},
         "breakdown_ms": {"score": score_ms, "select": sel_ms, "merge_pack": pack_ms,
                          "decode_per_step": dec_ms, "decode_total": dec_ms * D},
         "compress_tokens_per_s": tokens / ((score_ms + sel_ms + pack_ms) * 1e-3),
@@ -622,6 +665,7 @@ def run_gpu(args, cfg, rank, world):
                                  "(Compressor.compress_from_host)" if pipelined
                                  else "whole inputs, then the step")},
         "evict_per_step_next_f2": evict,
+        "tree_cuts_next_f3": tree,
         "gpu_launches": launches,
         "gpu_launches_detail": {"issued_by_host": host_launches,
                                 "in_graph_replays": graph_launches,
@@ -800,6 +844,8 @@ def main():
                     help="override the layer count (small profiling cases)")
     ap.add_argument("--head-full-frac", type=float, default=0.0,
                     help="head-level hybrid: fraction of heads that keep the full cache")
+    ap.add_argument("--tree-cuts", action="store_true",
+                    help="curvature-chosen prototype trees (kvc_tree_cuts) instead of midpoint trees")
     ap.add_argument("--evict", action="store_true",
                     help="time the per-step top-B eviction (DistillCache) leg also under --profile")
     ap.add_argument("--no-evict", action="store_true",

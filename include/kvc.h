@@ -104,6 +104,19 @@ typedef struct kvc_params {
   double  head_full_frac;  /* [DC] App. E.3 head-level hybrid: the
                               floor(frac*L*H) heads with the largest relevance
                               mass outside the window keep every token; 0 = off */
+  const uint8_t* tree_cuts;/* [GK] "Technical details": curvature-chosen trees.
+                              Device array [B, L, H, S_max, 8] (row (b*L + l)*H
+                              + h, slot s): byte j < 7 is the cut of internal
+                              node j (breadth-first; node j covers [a, b) and
+                              its children [a, t), [t, b)) as an offset t - x0
+                              from the slot start x0; byte 7 is unused.  Usually
+                              written by kvc_tree_cuts.  kvc_score,
+                              kvc_select and kvc_merge_pack read it; a cut that
+                              leaves a child fewer than 2 or more than 16
+                              tokens per leaf below it is replaced by the
+                              midpoint (and kvc_score records KVC_EDEVICE).  NULL = the depth-3 midpoint trees.
+                              The three calls of one compression must see the
+                              same table.                                        */
 } kvc_params;
 
 /* Human-readable name of a status code (static string). */
@@ -133,7 +146,7 @@ size_t kvc_workspace_bytes(int which, const kvc_params* p /* host */);
  * Entry e is position e/2, so half-integer representative positions
  * ([GK] "Inside one cache entry": rerotate at the span's mean position) index
  * it exactly.  Angles are formed and evaluated in double precision on the
- * device.  n_half must be >= 2*n_max. */
+ * device.  n_half must be >= 2*n_max.  kvc_tree_cuts reads them too. */
 int kvc_rope_table(int32_t d, float base, int64_t n_half, float* cos_tab, float* sin_tab,
                    void* stream);
 
@@ -340,6 +353,31 @@ int kvc_decode_attn_noalloc(const kvc_params* p, const void* q, const void* k_ne
 int kvc_partition(const kvc_params* p, const int32_t* ctx_len, const void* hidden, int32_t dh,
                   float* kappa, int32_t* slot_bounds, int32_t* n_slots, void* workspace,
                   size_t ws_bytes, void* stream);
+
+/* f3: curvature-chosen prototype trees ([GK] "Technical details and default
+ * settings": tree construction considers high-curvature split candidates plus
+ * the midpoint; the curvature of "01 Curvature-guided partition").  Per
+ * (b,l,h), the keys with RoPE removed and normalised, u_i = R(-i)k_i/|.|, give
+ *   kappa(t) = mean over w in {1,2,4,8} with w <= t < n_b - w of
+ *              1 - cos(u_t - u_{t-w}, u_{t+w} - u_t)   (cos = 1 for a zero chord),
+ * written to kappa (token layout, like kvc_score's features: rows
+ * (l*H + h)*n_b + i of sequence b's block).  Then, per slot tree, top-down,
+ * internal node j = [a, b) of depth k (c tokens, m = floor((a+b)/2)) is cut
+ * at the t maximising kappa(t) - lambda*((t - m)/(c/2))^2 with lambda the mean
+ * of kappa over [a, b) (summed in index order), among the t that leave each
+ * child 2 .. 16 tokens per leaf below it (2^(2-k) leaves; the midpoint always
+ * qualifies); ties go to the midpoint, then to the
+ * smaller t.  Every step of that decision is an individually rounded fp32
+ * operation in the order written.  cuts: [B, L, H, S_max, 8] bytes, the
+ * table kvc_params.tree_cuts takes (byte j < 7 = cut of node j minus the slot
+ * start; byte 7 = 0; all 8 bytes 0 for padding slots s >= n_slots[b]).
+ * K is the token layout of kvc_score; rope_cos / rope_sin as for kvc_score
+ * (n_half >= 2*n_max).  No workspace.  Slot bounds outside 16..128 tokens or
+ * beyond n_b - W leave that slot's bytes unwritten and record KVC_EDEVICE.
+ * Non-finite keys give unspecified (but valid) cuts. */
+int kvc_tree_cuts(const kvc_params* p, const int32_t* ctx_len, const void* K,
+                  const float* rope_cos, const float* rope_sin, const int32_t* slot_bounds,
+                  const int32_t* n_slots, float* kappa, uint8_t* cuts, void* stream);
 
 #ifdef __cplusplus
 }

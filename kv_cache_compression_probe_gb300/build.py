@@ -14,7 +14,7 @@ LIB = os.path.join(HERE, "libkvc.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 SOURCES = ["kvc_api.cu", "kvc_decode.cu", "kvc_select.cu", "kvc_pack.cu", "kvc_score.cu",
-           "kvc_score_tc.cu", "kvc_partition.cu", "kvc_decode_tc.cu", "kvc_evict.cu"]
+           "kvc_score_tc.cu", "kvc_partition.cu", "kvc_decode_tc.cu", "kvc_evict.cu", "kvc_tree.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,

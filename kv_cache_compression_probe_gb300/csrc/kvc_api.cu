@@ -1,6 +1,7 @@
 // Host plumbing of libkvc: status strings, the device error word, the launch
 // counter, parameter checks, workspace sizing and the RoPE table.
 #include <atomic>
+#include <cstddef>
 #include <cmath>
 #include <mutex>
 
@@ -8,7 +9,8 @@
 #include "kvc_internal.h"
 
 #include <cstddef>
-static_assert(sizeof(kvc_params) == 128, "kvc_params layout");
+static_assert(sizeof(kvc_params) == 136, "kvc_params layout");
+static_assert(offsetof(kvc_params, tree_cuts) == 128, "kvc_params layout");
 static_assert(offsetof(kvc_params, head_full_frac) == 120, "kvc_params layout");
 static_assert(offsetof(kvc_params, packed_rows) == 112, "kvc_params layout");
 static_assert(offsetof(kvc_params, total_ctx) == 104, "kvc_params layout");

@@ -177,6 +177,48 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// ---------------------------------------------------------------- prototype trees
+// The tree of a slot [x0, y0): 15 nodes in breadth-first order, node j's
+// children 2j+1 and 2j+2, nodes 7..14 the leaf prototypes.  Internal node j of
+// depth k covering [a, b) is cut at x0 + cuts[j] when a cut table is given and
+// that cut is valid (each child keeps 2..16 tokens per leaf below it, 2^(2-k)
+// leaves), otherwise at the midpoint floor((a + b) / 2), which is valid for
+// every node of a slot of 16..128 tokens.  Every kernel derives its nodes
+// through these helpers, so they all see one tree.
+__device__ __forceinline__ bool tree_cut_valid(int t, int depth, int a, int b) {
+  const int lo = 8 >> depth, hi = 64 >> depth;
+  return t - a >= lo && t - a <= hi && b - t >= lo && b - t <= hi;
+}
+__device__ __forceinline__ int tree_cut(const uint8_t* cuts, int j, int depth, int x0, int a,
+                                        int b) {
+  if (cuts) {
+    const int t = x0 + (int)cuts[j];
+    if (tree_cut_valid(t, depth, a, b)) return t;
+  }
+  return (a + b) >> 1;
+}
+__device__ __forceinline__ int tree_depth(int j) {
+  return (j >= 7) ? 3 : (j >= 3) ? 2 : (j >= 1) ? 1 : 0;
+}
+// Token range [a, b) of node j.
+__device__ __forceinline__ void tree_node_range(const uint8_t* cuts, int j, int x0, int y0,
+                                                int& a, int& b) {
+  const int depth = tree_depth(j);
+  const int k = j - ((1 << depth) - 1);
+  a = x0; b = y0;
+  int node = 0;
+  for (int lvl = depth - 1; lvl >= 0; --lvl) {
+    const int t = tree_cut(cuts, node, depth - 1 - lvl, x0, a, b);
+    if ((k >> lvl) & 1) { a = t; node = 2 * node + 2; } else { b = t; node = 2 * node + 1; }
+  }
+}
+// Cut table of slot s of (b,l,h) blh (8 bytes per slot, cuts of nodes 0..6 as
+// offsets from the slot start), or null for midpoint trees.
+__device__ __forceinline__ const uint8_t* tree_cuts_of(const kvc_params& p, long long blh,
+                                                       int s) {
+  return p.tree_cuts ? p.tree_cuts + ((long long)blh * p.S_max + s) * 8 : nullptr;
+}
+
 }  // namespace kvcd
 
 // ---------------------------------------------------------------- async copy / mbarrier

@@ -22,29 +22,30 @@
 #include "kvc_common.cuh"
 #include "kvc_internal.h"
 
+#ifndef KVC_PACK_WARPS
+#define KVC_PACK_WARPS 4
+#endif
+
 namespace {
 
 constexpr int kOps = 16;
+constexpr int kPackWarps = KVC_PACK_WARPS;   // slot trees (warps) per block
 
-__device__ __forceinline__ void node_range(int j, int x0, int y0, int& a, int& b) {
-  const int depth = (j >= 7) ? 3 : (j >= 3) ? 2 : (j >= 1) ? 1 : 0;
-  const int k = j - ((1 << depth) - 1);
-  a = x0; b = y0;
-  for (int lvl = depth - 1; lvl >= 0; --lvl) {
-    const int mid = (a + b) >> 1;
-    if ((k >> lvl) & 1) a = mid; else b = mid;
-  }
+__device__ __forceinline__ void node_range(const uint8_t* cuts, int j, int x0, int y0, int& a,
+                                           int& b) {
+  kvcd::tree_node_range(cuts, j, x0, y0, a, b);
 }
 
 // Stored entries of one slot tree: sum over taken ops of their cost
 // (Add 1, internal Split 1, leaf Split = leaf size - 1).
-__device__ __forceinline__ int tree_entries(const uint8_t* tk, int x0, int y0) {
+__device__ __forceinline__ int tree_entries(const uint8_t* cuts, const uint8_t* tk, int x0,
+                                            int y0) {
   int n = 0;
   for (int o = 0; o < 8; ++o) n += tk[o] ? 1 : 0;
   for (int j = 7; j < 15; ++j)
     if (tk[1 + j]) {
       int a, b;
-      node_range(j, x0, y0, a, b);
+      node_range(cuts, j, x0, y0, a, b);
       n += (b - a) - 1;
     }
   return n;
@@ -91,7 +92,8 @@ __global__ void pack_count_kernel(kvc_params p, PackArgs a) {
       if (s < S) {
         const int x0 = bd[s], y0 = bd[s + 1];
         if (x0 < 0 || y0 - x0 < 16 || y0 - x0 > 128 || y0 > n - p.W) ok = false;
-        else cnt = tree_entries(a.taken + (blh * p.S_max + s) * kOps, x0, y0);
+        else cnt = tree_entries(kvcd::tree_cuts_of(p, blh, s), a.taken + (blh * p.S_max + s) * kOps,
+                                x0, y0);
       }
       int incl = cnt;
 #pragma unroll
@@ -274,7 +276,8 @@ __device__ __forceinline__ void copy_exact(const PackArgs& a, const T* Kh, const
 // One warp per slot tree (plus one extra "slot" index S per (b,l,h) for the
 // window tokens).
 template <typename T, int D>
-__global__ void __launch_bounds__(128, 8) pack_tree_kernel(kvc_params p, PackArgs a) {
+__global__ void __launch_bounds__(32 * kPackWarps, 32 / kPackWarps)
+    pack_tree_kernel(kvc_params p, PackArgs a) {
   const int warps = blockDim.x >> 5;
   const long long item = (long long)blockIdx.x * warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -301,6 +304,7 @@ __global__ void __launch_bounds__(128, 8) pack_tree_kernel(kvc_params p, PackArg
   const int x0 = bd[s], y0 = bd[s + 1];
   const uint8_t* tk = a.taken + (blh * p.S_max + s) * kOps;
   if (!tk[0]) return;
+  const uint8_t* cuts = kvcd::tree_cuts_of(p, blh, s);
   int64_t dst = base + a.slot_base[blh * p.S_max + s];
   // left-to-right frontier walk with an explicit stack (depth <= 4)
   int stack[8];
@@ -309,7 +313,7 @@ __global__ void __launch_bounds__(128, 8) pack_tree_kernel(kvc_params p, PackArg
   while (sp > 0) {
     const int j = stack[--sp];
     int x, y;
-    node_range(j, x0, y0, x, y);
+    node_range(cuts, j, x0, y0, x, y);
     if (!tk[1 + j]) {
       write_prototype<T, D>(p, a, Kh, Vh, rh, x, y, dst, lane);
       ++dst;
@@ -371,13 +375,14 @@ extern "C" int kvc_merge_pack(const kvc_params* p, const int32_t* ctx_len, const
   // one warp per slot tree (+ one per window); 4-warp blocks so a long slot
   // holds few idle neighbours
   const long long items = blh * (p->S_max + 1);
-  const unsigned grid = (unsigned)((items + 3) / 4);
+  const unsigned grid = (unsigned)((items + kPackWarps - 1) / kPackWarps);
+  const unsigned threads = 32 * kPackWarps;
   if (p->dtype == KVC_BF16) {
-    if (p->d == 128) pack_tree_kernel<__nv_bfloat16, 128><<<grid, 128, 0, s>>>(*p, a);
-    else pack_tree_kernel<__nv_bfloat16, 64><<<grid, 128, 0, s>>>(*p, a);
+    if (p->d == 128) pack_tree_kernel<__nv_bfloat16, 128><<<grid, threads, 0, s>>>(*p, a);
+    else pack_tree_kernel<__nv_bfloat16, 64><<<grid, threads, 0, s>>>(*p, a);
   } else {
-    if (p->d == 128) pack_tree_kernel<float, 128><<<grid, 128, 0, s>>>(*p, a);
-    else pack_tree_kernel<float, 64><<<grid, 128, 0, s>>>(*p, a);
+    if (p->d == 128) pack_tree_kernel<float, 128><<<grid, threads, 0, s>>>(*p, a);
+    else pack_tree_kernel<float, 64><<<grid, threads, 0, s>>>(*p, a);
   }
   kvc::count_launch(2);
   return kvc::cuda_status(cudaGetLastError());

@@ -505,14 +505,11 @@ __global__ void __launch_bounds__(256, 1) prop_kernel(kvc_params p, ScoreArgs a)
 }
 
 // ---------------------------------------------------------------- nodes (a3 + a4)
-__device__ __forceinline__ void node_range(int j, int x0, int y0, int& x, int& y) {
-  const int depth = (j >= 7) ? 3 : (j >= 3) ? 2 : (j >= 1) ? 1 : 0;
-  const int k = j - ((1 << depth) - 1);
-  x = x0; y = y0;
-  for (int lvl = depth - 1; lvl >= 0; --lvl) {
-    const int mid = (x + y) >> 1;
-    if ((k >> lvl) & 1) x = mid; else y = mid;
-  }
+// Token range [x, y) of node j of the slot [x0, y0) (cut table `cuts`, or the
+// midpoint tree when null).
+__device__ __forceinline__ void node_range(const uint8_t* cuts, int j, int x0, int y0, int& x,
+                                           int& y) {
+  kvcd::tree_node_range(cuts, j, x0, y0, x, y);
 }
 
 template <int D>
@@ -577,6 +574,7 @@ __global__ void __launch_bounds__(256, 1) nodes_kernel(kvc_params p, ScoreArgs a
   const int n = a.ctx_len[b];
   const int x0 = a.bounds[(long long)b * (p.S_max + 1) + s];
   const int y0 = a.bounds[(long long)b * (p.S_max + 1) + s + 1];
+  const uint8_t* cuts = kvcd::tree_cuts_of(p, blh, s);
   const int len = y0 - x0;
   const int R = p.G * p.P;
   const int64_t row0 = kvcd::seq_token_base(a.ctx_len, b, p.L * p.H) + (int64_t)lh * n;
@@ -590,7 +588,7 @@ __global__ void __launch_bounds__(256, 1) nodes_kernel(kvc_params p, ScoreArgs a
   constexpr int VP = D / 64;
   for (int j = warp; j < 15; j += 8) {
     int x, y;
-    node_range(j, x0, y0, x, y);
+    node_range(cuts, j, x0, y0, x, y);
     const int c = y - x;
     float rs = 0.f;
     for (int i = x + lane; i < y; i += 32) rs += sm.r[i - x0];
@@ -691,7 +689,7 @@ __global__ void __launch_bounds__(256, 1) nodes_kernel(kvc_params p, ScoreArgs a
         for (int t = 0; t < VPL; ++t) Ud2[r][t] = Ud1[r][t] = Ur[r][t] = 0.f;
       for (int j = 7; j < 15; ++j) {
         int x, y;
-        node_range(j, x0, y0, x, y);
+        node_range(cuts, j, x0, y0, x, y);
         float Al[4] = {0, 0, 0, 0};
         float Ul[4][VPL];
 #pragma unroll
@@ -779,7 +777,7 @@ __global__ void __launch_bounds__(256, 1) nodes_kernel(kvc_params p, ScoreArgs a
         c = 1;
       } else {
         int x, y;
-        node_range(j, x0, y0, x, y);
+        node_range(cuts, j, x0, y0, x, y);
         c = y - x - 1;
         g = gainf(Dn[j], Dd[j]);
       }
@@ -923,6 +921,7 @@ __global__ void __launch_bounds__(128, 5) proto_kernel(kvc_params p, ScoreArgs a
   const int n = a.ctx_len[b];
   const int x0 = a.bounds[(long long)b * (p.S_max + 1) + s];
   const int y0 = a.bounds[(long long)b * (p.S_max + 1) + s + 1];
+  const uint8_t* cuts = kvcd::tree_cuts_of(p, blh, s);
   const int64_t row0 = kvcd::seq_token_base(a.ctx_len, b, p.L * p.H) + (int64_t)lh * n;
   const uint32_t* Kw = reinterpret_cast<const uint32_t*>(static_cast<const T*>(a.K) + row0 * D);
   const uint32_t* Vw = reinterpret_cast<const uint32_t*>(static_cast<const T*>(a.V) + row0 * D);
@@ -932,7 +931,7 @@ __global__ void __launch_bounds__(128, 5) proto_kernel(kvc_params p, ScoreArgs a
   float nv_sum = 0.f;                                    // sum of |v| over the slot's tokens
   for (int L = 0; L < 8; ++L) {
     int x, y;
-    node_range(7 + L, x0, y0, x, y);
+    node_range(cuts, 7 + L, x0, y0, x, y);
     ProtoAcc leaf;
     leaf.zero();
     // tokens in groups of 4: all loads of a group first, then four interleaved
@@ -1003,13 +1002,13 @@ __global__ void __launch_bounds__(128, 5) proto_kernel(kvc_params p, ScoreArgs a
     acc_to_smem(lv, 0, leaf, lane, (L & 1) != 0);           // depth 2 = leaf pair
     if (L & 1) {
       const int j2 = 3 + (L >> 1);
-      node_range(j2, x0, y0, x, y);
+      node_range(cuts, j2, x0, y0, x, y);
       const ProtoAcc d2 = acc_from_smem(lv, 0, lane);
       proto_finish(a, p.value_floor, j2, x, y, d2, out, lane);
       acc_to_smem(lv, 1, d2, lane, (L & 3) == 3);            // depth 1 = depth-2 pair
       if ((L & 3) == 3) {
         const int j1 = 1 + (L >> 2);
-        node_range(j1, x0, y0, x, y);
+        node_range(cuts, j1, x0, y0, x, y);
         const ProtoAcc d1 = acc_from_smem(lv, 1, lane);
         proto_finish(a, p.value_floor, j1, x, y, d1, out, lane);
         acc_to_smem(lv, 2, d1, lane, L == 7);                // root = depth-1 pair
@@ -1051,6 +1050,7 @@ __global__ void ops_kernel(kvc_params p, ScoreArgs a, const unsigned char* proto
   }
   const int x0 = a.bounds[(long long)b * (p.S_max + 1) + s];
   const int y0 = a.bounds[(long long)b * (p.S_max + 1) + s + 1];
+  const uint8_t* cuts = kvcd::tree_cuts_of(p, blh, s);
   const float* rv = reinterpret_cast<const float*>(proto + tree * kvc::kProtoBytes + kvc::kProtoRvOff);
   const float nu = a.nu[blh];
   const float invR = 1.f / (float)(p.G * p.P);
@@ -1079,7 +1079,7 @@ __global__ void ops_kernel(kvc_params p, ScoreArgs a, const unsigned char* proto
       c = 1;
     } else {
       int x, y;
-      node_range(j, x0, y0, x, y);
+      node_range(cuts, j, x0, y0, x, y);
       c = y - x - 1;
       g = gainf(Dn[j], Dd[j]);
     }
@@ -1102,6 +1102,19 @@ __global__ void score_check_kernel(kvc_params p, ScoreArgs a) {
     for (int s = 0; ok && s < S; ++s) {
       const int ln = bd[s + 1] - bd[s];
       ok = ln >= 16 && ln <= 128;
+    }
+    // a cut table entry that the tree helpers would replace by the midpoint
+    // is reported (the replacement keeps every kernel on one valid tree)
+    for (int s = 0; ok && p.tree_cuts && s < S; ++s) {
+      const uint8_t* cuts = kvcd::tree_cuts_of(p, blh, s);
+      for (int j = 0; j < 7; ++j) {
+        int x, y;
+        kvcd::tree_node_range(cuts, j, bd[s], bd[s + 1], x, y);
+        if (!kvcd::tree_cut_valid(bd[s] + (int)cuts[j], kvcd::tree_depth(j), x, y)) {
+          kvcd::record_error(a.err, KVC_EDEVICE);
+          break;
+        }
+      }
     }
   }
   a.ok[blh] = ok ? 1 : 0;
@@ -1239,6 +1252,7 @@ int launch_all(const kvc_params* p, ScoreArgs& a, cudaStream_t s) {
     kvc::NodeTcArgs nd;
     nd.ctx_len = a.ctx_len; nd.K = a.K; nd.V = a.V; nd.Qp = a.Qp; nd.lse2 = a.lse2; nd.ok = a.ok;
     nd.bounds = a.bounds; nd.n_slots = a.n_slots; nd.proto = a.proto; nd.npart = a.npart;
+    nd.tree_cuts = p->tree_cuts;
     nd.err = a.err; nd.B = p->B; nd.L = p->L; nd.H = p->H; nd.G = p->G; nd.P = p->P;
     nd.S_max = p->S_max; nd.q_scale2 = a.q_scale2;
     if ((st = kvc::nodes_tc_pass(nd, rows_total, s)) != KVC_OK) return st;

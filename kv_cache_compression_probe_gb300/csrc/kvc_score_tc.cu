@@ -801,14 +801,12 @@ __device__ __forceinline__ void tld8(uint32_t taddr, float (&v)[8]) {
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Leaf l of the slot [x0, y0): first token and token count (midpoint rule).
-__device__ __forceinline__ void leaf_range(int l, int x0, int y0, int& start, int& cnt) {
-  int a = x0, b = y0;
-#pragma unroll
-  for (int lvl = 2; lvl >= 0; --lvl) {
-    const int mid = (a + b) >> 1;
-    if ((l >> lvl) & 1) a = mid; else b = mid;
-  }
+// Leaf l of the slot [x0, y0): first token and token count (at most 16) of
+// node 7 + l of the tree with cut table `cuts` (null: midpoint tree).
+__device__ __forceinline__ void leaf_range(const uint8_t* cuts, int l, int x0, int y0, int& start,
+                                           int& cnt) {
+  int a, b;
+  kvcd::tree_node_range(cuts, 7 + l, x0, y0, a, b);
   start = a; cnt = b - a;
 }
 
@@ -889,6 +887,7 @@ __global__ void __maxnreg__(kNodeMaxRegs)
         const int s = s_begin + k;
         const long long tree = blh * a.S_max + s;
         const int x0 = bd[s], y0 = bd[s + 1];
+        const uint8_t* cuts = a.tree_cuts ? a.tree_cuts + tree * 8 : nullptr;
         // Kt / Kh are free once phase A of the previous slot completed and its
         // epilogue read ln m from Kh (a_ready)
         if (k >= 1 && (!kvcd::mbar_wait(&sm.k_empty, (uint32_t)((k - 1) & 1)) ||
@@ -900,7 +899,7 @@ __global__ void __maxnreg__(kNodeMaxRegs)
         kvcd::mbar_arrive_expect_tx(&sm.k_full, kTileBytes + kvc::kProtoHeadBytes);
         for (int l = 0; l < 8; ++l) {
           int st, cnt;
-          leaf_range(l, x0, y0, st, cnt);
+          leaf_range(cuts, l, x0, y0, st, cnt);
           for (int fb = 0; fb < 2; ++fb)
             tma_load_2d(&sm.Kt[fb][l * 2048], &kmap16, fb * 64, (int)(row0 + st), &sm.k_full);
         }
@@ -910,7 +909,7 @@ __global__ void __maxnreg__(kNodeMaxRegs)
         kvcd::mbar_arrive_expect_tx(&sm.v_full, kTileBytes);
         for (int l = 0; l < 8; ++l) {
           int st, cnt;
-          leaf_range(l, x0, y0, st, cnt);
+          leaf_range(cuts, l, x0, y0, st, cnt);
           for (int fb = 0; fb < 2; ++fb)
             tma_load_2d(&sm.Vt[fb][l * 2048], &vmap16, fb * 64, (int)(row0 + st), &sm.v_full);
         }
@@ -986,6 +985,7 @@ __global__ void __maxnreg__(kNodeMaxRegs)
       const int s = s_begin + k;
       const long long tree = blh * a.S_max + s;
       const int x0 = bd[s], y0 = bd[s + 1];
+      const uint8_t* cuts = a.tree_cuts ? a.tree_cuts + tree * 8 : nullptr;
       // ---- epilogue A: attention of this row to the slot's nodes and its key quarter
       if (!*abort_flag && !kvcd::mbar_wait(&sm.s_full, (uint32_t)(k & 1))) *abort_flag = 1;
       tc_fence_after();
@@ -1006,8 +1006,8 @@ __global__ void __maxnreg__(kNodeMaxRegs)
       int cnt0, cnt1;
       {
         int st;
-        leaf_range(2 * g, x0, y0, st, cnt0);
-        leaf_range(2 * g + 1, x0, y0, st, cnt1);
+        leaf_range(cuts, 2 * g, x0, y0, st, cnt0);
+        leaf_range(cuts, 2 * g + 1, x0, y0, st, cnt1);
       }
       if (k >= 1 && !*abort_flag && !kvcd::mbar_wait(&sm.b_done, (uint32_t)((k - 1) & 1)))
         *abort_flag = 1;

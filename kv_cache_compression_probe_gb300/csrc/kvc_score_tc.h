@@ -55,6 +55,7 @@ struct NodeTcArgs {
   const int32_t* n_slots;
   const unsigned char* proto;   // [BLH * S_max] records of kProtoBytes
   float* npart;           // [BLH * S_max, 2 tiles, 15 nodes, 4 sums]
+  const uint8_t* tree_cuts;     // [BLH * S_max, 8] cut table, or null (midpoint trees)
   int32_t* err;
   int B, L, H, G, P, S_max;
   float q_scale2;

@@ -70,29 +70,24 @@ __device__ __forceinline__ int op_parent(int o) {
   return j == 0 ? 0 : 1 + (j - 1) / 2;
 }
 
-// Depth-1, depth-2 and leaf node of token i in slot [x0, y0) (midpoint rule).
-__device__ __forceinline__ void token_path(int i, int x0, int y0, int& d1, int& d2, int& leaf) {
+// Depth-1, depth-2 and leaf node of token i in slot [x0, y0) (tree with cut
+// table `cuts`, or the midpoint tree when null).
+__device__ __forceinline__ void token_path(const uint8_t* cuts, int i, int x0, int y0, int& d1,
+                                           int& d2, int& leaf) {
   int a = x0, b = y0, j = 0;
   int path[3];
 #pragma unroll
   for (int lvl = 0; lvl < 3; ++lvl) {
-    const int mid = (a + b) >> 1;
-    if (i < mid) { j = 2 * j + 1; b = mid; } else { j = 2 * j + 2; a = mid; }
+    const int t = kvcd::tree_cut(cuts, j, lvl, x0, a, b);
+    if (i < t) { j = 2 * j + 1; b = t; } else { j = 2 * j + 2; a = t; }
     path[lvl] = j;
   }
   d1 = path[0]; d2 = path[1]; leaf = path[2];
 }
 
-__device__ __forceinline__ void node_range(int j, int x0, int y0, int& a, int& b) {
-  // walk down from the root following the bits of j's position
-  int depth = (j >= 7) ? 3 : (j >= 3) ? 2 : (j >= 1) ? 1 : 0;
-  int first = (1 << depth) - 1;
-  int k = j - first;
-  a = x0; b = y0;
-  for (int lvl = depth - 1; lvl >= 0; --lvl) {
-    const int mid = (a + b) >> 1;
-    if ((k >> lvl) & 1) a = mid; else b = mid;
-  }
+__device__ __forceinline__ void node_range(const uint8_t* cuts, int j, int x0, int y0, int& a,
+                                           int& b) {
+  kvcd::tree_node_range(cuts, j, x0, y0, a, b);
 }
 
 __device__ __forceinline__ unsigned long long floor_key(float r, float sens, uint32_t cidx) {
@@ -172,6 +167,7 @@ __global__ void floor_weights_kernel(kvc_params p, const int32_t* ctx_len,
   const int n = ctx_len[b];
   const int x0 = slot_bounds[(long long)b * (p.S_max + 1) + s];
   const int y0 = slot_bounds[(long long)b * (p.S_max + 1) + s + 1];
+  const uint8_t* cuts = kvcd::tree_cuts_of(p, blh, s);
   if (x0 < 0 || y0 - x0 < 16 || y0 - x0 > 128 || y0 > n - p.W) {
     if (lane == 0) kvcd::record_error(err, KVC_EDEVICE);
     return;
@@ -190,7 +186,7 @@ __global__ void floor_weights_kernel(kvc_params p, const int32_t* ctx_len,
   __syncwarp();
   if (lane < 15) {
     int a, bb;
-    node_range(lane, x0, y0, a, bb);
+    node_range(cuts, lane, x0, y0, a, bb);
     unsigned long long m = 0;
     for (int i = a; i < bb; ++i) m = max(m, s_key[w][i - x0]);
     s_gmax[w][lane] = m;
@@ -202,7 +198,7 @@ __global__ void floor_weights_kernel(kvc_params p, const int32_t* ctx_len,
     int c = 0;
     if (k != 0) {
       int d1, d2, leaf;
-      token_path(i, x0, y0, d1, d2, leaf);
+      token_path(cuts, i, x0, y0, d1, d2, leaf);
       if (k == s_gmax[w][leaf]) {
         c = cost[1 + leaf];
         if (k == s_gmax[w][d2]) c += cost[1 + d2];
@@ -397,6 +393,7 @@ __global__ void floor_mark_kernel(kvc_params p, const int32_t* ctx_len,
   const int n = ctx_len[b];
   const int x0 = slot_bounds[(long long)b * (p.S_max + 1) + s];
   const int y0 = slot_bounds[(long long)b * (p.S_max + 1) + s + 1];
+  const uint8_t* cuts = kvcd::tree_cuts_of(p, blh, s);
   if (x0 < 0 || y0 - x0 < 16 || y0 - x0 > 128 || y0 > n - p.W) return;
   const RadixState r0 = ws.rs[0 * p.B + b];
   const RadixState r1 = ws.rs[1 * p.B + b];
@@ -414,7 +411,7 @@ __global__ void floor_mark_kernel(kvc_params p, const int32_t* ctx_len,
     const unsigned long long k = floor_key(relevance[row0 + i], sens, (uint32_t)((long long)lh * n + i));
     if (k <= stop) continue;
     int d1, d2, leaf;
-    token_path(i, x0, y0, d1, d2, leaf);
+    token_path(cuts, i, x0, y0, d1, d2, leaf);
     tk[0] = 1; tk[1] = 1; tk[1 + d1] = 1; tk[1 + d2] = 1; tk[1 + leaf] = 1;
     spent += (unsigned long long)c;
     toks += 1;

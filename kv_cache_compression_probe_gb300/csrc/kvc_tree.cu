@@ -1,0 +1,235 @@
+// Curvature-chosen prototype trees (GraceKV "Technical details and default
+// settings": tree construction considers high-curvature split candidates plus
+// the midpoint; the curvature measure of "01 Curvature-guided partition").
+//
+// Per (b, l, h) the keys with RoPE removed, u_i = R(-i) k_i / |R(-i) k_i|, form a
+// trajectory; its multi-scale curvature is
+//   kappa(t) = mean over w in {1, 2, 4, 8} with w <= t < n - w of
+//              1 - cos(u_t - u_{t-w}, u_{t+w} - u_t)     (cos = 1 for a zero chord).
+// Every internal node [a, b) of a slot tree (depth k, c tokens, midpoint
+// m = floor((a+b)/2)) is cut, top-down, at the valid t maximising
+//   kappa(t) - lam * ((t - m) / (c / 2))^2,   lam = mean kappa over [a, b),
+// ties to the midpoint, then to the smaller t.  Valid: both children keep
+// 2..16 tokens per leaf below them (2^(2-k) leaves), the range of the midpoint
+// trees' leaves, so every leaf split stores at least 2 tokens.
+//
+// Kernel 1 (key_curv_kernel): one CTA per (b,l,h) and 64 positions; the unit
+// rows of positions [t0 - 8, t0 + 72) are staged in shared memory (one warp per
+// row: unrotate with the half-position table row 2i, one warp reduction for the
+// norm), then one warp per position forms the 4 scales' chords with lanes
+// owning 4 features each; the 12 dot products are reduced 4 at a time.
+// Kernel 2 (tree_cut_kernel): one warp per slot tree; the node mean is summed
+// in index order by every lane (the same fp32 sum the cut decision is checked
+// against), candidates are scored 32 at a time with explicitly rounded fp32
+// operations (no contraction) and the warp keeps the first maximum.
+#include "kvc_common.cuh"
+#include "kvc_internal.h"
+
+namespace {
+
+constexpr int kCurvTile = 64;                 // positions per CTA
+constexpr int kCurvHalo = 8;                  // largest scale
+constexpr int kCurvRows = kCurvTile + 2 * kCurvHalo;
+
+struct TreeArgs {
+  const int32_t* ctx_len;
+  const void* K;
+  const float* cos_tab;
+  const float* sin_tab;
+  const int32_t* bounds;
+  const int32_t* n_slots;
+  float* kappa;
+  uint8_t* cuts;
+  int32_t* err;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) key_curv_kernel(kvc_params p, TreeArgs a) {
+  constexpr int VP = D / 64;                   // RoPE pairs per lane
+  constexpr int HALF = D / 2;
+  __shared__ float urow[kCurvRows][D];
+  const long long blh = blockIdx.y;
+  const int lh = (int)(blh % ((long long)p.L * p.H));
+  const int b = (int)(blh / ((long long)p.L * p.H));
+  const int n = a.ctx_len[b];
+  const int t0 = blockIdx.x * kCurvTile;
+  if (n < 1 || n > p.n_max) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) kvcd::record_error(a.err, KVC_EDEVICE);
+    return;
+  }
+  if (t0 >= n) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t row0 = kvcd::seq_token_base(a.ctx_len, b, p.L * p.H) + (int64_t)lh * n;
+  const T* Kh = static_cast<const T*>(a.K) + row0 * D;
+  // unit rows u_i of positions t0 - 8 .. t0 + 71 (zero outside [0, n))
+  for (int r = warp; r < kCurvRows; r += 8) {
+    const int i = t0 - kCurvHalo + r;
+    float lo[VP], hi[VP];
+    float n2 = 0.f;
+    if (i >= 0 && i < n) {
+      const float* ct = a.cos_tab + (int64_t)(2 * i) * HALF + lane * VP;
+      const float* st = a.sin_tab + (int64_t)(2 * i) * HALF + lane * VP;
+#pragma unroll
+      for (int t = 0; t < VP; ++t) {
+        const float k0 = kvcd::to_f(Kh[(int64_t)i * D + lane * VP + t]);
+        const float k1 = kvcd::to_f(Kh[(int64_t)i * D + HALF + lane * VP + t]);
+        const float cs = __ldg(ct + t), sn = __ldg(st + t);
+        lo[t] = k0 * cs + k1 * sn;                       // R(-i)
+        hi[t] = k1 * cs - k0 * sn;
+        n2 += lo[t] * lo[t] + hi[t] * hi[t];
+      }
+    } else {
+#pragma unroll
+      for (int t = 0; t < VP; ++t) lo[t] = hi[t] = 0.f;
+    }
+    n2 = kvcd::warp_sum(n2);
+    const float inv = n2 > 0.f ? 1.f / sqrtf(n2) : 0.f;
+#pragma unroll
+    for (int t = 0; t < VP; ++t) {
+      urow[r][lane * VP + t] = lo[t] * inv;
+      urow[r][HALF + lane * VP + t] = hi[t] * inv;
+    }
+  }
+  __syncthreads();
+  constexpr int FL = D / 32;                   // features per lane in the chord sums
+  for (int q = warp; q < kCurvTile; q += 8) {
+    const int t = t0 + q;
+    if (t >= n) break;
+    const int rc = q + kCurvHalo;
+    float uc[FL];
+#pragma unroll
+    for (int f = 0; f < FL; ++f) uc[f] = urow[rc][lane + 32 * f];
+    float dot[4], na2[4], nb2[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int w = 1 << s;
+      dot[s] = na2[s] = nb2[s] = 0.f;
+      if (t >= w && t < n - w) {
+#pragma unroll
+        for (int f = 0; f < FL; ++f) {
+          const float ca = uc[f] - urow[rc - w][lane + 32 * f];
+          const float cb = urow[rc + w][lane + 32 * f] - uc[f];
+          dot[s] = fmaf(ca, cb, dot[s]);
+          na2[s] = fmaf(ca, ca, na2[s]);
+          nb2[s] = fmaf(cb, cb, nb2[s]);
+        }
+      }
+    }
+    kvcd::warp_sum4(dot, lane);
+    kvcd::warp_sum4(na2, lane);
+    kvcd::warp_sum4(nb2, lane);
+    if (lane == 0) {
+      float tot = 0.f;
+      int cnt = 0;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int w = 1 << s;
+        if (t >= w && t < n - w) {
+          const float nn = sqrtf(na2[s]) * sqrtf(nb2[s]);
+          const float cs = nn > 0.f ? dot[s] / nn : 1.f;
+          tot += 1.f - cs;
+          ++cnt;
+        }
+      }
+      a.kappa[row0 + t] = cnt > 0 ? tot / (float)cnt : 0.f;
+    }
+  }
+}
+
+// One warp per slot tree.
+__global__ void __launch_bounds__(256) tree_cut_kernel(kvc_params p, TreeArgs a) {
+  __shared__ float ks[8][128];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long tree = (long long)blockIdx.x * 8 + warp;
+  if (tree >= (long long)p.B * p.L * p.H * p.S_max) return;
+  const int s = (int)(tree % p.S_max);
+  const long long blh = tree / p.S_max;
+  const int lh = (int)(blh % ((long long)p.L * p.H));
+  const int b = (int)(blh / ((long long)p.L * p.H));
+  uint8_t* out = a.cuts + tree * 8;
+  const int S = a.n_slots[b];
+  if (s >= S) {
+    if (lane < 8) out[lane] = 0;
+    return;
+  }
+  const int n = a.ctx_len[b];
+  const int x0 = a.bounds[(long long)b * (p.S_max + 1) + s];
+  const int y0 = a.bounds[(long long)b * (p.S_max + 1) + s + 1];
+  if (S > p.S_max || n > p.n_max || x0 < 0 || y0 - x0 < 16 || y0 - x0 > 128 || y0 > n - p.W) {
+    if (lane == 0) kvcd::record_error(a.err, KVC_EDEVICE);
+    return;
+  }
+  const int64_t row0 = kvcd::seq_token_base(a.ctx_len, b, p.L * p.H) + (int64_t)lh * n;
+  float* k = ks[warp];
+  for (int i = lane; i < y0 - x0; i += 32) k[i] = a.kappa[row0 + x0 + i];
+  __syncwarp();
+  int na[15], nb[15];                          // node ranges (relative to x0)
+  na[0] = 0; nb[0] = y0 - x0;
+  uint8_t cut[7];
+#pragma unroll
+  for (int j = 0; j < 7; ++j) {
+    const int lo_n = na[j], hi_n = nb[j];
+    const int depth = kvcd::tree_depth(j);
+    const int lo = 8 >> depth, hi = 64 >> depth;   // 2 and 16 tokens per leaf below
+    const int c = hi_n - lo_n;
+    const int m = (lo_n + hi_n) >> 1;
+    float acc = 0.f;                          // index-order sum, the same on every lane
+    for (int i = lo_n; i < hi_n; ++i) acc = __fadd_rn(acc, k[i]);
+    const float lam = __fdiv_rn(acc, (float)c);
+    const float half = __fmul_rn((float)c, 0.5f);
+    auto score = [&](int t) {
+      const float r = __fdiv_rn((float)(t - m), half);
+      return __fsub_rn(k[t], __fmul_rn(lam, __fmul_rn(r, r)));
+    };
+    float best = -INFINITY;
+    int best_t = 0x7fffffff;
+    for (int t = lo_n + lo + lane; t <= hi_n - lo; t += 32) {
+      if (t - lo_n > hi || hi_n - t > hi) continue;
+      const float sc = score(t);
+      if (sc > best) { best = sc; best_t = t; }   // ascending t: first maximum per lane
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ob = __shfl_xor_sync(KVC_FULL_MASK, best, o);
+      const int ot = __shfl_xor_sync(KVC_FULL_MASK, best_t, o);
+      if (ob > best || (ob == best && ot < best_t)) { best = ob; best_t = ot; }
+    }
+    const int t = best > score(m) ? best_t : m;
+    cut[j] = (uint8_t)t;
+    na[2 * j + 1] = lo_n; nb[2 * j + 1] = t;
+    na[2 * j + 2] = t;    nb[2 * j + 2] = hi_n;
+  }
+  if (lane < 8) out[lane] = lane < 7 ? cut[lane] : (uint8_t)0;
+}
+
+}  // namespace
+
+extern "C" int kvc_tree_cuts(const kvc_params* p, const int32_t* ctx_len, const void* K,
+                             const float* rope_cos, const float* rope_sin,
+                             const int32_t* slot_bounds, const int32_t* n_slots, float* kappa,
+                             uint8_t* cuts, void* stream) {
+  int st = kvc::check_params(p);
+  if (st != KVC_OK) return st;
+  if (!ctx_len || !K || !rope_cos || !rope_sin || !slot_bounds || !n_slots || !kappa || !cuts)
+    return KVC_EINVAL;
+  const long long blh = kvc::lh_count(p);
+  if (blh > 65535) return KVC_EINVAL;
+  int32_t* err = kvc::err_word();
+  if (!err) return KVC_ECUDA;
+  TreeArgs a;
+  a.ctx_len = ctx_len; a.K = K; a.cos_tab = rope_cos; a.sin_tab = rope_sin;
+  a.bounds = slot_bounds; a.n_slots = n_slots; a.kappa = kappa; a.cuts = cuts; a.err = err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const dim3 g1((unsigned)((p->n_max + kCurvTile - 1) / kCurvTile), (unsigned)blh);
+  if (p->dtype == KVC_BF16) {
+    if (p->d == 128) key_curv_kernel<__nv_bfloat16, 128><<<g1, 256, 0, s>>>(*p, a);
+    else key_curv_kernel<__nv_bfloat16, 64><<<g1, 256, 0, s>>>(*p, a);
+  } else {
+    if (p->d == 128) key_curv_kernel<float, 128><<<g1, 256, 0, s>>>(*p, a);
+    else key_curv_kernel<float, 64><<<g1, 256, 0, s>>>(*p, a);
+  }
+  const long long trees = blh * p->S_max;
+  tree_cut_kernel<<<(unsigned)((trees + 7) / 8), 256, 0, s>>>(*p, a);
+  kvc::count_launch(2);
+  return kvc::cuda_status(cudaGetLastError());
+}

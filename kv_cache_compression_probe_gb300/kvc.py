@@ -25,7 +25,7 @@ EXPORTED = ("kvc_status_string", "kvc_last_cuda_error", "kvc_device_error", "kvc
             "kvc_rope_table", "kvc_score", "kvc_select", "kvc_merge_pack", "kvc_decode_attn",
             "kvc_partition", "kvc_decode_attn_noalloc", "kvc_decode_attn_lse", "kvc_token_alpha",
             "kvc_evict_workspace_bytes", "kvc_evict_topb", "kvc_set_phase_timing",
-            "kvc_score_phase_ms", "kvc_decode_attn_layers")
+            "kvc_score_phase_ms", "kvc_decode_attn_layers", "kvc_tree_cuts")
 
 
 class kvc_params(ctypes.Structure):
@@ -39,6 +39,7 @@ class kvc_params(ctypes.Structure):
         ("total_ctx", c_int64),
         ("packed_rows", c_int64),
         ("head_full_frac", c_double),
+        ("tree_cuts", ctypes.c_void_p),
     ]
 
 
@@ -93,6 +94,8 @@ def lib():
         L.kvc_score_phase_ms.restype = c_int
         L.kvc_partition.argtypes = [_P, vp, vp, c_int32, vp, vp, vp, vp, c_size_t, vp]
         L.kvc_partition.restype = c_int
+        L.kvc_tree_cuts.argtypes = [_P] + [vp] * 9
+        L.kvc_tree_cuts.restype = c_int
         _lib = L
     return _lib
 
@@ -129,7 +132,7 @@ def make_params(**kw) -> kvc_params:
     defaults = dict(rope_base=10000.0, hop_weight=0.3, n_hops=2, w_part=0.25, w_value=0.75,
                     value_floor=0.1, budget_ratio=0.25, budget_entries_per_lh=0,
                     floor_cap_frac=0.6, floor_cap_tokens=-1, decode_reserve=0, total_ctx=0,
-                    packed_rows=0, head_full_frac=0.0)
+                    packed_rows=0, head_full_frac=0.0, tree_cuts=None)
     defaults.update(kw)
     for k, v in defaults.items():
         setattr(p, k, v)
@@ -267,6 +270,13 @@ def kvc_partition(p, ctx_len, hidden, dh, kappa, slot_bounds, n_slots, workspace
     _check(lib().kvc_partition(ctypes.byref(p), _ptr(ctx_len), _ptr(hidden), dh, _ptr(kappa),
                                _ptr(slot_bounds), _ptr(n_slots), w, wb, _stream(stream)),
            "kvc_partition")
+
+
+def kvc_tree_cuts(p, ctx_len, K, rope_cos, rope_sin, slot_bounds, n_slots, kappa, cuts,
+                  stream=None):
+    _check(lib().kvc_tree_cuts(ctypes.byref(p), _ptr(ctx_len), _ptr(K), _ptr(rope_cos),
+                               _ptr(rope_sin), _ptr(slot_bounds), _ptr(n_slots), _ptr(kappa),
+                               _ptr(cuts), _stream(stream)), "kvc_tree_cuts")
 
 
 def workspace(which: int, p: kvc_params, device="cuda", zero=False) -> torch.Tensor:

@@ -31,7 +31,11 @@ def packed_capacity(p: kvc.kvc_params, ctx_len: Sequence[int]) -> int:
 
 class Compressor:
     def __init__(self, p: kvc.kvc_params, ctx_len: Sequence[int], device="cuda",
-                 tensor_cores: bool = True):
+                 tensor_cores: bool = True, tree_cuts: bool = False):
+        """tree_cuts=True: every scoring call first runs kvc_tree_cuts, and
+        scoring, selection and packing use those curvature-chosen trees
+        (p.tree_cuts points at this object's cut table); otherwise the
+        midpoint trees."""
         self.p = p
         self.device = device
         self.ctx_host = [int(n) for n in ctx_len]
@@ -69,6 +73,9 @@ class Compressor:
         self.ws_select = kvc.workspace(kvc.KVC_WS_SELECT, p, device)
         self.ws_pack = kvc.workspace(kvc.KVC_WS_PACK, p, device)
         self.ws_decode = kvc.workspace(kvc.KVC_WS_DECODE, p, device, zero=True)
+        self.tree_kappa = torch.empty((rows,), dtype=f32, **z) if tree_cuts else None
+        self.cuts = torch.zeros((B, L, H, S, 8), dtype=torch.uint8, **z) if tree_cuts else None
+        p.tree_cuts = self.cuts.data_ptr() if tree_cuts else None
         self._graphs = {}
 
     # ---------------------------------------------------------------- calls
@@ -99,6 +106,9 @@ class Compressor:
 
     def score(self, K, V, Qp, slot_bounds, n_slots, head_sens=None, stream=None, graph=False):
         def run(st):
+            if self.cuts is not None:
+                kvc.kvc_tree_cuts(self.p, self.ctx_len, K, self.rope_cos, self.rope_sin,
+                                  slot_bounds, n_slots, self.tree_kappa, self.cuts, st)
             kvc.kvc_score(self.p, self.ctx_len, K, V, Qp, self.rope_cos, self.rope_sin,
                           slot_bounds, n_slots, head_sens, self.lse, self.feats, self.relevance,
                           self.op_util, self.op_cost, self.ws_score, st)
@@ -174,6 +184,11 @@ class Compressor:
             cur.wait_event(events[c])
             pc = kvc.kvc_params.from_buffer_copy(p)
             pc.L = l1 - l0
+            if self.cuts is not None:
+                pc.tree_cuts = self.cuts[:, l0:l1].data_ptr()
+                kvc.kvc_tree_cuts(pc, self.ctx_len, K[r0:r1], self.rope_cos, self.rope_sin,
+                                  slot_bounds, n_slots, self.tree_kappa[r0:r1],
+                                  self.cuts[:, l0:l1], cur)
             kvc.kvc_score(pc, self.ctx_len, K[r0:r1], V[r0:r1], Qp[:, l0:l1], self.rope_cos,
                           self.rope_sin, slot_bounds, n_slots,
                           None if head_sens is None else head_sens[l0:l1], self.lse[:, l0:l1],

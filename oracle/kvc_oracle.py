@@ -339,7 +339,8 @@ def score_and_value_head(Kh, Vh, Qh, n: int, P: int, bounds: np.ndarray, sens: f
 
 
 # =============================================================================== f3: curvature-chosen trees
-LEAF_MAX = 16         # R18: a cut may not leave a leaf prototype of more than 16 tokens
+LEAF_MIN = 2          # R18: a cut keeps every leaf prototype at 2..16 tokens, the range of
+LEAF_MAX = 16         # the midpoint trees' leaves over slots of 16..128 tokens
 
 
 def key_curvature(Kh: np.ndarray, base: float, scales: Sequence[int] = (1, 2, 4, 8)) -> np.ndarray:
@@ -365,10 +366,11 @@ def tree_cuts(kappa: np.ndarray, x0: int, y0: int, dtype=np.float64) -> List[int
         score(t) = kappa[t] - lam * ((t - m) / (c / 2))^2,   lam = mean kappa[a:b)
     (the partition's curvature gain with its length-balance penalty, so the
     midpoint, penalty 0, wins unless a turn outweighs its imbalance).  A cut at
-    t makes children [a, t) and [t, b); it is valid when each child keeps one
-    token per leaf below it (2^(2-k)) and at most LEAF_MAX per leaf
-    (LEAF_MAX * 2^(2-k)); the midpoint of every slot of 16..128 tokens always
-    is.  Ties go to the midpoint, then to the smaller t.  Every operation is
+    t makes children [a, t) and [t, b); it is valid when each child keeps
+    LEAF_MIN..LEAF_MAX tokens per leaf below it (2^(2-k) leaves), so a leaf
+    split always stores at least 2 tokens for its cost; the midpoint of every
+    node of a slot of 16..128 tokens always is valid.  Ties go to the midpoint,
+    then to the smaller t.  Every operation is
     rounded to ``dtype`` in the order written (lam summed in index order), so
     ``dtype=np.float32`` reproduces a single-precision evaluation exactly.
     """
@@ -379,8 +381,8 @@ def tree_cuts(kappa: np.ndarray, x0: int, y0: int, dtype=np.float64) -> List[int
     for j in range(7):
         a, b = nodes[j]
         depth = 0 if j == 0 else (1 if j < 3 else 2)
-        lo = 2 ** (2 - depth)
-        hi = LEAF_MAX * lo
+        lo = LEAF_MIN * 2 ** (2 - depth)
+        hi = LEAF_MAX * 2 ** (2 - depth)
         c = b - a
         m = (a + b) // 2
         acc = f(0)

@@ -94,14 +94,14 @@ def test_full_slot_leaves_no_freedom():
         assert O.tree_nodes(30, 158, O.tree_cuts(kap, 30, 158)) == O.tree_nodes(30, 158)
 
 
-def _valid(lo_leaves, size):
-    return lo_leaves <= size <= O.LEAF_MAX * lo_leaves
+def _valid(leaves, size):
+    return O.LEAF_MIN * leaves <= size <= O.LEAF_MAX * leaves
 
 
 @pytest.mark.parametrize("dtype", [np.float64, np.float32])
 def test_random_curvature_trees_are_valid_and_optimal(dtype):
     """Random spiky curvature: every tree partitions its slot, every node keeps
-    one token per leaf below it and at most LEAF_MAX per leaf, and each cut's
+    LEAF_MIN..LEAF_MAX tokens per leaf below it, and each cut's
     score is at least that of every other valid cut of its node (brute force)."""
     rng = np.random.default_rng(3)
     f = np.dtype(dtype).type
