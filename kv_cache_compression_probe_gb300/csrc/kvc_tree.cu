@@ -14,14 +14,17 @@
 // trees' leaves, so every leaf split stores at least 2 tokens.
 //
 // Kernel 1 (key_curv_kernel): one CTA per (b,l,h) and 64 positions; the unit
-// rows of positions [t0 - 8, t0 + 72) are staged in shared memory (one warp per
-// row: unrotate with the half-position table row 2i, one warp reduction for the
-// norm), then one warp per position forms the 4 scales' chords with lanes
-// owning 4 features each; the 12 dot products are reduced 4 at a time.
+// rows of positions [t0 - 8, t0 + 72) are staged in shared memory (a warp per
+// row, 5 rows' loads in flight at once: unrotate with the half-position table
+// row 2i, one warp reduction for the norm), then one warp per position forms
+// the 4 scales' chords with lanes owning 4 consecutive features (one vector
+// load per row); the 12 dot products are reduced 4 at a time.
 // Kernel 2 (tree_cut_kernel): one warp per slot tree; the node mean is summed
 // in index order by every lane (the same fp32 sum the cut decision is checked
 // against), candidates are scored 32 at a time with explicitly rounded fp32
 // operations (no contraction) and the warp keeps the first maximum.
+#include <type_traits>
+
 #include "kvc_common.cuh"
 #include "kvc_internal.h"
 
@@ -47,7 +50,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(256) key_curv_kernel(kvc_params p, TreeArgs a) {
   constexpr int VP = D / 64;                   // RoPE pairs per lane
   constexpr int HALF = D / 2;
-  __shared__ float urow[kCurvRows][D];
+  __shared__ __align__(16) float urow[kCurvRows][D];
   const long long blh = blockIdx.y;
   const int lh = (int)(blh % ((long long)p.L * p.H));
   const int b = (int)(blh / ((long long)p.L * p.H));
@@ -61,54 +64,93 @@ __global__ void __launch_bounds__(256) key_curv_kernel(kvc_params p, TreeArgs a)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t row0 = kvcd::seq_token_base(a.ctx_len, b, p.L * p.H) + (int64_t)lh * n;
   const T* Kh = static_cast<const T*>(a.K) + row0 * D;
-  // unit rows u_i of positions t0 - 8 .. t0 + 71 (zero outside [0, n))
-  for (int r = warp; r < kCurvRows; r += 8) {
-    const int i = t0 - kCurvHalo + r;
-    float lo[VP], hi[VP];
-    float n2 = 0.f;
-    if (i >= 0 && i < n) {
-      const float* ct = a.cos_tab + (int64_t)(2 * i) * HALF + lane * VP;
-      const float* st = a.sin_tab + (int64_t)(2 * i) * HALF + lane * VP;
+  // unit rows u_i of positions t0 - 8 .. t0 + 71 (zero outside [0, n)); each
+  // warp owns rows warp, warp + 8, ..., in batches whose loads are all issued
+  // before the first use
+  constexpr int kRowsPerWarp = kCurvRows / 8;
+  constexpr int kBatch = 5;
+  static_assert(kRowsPerWarp % kBatch == 0, "row batches");
+#pragma unroll 1
+  for (int r0 = 0; r0 < kRowsPerWarp; r0 += kBatch) {
+    float klo[kBatch][VP], khi[kBatch][VP], cs[kBatch][VP], sn[kBatch][VP];
+    bool in[kBatch];
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      const int i = t0 - kCurvHalo + warp + 8 * (r0 + q);
+      in[q] = i >= 0 && i < n;
+      const int ic = in[q] ? i : 0;                     // a valid row, result discarded
+      const T* kr = Kh + (int64_t)ic * D;
+      const float* ct = a.cos_tab + (int64_t)(2 * ic) * HALF + lane * VP;
+      const float* st = a.sin_tab + (int64_t)(2 * ic) * HALF + lane * VP;
+      if constexpr (VP == 2) {
+        kvcd::VecLoad<T, 2>::ld(kr + lane * 2, klo[q]);
+        kvcd::VecLoad<T, 2>::ld(kr + HALF + lane * 2, khi[q]);
+        kvcd::VecLoad<float, 2>::ld(ct, cs[q]);
+        kvcd::VecLoad<float, 2>::ld(st, sn[q]);
+      } else {
+        klo[q][0] = kvcd::to_f(kr[lane]);
+        khi[q][0] = kvcd::to_f(kr[HALF + lane]);
+        cs[q][0] = __ldg(ct);
+        sn[q][0] = __ldg(st);
+      }
+    }
+    float n2[kBatch];
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      n2[q] = 0.f;
 #pragma unroll
       for (int t = 0; t < VP; ++t) {
-        const float k0 = kvcd::to_f(Kh[(int64_t)i * D + lane * VP + t]);
-        const float k1 = kvcd::to_f(Kh[(int64_t)i * D + HALF + lane * VP + t]);
-        const float cs = __ldg(ct + t), sn = __ldg(st + t);
-        lo[t] = k0 * cs + k1 * sn;                       // R(-i)
-        hi[t] = k1 * cs - k0 * sn;
-        n2 += lo[t] * lo[t] + hi[t] * hi[t];
+        const float lo = klo[q][t] * cs[q][t] + khi[q][t] * sn[q][t];     // R(-i)
+        const float hi = khi[q][t] * cs[q][t] - klo[q][t] * sn[q][t];
+        klo[q][t] = in[q] ? lo : 0.f;
+        khi[q][t] = in[q] ? hi : 0.f;
+        n2[q] += klo[q][t] * klo[q][t] + khi[q][t] * khi[q][t];
       }
-    } else {
-#pragma unroll
-      for (int t = 0; t < VP; ++t) lo[t] = hi[t] = 0.f;
     }
-    n2 = kvcd::warp_sum(n2);
-    const float inv = n2 > 0.f ? 1.f / sqrtf(n2) : 0.f;
+    static_assert(kBatch == 5, "one four-way and one single reduction");
+    kvcd::warp_sum4(*reinterpret_cast<float(*)[4]>(&n2[0]), lane);
+    n2[4] = kvcd::warp_sum(n2[4]);
 #pragma unroll
-    for (int t = 0; t < VP; ++t) {
-      urow[r][lane * VP + t] = lo[t] * inv;
-      urow[r][HALF + lane * VP + t] = hi[t] * inv;
+    for (int q = 0; q < kBatch; ++q) {
+      const int r = warp + 8 * (r0 + q);
+      const float inv = n2[q] > 0.f ? 1.f / sqrtf(n2[q]) : 0.f;
+#pragma unroll
+      for (int t = 0; t < VP; ++t) {
+        urow[r][lane * VP + t] = klo[q][t] * inv;
+        urow[r][HALF + lane * VP + t] = khi[q][t] * inv;
+      }
     }
   }
   __syncthreads();
-  constexpr int FL = D / 32;                   // features per lane in the chord sums
+  // one warp per position; lane owns FL consecutive features (one vector load
+  // per row), the 12 chord sums of a position are reduced four at a time
+  constexpr int FL = D / 32;
+  using VecF = typename std::conditional<FL == 4, float4, float2>::type;
+  auto ld = [&](int row, float* v) {
+    const VecF x = *reinterpret_cast<const VecF*>(&urow[row][lane * FL]);
+    v[0] = x.x; v[1] = x.y;
+    if constexpr (FL == 4) { v[2] = reinterpret_cast<const float4&>(x).z;
+                             v[3] = reinterpret_cast<const float4&>(x).w; }
+  };
   for (int q = warp; q < kCurvTile; q += 8) {
     const int t = t0 + q;
     if (t >= n) break;
     const int rc = q + kCurvHalo;
     float uc[FL];
-#pragma unroll
-    for (int f = 0; f < FL; ++f) uc[f] = urow[rc][lane + 32 * f];
+    ld(rc, uc);
     float dot[4], na2[4], nb2[4];
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
       const int w = 1 << s;
       dot[s] = na2[s] = nb2[s] = 0.f;
       if (t >= w && t < n - w) {
+        float um[FL], up[FL];
+        ld(rc - w, um);
+        ld(rc + w, up);
 #pragma unroll
         for (int f = 0; f < FL; ++f) {
-          const float ca = uc[f] - urow[rc - w][lane + 32 * f];
-          const float cb = urow[rc + w][lane + 32 * f] - uc[f];
+          const float ca = uc[f] - um[f];
+          const float cb = up[f] - uc[f];
           dot[s] = fmaf(ca, cb, dot[s]);
           na2[s] = fmaf(ca, ca, na2[s]);
           nb2[s] = fmaf(cb, cb, nb2[s]);
