@@ -340,6 +340,36 @@ def tree_cuts_leg(comp, K, bounds, n_slots, cfg, tokens, hbm, dev, reps=5):
                     "runs inside every timed step's scoring call"}
 
 
+def compression_reps(comp, K, V, Qp, bounds, n_slots, cfg, tokens, graph, dev, reps=20):
+    """Compression alone (kvc_score + kvc_select + kvc_merge_pack, graph replays
+    when the step uses them): `reps` repetitions after the step's warm-ups, each
+    bracketed by CUDA events on the launching stream; per-call and total
+    medians.  K and V (2 GB at 16K) exceed L2, so no flush is added."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    per = {"score": [], "select": [], "merge_pack": [], "total": []}
+    for _ in range(reps):
+        m = [ev() for _ in range(4)]
+        m[0].record(stream)
+        comp.score(K, V, Qp, bounds, n_slots, graph=graph)
+        m[1].record(stream)
+        comp.select(bounds, n_slots, graph=graph)
+        m[2].record(stream)
+        comp.merge_pack(K, V, bounds, n_slots, graph=graph)
+        m[3].record(stream)
+        torch.cuda.synchronize(dev)
+        per["score"].append(m[0].elapsed_time(m[1]))
+        per["select"].append(m[1].elapsed_time(m[2]))
+        per["merge_pack"].append(m[2].elapsed_time(m[3]))
+        per["total"].append(m[0].elapsed_time(m[3]))
+    med = {k: statistics.median(v) for k, v in per.items()}
+    return {"reps": reps, "median_ms": med,
+            "kv_tokens_per_s": tokens / (med["total"] * 1e-3),
+            "lh_entries_per_s": tokens * cfg.L * cfg.H / (med["total"] * 1e-3),
+            "min_ms": min(per["total"]), "max_ms": max(per["total"])}
+
+
 def scoring_gemm(comp, K, V, Qp, bounds, n_slots, cfg, tokens, tc_peak, dev):
     """Device time of the probe-times-key contraction passes of one kvc_score
     call (CUDA events the library records between its phases when phase
@@ -558,6 +588,8 @@ def run_gpu(args, cfg, rank, world):
     full_ms = None if args.profile else full_cache_decode_ms(p, cfg, seqs, K, V, q_all, kn_all,
                                                             vn_all, D, dev, stream)
 
+    creps = None if args.profile else compression_reps(comp, K, V, Qp, bounds, n_slots, cfg,
+                                                       sum(s[0] for s in seqs), cg, dev)
     gemm = None if args.profile else scoring_gemm(comp, K, V, Qp, bounds, n_slots, cfg,
                                                   sum(s[0] for s in seqs), measured_peaks()[1],
                                                   dev)
@@ -640,6 +672,7 @@ def run_gpu(args, cfg, rank, world):
         "breakdown_ms": {"score": score_ms, "select": sel_ms, "merge_pack": pack_ms,
                          "decode_per_step": dec_ms, "decode_total": dec_ms * D},
         "compress_tokens_per_s": tokens / ((score_ms + sel_ms + pack_ms) * 1e-3),
+        "compression_median_of_reps": creps,
         "decode_gbs": dec_gbs,
         "decode_eager_ms_per_step": eager_ms,
         "decode_full_ms_per_step": full_ms,

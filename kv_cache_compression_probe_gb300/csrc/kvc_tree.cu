@@ -18,7 +18,9 @@
 // row, 5 rows' loads in flight at once: unrotate with the half-position table
 // row 2i, one warp reduction for the norm), then one warp per position forms
 // the 4 scales' chords with lanes owning 4 consecutive features (one vector
-// load per row); the 12 dot products are reduced 4 at a time.
+// load per row); the 12 dot products are reduced by one 16-value
+// reduce-scatter and the 4 scale terms are finished on 4 lanes at once
+// (cos = dot * rsqrt(|a|^2 |b|^2)).
 // Kernel 2 (tree_cut_kernel): one warp per slot tree; the node mean is summed
 // in index order by every lane (the same fp32 sum the cut decision is checked
 // against), candidates are scored 32 at a time with explicitly rounded fp32
@@ -29,6 +31,26 @@
 #include "kvc_internal.h"
 
 namespace {
+
+// Sums v[0..15] over the warp as a reduce-scatter: each butterfly level keeps
+// half of the values and adds the partner's other half, so lanes 2j and 2j+1
+// end with the total of v[j] (16 shuffles for 16 sums).
+__device__ __forceinline__ float warp_reduce_scatter16(const float (&v)[16], int lane) {
+  float a[8], b[4], c[2];
+  const bool h16 = (lane & 16) != 0, h8 = (lane & 8) != 0, h4 = (lane & 4) != 0,
+             h2 = (lane & 2) != 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    a[i] = (h16 ? v[i + 8] : v[i]) + __shfl_xor_sync(KVC_FULL_MASK, h16 ? v[i] : v[i + 8], 16);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    b[i] = (h8 ? a[i + 4] : a[i]) + __shfl_xor_sync(KVC_FULL_MASK, h8 ? a[i] : a[i + 4], 8);
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    c[i] = (h4 ? b[i + 2] : b[i]) + __shfl_xor_sync(KVC_FULL_MASK, h4 ? b[i] : b[i + 2], 4);
+  float d = (h2 ? c[1] : c[0]) + __shfl_xor_sync(KVC_FULL_MASK, h2 ? c[0] : c[1], 2);
+  return d + __shfl_xor_sync(KVC_FULL_MASK, d, 1);
+}
 
 constexpr int kCurvTile = 64;                 // positions per CTA
 constexpr int kCurvHalo = 8;                  // largest scale
@@ -123,7 +145,7 @@ __global__ void __launch_bounds__(256) key_curv_kernel(kvc_params p, TreeArgs a)
   }
   __syncthreads();
   // one warp per position; lane owns FL consecutive features (one vector load
-  // per row), the 12 chord sums of a position are reduced four at a time
+  // per row)
   constexpr int FL = D / 32;
   using VecF = typename std::conditional<FL == 4, float4, float2>::type;
   auto ld = [&](int row, float* v) {
@@ -138,11 +160,12 @@ __global__ void __launch_bounds__(256) key_curv_kernel(kvc_params p, TreeArgs a)
     const int rc = q + kCurvHalo;
     float uc[FL];
     ld(rc, uc);
-    float dot[4], na2[4], nb2[4];
+    // v[4s + 0..2] = chord dot, |a|^2, |b|^2 of scale w = 2^s (v[4s + 3] = 0)
+    float v[16];
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
       const int w = 1 << s;
-      dot[s] = na2[s] = nb2[s] = 0.f;
+      v[4 * s] = v[4 * s + 1] = v[4 * s + 2] = v[4 * s + 3] = 0.f;
       if (t >= w && t < n - w) {
         float um[FL], up[FL];
         ld(rc - w, um);
@@ -151,30 +174,26 @@ __global__ void __launch_bounds__(256) key_curv_kernel(kvc_params p, TreeArgs a)
         for (int f = 0; f < FL; ++f) {
           const float ca = uc[f] - um[f];
           const float cb = up[f] - uc[f];
-          dot[s] = fmaf(ca, cb, dot[s]);
-          na2[s] = fmaf(ca, ca, na2[s]);
-          nb2[s] = fmaf(cb, cb, nb2[s]);
+          v[4 * s] = fmaf(ca, cb, v[4 * s]);
+          v[4 * s + 1] = fmaf(ca, ca, v[4 * s + 1]);
+          v[4 * s + 2] = fmaf(cb, cb, v[4 * s + 2]);
         }
       }
     }
-    kvcd::warp_sum4(dot, lane);
-    kvcd::warp_sum4(na2, lane);
-    kvcd::warp_sum4(nb2, lane);
-    if (lane == 0) {
-      float tot = 0.f;
-      int cnt = 0;
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const int w = 1 << s;
-        if (t >= w && t < n - w) {
-          const float nn = sqrtf(na2[s]) * sqrtf(nb2[s]);
-          const float cs = nn > 0.f ? dot[s] / nn : 1.f;
-          tot += 1.f - cs;
-          ++cnt;
-        }
-      }
-      a.kappa[row0 + t] = cnt > 0 ? tot / (float)cnt : 0.f;
-    }
+    // lane 8s ends with scale s's dot, and fetches its two squared norms
+    const float r = warp_reduce_scatter16(v, lane);
+    const float na2 = __shfl_sync(KVC_FULL_MASK, r, (lane & 24) + 2);
+    const float nb2 = __shfl_sync(KVC_FULL_MASK, r, (lane & 24) + 4);
+    const int w = 1 << (lane >> 3);
+    const bool fits = t >= w && t < n - w;
+    const float nn2 = na2 * nb2;
+    float term = fits ? 1.f - (nn2 > 0.f ? r * rsqrtf(nn2) : 1.f) : 0.f;
+    float cnt = fits ? 1.f : 0.f;
+    term += __shfl_xor_sync(KVC_FULL_MASK, term, 8);
+    cnt += __shfl_xor_sync(KVC_FULL_MASK, cnt, 8);
+    term += __shfl_xor_sync(KVC_FULL_MASK, term, 16);
+    cnt += __shfl_xor_sync(KVC_FULL_MASK, cnt, 16);
+    if (lane == 0) a.kappa[row0 + t] = cnt > 0.f ? term / cnt : 0.f;
   }
 }
 
