@@ -1103,22 +1103,34 @@ __global__ void score_check_kernel(kvc_params p, ScoreArgs a) {
       const int ln = bd[s + 1] - bd[s];
       ok = ln >= 16 && ln <= 128;
     }
-    // a cut table entry that the tree helpers would replace by the midpoint
-    // is reported (the replacement keeps every kernel on one valid tree)
-    for (int s = 0; ok && p.tree_cuts && s < S; ++s) {
-      const uint8_t* cuts = kvcd::tree_cuts_of(p, blh, s);
-      for (int j = 0; j < 7; ++j) {
-        int x, y;
-        kvcd::tree_node_range(cuts, j, bd[s], bd[s + 1], x, y);
-        if (!kvcd::tree_cut_valid(bd[s] + (int)cuts[j], kvcd::tree_depth(j), x, y)) {
-          kvcd::record_error(a.err, KVC_EDEVICE);
-          break;
-        }
-      }
-    }
   }
   a.ok[blh] = ok ? 1 : 0;
   if (!ok) kvcd::record_error(a.err, KVC_EDEVICE);
+}
+
+// One thread per slot tree: a cut table entry that the tree helpers would
+// replace by the midpoint is reported (the replacement keeps every kernel on
+// one valid tree).
+__global__ void cuts_check_kernel(kvc_params p, ScoreArgs a) {
+  const long long tree = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (tree >= (long long)p.B * p.L * p.H * p.S_max) return;
+  const int s = (int)(tree % p.S_max);
+  const long long blh = tree / p.S_max;
+  const int b = seq_of(p, blh);
+  const int S = a.n_slots[b];
+  if (s >= S || S > p.S_max) return;
+  const int x0 = a.bounds[(long long)b * (p.S_max + 1) + s];
+  const int y0 = a.bounds[(long long)b * (p.S_max + 1) + s + 1];
+  if (x0 < 0 || y0 - x0 < 16 || y0 - x0 > 128) return;   // score_check_kernel reports it
+  const uint8_t* cuts = kvcd::tree_cuts_of(p, blh, s);
+  for (int j = 0; j < 7; ++j) {
+    int x, y;
+    kvcd::tree_node_range(cuts, j, x0, y0, x, y);
+    if (!kvcd::tree_cut_valid(x0 + (int)cuts[j], kvcd::tree_depth(j), x, y)) {
+      kvcd::record_error(a.err, KVC_EDEVICE);
+      return;
+    }
+  }
 }
 
 int chunk_for(const kvc_params* p) {
@@ -1213,6 +1225,11 @@ int launch_all(const kvc_params* p, ScoreArgs& a, cudaStream_t s) {
   cudaFuncSetAttribute(nodes_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)sm_nodes);
   score_check_kernel<<<(unsigned)((blh + 255) / 256), 256, 0, s>>>(*p, a); ++launches;
+  if (p->tree_cuts) {
+    const long long trees = blh * p->S_max;
+    cuts_check_kernel<<<(unsigned)((trees + 255) / 256), 256, 0, s>>>(*p, a);
+    ++launches;
+  }
   if constexpr (std::is_same<T, __nv_bfloat16>::value && D == 128) {
    if (use_tc(p)) {
     // tensor-core probe-times-key passes

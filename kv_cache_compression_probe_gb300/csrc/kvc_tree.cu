@@ -18,15 +18,13 @@
 // row, 5 rows' loads in flight at once: unrotate with the half-position table
 // row 2i, one warp reduction for the norm), then one warp per position forms
 // the 4 scales' chords with lanes owning 4 consecutive features (one vector
-// load per row); the 12 dot products are reduced by one 16-value
+// load per row, packed f32x2 arithmetic); the 12 dot products are reduced by one 16-value
 // reduce-scatter and the 4 scale terms are finished on 4 lanes at once
 // (cos = dot * rsqrt(|a|^2 |b|^2)).
 // Kernel 2 (tree_cut_kernel): one warp per slot tree; the node mean is summed
 // in index order by every lane (the same fp32 sum the cut decision is checked
 // against), candidates are scored 32 at a time with explicitly rounded fp32
 // operations (no contraction) and the warp keeps the first maximum.
-#include <type_traits>
-
 #include "kvc_common.cuh"
 #include "kvc_internal.h"
 
@@ -50,6 +48,19 @@ __device__ __forceinline__ float warp_reduce_scatter16(const float (&v)[16], int
     c[i] = (h4 ? b[i + 2] : b[i]) + __shfl_xor_sync(KVC_FULL_MASK, h4 ? b[i] : b[i + 2], 4);
   float d = (h2 ? c[1] : c[0]) + __shfl_xor_sync(KVC_FULL_MASK, h2 ? c[0] : c[1], 2);
   return d + __shfl_xor_sync(KVC_FULL_MASK, d, 1);
+}
+
+// Packed pairs of fp32 (first element in the low half): one instruction
+// computes a * b + c on both halves.
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ float hsum2(uint64_t x) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+  return lo + hi;
 }
 
 constexpr int kCurvTile = 64;                 // positions per CTA
@@ -147,18 +158,22 @@ __global__ void __launch_bounds__(256) key_curv_kernel(kvc_params p, TreeArgs a)
   // one warp per position; lane owns FL consecutive features (one vector load
   // per row)
   constexpr int FL = D / 32;
-  using VecF = typename std::conditional<FL == 4, float4, float2>::type;
-  auto ld = [&](int row, float* v) {
-    const VecF x = *reinterpret_cast<const VecF*>(&urow[row][lane * FL]);
-    v[0] = x.x; v[1] = x.y;
-    if constexpr (FL == 4) { v[2] = reinterpret_cast<const float4&>(x).z;
-                             v[3] = reinterpret_cast<const float4&>(x).w; }
+  constexpr int NP = FL / 2;                   // packed feature pairs per lane
+  // chord arithmetic on packed pairs: a - b = fma(b, -1, a), rounded once
+  const uint64_t kNeg1 = ((uint64_t)__float_as_uint(-1.f) << 32) | __float_as_uint(-1.f);
+  auto ld = [&](int row, uint64_t* v) {
+    if constexpr (NP == 2) {
+      const ulonglong2 x = *reinterpret_cast<const ulonglong2*>(&urow[row][lane * FL]);
+      v[0] = x.x; v[1] = x.y;
+    } else {
+      v[0] = *reinterpret_cast<const unsigned long long*>(&urow[row][lane * FL]);
+    }
   };
   for (int q = warp; q < kCurvTile; q += 8) {
     const int t = t0 + q;
     if (t >= n) break;
     const int rc = q + kCurvHalo;
-    float uc[FL];
+    uint64_t uc[NP];
     ld(rc, uc);
     // v[4s + 0..2] = chord dot, |a|^2, |b|^2 of scale w = 2^s (v[4s + 3] = 0)
     float v[16];
@@ -167,17 +182,20 @@ __global__ void __launch_bounds__(256) key_curv_kernel(kvc_params p, TreeArgs a)
       const int w = 1 << s;
       v[4 * s] = v[4 * s + 1] = v[4 * s + 2] = v[4 * s + 3] = 0.f;
       if (t >= w && t < n - w) {
-        float um[FL], up[FL];
+        uint64_t um[NP], up[NP], dt = 0, aa = 0, bb = 0;
         ld(rc - w, um);
         ld(rc + w, up);
 #pragma unroll
-        for (int f = 0; f < FL; ++f) {
-          const float ca = uc[f] - um[f];
-          const float cb = up[f] - uc[f];
-          v[4 * s] = fmaf(ca, cb, v[4 * s]);
-          v[4 * s + 1] = fmaf(ca, ca, v[4 * s + 1]);
-          v[4 * s + 2] = fmaf(cb, cb, v[4 * s + 2]);
+        for (int f = 0; f < NP; ++f) {
+          const uint64_t ca = fma2(um[f], kNeg1, uc[f]);    // u_t - u_{t-w}
+          const uint64_t cb = fma2(uc[f], kNeg1, up[f]);    // u_{t+w} - u_t
+          dt = fma2(ca, cb, dt);
+          aa = fma2(ca, ca, aa);
+          bb = fma2(cb, cb, bb);
         }
+        v[4 * s] = hsum2(dt);
+        v[4 * s + 1] = hsum2(aa);
+        v[4 * s + 2] = hsum2(bb);
       }
     }
     // lane 8s ends with scale s's dot, and fetches its two squared norms
