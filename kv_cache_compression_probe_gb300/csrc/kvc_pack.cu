@@ -289,27 +289,38 @@ __global__ void __launch_bounds__(32 * kPackWarps, 32 / kPackWarps)
   if (item >= (long long)p.B * p.L * p.H * per) return;
   const int s = (int)(item % per);
   const long long blh = item / per;
-  if (!a.lh_ok[blh]) return;
   const int lh = (int)(blh % ((long long)p.L * p.H));
   const int b = (int)(blh / ((long long)p.L * p.H));
+  // every per-item word is loaded up front (one round trip instead of a chain
+  // of dependent ones); the window item (s == S_max) reads slot 0's words,
+  // which stay in range, and ignores them
+  const bool window = s == p.S_max;
+  const int sl = window ? 0 : s;
+  const int ok = a.lh_ok[blh];
   const int n = a.ctx_len[b];
   const int S = a.n_slots[b];
+  const int64_t base = a.off_lh[blh];
+  const int len = a.len_lh[blh];
+  const int32_t* bd = a.bounds + (long long)b * (p.S_max + 1);
+  const int x0 = bd[sl], y0 = bd[sl + 1];
+  const int sbase = a.slot_base[blh * p.S_max + sl];
+  const uint8_t* tk = a.taken + (blh * p.S_max + sl) * kOps;
+  uint32_t taken = 0;                                   // bit o = op o taken
+#pragma unroll
+  for (int o = 0; o < kOps; ++o) taken |= (tk[o] != 0 ? 1u : 0u) << o;
+  if (!ok) return;
   const int64_t row0 = kvcd::seq_token_base(a.ctx_len, b, p.L * p.H) + (int64_t)lh * n;
   const T* Kh = static_cast<const T*>(a.K) + row0 * D;
   const T* Vh = static_cast<const T*>(a.V) + row0 * D;
   const float* rh = a.rel + row0;
-  const int64_t base = a.off_lh[blh];
-  if (s == p.S_max) {                                   // window tokens
-    copy_exact<T, D>(a, Kh, Vh, n - p.W, p.W, base + a.len_lh[blh] - p.W, lane);
+  if (window) {                                         // window tokens
+    copy_exact<T, D>(a, Kh, Vh, n - p.W, p.W, base + len - p.W, lane);
     return;
   }
   if (s >= S) return;
-  const int32_t* bd = a.bounds + (long long)b * (p.S_max + 1);
-  const int x0 = bd[s], y0 = bd[s + 1];
-  const uint8_t* tk = a.taken + (blh * p.S_max + s) * kOps;
-  if (!tk[0]) return;
+  if (!(taken & 1u)) return;
   const uint8_t* cuts = kvcd::tree_cuts_of(p, blh, s);
-  int64_t dst = base + a.slot_base[blh * p.S_max + s];
+  int64_t dst = base + sbase;
   // left-to-right frontier walk with an explicit stack (depth <= 4)
   int stack[8];
   int sp = 0;
@@ -318,7 +329,7 @@ __global__ void __launch_bounds__(32 * kPackWarps, 32 / kPackWarps)
     const int j = stack[--sp];
     int x, y;
     node_range(cuts, j, x0, y0, x, y);
-    if (!tk[1 + j]) {
+    if (!((taken >> (1 + j)) & 1u)) {
       write_prototype<T, D>(p, a, Kh, Vh, rh, x, y, dst, lane);
       ++dst;
     } else if (j < 7) {
