@@ -24,6 +24,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -73,7 +74,8 @@ class ClockSampler:
 
     def __init__(self, gpu_index=0):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # the raw samples go to a scratch file; the JSON line carries their summary
+        self.path = os.path.join(tempfile.gettempdir(), f"kvc_bench_clocks_{os.getpid()}.csv")
         self.gpu = gpu_index
         self.t_begin = self.t_end = None
 
@@ -639,7 +641,7 @@ def run_gpu(args, cfg, rank, world):
     stored = packed_entries
     pack_bytes = (covered * (2 * d * esz + 4) + cfg.B * cfg.L * cfg.H * cfg.W * 2 * d * esz
                   + stored * (2 * d * esz + 8))
-    # score: K and V read once, features written (the spec accounting)
+    # score: K and V read once, features written (its HBM roofline's bytes)
     score_bytes = tokens * cfg.L * cfg.H * (2 * d * esz + 5 * 4)
     dec_tc = p.packed_rows > 0 and cfg.dtype == "bf16" and d == 128   # tensor-core decode
     # the committed DRAM capture covers the full 16K workload's launch (256 steps)
