@@ -16,11 +16,11 @@
 // Kernel 1 (key_curv_kernel): one CTA per (b,l,h) and 64 positions; the unit
 // rows of positions [t0 - 8, t0 + 72) are staged in shared memory (a warp per
 // row, 5 rows' loads in flight at once: unrotate with the half-position table
-// row 2i, one warp reduction for the norm), then one warp per position forms
-// the 4 scales' chords with lanes owning 4 consecutive features (one vector
-// load per row, packed f32x2 arithmetic); the 12 dot products are reduced by one 16-value
-// reduce-scatter and the 4 scale terms are finished on 4 lanes at once
-// (cos = dot * rsqrt(|a|^2 |b|^2)).
+// row 2i, one warp reduction for the norm), then every lane takes one
+// position and a quarter of the features (warp = 32-position group x
+// quarter) and sums the 12 chord terms of the 4 scales on packed f32x2 pairs
+// with no cross-lane reduction; the quarters meet in shared memory and one
+// thread per position finishes the scale terms (cos = dot * rsqrt(|a|^2 |b|^2)).
 // Kernel 2 (tree_cut_kernel): one warp per slot tree; the node mean is summed
 // in index order by every lane (the same fp32 sum the cut decision is checked
 // against), candidates are scored 32 at a time with explicitly rounded fp32
@@ -29,26 +29,6 @@
 #include "kvc_internal.h"
 
 namespace {
-
-// Sums v[0..15] over the warp as a reduce-scatter: each butterfly level keeps
-// half of the values and adds the partner's other half, so lanes 2j and 2j+1
-// end with the total of v[j] (16 shuffles for 16 sums).
-__device__ __forceinline__ float warp_reduce_scatter16(const float (&v)[16], int lane) {
-  float a[8], b[4], c[2];
-  const bool h16 = (lane & 16) != 0, h8 = (lane & 8) != 0, h4 = (lane & 4) != 0,
-             h2 = (lane & 2) != 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    a[i] = (h16 ? v[i + 8] : v[i]) + __shfl_xor_sync(KVC_FULL_MASK, h16 ? v[i] : v[i + 8], 16);
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    b[i] = (h8 ? a[i + 4] : a[i]) + __shfl_xor_sync(KVC_FULL_MASK, h8 ? a[i] : a[i + 4], 8);
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-    c[i] = (h4 ? b[i + 2] : b[i]) + __shfl_xor_sync(KVC_FULL_MASK, h4 ? b[i] : b[i + 2], 4);
-  float d = (h2 ? c[1] : c[0]) + __shfl_xor_sync(KVC_FULL_MASK, h2 ? c[0] : c[1], 2);
-  return d + __shfl_xor_sync(KVC_FULL_MASK, d, 1);
-}
 
 // Packed pairs of fp32 (first element in the low half): one instruction
 // computes a * b + c on both halves.
@@ -83,7 +63,14 @@ template <typename T, int D>
 __global__ void __launch_bounds__(256) key_curv_kernel(kvc_params p, TreeArgs a) {
   constexpr int VP = D / 64;                   // RoPE pairs per lane
   constexpr int HALF = D / 2;
-  __shared__ __align__(16) float urow[kCurvRows][D];
+  // unit rows, padded by 2 floats so that lanes on consecutive rows hit
+  // different banks; once the rows are consumed the same memory holds the
+  // chord partial sums of the 4 feature quarters
+  constexpr int RS = D + 2;
+  static_assert(4 * 12 * kCurvTile <= kCurvRows * RS, "partials alias the rows");
+  __shared__ __align__(16) float smem_f[kCurvRows * RS];
+  float (*urow)[RS] = reinterpret_cast<float (*)[RS]>(smem_f);
+  float (*part)[12][kCurvTile] = reinterpret_cast<float (*)[12][kCurvTile]>(smem_f);
   const long long blh = blockIdx.y;
   const int lh = (int)(blh % ((long long)p.L * p.H));
   const int b = (int)(blh / ((long long)p.L * p.H));
@@ -155,63 +142,64 @@ __global__ void __launch_bounds__(256) key_curv_kernel(kvc_params p, TreeArgs a)
     }
   }
   __syncthreads();
-  // one warp per position; lane owns FL consecutive features (one vector load
-  // per row)
-  constexpr int FL = D / 32;
-  constexpr int NP = FL / 2;                   // packed feature pairs per lane
-  // chord arithmetic on packed pairs: a - b = fma(b, -1, a), rounded once
+  // lane = position, warp = (32-position group, feature quarter): each lane
+  // sums its position's 12 chord terms over a quarter of the features on packed
+  // f32x2 pairs (no cross-lane reduction), the quarters meet in shared memory
+  constexpr int QF = D / 4;                    // features per quarter
+  const int grp = warp & 1, quarter = warp >> 1;
+  const int q = grp * 32 + lane;               // position within the tile
+  const int rc = q + kCurvHalo;
   const uint64_t kNeg1 = ((uint64_t)__float_as_uint(-1.f) << 32) | __float_as_uint(-1.f);
-  auto ld = [&](int row, uint64_t* v) {
-    if constexpr (NP == 2) {
-      const ulonglong2 x = *reinterpret_cast<const ulonglong2*>(&urow[row][lane * FL]);
-      v[0] = x.x; v[1] = x.y;
-    } else {
-      v[0] = *reinterpret_cast<const unsigned long long*>(&urow[row][lane * FL]);
-    }
+  uint64_t dt[4], aa[4], bb[4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) dt[s] = aa[s] = bb[s] = 0;
+  auto ld2 = [&](int row, int f) {
+    return *reinterpret_cast<const unsigned long long*>(&urow[row][f]);
   };
-  for (int q = warp; q < kCurvTile; q += 8) {
-    const int t = t0 + q;
-    if (t >= n) break;
-    const int rc = q + kCurvHalo;
-    uint64_t uc[NP];
-    ld(rc, uc);
-    // v[4s + 0..2] = chord dot, |a|^2, |b|^2 of scale w = 2^s (v[4s + 3] = 0)
-    float v[16];
+#pragma unroll 4
+  for (int f = quarter * QF; f < quarter * QF + QF; f += 2) {
+    const uint64_t uc = ld2(rc, f);
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
       const int w = 1 << s;
-      v[4 * s] = v[4 * s + 1] = v[4 * s + 2] = v[4 * s + 3] = 0.f;
-      if (t >= w && t < n - w) {
-        uint64_t um[NP], up[NP], dt = 0, aa = 0, bb = 0;
-        ld(rc - w, um);
-        ld(rc + w, up);
-#pragma unroll
-        for (int f = 0; f < NP; ++f) {
-          const uint64_t ca = fma2(um[f], kNeg1, uc[f]);    // u_t - u_{t-w}
-          const uint64_t cb = fma2(uc[f], kNeg1, up[f]);    // u_{t+w} - u_t
-          dt = fma2(ca, cb, dt);
-          aa = fma2(ca, ca, aa);
-          bb = fma2(cb, cb, bb);
-        }
-        v[4 * s] = hsum2(dt);
-        v[4 * s + 1] = hsum2(aa);
-        v[4 * s + 2] = hsum2(bb);
-      }
+      const uint64_t ca = fma2(ld2(rc - w, f), kNeg1, uc);      // u_t - u_{t-w}
+      const uint64_t cb = fma2(uc, kNeg1, ld2(rc + w, f));      // u_{t+w} - u_t
+      dt[s] = fma2(ca, cb, dt[s]);
+      aa[s] = fma2(ca, ca, aa[s]);
+      bb[s] = fma2(cb, cb, bb[s]);
     }
-    // lane 8s ends with scale s's dot, and fetches its two squared norms
-    const float r = warp_reduce_scatter16(v, lane);
-    const float na2 = __shfl_sync(KVC_FULL_MASK, r, (lane & 24) + 2);
-    const float nb2 = __shfl_sync(KVC_FULL_MASK, r, (lane & 24) + 4);
-    const int w = 1 << (lane >> 3);
-    const bool fits = t >= w && t < n - w;
-    const float nn2 = na2 * nb2;
-    float term = fits ? 1.f - (nn2 > 0.f ? r * rsqrtf(nn2) : 1.f) : 0.f;
-    float cnt = fits ? 1.f : 0.f;
-    term += __shfl_xor_sync(KVC_FULL_MASK, term, 8);
-    cnt += __shfl_xor_sync(KVC_FULL_MASK, cnt, 8);
-    term += __shfl_xor_sync(KVC_FULL_MASK, term, 16);
-    cnt += __shfl_xor_sync(KVC_FULL_MASK, cnt, 16);
-    if (lane == 0) a.kappa[row0 + t] = cnt > 0.f ? term / cnt : 0.f;
+  }
+  __syncthreads();                             // every warp is done with the rows
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    part[quarter][3 * s][q] = hsum2(dt[s]);
+    part[quarter][3 * s + 1][q] = hsum2(aa[s]);
+    part[quarter][3 * s + 2][q] = hsum2(bb[s]);
+  }
+  __syncthreads();
+  if (threadIdx.x < kCurvTile) {
+    const int qq = threadIdx.x;
+    const int t = t0 + qq;
+    if (t < n) {
+      float tot = 0.f;
+      int cnt = 0;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int w = 1 << s;
+        if (t >= w && t < n - w) {
+          const float dot = part[0][3 * s][qq] + part[1][3 * s][qq] + part[2][3 * s][qq] +
+                            part[3][3 * s][qq];
+          const float na2 = part[0][3 * s + 1][qq] + part[1][3 * s + 1][qq] +
+                            part[2][3 * s + 1][qq] + part[3][3 * s + 1][qq];
+          const float nb2 = part[0][3 * s + 2][qq] + part[1][3 * s + 2][qq] +
+                            part[2][3 * s + 2][qq] + part[3][3 * s + 2][qq];
+          const float nn2 = na2 * nb2;
+          tot += 1.f - (nn2 > 0.f ? dot * rsqrtf(nn2) : 1.f);
+          ++cnt;
+        }
+      }
+      a.kappa[row0 + t] = cnt > 0 ? tot / (float)cnt : 0.f;
+    }
   }
 }
 
