@@ -905,13 +905,22 @@ __device__ __forceinline__ ProtoAcc acc_from_smem(const ProtoLevels& sm, int lvl
   return s;
 }
 
+// One warp per block: slot trees differ in length and a block retires with its
+// slowest warp, so single-warp blocks let the block scheduler balance them
+// (the same choice as the pack kernel); 96 registers.
+#ifndef KVC_PROTO_WARPS
+#define KVC_PROTO_WARPS 1
+#endif
+constexpr int kProtoWarps = KVC_PROTO_WARPS;
+
 template <typename T, int D>
-__global__ void __launch_bounds__(128, 5) proto_kernel(kvc_params p, ScoreArgs a, unsigned char* proto) {
+__global__ void __launch_bounds__(32 * kProtoWarps, 20 / kProtoWarps)
+    proto_kernel(kvc_params p, ScoreArgs a, unsigned char* proto) {
   static_assert(D == 128 && sizeof(T) == 2, "tensor-core node path is bf16, d = 128");
-  __shared__ ProtoLevels levels[4];
+  __shared__ ProtoLevels levels[kProtoWarps];
   const int lane = threadIdx.x & 31;
   ProtoLevels& lv = levels[threadIdx.x >> 5];
-  const long long tree = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+  const long long tree = (long long)blockIdx.x * kProtoWarps + (threadIdx.x >> 5);
   if (tree >= (long long)p.B * p.L * p.H * p.S_max) return;
   const int s = (int)(tree % p.S_max);
   const long long blh = tree / p.S_max;
@@ -1262,7 +1271,8 @@ int launch_all(const kvc_params* p, ScoreArgs& a, cudaStream_t s) {
     }
     // prototypes, tensor-core node statistics, utilities
     if (timed) phase_mark(4, s);
-    proto_kernel<T, D><<<(unsigned)((blh * p->S_max + 3) / 4), 128, 0, s>>>(*p, a, a.proto);
+    proto_kernel<T, D><<<(unsigned)((blh * p->S_max + kProtoWarps - 1) / kProtoWarps),
+                         32 * kProtoWarps, 0, s>>>(*p, a, a.proto);
     nu_finish_slots_kernel<<<(unsigned)((blh + 127) / 128), 128, 0, s>>>(*p, a);
     ++launches;
     if (timed) phase_mark(5, s);
