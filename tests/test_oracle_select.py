@@ -149,7 +149,7 @@ def test_heap_greedy_equals_scan_and_effective_key(seed, budget_frac):
     assert ((t1 & ~pre) * cost).sum() == spent <= rem
 
 
-def floor_prefix(r, sens, bounds, cost, cap_entries, cap_tokens):
+def floor_prefix(r, sens, bounds, cost, cap_entries, cap_tokens, cuts=None):
     """Floor in prefix form: within the stop prefix every earlier candidate was
     taken, so a candidate's cost is fixed by which groups it opens first."""
     L, H, n = r.shape
@@ -170,7 +170,7 @@ def floor_prefix(r, sens, bounds, cost, cap_entries, cap_tokens):
         if cap_tokens >= 0 and tokens >= cap_tokens:
             break
         s = int(np.searchsorted(bounds, i, side="right") - 1)
-        leaf, path = _path(i, bounds, s)
+        leaf, path = _path(i, bounds, s, None if cuts is None else cuts[l, h, s])
         groups = [(l, h, s, j) for j in path]
         if (l, h, s, leaf) in seen:
             continue
@@ -189,8 +189,8 @@ def floor_prefix(r, sens, bounds, cost, cap_entries, cap_tokens):
     return taken, spent, tokens
 
 
-def _path(i, bounds, s):
-    nodes = O.tree_nodes(int(bounds[s]), int(bounds[s + 1]))
+def _path(i, bounds, s, cuts=None):
+    nodes = O.tree_nodes(int(bounds[s]), int(bounds[s + 1]), cuts)
     j = 0
     path = [0]
     while j < 7:
@@ -212,6 +212,36 @@ def test_floor_equals_prefix_form(seed, cap, cap_tokens):
     assert (sp, tk) == (sp2, tk2)
     assert sp <= cap and (cap_tokens < 0 or tk <= cap_tokens)
     assert (t1 * cost).sum() == sp
+    _tree_closed(t1)
+
+
+@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("cap", [5, 23, 400])
+def test_floor_equals_prefix_form_on_curvature_trees(seed, cap):
+    """The same cross-check on curvature-chosen trees (reading R18): every
+    (l, h) has its own cuts, the leaf split costs follow the leaves' sizes."""
+    util, cost, r, bounds, n = _instance(seed)
+    rng = np.random.default_rng(100 + seed)
+    L, H, S = cost.shape[:3]
+    cuts = np.zeros((L, H, S, 7), dtype=np.int64)
+    for l in range(L):
+        for h in range(H):
+            kap = rng.uniform(0, 0.2, n) + (rng.uniform(size=n) < 0.1) * 1.5
+            cuts[l, h] = O.slot_cuts(kap, bounds)
+            for s_ in range(S):
+                nodes = O.tree_nodes(int(bounds[s_]), int(bounds[s_ + 1]), cuts[l, h, s_])
+                for j in range(7, 15):
+                    cost[l, h, s_, 1 + j] = nodes[j][1] - nodes[j][0] - 1
+    mid = np.asarray([[(a + b) // 2 for a, b in O.tree_nodes(int(bounds[k]), int(bounds[k + 1]))[:7]]
+                      for k in range(S)])
+    assert (cuts != mid[None, None]).any()                 # not all midpoint trees
+    sens = np.ones((L, H), np.float32)
+    t1 = np.zeros(cost.shape, dtype=bool)
+    sp, tk = O.singleton_floor(r, sens, bounds, cost, cap, -1, t1, cuts)
+    t2, sp2, tk2 = floor_prefix(r, sens, bounds, cost, cap, -1, cuts)
+    np.testing.assert_array_equal(t1, t2)
+    assert (sp, tk) == (sp2, tk2)
+    assert (t1 * cost).sum() == sp <= cap
     _tree_closed(t1)
 
 
