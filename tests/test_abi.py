@@ -64,3 +64,17 @@ def test_binding_argument_counts_match_header(lib):
     for name, args in re.findall(r"\b(kvc_[a-z_0-9]+)\s*\(([^)]*)\)\s*;", src):
         n = 0 if args.strip() in ("", "void") else len(args.split(","))
         assert len(getattr(lib, name).argtypes) == n, name
+
+
+def test_tree_cuts_rejects_bad_arguments_on_the_host(lib):
+    """kvc_tree_cuts checks its arguments before touching the device: missing
+    pointers and more than 65535 (b,l,h) give KVC_EINVAL (no GPU needed)."""
+    from kv_cache_compression_probe_gb300 import kvc
+    p = kvc.make_params(B=1, L=2, H=2, G=4, d=128, P=64, W=128, dtype=kvc.KVC_BF16, n_max=4096,
+                        S_max=64)
+    fake = [ctypes.c_void_p(256 * (k + 1)) for k in range(8)]   # never dereferenced
+    assert lib.kvc_tree_cuts(ctypes.byref(p), None, *fake[1:], None) == kvc.KVC_EINVAL
+    assert lib.kvc_tree_cuts(ctypes.byref(p), *fake[:7], None, None) == kvc.KVC_EINVAL
+    big = kvc.make_params(B=1, L=300, H=256, G=1, d=128, P=64, W=128, dtype=kvc.KVC_BF16,
+                          n_max=4096, S_max=64)
+    assert lib.kvc_tree_cuts(ctypes.byref(big), *fake, None) == kvc.KVC_EINVAL
