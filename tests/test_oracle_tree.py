@@ -184,3 +184,46 @@ def test_head_utilities_gain_range():
         Rv = np.array([res.r[a:b].sum() for a, b in nodes])
         g = gains[s] / np.r_[Rv[0], Rv]
         assert (g >= -1e-15).all() and (g <= 1 + 1e-12).all()
+
+
+def _scored(K, V, Q, n, P, bounds):
+    # no hops: relevance is the probe attention alone, which involves no values
+    return O.score_and_value_head(K, V, Q, n, P, bounds, 1.0, n_hops=0)
+
+
+def test_distortion_and_utilities_invariant_to_value_scale():
+    """The value term divides by the mean value norm (R4), so scaling every
+    value by the same factor changes no distortion, gain or utility.  A
+    missing or misplaced normalisation fails this."""
+    rng = np.random.default_rng(21)
+    n, d, G, P = 260, 32, 2, 8
+    K = rng.standard_normal((n, d)); V = rng.standard_normal((n, d)); Q = rng.standard_normal((G, P, d))
+    bounds = np.array([0, 40, 100, 170, 230])
+    a = _scored(K, V, Q, n, P, bounds)
+    b = _scored(K, 3.5 * V, Q, n, P, bounds)
+    np.testing.assert_allclose(b.D, a.D, rtol=1e-10, atol=1e-14)
+    np.testing.assert_allclose(b.Ddrop, a.Ddrop, rtol=1e-10, atol=1e-14)
+    np.testing.assert_allclose(b.util, a.util, rtol=1e-9, atol=1e-14)
+    np.testing.assert_array_equal(b.cost, a.cost)
+
+
+@pytest.mark.parametrize("shift", [1, 37, 1000])
+def test_distortion_invariant_to_a_common_rope_shift(shift):
+    """Rotating every key and every probe by the same RoPE shift leaves the
+    probe attention unchanged (it depends on position differences) and rotates
+    each prototype key with its tokens, so every distortion and utility is
+    unchanged: the path sees keys and probes only through relative rotations.
+    (A wrong sign of the merge's own rotations keeps this property; the
+    one-token and identical-key prototype pins catch that.)"""
+    rng = np.random.default_rng(22)
+    n, d, G, P = 260, 32, 2, 8
+    K = _rot(rng.standard_normal((n, d)), np.arange(n))
+    V = rng.standard_normal((n, d))
+    Q = rng.standard_normal((G, P, d))
+    bounds = np.array([0, 40, 100, 170, 230])
+    a = _scored(K, V, Q, n, P, bounds)
+    b = _scored(_rot(K, float(shift)), V, _rot(Q, float(shift)), n, P, bounds)
+    np.testing.assert_allclose(b.lse, a.lse, rtol=1e-10)
+    np.testing.assert_allclose(b.D, a.D, rtol=1e-8, atol=1e-12)
+    np.testing.assert_allclose(b.Ddrop, a.Ddrop, rtol=1e-8, atol=1e-12)
+    np.testing.assert_allclose(b.util, a.util, rtol=1e-7, atol=1e-12)
