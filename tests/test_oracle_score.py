@@ -197,3 +197,21 @@ def test_two_hop_chain_raises_bridge_relevance():
             assert res.r[i] - alpha[i] >= 0.3 * alpha[a] * mass[i] * (1 - 1e-9)
             checked += 1
     assert checked > 0
+
+
+def test_second_hop_seeds_follow_the_first_hop():
+    """Hand-built case (R2: hop k seeds from r^(k-1)): token 0 has the largest
+    alpha and its value points at token 1's key, so hop 1 moves most of token
+    0's relevance onto token 1 (r^1_1 = 0.35 + 0.3 * 0.40 > r^1_0 = 0.40 + ~0);
+    with one seed per hop, hop 2 must seed from token 1, not token 0."""
+    alpha = np.array([0.40, 0.35, 0.10, 0.10, 0.05])
+    K = np.zeros((5, 2)); K[1] = [10.0, 0.0]
+    V = np.zeros((5, 2)); V[0] = [10.0, 0.0]
+    r, seeds = O.hop_relevance(alpha, K, V, 1, 0.3, 2)
+    assert list(seeds[0]) == [0] and list(seeds[1]) == [1]
+    # brute force: hop 1 from seed 0, hop 2 from seed 1 (v_1 = 0: uniform softmax)
+    sm0 = np.exp(K @ V[0] / np.sqrt(2)); sm0 /= sm0.sum()
+    r1 = alpha + 0.3 * alpha[0] * sm0
+    assert r1[1] > r1[0]
+    r2 = alpha + 0.3 * r1[1] * np.full(5, 0.2)
+    np.testing.assert_allclose(r, r2, rtol=1e-12)
