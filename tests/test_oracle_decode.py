@@ -130,3 +130,14 @@ def test_partition_recovers_planted_turns():
     inner = planted[1:-1]
     hit = [np.abs(cuts - p).min() <= 2 for p in inner]
     assert np.mean(hit) >= 0.95
+
+
+def test_partition_default_lambda_hand_worked():
+    """kappa = 1 everywhere on [0, 64): the default lambda is the mean curvature,
+    1.  Four 16-token slots gain 3 cuts and pay 4 * ((16 - 64)/64)^2 = 2.25:
+    +0.75; two 32-token slots 1 - 2 * 0.25 = +0.5; one slot 0; three slots at
+    most 2 - 1.33 = +0.67.  So the default gives four slots, while lambda = 2
+    (four slots -1.5, two slots 0, one slot 0) keeps the single slot."""
+    k = np.ones(80)
+    np.testing.assert_array_equal(O.partition_dp(k, 64), [0, 16, 32, 48, 64])
+    np.testing.assert_array_equal(O.partition_dp(k, 64, lam=2.0), [0, 64])

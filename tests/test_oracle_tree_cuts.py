@@ -165,3 +165,14 @@ def test_curvature_trees_keep_pack_and_floor_invariants():
             assert nodes[leaf][0] <= i < nodes[leaf][1] and path[-1] == leaf
             assert all(nodes[a][0] <= nodes[b][0] and nodes[b][1] <= nodes[a][1]
                        for a, b in zip(path, path[1:]))
+
+
+def test_sixteen_token_slot_is_always_the_midpoint_tree():
+    """Leaves keep at least 2 tokens (R18), so a 16-token slot (8 leaves) has
+    exactly one valid tree, the midpoint tree, whatever the curvature: a turn
+    at token 5 that would win with 1-token leaves (root children of 5 and 11)
+    cannot move the root cut from 8."""
+    k = np.zeros(20)
+    k[5] = 1.0
+    for dtype in (np.float64, np.float32):
+        assert O.tree_cuts(k, 0, 16, dtype) == [8, 4, 12, 2, 6, 10, 14]
