@@ -291,6 +291,7 @@ class HeadResult:
     D: np.ndarray        # [S, 15]
     Ddrop: np.ndarray    # [S, 15]
     protos: Optional[List[List[Prototype]]] = None
+    Rv: Optional[np.ndarray] = None   # [S, 15] node values R(N), as used by the ops
 
 
 def score_and_value_head(Kh, Vh, Qh, n: int, P: int, bounds: np.ndarray, sens: float,
@@ -313,6 +314,7 @@ def score_and_value_head(Kh, Vh, Qh, n: int, P: int, bounds: np.ndarray, sens: f
     util = np.zeros((S, N_OPS))
     cost = np.zeros((S, N_OPS), dtype=np.int64)
     Dall = np.zeros((S, N_NODES))
+    Rall = np.zeros((S, N_NODES))
     Ddall = np.zeros((S, N_NODES))
     protos_all = []
     for s in range(S):
@@ -331,11 +333,11 @@ def score_and_value_head(Kh, Vh, Qh, n: int, P: int, bounds: np.ndarray, sens: f
             sizes[j] = y - x
             plist.append(pr)
         util[s], cost[s] = slot_ops(D, Dd, Rv, sizes, sens)
-        Dall[s], Ddall[s] = D, Dd
+        Dall[s], Ddall[s], Rall[s] = D, Dd, Rv
         if keep_protos:
             protos_all.append(plist)
     return HeadResult(lse=sc.lse, feats=sc.feats, r=r, seeds=seeds, util=util, cost=cost,
-                      D=Dall, Ddrop=Ddall, protos=protos_all if keep_protos else None)
+                      D=Dall, Ddrop=Ddall, protos=protos_all if keep_protos else None, Rv=Rall)
 
 
 # =============================================================================== f3: curvature-chosen trees

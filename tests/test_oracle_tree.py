@@ -227,3 +227,44 @@ def test_distortion_invariant_to_a_common_rope_shift(shift):
     np.testing.assert_allclose(b.D, a.D, rtol=1e-8, atol=1e-12)
     np.testing.assert_allclose(b.Ddrop, a.Ddrop, rtol=1e-8, atol=1e-12)
     np.testing.assert_allclose(b.util, a.util, rtol=1e-7, atol=1e-12)
+
+
+def test_node_values_add_up_the_tree_and_feed_the_utilities():
+    """[GK] "03 Bottom-up value flow": a node's value is the sum of its tokens'
+    relevance, so a parent's value equals the sum of its children's, the
+    root's the slot's total; and each op's utility is that value times its
+    gain (times sens) per new entry."""
+    rng = np.random.default_rng(23)
+    n, d, G, P = 260, 32, 2, 8
+    K = rng.standard_normal((n, d)); V = rng.standard_normal((n, d)); Q = rng.standard_normal((G, P, d))
+    bounds = np.array([0, 40, 100, 170, 230])
+    res = O.score_and_value_head(K, V, Q, n, P, bounds, 0.7)
+    for s in range(4):
+        Rv = res.Rv[s]
+        x0, y0 = int(bounds[s]), int(bounds[s + 1])
+        np.testing.assert_allclose(Rv[0], res.r[x0:y0].sum(), rtol=1e-12)
+        for j in range(7):
+            np.testing.assert_allclose(Rv[j], Rv[2 * j + 1] + Rv[2 * j + 2], rtol=1e-12)
+        for j in range(7, 15):
+            a, b = O.tree_nodes(x0, y0)[j]
+            np.testing.assert_allclose(Rv[j], res.r[a:b].sum(), rtol=1e-12)
+        g_add = O.gain_fraction(res.Ddrop[s, 0] - res.D[s, 0], res.Ddrop[s, 0])
+        np.testing.assert_allclose(res.util[s, 0], Rv[0] * g_add * 0.7, rtol=1e-12)
+        for j in range(15):
+            num = res.D[s, j] - res.D[s, 2 * j + 1] - res.D[s, 2 * j + 2] if j < 7 else res.D[s, j]
+            g = O.gain_fraction(num, res.Ddrop[s, j])
+            np.testing.assert_allclose(res.util[s, 1 + j], Rv[j] * g * 0.7 / res.cost[s, 1 + j],
+                                       rtol=1e-12, atol=1e-300)
+
+
+def test_coherence_is_the_mean_cosine_to_the_mean_hand_worked():
+    """R7: kappa = mean over tokens of cos(unrotated key, unrotated mean).  Two
+    tokens with unrotated keys (1, 0) and (0, 3): the mean is (0.5, 1.5), the
+    cosines are 1/sqrt(10) and 3/sqrt(10), so kappa = 2/sqrt(10) and
+    m = 2 * kappa = 4/sqrt(10) (|mean| / mean |k| would give 0.79 instead)."""
+    u = np.array([[1.0, 0.0], [0.0, 3.0]])
+    x = 5
+    K = _rot(u, np.arange(x, x + 2))
+    pr = O.prototype(K, np.zeros((2, 2)), np.ones(2), x, x + 2, 10000.0, 0.1)
+    assert abs(pr.kappa - 2 / math.sqrt(10)) < 1e-12
+    assert abs(pr.m - 4 / math.sqrt(10)) < 1e-12
