@@ -421,3 +421,16 @@ def test_hybrid_leaving_no_budget_keeps_only_the_other_windows():
     np.testing.assert_array_equal(sel.lens[full], n)
     np.testing.assert_array_equal(sel.lens[~full], W)
     assert not sel.taken[~full].any()
+
+
+def test_floor_never_spends_beyond_the_allocatable_budget(tiny_scored):
+    """The floor cap is a hard maximum within the budget ([GK] technical details:
+    the singleton cap is a maximum, not a guaranteed spend); even a cap fraction
+    above 1 and no token cap cannot make the floor spend more than B_alloc."""
+    cfg, wl, seq, scored = tiny_scored
+    for beta in (0.15, 0.3):
+        sel = _select(cfg, seq, wl.head_sens, scored, budget_ratio=beta, floor_cap_frac=1.5,
+                      floor_cap_tokens=-1)
+        assert sel.floor_spent <= sel.B_alloc
+        assert sel.lens.sum() <= sel.B_tot
+        _tree_closed(sel.taken)

@@ -268,3 +268,19 @@ def test_coherence_is_the_mean_cosine_to_the_mean_hand_worked():
     pr = O.prototype(K, np.zeros((2, 2)), np.ones(2), x, x + 2, 10000.0, 0.1)
     assert abs(pr.kappa - 2 / math.sqrt(10)) < 1e-12
     assert abs(pr.m - 4 / math.sqrt(10)) < 1e-12
+
+
+def test_distortion_is_a_mean_over_probe_rows():
+    """R4 averages over the probe rows: duplicating every probe row (same query,
+    same attention, same LSE) leaves D and D_drop unchanged."""
+    e1, e2 = np.array([1.0, 0.0]), np.array([0.0, 1.0])
+    Kpost = np.stack([e1, _rot(e2, 1.0), _rot(e1, 2.0), _rot(e2, 3.0)])
+    V = np.stack([e1, e2, e1, e2])
+    q = np.array([[0.3, -0.2]])
+    sc = O.score_head(Kpost, V, q.reshape(1, 1, 2), 4, 1)
+    pr = O.prototype(Kpost[0:2], V[0:2], np.array([1.0, 0.5]), 0, 2, 10000.0, 0.1)
+    nu = float(sc.feats[:, 1].mean())
+    D1, Dd1 = O.node_distortion(sc.a[:, 0:2], V[0:2], q, sc.lse, pr, nu, 0.25, 0.75)
+    D2, Dd2 = O.node_distortion(np.repeat(sc.a[:, 0:2], 2, axis=0), V[0:2], np.repeat(q, 2, axis=0),
+                                np.repeat(sc.lse, 2), pr, nu, 0.25, 0.75)
+    assert abs(D2 - D1) < 1e-14 and abs(Dd2 - Dd1) < 1e-14
