@@ -141,3 +141,17 @@ def test_partition_default_lambda_hand_worked():
     k = np.ones(80)
     np.testing.assert_array_equal(O.partition_dp(k, 64), [0, 16, 32, 48, 64])
     np.testing.assert_array_equal(O.partition_dp(k, 64, lam=2.0), [0, 64])
+
+
+def test_curvature_zero_chord_convention():
+    """R1: a zero chord (a repeated state) counts as no turn (cos = 1): a
+    trajectory that stays put has kappa = 0 everywhere, and a single repeated
+    state inside a great-circle walk adds nothing at scale 1 there."""
+    h = np.tile(np.array([0.3, -1.2, 0.5]), (24, 1))
+    np.testing.assert_array_equal(O.curvature(h), 0.0)
+    ang = 0.2 * np.arange(24.0)
+    g = np.stack([np.cos(ang), np.sin(ang), np.zeros(24)], axis=1)
+    g[12] = g[11]                                       # repeat: chord 11 -> 12 is zero
+    k1 = O.curvature(g, scales=(1,))
+    assert k1[12] == 0.0 and k1[11] == 0.0             # both involve the zero chord
+    np.testing.assert_allclose(k1[5], 1 - np.cos(0.2), rtol=1e-9)

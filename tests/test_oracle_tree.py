@@ -284,3 +284,34 @@ def test_distortion_is_a_mean_over_probe_rows():
     D2, Dd2 = O.node_distortion(np.repeat(sc.a[:, 0:2], 2, axis=0), V[0:2], np.repeat(q, 2, axis=0),
                                 np.repeat(sc.lse, 2), pr, nu, 0.25, 0.75)
     assert abs(D2 - D1) < 1e-14 and abs(Dd2 - Dd1) < 1e-14
+
+
+def test_value_norm_scale_is_the_mean_over_the_head():
+    """R4: the value term divides by nu_bar, the mean |v| over the (l, h)'s
+    tokens.  Values of unequal norms (every fourth token 5x longer) make the
+    mean differ from other summaries; the head's distortions equal the node
+    distortions recomputed with that mean."""
+    rng = np.random.default_rng(24)
+    n, d, G, P = 200, 16, 2, 8
+    K = rng.standard_normal((n, d)); V = rng.standard_normal((n, d)); Q = rng.standard_normal((G, P, d))
+    V[::4] *= 5.0
+    bounds = np.array([0, 48, 100, 160])
+    res = O.score_and_value_head(K, V, Q, n, P, bounds, 1.0, n_hops=0)
+    nu = float(np.linalg.norm(V, axis=1).mean())
+    sc = O.score_head(K, V, Q, n, P)
+    q = Q.reshape(G * P, d)
+    for s in range(3):
+        for j, (x, y) in enumerate(O.tree_nodes(int(bounds[s]), int(bounds[s + 1]))):
+            pr = O.prototype(K[x:y], V[x:y], res.r[x:y], x, y, 10000.0, 0.1)
+            D, Dd = O.node_distortion(sc.a[:, x:y], V[x:y], q, sc.lse, pr, nu, 0.25, 0.75)
+            assert abs(res.D[s, j] - D) <= 1e-12 * max(1.0, abs(D))
+            assert abs(res.Ddrop[s, j] - Dd) <= 1e-12 * max(1.0, abs(Dd))
+
+
+def test_default_hop_seed_count_is_the_probe_count():
+    """R2: each hop seeds from the P tokens (the probe count) of largest relevance."""
+    rng = np.random.default_rng(25)
+    n, d, G, P = 120, 16, 2, 8
+    K = rng.standard_normal((n, d)); V = rng.standard_normal((n, d)); Q = rng.standard_normal((G, P, d))
+    res = O.score_and_value_head(K, V, Q, n, P, np.array([0, 48, 96]), 1.0)
+    assert [len(s) for s in res.seeds] == [P, P]
