@@ -434,3 +434,12 @@ def test_floor_never_spends_beyond_the_allocatable_budget(tiny_scored):
         assert sel.floor_spent <= sel.B_alloc
         assert sel.lens.sum() <= sel.B_tot
         _tree_closed(sel.taken)
+
+
+def test_offsets_hand_worked():
+    """Packed layout: capacity = length + decode reserve per (b, l, h), offsets
+    the exclusive prefix sum of the capacities in (b, l, h) order.  Lengths
+    (3, 5, 2, 4) with reserve 2: capacities (5, 7, 4, 6), offsets (0, 5, 12, 16)."""
+    caps, offs = O.offsets(np.array([[[3, 5], [2, 4]]]), 2)
+    np.testing.assert_array_equal(caps.reshape(-1), [5, 7, 4, 6])
+    np.testing.assert_array_equal(offs.reshape(-1), [0, 5, 12, 16])
