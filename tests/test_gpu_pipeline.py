@@ -254,18 +254,24 @@ def test_compression_graph_replay_equals_eager(built):
     assert comp.graph_launches > 0
 
 
-def test_compress_from_host_equals_compress(built):
+@pytest.mark.parametrize("tree_cuts", [False, True])
+def test_compress_from_host_equals_compress(built, tree_cuts):
     """Compressor.compress_from_host (layer chunks copied on a second stream while
     earlier chunks are scored) gives exactly the outputs of copying everything
-    first and calling compress()."""
+    first and calling compress(); with curvature-chosen trees each chunk cuts
+    its own layers' trees into its slice of the cut table."""
     from kv_cache_compression_probe_gb300 import kvc
     cfg = W.small_config(B=1, L=4, H=2, n=1500, n_min=1500)
     wl = W.make_workload(cfg)
-    p, comp, d, S_max = upload_workload(wl, tensor_cores=True)
+    p, comp, d, S_max = upload_workload(wl, tensor_cores=True, tree_cuts=tree_cuts)
     comp.compress(d["K"], d["V"], d["Qp"], d["bounds"], d["n_slots"], d["sens"])
     torch.cuda.synchronize()
+    assert kvc.kvc_device_error() == 0
     ref = [t.clone() for t in (comp.lse, comp.feats, comp.op_util, comp.taken, comp.len_lh,
                                comp.Kp, comp.Vp, comp.logm, comp.pos)]
+    if tree_cuts:
+        ref += [comp.cuts.clone(), comp.tree_kappa.clone()]
+        comp.cuts.zero_()
     h = [t.cpu().pin_memory() for t in (d["K"], d["V"], d["Qp"])]
     K2, V2, Q2 = (torch.zeros_like(d["K"]), torch.zeros_like(d["V"]), torch.zeros_like(d["Qp"]))
     comp.compress_from_host(h[0], h[1], h[2], K2, V2, Q2, d["bounds"], d["n_slots"], d["sens"],
@@ -273,7 +279,10 @@ def test_compress_from_host_equals_compress(built):
     torch.cuda.synchronize()
     assert kvc.kvc_device_error() == 0
     assert torch.equal(K2, d["K"]) and torch.equal(V2, d["V"]) and torch.equal(Q2, d["Qp"])
-    got = (comp.lse, comp.feats, comp.op_util, comp.taken, comp.len_lh, comp.Kp, comp.Vp,
-           comp.logm, comp.pos)
+    got = [comp.lse, comp.feats, comp.op_util, comp.taken, comp.len_lh, comp.Kp, comp.Vp,
+           comp.logm, comp.pos]
+    if tree_cuts:
+        got += [comp.cuts, comp.tree_kappa]
+    assert len(got) == len(ref)
     for a, b in zip(ref, got):
         assert torch.equal(a, b)
