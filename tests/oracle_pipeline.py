@@ -79,3 +79,46 @@ def pack_all(wl, taken_list, r_list, cfg=None):
                 lens[b, l, h] = len(K)
     caps, offs = O.offsets(lens, cfg.decode_reserve)
     return ent, lens, caps, offs
+
+
+def _score_job(job):
+    """One (layer, KV head) of the oracle's scoring, in a worker process."""
+    l, h, K, V, Q, n, P, bounds, sens, kw = job
+    res = O.score_and_value_head(K, V, Q, n, P, bounds, sens, **kw)
+    return l, h, res.util, res.cost, res.r
+
+
+_BLAS_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+
+
+def score_sequence_parallel(wl, b, processes):
+    """The oracle's float64 scoring of every (layer, KV head) of sequence b, spread
+    over a spawn process pool with one BLAS thread per worker.  Returns
+    (util [L, H, S, 16] float64, cost [L, H, S, 16], r [L, H, n])."""
+    import multiprocessing as mp
+    import os
+    cfg = wl.cfg
+    s = wl.seqs[b]
+    S = len(s.slot_bounds) - 1
+    kw = dict(base=cfg.rope_base, hop_weight=cfg.hop_weight, n_hops=cfg.n_hops,
+              w_part=cfg.w_part, w_value=cfg.w_value, value_floor=cfg.value_floor)
+    jobs = [(l, h, s.K[l, h], s.V[l, h], s.Qp[l, h * cfg.G:(h + 1) * cfg.G], s.n, cfg.P,
+             s.slot_bounds, float(wl.head_sens[l, h]), kw)
+            for l in range(cfg.L) for h in range(cfg.H)]
+    util = np.zeros((cfg.L, cfg.H, S, 16))
+    cost = np.zeros((cfg.L, cfg.H, S, 16), dtype=np.int64)
+    r = np.zeros((cfg.L, cfg.H, s.n))
+    saved = {k: os.environ.get(k) for k in _BLAS_VARS}
+    os.environ.update({k: "1" for k in _BLAS_VARS})
+    try:
+        pool = mp.get_context("spawn").Pool(max(1, processes))
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    with pool:
+        for l, h, u, c, rr in pool.imap_unordered(_score_job, jobs):
+            util[l, h], cost[l, h], r[l, h] = u, c, rr
+    return util, cost, r

@@ -7,13 +7,18 @@ checks that hold at any size:
   * the selection of every sequence, bit-exact against the oracle run on the
     device's fp32 keys (the budget couples every pair of a sequence, so the
     whole sequence is compared), with lengths, capacities and offsets;
+  * on the 16K Mistral-shaped workload, end to end: the oracle's own float64
+    scoring of all 256 (layer, KV head) pairs (a spawn process pool), then its
+    selection; the device's taken set must equal it up to near-ties (keys
+    within 1e-6 relative, resolved in the device's order), which are counted;
   * the packed entries of the sampled pairs (oracle pack of the device's
     taken set) and every decode output of theirs over all decode steps.
 The long-context case takes its slots from the device's curvature partition
-(checked against the oracle first).  The serving batch keeps its 64 sequences
-and their context mix but runs 2 of the 32 layers: its full K/V (86 GB in
-bf16, twice that as the host's fp32 arrays) is beyond what a test generates.
+(checked against the oracle first).  The serving batch (90 GB of K and V) has
+its own test with inputs generated on the device
+(tests/test_gpu_full_size_serving.py).
 """
+import json
 import os
 
 import numpy as np
@@ -27,11 +32,17 @@ from tests.gpu_helpers import (assert_bf16_close, assert_f32_close, dev, params_
 
 pytestmark = [pytest.mark.gpu, pytest.mark.gpu_full]
 
+# the kernels whose results the end-to-end selection report depends on
+PARITY_SOURCES = ("kv_cache_compression_probe_gb300/csrc/kvc_score.cu",
+                  "kv_cache_compression_probe_gb300/csrc/kvc_score_tc.cu",
+                  "kv_cache_compression_probe_gb300/csrc/kvc_select.cu",
+                  "kv_cache_compression_probe_gb300/csrc/kvc_common.cuh")
+
 CASES = {
-    "mistral16k": dict(cfg=lambda: W.get_config("mistral16k"), heads=[(0, 0, 0), (0, 17, 5)]),
+    "mistral16k": dict(cfg=lambda: W.get_config("mistral16k"), heads=[(0, 0, 0), (0, 17, 5)],
+                       end_to_end=True),
     "aggressive": dict(cfg=lambda: W.get_config("aggressive"), heads=[(0, 3, 2)]),
     "long": dict(cfg=lambda: W.get_config("long"), heads=[(1, 9, 4)], partition=True),
-    "serving": dict(cfg=lambda: W.get_config("serving").replace(L=2), heads=[(0, 0, 0), (37, 1, 6)]),
 }
 
 
@@ -104,6 +115,44 @@ def _check_head_scores(cfg, wl, b, l, h, lse, feats, rel, util, cost):
         assert (err <= 1e-5 * np.maximum(np.abs(o), 3 * scale)).all(), (tag, k, err.max())
 
 
+def _end_to_end_selection(name, cfg, wl, util, cost, rel, taken):
+    """The device's taken set against the oracle chain's own (float64 scoring of
+    every (l,h), then its floor and auction), up to near-ties of 1e-6 relative.
+    With KVC_PARITY_REPORT set, the counts are written there as JSON."""
+    from tests.oracle_pipeline import score_sequence_parallel
+    from tests.tie_check import TIE_REL, band_needed, check_sequence
+    report = {"workload": name, "tie_band_rel": TIE_REL, "sequences": []}
+    for b, s in enumerate(wl.seqs):
+        S = len(s.slot_bounds) - 1
+        u64, c64, r64 = score_sequence_parallel(wl, b, _procs())
+        np.testing.assert_array_equal(cost[b, :, :, :S], c64)
+        args = (u64, util[b, :, :, :S], c64, r64, token_view(rel, wl, b), wl.head_sens,
+                taken[b, :, :, :S], s.slot_bounds, s.n, cfg)
+        try:
+            rep = check_sequence(*args)
+        except AssertionError as e:
+            raise AssertionError(f"{name}, sequence {b}: {e}; band needed: {band_needed(*args)}") from None
+        report["sequences"].append(dict(b=b, ops=int(c64.size), ties_reported=rep.diff_ops,
+                                        tie_runs_reordered=rep.runs_moved_util,
+                                        floor_tie_runs_reordered=rep.runs_moved_floor,
+                                        util_max_abs_err=rep.max_abs_err,
+                                        util_max_rel_err=rep.max_rel_err))
+    print(f"{name} end-to-end selection: {report}")
+    path = os.environ.get("KVC_PARITY_REPORT")
+    if path:
+        import hashlib
+        h = hashlib.sha256()
+        root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+        for f in PARITY_SOURCES:
+            h.update(open(os.path.join(root, f), "rb").read())
+        report["source_sha256"] = h.hexdigest()
+        report["source_files"] = list(PARITY_SOURCES)
+        report["command"] = ("KVC_PARITY_REPORT=<path> python -m pytest "
+                             "tests/test_gpu_full_size.py -k mistral16k -m gpu -q")
+        with open(path, "w") as f:
+            json.dump(report, f, indent=1)
+
+
 @pytest.mark.parametrize("name", list(CASES))
 def test_full_size_against_sampled_oracle(kvc, name):
     spec = CASES[name]
@@ -138,6 +187,8 @@ def test_full_size_against_sampled_oracle(kvc, name):
         assert int(sel.lens.sum()) - cfg.W * cfg.L * cfg.H <= sel.B_alloc
         want_lens[b] = sel.lens
     np.testing.assert_array_equal(lens, want_lens)
+    if spec.get("end_to_end"):
+        _end_to_end_selection(name, cfg, wl, util, cost, rel, taken)
     wc, wo = O.offsets(want_lens, cfg.decode_reserve)
     np.testing.assert_array_equal(caps, wc)
     np.testing.assert_array_equal(offs, wo)

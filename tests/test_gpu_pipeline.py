@@ -162,18 +162,30 @@ def test_pack_matches_oracle(case):
 
 def test_end_to_end_taken_set_against_oracle_chain(case):
     """The GPU chain's taken set equals the oracle chain's (float64 keys) except
-    for ops whose oracle keys are within 1e-6 relative of a competing key."""
+    where near-ties (keys within 1e-6 relative) fell the other way: the device's
+    set must be the oracle's selection under one resolution of those ties (the
+    device's own key order inside each near-tie run); every differing op is a
+    reported tie.  Any other difference fails."""
     cfg, wl, run, p, comp, d, S_max = case
-    from tests.oracle_pipeline import select_all
+    from tests.tie_check import band_needed, check_sequence
     comp.select(d["bounds"], d["n_slots"], d["sens"])
+    torch.cuda.synchronize()
     taken = comp.taken.cpu().numpy().astype(bool)
-    sels = select_all(wl, run.util, run.cost, run.r)
-    diffs = 0
+    util = comp.op_util.cpu().numpy()
+    rel = comp.relevance.cpu().numpy()
+    cost = comp.op_cost.cpu().numpy().astype(np.int64)
+    ties = 0
     for b, s in enumerate(wl.seqs):
         S = len(s.slot_bounds) - 1
-        diffs += int((taken[b, :, :, :S] != sels[b].taken).sum())
-    print(f"end-to-end taken-set differences (reported ties): {diffs}")
-    assert diffs <= max(2, int(0.001 * taken.size))
+        args = (run.util[b, :, :, :S], util[b, :, :, :S], cost[b, :, :, :S], run.r[b],
+                token_view(rel, wl, b), wl.head_sens, taken[b, :, :, :S], s.slot_bounds, s.n, cfg)
+        try:
+            rep = check_sequence(*args)
+        except AssertionError as e:
+            raise AssertionError(f"sequence {b}: {e}; band needed: {band_needed(*args)}") from None
+        assert not taken[b, :, :, S:].any()
+        ties += rep.diff_ops
+    print(f"end-to-end: taken bits differing from the oracle chain through 1e-6 ties: {ties}")
 
 
 def test_full_budget_packs_the_input_bit_exact(built):
