@@ -20,12 +20,13 @@ KVC_OK, KVC_EINVAL, KVC_EBUDGET, KVC_ECAPACITY = 0, -1, -2, -3
 KVC_ECUDA, KVC_ETIMEOUT, KVC_EWORKSPACE, KVC_EDEVICE, KVC_ESCRATCH = -4, -5, -6, -7, -8
 KVC_F32, KVC_BF16 = 0, 1
 KVC_WS_SCORE, KVC_WS_SELECT, KVC_WS_PACK, KVC_WS_DECODE, KVC_WS_PARTITION = range(5)
+KVC_DECODE_STATIC_SCRATCH_BYTES = 48 << 20   # the allocation-free decode's array (kvc.h)
 
 EXPORTED = ("kvc_status_string", "kvc_last_cuda_error", "kvc_device_error", "kvc_launch_count", "kvc_workspace_bytes",
             "kvc_rope_table", "kvc_score", "kvc_select", "kvc_merge_pack", "kvc_decode_attn",
             "kvc_partition", "kvc_decode_attn_noalloc", "kvc_decode_attn_lse", "kvc_token_alpha",
             "kvc_evict_workspace_bytes", "kvc_evict_topb", "kvc_set_phase_timing",
-            "kvc_score_phase_ms", "kvc_decode_attn_layers", "kvc_tree_cuts")
+            "kvc_score_phase_ms", "kvc_decode_attn_layers", "kvc_tree_cuts", "kvc_set_wait_limit")
 
 
 class kvc_params(ctypes.Structure):
@@ -68,6 +69,8 @@ def lib():
         L.kvc_last_cuda_error.argtypes = []; L.kvc_last_cuda_error.restype = ctypes.c_char_p
         L.kvc_device_error.argtypes = [vp, ctypes.POINTER(c_int32)]; L.kvc_device_error.restype = c_int
         L.kvc_launch_count.argtypes = []; L.kvc_launch_count.restype = c_int64
+        L.kvc_set_wait_limit.argtypes = [ctypes.c_uint64, c_int32]
+        L.kvc_set_wait_limit.restype = c_int
         L.kvc_workspace_bytes.argtypes = [c_int, _P]; L.kvc_workspace_bytes.restype = c_size_t
         L.kvc_rope_table.argtypes = [c_int32, c_float, c_int64, vp, vp, vp]
         L.kvc_rope_table.restype = c_int
@@ -152,6 +155,11 @@ def kvc_device_error(stream=None) -> int:
 
 def kvc_launch_count() -> int:
     return int(lib().kvc_launch_count())
+
+
+def kvc_set_wait_limit(first_wait_ns: int, withhold_copies: bool = False):
+    _check(lib().kvc_set_wait_limit(int(first_wait_ns), 1 if withhold_copies else 0),
+           "kvc_set_wait_limit")
 
 
 def kvc_workspace_bytes(which: int, p: kvc_params) -> int:

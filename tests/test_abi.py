@@ -78,3 +78,15 @@ def test_tree_cuts_rejects_bad_arguments_on_the_host(lib):
     big = kvc.make_params(B=1, L=300, H=256, G=1, d=128, P=64, W=128, dtype=kvc.KVC_BF16,
                           n_max=4096, S_max=64)
     assert lib.kvc_tree_cuts(ctypes.byref(big), *fake, None) == kvc.KVC_EINVAL
+
+
+def test_binding_constants_match_header():
+    """Status codes and the allocation-free decode's scratch size agree with kvc.h."""
+    from kv_cache_compression_probe_gb300 import kvc
+    src = open(os.path.join(ROOT, "include", "kvc.h")).read()
+    defs = dict(re.findall(r"#define\s+(KVC_[A-Z_0-9]+)\s+(\S.*?)\s*(?:/\*.*)?$", src, flags=re.M))
+    for name in ("KVC_OK", "KVC_EINVAL", "KVC_EBUDGET", "KVC_ECAPACITY", "KVC_ECUDA",
+                 "KVC_ETIMEOUT", "KVC_EWORKSPACE", "KVC_EDEVICE", "KVC_ESCRATCH"):
+        assert int(defs[name]) == getattr(kvc, name), name
+    m = re.fullmatch(r"\((\d+)u\s*<<\s*(\d+)\)", defs["KVC_DECODE_STATIC_SCRATCH_BYTES"])
+    assert int(m.group(1)) << int(m.group(2)) == kvc.KVC_DECODE_STATIC_SCRATCH_BYTES
