@@ -134,6 +134,22 @@ int kvc_device_error(void* stream, int32_t* code /* host */);
 /* Number of kernels this library has launched since load (host counter). */
 int64_t kvc_launch_count(void);
 
+/* Bounded device waits (no counterpart on the pages: error handling of this
+ * library).  Kernels that pipeline copies and tensor-core products through
+ * mbarriers (the tensor-core passes of kvc_score, both decode kernels of the
+ * kvc_decode_attn family) give up a wait after first_wait_ns nanoseconds of
+ * global time: the CTA then stops issuing work, waits (with its own fixed
+ * limits: 2 s for copies and products already issued, 0.1 s in the probe
+ * passes) for what it has in flight, frees its tensor memory, records
+ * KVC_ETIMEOUT in the device error word and returns; the call's outputs are
+ * then unspecified, and a decode workspace must be zeroed again before its
+ * next use.  Default 2e9 ns; accepted range 1e3 .. 2e9.  withhold_copies != 0
+ * makes those kernels' producers issue no copies at all, so that their
+ * consumers' first waits can only end by the limit: a test of the timeout
+ * path that needs no fault.  Process-wide settings read at each launch; set
+ * them only while no call is in flight.  Returns KVC_OK or KVC_EINVAL. */
+int kvc_set_wait_limit(uint64_t first_wait_ns, int32_t withhold_copies);
+
 /* Bytes of workspace `which` (KVC_WS_*) needs for this parameter block.  The
  * workspace must be 256-byte aligned device memory; its contents need not be
  * initialised except for KVC_WS_DECODE, which must be zeroed once before its

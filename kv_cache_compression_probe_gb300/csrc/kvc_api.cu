@@ -28,6 +28,11 @@ static int32_t* g_err_ptr[256];
 
 void count_launch(int64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
+static std::atomic<uint64_t> g_wait_ns{kWaitNs};
+static std::atomic<int> g_withhold{0};
+uint64_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+int withhold_copies() { return g_withhold.load(std::memory_order_relaxed); }
+
 // Last CUDA runtime error seen by any call (diagnostics for KVC_ECUDA).
 std::atomic<int> g_last_cuda_error{0};
 int cuda_status(cudaError_t e) {
@@ -114,6 +119,13 @@ int kvc_device_error(void* stream, int32_t* code) {
 }
 
 int64_t kvc_launch_count(void) { return kvc::g_launches.load(); }
+
+int kvc_set_wait_limit(uint64_t first_wait_ns, int32_t withhold_copies) {
+  if (first_wait_ns < 1000 || first_wait_ns > kvc::kWaitNs) return KVC_EINVAL;
+  kvc::g_wait_ns.store(first_wait_ns, std::memory_order_relaxed);
+  kvc::g_withhold.store(withhold_copies ? 1 : 0, std::memory_order_relaxed);
+  return KVC_OK;
+}
 
 size_t kvc_workspace_bytes(int which, const kvc_params* p) {
   if (kvc::check_params(p) != KVC_OK) return 0;

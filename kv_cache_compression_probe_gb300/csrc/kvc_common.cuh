@@ -24,6 +24,13 @@ int check_params(const kvc_params* p);
 // Streaming multiprocessors of the current device (queried once per device; 0
 // when the query fails).
 int sm_count();
+// Give-up limit (ns) of the first wait of every pipeline stage in the kernels
+// with mbarrier pipelines, and whether their producers withhold their copies;
+// set by kvc_set_wait_limit (defaults: kWaitNs, 0).  Drains after an abort keep
+// their own limits.
+uint64_t wait_limit_ns();
+int withhold_copies();
+constexpr uint64_t kWaitNs = 2000000000ull;
 
 inline int64_t lh_count(const kvc_params* p) { return (int64_t)p->B * p->L * p->H; }
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }

@@ -53,6 +53,8 @@ struct DecodeArgs {
   int H, L, n_chunk_max;
   float scale_log2;    // log2(e) / sqrt(d)
   int32_t* err;
+  uint64_t wait_ns;    // first-wait limit and copy withholding (kvc_set_wait_limit)
+  int withhold;
 };
 
 template <typename T, int D, int G>
@@ -178,6 +180,7 @@ __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(DecodeArgs a) {
   const T* qp = static_cast<const T*>(a.q) + (bl * a.H * G + (int64_t)h * G) * D;
 
   auto issue = [&](int st) {                             // one thread: stage st -> slot st % kStages
+    if (a.withhold) return;                              // test of the timeout path: no copies
     const int slot = st % kStages;
     const int r0 = e0 + st * kStage;
     const int rows = min(kStage, stored_end - r0);
@@ -213,7 +216,7 @@ __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(DecodeArgs a) {
   int consumed = 0;
   for (int st = 0; st < nst; ++st) {
     const int slot = st % kStages;
-    if (!kvcd::mbar_wait(&sm.full[slot], (uint32_t)((st / kStages) & 1))) sm.abort = 1;
+    if (!kvcd::mbar_wait(&sm.full[slot], (uint32_t)((st / kStages) & 1), a.wait_ns)) sm.abort = 1;
     const int r0 = e0 + st * kStage;
     const int rows = min(kStage, stored_end - r0);
     for (int rb = warp * RPW; rb < warp * RPW + RPW; rb += EB) {
@@ -237,7 +240,7 @@ __global__ void __launch_bounds__(kThreads) decode_chunk_kernel(DecodeArgs a) {
       kvcd::record_error(a.err, KVC_ETIMEOUT);
       // copies still in flight: the stage whose wait failed and those issued after it
       const int first = max(0, consumed - 1);
-      for (int st = first; st < min(nst, first + kStages); ++st)
+      for (int st = first; st < min(nst, first + kStages) && !a.withhold; ++st)
         kvcd::mbar_wait(&sm.full[st % kStages], (uint32_t)((st / kStages) & 1));
     }
     return;
@@ -400,6 +403,7 @@ int run_decode(const kvc_params* p, const void* q, const void* k_new, const void
     t.lse_out = lse_out;
     t.scores_out = scores_out;
     t.lh_span = lh_span; t.lh_gap = lh_gap; t.lh_base = lh_base;
+    t.wait_ns = kvc::wait_limit_ns(); t.withhold = kvc::withhold_copies();
     return kvc::decode_tc_launch(t, s);
   }
   DecodeArgs a;
@@ -414,6 +418,7 @@ int run_decode(const kvc_params* p, const void* q, const void* k_new, const void
   a.lse_out = lse_out;
   a.scores_out = scores_out;
   a.lh_span = lh_span; a.lh_gap = lh_gap; a.lh_base = lh_base;
+  a.wait_ns = kvc::wait_limit_ns(); a.withhold = kvc::withhold_copies();
   dim3 grid(a.n_chunk_max, (unsigned)blh);
   if (p->dtype == KVC_BF16) {
     if (p->d == 128) launch_dg<__nv_bfloat16, 128>(p, a, grid, s);

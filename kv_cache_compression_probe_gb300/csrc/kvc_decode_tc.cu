@@ -333,11 +333,13 @@ __global__ void __launch_bounds__(256, 2)
         const int y_base = (int)(it.off + it.c * kChunkTc);
         for (int i = 0; i < 2 * it.ntiles; ++i, ++t) {
           const int s = t & 1;
-          if (t >= kSlots && !kvcd::mbar_wait(&sm.empty[s], (uint32_t)(((t >> 1) - 1) & 1))) {
+          if (t >= kSlots &&
+              !kvcd::mbar_wait(&sm.empty[s], (uint32_t)(((t >> 1) - 1) & 1), a.wait_ns)) {
             ok = false;
             break;
           }
           if (*abort_flag) { ok = false; break; }
+          if (a.withhold) continue;                  // test of the timeout path: no copies
           const bool is_k = i < it.ntiles;
           const int tt = is_k ? i : i - it.ntiles;
           kvcd::mbar_arrive_expect_tx(&sm.full[s], kTileBytes + (i == 0 ? 2u * 16 * 128 : 0u));
@@ -363,7 +365,7 @@ __global__ void __launch_bounds__(256, 2)
       if (it.ntiles == 0) continue;
       for (int i = 0; i < it.ntiles; ++i, ++t) {     // S^T blocks
         const int s = t & 1;
-        ok = __all_sync(KVC_FULL_MASK, kvcd::mbar_wait(&sm.full[s], (uint32_t)((t >> 1) & 1)));
+        ok = __all_sync(KVC_FULL_MASK, kvcd::mbar_wait(&sm.full[s], (uint32_t)((t >> 1) & 1), a.wait_ns));
         if (!ok) break;
         fence_after();
         if (lane == 0) {
@@ -377,12 +379,12 @@ __global__ void __launch_bounds__(256, 2)
       }
       if (!ok) break;
       if (lane == 0) commit(&sm.s_ready);
-      ok = __all_sync(KVC_FULL_MASK, kvcd::mbar_wait(&sm.p_ready, (uint32_t)(ne & 1)));
+      ok = __all_sync(KVC_FULL_MASK, kvcd::mbar_wait(&sm.p_ready, (uint32_t)(ne & 1), a.wait_ns));
       if (!ok) break;
       fence_after();
       for (int i = 0; i < it.ntiles; ++i, ++t) {     // O^T += V^T P
         const int s = t & 1;
-        ok = __all_sync(KVC_FULL_MASK, kvcd::mbar_wait(&sm.full[s], (uint32_t)((t >> 1) & 1)));
+        ok = __all_sync(KVC_FULL_MASK, kvcd::mbar_wait(&sm.full[s], (uint32_t)((t >> 1) & 1), a.wait_ns));
         if (!ok) break;
         const int nrem = it.nvalid - i * kTileRows;  // valid rows of this V tile
         if (nrem < kTileRows) {                      // rows past the chunk: zero (P is 0 there)
@@ -435,7 +437,7 @@ __global__ void __launch_bounds__(256, 2)
         lh[g] = 0.f;
       }
       if (it.ntiles > 0) {
-        if (!*abort_flag && !kvcd::mbar_wait(&sm.s_ready, (uint32_t)(ne & 1))) *abort_flag = 1;
+        if (!*abort_flag && !kvcd::mbar_wait(&sm.s_ready, (uint32_t)(ne & 1), a.wait_ns)) *abort_flag = 1;
         fence_after();
 #pragma unroll
         for (int t = 0; t < kTiles; ++t)
@@ -506,7 +508,7 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
       for (int g = 0; g < G; ++g) ov[g] = 0.f;
       if (it.ntiles > 0) {
-        if (!*abort_flag && !kvcd::mbar_wait(&sm.o_ready, (uint32_t)(ne & 1))) *abort_flag = 1;
+        if (!*abort_flag && !kvcd::mbar_wait(&sm.o_ready, (uint32_t)(ne & 1), a.wait_ns)) *abort_flag = 1;
         fence_after();
         tld<G>(tl + 64, ov);
         wait_ld();

@@ -39,6 +39,9 @@ struct DecodeTcArgs {
   // cap_lh, off_lh) at i + (i / lh_span) * lh_gap + lh_base (identity for all
   // layers: span = L*H, gap = 0, base = 0); everything else is local
   int64_t lh_span, lh_gap, lh_base;
+  // first-wait limit and copy withholding (kvc_set_wait_limit)
+  uint64_t wait_ns;
+  int withhold;
 };
 
 __host__ __device__ inline int64_t lh_global(int64_t i, int64_t span, int64_t gap, int64_t base) {

@@ -1249,6 +1249,7 @@ int launch_all(const kvc_params* p, ScoreArgs& a, cudaStream_t s) {
     t.B = p->B; t.L = p->L; t.H = p->H; t.G = p->G; t.P = p->P;
     t.chunk_tiles = kTcChunkTiles; t.n_chunks = tc_chunks(p);
     t.q_scale2 = a.q_scale2; t.hop_weight = p->hop_weight;
+    t.wait_ns = kvc::wait_limit_ns(); t.withhold = kvc::withhold_copies();
     a.n_chunks = t.n_chunks;                        // rowcombine loops over these partials
     const int64_t rows_total = p->total_ctx * p->L * p->H;
     const bool timed = phase_begin();
@@ -1282,6 +1283,7 @@ int launch_all(const kvc_params* p, ScoreArgs& a, cudaStream_t s) {
     nd.tree_cuts = p->tree_cuts;
     nd.err = a.err; nd.B = p->B; nd.L = p->L; nd.H = p->H; nd.G = p->G; nd.P = p->P;
     nd.S_max = p->S_max; nd.q_scale2 = a.q_scale2;
+    nd.wait_ns = t.wait_ns; nd.withhold = t.withhold;
     if ((st = kvc::nodes_tc_pass(nd, rows_total, s)) != KVC_OK) return st;
     if (timed) {
       phase_mark(6, s);

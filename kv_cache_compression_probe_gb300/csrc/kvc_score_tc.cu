@@ -152,7 +152,7 @@ struct TcSmem {
   alignas(1024) unsigned char A[NT][2][kBlockBytes];       // query rows, swizzled
   alignas(1024) unsigned char Bt[kStages][2][kBlockBytes]; // key tiles, swizzled
   float xch[4 / NT - 1][NT * kBM][3];                       // other column shares' (m, l, u)
-  uint64_t full[kStages], empty[kStages], tfull[2], tempty[2];
+  uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], mma_done;
   uint32_t tmem_base;
   int abort;
   int issued;
@@ -206,6 +206,7 @@ __global__ void __maxnreg__(kRsMaxRegs)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) { kvcd::mbar_init(&sm.full[s], 1); kvcd::mbar_init(&sm.empty[s], 1); }
     for (int s = 0; s < 2; ++s) { kvcd::mbar_init(&sm.tfull[s], 1); kvcd::mbar_init(&sm.tempty[s], kEpiWarps); }
+    kvcd::mbar_init(&sm.mma_done, 1);
     sm.abort = 0;
     sm.issued = 0;
     kvcd::fence_mbar_init();
@@ -227,10 +228,12 @@ __global__ void __maxnreg__(kRsMaxRegs)
     if (lane == 0) {
       for (int t = 0; t < ntiles; ++t) {
         const int s = t % kStages;
-        if (t >= kStages && !kvcd::mbar_wait(&sm.empty[s], (uint32_t)(((t / kStages) - 1) & 1))) {
+        if (t >= kStages &&
+            !kvcd::mbar_wait(&sm.empty[s], (uint32_t)(((t / kStages) - 1) & 1), a.wait_ns)) {
           sm.abort = 1;
           break;
         }
+        if (a.withhold) continue;                  // test of the timeout path: no copies
         kvcd::mbar_arrive_expect_tx(&sm.full[s], kTileBytes);
         const int y = (int)(row0 + k0 + t * kBN);
         tma_load_2d(sm.Bt[s][0], &kmap, 0, y, &sm.full[s]);
@@ -243,8 +246,8 @@ __global__ void __maxnreg__(kRsMaxRegs)
     if (lane == 0) {
       for (int t = 0; t < ntiles; ++t) {
         const int s = t % kStages, bf = t & 1;
-        if (!kvcd::mbar_wait(&sm.full[s], (uint32_t)((t / kStages) & 1))) { sm.abort = 1; break; }
-        if (t >= 2 && !kvcd::mbar_wait(&sm.tempty[bf], (uint32_t)(((t >> 1) - 1) & 1))) {
+        if (!kvcd::mbar_wait(&sm.full[s], (uint32_t)((t / kStages) & 1), a.wait_ns)) { sm.abort = 1; break; }
+        if (t >= 2 && !kvcd::mbar_wait(&sm.tempty[bf], (uint32_t)(((t >> 1) - 1) & 1), a.wait_ns)) {
           sm.abort = 1;
           break;
         }
@@ -287,7 +290,7 @@ __global__ void __maxnreg__(kRsMaxRegs)
       // every epilogue warp runs all ntiles iterations; after an abort the
       // waits are skipped and the work is void
       const int bf = t & 1;
-      if (!*abort_flag && !kvcd::mbar_wait(&sm.tfull[bf], (uint32_t)((t >> 1) & 1))) *abort_flag = 1;
+      if (!*abort_flag && !kvcd::mbar_wait(&sm.tfull[bf], (uint32_t)((t >> 1) & 1), a.wait_ns)) *abort_flag = 1;
       tc_fence_after();
       const int kt = k0 + t * kBN + sp * kCW;
       const uint32_t col0 = tbase + (uint32_t)((bf * NT + mt) * kBN + sp * kCW);
@@ -411,13 +414,21 @@ __global__ void __maxnreg__(kRsMaxRegs)
     }
   }
 
-  // ---- teardown: every role has finished; wait out copies of an aborted run
+  // ---- teardown: every role has finished; wait out copies and products of an
+  // aborted run before the tensor memory is freed
   __syncthreads();
   if (sm.abort && tid == 0) {
     kvcd::record_error(a.err, KVC_ETIMEOUT);
     // bounded wait for the key tiles still in flight (the last kStages issued)
     for (int t = max(0, sm.issued - kStages); t < sm.issued; ++t)
       kvcd::mbar_wait(&sm.full[t % kStages], (uint32_t)((t / kStages) & 1), 100000000ull);
+  }
+  if (sm.abort && warp == kEpiWarps + 1) {
+    if (lane == 0) {
+      mma_commit(&sm.mma_done);
+      kvcd::mbar_wait(&sm.mma_done, 0);
+    }
+    __syncwarp();
   }
   tc_fence_after();
   if (warp == kEpiWarps + 1) {
@@ -442,7 +453,7 @@ struct TcTSmem {
   alignas(16) float col_a[NT * kBM];                        // per row: minus its base-2 LSE (-inf: no row)
   alignas(16) float col_b[NT * kBM];                        // per row: H (FEATS) or seed weight (PROP)
   float xch[2][3][kBN][9];                                  // shares 1..3: per-key sums, by tile parity
-  uint64_t full[kStages], empty[kStages], tfull[2], tempty[2];
+  uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], mma_done;
   uint32_t tmem_base;
   int abort;
   int issued;
@@ -497,6 +508,7 @@ __global__ void __maxnreg__(kRsMaxRegs)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) { kvcd::mbar_init(&sm.full[s], 1); kvcd::mbar_init(&sm.empty[s], 1); }
     for (int s = 0; s < 2; ++s) { kvcd::mbar_init(&sm.tfull[s], 1); kvcd::mbar_init(&sm.tempty[s], kEpiWarps); }
+    kvcd::mbar_init(&sm.mma_done, 1);
     sm.abort = 0;
     sm.issued = 0;
     kvcd::fence_mbar_init();
@@ -518,10 +530,12 @@ __global__ void __maxnreg__(kRsMaxRegs)
     if (lane == 0) {
       for (int t = 0; t < ntiles; ++t) {
         const int s = t % kStages;
-        if (t >= kStages && !kvcd::mbar_wait(&sm.empty[s], (uint32_t)(((t / kStages) - 1) & 1))) {
+        if (t >= kStages &&
+            !kvcd::mbar_wait(&sm.empty[s], (uint32_t)(((t / kStages) - 1) & 1), a.wait_ns)) {
           sm.abort = 1;
           break;
         }
+        if (a.withhold) continue;                  // test of the timeout path: no copies
         kvcd::mbar_arrive_expect_tx(&sm.full[s], kTileBytes);
         const int y = (int)(row0 + k0 + t * kBN);
         tma_load_2d(sm.Bt[s][0], &kmap, 0, y, &sm.full[s]);
@@ -538,8 +552,8 @@ __global__ void __maxnreg__(kRsMaxRegs)
                                  ((uint32_t)(kBM >> 4) << 24);
       for (int t = 0; t < ntiles; ++t) {
         const int s = t % kStages, bf = t & 1;
-        if (!kvcd::mbar_wait(&sm.full[s], (uint32_t)((t / kStages) & 1))) { sm.abort = 1; break; }
-        if (t >= 2 && !kvcd::mbar_wait(&sm.tempty[bf], (uint32_t)(((t >> 1) - 1) & 1))) {
+        if (!kvcd::mbar_wait(&sm.full[s], (uint32_t)((t / kStages) & 1), a.wait_ns)) { sm.abort = 1; break; }
+        if (t >= 2 && !kvcd::mbar_wait(&sm.tempty[bf], (uint32_t)(((t >> 1) - 1) & 1), a.wait_ns)) {
           sm.abort = 1;
           break;
         }
@@ -569,7 +583,7 @@ __global__ void __maxnreg__(kRsMaxRegs)
     volatile int* abort_flag = &sm.abort;
     for (int t = 0; t < ntiles; ++t) {
       const int bf = t & 1;
-      if (!*abort_flag && !kvcd::mbar_wait(&sm.tfull[bf], (uint32_t)((t >> 1) & 1))) *abort_flag = 1;
+      if (!*abort_flag && !kvcd::mbar_wait(&sm.tfull[bf], (uint32_t)((t >> 1) & 1), a.wait_ns)) *abort_flag = 1;
       tc_fence_after();
       const int key = k0 + t * kBN + kl;
       const bool kvalid = key < k1;
@@ -710,6 +724,13 @@ __global__ void __maxnreg__(kRsMaxRegs)
     kvcd::record_error(a.err, KVC_ETIMEOUT);
     for (int t = max(0, sm.issued - kStages); t < sm.issued; ++t)
       kvcd::mbar_wait(&sm.full[t % kStages], (uint32_t)((t / kStages) & 1), 100000000ull);
+  }
+  if (sm.abort && warp == kEpiWarps + 1) {     // issued products finish before TMEM is freed
+    if (lane == 0) {
+      mma_commit(&sm.mma_done);
+      kvcd::mbar_wait(&sm.mma_done, 0);
+    }
+    __syncwarp();
   }
   tc_fence_after();
   if (warp == kEpiWarps + 1) {
@@ -890,11 +911,12 @@ __global__ void __maxnreg__(kNodeMaxRegs)
         const uint8_t* cuts = a.tree_cuts ? a.tree_cuts + tree * 8 : nullptr;
         // Kt / Kh are free once phase A of the previous slot completed and its
         // epilogue read ln m from Kh (a_ready)
-        if (k >= 1 && (!kvcd::mbar_wait(&sm.k_empty, (uint32_t)((k - 1) & 1)) ||
-                       !kvcd::mbar_wait(&sm.a_ready, (uint32_t)((k - 1) & 1)))) {
+        if (k >= 1 && (!kvcd::mbar_wait(&sm.k_empty, (uint32_t)((k - 1) & 1), a.wait_ns) ||
+                       !kvcd::mbar_wait(&sm.a_ready, (uint32_t)((k - 1) & 1), a.wait_ns))) {
           *abort_flag = 1;
           break;
         }
+        if (a.withhold) continue;                      // test of the timeout path: no copies
         ++nk;
         kvcd::mbar_arrive_expect_tx(&sm.k_full, kTileBytes + kvc::kProtoHeadBytes);
         for (int l = 0; l < 8; ++l) {
@@ -904,7 +926,7 @@ __global__ void __maxnreg__(kNodeMaxRegs)
             tma_load_2d(&sm.Kt[fb][l * 2048], &kmap16, fb * 64, (int)(row0 + st), &sm.k_full);
         }
         kvcd::bulk_g2s(sm.Kh, a.proto + tree * kvc::kProtoBytes, kvc::kProtoHeadBytes, &sm.k_full);
-        if (k >= 1 && !kvcd::mbar_wait(&sm.v_empty, (uint32_t)((k - 1) & 1))) { *abort_flag = 1; break; }
+        if (k >= 1 && !kvcd::mbar_wait(&sm.v_empty, (uint32_t)((k - 1) & 1), a.wait_ns)) { *abort_flag = 1; break; }
         ++nv;
         kvcd::mbar_arrive_expect_tx(&sm.v_full, kTileBytes);
         for (int l = 0; l < 8; ++l) {
@@ -913,7 +935,7 @@ __global__ void __maxnreg__(kNodeMaxRegs)
           for (int fb = 0; fb < 2; ++fb)
             tma_load_2d(&sm.Vt[fb][l * 2048], &vmap16, fb * 64, (int)(row0 + st), &sm.v_full);
         }
-        if (k >= 1 && !kvcd::mbar_wait(&sm.vh_free, (uint32_t)((k - 1) & 1))) { *abort_flag = 1; break; }
+        if (k >= 1 && !kvcd::mbar_wait(&sm.vh_free, (uint32_t)((k - 1) & 1), a.wait_ns)) { *abort_flag = 1; break; }
         ++nh;
         kvcd::mbar_arrive_expect_tx(&sm.vh_full, 15 * 128 * 4);
         kvcd::bulk_g2s(&sm.vh[0][0], a.proto + tree * kvc::kProtoBytes + kvc::kProtoVhOff,
@@ -929,7 +951,7 @@ __global__ void __maxnreg__(kNodeMaxRegs)
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       for (int k = 0; k < nsl; ++k) {
-        if (!kvcd::mbar_wait(&sm.k_full, (uint32_t)(k & 1))) { *abort_flag = 1; break; }
+        if (!kvcd::mbar_wait(&sm.k_full, (uint32_t)(k & 1), a.wait_ns)) { *abort_flag = 1; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
@@ -942,13 +964,13 @@ __global__ void __maxnreg__(kNodeMaxRegs)
         }
         mma_commit(&sm.s_full);
         mma_commit(&sm.k_empty);
-        if (!kvcd::mbar_wait(&sm.a_ready, (uint32_t)(k & 1)) ||
-            !kvcd::mbar_wait(&sm.v_full, (uint32_t)(k & 1))) { *abort_flag = 1; break; }
+        if (!kvcd::mbar_wait(&sm.a_ready, (uint32_t)(k & 1), a.wait_ns) ||
+            !kvcd::mbar_wait(&sm.v_full, (uint32_t)(k & 1), a.wait_ns)) { *abort_flag = 1; break; }
         tc_fence_after();
         bool ok = true;
         for (int j = 0; j < 15; ++j) {
           const int nn = k * 15 + j, bf = nn & 1;
-          if (nn >= 2 && !kvcd::mbar_wait(&sm.nempty[bf], (uint32_t)(((nn >> 1) - 1) & 1))) { ok = false; break; }
+          if (nn >= 2 && !kvcd::mbar_wait(&sm.nempty[bf], (uint32_t)(((nn >> 1) - 1) & 1), a.wait_ns)) { ok = false; break; }
           tc_fence_after();
           int l0, l1;
           node_leaves(j, l0, l1);
@@ -987,7 +1009,7 @@ __global__ void __maxnreg__(kNodeMaxRegs)
       const int x0 = bd[s], y0 = bd[s + 1];
       const uint8_t* cuts = a.tree_cuts ? a.tree_cuts + tree * 8 : nullptr;
       // ---- epilogue A: attention of this row to the slot's nodes and its key quarter
-      if (!*abort_flag && !kvcd::mbar_wait(&sm.s_full, (uint32_t)(k & 1))) *abort_flag = 1;
+      if (!*abort_flag && !kvcd::mbar_wait(&sm.s_full, (uint32_t)(k & 1), a.wait_ns)) *abort_flag = 1;
       tc_fence_after();
       float ah[15];
       {
@@ -1009,7 +1031,7 @@ __global__ void __maxnreg__(kNodeMaxRegs)
         leaf_range(cuts, 2 * g, x0, y0, st, cnt0);
         leaf_range(cuts, 2 * g + 1, x0, y0, st, cnt1);
       }
-      if (k >= 1 && !*abort_flag && !kvcd::mbar_wait(&sm.b_done, (uint32_t)((k - 1) & 1)))
+      if (k >= 1 && !*abort_flag && !kvcd::mbar_wait(&sm.b_done, (uint32_t)((k - 1) & 1), a.wait_ns))
         *abort_flag = 1;
       float lsum[2];
 #pragma unroll
@@ -1073,12 +1095,12 @@ __global__ void __maxnreg__(kNodeMaxRegs)
           an_fin[i] = v;
         }
       }
-      if (!*abort_flag && !kvcd::mbar_wait(&sm.vh_full, (uint32_t)(k & 1))) *abort_flag = 1;
+      if (!*abort_flag && !kvcd::mbar_wait(&sm.vh_full, (uint32_t)(k & 1), a.wait_ns)) *abort_flag = 1;
       // ---- epilogue B: 32 features of every node
 #pragma unroll
       for (int j = 0; j < 15; ++j) {
         const int nn = k * 15 + j, bf = nn & 1;
-        if (!*abort_flag && !kvcd::mbar_wait(&sm.nfull[bf], (uint32_t)((nn >> 1) & 1))) *abort_flag = 1;
+        if (!*abort_flag && !kvcd::mbar_wait(&sm.nfull[bf], (uint32_t)((nn >> 1) & 1), a.wait_ns)) *abort_flag = 1;
         tc_fence_after();
         float v[32];
         {

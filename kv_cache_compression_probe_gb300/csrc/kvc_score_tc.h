@@ -42,6 +42,8 @@ struct ProbeTcArgs {
   int n_chunks;
   float q_scale2;         // log2(e) / sqrt(d)
   float hop_weight;
+  uint64_t wait_ns;       // first-wait limit and copy withholding (kvc_set_wait_limit)
+  int withhold;
 };
 
 struct NodeTcArgs {
@@ -59,6 +61,8 @@ struct NodeTcArgs {
   int32_t* err;
   int B, L, H, G, P, S_max;
   float q_scale2;
+  uint64_t wait_ns;       // first-wait limit and copy withholding (kvc_set_wait_limit)
+  int withhold;
 };
 
 bool probe_tc_supported(const kvc_params* p);
