@@ -157,23 +157,65 @@ def hop_relevance(alpha: np.ndarray, Kh: np.ndarray, Vh: np.ndarray, S_h: int,
 
 
 # =============================================================================== a3: trees and prototypes
-def tree_nodes(x: int, y: int, cuts: Optional[Sequence[int]] = None) -> List[Tuple[int, int]]:
+def tree_nodes(x: int, y: int, cuts: Optional[Sequence[int]] = None,
+               extract: Optional[Sequence[int]] = None) -> List[Tuple[int, int]]:
     """The 15 prototype nodes of a slot [x, y) in breadth-first order (reading R3).
 
     Node j has children 2j+1 and 2j+2; a node [a, b) splits at floor((a+b)/2),
     or, when ``cuts`` is given, at the absolute position cuts[j] (j < 7; the
     curvature-chosen trees of reading R18).  Nodes 7..14 are the leaf
-    prototypes; splitting one yields its tokens.
+    prototypes; splitting one yields its tokens.  ``extract`` (reading R19)
+    gives, per depth-2 node j = 3..6, the absolute position t of the salient
+    token it isolates, or -1: such a node [a, b) has the three-way child set
+    {[a, t), token t, [t+1, b)}, so its leaves are [a, t) and [t+1, b) and t
+    belongs to no leaf.
     """
     nodes = [(x, y)]
     for j in range(7):
         a, b = nodes[j]
+        t = -1 if extract is None or j < 3 else int(extract[j - 3])
+        if t >= 0:
+            if not extract_valid(t, a, b):
+                raise ValueError(f"salient token {t} of node {j} invalid in [{a}, {b})")
+            nodes.append((a, t))
+            nodes.append((t + 1, b))
+            continue
         mid = (a + b) // 2 if cuts is None else int(cuts[j])
         if not a < mid < b:
             raise ValueError(f"cut {mid} of node {j} outside ({a}, {b})")
         nodes.append((a, mid))
         nodes.append((mid, b))
     return nodes
+
+
+SIDE_MIN = 2          # R19: each side span of a three-way child set keeps 2..15 tokens
+SIDE_MAX = 15
+
+
+def extract_valid(t: int, a: int, b: int) -> bool:
+    """Whether token t may be isolated from node [a, b) (reading R19): both side
+    spans [a, t) and [t+1, b) keep SIDE_MIN..SIDE_MAX tokens (a side of one
+    token would be a prototype identical to its token, and a leaf holds at
+    most 16 tokens)."""
+    return SIDE_MIN <= t - a <= SIDE_MAX and SIDE_MIN <= b - t - 1 <= SIDE_MAX
+
+
+def salient_tokens(r: np.ndarray, x0: int, y0: int, cuts: Optional[Sequence[int]] = None
+                   ) -> List[int]:
+    """The salient token each depth-2 node isolates (reading R19; [GK] "Technical
+    details and default settings": tree construction may isolate a salient
+    token with a three-way child set; "Exact-information safeguard": Split /
+    Extract of a name-bearing span).  For depth-2 node j = 3..6 of the binary
+    tree (midpoint or ``cuts``), t = the node's most relevant token (largest
+    r_i, ties to the smaller i); the node isolates it when ``extract_valid``,
+    else keeps its binary split (-1).  Comparisons only, in r's precision."""
+    nodes = tree_nodes(x0, y0, cuts)
+    out = []
+    for j in range(3, 7):
+        a, b = nodes[j]
+        t = a + int(np.argmax(np.asarray(r[a:b])))
+        out.append(t if extract_valid(t, a, b) else -1)
+    return out
 
 
 def node_parent(j: int) -> int:
@@ -253,13 +295,17 @@ def gain_fraction(x: float, ddrop: float) -> float:
     return min(max(x / ddrop, 0.0), 1.0)
 
 
-def slot_ops(D: np.ndarray, Ddrop: np.ndarray, Rv: np.ndarray, sizes: np.ndarray, sens: float):
+def slot_ops(D: np.ndarray, Ddrop: np.ndarray, Rv: np.ndarray, sizes: np.ndarray, sens: float,
+             extract: Optional[Sequence[int]] = None):
     """Utilities and costs of the 16 ops of one slot tree ([GK] "04 Top-down
     budget flow": utility per entry = relevance x fidelity gain x head
     sensitivity / new physical entries).
 
     Add: cost 1, gain = 1 - D(root)/D_drop(root).
     Split(internal N): cost 1, gain = (D(N) - D(c1) - D(c2)) / D_drop(N).
+    Split(depth-2 N with a three-way child set, reading R19): cost 2 (three
+    entries replace one), gain = (D(N) - D(c1) - D(c2)) / D_drop(N) (the
+    isolated token is exact, distortion 0).
     Split(leaf N of c tokens): cost c - 1, gain = D(N) / D_drop(N) (tokens are exact).
     Relevance of a node is the sum of its tokens' relevance ([GK] "03": parent
     value = sum of child values).
@@ -270,7 +316,7 @@ def slot_ops(D: np.ndarray, Ddrop: np.ndarray, Rv: np.ndarray, sizes: np.ndarray
     util[0] = Rv[0] * gain_fraction(Ddrop[0] - D[0], Ddrop[0]) * sens
     for j in range(N_NODES):
         if j < FIRST_LEAF:
-            c = 1
+            c = 2 if (extract is not None and j >= 3 and extract[j - 3] >= 0) else 1
             g = gain_fraction(D[j] - D[2 * j + 1] - D[2 * j + 2], Ddrop[j])
         else:
             c = int(sizes[j]) - 1
@@ -292,15 +338,20 @@ class HeadResult:
     Ddrop: np.ndarray    # [S, 15]
     protos: Optional[List[List[Prototype]]] = None
     Rv: Optional[np.ndarray] = None   # [S, 15] node values R(N), as used by the ops
+    extract: Optional[np.ndarray] = None   # [S, 4] salient tokens (R19), -1 = none
 
 
 def score_and_value_head(Kh, Vh, Qh, n: int, P: int, bounds: np.ndarray, sens: float,
                          base: float = 10000.0, hop_weight: float = 0.3, n_hops: int = 2,
                          w_part: float = 0.25, w_value: float = 0.75, value_floor: float = 0.1,
                          S_h: Optional[int] = None, keep_protos: bool = False,
-                         cuts: Optional[np.ndarray] = None) -> HeadResult:
+                         cuts: Optional[np.ndarray] = None, salient: bool = False,
+                         salient_r: Optional[np.ndarray] = None) -> HeadResult:
     """Everything the scoring call produces for one (layer, KV head): a1 -> a4.
-    ``cuts`` [S, 7] gives the trees' cut positions (R18); None = midpoint trees."""
+    ``cuts`` [S, 7] gives the trees' cut positions (R18); None = midpoint trees.
+    ``salient``: the depth-2 nodes isolate their salient tokens (R19), chosen on
+    ``salient_r`` when given (e.g. the device's float32 relevance, for a
+    bit-exact comparison of the choice), else on this oracle's relevance."""
     Kh = np.asarray(Kh, np.float64)
     Vh = np.asarray(Vh, np.float64)
     G = Qh.shape[0]
@@ -316,10 +367,16 @@ def score_and_value_head(Kh, Vh, Qh, n: int, P: int, bounds: np.ndarray, sens: f
     Dall = np.zeros((S, N_NODES))
     Rall = np.zeros((S, N_NODES))
     Ddall = np.zeros((S, N_NODES))
+    ext_all = np.full((S, 4), -1, dtype=np.int64)
     protos_all = []
     for s in range(S):
         x0, y0 = int(bounds[s]), int(bounds[s + 1])
-        nodes = tree_nodes(x0, y0, None if cuts is None else cuts[s])
+        cs = None if cuts is None else cuts[s]
+        ext = None
+        if salient:
+            ext = salient_tokens(r if salient_r is None else salient_r, x0, y0, cs)
+            ext_all[s] = ext
+        nodes = tree_nodes(x0, y0, cs, ext)
         D = np.zeros(N_NODES)
         Dd = np.zeros(N_NODES)
         Rv = np.zeros(N_NODES)
@@ -332,12 +389,13 @@ def score_and_value_head(Kh, Vh, Qh, n: int, P: int, bounds: np.ndarray, sens: f
             Rv[j] = r[x:y].sum()
             sizes[j] = y - x
             plist.append(pr)
-        util[s], cost[s] = slot_ops(D, Dd, Rv, sizes, sens)
+        util[s], cost[s] = slot_ops(D, Dd, Rv, sizes, sens, ext)
         Dall[s], Ddall[s], Rall[s] = D, Dd, Rv
         if keep_protos:
             protos_all.append(plist)
     return HeadResult(lse=sc.lse, feats=sc.feats, r=r, seeds=seeds, util=util, cost=cost,
-                      D=Dall, Ddrop=Ddall, protos=protos_all if keep_protos else None, Rv=Rall)
+                      D=Dall, Ddrop=Ddall, protos=protos_all if keep_protos else None, Rv=Rall,
+                      extract=ext_all if salient else None)
 
 
 # =============================================================================== f3: curvature-chosen trees
@@ -435,12 +493,15 @@ def budget(n: int, L: int, H: int, W: int, budget_ratio: float, budget_entries_p
     return B_tot, B_alloc, cap
 
 
-def _leaf_of(i: int, x0: int, y0: int, cuts=None) -> Tuple[int, List[int]]:
-    """Leaf node containing token i and the node path root..leaf."""
-    nodes = tree_nodes(x0, y0, cuts)
+def _leaf_of(i: int, x0: int, y0: int, cuts=None, extract=None) -> Tuple[int, List[int]]:
+    """The node whose split makes token i exact (its leaf, or the depth-2 node
+    that isolates it, reading R19) and the node path root..that node."""
+    nodes = tree_nodes(x0, y0, cuts, extract)
     j = 0
     path = [0]
     while j < FIRST_LEAF:
+        if extract is not None and j >= 3 and int(extract[j - 3]) == i:
+            return j, path
         c1 = 2 * j + 1
         j = c1 if i < nodes[c1][1] else c1 + 1
         path.append(j)
@@ -460,7 +521,7 @@ class Selection:
 
 def singleton_floor(r: np.ndarray, sens: np.ndarray, bounds: np.ndarray, cost: np.ndarray,
                     cap_entries: int, cap_tokens: int, taken: np.ndarray,
-                    cuts: Optional[np.ndarray] = None):
+                    cuts: Optional[np.ndarray] = None, extract: Optional[np.ndarray] = None):
     """Capped singleton floor before the auction ([GK] "Exact-information
     safeguard" and technical details), reading R6.
 
@@ -473,6 +534,8 @@ def singleton_floor(r: np.ndarray, sens: np.ndarray, bounds: np.ndarray, cost: n
     once cap_tokens tokens are counted (cap_tokens < 0: no token cap).
     The key r * sens is computed in the precision of ``r``.  ``cuts`` [L, H,
     S, 7] gives the trees' cut positions (R18); None = midpoint trees.
+    ``extract`` [L, H, S, 4]: the salient tokens the depth-2 nodes isolate
+    (R19; -1 = none): such a token's path ends at its depth-2 node's split.
     Mutates ``taken`` and returns (spent, tokens).
     """
     L, H, n_ = r.shape
@@ -497,7 +560,8 @@ def singleton_floor(r: np.ndarray, sens: np.ndarray, bounds: np.ndarray, cost: n
         l, h = divmod(lh, H)
         s = int(slot_of[i])
         x0, y0 = int(bounds[s]), int(bounds[s + 1])
-        leaf, path = _leaf_of(i, x0, y0, None if cuts is None else cuts[l, h, s])
+        leaf, path = _leaf_of(i, x0, y0, None if cuts is None else cuts[l, h, s],
+                              None if extract is None else extract[l, h, s])
         t = taken[l, h, s]
         if t[1 + leaf]:
             continue                                   # already exact
@@ -586,14 +650,16 @@ def full_heads(r: np.ndarray, end: int, frac: float) -> np.ndarray:
 def select_sequence(util: np.ndarray, cost: np.ndarray, r: np.ndarray, sens: np.ndarray,
                     bounds: np.ndarray, n: int, W: int, budget_ratio: float,
                     budget_entries_per_lh: int, floor_cap_frac: float, floor_cap_tokens: int,
-                    head_full_frac: float = 0.0, cuts: Optional[np.ndarray] = None) -> Selection:
+                    head_full_frac: float = 0.0, cuts: Optional[np.ndarray] = None,
+                    extract: Optional[np.ndarray] = None) -> Selection:
     """Budget -> singleton floor -> greedy auction for one sequence (a5).
 
     With head_full_frac > 0 (the head-level hybrid, R16) the full heads store
     every token exact (all ops taken, len = n) and pay n - W beyond their
     window from the same budget; the floor and the auction run on the other
     heads with B_alloc = B_tot - W*L*H - F*(n - W) and the floor cap taken of
-    that reduced pool.  ``cuts`` [L, H, S, 7]: the trees' cut positions (R18)."""
+    that reduced pool.  ``cuts`` [L, H, S, 7]: the trees' cut positions (R18);
+    ``extract`` [L, H, S, 4]: the depth-2 nodes' isolated salient tokens (R19)."""
     L, H, S, _ = util.shape
     B_tot, B_alloc, cap = budget(n, L, H, W, budget_ratio, budget_entries_per_lh, floor_cap_frac)
     taken = np.zeros((L, H, S, N_OPS), dtype=bool)
@@ -605,7 +671,7 @@ def select_sequence(util: np.ndarray, cost: np.ndarray, r: np.ndarray, sens: np.
             raise ValueError("budget smaller than the full heads and the windows")
         cap = int(math.floor(floor_cap_frac * B_alloc))
     fs, ft = singleton_floor(r, sens, bounds, cost, min(cap, B_alloc), floor_cap_tokens, taken,
-                             cuts)
+                             cuts, extract)
     asp = greedy_auction(util, cost, taken, B_alloc - fs)
     lens = W + (taken * cost).sum(axis=(2, 3))
     return Selection(taken=taken, floor_spent=fs, floor_tokens=ft, auction_spent=asp,
@@ -613,15 +679,19 @@ def select_sequence(util: np.ndarray, cost: np.ndarray, r: np.ndarray, sens: np.
 
 
 # =============================================================================== a6: pack
-def frontier(t: np.ndarray, x0: int, y0: int, cuts=None) -> List[Tuple[str, int]]:
+def frontier(t: np.ndarray, x0: int, y0: int, cuts=None, extract=None) -> List[Tuple[str, int]]:
     """Stored entries of one slot tree, left to right ([GK] "05 Physical cache
     packing"): an absent root stores nothing, a present unsplit node stores its
-    prototype, a split leaf prototype stores its tokens exactly."""
-    nodes = tree_nodes(x0, y0, cuts)
+    prototype, a split leaf prototype stores its tokens exactly, and a split
+    depth-2 node with a three-way child set (R19) stores its left side, its
+    salient token exactly, then its right side."""
+    nodes = tree_nodes(x0, y0, cuts, extract)
 
     def visit(j):
         if not t[1 + j]:
             return [("node", j)]
+        if extract is not None and 3 <= j < FIRST_LEAF and extract[j - 3] >= 0:
+            return visit(2 * j + 1) + [("tok", int(extract[j - 3]))] + visit(2 * j + 2)
         if j < FIRST_LEAF:
             return visit(2 * j + 1) + visit(2 * j + 2)
         a, b = nodes[j]
@@ -642,17 +712,19 @@ class Packed:
 
 
 def pack_head(Kh, Vh, r, bounds, t_lh, n: int, W: int, base: float, value_floor: float,
-              cuts: Optional[np.ndarray] = None):
+              cuts: Optional[np.ndarray] = None, extract: Optional[np.ndarray] = None):
     """Entries of one (l, h): slots ascending, frontier left to right, then the
-    window tokens [n - W, n).  Exact tokens keep their K/V and get log m = 0."""
+    window tokens [n - W, n).  Exact tokens keep their K/V and get log m = 0.
+    ``cuts`` [S, 7] (R18), ``extract`` [S, 4] (R19) describe the trees."""
     Kh = np.asarray(Kh, np.float64)
     Vh = np.asarray(Vh, np.float64)
     ks, vs, lm, ps = [], [], [], []
     for s in range(len(bounds) - 1):
         x0, y0 = int(bounds[s]), int(bounds[s + 1])
         cs = None if cuts is None else cuts[s]
-        nodes = tree_nodes(x0, y0, cs)
-        for kind, j in frontier(t_lh[s], x0, y0, cs):
+        es = None if extract is None else extract[s]
+        nodes = tree_nodes(x0, y0, cs, es)
+        for kind, j in frontier(t_lh[s], x0, y0, cs, es):
             if kind == "tok":
                 ks.append(Kh[j]); vs.append(Vh[j]); lm.append(0.0); ps.append(float(j))
             else:
