@@ -159,6 +159,38 @@ def kernel_traffic(name: str, src_files):
     return rec.get("dram_bytes_per_launch")
 
 
+# the kernels the committed end-to-end selection record depends on (the same
+# list as tests/test_gpu_full_size.py)
+PARITY_SOURCES = ("kv_cache_compression_probe_gb300/csrc/kvc_score.cu",
+                  "kv_cache_compression_probe_gb300/csrc/kvc_score_tc.cu",
+                  "kv_cache_compression_probe_gb300/csrc/kvc_select.cu",
+                  "kv_cache_compression_probe_gb300/csrc/kvc_common.cuh")
+
+
+def parity_record(name: str):
+    """The end-to-end selection parity of a workload (device chain against the
+    float64 oracle chain, near-ties within 1e-6 counted) as written by the
+    full-size GPU test and committed under profiles/; marked stale when the
+    kernels it depends on changed since."""
+    path = os.path.join(ROOT, "profiles", f"parity_{name}.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    h = hashlib.sha256()
+    for f in PARITY_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    seqs = rec.get("sequences", [])
+    return {"source": "profiles/parity_%s.json (tests/test_gpu_full_size.py)" % name,
+            "current": rec.get("source_sha256") == h.hexdigest(),
+            "selection_end_to_end": "device taken set == oracle chain's up to 1e-6 ties",
+            "tie_band_rel": rec.get("tie_band_rel"),
+            "ops": sum(x["ops"] for x in seqs),
+            "ties_reported": sum(x["ties_reported"] for x in seqs),
+            "tie_runs_reordered": sum(x["tie_runs_reordered"] for x in seqs),
+            "max_abs_err": max((x["util_max_abs_err"] for x in seqs), default=None),
+            "max_rel_err": max((x["util_max_rel_err"] for x in seqs), default=None)}
+
+
 # --------------------------------------------------------------------------- GPU arm
 def full_cache_decode_ms(p, cfg, seqs, K, V, q_all, kn_all, vn_all, D, dev, stream):
     """Mean ms per decode step of the same decode call over the uncompressed cache.
@@ -705,6 +737,9 @@ def run_gpu(args, cfg, rank, world):
                                  else "whole inputs, then the step")},
         "evict_per_step_next_f2": evict,
         "tree_cuts_next_f3": tree,
+        "parity": parity_record(cfg.name) if (cfg.name == "mistral16k" and not args.layers
+                                              and not args.tree_cuts
+                                              and args.head_full_frac == 0.0) else None,
         "gpu_launches": launches,
         "gpu_launches_detail": {"issued_by_host": host_launches,
                                 "in_graph_replays": graph_launches,
@@ -713,6 +748,158 @@ def run_gpu(args, cfg, rank, world):
         "clocks": clk,
     }
     return line
+
+
+# --------------------------------------------------------------------------- other workloads
+def workload_leg(name: str, args, dev, with_cpu: bool):
+    """One of the other workloads at full size (long context with its curvature
+    partition, the 128x aggressive config, the 64-sequence serving batch):
+    inputs generated on the device (synth.device_gen), compression timed as
+    the median of `reps` graph replays after warm-ups (kvc_partition included
+    for the long-context config), then the workload's decode steps as one
+    graph replay.  Returns a record with throughput and roofline fractions."""
+    import torch
+    from kv_cache_compression_probe_gb300 import kvc
+    from kv_cache_compression_probe_gb300.pipeline import Compressor, pad_bounds
+    from synth import device_gen as DG
+    from synth import workloads as W
+    cfg = W.get_config(name)
+    L, H, G, P, d, D = cfg.L, cfg.H, cfg.G, cfg.P, cfg.d, cfg.n_decode
+    esz = 2
+    ns = W.context_lengths(cfg)
+    tokens = int(ns.sum())
+    bf = torch.bfloat16
+    K = torch.empty((tokens * L * H, d), dtype=bf, device=dev)
+    V = torch.empty_like(K)
+    Qp = torch.empty((cfg.B, L, H * G, P, d), dtype=bf, device=dev)
+    t_gen = time.perf_counter()
+    ns, planted = DG.fill_workload(cfg, K, V, Qp)
+    ctx32 = torch.tensor(ns.astype(np.int32), device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    mk = dict(B=cfg.B, L=L, H=H, G=G, d=d, P=P, W=cfg.W, dtype=kvc.KVC_BF16,
+              n_max=int(ns.max()), rope_base=cfg.rope_base, budget_ratio=cfg.budget_ratio,
+              budget_entries_per_lh=cfg.budget_entries_per_lh, floor_cap_frac=cfg.floor_cap_frac,
+              floor_cap_tokens=cfg.floor_cap_tokens, decode_reserve=D + 1)
+    partition = None
+    if cfg.slots == "curvature":
+        dh = cfg.hidden_dim
+        hid = torch.zeros((cfg.B, int(ns.max()), dh), dtype=bf, device=dev)
+        for b, n in enumerate(ns):
+            hid[b, :int(n)] = DG.hidden_states(cfg, b, int(n), planted[b], dev)
+        # a first partition with room for any slot count fixes S_max
+        S_room = max(int(n - cfg.W) // 16 + 1 for n in ns)
+        p0 = kvc.make_params(S_max=S_room, **mk)
+        ws0 = kvc.workspace(kvc.KVC_WS_PARTITION, p0, dev)
+        kap = torch.empty((cfg.B, int(ns.max())), dtype=torch.float32, device=dev)
+        b0 = torch.zeros((cfg.B, S_room + 1), dtype=torch.int32, device=dev)
+        n0 = torch.zeros((cfg.B,), dtype=torch.int32, device=dev)
+        kvc.kvc_partition(p0, ctx32, hid, dh, kap, b0, n0, ws0)
+        S_max = int(n0.max())
+        bounds = torch.zeros((cfg.B, S_max + 1), dtype=torch.int32, device=dev)
+        n_slots = torch.zeros_like(n0)
+
+        def partition():
+            kvc.kvc_partition(p, ctx32, hid, dh, kap, bounds, n_slots, ws0, stream)
+    else:
+        S_max = max(len(bd) - 1 for bd in planted)
+        bounds = torch.from_numpy(pad_bounds(planted, S_max)).to(dev)
+        n_slots = torch.tensor([len(bd) - 1 for bd in planted], dtype=torch.int32, device=dev)
+    p = kvc.make_params(S_max=S_max, **mk)
+    comp = Compressor(p, [int(n) for n in ns], device=dev)
+    torch.cuda.synchronize(dev)
+    t_gen = time.perf_counter() - t_gen
+
+    def compress():
+        if partition is not None:
+            partition()
+        comp.compress(K, V, Qp, bounds, n_slots, graph=True)
+
+    for _ in range(2):
+        compress()
+    torch.cuda.synchronize(dev)
+    if kvc.kvc_device_error() != 0:
+        raise RuntimeError(f"device error in the {name} workload's compression")
+    per = {"partition": [], "score": [], "select": [], "merge_pack": [], "total": []}
+    for _ in range(args.workload_reps):
+        m = [ev() for _ in range(5)]
+        m[0].record(stream)
+        if partition is not None:
+            partition()
+        m[1].record(stream)
+        comp.score(K, V, Qp, bounds, n_slots, graph=True)
+        m[2].record(stream)
+        comp.select(bounds, n_slots, graph=True)
+        m[3].record(stream)
+        comp.merge_pack(K, V, bounds, n_slots, graph=True)
+        m[4].record(stream)
+        torch.cuda.synchronize(dev)
+        for k, (i, j) in zip(per, ((0, 1), (1, 2), (2, 3), (3, 4), (0, 4))):
+            per[k].append(m[i].elapsed_time(m[j]))
+    med = {k: statistics.median(v) for k, v in per.items()}
+    # decode: D steps as one graph replay over the packed cache (fresh lengths)
+    q_all, kn_all, vn_all = DG.decode_inputs(cfg, D, dev)
+    out = torch.empty(tuple(q_all.shape), dtype=bf, device=dev)
+    len0 = comp.len_lh.clone()
+    comp.decode_many(q_all, kn_all, vn_all, out)           # capture + warm
+    comp.len_lh.copy_(len0)
+    torch.cuda.synchronize(dev)
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    comp.decode_many(q_all, kn_all, vn_all, out)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if kvc.kvc_device_error() != 0:
+        raise RuntimeError(f"device error in the {name} workload's decode")
+    dec_ms = e0.elapsed_time(e1) / D
+    hbm, tc, src = measured_peaks()
+    LHB = cfg.B * L * H
+    packed_entries = int(comp.total.cpu()[0]) - LHB * p.decode_reserve
+    avg_entries = packed_entries + LHB * ((D + 1) / 2.0)
+    dec_bytes = (avg_entries * (2 * d * esz + 4) + LHB * (2 * d * esz + 8)
+                 + 2 * LHB * G * d * esz)
+    taken_add = comp.taken[..., 0].bool().cpu().numpy()
+    bnd = bounds.cpu().numpy().astype(np.int64)
+    nsl = n_slots.cpu().numpy()
+    covered = 0
+    for b in range(cfg.B):
+        slot_len = np.diff(bnd[b, :int(nsl[b]) + 1])
+        covered += int((taken_add[b, :, :, :len(slot_len)] * slot_len[None, None, :]).sum())
+    pack_bytes = (covered * (2 * d * esz + 4) + LHB * cfg.W * 2 * d * esz
+                  + packed_entries * (2 * d * esz + 8))
+    score_flops = 2.0 * L * H * G * P * tokens * d * 3 + 2.0 * L * H * P * tokens * d * 2 * cfg.n_hops
+    comp_ms = med["total"]
+    rec = {
+        "workload": cfg.name + ": " + cfg.description, "batch": cfg.B,
+        "context": int(ns.max()) if cfg.B == 1 else [int(ns.min()), int(ns.max())],
+        "kv_tokens": tokens, "decode_steps": D,
+        "ms_per_step": comp_ms + dec_ms * D,
+        "kv_tokens_per_s": tokens / ((comp_ms + dec_ms * D) * 1e-3),
+        "compression_median_ms": med, "compression_reps": args.workload_reps,
+        "compress_kv_tokens_per_s": tokens / (comp_ms * 1e-3),
+        "compress_lh_entries_per_s": tokens * L * H / (comp_ms * 1e-3),
+        "decode_ms_per_step": dec_ms,
+        "decode_roofline": {"bound": "hbm", "achieved": dec_bytes / (dec_ms * 1e-3) / 1e9,
+                            "peak": hbm, "unit": "GB/s",
+                            "frac": dec_bytes / (dec_ms * 1e-3) / 1e9 / hbm,
+                            "algorithmic_bytes_per_launch": dec_bytes},
+        "merge_pack_roofline": {"bound": "hbm",
+                                "achieved": pack_bytes / (med["merge_pack"] * 1e-3) / 1e9,
+                                "peak": hbm, "unit": "GB/s",
+                                "frac": pack_bytes / (med["merge_pack"] * 1e-3) / 1e9 / hbm,
+                                "algorithmic_bytes": pack_bytes},
+        "score_tc_frac_of_bf16_peak": score_flops / (med["score"] * 1e-3) / 1e12 / tc,
+        "packed_entries": packed_entries,
+        "compression_ratio": tokens * L * H / packed_entries,
+        "inputs": "generated on the device (synth.device_gen), %.1f s; K+V %.1f GB" %
+                  (t_gen, 2 * tokens * L * H * d * esz / 1e9),
+        "peaks": src + " (MEASURED_PEAKS.json)",
+    }
+    del comp, K, V, Qp, q_all, kn_all, vn_all, out
+    torch.cuda.empty_cache()
+    if with_cpu:
+        rec["cpu_baseline"] = cpu_baseline(cfg, D, single_process=False)
+    return rec
 
 
 # --------------------------------------------------------------------------- oracle (CPU)
@@ -819,14 +1006,20 @@ def oracle_sample_parallel(cfg, heads, decode_steps, workers):
     return wall, n * len(heads) / (cfg.L * cfg.H)
 
 
-def cpu_baseline(cfg, decode_steps, n_heads=4):
+def cpu_baseline(cfg, decode_steps, n_heads=4, single_process=True):
     """The oracle on the host cores: all cores (one (layer, KV head) per worker)
-    as the reported baseline, and one process on `n_heads` heads beside it."""
+    as the reported baseline, and (single_process) one process on `n_heads`
+    heads beside it."""
     workers = max(1, min(os.cpu_count() or 1, 16, cfg.L * cfg.H))
     heads = [(k % cfg.L, k // cfg.L) for k in range(workers)]
     pwall, ptoks = oracle_sample_parallel(cfg, heads, decode_steps, workers)
     n_heads = min(n_heads, cfg.L * cfg.H)
-    secs, toks = oracle_sample(cfg, [(k % cfg.L, k // cfg.L) for k in range(n_heads)], decode_steps)
+    single = None
+    if single_process:
+        secs, toks = oracle_sample(cfg, [(k % cfg.L, k // cfg.L) for k in range(n_heads)],
+                                   decode_steps)
+        single = {"value": toks / secs, "cores": os.cpu_count(), "heads": n_heads,
+                  "seconds": secs, "note": "one process; numpy's BLAS threads use every core"}
     return {"value": ptoks / pwall, "unit": UNIT, "cores": workers, "kind": "oracle",
             "sample": f"{workers} of {cfg.L * cfg.H} (layer, KV head) pairs of the {cfg.n}-token "
                       f"sequence, one per worker process: score+hops+utilities, floor+auction "
@@ -834,9 +1027,7 @@ def cpu_baseline(cfg, decode_steps, n_heads=4):
                       f"steps; float64 numpy; wall {pwall:.1f} s (host reports "
                       f"{os.cpu_count()} cores)",
             "seconds": pwall,
-            "single_process": {"value": toks / secs, "cores": os.cpu_count(), "heads": n_heads,
-                               "seconds": secs,
-                               "note": "one process; numpy's BLAS threads use every core"}}
+            "single_process": single}
 
 
 def run_reference(args, cfg, rank, world):
@@ -895,6 +1086,10 @@ def main():
                     help="issue the compression calls directly instead of as CUDA graph replays")
     ap.add_argument("--eager-decode", action="store_true",
                     help="issue the decode steps one call at a time instead of one CUDA graph")
+    ap.add_argument("--workloads", default="long,aggressive,serving",
+                    help="other workloads timed after the headline line (comma list; '' = none)")
+    ap.add_argument("--workload-reps", type=int, default=5,
+                    help="compression repetitions per other workload (median)")
     ap.add_argument("--profile", action="store_true",
                     help="profiling run: no warm-up, one step, no CPU baseline, no e2e leg")
     args = ap.parse_args()
@@ -922,6 +1117,14 @@ def main():
     line = run_gpu(args, cfg, rank, world)
     if rank == 0:
         line["cpu_baseline"] = cpu
+        names = [w for w in args.workloads.split(",") if w] if world == 1 and not args.profile \
+            and not args.layers else []
+        if names:
+            import torch
+            torch.cuda.empty_cache()
+            dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+            line["other_workloads"] = {w: workload_leg(w, args, dev, not args.no_cpu_baseline)
+                                       for w in names}
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
