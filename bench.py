@@ -500,7 +500,8 @@ def run_gpu(args, cfg, rank, world):
     h_kn = torch.from_numpy(np.stack([x[1] for x in dec])).to(dt).pin_memory()
     h_vn = torch.from_numpy(np.stack([x[2] for x in dec])).to(dt).pin_memory()
     q_all, kn_all, vn_all = h_q.to(dev), h_kn.to(dev), h_vn.to(dev)
-    comp = Compressor(p, [s[0] for s in seqs], device=dev, tree_cuts=args.tree_cuts)
+    comp = Compressor(p, [s[0] for s in seqs], device=dev, tree_cuts=args.tree_cuts,
+                      salient=args.salient)
     out = torch.empty((D,) + tuple(q_all.shape[1:]), dtype=dt, device=dev)
     h_out = torch.empty(out.shape, dtype=dt).pin_memory()
     stream = torch.cuda.current_stream(dev)
@@ -569,6 +570,13 @@ def run_gpu(args, cfg, rank, world):
     clocks.end()
     host_launches = kvc.kvc_launch_count() - launches0
     graph_launches = rec["graph_launches"]
+    # three-way salient child sets of the last timed compression (other legs
+    # rewrite the cut table)
+    salient_stat = None
+    if args.salient:
+        bits = np.unpackbits(comp.cuts[..., 7].cpu().numpy().reshape(-1, 1), axis=1)
+        salient_stat = {"isolated_tokens": int(bits.sum()),
+                        "depth2_nodes": 4 * sum(len(sq[1]) - 1 for sq in seqs) * cfg.L * cfg.H}
     launches = host_launches + graph_launches
     # the same D decode steps issued one call at a time, for comparison
     eager_ms = None
@@ -702,7 +710,8 @@ def run_gpu(args, cfg, rank, world):
                    "decode_steps": D, "l2": "inputs larger than L2 (K+V %.2f GB)" %
                    (2 * tokens * cfg.L * cfg.H * d * esz / 1e9), "parallelism": f"replicas x{world}",
                    "head_full_frac": args.head_full_frac,
-                   "trees": "curvature-chosen (kvc_tree_cuts)" if args.tree_cuts else "midpoint"},
+                   "trees": ("curvature-chosen (kvc_tree_cuts)" if args.tree_cuts else "midpoint")
+                            + (", three-way salient child sets" if args.salient else "")},
         "breakdown_ms": {"score": score_ms, "select": sel_ms, "merge_pack": pack_ms,
                          "decode_per_step": dec_ms, "decode_total": dec_ms * D},
         "compress_tokens_per_s": tokens / ((score_ms + sel_ms + pack_ms) * 1e-3),
@@ -738,8 +747,9 @@ def run_gpu(args, cfg, rank, world):
         "evict_per_step_next_f2": evict,
         "tree_cuts_next_f3": tree,
         "parity": parity_record(cfg.name) if (cfg.name == "mistral16k" and not args.layers
-                                              and not args.tree_cuts
+                                              and not args.tree_cuts and not args.salient
                                               and args.head_full_frac == 0.0) else None,
+        "salient_next_f3": salient_stat,
         "gpu_launches": launches,
         "gpu_launches_detail": {"issued_by_host": host_launches,
                                 "in_graph_replays": graph_launches,
@@ -1076,6 +1086,8 @@ def main():
                     help="head-level hybrid: fraction of heads that keep the full cache")
     ap.add_argument("--tree-cuts", action="store_true",
                     help="curvature-chosen prototype trees (kvc_tree_cuts) instead of midpoint trees")
+    ap.add_argument("--salient", action="store_true",
+                    help="three-way salient-token child sets in the prototype trees")
     ap.add_argument("--evict", action="store_true",
                     help="time the per-step top-B eviction (DistillCache) leg also under --profile")
     ap.add_argument("--no-evict", action="store_true",

@@ -104,19 +104,37 @@ typedef struct kvc_params {
   double  head_full_frac;  /* [DC] App. E.3 head-level hybrid: the
                               floor(frac*L*H) heads with the largest relevance
                               mass outside the window keep every token; 0 = off */
-  const uint8_t* tree_cuts;/* [GK] "Technical details": curvature-chosen trees.
+  uint8_t* tree_cuts;      /* [GK] "Technical details": curvature-chosen trees.
                               Device array [B, L, H, S_max, 8] (row (b*L + l)*H
                               + h, slot s): byte j < 7 is the cut of internal
                               node j (breadth-first; node j covers [a, b) and
                               its children [a, t), [t, b)) as an offset t - x0
-                              from the slot start x0; byte 7 is unused.  Usually
-                              written by kvc_tree_cuts.  kvc_score,
+                              from the slot start x0; byte 7 holds the salient
+                              flags (below, 0 without salient extraction).
+                              Usually written by kvc_tree_cuts.  kvc_score,
                               kvc_select and kvc_merge_pack read it; a cut that
                               leaves a child fewer than 2 or more than 16
                               tokens per leaf below it is replaced by the
-                              midpoint (and kvc_score records KVC_EDEVICE).  NULL = the depth-3 midpoint trees.
-                              The three calls of one compression must see the
-                              same table.                                        */
+                              midpoint (and kvc_score records KVC_EDEVICE).
+                              NULL = the depth-3 midpoint trees (an all-zero
+                              table gives the same trees).  The three calls of
+                              one compression must see the same table.        */
+  int32_t salient_extract; /* [GK] "Technical details": tree construction may
+                              isolate a salient token with a three-way child
+                              set.  Non-zero: kvc_score decides, after the
+                              relevance hops, for every depth-2 node j = 3..6
+                              covering [a, b) of the binary tree, its most
+                              relevant token t (largest relevance, ties to the
+                              smaller position, fp32); when both sides keep
+                              2..15 tokens the node's children become [a, t),
+                              the token t, [t+1, b) (its split costs 2), and
+                              kvc_score records the choice in tree_cuts (byte j
+                              = t - x0, bit j - 3 of byte 7 set), which must
+                              then be non-NULL and hold the binary cuts (a
+                              fresh kvc_tree_cuts output, or zeros for the
+                              midpoint trees) when kvc_score starts; kvc_select
+                              and kvc_merge_pack then follow the three-way
+                              trees.  0 = binary trees only (byte 7 must be 0).*/
 } kvc_params;
 
 /* Human-readable name of a status code (static string). */

@@ -9,7 +9,8 @@
 #include "kvc_internal.h"
 
 #include <cstddef>
-static_assert(sizeof(kvc_params) == 136, "kvc_params layout");
+static_assert(sizeof(kvc_params) == 144, "kvc_params layout");
+static_assert(offsetof(kvc_params, salient_extract) == 136, "kvc_params layout");
 static_assert(offsetof(kvc_params, tree_cuts) == 128, "kvc_params layout");
 static_assert(offsetof(kvc_params, head_full_frac) == 120, "kvc_params layout");
 static_assert(offsetof(kvc_params, packed_rows) == 112, "kvc_params layout");

@@ -207,7 +207,21 @@ __device__ __forceinline__ int tree_cut(const uint8_t* cuts, int j, int depth, i
 __device__ __forceinline__ int tree_depth(int j) {
   return (j >= 7) ? 3 : (j >= 3) ? 2 : (j >= 1) ? 1 : 0;
 }
-// Token range [a, b) of node j.
+// Whether depth-2 node [a, b) may isolate token t (a three-way child set [a, t),
+// t, [t+1, b)): both sides keep 2..15 tokens.
+__device__ __forceinline__ bool tree_extract_valid(int t, int a, int b) {
+  const int l = t - a, r = b - t - 1;
+  return l >= 2 && l <= 15 && r >= 2 && r <= 15;
+}
+// The salient token isolated by depth-2 node j (3..6) covering [a, b), or -1:
+// bit j - 3 of byte 7 set and byte j = t - x0 a valid three-way cut.
+__device__ __forceinline__ int tree_extract(const uint8_t* cuts, int j, int x0, int a, int b) {
+  if (!cuts || j < 3 || j > 6 || !((cuts[7] >> (j - 3)) & 1)) return -1;
+  const int t = x0 + (int)cuts[j];
+  return tree_extract_valid(t, a, b) ? t : -1;
+}
+// Token range [a, b) of node j (the leaves below a three-way depth-2 node
+// exclude its salient token).
 __device__ __forceinline__ void tree_node_range(const uint8_t* cuts, int j, int x0, int y0,
                                                 int& a, int& b) {
   const int depth = tree_depth(j);
@@ -215,8 +229,14 @@ __device__ __forceinline__ void tree_node_range(const uint8_t* cuts, int j, int 
   a = x0; b = y0;
   int node = 0;
   for (int lvl = depth - 1; lvl >= 0; --lvl) {
+    const bool right = (k >> lvl) & 1;
+    const int e = depth - 1 - lvl == 2 ? tree_extract(cuts, node, x0, a, b) : -1;
+    if (e >= 0) {
+      if (right) { a = e + 1; node = 2 * node + 2; } else { b = e; node = 2 * node + 1; }
+      continue;
+    }
     const int t = tree_cut(cuts, node, depth - 1 - lvl, x0, a, b);
-    if ((k >> lvl) & 1) { a = t; node = 2 * node + 2; } else { b = t; node = 2 * node + 1; }
+    if (right) { a = t; node = 2 * node + 2; } else { b = t; node = 2 * node + 1; }
   }
 }
 // Cut table of slot s of (b,l,h) blh (8 bytes per slot, cuts of nodes 0..6 as

@@ -41,11 +41,17 @@ __device__ __forceinline__ void node_range(const uint8_t* cuts, int j, int x0, i
 }
 
 // Stored entries of one slot tree: sum over taken ops of their cost
-// (Add 1, internal Split 1, leaf Split = leaf size - 1).
+// (Add 1, internal Split 1, three-way depth-2 Split 2, leaf Split = leaf size - 1).
 __device__ __forceinline__ int tree_entries(const uint8_t* cuts, const uint8_t* tk, int x0,
                                             int y0) {
   int n = 0;
   for (int o = 0; o < 8; ++o) n += tk[o] ? 1 : 0;
+  for (int j = 3; j < 7; ++j)
+    if (tk[1 + j]) {
+      int a, b;
+      node_range(cuts, j, x0, y0, a, b);
+      n += kvcd::tree_extract(cuts, j, x0, a, b) >= 0 ? 1 : 0;
+    }
   for (int j = 7; j < 15; ++j)
     if (tk[1 + j]) {
       int a, b;
@@ -321,19 +327,27 @@ __global__ void __launch_bounds__(32 * kPackWarps, 32 / kPackWarps)
   if (!(taken & 1u)) return;
   const uint8_t* cuts = kvcd::tree_cuts_of(p, blh, s);
   int64_t dst = base + sbase;
-  // left-to-right frontier walk with an explicit stack (depth <= 4)
+  // left-to-right frontier walk with an explicit stack (depth <= 4); an entry
+  // -1 - t stands for the salient token t a three-way depth-2 node isolates
   int stack[8];
   int sp = 0;
   stack[sp++] = 0;
   while (sp > 0) {
     const int j = stack[--sp];
+    if (j < 0) {
+      copy_exact<T, D>(a, Kh, Vh, -1 - j, 1, dst, lane);
+      ++dst;
+      continue;
+    }
     int x, y;
     node_range(cuts, j, x0, y0, x, y);
     if (!((taken >> (1 + j)) & 1u)) {
       write_prototype<T, D>(p, a, Kh, Vh, rh, x, y, dst, lane);
       ++dst;
     } else if (j < 7) {
+      const int e = j >= 3 ? kvcd::tree_extract(cuts, j, x0, x, y) : -1;
       stack[sp++] = 2 * j + 2;
+      if (e >= 0) stack[sp++] = -1 - e;
       stack[sp++] = 2 * j + 1;
     } else {
       copy_exact<T, D>(a, Kh, Vh, x, y - x, dst, lane);

@@ -512,6 +512,15 @@ __device__ __forceinline__ void node_range(const uint8_t* cuts, int j, int x0, i
   kvcd::tree_node_range(cuts, j, x0, y0, x, y);
 }
 
+// Cost of Split(node j), j < 7: a three-way depth-2 node stores three entries
+// in place of one (2), every other internal node two (1).
+__device__ __forceinline__ int internal_split_cost(const uint8_t* cuts, int j, int x0, int y0) {
+  if (j < 3 || !cuts) return 1;
+  int x, y;
+  node_range(cuts, j, x0, y0, x, y);
+  return kvcd::tree_extract(cuts, j, x0, x, y) >= 0 ? 2 : 1;
+}
+
 template <int D>
 struct NodeSmem {
   float K[128][D];
@@ -716,6 +725,21 @@ __global__ void __launch_bounds__(256, 1) nodes_kernel(kvc_params p, ScoreArgs a
 #pragma unroll
           for (int t = 0; t < VPL; ++t) Ud2[r][t] += Ul[r][t];
         }
+        if (j & 1) {                               // left leaf: the isolated token follows
+          int x2, y2;
+          node_range(cuts, (j - 1) / 2, x0, y0, x2, y2);
+          const int e = kvcd::tree_extract(cuts, (j - 1) / 2, x0, x2, y2);
+          if (e >= 0) {
+            const float4 av = *reinterpret_cast<const float4*>(&sm.A[e - x0][rq]);
+            const float aa[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              Ad2[r] += aa[r];
+#pragma unroll
+              for (int t = 0; t < VPL; ++t) Ud2[r][t] = fmaf(aa[r], sm.V[e - x0][lane * VPL + t], Ud2[r][t]);
+            }
+          }
+        }
         if ((j & 1) == 0) {                        // right child: depth-2 node done
           const int j2 = (j - 1) / 2;
           finish_node<D>(sm, j2, rq, Ad2, Ud2, lane);
@@ -774,7 +798,7 @@ __global__ void __launch_bounds__(256, 1) nodes_kernel(kvc_params p, ScoreArgs a
       int c;
       if (j < 7) {
         g = gainf(Dn[j] - Dn[2 * j + 1] - Dn[2 * j + 2], Dd[j]);
-        c = 1;
+        c = internal_split_cost(cuts, j, x0, y0);
       } else {
         int x, y;
         node_range(cuts, j, x0, y0, x, y);
@@ -938,11 +962,8 @@ __global__ void __launch_bounds__(32 * kProtoWarps, 20 / kProtoWarps)
   unsigned char* out = proto + tree * kvc::kProtoBytes;
   const float inv_pos = 1.f / (float)max(n - 1, 1);
   float nv_sum = 0.f;                                    // sum of |v| over the slot's tokens
-  for (int L = 0; L < 8; ++L) {
-    int x, y;
-    node_range(cuts, 7 + L, x0, y0, x, y);
-    ProtoAcc leaf;
-    leaf.zero();
+  // tokens [x, y) into `acc` (and their |v| and position features)
+  auto stream = [&](int x, int y, ProtoAcc& leaf) {
     // tokens in groups of 4: all loads of a group first, then four interleaved
     // |u| reductions
     for (int i0 = x; i0 < y; i0 += 4) {
@@ -1007,8 +1028,26 @@ __global__ void __launch_bounds__(32 * kProtoWarps, 20 / kProtoWarps)
         }
       }
     }
+  };
+  for (int L = 0; L < 8; ++L) {
+    int x, y;
+    node_range(cuts, 7 + L, x0, y0, x, y);
+    ProtoAcc leaf;
+    leaf.zero();
+    stream(x, y, leaf);
     proto_finish(a, p.value_floor, 7 + L, x, y, leaf, out, lane);
     acc_to_smem(lv, 0, leaf, lane, (L & 1) != 0);           // depth 2 = leaf pair
+    if (!(L & 1)) {                                          // and its isolated token
+      int x2, y2;
+      node_range(cuts, 3 + (L >> 1), x0, y0, x2, y2);
+      const int e = kvcd::tree_extract(cuts, 3 + (L >> 1), x0, x2, y2);
+      if (e >= 0) {
+        ProtoAcc tok;
+        tok.zero();
+        stream(e, e + 1, tok);
+        acc_to_smem(lv, 0, tok, lane, true);
+      }
+    }
     if (L & 1) {
       const int j2 = 3 + (L >> 1);
       node_range(cuts, j2, x0, y0, x, y);
@@ -1085,7 +1124,7 @@ __global__ void ops_kernel(kvc_params p, ScoreArgs a, const unsigned char* proto
     int c;
     if (j < 7) {
       g = gainf(Dn[j] - Dn[2 * j + 1] - Dn[2 * j + 2], Dd[j]);
-      c = 1;
+      c = internal_split_cost(cuts, j, x0, y0);
     } else {
       int x, y;
       node_range(cuts, j, x0, y0, x, y);
@@ -1135,11 +1174,59 @@ __global__ void cuts_check_kernel(kvc_params p, ScoreArgs a) {
   for (int j = 0; j < 7; ++j) {
     int x, y;
     kvcd::tree_node_range(cuts, j, x0, y0, x, y);
-    if (!kvcd::tree_cut_valid(x0 + (int)cuts[j], kvcd::tree_depth(j), x, y)) {
+    const bool three = j >= 3 && ((cuts[7] >> (j - 3)) & 1);
+    const bool ok = three ? kvcd::tree_extract_valid(x0 + (int)cuts[j], x, y)
+                          : (cuts[j] == 0 ||     // unset: the midpoint
+                             kvcd::tree_cut_valid(x0 + (int)cuts[j], kvcd::tree_depth(j), x, y));
+    if (!ok) {
       kvcd::record_error(a.err, KVC_EDEVICE);
       return;
     }
   }
+}
+
+// Three-way salient child sets ([GK] "Technical details and default settings":
+// tree construction may isolate a salient token with a three-way child set).
+// One warp per slot tree, after the relevance hops: each depth-2 node j = 3..6
+// covering [a, b) (at most 32 tokens, one per lane) takes its most relevant
+// token t (largest relevance, ties to the smaller position); when both sides
+// keep 2..15 tokens the node isolates it: byte j = t - x0 and bit j - 3 of
+// byte 7 are set, otherwise the bit is cleared and byte j (the binary cut) is
+// left as it is.
+__global__ void salient_kernel(kvc_params p, ScoreArgs a) {
+  const long long tree = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (tree >= (long long)p.B * p.L * p.H * p.S_max) return;
+  const int s = (int)(tree % p.S_max);
+  const long long blh = tree / p.S_max;
+  const int b = seq_of(p, blh);
+  const int lh = (int)(blh % ((long long)p.L * p.H));
+  if (!a.ok[blh] || s >= a.n_slots[b]) return;
+  const int n = a.ctx_len[b];
+  const int x0 = a.bounds[(long long)b * (p.S_max + 1) + s];
+  const int y0 = a.bounds[(long long)b * (p.S_max + 1) + s + 1];
+  uint8_t* cuts = p.tree_cuts + ((long long)blh * p.S_max + s) * 8;
+  const float* rel = a.rel + kvcd::seq_token_base(a.ctx_len, b, p.L * p.H) + (int64_t)lh * n;
+  unsigned flags = 0;
+#pragma unroll
+  for (int j = 3; j < 7; ++j) {
+    int x, y;
+    node_range(cuts, j, x0, y0, x, y);           // depth-2 ranges: cuts of nodes 0..2 only
+    const int i = x + lane;
+    float best = i < y ? rel[i] : -INFINITY;
+    int bi = i < y ? i : 0x7fffffff;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ob = __shfl_xor_sync(KVC_FULL_MASK, best, o);
+      const int oi = __shfl_xor_sync(KVC_FULL_MASK, bi, o);
+      if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
+    }
+    if (bi != 0x7fffffff && kvcd::tree_extract_valid(bi, x, y)) {
+      flags |= 1u << (j - 3);
+      if (lane == 0) cuts[j] = (uint8_t)(bi - x0);
+    }
+  }
+  if (lane == 0) cuts[7] = (uint8_t)flags;
 }
 
 int chunk_for(const kvc_params* p) {
@@ -1270,6 +1357,10 @@ int launch_all(const kvc_params* p, ScoreArgs& a, cudaStream_t s) {
       if ((st = kvc::probe_tc_pass(kvc::kTcProp, t, rows_total, s)) != KVC_OK) return st;
       launches += 2;
     }
+    if (p->salient_extract) {
+      salient_kernel<<<(unsigned)((blh * p->S_max * 32 + 255) / 256), 256, 0, s>>>(*p, a);
+      ++launches;
+    }
     // prototypes, tensor-core node statistics, utilities
     if (timed) phase_mark(4, s);
     proto_kernel<T, D><<<(unsigned)((blh * p->S_max + kProtoWarps - 1) / kProtoWarps),
@@ -1311,6 +1402,10 @@ int launch_all(const kvc_params* p, ScoreArgs& a, cudaStream_t s) {
     rowcombine_kernel<true><<<(unsigned)blh, 256, 0, s>>>(*p, a);
     prop_kernel<T, D><<<g_tiles, 256, sm_tile, s>>>(*p, a);
     launches += 4;
+  }
+  if (p->salient_extract) {
+    salient_kernel<<<(unsigned)((blh * p->S_max * 32 + 255) / 256), 256, 0, s>>>(*p, a);
+    ++launches;
   }
   nodes_kernel<T, D><<<(unsigned)(blh * p->S_max), 256, sm_nodes, s>>>(*p, a);
   ++launches;
@@ -1358,6 +1453,7 @@ extern "C" int kvc_score(const kvc_params* p, const int32_t* ctx_len, const void
     return KVC_EWORKSPACE;
   if (kvc::lh_count(p) > 65535 || (long long)kvc::lh_count(p) * p->S_max > 0x7fffffffLL)
     return KVC_EINVAL;
+  if (p->salient_extract && !p->tree_cuts) return KVC_EINVAL;   // the choice is written there
   int32_t* err = kvc::err_word();
   if (!err) return KVC_ECUDA;
   ScoreArgs a;

@@ -774,11 +774,12 @@ struct NodeSmem {
   alignas(1024) unsigned char Kh[kvc::kProtoHeadBytes]; // k^ parts (phase A operand), ln m, Rv
   alignas(16) float vh[15][128];                          // v^ of the slot's nodes
   float Al[8][128];                                       // per-row leaf masses
+  float At[4][128];                                       // per-row mass of each isolated token
   float red[2][4][15][4];                                 // per-quarter node sums
   uint64_t k_full, k_empty, v_full, v_empty, s_full, a_ready, b_done;
   uint64_t vh_full, vh_free;
   uint64_t nfull[2], nempty[2];
-  uint64_t mma_done;
+  uint64_t mma_done, mid_done;
   uint32_t tmem_base;
   int abort;
 };
@@ -880,6 +881,7 @@ __global__ void __maxnreg__(kNodeMaxRegs)
     kvcd::mbar_init(&sm.s_full, 1); kvcd::mbar_init(&sm.a_ready, kEpiWarps);
     kvcd::mbar_init(&sm.b_done, 1);
     kvcd::mbar_init(&sm.mma_done, 1);
+    kvcd::mbar_init(&sm.mid_done, 1);
     kvcd::mbar_init(&sm.vh_full, 1); kvcd::mbar_init(&sm.vh_free, kEpiWarps);
     for (int i = 0; i < 2; ++i) {
       kvcd::mbar_init(&sm.nfull[i], 1);
@@ -950,7 +952,25 @@ __global__ void __maxnreg__(kNodeMaxRegs)
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
+      int nmid = 0;                                  // uses of mid_done so far
       for (int k = 0; k < nsl; ++k) {
+        // key slot of each depth-2 node's isolated token in its left leaf's
+        // box (-1: none); the token counts in the node and its ancestors but
+        // not in the leaf, so its V rows are zeroed before the leaf products
+        int salc[4];
+        bool sal_any = false;
+        {
+          const int s = s_begin + k;
+          const uint8_t* cuts = a.tree_cuts ? a.tree_cuts + (blh * a.S_max + s) * 8 : nullptr;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            int a2, b2;
+            kvcd::tree_node_range(cuts, 3 + g, bd[s], bd[s + 1], a2, b2);
+            const int e = kvcd::tree_extract(cuts, 3 + g, bd[s], a2, b2);
+            salc[g] = e >= 0 ? e - a2 : -1;
+            sal_any |= e >= 0;
+          }
+        }
         if (!kvcd::mbar_wait(&sm.k_full, (uint32_t)(k & 1), a.wait_ns)) { *abort_flag = 1; break; }
         tc_fence_after();
 #pragma unroll
@@ -970,6 +990,22 @@ __global__ void __maxnreg__(kNodeMaxRegs)
         bool ok = true;
         for (int j = 0; j < 15; ++j) {
           const int nn = k * 15 + j, bf = nn & 1;
+          if (j == 7 && sal_any) {                   // depth-2 products done: drop the isolated rows
+            mma_commit(&sm.mid_done);
+            if (!kvcd::mbar_wait(&sm.mid_done, (uint32_t)(nmid & 1), a.wait_ns)) { ok = false; break; }
+            ++nmid;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              if (salc[g] < 0) continue;
+#pragma unroll
+              for (int fb = 0; fb < 2; ++fb) {
+                uint4* row = reinterpret_cast<uint4*>(&sm.Vt[fb][(2 * g) * 2048 + salc[g] * 128]);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
+              }
+            }
+            kvcd::fence_proxy_async_smem();
+          }
           if (nn >= 2 && !kvcd::mbar_wait(&sm.nempty[bf], (uint32_t)(((nn >> 1) - 1) & 1), a.wait_ns)) { ok = false; break; }
           tc_fence_after();
           int l0, l1;
@@ -1025,12 +1061,16 @@ __global__ void __maxnreg__(kNodeMaxRegs)
           ah[j] = rv ? kvcd::ex2(sc) : 0.f;
         }
       }
-      int cnt0, cnt1;
+      int cnt0, cnt1, salc;
       {
         int st;
         leaf_range(cuts, 2 * g, x0, y0, st, cnt0);
         leaf_range(cuts, 2 * g + 1, x0, y0, st, cnt1);
+        int a2, b2;
+        kvcd::tree_node_range(cuts, 3 + g, x0, y0, a2, b2);
+        salc = kvcd::tree_extract(cuts, 3 + g, x0, a2, b2) >= 0 ? 1 : 0;   // at column cnt0
       }
+      float at_acc = 0.f;                              // a of the isolated token
       if (k >= 1 && !*abort_flag && !kvcd::mbar_wait(&sm.b_done, (uint32_t)((k - 1) & 1), a.wait_ns))
         *abort_flag = 1;
       float lsum[2];
@@ -1040,6 +1080,7 @@ __global__ void __maxnreg__(kNodeMaxRegs)
         tmem_ld16_nw(tmem + lane_off + (uint32_t)(32 * g + 16 * hq), v);
         tmem_wait();
         const int cntl = hq ? cnt1 : cnt0;
+        const int cntv = hq ? cnt1 : cnt0 + salc;      // key slots that carry a
         float sacc = 0.f;
         uint32_t pk[3][8];
 #pragma unroll
@@ -1047,8 +1088,10 @@ __global__ void __maxnreg__(kNodeMaxRegs)
           float av[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u)
-            av[u] = (rv && t + u < cntl) ? kvcd::ex2(v[t + u] * a.q_scale2 - l2) : 0.f;
-          sacc += av[0] + av[1];
+            av[u] = (rv && t + u < cntv) ? kvcd::ex2(v[t + u] * a.q_scale2 - l2) : 0.f;
+          const float in0 = t < cntl ? av[0] : 0.f, in1 = t + 1 < cntl ? av[1] : 0.f;
+          sacc += in0 + in1;
+          at_acc += (av[0] - in0) + (av[1] - in1);     // the isolated token's column only
           // a = p0 + p1 + p2 in bf16 pairs (element t in the low half)
           const __nv_bfloat162 p0 = __floats2bfloat162_rn(av[0], av[1]);
           const float2 f0 = __bfloat1622float2(p0);
@@ -1074,6 +1117,7 @@ __global__ void __maxnreg__(kNodeMaxRegs)
       }
       sm.Al[2 * g][rl] = lsum[0];
       sm.Al[2 * g + 1][rl] = lsum[1];
+      sm.At[g][rl] = at_acc;
       kvcd::fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -1085,7 +1129,8 @@ __global__ void __maxnreg__(kNodeMaxRegs)
 #pragma unroll
         for (int l = 0; l < 8; ++l) an[7 + l] = sm.Al[l][rl];
 #pragma unroll
-        for (int j = 6; j >= 0; --j) an[j] = an[2 * j + 1] + an[2 * j + 2];
+        for (int j = 6; j >= 0; --j)
+          an[j] = an[2 * j + 1] + an[2 * j + 2] + (j >= 3 ? sm.At[j - 3][rl] : 0.f);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           float v = 0.f;

@@ -71,18 +71,25 @@ __device__ __forceinline__ int op_parent(int o) {
 }
 
 // Depth-1, depth-2 and leaf node of token i in slot [x0, y0) (tree with cut
-// table `cuts`, or the midpoint tree when null).
+// table `cuts`, or the midpoint tree when null); leaf = -1 for the salient
+// token a three-way depth-2 node isolates (its depth-2 split makes it exact).
 __device__ __forceinline__ void token_path(const uint8_t* cuts, int i, int x0, int y0, int& d1,
                                            int& d2, int& leaf) {
   int a = x0, b = y0, j = 0;
   int path[3];
 #pragma unroll
-  for (int lvl = 0; lvl < 3; ++lvl) {
+  for (int lvl = 0; lvl < 2; ++lvl) {
     const int t = kvcd::tree_cut(cuts, j, lvl, x0, a, b);
     if (i < t) { j = 2 * j + 1; b = t; } else { j = 2 * j + 2; a = t; }
     path[lvl] = j;
   }
-  d1 = path[0]; d2 = path[1]; leaf = path[2];
+  d1 = path[0]; d2 = path[1];
+  const int e = kvcd::tree_extract(cuts, d2, x0, a, b);
+  if (e >= 0) {
+    leaf = i == e ? -1 : (i < e ? 2 * d2 + 1 : 2 * d2 + 2);
+  } else {
+    leaf = i < kvcd::tree_cut(cuts, d2, 2, x0, a, b) ? 2 * d2 + 1 : 2 * d2 + 2;
+  }
 }
 
 __device__ __forceinline__ void node_range(const uint8_t* cuts, int j, int x0, int y0, int& a,
@@ -199,9 +206,10 @@ __global__ void floor_weights_kernel(kvc_params p, const int32_t* ctx_len,
     if (k != 0) {
       int d1, d2, leaf;
       token_path(cuts, i, x0, y0, d1, d2, leaf);
-      if (k == s_gmax[w][leaf]) {
-        c = cost[1 + leaf];
-        if (k == s_gmax[w][d2]) c += cost[1 + d2];
+      const int ex = leaf >= 0 ? leaf : d2;            // the split that makes token i exact
+      if (k == s_gmax[w][ex]) {
+        c = cost[1 + ex];
+        if (leaf >= 0 && k == s_gmax[w][d2]) c += cost[1 + d2];
         if (k == s_gmax[w][d1]) c += cost[1 + d1];
         if (k == s_gmax[w][0]) c += cost[0] + cost[1];
       }
@@ -412,7 +420,8 @@ __global__ void floor_mark_kernel(kvc_params p, const int32_t* ctx_len,
     if (k <= stop) continue;
     int d1, d2, leaf;
     token_path(cuts, i, x0, y0, d1, d2, leaf);
-    tk[0] = 1; tk[1] = 1; tk[1 + d1] = 1; tk[1 + d2] = 1; tk[1 + leaf] = 1;
+    tk[0] = 1; tk[1] = 1; tk[1 + d1] = 1; tk[1 + d2] = 1;
+    if (leaf >= 0) tk[1 + leaf] = 1;
     spent += (unsigned long long)c;
     toks += 1;
   }

@@ -41,6 +41,7 @@ class kvc_params(ctypes.Structure):
         ("packed_rows", c_int64),
         ("head_full_frac", c_double),
         ("tree_cuts", ctypes.c_void_p),
+        ("salient_extract", c_int32),
     ]
 
 

@@ -31,11 +31,15 @@ def packed_capacity(p: kvc.kvc_params, ctx_len: Sequence[int]) -> int:
 
 class Compressor:
     def __init__(self, p: kvc.kvc_params, ctx_len: Sequence[int], device="cuda",
-                 tensor_cores: bool = True, tree_cuts: bool = False):
+                 tensor_cores: bool = True, tree_cuts: bool = False, salient: bool = False):
         """tree_cuts=True: every scoring call first runs kvc_tree_cuts, and
         scoring, selection and packing use those curvature-chosen trees
         (p.tree_cuts points at this object's cut table); otherwise the
-        midpoint trees."""
+        midpoint trees.  salient=True: the depth-2 nodes may isolate their most
+        relevant token in a three-way child set (kvc_params.salient_extract);
+        kvc_score records the choice in the cut table, which is reset to the
+        binary cuts (kvc_tree_cuts, or zeros for midpoint trees) before every
+        scoring call."""
         self.p = p
         self.device = device
         self.ctx_host = [int(n) for n in ctx_len]
@@ -74,8 +78,11 @@ class Compressor:
         self.ws_pack = kvc.workspace(kvc.KVC_WS_PACK, p, device)
         self.ws_decode = kvc.workspace(kvc.KVC_WS_DECODE, p, device, zero=True)
         self.tree_kappa = torch.empty((rows,), dtype=f32, **z) if tree_cuts else None
-        self.cuts = torch.zeros((B, L, H, S, 8), dtype=torch.uint8, **z) if tree_cuts else None
-        p.tree_cuts = self.cuts.data_ptr() if tree_cuts else None
+        self.curvature_trees = bool(tree_cuts)
+        self.cuts = (torch.zeros((B, L, H, S, 8), dtype=torch.uint8, **z)
+                     if (tree_cuts or salient) else None)
+        p.tree_cuts = self.cuts.data_ptr() if self.cuts is not None else None
+        p.salient_extract = 1 if salient else 0
         self._graphs = {}
 
     # ---------------------------------------------------------------- calls
@@ -106,9 +113,12 @@ class Compressor:
 
     def score(self, K, V, Qp, slot_bounds, n_slots, head_sens=None, stream=None, graph=False):
         def run(st):
-            if self.cuts is not None:
+            if self.curvature_trees:
                 kvc.kvc_tree_cuts(self.p, self.ctx_len, K, self.rope_cos, self.rope_sin,
                                   slot_bounds, n_slots, self.tree_kappa, self.cuts, st)
+            elif self.cuts is not None:              # midpoint trees: an all-zero table
+                with torch.cuda.stream(torch.cuda.current_stream() if st is None else st):
+                    self.cuts.zero_()
             kvc.kvc_score(self.p, self.ctx_len, K, V, Qp, self.rope_cos, self.rope_sin,
                           slot_bounds, n_slots, head_sens, self.lse, self.feats, self.relevance,
                           self.op_util, self.op_cost, self.ws_score, st)
@@ -184,7 +194,11 @@ class Compressor:
             cur.wait_event(events[c])
             pc = kvc.kvc_params.from_buffer_copy(p)
             pc.L = l1 - l0
-            if self.cuts is not None:
+            if self.cuts is not None and not self.curvature_trees:
+                pc.tree_cuts = self.cuts[:, l0:l1].data_ptr()
+                with torch.cuda.stream(cur):
+                    self.cuts[:, l0:l1].zero_()
+            if self.curvature_trees:
                 pc.tree_cuts = self.cuts[:, l0:l1].data_ptr()
                 kvc.kvc_tree_cuts(pc, self.ctx_len, K[r0:r1], self.rope_cos, self.rope_sin,
                                   slot_bounds, n_slots, self.tree_kappa[r0:r1],

@@ -48,7 +48,7 @@ def params_for(cfg, n_max=None, S_max=None, **over):
     return kvc.make_params(**kw)
 
 
-def upload_workload(wl, tensor_cores=True, tree_cuts=False, **over):
+def upload_workload(wl, tensor_cores=True, tree_cuts=False, salient=False, **over):
     """Device copies of a synthetic workload plus a Compressor sized for it."""
     from kv_cache_compression_probe_gb300.pipeline import Compressor, pad_bounds
     cfg = wl.cfg
@@ -62,7 +62,8 @@ def upload_workload(wl, tensor_cores=True, tree_cuts=False, **over):
              bounds=dev(pad_bounds([s.slot_bounds for s in wl.seqs], S_max)),
              n_slots=dev(np.asarray([len(s.slot_bounds) - 1 for s in wl.seqs], np.int32)),
              sens=dev(wl.head_sens))
-    comp = Compressor(p, [s.n for s in wl.seqs], tensor_cores=tensor_cores, tree_cuts=tree_cuts)
+    comp = Compressor(p, [s.n for s in wl.seqs], tensor_cores=tensor_cores, tree_cuts=tree_cuts,
+                      salient=salient)
     return p, comp, d, S_max
 
 

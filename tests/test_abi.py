@@ -47,8 +47,9 @@ def test_host_only_calls(lib):
 
 def test_params_struct_layout_matches_header():
     from kv_cache_compression_probe_gb300 import kvc
-    assert ctypes.sizeof(kvc.kvc_params) == 136
+    assert ctypes.sizeof(kvc.kvc_params) == 144
     assert kvc.kvc_params.tree_cuts.offset == 128
+    assert kvc.kvc_params.salient_extract.offset == 136
     assert kvc.kvc_params.total_ctx.offset == 104
     assert kvc.kvc_params.packed_rows.offset == 112
     assert kvc.kvc_params.head_full_frac.offset == 120
