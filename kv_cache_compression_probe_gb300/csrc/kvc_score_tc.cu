@@ -590,7 +590,10 @@ __global__ void __maxnreg__(kRsMaxRegs)
       // FEATS: probe row c sees keys <= n - P + (c % P), i.e. c % P >= thr
       const int thr = MODE == kvc::kTcFeats ? key - (n - a.P) : 0;
       const bool full_cols = kvalid && thr <= 0;
-      float gs[8], sh = 0.f, acc = 0.f;
+      // with P equal to the share width every share is one query head: its
+      // head sum and its sum of a H are all the other shares need
+      const bool one_head = MODE == kvc::kTcFeats && a.P == kCW && a.G == 4;
+      float gs[8], sh = 0.f, acc = 0.f, own = 0.f;
 #pragma unroll
       for (int g = 0; g < 8; ++g) gs[g] = 0.f;
       const uint32_t col0 = tmem + lane_off + (uint32_t)(bf * kN + sp * kCW);
@@ -604,6 +607,9 @@ __global__ void __maxnreg__(kRsMaxRegs)
         const int cb = sp * kCW + c * kCh;           // first column of the batch
         const float4* ca = reinterpret_cast<const float4*>(&sm.col_a[cb]);
         const float4* cbv = reinterpret_cast<const float4*>(&sm.col_b[cb]);
+        // the same column parameters read as packed pairs (column 2i in the low half)
+        const ulonglong2* ca2 = reinterpret_cast<const ulonglong2*>(&sm.col_a[cb]);
+        const ulonglong2* cb2 = reinterpret_cast<const ulonglong2*>(&sm.col_b[cb]);
         float cs = 0.f, chs = 0.f;
         if (full_cols) {
           // unmasked batch on packed pairs: t = S c - LSE, e = 2^t,
@@ -612,17 +618,17 @@ __global__ void __maxnreg__(kRsMaxRegs)
           uint64_t s1 = f2(0.f, 0.f), s2 = f2(0.f, 0.f);
 #pragma unroll
           for (int j4 = 0; j4 < kCh / 4; ++j4) {
-            const float4 la = ca[j4], lb = cbv[j4];
-            const uint64_t t0 = fma2(f2(v[4 * j4], v[4 * j4 + 1]), c2, f2(la.x, la.y));
-            const uint64_t t1 = fma2(f2(v[4 * j4 + 2], v[4 * j4 + 3]), c2, f2(la.z, la.w));
+            const ulonglong2 la = ca2[j4], lb = cb2[j4];
+            const uint64_t t0 = fma2(f2(v[4 * j4], v[4 * j4 + 1]), c2, la.x);
+            const uint64_t t1 = fma2(f2(v[4 * j4 + 2], v[4 * j4 + 3]), c2, la.y);
             const float2 u0 = uf2(t0), u1 = uf2(t1);
             const uint64_t e0 = f2(kvcd::ex2(u0.x), kvcd::ex2(u0.y));
             const uint64_t e1 = f2(kvcd::ex2(u1.x), kvcd::ex2(u1.y));
             if (MODE == kvc::kTcFeats) {
               s1 = add2(s1, add2(e0, e1));
-              s2 = fma2(e0, f2(lb.x, lb.y), fma2(e1, f2(lb.z, lb.w), s2));
+              s2 = fma2(e0, lb.x, fma2(e1, lb.y, s2));
             } else {
-              s1 = fma2(e0, f2(lb.x, lb.y), fma2(e1, f2(lb.z, lb.w), s1));
+              s1 = fma2(e0, lb.x, fma2(e1, lb.y, s1));
             }
           }
           if (MODE == kvc::kTcFeats) {
@@ -653,10 +659,14 @@ __global__ void __maxnreg__(kRsMaxRegs)
           }
         }
         if (MODE == kvc::kTcFeats) {
-          const int head = cb / a.P;                 // P % 32 == 0: one head per batch
+          if (one_head) {
+            own += cs;
+          } else {
+            const int head = cb / a.P;               // P % 32 == 0: one head per batch
 #pragma unroll
-          for (int g = 0; g < 8; ++g)
-            if (g == head) gs[g] += cs;
+            for (int g = 0; g < 8; ++g)
+              if (g == head) gs[g] += cs;
+          }
           sh += chs;
         }
         if (c + 1 < kCW / kCh) {
@@ -675,9 +685,14 @@ __global__ void __maxnreg__(kRsMaxRegs)
       float (*xc)[kBN][9] = sm.xch[t & 1];
       if (sp > 0) {
         if (MODE == kvc::kTcFeats) {
+          if (one_head) {
+            xc[sp - 1][kl][0] = own;
+            xc[sp - 1][kl][1] = sh;
+          } else {
 #pragma unroll
-          for (int g = 0; g < 8; ++g) xc[sp - 1][kl][g] = gs[g];
-          xc[sp - 1][kl][8] = sh;
+            for (int g = 0; g < 8; ++g) xc[sp - 1][kl][g] = gs[g];
+            xc[sp - 1][kl][8] = sh;
+          }
         } else {
           xc[sp - 1][kl][0] = acc;
         }
@@ -689,11 +704,20 @@ __global__ void __maxnreg__(kRsMaxRegs)
           for (int o = 0; o < 3; ++o) acc += xc[o][kl][0];
           a.rel[row0 + key] = a.feats[(row0 + key) * 5] + a.hop_weight * acc;
         } else {
+          if (one_head) {
+            gs[0] = own;
 #pragma unroll
-          for (int o = 0; o < 3; ++o) {
+            for (int o = 0; o < 3; ++o) {
+              gs[1 + o] = xc[o][kl][0];
+              sh += xc[o][kl][1];
+            }
+          } else {
 #pragma unroll
-            for (int g = 0; g < 8; ++g) gs[g] += xc[o][kl][g];
-            sh += xc[o][kl][8];
+            for (int o = 0; o < 3; ++o) {
+#pragma unroll
+              for (int g = 0; g < 8; ++g) gs[g] += xc[o][kl][g];
+              sh += xc[o][kl][8];
+            }
           }
           float sa = 0.f, mean = 0.f;
 #pragma unroll

@@ -156,27 +156,35 @@ def decode_inputs(cfg, steps: int, device, dtype=torch.bfloat16, B=None):
 def hidden_states(cfg, b: int, n: int, planted: np.ndarray, device, dtype=torch.bfloat16,
                   noise: float = 0.002) -> torch.Tensor:
     """Piecewise-smooth hidden-state trajectory [n, hidden_dim] with turns at
-    ``planted`` (the recipe of ``synth.workloads.hidden_states``): inside a
-    segment the state moves one unit per token along a direction rotating at
-    0.01..0.03 rad/token in a random 2-plane; each boundary starts a new plane.
-    Accumulated in float64, rounded to `dtype`."""
+    ``planted`` (the recipe of ``synth.workloads.hidden_states``): the state
+    moves on the sphere of radius sqrt(dim) along a great circle at 0.02..0.06
+    rad per token; each boundary starts a new great circle through the
+    current state in a random direction.  Built in float64, rounded to `dtype`;
+    the segments' start states are chained in a short loop."""
     dim = cfg.hidden_dim
     g = torch.Generator(device=device)
     g.manual_seed(((cfg.seed * 1_000_003 + b) * 1_009 + 105) & 0x7FFFFFFFFFFFFFFF)
     full = np.asarray(planted, np.int64)
     if full[-1] != n:
         full = np.concatenate([full, [n]])
-    bd = torch.as_tensor(full, device=device)
     S = len(full) - 1
-    seg = torch.repeat_interleave(torch.arange(S, device=device), bd[1:] - bd[:-1])
-    t_in = (torch.arange(n, device=device) - bd[:-1][seg]).to(torch.float64)
-    e1 = _unit(torch.randn((S, dim), generator=g, device=device, dtype=torch.float64))
-    e2 = torch.randn((S, dim), generator=g, device=device, dtype=torch.float64)
-    e2 = _unit(e2 - (e2 * e1).sum(-1, keepdim=True) * e1)
-    om = 0.01 + 0.02 * torch.rand((S,), generator=g, device=device, dtype=torch.float64)
-    ang = om[seg] * t_in
-    h = torch.cos(ang)[:, None] * e1[seg] + torch.sin(ang)[:, None] * e2[seg]
-    h = torch.cumsum(h, dim=0)
-    h += 4.0 * torch.randn((dim,), generator=g, device=device, dtype=torch.float64)[None, :]
+    rho = float(np.sqrt(dim))
+    e2s = torch.randn((S, dim), generator=g, device=device, dtype=torch.float64)
+    oms = 0.02 + 0.04 * torch.rand((S,), generator=g, device=device, dtype=torch.float64)
+    cur = _unit(torch.randn((dim,), generator=g, device=device, dtype=torch.float64))
+    lens = np.diff(full)
+    starts = torch.empty((S, dim), device=device, dtype=torch.float64)
+    dirs = torch.empty((S, dim), device=device, dtype=torch.float64)
+    for s_ in range(S):
+        e2 = _unit(e2s[s_] - (e2s[s_] @ cur) * cur)
+        starts[s_], dirs[s_] = cur, e2
+        ang = oms[s_] * float(lens[s_])
+        cur = _unit(torch.cos(ang) * cur + torch.sin(ang) * e2)
+    seg = torch.repeat_interleave(torch.arange(S, device=device),
+                                  torch.as_tensor(lens, device=device))
+    t_in = (torch.arange(n, device=device) -
+            torch.as_tensor(full[:-1], device=device)[seg]).to(torch.float64)
+    ang = oms[seg] * t_in
+    h = rho * (torch.cos(ang)[:, None] * starts[seg] + torch.sin(ang)[:, None] * dirs[seg])
     h += noise * torch.randn((n, dim), generator=g, device=device, dtype=torch.float64)
     return h.to(torch.float32).to(dtype)

@@ -374,26 +374,30 @@ def hidden_states(cfg: Config, b: int, n: int, planted: np.ndarray,
                   dim: Optional[int] = None, noise: float = 0.002) -> np.ndarray:
     """Piecewise-smooth hidden-state trajectory [n, dim] with turns at ``planted``.
 
-    Within a segment the state moves one unit per token along a direction that
-    rotates slowly (0.01-0.03 rad/token) inside a random 2-plane; each planted
-    boundary starts a new random plane, so the direction of motion turns there.
+    The state moves on the sphere of radius sqrt(dim) (components of order 1,
+    so bf16 resolves the motion): inside a segment it travels along a great
+    circle at 0.02-0.06 rad per token; each planted boundary starts a new
+    great circle through the current state in a random direction, so the
+    direction of motion turns there while the state stays continuous.
     """
     dim = cfg.hidden_dim if dim is None else dim
     r = _rng(cfg, b, TAG_HID)
+    rho = np.sqrt(dim)
     h = np.empty((n, dim), dtype=np.float64)
-    cur = r.standard_normal(dim) * 4.0
+    cur = r.standard_normal(dim)
+    cur /= np.linalg.norm(cur)
     bounds = list(planted.astype(np.int64))
     if bounds[-1] != n:
         bounds.append(n)
     for s in range(len(bounds) - 1):
         x0, x1 = bounds[s], bounds[s + 1]
-        e1 = r.standard_normal(dim); e1 /= np.linalg.norm(e1)
-        e2 = r.standard_normal(dim); e2 -= (e2 @ e1) * e1; e2 /= np.linalg.norm(e2)
-        om = r.uniform(0.01, 0.03)
-        t = np.arange(x1 - x0, dtype=np.float64)
-        dirs = np.cos(om * t)[:, None] * e1[None, :] + np.sin(om * t)[:, None] * e2[None, :]
-        path = cur[None, :] + np.cumsum(dirs, axis=0)
-        h[x0:x1] = path
-        cur = path[-1]
+        e2 = r.standard_normal(dim)
+        e2 -= (e2 @ cur) * cur
+        e2 /= np.linalg.norm(e2)
+        om = r.uniform(0.02, 0.06)
+        ang = om * np.arange(x1 - x0 + 1, dtype=np.float64)
+        path = np.cos(ang)[:, None] * cur[None, :] + np.sin(ang)[:, None] * e2[None, :]
+        h[x0:x1] = rho * path[:-1]
+        cur = path[-1] / np.linalg.norm(path[-1])
     h += r.standard_normal((n, dim)) * noise
     return _to_dtype(cfg, h.astype(np.float32))
