@@ -5,15 +5,17 @@
 // averaged over the scales w in {1, 2, 4, 8} that fit, then a dynamic program
 // over cut positions in [0, n - W) maximising
 //   sum_{interior cuts c} kappa(c) - lambda * sum_slots ((len - 64) / 64)^2,
-// 16 <= len <= 128, lambda = mean of kappa over [0, n - W) (summed in index
-// order in double precision).  Ties go to the smaller previous cut.
+// 16 <= len <= 128, lambda = mean of kappa over [0, n - W) (summed in a
+// fixed order in double precision, see dp_kernel).  Ties go to the smaller
+// previous cut.
 //
 // Kernels: norms (one warp per row), curvature (one CTA per 64 positions; the
 // 80 rows it needs are staged 128 features at a time and each warp keeps the
-// 12 partial dot products of its positions), and the DP (one warp per
-// sequence: lanes score the 113 candidate lengths, fp64, ring buffer of the
-// last 129 best scores, back-pointers in the workspace).
+// 12 partial dot products of its positions), and the DP (one CTA per
+// sequence scoring 16 positions at a time, fp64, ring buffer of the last 256
+// best scores, back-pointers in the workspace).
 #include <float.h>
+#include <limits.h>
 
 #include "kvc_common.cuh"
 #include "kvc_internal.h"
@@ -108,60 +110,97 @@ __global__ void __launch_bounds__(256) curvature_kernel(kvc_params p, const int3
   }
 }
 
-// One warp per sequence.
-__global__ void dp_kernel(kvc_params p, const int32_t* ctx_len, const float* kappa,
-                          int16_t* back, int32_t* slot_bounds, int32_t* n_slots, int32_t* err) {
+// Candidate scores are compared as integers: for a double v that is not NaN
+// and not -0, key(v) orders like v.  The scores here are never -0 (the gains
+// and the penalties are never -0 and best[0] = +0), and -0 is mapped to +0.
+__device__ __forceinline__ long long order_key(double v) {
+  long long bits = __double_as_longlong(v);
+  if (bits == LLONG_MIN) bits = 0;
+  return bits >= 0 ? bits : bits ^ LLONG_MAX;
+}
+__device__ __forceinline__ double from_key(long long key) {
+  return __longlong_as_double(key >= 0 ? key : key ^ LLONG_MAX);
+}
+
+// One CTA of kDpWarps warps per sequence.  Every slot is at least kLmin
+// tokens long, so best[y] for the kLmin positions of a block [Y, Y + kLmin)
+// depends only on best[x] with x < Y: warp w scores position Y + w, its lanes
+// the candidate lengths, and the CTA synchronises once per block.  Each
+// candidate is scored as (best[x] - lambda * d^2) + gain in fp64, as in the
+// sequential recurrence, so the result does not depend on the blocking.
+constexpr int kDpWarps = kLmin;
+constexpr int kDpThreads = kDpWarps * 32;
+constexpr int kRing = 256;                                  // > kLmax + kDpWarps
+__global__ void __launch_bounds__(kDpThreads) dp_kernel(kvc_params p, const int32_t* ctx_len,
+                                                        const float* kappa, int16_t* back,
+                                                        int32_t* slot_bounds, int32_t* n_slots,
+                                                        int32_t* err) {
   const int b = blockIdx.x;
-  const int lane = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = ctx_len[b];
   const int end = n - p.W;
-  __shared__ double ring[kLmax + 1];                     // best[x] for x in (y - 129, y]
+  __shared__ double ring[kRing];                          // best[x] at x % kRing
+  __shared__ double pen[kLmax - kLmin + 1];               // lambda * ((len - 64) / 64)^2
+  __shared__ double part[kDpThreads];
   const float* kap = kappa + (int64_t)b * p.n_max;
   int16_t* bk = back + (int64_t)b * p.n_max;
   int32_t* bd = slot_bounds + (int64_t)b * (p.S_max + 1);
   if (end < kLmin || end > p.n_max) {
-    if (lane == 0) { kvcd::record_error(err, KVC_EDEVICE); n_slots[b] = 0; }
+    if (tid == 0) { kvcd::record_error(err, KVC_EDEVICE); n_slots[b] = 0; }
     return;
   }
-  // lambda = mean kappa over [0, end), summed in index order
-  double lam = 0.0;
-  if (lane == 0) {
-    for (int t = 0; t < end; ++t) lam += (double)kap[t];
-    lam /= (double)end;
+  // lambda = mean kappa over [0, end): thread i sums t = i, i + 512, ... in
+  // order, then the 512 partial sums are added pairwise, halving the stride
+  double acc = 0.0;
+  for (int t = tid; t < end; t += kDpThreads) acc += (double)kap[t];
+  part[tid] = acc;
+  __syncthreads();
+  for (int h = kDpThreads / 2; h > 0; h >>= 1) {
+    if (tid < h) part[tid] = part[tid] + part[tid + h];
+    __syncthreads();
   }
-  lam = __shfl_sync(KVC_FULL_MASK, lam, 0);
-  for (int i = lane; i <= kLmax; i += 32) ring[i] = -DBL_MAX;
-  __syncwarp();
-  if (lane == 0) ring[0] = 0.0;                           // best[0]
-  __syncwarp();
-  for (int y = 1; y <= end; ++y) {
-    const double gain = y < end ? (double)kap[y] : 0.0;
-    double bv = -DBL_MAX;
-    int bl = 0;                                           // best length (larger wins ties)
-    for (int ln = kLmin + lane; ln <= kLmax; ln += 32) {
-      const int x = y - ln;
-      if (x < 0) continue;
-      const double bx = ring[x % (kLmax + 1)];
-      if (bx == -DBL_MAX) continue;
-      const double d = (double)(ln - kTarget) / (double)kTarget;
-      const double v = bx - lam * (d * d) + gain;
-      if (v > bv || (v == bv && ln > bl)) { bv = v; bl = ln; }
-    }
+  const double lam = part[0] / (double)end;
+  const long long neg_bits = __double_as_longlong(-DBL_MAX);
+  if (tid <= kLmax - kLmin) {
+    const double d = (double)(tid + kLmin - kTarget) * (1.0 / (double)kTarget);   // exact
+    pen[tid] = lam * (d * d);
+  }
+  for (int i = tid; i < kRing; i += kDpThreads) ring[i] = i == 0 ? 0.0 : -DBL_MAX;
+  __syncthreads();
+  float g_next = warp + 1 < end ? kap[warp + 1] : 0.f;
+  for (int Y = 1; Y <= end; Y += kDpWarps) {
+    const int y = Y + warp;
+    const float g_now = g_next;
+    if (y + kDpWarps < end) g_next = kap[y + kDpWarps];  // next block's gain, in flight
+    if (y <= end) {                                       // warp-uniform
+      const double gain = y < end ? (double)g_now : 0.0;
+      long long bkey = LLONG_MIN;
+      int bl = 0;                                         // best length (larger wins ties)
+      for (int ln = kLmin + lane; ln <= kLmax; ln += 32) {
+        const int x = y - ln;
+        if (x < 0) break;
+        const double bx = ring[x & (kRing - 1)];
+        if (__double_as_longlong(bx) == neg_bits) continue;
+        const long long key = order_key((bx - pen[ln - kLmin]) + gain);
+        if (key >= bkey) { bkey = key; bl = ln; }         // ln ascends: ties go to the larger
+      }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const double ov = __shfl_xor_sync(KVC_FULL_MASK, bv, o);
-      const int ol = __shfl_xor_sync(KVC_FULL_MASK, bl, o);
-      if (ov > bv || (ov == bv && ol > bl)) { bv = ov; bl = ol; }
+      for (int o = 16; o > 0; o >>= 1) {
+        const long long ok = __shfl_xor_sync(KVC_FULL_MASK, bkey, o);
+        const int ol = __shfl_xor_sync(KVC_FULL_MASK, bl, o);
+        if (ok > bkey || (ok == bkey && ol > bl)) { bkey = ok; bl = ol; }
+      }
+      if (lane == 0) {
+        ring[y & (kRing - 1)] = bl > 0 ? from_key(bkey) : -DBL_MAX;
+        bk[y] = (int16_t)bl;
+      }
     }
-    __syncwarp();
-    if (lane == 0) {
-      ring[y % (kLmax + 1)] = bl > 0 ? bv : -DBL_MAX;
-      bk[y] = (int16_t)bl;
-    }
-    __syncwarp();
+    __syncthreads();
   }
-  if (lane == 0) {
-    if (ring[end % (kLmax + 1)] == -DBL_MAX) { kvcd::record_error(err, KVC_EDEVICE); n_slots[b] = 0; return; }
+  if (tid == 0) {
+    if (__double_as_longlong(ring[end & (kRing - 1)]) == neg_bits) {
+      kvcd::record_error(err, KVC_EDEVICE); n_slots[b] = 0; return;
+    }
     int cnt = 0;
     for (int y = end; y > 0 && cnt <= p.S_max; y -= bk[y]) {
       if (bk[y] < kLmin || bk[y] > y) { cnt = p.S_max + 1; break; }   // never for a reachable end
@@ -197,7 +236,7 @@ void launch(const kvc_params* p, const int32_t* ctx_len, const void* hidden, int
   norms_kernel<T><<<dim3((p->n_max + 7) / 8, p->B), 256, 0, s>>>(*p, ctx_len, h, dh, inv);
   curvature_kernel<T><<<dim3((p->n_max + kPosPerCta - 1) / kPosPerCta, p->B), 256, 0, s>>>(
       *p, ctx_len, h, dh, inv, kappa);
-  dp_kernel<<<p->B, 32, 0, s>>>(*p, ctx_len, kappa, back, bounds, n_slots, err);
+  dp_kernel<<<p->B, kDpThreads, 0, s>>>(*p, ctx_len, kappa, back, bounds, n_slots, err);
   kvc::count_launch(3);
 }
 

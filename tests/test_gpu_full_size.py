@@ -29,6 +29,7 @@ import oracle as O
 from synth import workloads as W
 from tests.gpu_helpers import (assert_bf16_close, assert_f32_close, dev, params_for,
                                token_view, upload_workload)
+from tests.partition_lambda import partition_lambda
 
 pytestmark = [pytest.mark.gpu, pytest.mark.gpu_full]
 
@@ -82,10 +83,7 @@ def _partition_on_device(kvc, cfg, wl):
         end = s.n - cfg.W
         hb = W.round_bf16(hid[b, :s.n]).astype(np.float64)
         assert np.abs(kg[b, :s.n] - O.curvature(hb)).max() < 2e-5
-        lam = 0.0
-        for t in range(end):
-            lam += float(kg[b, t])
-        cuts = O.partition_dp(kg[b], end, lam=lam / end)
+        cuts = O.partition_dp(kg[b], end, lam=partition_lambda(kg[b], end))
         np.testing.assert_array_equal(bg[b, :int(ng[b]) + 1], cuts)
         s.slot_bounds = cuts.astype(np.int32)
 

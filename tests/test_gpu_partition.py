@@ -9,6 +9,7 @@ import torch
 import oracle as O
 from synth import workloads as W
 from tests.gpu_helpers import DT, dev, params_for
+from tests.partition_lambda import partition_lambda
 
 pytestmark = pytest.mark.gpu
 
@@ -52,11 +53,7 @@ def test_partition_matches_oracle(kvc, dtype):
         # curvature: 1 - cos of fp32 differences; absolute tolerance
         assert np.abs(kg[b, :n] - ko).max() < 2e-5
         # the DP on the same kappa and the same lambda is bit-exact
-        lam = 0.0
-        for t in range(end):
-            lam += float(kg[b, t])
-        lam /= end
-        cuts = O.partition_dp(kg[b], end, lam=lam)
+        cuts = O.partition_dp(kg[b], end, lam=partition_lambda(kg[b], end))
         S = int(ng[b])
         np.testing.assert_array_equal(bg[b, :S + 1], cuts)
         assert all(16 <= y - x <= 128 for x, y in zip(cuts[:-1], cuts[1:]))

@@ -29,10 +29,23 @@ def built():
 _WL = {}
 
 
+# slot lengths whose depth-2 nodes span every case of the three-way rule: 4
+# tokens (never), 5 (only t = a + 2), 6..8, 15..16, 31 (only t = a + 15), 32
+# (never), 18..19
+EDGE_SLOTS = (16, 20, 24, 31, 62, 124, 128, 75)
+
+
 def _workload(name):
     if name not in _WL:
-        cfg = W.get_config("tiny") if name == "tiny" else W.small_config()
-        _WL[name] = W.make_workload(cfg)
+        if name == "edges":
+            wl = W.make_workload(W.get_config("tiny"))
+            s = wl.seqs[0]
+            assert sum(EDGE_SLOTS) == s.n - wl.cfg.W
+            s.slot_bounds = np.concatenate([[0], np.cumsum(EDGE_SLOTS)]).astype(np.int32)
+            _WL[name] = wl
+        else:
+            cfg = W.get_config("tiny") if name == "tiny" else W.small_config()
+            _WL[name] = W.make_workload(cfg)
     return _WL[name]
 
 
@@ -51,7 +64,8 @@ def _device_trees(comp, wl, b, l, h, S, curvature):
 
 
 @pytest.fixture(scope="module",
-                params=["tiny", "small-tc", "small-simt", "small-tc-curv", "tiny-curv"])
+                params=["tiny", "small-tc", "small-simt", "small-tc-curv", "tiny-curv", "edges",
+                        "edges-curv"])
 def case(request, built):
     from kv_cache_compression_probe_gb300 import kvc
     name = request.param.split("-")[0]
