@@ -29,6 +29,50 @@ def packed_capacity(p: kvc.kvc_params, ctx_len: Sequence[int]) -> int:
     return int(rows)
 
 
+# ---------------------------------------------------------------- packed-cache files
+PACKED_FORMAT = 1
+_PACKED_ARRAYS = ("Kp", "Vp", "logm", "pos", "len_lh", "cap_lh", "off_lh")
+
+
+def write_packed(path: str, p: kvc.kvc_params, tensors: dict) -> None:
+    """Writes a packed cache to an .npz file: the parameter block's scalar
+    fields, and Kp, Vp, logm, pos (the first sum(cap_lh) rows, i.e. every
+    (b, l, h)'s entries and its decode reserve) with len_lh, cap_lh and
+    off_lh.  bf16 rows are stored as their uint16 bit patterns, so a reload is
+    bit for bit.  Tensors may live on any device."""
+    rows = int(tensors["cap_lh"].to(torch.int64).sum())
+    out = {"format": np.int64(PACKED_FORMAT)}
+    for name, ctype in p._fields_:
+        if name == "tree_cuts":                      # a pointer: not part of the cache
+            continue
+        out["param_" + name] = np.asarray(getattr(p, name))
+    for name in _PACKED_ARRAYS:
+        t = tensors[name].detach()
+        if name in ("Kp", "Vp", "logm", "pos"):
+            t = t[:rows]
+        t = t.cpu().contiguous()
+        if t.dtype == torch.bfloat16:
+            out[name + "_bf16bits"] = t.view(torch.int16).numpy()
+        else:
+            out[name] = t.numpy()
+    np.savez(path, **out)
+
+
+def read_packed(path: str):
+    """(params dict, tensors dict on the CPU) of a file written by write_packed."""
+    with np.load(path) as z:
+        if int(z["format"]) != PACKED_FORMAT:
+            raise ValueError(f"{path}: packed-cache format {int(z['format'])}, expected {PACKED_FORMAT}")
+        params = {k[len("param_"):]: z[k].item() for k in z.files if k.startswith("param_")}
+        tensors = {}
+        for name in _PACKED_ARRAYS:
+            if name + "_bf16bits" in z.files:
+                tensors[name] = torch.from_numpy(z[name + "_bf16bits"].copy()).view(torch.bfloat16)
+            else:
+                tensors[name] = torch.from_numpy(z[name].copy())
+    return params, tensors
+
+
 class Compressor:
     def __init__(self, p: kvc.kvc_params, ctx_len: Sequence[int], device="cuda",
                  tensor_cores: bool = True, tree_cuts: bool = False, salient: bool = False):
@@ -210,6 +254,32 @@ class Compressor:
                           self.op_cost[:, l0:l1], self.ws_score, cur)
         self.select(slot_bounds, n_slots, head_sens, graph=graph)
         self.merge_pack(K, V, slot_bounds, n_slots, graph=graph)
+
+    # ---------------------------------------------------------------- packed-cache files
+    def save_packed(self, path: str) -> None:
+        """Writes this object's packed cache (after kvc_merge_pack and any
+        decode steps) to an .npz file (write_packed)."""
+        torch.cuda.synchronize(self.Kp.device)
+        write_packed(path, self.p, {n: getattr(self, n) for n in _PACKED_ARRAYS})
+
+    def load_packed(self, path: str) -> None:
+        """Replaces this object's packed cache with a saved one, so decoding
+        resumes where the saving process stopped.  The file's shape fields
+        (B, L, H, G, d, dtype) must match this object's and its rows must fit
+        the packed buffers."""
+        params, t = read_packed(path)
+        for k in ("B", "L", "H", "G", "d", "dtype"):
+            if params[k] != getattr(self.p, k):
+                raise ValueError(f"{path}: {k} = {params[k]}, this cache has {getattr(self.p, k)}")
+        rows = t["Kp"].shape[0]
+        if rows > self.Kp.shape[0]:
+            raise ValueError(f"{path}: {rows} rows, the packed buffers hold {self.Kp.shape[0]}")
+        for n in ("Kp", "Vp", "logm", "pos"):
+            getattr(self, n)[:rows].copy_(t[n])
+        for n in ("len_lh", "cap_lh", "off_lh"):
+            getattr(self, n).copy_(t[n].view(getattr(self, n).shape))
+        self.ws_decode.zero_()                       # fresh arrival counters
+        torch.cuda.synchronize(self.Kp.device)
 
     def decode(self, q, k_new, v_new, out, pos_new=None, stream=None):
         kvc.kvc_decode_attn(self.p, q, k_new, v_new, pos_new, self.Kp, self.Vp, self.logm,
