@@ -188,7 +188,13 @@ def parity_record(name: str):
             "ties_reported": sum(x["ties_reported"] for x in seqs),
             "tie_runs_reordered": sum(x["tie_runs_reordered"] for x in seqs),
             "max_abs_err": max((x["util_max_abs_err"] for x in seqs), default=None),
-            "max_rel_err": max((x["util_max_rel_err"] for x in seqs), default=None)}
+            "max_rel_err": max((x["util_max_rel_err"] for x in seqs), default=None),
+            "util_within_1e5_rel": sum(x.get("util_within_1e5_rel", 0) for x in seqs) or None,
+            "util_within_scale_term_only": (sum(x["util_within_scale_term_only"] for x in seqs)
+                                            if seqs and "util_within_scale_term_only" in seqs[0]
+                                            else None),
+            "util_worst_err_over_bound": max((x.get("util_worst_err_over_bound", 0) for x in seqs),
+                                             default=None)}
 
 
 # --------------------------------------------------------------------------- GPU arm

@@ -174,25 +174,35 @@ __global__ void __launch_bounds__(kDpThreads) dp_kernel(kvc_params p, const int3
     if (y + kDpWarps < end) g_next = kap[y + kDpWarps];  // next block's gain, in flight
     if (y <= end) {                                       // warp-uniform
       const double gain = y < end ? (double)g_now : 0.0;
-      long long bkey = LLONG_MIN;
+      // lane: lengths kLmin + lane + 32 i; the four candidates are scored
+      // without branches so their loads and fp64 adds overlap
+      unsigned long long bkey = 0;                        // 0: no candidate
       int bl = 0;                                         // best length (larger wins ties)
-      for (int ln = kLmin + lane; ln <= kLmax; ln += 32) {
-        const int x = y - ln;
-        if (x < 0) break;
-        const double bx = ring[x & (kRing - 1)];
-        if (__double_as_longlong(bx) == neg_bits) continue;
-        const long long key = order_key((bx - pen[ln - kLmin]) + gain);
-        if (key >= bkey) { bkey = key; bl = ln; }         // ln ascends: ties go to the larger
-      }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const long long ok = __shfl_xor_sync(KVC_FULL_MASK, bkey, o);
-        const int ol = __shfl_xor_sync(KVC_FULL_MASK, bl, o);
-        if (ok > bkey || (ok == bkey && ol > bl)) { bkey = ok; bl = ol; }
+      for (int i = 0; i < 4; ++i) {
+        const int ln = kLmin + lane + 32 * i;
+        const int x = y - ln;
+        const bool in = ln <= kLmax && x >= 0;
+        const double bx = ring[(in ? x : 0) & (kRing - 1)];
+        const double v = (bx - pen[(in ? ln : kLmin) - kLmin]) + gain;
+        // unsigned key: order_key shifted so that 0 is below every score
+        const unsigned long long key =
+            (unsigned long long)order_key(v) ^ 0x8000000000000000ull;
+        const bool ok = in && __double_as_longlong(bx) != neg_bits;
+        if (ok && key >= bkey) { bkey = key; bl = ln; }   // ln ascends: ties go to the larger
       }
+      // warp maximum of (key, length): the high word, then the low word among
+      // the lanes holding that high word, then the largest length among the
+      // lanes holding the whole key
+      const unsigned hi = (unsigned)(bkey >> 32), lo = (unsigned)bkey;
+      const unsigned mhi = __reduce_max_sync(KVC_FULL_MASK, hi);
+      const unsigned mlo = __reduce_max_sync(KVC_FULL_MASK, hi == mhi ? lo : 0u);
+      const unsigned mbl = __reduce_max_sync(KVC_FULL_MASK, (hi == mhi && lo == mlo) ? (unsigned)bl : 0u);
       if (lane == 0) {
-        ring[y & (kRing - 1)] = bl > 0 ? from_key(bkey) : -DBL_MAX;
-        bk[y] = (int16_t)bl;
+        const unsigned long long best = ((unsigned long long)mhi << 32) | mlo;
+        ring[y & (kRing - 1)] =
+            mbl > 0 ? from_key((long long)(best ^ 0x8000000000000000ull)) : -DBL_MAX;
+        bk[y] = (int16_t)mbl;
       }
     }
     __syncthreads();

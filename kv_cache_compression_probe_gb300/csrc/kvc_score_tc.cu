@@ -332,23 +332,24 @@ __global__ void __maxnreg__(kRsMaxRegs)
           if constexpr (!kMasked) {
             // arguments, products and the two tree sums on packed pairs
             const uint64_t c2 = f2(a.q_scale2, a.q_scale2), nm2 = f2(-mx, -mx);
-            uint64_t e2[kCh / 2], d2[kCh / 2];
+            // sum e as a tree, sum e t as two fused multiply-add chains
+            uint64_t e2[kCh / 2], dA = f2(0.f, 0.f), dB = f2(0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < kCh / 2; ++j) {
               const uint64_t t2 = fma2(f2(raw[2 * j], raw[2 * j + 1]), c2, nm2);
               const float2 tt = uf2(t2);
               e2[j] = f2(kvcd::ex2(tt.x), kvcd::ex2(tt.y));
-              if (kU) d2[j] = mul2(e2[j], t2);
+              if (kU) {
+                if (j & 1) dB = fma2(e2[j], t2, dB);
+                else dA = fma2(e2[j], t2, dA);
+              }
             }
 #pragma unroll
             for (int w = kCh / 4; w >= 1; w >>= 1)
 #pragma unroll
-              for (int j = 0; j < w; ++j) {
-                e2[j] = add2(e2[j], e2[j + w]);
-                if (kU) d2[j] = add2(d2[j], d2[j + w]);
-              }
+              for (int j = 0; j < w; ++j) e2[j] = add2(e2[j], e2[j + w]);
             esum = hsum2(e2[0]);
-            if (kU) dsum = hsum2(d2[0]);
+            if (kU) dsum = hsum2(add2(dA, dB));
           } else {
             float e[kCh], d[kCh];
 #pragma unroll
@@ -1012,6 +1013,12 @@ __global__ void __maxnreg__(kNodeMaxRegs)
             !kvcd::mbar_wait(&sm.v_full, (uint32_t)(k & 1), a.wait_ns)) { *abort_flag = 1; break; }
         tc_fence_after();
         bool ok = true;
+        // operand descriptors: the start-address field counts 16-byte units, so
+        // a key step or another operand block is an addition to the base
+        const uint64_t dA0 = sw128_desc(kvcd::smem_u32(sm.Ap[0][0]));
+        const uint64_t dV0 = sw128_mn_desc(kvcd::smem_u32(sm.Vt[0]), kBlockBytes);
+        static_assert(sizeof(sm.Ap[0][0]) == kBlockBytes, "Ap blocks are contiguous");
+#pragma unroll
         for (int j = 0; j < 15; ++j) {
           const int nn = k * 15 + j, bf = nn & 1;
           if (j == 7 && sal_any) {                   // depth-2 products done: drop the isolated rows
@@ -1035,13 +1042,14 @@ __global__ void __maxnreg__(kNodeMaxRegs)
           int l0, l1;
           node_leaves(j, l0, l1);
           const uint32_t d = tmem + 256 + bf * 128;
-          uint32_t acc = 0;
+#pragma unroll
           for (int part = 0; part < 3; ++part)
+#pragma unroll
             for (int ks = l0; ks < l1; ++ks) {
-              const uint64_t aa = sw128_desc(kvcd::smem_u32(sm.Ap[part][ks >> 2]) + (ks & 3) * 32);
-              const uint64_t bb = sw128_mn_desc(kvcd::smem_u32(sm.Vt[0]) + ks * 2048, kBlockBytes);
-              mma_bf16_i(d, aa, bb, kIdescVmn, acc);
-              acc = 1;
+              const uint64_t aa =
+                  dA0 + (uint64_t)((part * 2 + (ks >> 2)) * (kBlockBytes >> 4) + (ks & 3) * 2);
+              const uint64_t bb = dV0 + (uint64_t)(ks * (2048 >> 4));
+              mma_bf16_i(d, aa, bb, kIdescVmn, (part > 0 || ks > l0) ? 1u : 0u);
             }
           mma_commit(&sm.nfull[bf]);
         }

@@ -118,12 +118,17 @@ def _end_to_end_selection(name, cfg, wl, util, cost, rel, taken):
     every (l,h), then its floor and auction), up to near-ties of 1e-6 relative.
     With KVC_PARITY_REPORT set, the counts are written there as JSON."""
     from tests.oracle_pipeline import score_sequence_parallel
-    from tests.tie_check import TIE_REL, band_needed, check_sequence
+    from tests.tie_check import TIE_REL, band_needed, check_sequence, utility_slack
     report = {"workload": name, "tie_band_rel": TIE_REL, "sequences": []}
     for b, s in enumerate(wl.seqs):
         S = len(s.slot_bounds) - 1
         u64, c64, r64 = score_sequence_parallel(wl, b, _procs())
         np.testing.assert_array_equal(cost[b, :, :, :S], c64)
+        n_ops, n_rel, n_scale, worst = utility_slack(u64, util[b, :, :, :S], c64, r64,
+                                                     wl.head_sens, s.slot_bounds)
+        # fp32 reaches most utilities to 1e-5 relative; the rest are near zero
+        # after the clamped difference cancels and pass through the scale term
+        assert n_scale <= 0.05 * n_ops, (n_scale, n_ops)
         args = (u64, util[b, :, :, :S], c64, r64, token_view(rel, wl, b), wl.head_sens,
                 taken[b, :, :, :S], s.slot_bounds, s.n, cfg)
         try:
@@ -134,7 +139,10 @@ def _end_to_end_selection(name, cfg, wl, util, cost, rel, taken):
                                         tie_runs_reordered=rep.runs_moved_util,
                                         floor_tie_runs_reordered=rep.runs_moved_floor,
                                         util_max_abs_err=rep.max_abs_err,
-                                        util_max_rel_err=rep.max_rel_err))
+                                        util_max_rel_err=rep.max_rel_err,
+                                        util_within_1e5_rel=n_rel,
+                                        util_within_scale_term_only=n_scale,
+                                        util_worst_err_over_bound=worst))
     print(f"{name} end-to-end selection: {report}")
     path = os.environ.get("KVC_PARITY_REPORT")
     if path:

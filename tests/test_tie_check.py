@@ -122,3 +122,21 @@ def test_a_relevance_error_that_changes_the_floor_is_rejected():
         pytest.fail("no single relevance change moved the floor")
     with pytest.raises(AssertionError):
         check_sequence(util, util, cost, r, rd, sens, taken, bounds, n, cfg)
+
+
+def test_utility_slack_counts_and_rejects():
+    from tests.tie_check import utility_slack
+    rng = np.random.default_rng(9)
+    bounds = np.array([0, 40, 104], np.int64)
+    r = rng.random((1, 1, 104))
+    cost = np.ones((1, 1, 2, 16), np.int64)
+    sens = np.ones((1, 1))
+    u = rng.random((1, 1, 2, 16)) * 1e-3
+    u[0, 0, 1, 3] = 0.0                       # a utility that cancelled to zero
+    got = u.astype(np.float32)
+    got[0, 0, 1, 3] = 1e-7                    # within the scale term only
+    n, n_rel, n_scale, worst = utility_slack(u, got, cost, r, sens, bounds)
+    assert n == 32 and n_scale >= 1 and n_rel + n_scale == 32 and worst <= 1.0
+    got[0, 0, 0, 5] = u[0, 0, 0, 5] + 1.0     # far outside any bound
+    with pytest.raises(AssertionError):
+        utility_slack(u, got, cost, r, sens, bounds)

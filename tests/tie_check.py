@@ -110,3 +110,34 @@ def band_needed(util64, util_dev, cost, r64, r_dev, sens, taken_dev, bounds, n, 
         except AssertionError:
             continue
     return None
+
+
+def utility_slack(u64, u_dev, cost, r64, sens, bounds):
+    """Every utility of one sequence against the utility tolerance of the
+    tests: |g - o| <= 1e-5 * max(|o|, 3 * scale), scale = R(N) * sens / cost
+    per op (R(N) the node's oracle relevance mass; the Add op uses the root's).
+    A utility is scale times a clamped difference of normalised distortions,
+    so fp32 reaches it to an accuracy relative to the scale, not to |u|.
+    Returns (ops, ops within 1e-5 * |o|, ops that pass only through the scale
+    term, worst err / bound); asserts that every op passes."""
+    from oracle import kvc_oracle as O
+    L, H, S, _ = u64.shape
+    scale = np.empty_like(u64)
+    for l in range(L):
+        for h in range(H):
+            cs = np.r_[0.0, np.cumsum(r64[l, h])]
+            for k in range(S):
+                nodes = O.tree_nodes(int(bounds[k]), int(bounds[k + 1]))
+                Rv = np.array([cs[y] - cs[x] for x, y in nodes])
+                scale[l, h, k] = np.r_[Rv[0], Rv] * float(sens[l, h]) / cost[l, h, k]
+    err = np.abs(u_dev.astype(np.float64) - u64)
+    bound = 1e-5 * np.maximum(np.abs(u64), 3 * scale)
+    worst = float((err / np.maximum(bound, 1e-300)).max())
+    bad = err > bound
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"utility outside tolerance at (l, h, slot, op) {tuple(i)}: "
+                             f"device {u_dev[tuple(i)]!r}, oracle {u64[tuple(i)]!r}, "
+                             f"bound {bound[tuple(i)]!r}")
+    rel_ok = err <= 1e-5 * np.abs(u64)
+    return int(u64.size), int(rel_ok.sum()), int((~rel_ok).sum()), worst
