@@ -124,11 +124,6 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
 }
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
 __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
@@ -252,14 +247,16 @@ __global__ void __maxnreg__(kRsMaxRegs)
           break;
         }
         tc_fence_after();
+        // descriptors advance by 16-byte units: a base per operand, constant steps
+        const uint64_t dB = sw128_desc(kvcd::smem_u32(sm.Bt[s][0]));
 #pragma unroll
         for (int mt = 0; mt < NT; ++mt) {
           const uint32_t d = tmem + (uint32_t)((bf * NT + mt) * kBN);
+          const uint64_t dA = sw128_desc(kvcd::smem_u32(sm.A[mt][0]));
 #pragma unroll
           for (int k = 0; k < kD / 16; ++k) {
-            const uint32_t aoff = kvcd::smem_u32(sm.A[mt][k >> 2]) + (k & 3) * 32;
-            const uint32_t boff = kvcd::smem_u32(sm.Bt[s][k >> 2]) + (k & 3) * 32;
-            mma_bf16(d, sw128_desc(aoff), sw128_desc(boff), k > 0 ? 1u : 0u);
+            const uint64_t step = (uint64_t)((k >> 2) * (kBlockBytes >> 4) + (k & 3) * 2);
+            mma_bf16(d, dA + step, dB + step, k > 0 ? 1u : 0u);
           }
         }
         mma_commit(&sm.empty[s]);
@@ -559,14 +556,16 @@ __global__ void __maxnreg__(kRsMaxRegs)
           break;
         }
         tc_fence_after();
+        // descriptors advance by 16-byte units: a base per operand, constant steps
+        const uint64_t dK = sw128_desc(kvcd::smem_u32(sm.Bt[s][0]));
 #pragma unroll
         for (int nb = 0; nb < NT; ++nb) {
           const uint32_t d = tmem + (uint32_t)(bf * kN + nb * 128);
+          const uint64_t dQ = sw128_desc(kvcd::smem_u32(sm.A[nb][0]));
 #pragma unroll
           for (int k = 0; k < kD / 16; ++k) {
-            const uint32_t aoff = kvcd::smem_u32(sm.Bt[s][k >> 2]) + (k & 3) * 32;
-            const uint32_t boff = kvcd::smem_u32(sm.A[nb][k >> 2]) + (k & 3) * 32;
-            mma_bf16_i(d, sw128_desc(aoff), sw128_desc(boff), idesc, k > 0 ? 1u : 0u);
+            const uint64_t step = (uint64_t)((k >> 2) * (kBlockBytes >> 4) + (k & 3) * 2);
+            mma_bf16_i(d, dK + step, dQ + step, idesc, k > 0 ? 1u : 0u);
           }
         }
         mma_commit(&sm.empty[s]);
@@ -800,6 +799,8 @@ struct NodeSmem {
   alignas(16) float vh[15][128];                          // v^ of the slot's nodes
   float Al[8][128];                                       // per-row leaf masses
   float At[4][128];                                       // per-row mass of each isolated token
+  uint4 vsave[4][2][8];                                   // V rows of the isolated tokens
+  int bds[kNodeSlots + 1];                                // this CTA's slot bounds
   float red[2][4][15][4];                                 // per-quarter node sums
   uint64_t k_full, k_empty, v_full, v_empty, s_full, a_ready, b_done;
   uint64_t vh_full, vh_free;
@@ -856,6 +857,12 @@ __device__ __forceinline__ void leaf_range(const uint8_t* cuts, int l, int x0, i
   kvcd::tree_node_range(cuts, 7 + l, x0, y0, a, b);
   start = a; cnt = b - a;
 }
+
+// Order of the node products and their statistics: the eight leaves first
+// (few products each, so the epilogue starts at once), then depth 2, depth 1
+// and the root, whose products the tensor pipe runs while the epilogue works
+// through the leaves.
+__device__ constexpr int kNodeOrder[15] = {7, 8, 9, 10, 11, 12, 13, 14, 3, 4, 5, 6, 1, 2, 0};
 
 // Leaves [l0, l1) covered by node j of the depth-3 tree.
 __device__ __forceinline__ void node_leaves(int j, int& l0, int& l1) {
@@ -998,14 +1005,21 @@ __global__ void __maxnreg__(kNodeMaxRegs)
         }
         if (!kvcd::mbar_wait(&sm.k_full, (uint32_t)(k & 1), a.wait_ns)) { *abort_flag = 1; break; }
         tc_fence_after();
+        {
+          // descriptors advance by 16-byte units: one base each, constant steps
+          const uint64_t dQ = sw128_desc(kvcd::smem_u32(sm.Q[0]));
+          const uint64_t dK = sw128_desc(kvcd::smem_u32(sm.Kt[0]));
+          const uint64_t dH = sw128_desc(kvcd::smem_u32(sm.Kh));
+          static_assert(sizeof(sm.Q[0]) == kBlockBytes && sizeof(sm.Kt[0]) == kBlockBytes,
+                        "operand blocks are contiguous");
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint64_t aq = sw128_desc(kvcd::smem_u32(sm.Q[kk >> 2]) + (kk & 3) * 32);
-          mma_bf16_i(tmem, aq, sw128_desc(kvcd::smem_u32(sm.Kt[kk >> 2]) + (kk & 3) * 32), kIdesc,
-                     kk > 0 ? 1u : 0u);
-          mma_bf16_i(tmem + 128, aq,
-                     sw128_desc(kvcd::smem_u32(sm.Kh) + (kk >> 2) * 6144 + (kk & 3) * 32),
-                     kIdescN48, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint64_t step = (uint64_t)((kk >> 2) * (kBlockBytes >> 4) + (kk & 3) * 2);
+            mma_bf16_i(tmem, dQ + step, dK + step, kIdesc, kk > 0 ? 1u : 0u);
+            mma_bf16_i(tmem + 128, dQ + step,
+                       dH + (uint64_t)((kk >> 2) * (6144 >> 4) + (kk & 3) * 2), kIdescN48,
+                       kk > 0 ? 1u : 0u);
+          }
         }
         mma_commit(&sm.s_full);
         mma_commit(&sm.k_empty);
@@ -1018,10 +1032,30 @@ __global__ void __maxnreg__(kNodeMaxRegs)
         const uint64_t dA0 = sw128_desc(kvcd::smem_u32(sm.Ap[0][0]));
         const uint64_t dV0 = sw128_mn_desc(kvcd::smem_u32(sm.Vt[0]), kBlockBytes);
         static_assert(sizeof(sm.Ap[0][0]) == kBlockBytes, "Ap blocks are contiguous");
+        // the leaf products must not see the isolated tokens: their V rows are
+        // zeroed (and kept) until the leaves are done, then put back for the
+        // depth-2 and higher products
+        if (sal_any) {
 #pragma unroll
-        for (int j = 0; j < 15; ++j) {
-          const int nn = k * 15 + j, bf = nn & 1;
-          if (j == 7 && sal_any) {                   // depth-2 products done: drop the isolated rows
+          for (int g = 0; g < 4; ++g) {
+            if (salc[g] < 0) continue;
+#pragma unroll
+            for (int fb = 0; fb < 2; ++fb) {
+              uint4* row = reinterpret_cast<uint4*>(&sm.Vt[fb][(2 * g) * 2048 + salc[g] * 128]);
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                sm.vsave[g][fb][c] = row[c];
+                row[c] = make_uint4(0, 0, 0, 0);
+              }
+            }
+          }
+          kvcd::fence_proxy_async_smem();
+        }
+#pragma unroll
+        for (int pj = 0; pj < 15; ++pj) {
+          const int j = kNodeOrder[pj];
+          const int nn = k * 15 + pj, bf = nn & 1;
+          if (pj == 8 && sal_any) {                  // leaf products done: the rows go back
             mma_commit(&sm.mid_done);
             if (!kvcd::mbar_wait(&sm.mid_done, (uint32_t)(nmid & 1), a.wait_ns)) { ok = false; break; }
             ++nmid;
@@ -1032,7 +1066,7 @@ __global__ void __maxnreg__(kNodeMaxRegs)
               for (int fb = 0; fb < 2; ++fb) {
                 uint4* row = reinterpret_cast<uint4*>(&sm.Vt[fb][(2 * g) * 2048 + salc[g] * 128]);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
+                for (int c = 0; c < 8; ++c) row[c] = sm.vsave[g][fb][c];
               }
             }
             kvcd::fence_proxy_async_smem();
@@ -1155,7 +1189,7 @@ __global__ void __maxnreg__(kNodeMaxRegs)
       __syncwarp();
       if (lane == 0) kvcd::mbar_arrive(&sm.a_ready);
       named_bar(qbar, 128);                          // leaf masses of these rows complete
-      float an_fin[4];                               // masses of the nodes g, g+4, g+8, g+12
+      float an_fin[4];                               // masses of the nodes at positions g, g+4, ...
       {
         float an[15];
 #pragma unroll
@@ -1167,16 +1201,17 @@ __global__ void __maxnreg__(kNodeMaxRegs)
         for (int i = 0; i < 4; ++i) {
           float v = 0.f;
 #pragma unroll
-          for (int j = i * 4; j < i * 4 + 4 && j < 15; ++j)
-            if ((j & 3) == g) v = an[j];
+          for (int pj = i * 4; pj < i * 4 + 4 && pj < 15; ++pj)
+            if ((pj & 3) == g) v = an[kNodeOrder[pj]];
           an_fin[i] = v;
         }
       }
       if (!*abort_flag && !kvcd::mbar_wait(&sm.vh_full, (uint32_t)(k & 1), a.wait_ns)) *abort_flag = 1;
       // ---- epilogue B: 32 features of every node
 #pragma unroll
-      for (int j = 0; j < 15; ++j) {
-        const int nn = k * 15 + j, bf = nn & 1;
+      for (int pj = 0; pj < 15; ++pj) {
+        const int j = kNodeOrder[pj];
+        const int nn = k * 15 + pj, bf = nn & 1;
         if (!*abort_flag && !kvcd::mbar_wait(&sm.nfull[bf], (uint32_t)((nn >> 1) & 1), a.wait_ns)) *abort_flag = 1;
         tc_fence_after();
         float v[32];
@@ -1205,25 +1240,27 @@ __global__ void __maxnreg__(kNodeMaxRegs)
           uu0 = fma2(ua, ua, uu0);
           uu1 = fma2(ub, ub, uu1);
         }
-        // partials of nodes 4t .. 4t+3 go to the spare TMEM columns of parity
-        // t & 1 (one barrier per four nodes; group jj & 3 finishes node jj,
-        // adding the groups' partials in group order)
-        tmem_st2(tmem + lane_off + part_col(j, g), hsum2(dd0) + hsum2(dd1), hsum2(uu0) + hsum2(uu1));
-        if ((j & 3) == 3 || j == 14) {
+        // partials of the nodes at positions 4t .. 4t+3 go to the spare TMEM
+        // columns of parity t & 1 (one barrier per four nodes; group pp & 3
+        // finishes the node at position pp, adding the groups' partials in
+        // group order)
+        tmem_st2(tmem + lane_off + part_col(pj, g), hsum2(dd0) + hsum2(dd1), hsum2(uu0) + hsum2(uu1));
+        if ((pj & 3) == 3 || pj == 14) {
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
           tc_fence_before();
           named_bar(qbar, 128);
           tc_fence_after();
 #pragma unroll
-          for (int jj = j & ~3; jj <= j; ++jj) {
-            if (g == (jj & 3)) {                         // finisher of node jj for these rows
+          for (int pp_ = pj & ~3; pp_ <= pj; ++pp_) {
+            const int jj = kNodeOrder[pp_];
+            if (g == (pp_ & 3)) {                        // finisher of node jj for these rows
               float pp[8];
-              tld8(tmem + lane_off + part_col(jj, 0), pp);
+              tld8(tmem + lane_off + part_col(pp_, 0), pp);
               const float ddt = (pp[0] + pp[2]) + (pp[4] + pp[6]);
               const float uut = (pp[1] + pp[3]) + (pp[5] + pp[7]);
               float st[4];
-              st[0] = rv ? fabsf(an_fin[jj >> 2] - ah[jj]) : 0.f;
-              st[1] = rv ? an_fin[jj >> 2] : 0.f;
+              st[0] = rv ? fabsf(an_fin[pp_ >> 2] - ah[jj]) : 0.f;
+              st[1] = rv ? an_fin[pp_ >> 2] : 0.f;
               st[2] = rv ? sqrtf(ddt) : 0.f;
               st[3] = rv ? sqrtf(uut) : 0.f;
               kvcd::warp_sum4(st, lane);               // totals on every lane
