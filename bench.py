@@ -167,6 +167,22 @@ PARITY_SOURCES = ("kv_cache_compression_probe_gb300/csrc/kvc_score.cu",
                   "kv_cache_compression_probe_gb300/csrc/kvc_common.cuh")
 
 
+def select_roofline(cfg, seqs, sel_ms, hbm):
+    """kvc_select against HBM: each of the up to 8 radix passes (8-bit digits of
+    a 64-bit key) of the floor reads every token's weight byte and relevance
+    (5 B) and each of the auction reads every op's key and cost (12 B); the
+    tail replays and offsets are negligible.  The passes are many small
+    launches, so the call is bound by launch and reduction latency."""
+    LH = cfg.L * cfg.H
+    ops = sum(LH * (len(s[1]) - 1) * 16 for s in seqs)
+    toks = sum(LH * s[0] for s in seqs)
+    nbytes = 8 * (ops * 12 + toks * 5)
+    gbs = nbytes / (sel_ms * 1e-3) / 1e9
+    return {"bound": "latency (launches and reductions)", "achieved": gbs, "peak": hbm,
+            "unit": "GB/s", "frac": gbs / hbm, "algorithmic_bytes": nbytes,
+            "bytes_note": "8 radix passes x (ops x 12 B + tokens x 5 B), an upper bound"}
+
+
 def parity_record(name: str):
     """The end-to-end selection parity of a workload (device chain against the
     float64 oracle chain, near-ties within 1e-6 counted) as written by the
@@ -739,6 +755,7 @@ def run_gpu(args, cfg, rank, world):
                                 "peak": hbm, "unit": "GB/s",
                                 "frac": pack_bytes / (pack_ms * 1e-3) / 1e9 / hbm,
                                 "algorithmic_bytes": pack_bytes},
+        "select_roofline": select_roofline(cfg, seqs, sel_ms, hbm),
         "score_hbm_frac": score_bytes / (score_ms * 1e-3) / 1e9 / hbm,
         "score_tflops": score_flops / (score_ms * 1e-3) / 1e12,
         "score_tc_frac_of_bf16_peak": score_flops / (score_ms * 1e-3) / 1e12 / tc,
@@ -1106,7 +1123,7 @@ def main():
                     help="issue the decode steps one call at a time instead of one CUDA graph")
     ap.add_argument("--workloads", default="long,aggressive,serving",
                     help="other workloads timed after the headline line (comma list; '' = none)")
-    ap.add_argument("--workload-reps", type=int, default=5,
+    ap.add_argument("--workload-reps", type=int, default=20,
                     help="compression repetitions per other workload (median)")
     ap.add_argument("--profile", action="store_true",
                     help="profiling run: no warm-up, one step, no CPU baseline, no e2e leg")
