@@ -803,6 +803,7 @@ struct NodeSmem {
   int bds[kNodeSlots + 1];                                // this CTA's slot bounds
   float red[2][4][15][4];                                 // per-quarter node sums
   uint64_t k_full, k_empty, v_full, v_empty, s_full, a_ready, b_done;
+  uint64_t h_full, xch_free;                              // A^ ready; partials read
   uint64_t vh_full, vh_free;
   uint64_t nfull[2], nempty[2];
   uint64_t mma_done, mid_done;
@@ -827,11 +828,12 @@ __device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr, uint32_t lbo_b
 
 
 
-// Spare TMEM columns 176..239 (no MMA writes there) hold the per-row partial
-// sums of node j from group g: parity of j's group of four nodes, j mod 4,
-// group, (dd, uu).
-__device__ __forceinline__ uint32_t part_col(int j, int g) {
-  return 176u + (uint32_t)(((j >> 2) & 1) * 32 + (j & 3) * 8 + 2 * g);
+// TMEM columns 128..247 hold, during epilogue B, the per-row partial sums of
+// the node at position p from group g: (dd, uu) at 128 + 8p + 2g.  They
+// overlap A^ (128..175), which epilogue A has read by then; the next slot's
+// A^ product waits until these partials are read (xch_free).
+__device__ __forceinline__ uint32_t part_col(int p, int g) {
+  return 128u + (uint32_t)(p * 8 + 2 * g);
 }
 __device__ __forceinline__ void tmem_st2(uint32_t taddr, float a, float b) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr),
@@ -911,6 +913,7 @@ __global__ void __maxnreg__(kNodeMaxRegs)
     kvcd::mbar_init(&sm.k_full, 1); kvcd::mbar_init(&sm.k_empty, 1);
     kvcd::mbar_init(&sm.v_full, 1); kvcd::mbar_init(&sm.v_empty, 1);
     kvcd::mbar_init(&sm.s_full, 1); kvcd::mbar_init(&sm.a_ready, kEpiWarps);
+    kvcd::mbar_init(&sm.h_full, 1); kvcd::mbar_init(&sm.xch_free, kEpiWarps);
     kvcd::mbar_init(&sm.b_done, 1);
     kvcd::mbar_init(&sm.mma_done, 1);
     kvcd::mbar_init(&sm.mid_done, 1);
@@ -1016,12 +1019,23 @@ __global__ void __maxnreg__(kNodeMaxRegs)
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint64_t step = (uint64_t)((kk >> 2) * (kBlockBytes >> 4) + (kk & 3) * 2);
             mma_bf16_i(tmem, dQ + step, dK + step, kIdesc, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&sm.s_full);
+          // A^ lands on the columns of the previous slot's node partials
+          if (k >= 1 && !kvcd::mbar_wait(&sm.xch_free, (uint32_t)((k - 1) & 1), a.wait_ns)) {
+            *abort_flag = 1;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint64_t step = (uint64_t)((kk >> 2) * (kBlockBytes >> 4) + (kk & 3) * 2);
             mma_bf16_i(tmem + 128, dQ + step,
                        dH + (uint64_t)((kk >> 2) * (6144 >> 4) + (kk & 3) * 2), kIdescN48,
                        kk > 0 ? 1u : 0u);
           }
         }
-        mma_commit(&sm.s_full);
+        mma_commit(&sm.h_full);
         mma_commit(&sm.k_empty);
         if (!kvcd::mbar_wait(&sm.a_ready, (uint32_t)(k & 1), a.wait_ns) ||
             !kvcd::mbar_wait(&sm.v_full, (uint32_t)(k & 1), a.wait_ns)) { *abort_flag = 1; break; }
@@ -1113,20 +1127,6 @@ __global__ void __maxnreg__(kNodeMaxRegs)
       // ---- epilogue A: attention of this row to the slot's nodes and its key quarter
       if (!*abort_flag && !kvcd::mbar_wait(&sm.s_full, (uint32_t)(k & 1), a.wait_ns)) *abort_flag = 1;
       tc_fence_after();
-      float ah[15];
-      {
-        float d0[16], d1[16], d2[16];
-        tmem_ld16_nw(tmem + lane_off + 128, d0);
-        tmem_ld16_nw(tmem + lane_off + 144, d1);
-        tmem_ld16_nw(tmem + lane_off + 160, d2);
-        tmem_wait();
-        const float* lmv = reinterpret_cast<const float*>(sm.Kh + kvc::kProtoLogmOff);
-#pragma unroll
-        for (int j = 0; j < 15; ++j) {
-          const float sc = (d0[j] + d1[j] + d2[j]) * a.q_scale2 + lmv[j] * 1.4426950408889634f - l2;
-          ah[j] = rv ? kvcd::ex2(sc) : 0.f;
-        }
-      }
       int cnt0, cnt1, salc;
       {
         int st;
@@ -1184,6 +1184,24 @@ __global__ void __maxnreg__(kNodeMaxRegs)
       sm.Al[2 * g][rl] = lsum[0];
       sm.Al[2 * g + 1][rl] = lsum[1];
       sm.At[g][rl] = at_acc;
+      // the attention of this row to the 15 node prototypes, from A^ (its
+      // product waited for the previous slot's partials, so it comes last)
+      if (!*abort_flag && !kvcd::mbar_wait(&sm.h_full, (uint32_t)(k & 1), a.wait_ns)) *abort_flag = 1;
+      tc_fence_after();
+      float ah[15];
+      {
+        float d0[16], d1[16], d2[16];
+        tmem_ld16_nw(tmem + lane_off + 128, d0);
+        tmem_ld16_nw(tmem + lane_off + 144, d1);
+        tmem_ld16_nw(tmem + lane_off + 160, d2);
+        tmem_wait();
+        const float* lmv = reinterpret_cast<const float*>(sm.Kh + kvc::kProtoLogmOff);
+#pragma unroll
+        for (int j = 0; j < 15; ++j) {
+          const float sc = (d0[j] + d1[j] + d2[j]) * a.q_scale2 + lmv[j] * 1.4426950408889634f - l2;
+          ah[j] = rv ? kvcd::ex2(sc) : 0.f;
+        }
+      }
       kvcd::fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -1240,38 +1258,40 @@ __global__ void __maxnreg__(kNodeMaxRegs)
           uu0 = fma2(ua, ua, uu0);
           uu1 = fma2(ub, ub, uu1);
         }
-        // partials of the nodes at positions 4t .. 4t+3 go to the spare TMEM
-        // columns of parity t & 1 (one barrier per four nodes; group pp & 3
-        // finishes the node at position pp, adding the groups' partials in
-        // group order)
+        // this group's partial sums of the node go to TMEM; the four groups
+        // meet once the slot's 15 nodes are done
         tmem_st2(tmem + lane_off + part_col(pj, g), hsum2(dd0) + hsum2(dd1), hsum2(uu0) + hsum2(uu1));
-        if ((pj & 3) == 3 || pj == 14) {
-          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-          tc_fence_before();
-          named_bar(qbar, 128);
-          tc_fence_after();
+      }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      named_bar(qbar, 128);
+      tc_fence_after();
+      // group g finishes the nodes at positions g, g + 4, ...: it adds the
+      // groups' partials in group order and sums |A - A^|, A, |U - A^ v^| and
+      // |U| over its 32 rows
 #pragma unroll
-          for (int pp_ = pj & ~3; pp_ <= pj; ++pp_) {
-            const int jj = kNodeOrder[pp_];
-            if (g == (pp_ & 3)) {                        // finisher of node jj for these rows
-              float pp[8];
-              tld8(tmem + lane_off + part_col(pp_, 0), pp);
-              const float ddt = (pp[0] + pp[2]) + (pp[4] + pp[6]);
-              const float uut = (pp[1] + pp[3]) + (pp[5] + pp[7]);
-              float st[4];
-              st[0] = rv ? fabsf(an_fin[pp_ >> 2] - ah[jj]) : 0.f;
-              st[1] = rv ? an_fin[pp_ >> 2] : 0.f;
-              st[2] = rv ? sqrtf(ddt) : 0.f;
-              st[3] = rv ? sqrtf(uut) : 0.f;
-              kvcd::warp_sum4(st, lane);               // totals on every lane
-              if (lane == 0) {
+      for (int pp_ = 0; pp_ < 15; ++pp_) {
+        const int jj = kNodeOrder[pp_];
+        if (g == (pp_ & 3)) {
+          float pp[8];
+          tld8(tmem + lane_off + part_col(pp_, 0), pp);
+          const float ddt = (pp[0] + pp[2]) + (pp[4] + pp[6]);
+          const float uut = (pp[1] + pp[3]) + (pp[5] + pp[7]);
+          float st[4];
+          st[0] = rv ? fabsf(an_fin[pp_ >> 2] - ah[jj]) : 0.f;
+          st[1] = rv ? an_fin[pp_ >> 2] : 0.f;
+          st[2] = rv ? sqrtf(ddt) : 0.f;
+          st[3] = rv ? sqrtf(uut) : 0.f;
+          kvcd::warp_sum4(st, lane);                   // totals on every lane
+          if (lane == 0) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) sm.red[k & 1][q][jj][e] = st[e];
-              }
-            }
+            for (int e = 0; e < 4; ++e) sm.red[k & 1][q][jj][e] = st[e];
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) kvcd::mbar_arrive(&sm.xch_free);   // the partial columns are free
       named_bar(5, kEpiWarps * 32);                  // every node of this slot finished
       if (tid < 60) {
         const int j = tid >> 2, e = tid & 3;
