@@ -840,16 +840,6 @@ __device__ __forceinline__ void tmem_st2(uint32_t taddr, float a, float b) {
                "r"(__float_as_uint(a)), "r"(__float_as_uint(b))
                : "memory");
 }
-__device__ __forceinline__ void tld8(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                 "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 // Leaf l of the slot [x0, y0): first token and token count (at most 16) of
 // node 7 + l of the tree with cut table `cuts` (null: midpoint tree).
@@ -1266,27 +1256,58 @@ __global__ void __maxnreg__(kNodeMaxRegs)
       tc_fence_before();
       named_bar(qbar, 128);
       tc_fence_after();
-      // group g finishes the nodes at positions g, g + 4, ...: it adds the
-      // groups' partials in group order and sums |A - A^|, A, |U - A^ v^| and
-      // |U| over its 32 rows
+      // group g finishes the nodes at positions g, g + 4, g + 8, g + 12: it
+      // adds the groups' partials in group order and sums |A - A^|, A,
+      // |U - A^ v^| and |U| over its 32 rows (16 sums reduced together)
+      {
+        float pp[4][8];
 #pragma unroll
-      for (int pp_ = 0; pp_ < 15; ++pp_) {
-        const int jj = kNodeOrder[pp_];
-        if (g == (pp_ & 3)) {
-          float pp[8];
-          tld8(tmem + lane_off + part_col(pp_, 0), pp);
-          const float ddt = (pp[0] + pp[2]) + (pp[4] + pp[6]);
-          const float uut = (pp[1] + pp[3]) + (pp[5] + pp[7]);
-          float st[4];
-          st[0] = rv ? fabsf(an_fin[pp_ >> 2] - ah[jj]) : 0.f;
-          st[1] = rv ? an_fin[pp_ >> 2] : 0.f;
-          st[2] = rv ? sqrtf(ddt) : 0.f;
-          st[3] = rv ? sqrtf(uut) : 0.f;
-          kvcd::warp_sum4(st, lane);                   // totals on every lane
-          if (lane == 0) {
+        for (int i = 0; i < 4; ++i) {
+          const int pos = 4 * i + g < 15 ? 4 * i + g : 4 * i;   // position 15: none (read, unused)
+          uint32_t r[8];
+          asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                         "=r"(r[6]), "=r"(r[7])
+                       : "r"(tmem + lane_off + part_col(pos, 0)));
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sm.red[k & 1][q][jj][e] = st[e];
+          for (int e = 0; e < 8; ++e) pp[i][e] = __uint_as_float(r[e]);
+        }
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        float st[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const bool real = 4 * i + g < 15 && rv;
+          const float ddt = (pp[i][0] + pp[i][2]) + (pp[i][4] + pp[i][6]);
+          const float uut = (pp[i][1] + pp[i][3]) + (pp[i][5] + pp[i][7]);
+          float ahj = 0.f;
+#pragma unroll
+          for (int pq = i * 4; pq < i * 4 + 4 && pq < 15; ++pq)
+            if ((pq & 3) == g) ahj = ah[kNodeOrder[pq]];
+          st[4 * i + 0] = real ? fabsf(an_fin[i] - ahj) : 0.f;
+          st[4 * i + 1] = real ? an_fin[i] : 0.f;
+          st[4 * i + 2] = real ? sqrtf(ddt) : 0.f;
+          st[4 * i + 3] = real ? sqrtf(uut) : 0.f;
+        }
+        // reduce-scatter over the lanes: after it, lanes 2v and 2v + 1 hold
+        // the warp total of value v
+#pragma unroll
+        for (int o = 16, n = 8; o >= 2; o >>= 1, n >>= 1) {
+          const bool hi = (lane & o) != 0;
+#pragma unroll
+          for (int i = 0; i < n; ++i) {
+            const float send = hi ? st[i] : st[i + n];
+            const float keep = hi ? st[i + n] : st[i];
+            st[i] = keep + __shfl_xor_sync(KVC_FULL_MASK, send, o);
           }
+        }
+        st[0] += __shfl_xor_sync(KVC_FULL_MASK, st[0], 1);
+        const int vi = lane >> 1, ni = vi >> 2;        // value, node of the group
+        if (!(lane & 1) && 4 * ni + g < 15) {
+          int jj = 0;
+#pragma unroll
+          for (int pq = 0; pq < 15; ++pq)
+            if ((pq & 3) == g && (pq >> 2) == ni) jj = kNodeOrder[pq];
+          sm.red[k & 1][q][jj][vi & 3] = st[0];
         }
       }
       tc_fence_before();
