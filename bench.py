@@ -935,6 +935,76 @@ def workload_leg(name: str, args, dev, with_cpu: bool):
     return rec
 
 
+def tiny_leg(args, dev, with_cpu: bool):
+    """The tiny config (fp32, d = 64: the SIMT scoring, pack and decode kernels):
+    the whole workload compressed and decoded, timed like the other legs, and
+    the oracle on one process over the whole workload beside it."""
+    import torch
+    from kv_cache_compression_probe_gb300 import kvc
+    from kv_cache_compression_probe_gb300.pipeline import Compressor, pad_bounds
+    from synth import workloads as W
+    cfg = W.get_config("tiny")
+    wl = W.make_workload(cfg)
+    D = cfg.n_decode
+    S_max = max(len(s.slot_bounds) - 1 for s in wl.seqs)
+    p = kvc.make_params(B=cfg.B, L=cfg.L, H=cfg.H, G=cfg.G, d=cfg.d, P=cfg.P, W=cfg.W,
+                        dtype=kvc.KVC_F32, n_max=max(s.n for s in wl.seqs), S_max=S_max,
+                        rope_base=cfg.rope_base, budget_ratio=cfg.budget_ratio,
+                        budget_entries_per_lh=cfg.budget_entries_per_lh,
+                        floor_cap_frac=cfg.floor_cap_frac, floor_cap_tokens=cfg.floor_cap_tokens,
+                        decode_reserve=D + 1)
+    f32 = torch.float32
+    K = torch.from_numpy(np.concatenate([s.K.reshape(-1, cfg.d) for s in wl.seqs])).to(dev, f32)
+    V = torch.from_numpy(np.concatenate([s.V.reshape(-1, cfg.d) for s in wl.seqs])).to(dev, f32)
+    Qp = torch.from_numpy(np.stack([s.Qp for s in wl.seqs])).to(dev, f32)
+    bounds = torch.from_numpy(pad_bounds([s.slot_bounds for s in wl.seqs], S_max)).to(dev)
+    n_slots = torch.tensor([len(s.slot_bounds) - 1 for s in wl.seqs], dtype=torch.int32,
+                           device=dev)
+    comp = Compressor(p, [s.n for s in wl.seqs], device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        comp.compress(K, V, Qp, bounds, n_slots, graph=True)
+    torch.cuda.synchronize(dev)
+    times = []
+    for _ in range(max(20, args.workload_reps)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        comp.compress(K, V, Qp, bounds, n_slots, graph=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1))
+    comp_ms = statistics.median(times)
+    dec = [W.decode_inputs(cfg, t) for t in range(D)]
+    q_all = torch.from_numpy(np.stack([x[0] for x in dec])).to(dev, f32)
+    kn_all = torch.from_numpy(np.stack([x[1] for x in dec])).to(dev, f32)
+    vn_all = torch.from_numpy(np.stack([x[2] for x in dec])).to(dev, f32)
+    out = torch.empty(tuple(q_all.shape), dtype=f32, device=dev)
+    len0 = comp.len_lh.clone()
+    comp.decode_many(q_all, kn_all, vn_all, out)
+    comp.len_lh.copy_(len0)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    comp.decode_many(q_all, kn_all, vn_all, out)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if kvc.kvc_device_error() != 0:
+        raise RuntimeError("device error in the tiny workload")
+    dec_ms = e0.elapsed_time(e1) / D
+    tokens = sum(s.n for s in wl.seqs)
+    rec = {"workload": cfg.name + ": " + cfg.description, "kv_tokens": tokens, "decode_steps": D,
+           "dtype": "f32", "paths": "SIMT scoring, pack and decode (fp32, d = 64)",
+           "compression_median_ms": comp_ms, "compression_reps": len(times),
+           "decode_ms_per_step": dec_ms, "ms_per_step": comp_ms + dec_ms * D,
+           "kv_tokens_per_s": tokens / ((comp_ms + dec_ms * D) * 1e-3),
+           "note": "a parity-sized case: launch latency bounds every call"}
+    if with_cpu:
+        secs, toks = oracle_sample(cfg, [(l, h) for l in range(cfg.L) for h in range(cfg.H)], D)
+        rec["cpu_baseline"] = {"value": toks / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+                               "sample": "the whole workload, one process", "seconds": secs}
+    return rec
+
+
 # --------------------------------------------------------------------------- oracle (CPU)
 def oracle_sample(cfg, heads, decode_steps):
     """The float64 oracle over a bounded sample: `heads` (layer, KV head) pairs of
@@ -1121,7 +1191,7 @@ def main():
                     help="issue the compression calls directly instead of as CUDA graph replays")
     ap.add_argument("--eager-decode", action="store_true",
                     help="issue the decode steps one call at a time instead of one CUDA graph")
-    ap.add_argument("--workloads", default="long,aggressive,serving",
+    ap.add_argument("--workloads", default="tiny,long,aggressive,serving",
                     help="other workloads timed after the headline line (comma list; '' = none)")
     ap.add_argument("--workload-reps", type=int, default=20,
                     help="compression repetitions per other workload (median)")
@@ -1158,7 +1228,9 @@ def main():
             import torch
             torch.cuda.empty_cache()
             dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-            line["other_workloads"] = {w: workload_leg(w, args, dev, not args.no_cpu_baseline)
+            line["other_workloads"] = {w: (tiny_leg(args, dev, not args.no_cpu_baseline)
+                                           if w == "tiny" else
+                                           workload_leg(w, args, dev, not args.no_cpu_baseline))
                                        for w in names}
         print(json.dumps(line))
     if world > 1:
