@@ -931,14 +931,16 @@ __device__ __forceinline__ ProtoAcc acc_from_smem(const ProtoLevels& sm, int lvl
 
 // One warp per block: slot trees differ in length and a block retires with its
 // slowest warp, so single-warp blocks let the block scheduler balance them
-// (the same choice as the pack kernel); 96 registers.
+// (the same choice as the pack kernel).  24 blocks per SM at 80 registers:
+// measured at 16K, 1.03 ms against 1.15 with 20 blocks at 96 registers and
+// 1.10 with 28 at 72.
 #ifndef KVC_PROTO_WARPS
 #define KVC_PROTO_WARPS 1
 #endif
 constexpr int kProtoWarps = KVC_PROTO_WARPS;
 
 template <typename T, int D>
-__global__ void __launch_bounds__(32 * kProtoWarps, 20 / kProtoWarps)
+__global__ void __launch_bounds__(32 * kProtoWarps, 24 / kProtoWarps)
     proto_kernel(kvc_params p, ScoreArgs a, unsigned char* proto) {
   static_assert(D == 128 && sizeof(T) == 2, "tensor-core node path is bf16, d = 128");
   __shared__ ProtoLevels levels[kProtoWarps];
