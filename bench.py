@@ -630,13 +630,18 @@ def run_gpu(args, cfg, rank, world):
         torch.cuda.synchronize(dev)
         a0, a1 = ev(), ev()
         a0.record(stream)
-        q_all.copy_(h_q, non_blocking=True); kn_all.copy_(h_kn, non_blocking=True)
-        vn_all.copy_(h_vn, non_blocking=True)
         if pipelined:
             comp.compress_from_host(h_K, h_V, h_Q, K, V, Qp, bounds, n_slots, chunks=8,
                                     copy_stream=copy_stream, graph=cg)
+            # the decode inputs follow the cache chunks on the copy stream
+            with torch.cuda.stream(copy_stream):
+                q_all.copy_(h_q, non_blocking=True); kn_all.copy_(h_kn, non_blocking=True)
+                vn_all.copy_(h_vn, non_blocking=True)
+            stream.wait_stream(copy_stream)
             comp.decode_many(q_all, kn_all, vn_all, out, graph=not args.eager_decode)
         else:
+            q_all.copy_(h_q, non_blocking=True); kn_all.copy_(h_kn, non_blocking=True)
+            vn_all.copy_(h_vn, non_blocking=True)
             K.copy_(h_K, non_blocking=True); V.copy_(h_V, non_blocking=True)
             Qp.copy_(h_Q, non_blocking=True)
             step(False)

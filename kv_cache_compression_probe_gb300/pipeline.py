@@ -208,8 +208,10 @@ class Compressor:
         device buffers K, V, Qp one layer chunk at a time on `copy_stream` while the
         chunks already on the device are scored on the current stream (scoring has
         no coupling across layers; the budget couples them only in select), then
-        selects and packs (as graph replays with graph=True).  Same results as
-        copying everything, then compress()."""
+        selects and packs (as graph replays with graph=True).  The first chunk is
+        about half the size of the others, so less of the copy is exposed.  Same
+        results as copying everything, then compress().  Copies the caller queues
+        on `copy_stream` afterwards run behind the chunks."""
         p = self.p
         if p.B != 1:
             raise ValueError("compress_from_host copies layer chunks of one sequence")
@@ -218,7 +220,11 @@ class Compressor:
         cur = torch.cuda.current_stream(dev)
         cs = copy_stream if copy_stream is not None else torch.cuda.Stream(device=dev)
         cs.wait_stream(cur)                          # the buffers are free to overwrite
-        cuts = [round(c * L / chunks) for c in range(chunks + 1)]
+        # a small first chunk, so scoring starts early; the rest in equal parts
+        chunks = max(1, min(chunks, L))
+        first = max(1, -(-L // (2 * chunks))) if chunks > 1 else L
+        cuts = [0] + [first + round(c * (L - first) / (chunks - 1)) for c in range(chunks)] \
+            if chunks > 1 else [0, L]
         events = []
         for c in range(chunks):
             l0, l1 = cuts[c], cuts[c + 1]
