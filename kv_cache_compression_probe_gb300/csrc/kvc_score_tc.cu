@@ -800,7 +800,6 @@ struct NodeSmem {
   float Al[8][128];                                       // per-row leaf masses
   float At[4][128];                                       // per-row mass of each isolated token
   uint4 vsave[4][2][8];                                   // V rows of the isolated tokens
-  int bds[kNodeSlots + 1];                                // this CTA's slot bounds
   float red[2][4][15][4];                                 // per-quarter node sums
   uint64_t k_full, k_empty, v_full, v_empty, s_full, a_ready, b_done;
   uint64_t h_full, xch_free;                              // A^ ready; partials read
