@@ -405,9 +405,9 @@ int kvc_partition(const kvc_params* p, const int32_t* ctx_len, const void* hidde
  * operation in the order written.  cuts: [B, L, H, S_max, 8] bytes, the
  * table kvc_params.tree_cuts takes (byte j < 7 = cut of node j minus the slot
  * start; byte 7 = 0; all 8 bytes 0 for padding slots s >= n_slots[b]).
- * K is the token layout of kvc_score; rope_cos / rope_sin as for kvc_score
- * (n_half >= 2*n_max).  No workspace.  B*L*H must be at most 65535
- * (KVC_EINVAL before any launch).  Slot bounds outside 16..128 tokens or
+ * K is the token layout of kvc_score, 16-byte aligned; rope_cos / rope_sin
+ * as for kvc_score (n_half >= 2*n_max).  No workspace.  B*L*H must be at most
+ * 65535 and K aligned (KVC_EINVAL before any launch).  Slot bounds outside 16..128 tokens or
  * beyond n_b - W leave that slot's bytes unwritten and record KVC_EDEVICE.
  * Non-finite keys give unspecified (but valid) cuts. */
 int kvc_tree_cuts(const kvc_params* p, const int32_t* ctx_len, const void* K,

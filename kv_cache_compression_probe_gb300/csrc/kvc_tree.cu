@@ -279,6 +279,7 @@ extern "C" int kvc_tree_cuts(const kvc_params* p, const int32_t* ctx_len, const 
   if (st != KVC_OK) return st;
   if (!ctx_len || !K || !rope_cos || !rope_sin || !slot_bounds || !n_slots || !kappa || !cuts)
     return KVC_EINVAL;
+  if (reinterpret_cast<uintptr_t>(K) & 15) return KVC_EINVAL;   // vector loads of key rows
   const long long blh = kvc::lh_count(p);
   if (blh > 65535) return KVC_EINVAL;
   int32_t* err = kvc::err_word();

@@ -103,3 +103,18 @@ def test_budget_below_the_window_is_reported(lib):
 def test_workspace_size_of_a_malformed_block_is_zero(lib):
     for which in range(5):
         assert lib.kvc_workspace_bytes(which, ctypes.byref(_params(d=96))) == 0
+
+
+def test_tree_cuts_rejects_bad_arguments(lib):
+    """kvc_tree_cuts (no workspace): a malformed block, each missing pointer
+    and a key pointer off a 16-byte boundary (the key rows are read with
+    vector loads) are rejected before any launch."""
+    args = _fake(8)                      # ctx_len, K, cos, sin, bounds, n_slots, kappa, cuts
+    assert lib.kvc_tree_cuts(ctypes.byref(_params(B=0)), *args, None) == kvc.KVC_EINVAL
+    for i in range(8):
+        a = list(args)
+        a[i] = None
+        assert lib.kvc_tree_cuts(ctypes.byref(_params()), *a, None) == kvc.KVC_EINVAL, i
+    a = list(args)
+    a[1] = VP(4096 + 8)
+    assert lib.kvc_tree_cuts(ctypes.byref(_params()), *a, None) == kvc.KVC_EINVAL
