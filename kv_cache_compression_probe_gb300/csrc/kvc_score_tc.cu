@@ -105,6 +105,22 @@ __device__ __forceinline__ void tmem_ld16_nw(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 32 consecutive TMEM columns of this thread's lane (issue only; see tmem_wait).
+__device__ __forceinline__ void tmem_ld32_nw(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
 
 
 // Packed pairs of fp32 (a in the low half): element-wise a * b + c, a * b,
@@ -803,6 +819,7 @@ struct NodeSmem {
   float red[2][4][15][4];                                 // per-quarter node sums
   uint64_t k_full, k_empty, v_full, v_empty, s_full, a_ready, b_done;
   uint64_t h_full, xch_free;                              // A^ ready; partials read
+  uint64_t ap_ready;                                      // the a operand is in shared memory
   uint64_t vh_full, vh_free;
   uint64_t nfull[2], nempty[2];
   uint64_t mma_done, mid_done;
@@ -903,6 +920,7 @@ __global__ void __maxnreg__(kNodeMaxRegs)
     kvcd::mbar_init(&sm.v_full, 1); kvcd::mbar_init(&sm.v_empty, 1);
     kvcd::mbar_init(&sm.s_full, 1); kvcd::mbar_init(&sm.a_ready, kEpiWarps);
     kvcd::mbar_init(&sm.h_full, 1); kvcd::mbar_init(&sm.xch_free, kEpiWarps);
+    kvcd::mbar_init(&sm.ap_ready, kEpiWarps);
     kvcd::mbar_init(&sm.b_done, 1);
     kvcd::mbar_init(&sm.mma_done, 1);
     kvcd::mbar_init(&sm.mid_done, 1);
@@ -1026,7 +1044,9 @@ __global__ void __maxnreg__(kNodeMaxRegs)
         }
         mma_commit(&sm.h_full);
         mma_commit(&sm.k_empty);
-        if (!kvcd::mbar_wait(&sm.a_ready, (uint32_t)(k & 1), a.wait_ns) ||
+        // the node products need only the a operand: they start while the
+        // epilogue still forms the prototype attention from A^
+        if (!kvcd::mbar_wait(&sm.ap_ready, (uint32_t)(k & 1), a.wait_ns) ||
             !kvcd::mbar_wait(&sm.v_full, (uint32_t)(k & 1), a.wait_ns)) { *abort_flag = 1; break; }
         tc_fence_after();
         bool ok = true;
@@ -1173,6 +1193,10 @@ __global__ void __maxnreg__(kNodeMaxRegs)
       sm.Al[2 * g][rl] = lsum[0];
       sm.Al[2 * g + 1][rl] = lsum[1];
       sm.At[g][rl] = at_acc;
+      kvcd::fence_proxy_async_smem();                // the a operand, visible to the MMAs
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) kvcd::mbar_arrive(&sm.ap_ready);
       // the attention of this row to the 15 node prototypes, from A^ (its
       // product waited for the previous slot's partials, so it comes last)
       if (!*abort_flag && !kvcd::mbar_wait(&sm.h_full, (uint32_t)(k & 1), a.wait_ns)) *abort_flag = 1;
@@ -1222,15 +1246,8 @@ __global__ void __maxnreg__(kNodeMaxRegs)
         if (!*abort_flag && !kvcd::mbar_wait(&sm.nfull[bf], (uint32_t)((nn >> 1) & 1), a.wait_ns)) *abort_flag = 1;
         tc_fence_after();
         float v[32];
-        {
-          float v0[16], v1[16];
-          const uint32_t col = tmem + lane_off + 256 + bf * 128 + 32 * g;
-          tmem_ld16_nw(col, v0);
-          tmem_ld16_nw(col + 16, v1);
-          tmem_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) { v[i] = v0[i]; v[16 + i] = v1[i]; }
-        }
+        tmem_ld32_nw(tmem + lane_off + 256 + bf * 128 + 32 * g, v);
+        tmem_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) kvcd::mbar_arrive(&sm.nempty[bf]);
