@@ -196,8 +196,9 @@ int kvc_rope_table(int32_t d, float base, int64_t n_half, float* cos_tab, float*
  * Out: lse [B,L,H,R]; feats [rows,5] (alpha, |v|, sigma, H, pos);
  *      relevance [rows]; op_util [B,L,H,S_max,16] f32 (0 for padding);
  *      op_cost [B,L,H,S_max,16] int32 (0 for padding).
- * Slots must have 16..128 tokens.  Errors: KVC_EINVAL, KVC_EWORKSPACE,
- * KVC_ECUDA; bad per-sequence values are reported via kvc_device_error. */
+ * Slots must have 16..128 tokens; K, V and Qp must be 16-byte aligned
+ * (KVC_EINVAL otherwise).  Errors: KVC_EINVAL, KVC_EWORKSPACE, KVC_ECUDA; bad
+ * per-sequence values are reported via kvc_device_error. */
 int kvc_score(const kvc_params* p, const int32_t* ctx_len, const void* K, const void* V,
               const void* Qp, const float* rope_cos, const float* rope_sin,
               const int32_t* slot_bounds, const int32_t* n_slots, const float* head_sens,
@@ -246,7 +247,8 @@ int kvc_select(const kvc_params* p, const int32_t* ctx_len, const int32_t* slot_
  * prototype (k_hat, v_hat, ln m, mean position).  Rows between len and cap
  * are left untouched for appends.  capacity = rows of Kp/Vp/logm/pos; a
  * sequence whose entries would overflow it is skipped and reported via
- * kvc_device_error.  Errors: KVC_EINVAL, KVC_EWORKSPACE, KVC_ECUDA. */
+ * kvc_device_error.  K, V, Kp and Vp must be 16-byte aligned (KVC_EINVAL
+ * otherwise).  Errors: KVC_EINVAL, KVC_EWORKSPACE, KVC_ECUDA. */
 int kvc_merge_pack(const kvc_params* p, const int32_t* ctx_len, const void* K, const void* V,
                    const float* relevance, const float* rope_cos, const float* rope_sin,
                    const int32_t* slot_bounds, const int32_t* n_slots, const uint8_t* taken,

@@ -308,6 +308,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   return true;
 }
 
+// Asynchronous prefetch of the global range [src, src + bytes) into L2 (a
+// hint: nothing waits for it; 16-byte aligned, bytes % 16 == 0, in bounds).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 1-D bulk asynchronous copy global -> shared (16-byte aligned, size % 16 == 0),
 // completing `bytes` transactions on `bar`.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,

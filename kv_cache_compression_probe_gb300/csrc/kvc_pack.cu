@@ -384,6 +384,9 @@ extern "C" int kvc_merge_pack(const kvc_params* p, const int32_t* ctx_len, const
   if (!ctx_len || !K || !V || !relevance || !rope_cos || !rope_sin || !slot_bounds || !n_slots ||
       !taken || !len_lh || !off_lh || !Kp || !Vp || !logm || !pos || capacity < 0)
     return KVC_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(K) | reinterpret_cast<uintptr_t>(V) |
+       reinterpret_cast<uintptr_t>(Kp) | reinterpret_cast<uintptr_t>(Vp)) & 15)
+    return KVC_EINVAL;                             // 16-byte row copies
   const Layout lay = layout(p);
   if (!workspace || ws_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return KVC_EWORKSPACE;

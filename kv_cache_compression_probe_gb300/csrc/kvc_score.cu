@@ -1450,6 +1450,9 @@ extern "C" int kvc_score(const kvc_params* p, const int32_t* ctx_len, const void
   if (!ctx_len || !K || !V || !Qp || !rope_cos || !rope_sin || !slot_bounds || !n_slots || !lse ||
       !feats || !relevance || !op_util || !op_cost)
     return KVC_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(K) | reinterpret_cast<uintptr_t>(V) |
+       reinterpret_cast<uintptr_t>(Qp)) & 15)
+    return KVC_EINVAL;                             // bulk copies and vector loads of rows
   const Layout lay = layout(p);
   if (!workspace || ws_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return KVC_EWORKSPACE;

@@ -84,6 +84,10 @@ __global__ void __launch_bounds__(256) key_curv_kernel(kvc_params p, TreeArgs a)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t row0 = kvcd::seq_token_base(a.ctx_len, b, p.L * p.H) + (int64_t)lh * n;
   const T* Kh = static_cast<const T*>(a.K) + row0 * D;
+  if (threadIdx.x == 0) {          // the tile's key rows (contiguous) start towards L2 at once
+    const int lo = max(0, t0 - kCurvHalo), hi = min(n, t0 - kCurvHalo + kCurvRows);
+    kvcd::prefetch_l2(Kh + (int64_t)lo * D, (uint32_t)((hi - lo) * D * sizeof(T)));
+  }
   // unit rows u_i of positions t0 - 8 .. t0 + 71 (zero outside [0, n)); each
   // warp owns rows warp, warp + 8, ..., in batches whose loads are all issued
   // before the first use

@@ -118,3 +118,19 @@ def test_tree_cuts_rejects_bad_arguments(lib):
     a = list(args)
     a[1] = VP(4096 + 8)
     assert lib.kvc_tree_cuts(ctypes.byref(_params()), *a, None) == kvc.KVC_EINVAL
+
+
+@pytest.mark.parametrize("name,idx", [("kvc_score", 1), ("kvc_score", 2), ("kvc_score", 3),
+                                      ("kvc_merge_pack", 1), ("kvc_merge_pack", 2),
+                                      ("kvc_merge_pack", 11), ("kvc_merge_pack", 12)])
+def test_row_arrays_off_a_16_byte_boundary_are_rejected(lib, name, idx):
+    """K, V, Qp (score) and K, V, Kp, Vp (pack) are read or written as whole
+    16-byte vectors and prefetched in bulk: an array off a 16-byte boundary is
+    rejected before any launch (the workspace is valid, so the status can only
+    come from the pointer)."""
+    p = _params()
+    n, kind, _ = CALLS[name]
+    need = kvc.kvc_workspace_bytes(kind, p)
+    ptrs = _fake(n)
+    ptrs[idx] = VP(4096 * (idx + 1) + 8)
+    assert _call(lib, name, p, ptrs, VP(1 << 30), need) == kvc.KVC_EINVAL
