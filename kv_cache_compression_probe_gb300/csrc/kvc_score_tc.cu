@@ -788,15 +788,17 @@ __global__ void __maxnreg__(kRsMaxRegs)
 //            K-major operand over the 128 leaf-padded key slots (each of the
 //            four epilogue groups takes 32 key slots = two leaves); per-row
 //            leaf masses to shared memory;
-//   phase B  for each of the 15 nodes: U_N = sum over parts and over the node's
-//            key slots of a_part V (V read as an MN-major operand straight from
-//            TMA) into one of two TMEM buffers;
-//   epi B    every group reads 32 of the 128 features of each node buffer and
+//   phase B  for each node but the root: U_N = sum over parts and over the
+//            node's key slots of a_part V (V read as an MN-major operand
+//            straight from TMA) into one of two TMEM buffers;
+//   epi B    every group reads 32 of the 128 features of each node buffer (the
+//            root's U is the sum of the two depth-1 buffers, added here) and
 //            forms per-row partial sums of |U - A^ v^|^2 and |U|^2 (packed
-//            f32x2 FMAs) into spare TMEM columns; after every four nodes the
-//            four warps sharing a row quarter meet, and warp g finishes node
-//            4t + g: it adds the partials in a fixed order and forms the row's
-//            |U - A^ v^|, |U|, |A - A^| and A, summed over its 32 rows.
+//            f32x2 FMAs) into spare TMEM columns; once per slot the four warps
+//            sharing a row quarter meet, and warp g finishes the nodes at
+//            positions g, g + 4, ...: it adds the partials in a fixed order and
+//            forms the row's |U - A^ v^|, |U|, |A - A^| and A, summed over its
+//            32 rows.
 // Per-(slot, tile) sums go to `npart`; a small kernel forms D and utilities.
 constexpr int kNodeSlots = 8;
 constexpr int kEpiWarps = 16;                      // 4 groups x 4 row quarters
@@ -871,6 +873,10 @@ __device__ __forceinline__ void leaf_range(const uint8_t* cuts, int l, int x0, i
 // and the root, whose products the tensor pipe runs while the epilogue works
 // through the leaves.
 __device__ constexpr int kNodeOrder[15] = {7, 8, 9, 10, 11, 12, 13, 14, 3, 4, 5, 6, 1, 2, 0};
+// Nodes with products of their own: all but the root, whose aggregate the
+// epilogue forms from the two depth-1 buffers (positions 12 and 13).
+constexpr int kMmaNodes = 14;
+static_assert(kMmaNodes % 2 == 0, "buffer of position pj is pj & 1");
 
 // Leaves [l0, l1) covered by node j of the depth-3 tree.
 __device__ __forceinline__ void node_leaves(int j, int& l0, int& l1) {
@@ -1074,10 +1080,12 @@ __global__ void __maxnreg__(kNodeMaxRegs)
           }
           kvcd::fence_proxy_async_smem();
         }
+        // the root (last in the order) is the sum of the two depth-1 nodes: the
+        // epilogue adds their buffers, so 14 nodes a slot have products
 #pragma unroll
-        for (int pj = 0; pj < 15; ++pj) {
+        for (int pj = 0; pj < kMmaNodes; ++pj) {
           const int j = kNodeOrder[pj];
-          const int nn = k * 15 + pj, bf = nn & 1;
+          const int nn = k * kMmaNodes + pj, bf = pj & 1;
           if (pj == 8 && sal_any) {                  // leaf products done: the rows go back
             mma_commit(&sm.mid_done);
             if (!kvcd::mbar_wait(&sm.mid_done, (uint32_t)(nmid & 1), a.wait_ns)) { ok = false; break; }
@@ -1242,27 +1250,56 @@ __global__ void __maxnreg__(kNodeMaxRegs)
 #pragma unroll
       for (int pj = 0; pj < 15; ++pj) {
         const int j = kNodeOrder[pj];
-        const int nn = k * 15 + pj, bf = nn & 1;
-        if (!*abort_flag && !kvcd::mbar_wait(&sm.nfull[bf], (uint32_t)((nn >> 1) & 1), a.wait_ns)) *abort_flag = 1;
-        tc_fence_after();
-        float v[32];
-        tmem_ld32_nw(tmem + lane_off + 256 + bf * 128 + 32 * g, v);
-        tmem_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) kvcd::mbar_arrive(&sm.nempty[bf]);
         const uint64_t nah = f2(-ah[j], -ah[j]);
         const ulonglong2* w2 = reinterpret_cast<const ulonglong2*>(&sm.vh[j][32 * g]);
         uint64_t dd0 = 0, dd1 = 0, uu0 = 0, uu1 = 0;
+        // features 16h .. 16h + 15 of this group's 32
+        auto accumulate = [&](const float (&v)[16], int h) {
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const ulonglong2 w = w2[t];
-          const uint64_t ua = f2(v[4 * t], v[4 * t + 1]), ub = f2(v[4 * t + 2], v[4 * t + 3]);
-          const uint64_t da = fma2(nah, w.x, ua), db = fma2(nah, w.y, ub);
-          dd0 = fma2(da, da, dd0);
-          dd1 = fma2(db, db, dd1);
-          uu0 = fma2(ua, ua, uu0);
-          uu1 = fma2(ub, ub, uu1);
+          for (int t = 0; t < 4; ++t) {
+            const ulonglong2 w = w2[4 * h + t];
+            const uint64_t ua = f2(v[4 * t], v[4 * t + 1]), ub = f2(v[4 * t + 2], v[4 * t + 3]);
+            const uint64_t da = fma2(nah, w.x, ua), db = fma2(nah, w.y, ub);
+            dd0 = fma2(da, da, dd0);
+            dd1 = fma2(db, db, dd1);
+            uu0 = fma2(ua, ua, uu0);
+            uu1 = fma2(ub, ub, uu1);
+          }
+        };
+        if (pj < kMmaNodes) {
+          const int nn = k * kMmaNodes + pj, bf = pj & 1;
+          if (!*abort_flag && !kvcd::mbar_wait(&sm.nfull[bf], (uint32_t)((nn >> 1) & 1), a.wait_ns)) *abort_flag = 1;
+          tc_fence_after();
+          float v[32];
+          tmem_ld32_nw(tmem + lane_off + 256 + bf * 128 + 32 * g, v);
+          tmem_wait();
+          if (pj < kMmaNodes - 2) {                   // the depth-1 buffers stay for the root
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) kvcd::mbar_arrive(&sm.nempty[bf]);
+          }
+          accumulate(*reinterpret_cast<const float(*)[16]>(&v[0]), 0);
+          accumulate(*reinterpret_cast<const float(*)[16]>(&v[16]), 1);
+        } else {
+          // root: U = U(node 1) + U(node 2), from buffers 0 and 1, in two halves
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float u1[16], u2[16];
+            tmem_ld16_nw(tmem + lane_off + 256 + 32 * g + 16 * h, u1);
+            tmem_ld16_nw(tmem + lane_off + 384 + 32 * g + 16 * h, u2);
+            tmem_wait();
+            if (h == 1) {                              // both depth-1 buffers are read
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) {
+                kvcd::mbar_arrive(&sm.nempty[0]);
+                kvcd::mbar_arrive(&sm.nempty[1]);
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) u1[i] += u2[i];
+            accumulate(u1, h);
+          }
         }
         // this group's partial sums of the node go to TMEM; the four groups
         // meet once the slot's 15 nodes are done
